@@ -1,0 +1,278 @@
+"""GB300-native exact k-NN, HDBSCAN core distances and mutual-reachability MST.
+
+A thin Python binding over the C ABI of ``libhdbmst.so`` (declared in
+``include/hdbmst.h``): it checks shapes, allocates outputs and the workspace
+with PyTorch on the device, and passes raw pointers and the current CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path.  If the library has not been built or cannot be loaded
+the functions raise ``HdbmstUnavailable``.
+
+Point sets are float32, feature-major ``[d, n]`` (each row one feature, each
+column one point), as torch CUDA tensors with unit column stride.  Host inputs
+(numpy arrays or CPU tensors) are accepted too: they are copied to the device,
+and the results are copied back to the host.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "knn", "core_distances", "mr_mst", "hdbscan_mst", "HdbmstError", "HdbmstUnavailable",
+    "launch_count", "profile_enable", "profile_read", "library_path", "KMAX",
+]
+
+KMAX = 32
+OP_KNN, OP_CORE, OP_MST = 0, 1, 2
+
+STATUS = {
+    0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
+    4: "non-finite value", 5: "Boruvka made no progress", 6: "CUDA error",
+}
+
+
+class HdbmstError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status})")
+
+
+class HdbmstUnavailable(ImportError):
+    pass
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise HdbmstUnavailable(
+            f"{_build.LIB} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+    try:
+        L = ctypes.CDLL(_build.LIB)
+    except OSError as e:  # pragma: no cover - depends on the machine
+        raise HdbmstUnavailable(f"cannot load {_build.LIB}: {e}") from e
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.hdbmst_workspace_bytes.argtypes = [i32, i64, i64, i32, i32]
+    L.hdbmst_workspace_bytes.restype = sz
+    L.hdbmst_knn.argtypes = [vp, i64, i64, vp, i64, i64, i32, i32, vp, vp, vp, sz, vp]
+    L.hdbmst_knn.restype = i32
+    L.hdbmst_core_distances.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.hdbmst_core_distances.restype = i32
+    L.hdbmst_mr_mst.argtypes = [vp, i64, i64, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.hdbmst_mr_mst.restype = i32
+    L.hdbmst_status_string.argtypes = [i32]
+    L.hdbmst_status_string.restype = ctypes.c_char_p
+    L.hdbmst_version.restype = i32
+    L.hdbmst_launch_count.restype = ctypes.c_uint64
+    L.hdbmst_profile_enable.argtypes = [i32]
+    L.hdbmst_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_int64), i32]
+    L.hdbmst_profile_read.restype = i32
+    L.hdbmst_profile_kernel_name.argtypes = [i32]
+    L.hdbmst_profile_kernel_name.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def lib():
+    """The loaded ctypes library (loads it on first use)."""
+    return _load()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise HdbmstError(status, what)
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _device_points(X, name: str):
+    """Return (tensor on CUDA [d, n] float32 with unit column stride, was_host)."""
+    host = False
+    if isinstance(X, np.ndarray):
+        X = torch.from_numpy(np.ascontiguousarray(X, dtype=np.float32))
+        host = True
+    if not isinstance(X, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor or numpy array")
+    if X.dim() != 2:
+        raise ValueError(f"{name} must be feature-major [d, n]")
+    if X.device.type != "cuda":
+        host = True
+        X = X.to(dtype=torch.float32).pin_memory().to("cuda", non_blocking=True)
+    if X.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    if X.stride(1) != 1 or (X.shape[0] > 1 and X.stride(0) < X.shape[1]):
+        X = X.contiguous()
+    return X, host
+
+
+def _ld(X) -> int:
+    return X.stride(0) if X.shape[0] > 1 else max(X.shape[1], 1)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    if nbytes == 0:
+        raise HdbmstError(1, "workspace size")
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes or workspace.data_ptr() % 256:
+            raise HdbmstError(3, "caller workspace")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _out(t, host):
+    return t.cpu() if host else t
+
+
+# ---------------------------------------------------------------- operations
+
+def knn(X, Y, k: int, *, workspace=None):
+    """Exact k nearest columns of ``Y [d, m]`` for every column of ``X [d, n]``.
+
+    Returns ``(idx int32 [n, k], dist float32 [n, k])`` ordered by
+    (distance, index); a query that is also in Y finds itself at distance 0.
+    """
+    L = _load()
+    X, hx = _device_points(X, "X")
+    Y, hy = _device_points(Y, "Y")
+    d, n = X.shape
+    if Y.shape[0] != d:
+        raise ValueError("X and Y must have the same number of features")
+    m = Y.shape[1]
+    dev = X.device
+    idx = torch.empty((n, k), dtype=torch.int32, device=dev)
+    dist = torch.empty((n, k), dtype=torch.float32, device=dev)
+    nb = L.hdbmst_workspace_bytes(OP_KNN, n, m, d, k)
+    if nb == 0:
+        _check(2 if k > KMAX else 1, "knn")
+    ws = _workspace(nb, dev, workspace)
+    st = L.hdbmst_knn(X.data_ptr(), _ld(X), n, Y.data_ptr(), _ld(Y), m, d, k, idx.data_ptr(),
+                      dist.data_ptr(), ws.data_ptr(), nb, _stream())
+    _check(st, "hdbmst_knn")
+    host = hx or hy
+    return _out(idx, host), _out(dist, host)
+
+
+def core_distances(X, min_samples: int, *, lists: bool = True, workspace=None):
+    """HDBSCAN core distances: each point's distance to its min_samples-th
+    nearest point, itself counted first.
+
+    Returns ``core float32 [n]`` and, with ``lists=True``, the neighbour lists
+    ``(idx int32 [n, L], dist float32 [n, L])`` with ``L = min(min_samples + 1, n)``,
+    which :func:`mr_mst` uses for its exact shortcuts.
+    """
+    L_ = _load()
+    X, host = _device_points(X, "X")
+    d, n = X.shape
+    dev = X.device
+    L = min(min_samples + 1, n)
+    core = torch.empty(n, dtype=torch.float32, device=dev)
+    idx = torch.empty((n, L), dtype=torch.int32, device=dev) if lists else None
+    dist = torch.empty((n, L), dtype=torch.float32, device=dev) if lists else None
+    nb = L_.hdbmst_workspace_bytes(OP_CORE, n, 0, d, min_samples)
+    if nb == 0:
+        _check(2 if min_samples + 1 > KMAX and min_samples <= n else 1, "core_distances")
+    ws = _workspace(nb, dev, workspace)
+    st = L_.hdbmst_core_distances(X.data_ptr(), _ld(X), n, d, min_samples, core.data_ptr(),
+                                  idx.data_ptr() if lists else None,
+                                  dist.data_ptr() if lists else None, ws.data_ptr(), nb,
+                                  _stream())
+    _check(st, "hdbmst_core_distances")
+    if not lists:
+        return _out(core, host)
+    return _out(core, host), _out(idx, host), _out(dist, host)
+
+
+def mr_mst(X, core, knn_idx=None, knn_dist=None, *, workspace=None):
+    """Minimum spanning tree of max(core_a, core_b, |a - b|) by Boruvka.
+
+    ``knn_idx``/``knn_dist`` (both or neither): the lists from
+    :func:`core_distances` on the same X; they enable the exact shortcuts and
+    do not change the result.  Returns ``(edges int32 [n-1, 2], w float32 [n-1])``
+    with ``edges[:, 0] < edges[:, 1]``, ordered by (w, lo, hi).
+    """
+    Lb = _load()
+    X, host = _device_points(X, "X")
+    d, n = X.shape
+    dev = X.device
+    core = torch.as_tensor(core, dtype=torch.float32).to(dev).contiguous()
+    if core.shape != (n,):
+        raise ValueError("core must have one entry per point")
+    if (knn_idx is None) != (knn_dist is None):
+        raise ValueError("pass both neighbour lists or neither")
+    kl = 0
+    if knn_idx is not None:
+        knn_idx = torch.as_tensor(knn_idx, dtype=torch.int32).to(dev).contiguous()
+        knn_dist = torch.as_tensor(knn_dist, dtype=torch.float32).to(dev).contiguous()
+        if knn_idx.dim() != 2 or knn_idx.shape[0] != n or knn_dist.shape != knn_idx.shape:
+            raise ValueError("neighbour lists must be [n, L]")
+        kl = knn_idx.shape[1]
+    ne = max(n - 1, 0)
+    edges = torch.empty((ne, 2), dtype=torch.int32, device=dev)
+    w = torch.empty(ne, dtype=torch.float32, device=dev)
+    nb = Lb.hdbmst_workspace_bytes(OP_MST, n, 0, d, kl)
+    if nb == 0:
+        _check(1, "mr_mst")
+    ws = _workspace(nb, dev, workspace)
+    st = Lb.hdbmst_mr_mst(X.data_ptr(), _ld(X), n, d, core.data_ptr(),
+                          knn_idx.data_ptr() if kl else None, knn_dist.data_ptr() if kl else None,
+                          kl, edges.data_ptr(), w.data_ptr(), ws.data_ptr(), nb, _stream())
+    _check(st, "hdbmst_mr_mst")
+    return _out(edges, host), _out(w, host)
+
+
+def hdbscan_mst(X, min_samples: int, *, shortcuts: bool = True):
+    """Core distances and the mutual-reachability MST of X in one call.
+
+    Returns ``(core [n], edges [n-1, 2], w [n-1])``; host inputs give host outputs.
+    """
+    X, host = _device_points(X, "X")
+    core, idx, dist = core_distances(X, min_samples, lists=True)
+    if shortcuts:
+        edges, w = mr_mst(X, core, idx, dist)
+    else:
+        edges, w = mr_mst(X, core)
+    return _out(core, host), _out(edges, host), _out(w, host)
+
+
+# ---------------------------------------------------------------- instrumentation
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(_load().hdbmst_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Record CUDA events around every kernel launch (on the launching stream)."""
+    _load().hdbmst_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """Per-kernel ``{name: (total_ms, launches)}`` since the last read; clears the record."""
+    L = _load()
+    ms = (ctypes.c_double * 64)()
+    cnt = (ctypes.c_int64 * 64)()
+    nk = L.hdbmst_profile_read(ms, cnt, 64)
+    out = {}
+    for i in range(nk):
+        if cnt[i]:
+            out[L.hdbmst_profile_kernel_name(i).decode()] = (ms[i], int(cnt[i]))
+    return out

@@ -1,0 +1,566 @@
+// C ABI of the hdbmst library: argument checks, workspace layout, the
+// host-side sequencing of the kernels, and launch accounting.
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "../../include/hdbmst.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace hdbmst;
+
+namespace {
+
+// ------------------------------------------------------------------ accounting
+
+std::atomic<uint64_t> g_launches{0};
+bool g_prof = false;
+struct ProfRec {
+    int id;
+    cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+const char *const kKernelNames[K_COUNT] = {
+    "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
+    "nbr_candidate", "active", "gather", "boruvka_scan", "comp_min", "hook",
+    "roots",  "relabel",    "sort_edges"};
+
+cudaEvent_t take_event() {
+    if (!g_pool.empty()) {
+        cudaEvent_t e = g_pool.back();
+        g_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+void before(int id, cudaStream_t s) {
+    if (!g_prof) return;
+    ProfRec r{id, take_event(), nullptr};
+    cudaEventRecord(r.a, s);
+    g_recs.push_back(r);
+}
+
+void after(int id, cudaStream_t s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_prof || g_recs.empty()) return;
+    ProfRec &r = g_recs.back();
+    if (r.id != id || r.b) return;
+    r.b = take_event();
+    cudaEventRecord(r.b, s);
+}
+
+#define LAUNCH(id, stream, call)                      \
+    do {                                              \
+        before(id, stream);                           \
+        cudaError_t e_ = (call);                      \
+        after(id, stream);                            \
+        if (e_ != cudaSuccess) return HDBMST_ERR_CUDA; \
+    } while (0)
+
+#define CUDA_OK(call)                                  \
+    do {                                               \
+        if ((call) != cudaSuccess) return HDBMST_ERR_CUDA; \
+    } while (0)
+
+// ------------------------------------------------------------------ workspace
+
+struct Carver {
+    char *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base(static_cast<char *>(b)) {}
+    template <class T>
+    T *take(size_t count) {
+        off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 256));
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+struct DevStatus {
+    unsigned status;
+    unsigned nbmax_bits;
+    int fb_count;
+    int act_count;
+    int edge_count;
+    int pad[3];
+};
+
+constexpr int kMaxSplits = 8;
+constexpr size_t kPartialBudget = size_t(256) << 20;  // bytes of partial lists per chunk
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 148;
+    return sms;
+}
+
+// Column splits that fill the GPU's CTA slots in whole waves.
+int choose_splits(int row_tiles, int col_tiles, int slots) {
+    int best = 1;
+    double best_eff = 0.0;
+    const int smax = std::max(1, std::min(kMaxSplits, col_tiles));
+    for (int S = 1; S <= smax; ++S) {
+        const int64_t units = static_cast<int64_t>(row_tiles) * S;
+        const int64_t waves = (units + slots - 1) / slots;
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * slots);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    return best;
+}
+
+struct KnnPlan {
+    int n, m, d, dk, k, KP;
+    int64_t n_pad, m_pad;
+    bool alias;
+    int col_tiles;
+    int chunk_rows;  // multiple of kBM
+};
+
+KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
+    KnnPlan p{};
+    p.n = static_cast<int>(n);
+    p.m = static_cast<int>(m);
+    p.d = d;
+    p.dk = static_cast<int>(round_up(d, kBK));
+    p.k = k;
+    p.KP = k <= 12 ? 16 : 32;
+    p.n_pad = round_up(std::max<int64_t>(n, 1), kBM);
+    p.m_pad = alias ? p.n_pad : round_up(m, kBN);
+    p.alias = alias;
+    p.col_tiles = static_cast<int>(p.m_pad / kBN);
+    const int64_t per_row = static_cast<int64_t>(kMaxSplits) * p.KP * 8;
+    int64_t rows = static_cast<int64_t>(kPartialBudget) / per_row / kBM * kBM;
+    rows = std::max<int64_t>(rows, kBM);
+    p.chunk_rows = static_cast<int>(std::min<int64_t>(rows, p.n_pad));
+    return p;
+}
+
+struct KnnBufs {
+    float *Xf, *Xp, *xnorm, *Yf, *Yp, *ynorm;
+    float *part_key;
+    int *part_idx;
+    int *fb_rows;
+    DevStatus *st;
+    int32_t *list_idx;  // core distances without caller lists
+    float *list_dist;
+};
+
+void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
+    b.Xf = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xp = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.xnorm = c.take<float>(p.n_pad);
+    if (p.alias) {
+        b.Yf = b.Xf;
+        b.Yp = b.Xp;
+        b.ynorm = b.xnorm;
+    } else {
+        b.Yf = c.take<float>(static_cast<size_t>(p.dk) * p.m_pad);
+        b.Yp = c.take<float>(static_cast<size_t>(p.dk) * p.m_pad);
+        b.ynorm = c.take<float>(p.m_pad);
+    }
+    const size_t part = static_cast<size_t>(kMaxSplits) * p.chunk_rows * p.KP;
+    b.part_key = c.take<float>(part);
+    b.part_idx = c.take<int>(part);
+    b.fb_rows = c.take<int>(std::max(p.n, 1));
+    b.st = c.take<DevStatus>(1);
+    if (own_lists) {
+        b.list_idx = c.take<int32_t>(static_cast<size_t>(std::max(p.n, 1)) * p.k);
+        b.list_dist = c.take<float>(static_cast<size_t>(std::max(p.n, 1)) * p.k);
+    } else {
+        b.list_idx = nullptr;
+        b.list_dist = nullptr;
+    }
+}
+
+bool ws_ok(const void *ws, size_t have, size_t need) {
+    return ws && (reinterpret_cast<uintptr_t>(ws) % 256 == 0) && have >= need;
+}
+
+hdbmst_status read_status(DevStatus *dev, DevStatus &host, cudaStream_t s) {
+    CUDA_OK(cudaMemcpyAsync(&host, dev, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaStreamSynchronize(s));
+    return HDBMST_OK;
+}
+
+// Pack, tile search, refine and exact fallback.  Writes out_idx / out_dist
+// ([n, k]) and out_core (rank core_rank) when not NULL.
+hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_t ldx,
+                      const float *Y, int64_t ldy, int32_t *out_idx, float *out_dist,
+                      float *out_core, int core_rank, cudaStream_t s) {
+    CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
+    if (p.alias) {
+        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
+                                      b.Xp, b.xnorm, &b.st->status, &b.st->nbmax_bits, s));
+    } else {
+        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
+                                      b.Xp, b.xnorm, &b.st->status, nullptr, s));
+        LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
+                                      b.Yp, b.ynorm, &b.st->status, &b.st->nbmax_bits, s));
+    }
+    const int slots = 2 * sm_count();
+    for (int base = 0; base < p.n; base += p.chunk_rows) {
+        const int rows = std::min(p.chunk_rows, p.n - base);
+        const int row_tiles = (rows + kBM - 1) / kBM;
+        const int S0 = choose_splits(row_tiles, p.col_tiles, slots);
+        const int tps = (p.col_tiles + S0 - 1) / S0;
+        const int S = (p.col_tiles + tps - 1) / tps;
+        KnnTileArgs ta{};
+        ta.Xf = b.Xf;
+        ta.Yf = b.Yf;
+        ta.ynorm = b.ynorm;
+        ta.ldx = p.n_pad;
+        ta.ldy = p.m_pad;
+        ta.dk = p.dk;
+        ta.row_base = base;
+        ta.row_end = p.n;
+        ta.chunk_rows_pad = p.chunk_rows;
+        ta.col_tiles = p.col_tiles;
+        ta.tiles_per_split = tps;
+        ta.part_key = b.part_key;
+        ta.part_idx = b.part_idx;
+        LAUNCH(K_KNN_TILE, s, launch_knn_tile(p.KP, ta, row_tiles, S, s));
+        KnnRefineArgs ra{};
+        ra.part_key = b.part_key;
+        ra.part_idx = b.part_idx;
+        ra.splits = S;
+        ra.chunk_rows_pad = p.chunk_rows;
+        ra.row_base = base;
+        ra.row_end = p.n;
+        ra.Xp = b.Xp;
+        ra.Yp = b.Yp;
+        ra.xnorm = b.xnorm;
+        ra.nbmax_bits = &b.st->nbmax_bits;
+        ra.d = p.d;
+        ra.dk = p.dk;
+        ra.k = p.k;
+        ra.m = p.m;
+        ra.core_rank = out_core ? core_rank : 0;
+        ra.out_idx = out_idx;
+        ra.out_dist = out_dist;
+        ra.out_core = out_core;
+        ra.fb_count = &b.st->fb_count;
+        ra.fb_rows = b.fb_rows;
+        LAUNCH(K_KNN_REFINE, s, launch_knn_refine(p.KP, ra, rows, s));
+    }
+    KnnExactArgs xa{};
+    xa.fb_count = &b.st->fb_count;
+    xa.fb_rows = b.fb_rows;
+    xa.Xp = b.Xp;
+    xa.Yp = b.Yp;
+    xa.dk = p.dk;
+    xa.k = p.k;
+    xa.m = p.m;
+    xa.core_rank = out_core ? core_rank : 0;
+    xa.out_idx = out_idx;
+    xa.out_dist = out_dist;
+    xa.out_core = out_core;
+    LAUNCH(K_KNN_EXACT, s, launch_knn_exact(p.KP, xa, 2 * sm_count(), s));
+    DevStatus h{};
+    hdbmst_status st = read_status(b.st, h, s);
+    if (st != HDBMST_OK) return st;
+    if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+    return HDBMST_OK;
+}
+
+// ------------------------------------------------------------------ MST layout
+
+struct MstPlan {
+    int n, d, dk, L;
+    int64_t n_pad;
+    int index_bits;
+};
+
+MstPlan make_mst_plan(int64_t n, int d, int L) {
+    MstPlan p{};
+    p.n = static_cast<int>(n);
+    p.d = d;
+    p.dk = static_cast<int>(round_up(d, kBK));
+    p.L = L;
+    p.n_pad = round_up(std::max<int64_t>(n, 1), kBM);
+    int bits = 1;
+    while (bits < 31 && (int64_t(1) << bits) <= std::max<int64_t>(n - 1, 1)) ++bits;
+    p.index_bits = bits;
+    return p;
+}
+
+struct MstBufs {
+    float *Xf, *norm, *Xa, *act_core;
+    int *act_comp, *act_idx, *comp, *parent, *root_of;
+    unsigned long long *cand, *ck64;
+    unsigned *chi, *ub;
+    unsigned char *proven;
+    int *e_lo, *e_hi, *lo2, *hi2;
+    unsigned *e_w, *w2, *hist;
+    DevStatus *st;
+};
+
+void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
+    const size_t n = static_cast<size_t>(std::max(p.n, 1));
+    b.Xf = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.norm = c.take<float>(p.n_pad);
+    b.Xa = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.act_core = c.take<float>(p.n_pad);
+    b.act_comp = c.take<int>(p.n_pad);
+    b.act_idx = c.take<int>(n);
+    b.comp = c.take<int>(n);
+    b.parent = c.take<int>(n);
+    b.root_of = c.take<int>(n);
+    b.cand = c.take<unsigned long long>(n);
+    b.ck64 = c.take<unsigned long long>(n);
+    b.chi = c.take<unsigned>(n);
+    b.ub = c.take<unsigned>(n);
+    b.proven = c.take<unsigned char>(n);
+    b.e_lo = c.take<int>(n);
+    b.e_hi = c.take<int>(n);
+    b.e_w = c.take<unsigned>(n);
+    b.lo2 = c.take<int>(n);
+    b.hi2 = c.take<int>(n);
+    b.w2 = c.take<unsigned>(n);
+    b.hist = c.take<unsigned>(sort_hist_entries(static_cast<int>(n)));
+    b.st = c.take<DevStatus>(1);
+}
+
+bool bad_sizes(int64_t n, int d) { return n < 0 || d < 1; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int hdbmst_version(void) { return 100; }
+
+const char *hdbmst_status_string(hdbmst_status status) {
+    switch (status) {
+        case HDBMST_OK: return "ok";
+        case HDBMST_ERR_ARG: return "invalid argument";
+        case HDBMST_ERR_UNSUPPORTED: return "unsupported size (k, min_samples, d or n beyond the build's limits)";
+        case HDBMST_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case HDBMST_ERR_NONFINITE: return "non-finite value in the points or core distances";
+        case HDBMST_ERR_NOCONVERGE: return "Boruvka made no progress";
+        case HDBMST_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+size_t hdbmst_workspace_bytes(int op, int64_t n, int64_t m, int d, int k) {
+    if (d < 1 || d > HDBMST_DMAX || n < 0 || n > HDBMST_NMAX) return 0;
+    Carver c(nullptr);
+    if (op == HDBMST_OP_KNN) {
+        if (m < 1 || m > HDBMST_NMAX || k < 1 || k > HDBMST_KMAX) return 0;
+        KnnPlan p = make_knn_plan(n, m, d, k, false);
+        KnnBufs b{};
+        carve_knn(c, p, b, false);
+        return c.off;
+    }
+    if (op == HDBMST_OP_CORE) {
+        if (n < 1 || k < 1 || k > n || k + 1 > HDBMST_KMAX) return 0;
+        const int L = static_cast<int>(std::min<int64_t>(k + 1, n));
+        KnnPlan p = make_knn_plan(n, n, d, L, true);
+        KnnBufs b{};
+        carve_knn(c, p, b, true);
+        return c.off;
+    }
+    if (op == HDBMST_OP_MST) {
+        if (k < 0 || k > HDBMST_KMAX) return 0;
+        MstPlan p = make_mst_plan(n, d, k);
+        MstBufs b{};
+        carve_mst(c, p, b);
+        return c.off;
+    }
+    return 0;
+}
+
+hdbmst_status hdbmst_knn(const float *X, int64_t ldx, int64_t n, const float *Y, int64_t ldy,
+                         int64_t m, int d, int k, int32_t *out_idx, float *out_dist,
+                         void *workspace, size_t workspace_bytes, hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bad_sizes(n, d) || m < 1 || k < 1 || k > m || ldx < n || ldy < m) return HDBMST_ERR_ARG;
+    if (k > HDBMST_KMAX || d > HDBMST_DMAX || n > HDBMST_NMAX || m > HDBMST_NMAX)
+        return HDBMST_ERR_UNSUPPORTED;
+    if (n == 0) return HDBMST_OK;
+    if (!X || !Y || !out_idx || !out_dist) return HDBMST_ERR_ARG;
+    const size_t need = hdbmst_workspace_bytes(HDBMST_OP_KNN, n, m, d, k);
+    if (!ws_ok(workspace, workspace_bytes, need)) return HDBMST_ERR_WORKSPACE;
+    const bool alias = (X == Y && ldx == ldy && n == m);
+    KnnPlan p = make_knn_plan(n, m, d, k, alias);
+    Carver c(workspace);
+    KnnBufs b{};
+    carve_knn(c, p, b, false);
+    return run_knn(p, b, X, ldx, Y, ldy, out_idx, out_dist, nullptr, 0, s);
+}
+
+hdbmst_status hdbmst_core_distances(const float *X, int64_t ldx, int64_t n, int d,
+                                    int min_samples, float *out_core, int32_t *out_knn_idx,
+                                    float *out_knn_dist, void *workspace,
+                                    size_t workspace_bytes, hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bad_sizes(n, d) || n < 1 || ldx < n || min_samples < 1 || min_samples > n)
+        return HDBMST_ERR_ARG;
+    if ((out_knn_idx == nullptr) != (out_knn_dist == nullptr)) return HDBMST_ERR_ARG;
+    if (min_samples + 1 > HDBMST_KMAX || d > HDBMST_DMAX || n > HDBMST_NMAX)
+        return HDBMST_ERR_UNSUPPORTED;
+    if (!X || !out_core) return HDBMST_ERR_ARG;
+    const size_t need = hdbmst_workspace_bytes(HDBMST_OP_CORE, n, 0, d, min_samples);
+    if (!ws_ok(workspace, workspace_bytes, need)) return HDBMST_ERR_WORKSPACE;
+    const int L = static_cast<int>(std::min<int64_t>(min_samples + 1, n));
+    KnnPlan p = make_knn_plan(n, n, d, L, true);
+    Carver c(workspace);
+    KnnBufs b{};
+    carve_knn(c, p, b, true);
+    int32_t *li = out_knn_idx ? out_knn_idx : b.list_idx;
+    float *ld = out_knn_dist ? out_knn_dist : b.list_dist;
+    return run_knn(p, b, X, ldx, X, ldx, li, ld, out_core, min_samples, s);
+}
+
+hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const float *core,
+                            const int32_t *knn_idx, const float *knn_dist, int knn_len,
+                            int32_t *out_edges, float *out_w, void *workspace,
+                            size_t workspace_bytes, hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bad_sizes(n, d) || ldx < n) return HDBMST_ERR_ARG;
+    if ((knn_idx == nullptr) != (knn_dist == nullptr)) return HDBMST_ERR_ARG;
+    const bool shortcuts = knn_idx != nullptr;
+    if (shortcuts && (knn_len < 1 || knn_len > n)) return HDBMST_ERR_ARG;
+    if (d > HDBMST_DMAX || n > HDBMST_NMAX || (shortcuts && knn_len > HDBMST_KMAX))
+        return HDBMST_ERR_UNSUPPORTED;
+    if (n <= 1) return HDBMST_OK;
+    if (!X || !core || !out_edges || !out_w) return HDBMST_ERR_ARG;
+    const int L = shortcuts ? knn_len : 0;
+    const size_t need = hdbmst_workspace_bytes(HDBMST_OP_MST, n, 0, d, L);
+    if (!ws_ok(workspace, workspace_bytes, need)) return HDBMST_ERR_WORKSPACE;
+
+    MstPlan p = make_mst_plan(n, d, L);
+    Carver c(workspace);
+    MstBufs b{};
+    carve_mst(c, p, b);
+    const int N = p.n;
+    const int slots = 2 * sm_count();
+    const int col_tiles = static_cast<int>(p.n_pad / kBN);
+
+    CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
+    LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, nullptr,
+                                  b.norm, &b.st->status, nullptr, s));
+    LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
+    LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, s));
+
+    int max_rounds = 2;
+    while ((int64_t(1) << (max_rounds - 2)) < N) ++max_rounds;  // ceil(log2 n) + 2
+    int edges = 0;
+    DevStatus h{};
+    for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
+        ScanArgs sa{};
+        int na = N;
+        if (shortcuts) {
+            LAUNCH(K_NBR_CANDIDATE, s, launch_nbr_candidate(N, L, knn_idx, knn_dist, core, b.comp,
+                                                            b.cand, b.proven, b.ub,
+                                                            &b.st->status, s));
+            CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
+            LAUNCH(K_ACTIVE, s, launch_active(N, b.proven, core, b.comp, b.ub, b.act_idx,
+                                              &b.st->act_count, s));
+            hdbmst_status rs = read_status(b.st, h, s);
+            if (rs != HDBMST_OK) return rs;
+            if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+            if (h.status & kStatusBadList) return HDBMST_ERR_ARG;
+            na = h.act_count;
+            if (na > 0) {
+                const int na_pad = static_cast<int>(round_up(na, kBM));
+                LAUNCH(K_GATHER, s, launch_gather(na, na_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
+                                                  b.comp, b.Xa, b.act_core, b.act_comp, s));
+                sa.Xa = b.Xa;
+                sa.lda = na_pad;
+                sa.act_idx = b.act_idx;
+                sa.act_core = b.act_core;
+                sa.act_comp = b.act_comp;
+            }
+        } else {
+            sa.Xa = b.Xf;
+            sa.lda = p.n_pad;
+            sa.act_idx = nullptr;
+            sa.act_core = core;
+            sa.act_comp = b.comp;
+        }
+        if (na > 0) {
+            sa.na = na;
+            sa.Xf = b.Xf;
+            sa.ldx = p.n_pad;
+            sa.core = core;
+            sa.comp = b.comp;
+            sa.n = N;
+            sa.dk = p.dk;
+            sa.col_tiles = col_tiles;
+            const int row_tiles = (na + kBM - 1) / kBM;
+            const int S0 = choose_splits(row_tiles, col_tiles, slots);
+            const int tps = (col_tiles + S0 - 1) / S0;
+            const int S = (col_tiles + tps - 1) / tps;
+            sa.tiles_per_split = tps;
+            sa.cand = b.cand;
+            LAUNCH(K_SCAN, s, launch_scan(sa, row_tiles, S, s));
+        }
+        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, s, 0));
+        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, s, 1));
+        LAUNCH(K_HOOK, s, launch_hook(N, b.comp, b.ck64, b.chi, b.parent, b.e_lo, b.e_hi,
+                                      reinterpret_cast<float *>(b.e_w), &b.st->edge_count,
+                                      &b.st->status, s));
+        LAUNCH(K_ROOTS, s, launch_roots(N, b.comp, b.parent, b.root_of, &b.st->status, s));
+        LAUNCH(K_RELABEL, s, launch_relabel(N, b.comp, b.root_of, b.cand, b.ck64, b.chi, b.ub, s));
+        hdbmst_status rs = read_status(b.st, h, s);
+        if (rs != HDBMST_OK) return rs;
+        if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+        if (h.status & (kStatusNoConverge | kStatusOverflow)) return HDBMST_ERR_NOCONVERGE;
+        if (h.edge_count <= edges) return HDBMST_ERR_NOCONVERGE;
+        edges = h.edge_count;
+    }
+    if (edges != N - 1) return HDBMST_ERR_NOCONVERGE;
+    cudaError_t e = sort_edges(N - 1, p.index_bits, b.e_w, b.e_lo, b.e_hi, b.w2, b.lo2, b.hi2,
+                               b.hist, out_edges, out_w, s, before, after);
+    return e == cudaSuccess ? HDBMST_OK : HDBMST_ERR_CUDA;
+}
+
+uint64_t hdbmst_launch_count(void) { return g_launches.load(); }
+
+void hdbmst_profile_enable(int on) { g_prof = on != 0; }
+
+int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels) {
+    double ms[K_COUNT] = {0};
+    int64_t cnt[K_COUNT] = {0};
+    for (ProfRec &r : g_recs) {
+        if (r.b) {
+            float t = 0.f;
+            if (cudaEventSynchronize(r.b) == cudaSuccess &&
+                cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+                ms[r.id] += t;
+                cnt[r.id] += 1;
+            }
+            g_pool.push_back(r.b);
+        }
+        g_pool.push_back(r.a);
+    }
+    g_recs.clear();
+    for (int i = 0; i < std::min(max_kernels, static_cast<int>(K_COUNT)); ++i) {
+        if (total_ms) total_ms[i] = ms[i];
+        if (launches) launches[i] = cnt[i];
+    }
+    return K_COUNT;
+}
+
+const char *hdbmst_profile_kernel_name(int i) {
+    return (i >= 0 && i < K_COUNT) ? kKernelNames[i] : "";
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// Device helpers shared by the kernels of the hdbmst library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace hdbmst {
+
+// Distance-tile geometry: a CTA of 256 threads owns 128 rows x 128 columns,
+// each thread an 8 x 8 register block; features stream in chunks of 16.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 16;
+constexpr int kThreads = 256;
+
+// Bits of the device status word.
+constexpr unsigned kStatusNonFinite = 1u;
+constexpr unsigned kStatusNoConverge = 2u;
+constexpr unsigned kStatusOverflow = 4u;
+constexpr unsigned kStatusBadList = 8u;
+
+constexpr unsigned long long kNoKey = ~0ull;
+
+__host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+// One feature of the distance every kernel uses: the float32 difference,
+// squared and added to the running float32 sum by one fused multiply-add.
+// Summed in ascending feature order this is the library's single definition
+// of the squared distance (symmetric: a - b and b - a differ only in sign).
+__device__ __forceinline__ float sqdiff_fma(float a, float b, float acc) {
+    const float t = __fsub_rn(a, b);
+    return __fmaf_rn(t, t, acc);
+}
+
+// A non-negative float and a 32-bit index packed so that unsigned 64-bit
+// order is (value, index) order: non-negative IEEE floats order like their bits.
+__device__ __forceinline__ unsigned long long key64(float w, unsigned idx) {
+    return (static_cast<unsigned long long>(__float_as_uint(w)) << 32) | idx;
+}
+__device__ __forceinline__ float key_w(unsigned long long k) {
+    return __uint_as_float(static_cast<unsigned>(k >> 32));
+}
+__device__ __forceinline__ unsigned key_i(unsigned long long k) { return static_cast<unsigned>(k); }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// 16-byte asynchronous global -> shared copy (L2 only), and its group fences.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+}  // namespace hdbmst

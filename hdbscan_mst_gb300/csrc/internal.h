@@ -1,0 +1,141 @@
+// Host-side launch wrappers of the hdbmst kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace hdbmst {
+
+// ---------------------------------------------------------------- pack.cu
+// Copy a caller [d, n] set (leading dim ld) into the padded feature-major
+// buffer Xf [dk][n_pad] and, if Xp != nullptr, the point-major buffer
+// Xp [n_pad][dk]; write norm[i] = sum of x^2 (+inf for padding points);
+// flag non-finite values; raise *nbmax_bits to the largest norm's bits.
+cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
+                        float *Xp, float *norm, unsigned *status, unsigned *nbmax_bits,
+                        cudaStream_t s);
+// Flag core distances that are negative or not finite.
+cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
+
+// ---------------------------------------------------------------- knn.cu
+struct KnnTileArgs {
+    const float *Xf;     // [dk][ldx] query rows, feature-major, padded
+    const float *Yf;     // [dk][ldy] searched columns, feature-major, padded
+    const float *ynorm;  // [ldy] squared norms, +inf past the last column
+    int64_t ldx, ldy;
+    int dk;
+    int row_base;        // first query row of this chunk
+    int row_end;         // one past the last valid query row (n)
+    int chunk_rows_pad;  // rows per split slab of the partial lists
+    int col_tiles;       // ceil(m / kBN)
+    int tiles_per_split;
+    float *part_key;     // [S][chunk_rows_pad][KP] approximate keys
+    int *part_idx;       // [S][chunk_rows_pad][KP] column indices
+};
+cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
+                            cudaStream_t s);
+
+struct KnnRefineArgs {
+    const float *part_key;
+    const int *part_idx;
+    int splits, chunk_rows_pad, row_base, row_end;
+    const float *Xp, *Yp;  // point-major [.][dk]
+    const float *xnorm;
+    const unsigned *nbmax_bits;
+    int d, dk, k, m;
+    int core_rank;  // 1-based list position copied to out_core (0: none)
+    int32_t *out_idx;
+    float *out_dist;
+    float *out_core;
+    int *fb_count;
+    int *fb_rows;
+};
+cudaError_t launch_knn_refine(int KP, const KnnRefineArgs &a, int rows, cudaStream_t s);
+
+struct KnnExactArgs {
+    const int *fb_count;
+    const int *fb_rows;
+    const float *Xp, *Yp;
+    int dk, k, m;
+    int core_rank;
+    int32_t *out_idx;
+    float *out_dist;
+    float *out_core;
+};
+cudaError_t launch_knn_exact(int KP, const KnnExactArgs &a, int blocks, cudaStream_t s);
+
+// ---------------------------------------------------------------- boruvka.cu
+cudaError_t launch_mst_init(int n, int *comp, unsigned long long *cand, unsigned long long *ck64,
+                            unsigned *chi, unsigned *ub, cudaStream_t s);
+cudaError_t launch_nbr_candidate(int n, int L, const int32_t *kidx, const float *kdist,
+                                 const float *core, const int *comp, unsigned long long *cand,
+                                 unsigned char *proven, unsigned *ub, unsigned *status,
+                                 cudaStream_t s);
+cudaError_t launch_active(int n, const unsigned char *proven, const float *core, const int *comp,
+                          const unsigned *ub, int *act_idx, int *act_count, cudaStream_t s);
+cudaError_t launch_gather(int na, int na_pad, int dk, const int *act_idx, const float *Xf,
+                          int64_t ldx, const float *core, const int *comp, float *Xa,
+                          float *act_core, int *act_comp, cudaStream_t s);
+
+struct ScanArgs {
+    const float *Xa;        // [dk][lda] active rows, feature-major
+    int64_t lda;
+    const int *act_idx;     // [na] global index of each active row, or nullptr (identity)
+    const float *act_core;  // [na]
+    const int *act_comp;    // [na]
+    int na;
+    const float *Xf;        // [dk][ldx] all points
+    int64_t ldx;
+    const float *core;      // [n]
+    const int *comp;        // [n]
+    int n;
+    int dk;
+    int col_tiles, tiles_per_split;
+    unsigned long long *cand;  // [n] per-point least edge key, lowered by atomicMin
+};
+cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);
+
+cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *comp,
+                            unsigned long long *ck64, unsigned *chi, cudaStream_t s,
+                            int stage);
+cudaError_t launch_hook(int n, const int *comp, const unsigned long long *ck64,
+                        const unsigned *chi, int *parent, int *e_lo, int *e_hi, float *e_w,
+                        int *edge_count, unsigned *status, cudaStream_t s);
+cudaError_t launch_roots(int n, const int *comp, const int *parent, int *root_of,
+                         unsigned *status, cudaStream_t s);
+cudaError_t launch_relabel(int n, int *comp, const int *root_of, unsigned long long *cand,
+                           unsigned long long *ck64, unsigned *chi, unsigned *ub,
+                           cudaStream_t s);
+
+// ---------------------------------------------------------------- sort.cu
+// Sort N edges by (w, lo, hi) ascending and write (lo, hi) pairs and weights.
+// tmp buffers hold N entries each; hist holds sort_hist_entries(N) entries.
+size_t sort_hist_entries(int N);
+int sort_launches(int N, int index_bits);
+cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, unsigned *w2,
+                       int *lo2, int *hi2, unsigned *hist, int32_t *out_edges, float *out_w,
+                       cudaStream_t s, void (*before)(int, cudaStream_t),
+                       void (*after)(int, cudaStream_t));
+
+// Kernel ids for launch accounting and profiling.
+enum KernelId {
+    K_PACK = 0,
+    K_CHECK_CORE,
+    K_KNN_TILE,
+    K_KNN_REFINE,
+    K_KNN_EXACT,
+    K_MST_INIT,
+    K_NBR_CANDIDATE,
+    K_ACTIVE,
+    K_GATHER,
+    K_SCAN,
+    K_COMP_MIN,
+    K_HOOK,
+    K_ROOTS,
+    K_RELABEL,
+    K_SORT,
+    K_COUNT
+};
+
+}  // namespace hdbmst

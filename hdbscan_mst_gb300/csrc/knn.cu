@@ -1,0 +1,504 @@
+// K1 / K1r / K1x: exact k-nearest neighbours.
+//
+// Page "Kilosort4 clustering and matching" (neuro-kitchen dsp-kitchen
+// gpu/clustering), section "k-nearest neighbours are a matrix product": with
+// |x - y|^2 = |x|^2 + |y|^2 - 2 x.y the distances of a block of rows to a set
+// are one matrix product plus two norm vectors, a small selection keeps the
+// smallest per row, and rows go in chunks so scratch stays bounded.  Page
+// "HDBSCAN" (gpu/hdbscan), section "The hang": the nearest list is kept by a
+// fixed sequence of compare-and-swaps, no loop waits on a flag, and equal
+// distances keep their order (lowest index first).
+//
+// The GB300 design:
+//  * K1 (knn_tile_kernel): a 128 x 128 register-blocked FFMA tile (8 x 8 per
+//    thread) over feature chunks of 16 staged in shared memory by cp.async
+//    double buffering.  The product never reaches global memory: per pair the
+//    epilogue forms t = |y|^2 - 2 x.y (the row's |x|^2 is a constant shift)
+//    and tests it against the row's current KP-th best.  A warp owns 16 whole
+//    rows, so candidates go to warp-private shared buffers and one lane per
+//    row folds them into the row's sorted list with unrolled compare-and-swap;
+//    no block-wide barrier is spent on selection.  Columns are split across
+//    CTAs so the grid fills every SM; each CTA writes a partial list.
+//  * K1r (knn_refine_kernel): merges the partial lists, re-evaluates every kept
+//    candidate with the library's exact distance (direct differences), sorts
+//    by (dist, index) and proves, from a bound on the expansion's rounding
+//    error, that no dropped column could enter the top k.  Rows it cannot prove
+//    are queued for K1x.
+//  * K1x (knn_exact_kernel): searches queued rows again with the exact
+//    distance over every column.
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hdbmst {
+
+namespace {
+
+constexpr int kCap = 16;               // candidate slots per row per merge
+constexpr int kMaxPass = kBN / kCap + 2;  // pushes per tile are bounded by kBN per row
+
+template <int KP>
+struct TileSmem {
+    float As[2][kBK][kBM];
+    float Bs[2][kBK][kBN];
+    float lkey[kBM][KP + 1];  // +1: rows of consecutive lanes fall in different banks
+    int lidx[kBM][KP + 1];
+    float ckey[kBM][kCap + 1];
+    int cidx[kBM][kCap + 1];
+    int ccnt[kBM];
+    float tau[kBM];
+};
+
+// Local row of register-block row i (0..7) of thread row ty, and local column
+// of block column j of thread column tx: two 4-wide halves 64 apart, so the
+// float4 shared loads of a warp are conflict-free.
+__device__ __forceinline__ int row_of(int ty, int i) { return (i < 4 ? 0 : 60) + ty * 4 + i; }
+__device__ __forceinline__ int col_of(int tx, int j) { return (j < 4 ? 0 : 60) + tx * 4 + j; }
+// The 16 local rows that warp w owns (thread rows ty = 2w and 2w + 1).
+__device__ __forceinline__ int warp_row(int w, int q) { return (q < 8 ? 0 : 56) + w * 8 + q; }
+
+__device__ __forceinline__ bool key_less(float a, int ai, float b, int bi) {
+    return a < b || (a == b && ai < bi);
+}
+
+// Fold row r's queued candidates into its sorted list.  Each insertion is
+// the same fixed compare-and-swap pass as a register list would take (the
+// newcomer replaces the last entry and sinks), done on the row's shared
+// memory slots so the 64 tile accumulators keep their registers.  The pass
+// stops early once the newcomer is in place; its length is bounded by KP.
+template <int KP>
+__device__ __forceinline__ void merge_row(TileSmem<KP> &S, int r) {
+    int cnt = S.ccnt[r];
+    if (cnt == 0) return;
+    cnt = min(cnt, kCap);
+    S.ccnt[r] = 0;
+    float *lk = S.lkey[r];
+    int *li = S.lidx[r];
+    for (int c = 0; c < cnt; ++c) {
+        const float t = S.ckey[r][c];
+        const int j = S.cidx[r][c];
+        if (!key_less(t, j, lk[KP - 1], li[KP - 1])) continue;
+        int p = KP - 1;
+#pragma unroll 4
+        for (int s = 0; s < KP - 1; ++s) {
+            const float pk = lk[p - 1];
+            const int pi = li[p - 1];
+            if (!key_less(t, j, pk, pi)) break;
+            lk[p] = pk;
+            li[p] = pi;
+            --p;
+        }
+        lk[p] = t;
+        li[p] = j;
+    }
+    S.tau[r] = lk[KP - 1];
+}
+
+// Rare path of the selection: some row's buffer filled up (in practice only in
+// a CTA's first tiles, while the thresholds are still loose).  Retry the
+// pending pairs against the tightened thresholds.  Each pass stores kCap
+// candidates of every row that still has pending ones, so kMaxPass passes
+// always suffice; the bound is a constant, never a flag.  Kept out of line:
+// it takes the tile's values through a local copy so that the main loop's
+// accumulators never leave registers.
+template <int KP>
+__device__ __noinline__ void overflow_retry(TileSmem<KP> &S, const float *tv,
+                                            unsigned long long pend, int col0, int warp,
+                                            int lane, int ty, int tx) {
+    for (int pass = 1; pass < kMaxPass; ++pass) {
+        if (!__any_sync(0xffffffffu, pend != 0ull)) break;
+        unsigned long long rem = pend;
+        for (int it = 0; it < 64 && rem != 0ull; ++it) {
+            const int b = __ffsll(static_cast<long long>(rem)) - 1;
+            rem &= rem - 1ull;
+            const int i = b >> 3, j = b & 7;
+            const int r = row_of(ty, i);
+            const float t = tv[b];
+            if (t < S.tau[r]) {
+                const int pos = atomicAdd(&S.ccnt[r], 1);
+                if (pos < kCap) {
+                    S.ckey[r][pos] = t;
+                    S.cidx[r][pos] = col0 + col_of(tx, j);
+                    pend &= ~(1ull << b);
+                }
+            } else {
+                pend &= ~(1ull << b);
+            }
+        }
+        __syncwarp();
+        if (lane < 16) merge_row<KP>(S, warp_row(warp, lane));
+        __syncwarp();
+    }
+}
+
+// Selection epilogue of one 128-column tile, run by each warp on its own rows.
+template <int KP>
+__device__ __forceinline__ void tile_epilogue(TileSmem<KP> &S, float (&acc)[8][8],
+                                              const float *__restrict__ ynorm, int col0,
+                                              int warp, int lane, int ty, int tx) {
+    float yn[8];
+    {
+        const float4 v0 = __ldg(reinterpret_cast<const float4 *>(ynorm + col0 + tx * 4));
+        const float4 v1 = __ldg(reinterpret_cast<const float4 *>(ynorm + col0 + 64 + tx * 4));
+        yn[0] = v0.x; yn[1] = v0.y; yn[2] = v0.z; yn[3] = v0.w;
+        yn[4] = v1.x; yn[5] = v1.y; yn[6] = v1.z; yn[7] = v1.w;
+    }
+    unsigned long long pend = 0ull;  // pairs that found their row's buffer full
+    bool pushed = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = row_of(ty, i);
+        const float tau = S.tau[r];
+        float mn = INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[i][j] = __fmaf_rn(-2.f, acc[i][j], yn[j]);
+            mn = fminf(mn, acc[i][j]);
+        }
+        if (mn < tau) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (acc[i][j] < tau) {
+                    const int pos = atomicAdd(&S.ccnt[r], 1);
+                    if (pos < kCap) {
+                        S.ckey[r][pos] = acc[i][j];
+                        S.cidx[r][pos] = col0 + col_of(tx, j);
+                        pushed = true;
+                    } else {
+                        pend |= 1ull << (i * 8 + j);
+                    }
+                }
+            }
+        }
+    }
+    if (!__any_sync(0xffffffffu, pushed || pend != 0ull)) return;
+    __syncwarp();
+    if (lane < 16) merge_row<KP>(S, warp_row(warp, lane));
+    __syncwarp();
+    if (__any_sync(0xffffffffu, pend != 0ull)) {
+        float tv[64];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tv[i * 8 + j] = acc[i][j];
+        overflow_retry<KP>(S, tv, pend, col0, warp, lane, ty, tx);
+    }
+}
+
+template <int KP>
+__global__ void __launch_bounds__(kThreads, 2) knn_tile_kernel(const KnnTileArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    TileSmem<KP> &S = *reinterpret_cast<TileSmem<KP> *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = tid >> 4, tx = tid & 15;
+    const int row_tile = blockIdx.x;
+    const int split = blockIdx.y;
+    const int r0 = a.row_base + row_tile * kBM;
+    const int ct_begin = split * a.tiles_per_split;
+    const int ct_end = min(ct_begin + a.tiles_per_split, a.col_tiles);
+
+    if (lane < 16) {
+        const int r = warp_row(warp, lane);
+#pragma unroll
+        for (int p = 0; p < KP; ++p) {
+            S.lkey[r][p] = INFINITY;
+            S.lidx[r][p] = INT_MAX;
+        }
+        S.ccnt[r] = 0;
+        S.tau[r] = INFINITY;
+    }
+    __syncwarp();
+
+    const int nchunks = a.dk / kBK;
+    const int nsteps = max(ct_end - ct_begin, 0) * nchunks;
+
+    auto issue = [&](int step, int buf) {
+        const int ct = ct_begin + step / nchunks;
+        const int kc = step - (step / nchunks) * nchunks;
+        const float *ga = a.Xf + static_cast<int64_t>(kc * kBK) * a.ldx + r0;
+        const float *gb = a.Yf + static_cast<int64_t>(kc * kBK) * a.ldy + static_cast<int64_t>(ct) * kBN;
+#pragma unroll
+        for (int v = tid; v < kBK * kBM / 4; v += kThreads) {
+            const int kr = v >> 5, c4 = (v & 31) * 4;
+            cp_async16(&S.As[buf][kr][c4], ga + static_cast<int64_t>(kr) * a.ldx + c4);
+            cp_async16(&S.Bs[buf][kr][c4], gb + static_cast<int64_t>(kr) * a.ldy + c4);
+        }
+        cp_async_commit();
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    if (nsteps > 0) issue(0, 0);
+    for (int step = 0; step < nsteps; ++step) {
+        const int buf = step & 1;
+        cp_async_wait_all();
+        __syncthreads();
+        if (step + 1 < nsteps) issue(step + 1, buf ^ 1);
+#pragma unroll
+        for (int kk = 0; kk < kBK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][64 + tx * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+        }
+        if ((step + 1) % nchunks == 0) {
+            const int ct = ct_begin + step / nchunks;
+            tile_epilogue<KP>(S, acc, a.ynorm, ct * kBN, warp, lane, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        }
+    }
+    __syncwarp();
+    if (lane < 16) {
+        const int r = warp_row(warp, lane);
+        const int local = row_tile * kBM + r;
+        if (a.row_base + local < a.row_end) {
+            const int64_t o = (static_cast<int64_t>(split) * a.chunk_rows_pad + local) * KP;
+#pragma unroll
+            for (int p = 0; p < KP; ++p) {
+                a.part_key[o + p] = S.lkey[r][p];
+                a.part_idx[o + p] = S.lidx[r][p];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ refine
+
+// Groups of KP lanes; each group owns one query row.
+template <int KP>
+__global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) {
+    __shared__ float sel_t[128];
+    __shared__ int sel_j[128];
+    const int gl = threadIdx.x % KP;
+    const int group = threadIdx.x / KP;
+    const int local = blockIdx.x * (128 / KP) + group;
+    const int row = a.row_base + local;
+    const bool active = row < a.row_end;
+    const int leader = (threadIdx.x & 31) & ~(KP - 1);
+
+    // 1. Merge the sorted partial lists of the splits into the KP best by
+    //    (t, index); one lane walks the list heads.
+    float A = INFINITY;
+    if (active && gl == 0) {
+        int head[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) head[s] = 0;
+        for (int p = 0; p < KP; ++p) {
+            float bt = INFINITY;
+            int bj = INT_MAX, bs = -1;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                if (s < a.splits && head[s] < KP) {
+                    const int64_t o = (static_cast<int64_t>(s) * a.chunk_rows_pad + local) * KP + head[s];
+                    const float t = a.part_key[o];
+                    const int j = a.part_idx[o];
+                    if (key_less(t, j, bt, bj)) {
+                        bt = t;
+                        bj = j;
+                        bs = s;
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (s == bs) ++head[s];
+            sel_t[group * KP + p] = bt;
+            sel_j[group * KP + p] = bj;
+        }
+        A = sel_t[group * KP + KP - 1];
+    }
+    __syncwarp();
+    A = __shfl_sync(0xffffffffu, A, leader);
+
+    // 2. Exact distance of every kept candidate.
+    const int j = sel_j[group * KP + gl];
+    unsigned long long key = kNoKey;
+    if (active && j >= 0 && j < a.m) {
+        const float4 *xp = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(row) * a.dk);
+        const float4 *yp = reinterpret_cast<const float4 *>(a.Yp + static_cast<int64_t>(j) * a.dk);
+        float acc = 0.f;
+        for (int q = 0; q < a.dk / 4; ++q) {
+            const float4 x = __ldg(xp + q), y = __ldg(yp + q);
+            acc = sqdiff_fma(x.x, y.x, acc);
+            acc = sqdiff_fma(x.y, y.y, acc);
+            acc = sqdiff_fma(x.z, y.z, acc);
+            acc = sqdiff_fma(x.w, y.w, acc);
+        }
+        key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+    }
+
+    // 3. Bitonic sort of the group's KP keys, ascending.
+#pragma unroll
+    for (int size = 2; size <= KP; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
+            const bool up = (gl & size) == 0;
+            const bool lower = (gl & stride) == 0;
+            key = (lower == up) ? min(key, other) : max(key, other);
+        }
+    }
+
+    if (!active) return;
+    const int64_t o = static_cast<int64_t>(row) * a.k;
+    if (gl < a.k) {
+        a.out_idx[o + gl] = static_cast<int32_t>(key_i(key));
+        a.out_dist[o + gl] = key_w(key);
+    }
+    if (a.out_core && gl == a.core_rank - 1) a.out_core[row] = key_w(key);
+
+    // 4. Proof that the kept set holds the exact top k.  Every dropped column
+    //    z has t_z >= A.  With u = 2^-24, the expansion t + |x|^2 differs from
+    //    the true squared distance by at most E = (2d + 4) u (|x|^2 + max|y|^2)
+    //    (dot product and norms are FMA chains of length d, plus two
+    //    roundings), and the exact float32 evaluation is at least
+    //    (1 - (d + 3) u) times the true value.  If that lower bound still
+    //    exceeds the k-th kept distance squared (with sqrt rounding slack),
+    //    no dropped column can rank in the top k.
+    if (gl == a.k - 1 && A < INFINITY) {
+        const double u = 5.9604644775390625e-8;
+        const double dk = key_w(key);
+        const double na = a.xnorm[row];
+        const double nb = __uint_as_float(*a.nbmax_bits);
+        const double E = (2.0 * a.d + 4.0) * u * 1.01 * (na + nb);
+        const double lb = (static_cast<double>(A) + na - E) * (1.0 - (a.d + 3.0) * u);
+        if (!(lb * (1.0 - 4.0 * u) > dk * dk)) {
+            const int pos = atomicAdd(a.fb_count, 1);
+            a.fb_rows[pos] = row;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ exact rows
+
+template <int KP>
+__global__ void __launch_bounds__(256) knn_exact_kernel(const KnnExactArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned long long *lists = reinterpret_cast<unsigned long long *>(smem_raw);  // [256][KP]
+    float *xrow = reinterpret_cast<float *>(lists + 256 * KP);                       // [dk]
+    __shared__ unsigned long long wmin[8];
+    const int tid = threadIdx.x;
+    const int count = *a.fb_count;
+    for (int f = blockIdx.x; f < count; f += gridDim.x) {
+        const int row = a.fb_rows[f];
+        for (int q = tid; q < a.dk; q += 256) xrow[q] = a.Xp[static_cast<int64_t>(row) * a.dk + q];
+        __syncthreads();
+        unsigned long long L[KP];
+#pragma unroll
+        for (int p = 0; p < KP; ++p) L[p] = kNoKey;
+        for (int j = tid; j < a.m; j += 256) {
+            const float4 *yp = reinterpret_cast<const float4 *>(a.Yp + static_cast<int64_t>(j) * a.dk);
+            const float4 *xp = reinterpret_cast<const float4 *>(xrow);
+            float acc = 0.f;
+            for (int q = 0; q < a.dk / 4; ++q) {
+                const float4 x = xp[q], y = __ldg(yp + q);
+                acc = sqdiff_fma(x.x, y.x, acc);
+                acc = sqdiff_fma(x.y, y.y, acc);
+                acc = sqdiff_fma(x.z, y.z, acc);
+                acc = sqdiff_fma(x.w, y.w, acc);
+            }
+            const unsigned long long key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+            if (key < L[KP - 1]) {
+                L[KP - 1] = key;
+#pragma unroll
+                for (int p = KP - 1; p > 0; --p) {
+                    const unsigned long long lo = min(L[p - 1], L[p]);
+                    const unsigned long long hi = max(L[p - 1], L[p]);
+                    L[p - 1] = lo;
+                    L[p] = hi;
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < KP; ++p) lists[tid * KP + p] = L[p];
+        __syncthreads();
+        // k rounds of a block-wide minimum over the list heads (keys are unique).
+        int h = 0;
+        for (int p = 0; p < a.k; ++p) {
+            const unsigned long long mine = h < KP ? lists[tid * KP + h] : kNoKey;
+            unsigned long long m = mine;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if ((tid & 31) == 0) wmin[tid >> 5] = m;
+            __syncthreads();
+            m = wmin[0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m = min(m, wmin[w]);
+            if (mine == m && m != kNoKey) ++h;
+            if (tid == 0) {
+                const int64_t o = static_cast<int64_t>(row) * a.k + p;
+                a.out_idx[o] = static_cast<int32_t>(key_i(m));
+                a.out_dist[o] = key_w(m);
+                if (a.out_core && p == a.core_rank - 1) a.out_core[row] = key_w(m);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int KP>
+cudaError_t tile_launch(const KnnTileArgs &a, int row_tiles, int splits, cudaStream_t s) {
+    const size_t smem = sizeof(TileSmem<KP>);
+    cudaError_t e = cudaFuncSetAttribute(knn_tile_kernel<KP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    knn_tile_kernel<KP><<<dim3(row_tiles, splits), kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int KP>
+cudaError_t exact_launch(const KnnExactArgs &a, int blocks, cudaStream_t s) {
+    const size_t smem = 256 * KP * sizeof(unsigned long long) + a.dk * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(knn_exact_kernel<KP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    knn_exact_kernel<KP><<<blocks, 256, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
+                            cudaStream_t s) {
+    if (KP == 16) return tile_launch<16>(a, row_tiles, splits, s);
+    if (KP == 32) return tile_launch<32>(a, row_tiles, splits, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_knn_refine(int KP, const KnnRefineArgs &a, int rows, cudaStream_t s) {
+    const int per_block = 128 / KP;
+    const int blocks = (rows + per_block - 1) / per_block;
+    if (KP == 16)
+        knn_refine_kernel<16><<<blocks, 128, 0, s>>>(a);
+    else if (KP == 32)
+        knn_refine_kernel<32><<<blocks, 128, 0, s>>>(a);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_knn_exact(int KP, const KnnExactArgs &a, int blocks, cudaStream_t s) {
+    if (KP == 16) return exact_launch<16>(a, blocks, s);
+    if (KP == 32) return exact_launch<32>(a, blocks, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hdbmst

@@ -1,0 +1,82 @@
+// K0: pack a caller point set into the library's padded layouts and compute
+// squared norms.
+//
+// The caller's set is feature-major [d, n] with any leading dimension; the
+// distance tiles want rows padded to the tile width with 16-byte-aligned
+// strides, and the exact re-evaluation wants each point's features
+// contiguous.  One pass writes both copies and the norm |x|^2 that the
+// expansion |x|^2 + |y|^2 - 2 x.y needs (page "Kilosort4 clustering and
+// matching", gpu/clustering, "k-nearest neighbours are a matrix product").
+// Padding features and padding points are zero; a padding point's norm is
+// +inf so that it never ranks as a neighbour.
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hdbmst {
+
+namespace {
+
+__global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, int64_t ld, int n,
+                                                   int d, int n_pad, int dk,
+                                                   float *__restrict__ Xf,
+                                                   float *__restrict__ Xp,
+                                                   float *__restrict__ norm,
+                                                   unsigned *__restrict__ status,
+                                                   unsigned *__restrict__ nbmax_bits) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const bool inside = i < n_pad;
+    const bool valid = i < n;
+    float acc = 0.f;
+    bool finite = true;
+    if (inside) {
+        for (int f = 0; f < dk; f += 4) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int ff = f + q;
+                v[q] = (valid && ff < d) ? X[static_cast<int64_t>(ff) * ld + i] : 0.f;
+                finite = finite && isfinite(v[q]);
+                Xf[static_cast<int64_t>(ff) * n_pad + i] = v[q];
+                acc = __fmaf_rn(v[q], v[q], acc);
+            }
+            if (Xp)
+                *reinterpret_cast<float4 *>(Xp + static_cast<int64_t>(i) * dk + f) =
+                    make_float4(v[0], v[1], v[2], v[3]);
+        }
+        norm[i] = valid ? acc : INFINITY;
+    }
+    if (!finite) atomicOr(status, kStatusNonFinite);
+    // largest norm over valid points: warp maximum, one atomic per warp
+    unsigned bits = valid ? __float_as_uint(acc) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bits = max(bits, __shfl_xor_sync(0xffffffffu, bits, o));
+    if ((threadIdx.x & 31) == 0 && nbmax_bits && bits) atomicMax(nbmax_bits, bits);
+}
+
+__global__ void check_core_kernel(const float *__restrict__ core, int n,
+                                  unsigned *__restrict__ status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const float c = core[i];
+        if (!(isfinite(c) && c >= 0.f)) atomicOr(status, kStatusNonFinite);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
+                        float *Xp, float *norm, unsigned *status, unsigned *nbmax_bits,
+                        cudaStream_t s) {
+    const int blocks = static_cast<int>((n_pad + 255) / 256);
+    pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, norm, status, nbmax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s) {
+    check_core_kernel<<<(n + 255) / 256, 256, 0, s>>>(core, n, status);
+    return cudaGetLastError();
+}
+
+}  // namespace hdbmst

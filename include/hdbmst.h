@@ -1,0 +1,177 @@
+/*
+ * hdbmst: exact k-nearest neighbours, HDBSCAN core distances and the minimum
+ * spanning tree of the mutual-reachability distance, on one GPU (sm_103a).
+ *
+ * C ABI.  Every entry point takes plain pointers and sizes.  Unless stated
+ * otherwise a pointer is a DEVICE pointer, the caller owns every buffer
+ * (inputs, outputs and the workspace), and the library allocates no device
+ * memory.  Work is queued on `stream`; a call returns once its result is
+ * final on that stream (entry points that must read a device status word
+ * synchronise the stream before returning, as stated per call).
+ *
+ * Point sets are float32 and feature-major: a set of n points with d
+ * features is a [d, n] array with leading dimension ld >= n, feature f of
+ * point i at X[f * ld + i].  X is that set "as stored": a block of points is a
+ * transposed view of it and no copy is needed to read it (page "Kilosort4
+ * clustering and matching", neuro-kitchen dsp-kitchen gpu/clustering, section
+ * "k-nearest neighbours are a matrix product").
+ *
+ * Distance.  dist(a, b) is the float32 square root of the float32 sum of
+ * squared differences, accumulated in ascending feature order with one fused
+ * multiply-add per feature.  It is symmetric and every entry point evaluates
+ * exactly this function, so equal inputs give equal bits everywhere.
+ * Internally the k-NN search ranks candidates by the expansion
+ * |x|^2 + |y|^2 - 2 x.y (same page and section) and then re-evaluates the
+ * kept candidates with dist(); a per-row error bound proves the kept set holds
+ * the true neighbours, and rows it cannot prove are searched again exactly.
+ */
+#ifndef HDBMST_H_
+#define HDBMST_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *hdbmst_stream;
+
+typedef enum {
+    HDBMST_OK = 0,
+    HDBMST_ERR_ARG = 1,         /* a size, pointer, stride or count is invalid        */
+    HDBMST_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (k > KMAX ...) */
+    HDBMST_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
+    HDBMST_ERR_NONFINITE = 4,   /* a NaN or infinity in the points or core distances   */
+    HDBMST_ERR_NOCONVERGE = 5,  /* Boruvka made no progress in a round (cannot happen   */
+                                /* with a consistent weight function; reported, never  */
+                                /* looped on)                                          */
+    HDBMST_ERR_CUDA = 6         /* a CUDA runtime call or kernel launch failed         */
+} hdbmst_status;
+
+/* Largest k for hdbmst_knn, and largest min_samples + 1 for hdbmst_core_distances. */
+#define HDBMST_KMAX 32
+/* Largest feature count. */
+#define HDBMST_DMAX 4096
+/* Largest number of points in a set (indices are int32). */
+#define HDBMST_NMAX 1073741823LL
+
+typedef enum { HDBMST_OP_KNN = 0, HDBMST_OP_CORE = 1, HDBMST_OP_MST = 2 } hdbmst_op;
+
+/*
+ * Workspace bytes that `op` needs for these sizes (m and k are ignored where
+ * they do not apply: CORE takes k = min_samples, MST takes k = the
+ * neighbour-list length or 0).  Returns 0 for invalid sizes.  The workspace
+ * must be 256-byte aligned; its contents need no initialisation and are
+ * garbage afterwards.
+ */
+size_t hdbmst_workspace_bytes(int op, int64_t n, int64_t m, int d, int k);
+
+/*
+ * Exact k-nearest neighbours (page "Kilosort4 clustering and matching",
+ * gpu/clustering, section "k-nearest neighbours are a matrix product": the k
+ * smallest distances of each row against a set, rows in chunks so scratch
+ * stays bounded; equal distances by ascending index as on page "HDBSCAN",
+ * gpu/hdbscan, sections "The hang" and "Exact shortcuts").
+ *
+ *   X [d, n], leading dim ldx >= n: the query points.
+ *   Y [d, m], leading dim ldy >= m: the searched points (may alias X).
+ *   1 <= k <= min(m, HDBMST_KMAX), 1 <= d <= HDBMST_DMAX.
+ *   out_idx  [n, k] int32, row-major: for query i, indices into Y of its k
+ *            nearest points ordered by (dist, index); a query that is also in
+ *            Y finds itself (distance 0).
+ *   out_dist [n, k] float32: dist() of those pairs.
+ *   workspace: hdbmst_workspace_bytes(HDBMST_OP_KNN, n, m, d, k) bytes.
+ *
+ * Errors: ERR_ARG (bad sizes or NULL pointers), ERR_UNSUPPORTED (k or d too
+ * large), ERR_WORKSPACE, ERR_NONFINITE (checked on the device; the stream is
+ * synchronised once at the end to read it), ERR_CUDA.  Outputs are
+ * unspecified after an error.
+ */
+hdbmst_status hdbmst_knn(const float *X, int64_t ldx, int64_t n, const float *Y, int64_t ldy,
+                         int64_t m, int d, int k, int32_t *out_idx, float *out_dist,
+                         void *workspace, size_t workspace_bytes, hdbmst_stream stream);
+
+/*
+ * HDBSCAN core distances (page "HDBSCAN", gpu/hdbscan, section "The algorithm
+ * on the device"): core_i is the distance from point i to its
+ * min_samples-th nearest point of X, counting i itself first.
+ *
+ *   X [d, n], leading dim ldx >= n; 1 <= min_samples <= n,
+ *   min_samples + 1 <= HDBMST_KMAX.
+ *   out_core     [n] float32.
+ *   out_knn_idx  [n, L] int32 or NULL, out_knn_dist [n, L] float32 or NULL,
+ *                with L = min(min_samples + 1, n): each point's L nearest
+ *                points of X (itself included) as hdbmst_knn returns them.
+ *                Keeping one neighbour more than min_samples is what lets
+ *                hdbmst_mr_mst prove some cheapest edges without a scan
+ *                (same page, section "Exact shortcuts").  Pass both or neither.
+ *   workspace: hdbmst_workspace_bytes(HDBMST_OP_CORE, n, 0, d, min_samples).
+ *
+ * Errors as hdbmst_knn; synchronises the stream once at the end.
+ */
+hdbmst_status hdbmst_core_distances(const float *X, int64_t ldx, int64_t n, int d,
+                                    int min_samples, float *out_core, int32_t *out_knn_idx,
+                                    float *out_knn_dist, void *workspace,
+                                    size_t workspace_bytes, hdbmst_stream stream);
+
+/*
+ * Minimum spanning tree of the mutual-reachability distance
+ * w(a, b) = max(core_a, core_b, dist(a, b)) by Boruvka, ties broken by
+ * (weight, lower index, higher index) so the tree is unique (page "HDBSCAN",
+ * gpu/hdbscan, section "The algorithm on the device").  Each round finds every
+ * component's cheapest edge to another component and merges along them.
+ *
+ *   X [d, n], leading dim ldx >= n.
+ *   core [n] float32, finite and >= 0 (normally hdbmst_core_distances' output).
+ *   knn_idx [n, L], knn_dist [n, L] (L = knn_len) or both NULL: when given,
+ *            the rounds use the two exact shortcuts of section "Exact
+ *            shortcuts" (a listed neighbour edge that reaches the point's own
+ *            core distance is its cheapest edge when the list provably holds
+ *            every point within that distance; a point whose core distance
+ *            exceeds its component's lightest neighbour edge is not scanned).
+ *            The lists MUST be exact nearest-neighbour lists of X under dist()
+ *            ordered by (dist, index), as hdbmst_core_distances writes them;
+ *            the tree is the same with or without them.
+ *   out_edges [n - 1, 2] int32 (lo, hi) with lo < hi, and out_w [n - 1]
+ *            float32 weights, ordered by (w, lo, hi).  n = 1 writes nothing.
+ *   workspace: hdbmst_workspace_bytes(HDBMST_OP_MST, n, 0, d, knn_len).
+ *
+ * The host reads one small status block per Boruvka round (at most
+ * ceil(log2 n) + 1 rounds), so this call synchronises the stream each round.
+ * Errors: ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE (points or
+ * core), ERR_NOCONVERGE, ERR_CUDA.
+ */
+hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const float *core,
+                            const int32_t *knn_idx, const float *knn_dist, int knn_len,
+                            int32_t *out_edges, float *out_w, void *workspace,
+                            size_t workspace_bytes, hdbmst_stream stream);
+
+/* Human-readable text of a status code (a static string). */
+const char *hdbmst_status_string(hdbmst_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int hdbmst_version(void);
+
+/*
+ * Instrumentation (host-side, process-wide, not thread-safe).
+ *
+ * hdbmst_launch_count: kernels this library has launched since load.
+ * hdbmst_profile_enable(1): record a CUDA event pair around every kernel
+ *   launch, on the launching stream, grouped by kernel; 0 stops recording.
+ * hdbmst_profile_read: synchronises the recorded events, writes per-kernel
+ *   total milliseconds and launch counts for up to max_kernels kernels
+ *   (either pointer may be NULL), clears the record and returns the number of
+ *   kernels.  hdbmst_profile_kernel_name(i) names entry i.
+ */
+uint64_t hdbmst_launch_count(void);
+void hdbmst_profile_enable(int on);
+int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels);
+const char *hdbmst_profile_kernel_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HDBMST_H_ */

@@ -133,6 +133,13 @@ class Oracle:
             raise ValueError(f"oracle_pair_dist rejected its arguments ({rc})")
         return out
 
+    def pair_dist_xy(self, Xq, Y, a, b) -> np.ndarray:
+        """float64 distance of each pair (column a[e] of Xq, column b[e] of Y)."""
+        Xq, Y = _fm(Xq), _fm(Y)
+        Z = np.ascontiguousarray(np.concatenate([Xq, Y], axis=1))
+        off = Xq.shape[1]
+        return self.pair_dist(Z, np.asarray(a, dtype=np.int64), np.asarray(b, dtype=np.int64) + off)
+
     def mr_weights(self, X, core, a, b) -> np.ndarray:
         """float64 mutual-reachability weight max(core_a, core_b, |a - b|) of each pair;
         ``core`` is indexed by point."""
@@ -172,6 +179,10 @@ def prim_mst(X, core):
 
 def pair_dist(X, a, b):
     return default().pair_dist(X, a, b)
+
+
+def pair_dist_xy(Xq, Y, a, b):
+    return default().pair_dist_xy(Xq, Y, a, b)
 
 
 def mr_weights(X, core, a, b):
