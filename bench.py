@@ -1,0 +1,404 @@
+"""Throughput of the hot path on one GB300 (or N independent replicas).
+
+A step is one pass of the whole path over the 200 000-clip workload: core
+distances (exact k-NN of every clip against all clips, min_samples = 10) and
+the mutual-reachability minimum spanning tree (Boruvka with the exact
+shortcuts).  ``value`` is clips per second with the clips already resident in
+device memory; ``e2e`` is the same metric through the public Python API with
+host buffers (host->device copy of the clips and device->host copy of the
+core distances and the tree inside the timed region).  A secondary line item
+times exact k-NN on the 200 000 x 192 workload against its 20 000-point
+subset (rows per second).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the float64 CPU oracle instead (a bounded sample of
+the same workload on the host cores).  Under torchrun (N > 1) every rank runs
+the full workload on its own GPU (replicas: the path needs no exchange);
+rank 0 prints the line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MR-MST clips/s & exact k-NN rows/s; distance-tile FLOP/s vs GB300 peak"
+WORKLOAD = "hdbscan_200k_d61"
+KNN_WORKLOAD = "knn_200k_d192"
+WORKLOAD_TEXT = ("200,000 clips x 61 fp32 features, 50 Gaussian clusters (sigma ~ U(0.5,2)), "
+                 "10% uniform outliers, 1% exact duplicates, min_samples=10; core distances + "
+                 "mutual-reachability MST by Boruvka with exact shortcuts")
+KNN_TEXT = "200,000 points x 192 fp32 features, 100 clusters, k=10 against every 10th point (20,000)"
+L2_FLUSH_BYTES = 256 << 20
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# FP32 FFMA: 128 lanes per SM, 2 flops per lane per clock
+FP32_LANES_PER_SM = 128
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={SMI_FIELDS}", "--format=csv",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = [ln.strip() for ln in open(self.path) if ln.strip()]
+        os.unlink(self.path)
+        if len(rows) < 2:
+            return None
+        sms, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows[1:]:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sms.append(float(f[1].split()[0]))
+                mx = float(f[2].split()[0])
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names[1:], f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(ws, "nccl")
+    import hdbscan_mst_gb300 as H
+
+    X, task = workloads.workload(args.workload)
+    ms = task["min_samples"]
+    d, n = X.shape
+    Xd = torch.from_numpy(X).to(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        core, idx, dist_ = H.core_distances(Xd, ms)
+        edges, w = H.mr_mst(Xd, core, idx, dist_)
+        return core, edges, w
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: data resident, L2 flushed between steps (outside the events)
+    H.profile_enable(True)
+    H.profile_read()
+    launches0 = H.launch_count()
+    times = []
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        torch.cuda.synchronize(device)
+    barrier(dist, device)
+    launches = H.launch_count() - launches0
+    rounds = H.last_mst_rounds()
+    prof = H.profile_read()
+    H.profile_enable(False)
+    clocks = clk.summary()
+    total_ms = max_over_ranks(dist, sum(times), device)
+    ms_per_step = total_ms / args.steps
+    value = ws * n * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    Xh = torch.from_numpy(X).pin_memory()
+    e2e_times = []
+    for i in range(0 if args.skip_e2e else args.warmup + args.steps):
+        flush_l2(flush)
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        core, edges, w = H.hdbscan_mst(Xh, ms)  # host in, host out
+        t1 = time.perf_counter()
+        if i >= args.warmup:
+            e2e_times.append((t1 - t0) * 1e3)
+    e2e_total = max_over_ranks(dist, sum(e2e_times), device)
+    h2d = X.nbytes
+    d2h = n * 4 + (n - 1) * 12  # core distances, (lo, hi) pairs, weights
+
+    # ---- secondary: exact k-NN rows/s on the 200k x 192 workload
+    Xk, tk = workloads.workload(KNN_WORKLOAD if not args.skip_knn else "knn_1416_d102")
+    Yk = workloads.subset_columns(Xk, tk["y_stride"])
+    Xkd, Ykd = torch.from_numpy(Xk).to(device), torch.from_numpy(Yk).to(device)
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        H.knn(Xkd, Ykd, tk["k"])
+    torch.cuda.synchronize(device)
+    H.profile_enable(True)
+    H.profile_read()
+    kt = []
+    for _ in range(args.steps):
+        flush_l2(flush)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        H.knn(Xkd, Ykd, tk["k"])
+        e1.record(stream)
+        e1.synchronize()
+        kt.append(e0.elapsed_time(e1))
+    kprof = H.profile_read()
+    H.profile_enable(False)
+    k_total = max_over_ranks(dist, sum(kt), device)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    max_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12  # TFLOP/s
+
+    def roofline(prof_, name, flops_per_launch):
+        if name not in prof_:
+            return None
+        tot_ms, nl = prof_[name]
+        avg_s = tot_ms / nl / 1e3
+        ach = flops_per_launch / avg_s / 1e12
+        return {"kernel": name, "bound": "alu", "achieved": round(ach, 2),
+                "peak": round(fp32_peak, 2), "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
+                "traffic": None, "avg_launch_ms": round(avg_s * 1e3, 3),
+                "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz",
+                "flops_per_launch": flops_per_launch}
+
+    # core distances: every clip against every clip, 2 d flops per pair (one launch)
+    main_roof = roofline(prof, "knn_tile", 2.0 * d * n * n)
+    knn_roof = roofline(kprof, "knn_tile", 2.0 * Xk.shape[0] * Xk.shape[1] * Yk.shape[1])
+    breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
+                 for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "clips/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT if args.workload == WORKLOAD else args.workload,
+                   "n": n, "d": d, "min_samples": ms,
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": main_roof,
+        "kernel_ms_per_step": breakdown,
+        "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e}
+                           for a, e in rounds],
+        "gpu_launches": launches,
+        "e2e": None if args.skip_e2e else {
+            "value": round(ws * n * args.steps / (e2e_total / 1e3), 1), "unit": "clips/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "clocks": clocks,
+        "knn": None if args.skip_knn else {"metric": "exact k-NN rows/s", "workload": KNN_TEXT,
+                "value": round(ws * Xk.shape[1] * args.steps / (k_total / 1e3), 1),
+                "unit": "rows/s", "ms_per_step": round(k_total / args.steps, 3),
+                "roofline": knn_roof},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p))
+        except ValueError:
+            pass
+    return {}
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def oracle_sample_rate(n_sample: int):
+    """Time the oracle (core distances + dense Prim) on the first ``n_sample``
+    clips of the workload; return (seconds, clips/s at the full size by the
+    oracle's O(n^2) cost, threads)."""
+    import oracle
+    X, task = workloads.workload(WORKLOAD)
+    n = X.shape[1]
+    Xs = np.ascontiguousarray(X[:, :n_sample])
+    t0 = time.perf_counter()
+    core = oracle.core_distances(Xs, task["min_samples"])
+    oracle.prim_mst(Xs, core)
+    dt = time.perf_counter() - t0
+    full_seconds = dt * (n / n_sample) ** 2
+    return dt, n / full_seconds, oracle.threads()
+
+
+def cpu_baseline(args, n_sample: int = 40000):
+    dt, rate, thr = oracle_sample_rate(n_sample)
+    return {"value": round(rate, 2), "unit": "clips/s", "cores": thr, "kind": "oracle",
+            "sample": (f"oracle core distances + dense Prim on the first {n_sample} of the "
+                       f"200,000 clips ({dt:.1f} s), scaled to 200,000 by the oracle's "
+                       f"O(n^2) cost"),
+            "measured_sample_clips_per_s": round(n_sample / dt, 1)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    # each step a bounded sample sized so the whole run stays within a few minutes
+    per_step_s = 150.0 / max(1, args.steps + args.warmup)
+    n_sample = int(max(4000, min(40000, 40000 * math.sqrt(per_step_s / 10.0))))
+    for _ in range(args.warmup):
+        oracle_sample_rate(n_sample)
+    secs, rates, thr = [], [], 0
+    for _ in range(args.steps):
+        dt, rate, thr = oracle_sample_rate(n_sample)
+        secs.append(dt)
+        rates.append(rate)
+    value = args.steps * 200000 / (sum(secs) * (200000 / n_sample) ** 2)
+    sample = (f"oracle core distances + dense Prim on the first {n_sample} of the 200,000 clips "
+              f"per step, scaled to 200,000 by the oracle's O(n^2) cost")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "clips/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(secs) / args.steps * (200000 / n_sample) ** 2, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT, "n": 200000, "d": 61, "min_samples": 10,
+                   "sample_clips": n_sample},
+        "cpu_baseline": {"value": round(value, 2), "unit": "clips/s", "cores": thr,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "clips/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the oracle on the host (the line omits cpu_baseline)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(
+        k for k, v in workloads.WORKLOADS.items() if v["task"] == "mst"),
+        help="HDBSCAN workload of the main step (profiling runs use smaller ones)")
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer leg")
+    ap.add_argument("--skip-knn", action="store_true", help="omit the k-NN line item")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least three untimed steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -25,7 +25,7 @@ from . import build as _build
 
 __all__ = [
     "knn", "core_distances", "mr_mst", "hdbscan_mst", "HdbmstError", "HdbmstUnavailable",
-    "launch_count", "profile_enable", "profile_read", "library_path", "KMAX",
+    "launch_count", "profile_enable", "profile_read", "last_mst_rounds", "library_path", "KMAX",
 ]
 
 KMAX = 32
@@ -84,6 +84,9 @@ def _load():
     L.hdbmst_profile_read.restype = i32
     L.hdbmst_profile_kernel_name.argtypes = [i32]
     L.hdbmst_profile_kernel_name.restype = ctypes.c_char_p
+    L.hdbmst_last_mst_rounds.argtypes = [ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.POINTER(ctypes.c_int64), i32]
+    L.hdbmst_last_mst_rounds.restype = i32
     _lib = L
     return L
 
@@ -263,6 +266,15 @@ def launch_count() -> int:
 def profile_enable(on: bool = True) -> None:
     """Record CUDA events around every kernel launch (on the launching stream)."""
     _load().hdbmst_profile_enable(1 if on else 0)
+
+
+def last_mst_rounds() -> list[tuple[int, int]]:
+    """``[(points scanned, edges so far), ...]`` per Boruvka round of the last mr_mst call."""
+    L = _load()
+    a = (ctypes.c_int64 * 64)()
+    e = (ctypes.c_int64 * 64)()
+    r = L.hdbmst_last_mst_rounds(a, e, 64)
+    return [(int(a[i]), int(e[i])) for i in range(min(r, 64))]
 
 
 def profile_read() -> dict:

@@ -25,6 +25,8 @@ struct ProfRec {
 };
 std::vector<ProfRec> g_recs;
 std::vector<cudaEvent_t> g_pool;
+// per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
+std::vector<int64_t> g_round_active, g_round_edges;
 
 const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
@@ -463,6 +465,8 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     while ((int64_t(1) << (max_rounds - 2)) < N) ++max_rounds;  // ceil(log2 n) + 2
     int edges = 0;
     DevStatus h{};
+    g_round_active.clear();
+    g_round_edges.clear();
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
         ScanArgs sa{};
         int na = N;
@@ -525,6 +529,8 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         if (h.status & (kStatusNoConverge | kStatusOverflow)) return HDBMST_ERR_NOCONVERGE;
         if (h.edge_count <= edges) return HDBMST_ERR_NOCONVERGE;
         edges = h.edge_count;
+        g_round_active.push_back(na);
+        g_round_edges.push_back(edges);
     }
     if (edges != N - 1) return HDBMST_ERR_NOCONVERGE;
     cudaError_t e = sort_edges(N - 1, p.index_bits, b.e_w, b.e_lo, b.e_hi, b.w2, b.lo2, b.hi2,
@@ -557,6 +563,15 @@ int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels) {
         if (launches) launches[i] = cnt[i];
     }
     return K_COUNT;
+}
+
+int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int max_rounds) {
+    const int r = static_cast<int>(g_round_active.size());
+    for (int i = 0; i < std::min(r, max_rounds); ++i) {
+        if (active) active[i] = g_round_active[i];
+        if (edges) edges[i] = g_round_edges[i];
+    }
+    return r;
 }
 
 const char *hdbmst_profile_kernel_name(int i) {

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(int N, const unsigne
 }
 
 // Exclusive scan of `total` counters in place, one block, chunks of 1024.
-__global__ void __launch_bounds__(1024) scan_kernel(unsigned *__restrict__ v, int total) {
+__global__ void __launch_bounds__(1024) prefix_kernel(unsigned *__restrict__ v, int total) {
     __shared__ unsigned warp_sum[32];
     __shared__ unsigned carry;
     if (threadIdx.x == 0) carry = 0;
@@ -163,7 +163,7 @@ cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, uns
         hist_kernel<<<tiles, kSortThreads, 0, s>>>(N, key, passes[p].shift, hist, tiles);
         after(K_SORT, s);
         before(K_SORT, s);
-        scan_kernel<<<1, 1024, 0, s>>>(hist, 256 * tiles);
+        prefix_kernel<<<1, 1024, 0, s>>>(hist, 256 * tiles);
         after(K_SORT, s);
         before(K_SORT, s);
         scatter_kernel<<<tiles, kSortThreads, 0, s>>>(N, passes[p].shift, passes[p].which, sw, slo,

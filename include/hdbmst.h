@@ -170,6 +170,14 @@ void hdbmst_profile_enable(int on);
 int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels);
 const char *hdbmst_profile_kernel_name(int i);
 
+/*
+ * Rounds of the most recent hdbmst_mr_mst call in this process: returns the
+ * number of Boruvka rounds; for each of the first max_rounds rounds writes
+ * the number of points scanned against all others (active[i]) and the tree
+ * edges found so far (edges[i]).  Either pointer may be NULL.
+ */
+int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int max_rounds);
+
 #ifdef __cplusplus
 }
 #endif
