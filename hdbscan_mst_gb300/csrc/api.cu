@@ -5,6 +5,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/hdbmst.h"
@@ -339,6 +340,50 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
 
 bool bad_sizes(int64_t n, int d) { return n < 0 || d < 1; }
 
+// ------------------------------------------------------------------ fixed scratch
+
+// Scratch of hdbmst_knn_noalloc: one array per GPU, part of the device image,
+// so the entry point never allocates.  Host code may not take its address
+// directly (that would be a host-side stand-in); the device address is looked
+// up once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HDBMST_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (nullptr on error).
+void *noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+// k-NN plan whose partial lists take what the fixed scratch leaves after the
+// packed copies; chunk_rows = 0 when even one 128-row chunk does not fit.
+KnnPlan make_knn_plan_fixed(int64_t n, int64_t m, int d, int k, bool alias, size_t capacity) {
+    KnnPlan p = make_knn_plan(n, m, d, k, alias);
+    p.chunk_rows = kBM;
+    Carver c(nullptr);
+    KnnBufs b{};
+    carve_knn(c, p, b, false);
+    if (c.off > capacity) {
+        p.chunk_rows = 0;
+        return p;
+    }
+    const size_t per_chunk_row = static_cast<size_t>(kMaxSplits) * p.KP * 8;
+    const size_t spare = capacity - c.off;
+    const int64_t extra = static_cast<int64_t>(spare / per_chunk_row) / kBM * kBM;
+    p.chunk_rows = static_cast<int>(std::min<int64_t>(kBM + extra, p.n_pad));
+    return p;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
@@ -356,6 +401,7 @@ const char *hdbmst_status_string(hdbmst_status status) {
         case HDBMST_ERR_NONFINITE: return "non-finite value in the points or core distances";
         case HDBMST_ERR_NOCONVERGE: return "Boruvka made no progress";
         case HDBMST_ERR_CUDA: return "CUDA error";
+        case HDBMST_ERR_TOO_LARGE: return "problem too large for the fixed scratch of hdbmst_knn_noalloc";
     }
     return "unknown status";
 }
@@ -536,6 +582,30 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     cudaError_t e = sort_edges(N - 1, p.index_bits, b.e_w, b.e_lo, b.e_hi, b.w2, b.lo2, b.hi2,
                                b.hist, out_edges, out_w, s, before, after);
     return e == cudaSuccess ? HDBMST_OK : HDBMST_ERR_CUDA;
+}
+
+hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const float *Y,
+                                 int64_t ldy, int64_t m, int d, int k, int32_t *out_idx,
+                                 float *out_dist, hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bad_sizes(n, d) || m < 1 || k < 1 || k > m || ldx < n || ldy < m) return HDBMST_ERR_ARG;
+    if (k > HDBMST_KMAX || d > HDBMST_DMAX || n > HDBMST_NMAX || m > HDBMST_NMAX)
+        return HDBMST_ERR_UNSUPPORTED;
+    if (n == 0) return HDBMST_OK;
+    if (!X || !Y || !out_idx || !out_dist) return HDBMST_ERR_ARG;
+    const bool alias = (X == Y && ldx == ldy && n == m);
+    KnnPlan p = make_knn_plan_fixed(n, m, d, k, alias, HDBMST_NOALLOC_SCRATCH_BYTES);
+    if (p.chunk_rows == 0) return HDBMST_ERR_TOO_LARGE;
+    Carver need(nullptr);
+    KnnBufs nb{};
+    carve_knn(need, p, nb, false);
+    if (need.off > HDBMST_NOALLOC_SCRATCH_BYTES) return HDBMST_ERR_TOO_LARGE;
+    void *scratch = noalloc_scratch();
+    if (!scratch) return HDBMST_ERR_CUDA;
+    Carver c(scratch);
+    KnnBufs b{};
+    carve_knn(c, p, b, false);
+    return run_knn(p, b, X, ldx, Y, ldy, out_idx, out_dist, nullptr, 0, s);
 }
 
 uint64_t hdbmst_launch_count(void) { return g_launches.load(); }

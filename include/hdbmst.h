@@ -47,7 +47,9 @@ typedef enum {
     HDBMST_ERR_NOCONVERGE = 5,  /* Boruvka made no progress in a round (cannot happen   */
                                 /* with a consistent weight function; reported, never  */
                                 /* looped on)                                          */
-    HDBMST_ERR_CUDA = 6         /* a CUDA runtime call or kernel launch failed         */
+    HDBMST_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed         */
+    HDBMST_ERR_TOO_LARGE = 7    /* the problem does not fit hdbmst_knn_noalloc's fixed */
+                                /* scratch (HDBMST_NOALLOC_SCRATCH_BYTES)              */
 } hdbmst_status;
 
 /* Largest k for hdbmst_knn, and largest min_samples + 1 for hdbmst_core_distances. */
@@ -147,6 +149,44 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                             const int32_t *knn_idx, const float *knn_dist, int knn_len,
                             int32_t *out_edges, float *out_w, void *workspace,
                             size_t workspace_bytes, hdbmst_stream stream);
+
+/*
+ * k-NN for callers that may not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for users of
+ * the library, not for the method.  Some callers cannot call cudaMalloc or
+ * hand the library a workspace: a host application that reserved all device
+ * memory up front and gives its plugins no allocator, a latency-critical loop
+ * where an allocation could synchronise the device, a process under a hard
+ * memory quota.  hdbmst_knn_noalloc computes exactly what hdbmst_knn computes
+ * (same kernels, same results bit for bit) but takes its scratch from one
+ * fixed array of HDBMST_NOALLOC_SCRATCH_BYTES in the library's device image
+ * instead of a caller workspace.  The caller still owns X, Y, out_idx and
+ * out_dist, with the meaning, layout and limits of hdbmst_knn.
+ *
+ *  - The array is allocated once per GPU when the library's device code is
+ *    loaded there and stays allocated until the process exits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device uses the same array, so calls whose work overlaps
+ *    on the GPU (two streams, or two host threads) race and give wrong
+ *    results: serialise them.  The array keeps the last call's contents; the
+ *    call clears what must start at zero itself.
+ *  - Problems that need more scratch than the array holds return
+ *    HDBMST_ERR_TOO_LARGE before any GPU work.  The need is about
+ *    8 * round_up(d, 16) * (round_up(n, 128) + round_up(m, 128)) bytes for the
+ *    packed copies (half that when Y is X), plus 4 bytes per query and at
+ *    least 64 KiB for the neighbour candidates (128 KiB when k > 12).
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine; it
+ *    synchronises the stream once at the end, as hdbmst_knn does.
+ *
+ * Errors: those of hdbmst_knn (except ERR_WORKSPACE), and ERR_TOO_LARGE.
+ */
+#define HDBMST_NOALLOC_SCRATCH_BYTES (64u << 20)
+hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const float *Y,
+                                 int64_t ldy, int64_t m, int d, int k, int32_t *out_idx,
+                                 float *out_dist, hdbmst_stream stream);
 
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);
