@@ -289,8 +289,8 @@ def run_gpu(args):
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": main_roof,
         "kernel_ms_per_step": breakdown,
-        "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e}
-                           for a, e in rounds],
+        "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e,
+                            "exact_rows": x} for a, e, x in rounds],
         "gpu_launches": launches,
         "e2e": None if args.skip_e2e else {
             "value": round(ws * n * args.steps / (e2e_total / 1e3), 1), "unit": "clips/s",

@@ -85,6 +85,7 @@ def _load():
     L.hdbmst_profile_kernel_name.argtypes = [i32]
     L.hdbmst_profile_kernel_name.restype = ctypes.c_char_p
     L.hdbmst_last_mst_rounds.argtypes = [ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.POINTER(ctypes.c_int64),
                                          ctypes.POINTER(ctypes.c_int64), i32]
     L.hdbmst_last_mst_rounds.restype = i32
     _lib = L
@@ -268,13 +269,15 @@ def profile_enable(on: bool = True) -> None:
     _load().hdbmst_profile_enable(1 if on else 0)
 
 
-def last_mst_rounds() -> list[tuple[int, int]]:
-    """``[(points scanned, edges so far), ...]`` per Boruvka round of the last mr_mst call."""
+def last_mst_rounds() -> list[tuple[int, int, int]]:
+    """``[(points scanned, edges so far, points searched again exactly), ...]``
+    per Boruvka round of the last mr_mst call."""
     L = _load()
     a = (ctypes.c_int64 * 64)()
     e = (ctypes.c_int64 * 64)()
-    r = L.hdbmst_last_mst_rounds(a, e, 64)
-    return [(int(a[i]), int(e[i])) for i in range(min(r, 64))]
+    x = (ctypes.c_int64 * 64)()
+    r = L.hdbmst_last_mst_rounds(a, e, x, 64)
+    return [(int(a[i]), int(e[i]), int(x[i])) for i in range(min(r, 64))]
 
 
 def profile_read() -> dict:

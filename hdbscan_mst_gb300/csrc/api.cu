@@ -27,11 +27,12 @@ struct ProfRec {
 std::vector<ProfRec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
-std::vector<int64_t> g_round_active, g_round_edges;
+std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
 
 const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
-    "nbr_candidate", "active", "gather", "boruvka_scan", "comp_min", "hook",
+    "nbr_candidate", "active", "gather", "boruvka_scan", "boruvka_refine", "boruvka_exact",
+    "comp_min", "hook",
     "roots",  "relabel",    "sort_edges"};
 
 cudaEvent_t take_event() {
@@ -302,9 +303,14 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
 }
 
 struct MstBufs {
-    float *Xf, *norm, *Xa, *act_core;
-    int *act_comp, *act_idx, *comp, *parent, *root_of;
-    unsigned long long *cand, *ck64;
+    float *Xf, *Xp, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
+    int *act_comp, *act_idx, *comp, *parent, *root_of, *perm, *col_comp, *start, *act_start;
+    int *counters;  // [4n + 8]: size, act_size, cursor, act_cursor, totals (zeroed per round)
+    unsigned char *act_flag;
+    unsigned long long *part_key;
+    float *part_tau;
+    int *fb_rows;
+    unsigned long long *cand, *ck64, *cache;
     unsigned *chi, *ub;
     unsigned char *proven;
     int *e_lo, *e_hi, *lo2, *hi2;
@@ -315,15 +321,30 @@ struct MstBufs {
 void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     const size_t n = static_cast<size_t>(std::max(p.n, 1));
     b.Xf = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xp = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.norm = c.take<float>(p.n_pad);
     b.Xa = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.act_core = c.take<float>(p.n_pad);
     b.act_comp = c.take<int>(p.n_pad);
+    b.act_norm = c.take<float>(p.n_pad);
+    b.Xs = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.col_core = c.take<float>(n);
+    b.col_norm = c.take<float>(p.n_pad);
+    b.perm = c.take<int>(n);
+    b.col_comp = c.take<int>(n);
+    b.start = c.take<int>(n);
+    b.act_start = c.take<int>(n);
+    b.counters = c.take<int>(4 * n + 8);
+    b.act_flag = c.take<unsigned char>(n);
+    b.part_key = c.take<unsigned long long>(scan_part_entries(kMaxSplits, p.n_pad));
+    b.part_tau = c.take<float>(static_cast<size_t>(kMaxSplits) * p.n_pad);
+    b.fb_rows = c.take<int>(n);
     b.act_idx = c.take<int>(n);
     b.comp = c.take<int>(n);
     b.parent = c.take<int>(n);
     b.root_of = c.take<int>(n);
     b.cand = c.take<unsigned long long>(n);
+    b.cache = c.take<unsigned long long>(n);
     b.ck64 = c.take<unsigned long long>(n);
     b.chi = c.take<unsigned>(n);
     b.ub = c.take<unsigned>(n);
@@ -502,10 +523,10 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     const int col_tiles = static_cast<int>(p.n_pad / kBN);
 
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
-    LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, nullptr,
-                                  b.norm, &b.st->status, nullptr, s));
+    LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, b.Xp,
+                                  b.norm, &b.st->status, &b.st->nbmax_bits, s));
     LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
-    LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, s));
+    LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, b.cache, s));
 
     int max_rounds = 2;
     while ((int64_t(1) << (max_rounds - 2)) < N) ++max_rounds;  // ceil(log2 n) + 2
@@ -513,45 +534,58 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     DevStatus h{};
     g_round_active.clear();
     g_round_edges.clear();
+    g_round_exact.clear();
+    int *size = b.counters, *act_size = b.counters + N, *cursor = b.counters + 2 * N,
+        *act_cursor = b.counters + 3 * N, *totals = b.counters + 4 * N;
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
-        ScanArgs sa{};
-        int na = N;
+        int fallback = 0;
         if (shortcuts) {
             LAUNCH(K_NBR_CANDIDATE, s, launch_nbr_candidate(N, L, knn_idx, knn_dist, core, b.comp,
-                                                            b.cand, b.proven, b.ub,
+                                                            b.cache, b.cand, b.proven, b.ub,
                                                             &b.st->status, s));
-            CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
-            LAUNCH(K_ACTIVE, s, launch_active(N, b.proven, core, b.comp, b.ub, b.act_idx,
-                                              &b.st->act_count, s));
-            hdbmst_status rs = read_status(b.st, h, s);
-            if (rs != HDBMST_OK) return rs;
-            if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
-            if (h.status & kStatusBadList) return HDBMST_ERR_ARG;
-            na = h.act_count;
-            if (na > 0) {
-                const int na_pad = static_cast<int>(round_up(na, kBM));
-                LAUNCH(K_GATHER, s, launch_gather(na, na_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
-                                                  b.comp, b.Xa, b.act_core, b.act_comp, s));
-                sa.Xa = b.Xa;
-                sa.lda = na_pad;
-                sa.act_idx = b.act_idx;
-                sa.act_core = b.act_core;
-                sa.act_comp = b.act_comp;
-            }
-        } else {
-            sa.Xa = b.Xf;
-            sa.lda = p.n_pad;
-            sa.act_idx = nullptr;
-            sa.act_core = core;
-            sa.act_comp = b.comp;
         }
+        CUDA_OK(cudaMemsetAsync(b.counters, 0, sizeof(int) * (4 * static_cast<size_t>(N) + 8), s));
+        CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
+        LAUNCH(K_ACTIVE, s, launch_classify(N, shortcuts ? b.proven : nullptr, core, b.comp,
+                                            shortcuts ? b.ub : nullptr, b.act_flag, size, act_size,
+                                            &b.st->act_count, s));
+        hdbmst_status rs = read_status(b.st, h, s);
+        if (rs != HDBMST_OK) return rs;
+        if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+        if (h.status & kStatusBadList) return HDBMST_ERR_ARG;
+        const int na = h.act_count;
         if (na > 0) {
+            const int na_pad = static_cast<int>(round_up(na, kBM));
+            LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), p.dk, b.comp, core,
+                                             b.norm, b.act_flag, size, act_size, b.start,
+                                             b.act_start, cursor, act_cursor, totals, b.perm,
+                                             b.col_comp, b.col_core, b.col_norm, b.act_idx, b.Xf,
+                                             b.Xs, s));
+            LAUNCH(K_GATHER, s, launch_gather(na, na_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
+                                              b.comp, b.norm, b.Xa, b.act_core, b.act_comp,
+                                              b.act_norm, s));
+            ScanArgs sa{};
+            sa.Xa = b.Xa;
+            sa.lda = na_pad;
+            sa.act_idx = b.act_idx;
+            sa.act_core = b.act_core;
+            sa.act_comp = b.act_comp;
+            sa.act_norm = b.act_norm;
             sa.na = na;
-            sa.Xf = b.Xf;
+            sa.Xs = b.Xs;
             sa.ldx = p.n_pad;
+            sa.col_orig = b.perm;
+            sa.col_norm = b.col_norm;
+            sa.col_core = b.col_core;
+            sa.col_comp = b.col_comp;
+            sa.comp_start = b.start;
+            sa.comp_size = size;
+            sa.Xp = b.Xp;
             sa.core = core;
             sa.comp = b.comp;
+            sa.nbmax_bits = &b.st->nbmax_bits;
             sa.n = N;
+            sa.d = d;
             sa.dk = p.dk;
             sa.col_tiles = col_tiles;
             const int row_tiles = (na + kBM - 1) / kBM;
@@ -559,17 +593,50 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             const int tps = (col_tiles + S0 - 1) / S0;
             const int S = (col_tiles + tps - 1) / tps;
             sa.tiles_per_split = tps;
+            sa.splits = S;
+            sa.part_key = b.part_key;
+            sa.part_tau = b.part_tau;
             sa.cand = b.cand;
+            sa.fb_count = &b.st->fb_count;
+            sa.fb_rows = b.fb_rows;
+            CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
             LAUNCH(K_SCAN, s, launch_scan(sa, row_tiles, S, s));
+            LAUNCH(K_SCAN_REFINE, s, launch_scan_refine(sa, s));
+            rs = read_status(b.st, h, s);
+            if (rs != HDBMST_OK) return rs;
+            const int nf = h.fb_count;
+            fallback = nf;
+            if (nf > 0) {
+                // rows the rounding proof left open: gather them as rows and
+                // search them again with the exact weight
+                const int nf_pad = static_cast<int>(round_up(nf, kBM));
+                LAUNCH(K_GATHER, s, launch_gather(nf, nf_pad, p.dk, b.fb_rows, b.Xf, p.n_pad,
+                                                  core, b.comp, b.norm, b.Xa, b.act_core,
+                                                  b.act_comp, b.act_norm, s));
+                ScanArgs xa = sa;
+                xa.lda = nf_pad;
+                xa.act_idx = b.fb_rows;
+                xa.na = nf;
+                const int xt = (nf + kBM - 1) / kBM;
+                // no partial lists here (atomicMin per row), so split the
+                // columns finely enough to give every CTA slot work
+                const int X0 = std::max(1, std::min(col_tiles, (slots + xt - 1) / xt));
+                const int xtps = (col_tiles + X0 - 1) / X0;
+                xa.tiles_per_split = xtps;
+                xa.splits = (col_tiles + xtps - 1) / xtps;
+                LAUNCH(K_SCAN_EXACT, s, launch_scan_exact(xa, xt, xa.splits, s));
+            }
         }
-        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, s, 0));
-        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, s, 1));
+        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, b.proven,
+                                              b.act_flag, shortcuts ? b.cache : nullptr, s, 0));
+        LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, nullptr, nullptr,
+                                              nullptr, s, 1));
         LAUNCH(K_HOOK, s, launch_hook(N, b.comp, b.ck64, b.chi, b.parent, b.e_lo, b.e_hi,
                                       reinterpret_cast<float *>(b.e_w), &b.st->edge_count,
                                       &b.st->status, s));
         LAUNCH(K_ROOTS, s, launch_roots(N, b.comp, b.parent, b.root_of, &b.st->status, s));
         LAUNCH(K_RELABEL, s, launch_relabel(N, b.comp, b.root_of, b.cand, b.ck64, b.chi, b.ub, s));
-        hdbmst_status rs = read_status(b.st, h, s);
+        rs = read_status(b.st, h, s);
         if (rs != HDBMST_OK) return rs;
         if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
         if (h.status & (kStatusNoConverge | kStatusOverflow)) return HDBMST_ERR_NOCONVERGE;
@@ -577,6 +644,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         edges = h.edge_count;
         g_round_active.push_back(na);
         g_round_edges.push_back(edges);
+        g_round_exact.push_back(fallback);
     }
     if (edges != N - 1) return HDBMST_ERR_NOCONVERGE;
     cudaError_t e = sort_edges(N - 1, p.index_bits, b.e_w, b.e_lo, b.e_hi, b.w2, b.lo2, b.hi2,
@@ -635,11 +703,13 @@ int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels) {
     return K_COUNT;
 }
 
-int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int max_rounds) {
+int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
+                           int max_rounds) {
     const int r = static_cast<int>(g_round_active.size());
     for (int i = 0; i < std::min(r, max_rounds); ++i) {
         if (active) active[i] = g_round_active[i];
         if (edges) edges[i] = g_round_edges[i];
+        if (exact_rows) exact_rows[i] = g_round_exact[i];
     }
     return r;
 }

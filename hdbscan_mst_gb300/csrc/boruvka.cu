@@ -1,4 +1,5 @@
-// K3-K8: Boruvka rounds of the mutual-reachability minimum spanning tree.
+// K3-K5, K7, K8: Boruvka rounds of the mutual-reachability minimum spanning
+// tree (the scan, K6, is in scan.cu).
 //
 // Page "HDBSCAN" (neuro-kitchen dsp-kitchen gpu/hdbscan):
 //  * "The algorithm on the device": w(a, b) = max(core_a, core_b, |a - b|);
@@ -32,11 +33,13 @@ namespace hdbmst {
 namespace {
 
 __global__ void mst_init_kernel(int n, int *comp, unsigned long long *cand,
-                                unsigned long long *ck64, unsigned *chi, unsigned *ub) {
+                                unsigned long long *ck64, unsigned *chi, unsigned *ub,
+                                unsigned long long *cache) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     comp[i] = i;
     cand[i] = kNoKey;
+    cache[i] = kNoKey;
     ck64[i] = kNoKey;
     chi[i] = 0xffffffffu;
     ub[i] = __float_as_uint(INFINITY);
@@ -44,9 +47,15 @@ __global__ void mst_init_kernel(int n, int *comp, unsigned long long *cand,
 
 // K3: per point, its lightest listed edge into another component (a real
 // edge), whether that edge is proven cheapest, and the component bound.
+//
+// A point also keeps the exact cheapest edge it had in the previous round
+// (cache).  Components only grow, so the points outside its component now are
+// a subset of those then; if that edge's other end is still outside, it is
+// still the cheapest and the point needs no scan.
 __global__ void nbr_candidate_kernel(int n, int L, const int32_t *__restrict__ kidx,
                                      const float *__restrict__ kdist,
                                      const float *__restrict__ core, const int *__restrict__ comp,
+                                     const unsigned long long *__restrict__ cache,
                                      unsigned long long *__restrict__ cand,
                                      unsigned char *__restrict__ proven,
                                      unsigned *__restrict__ ub, unsigned *__restrict__ status) {
@@ -54,6 +63,13 @@ __global__ void nbr_candidate_kernel(int n, int L, const int32_t *__restrict__ k
     if (a >= n) return;
     const float ca = core[a];
     const int cc = comp[a];
+    const unsigned long long held = cache[a];
+    if (held != kNoKey && comp[key_i(held)] != cc) {
+        cand[a] = held;
+        proven[a] = 1;
+        atomicMin(&ub[cc], static_cast<unsigned>(held >> 32));
+        return;
+    }
     unsigned long long best = kNoKey;
     const int64_t o = static_cast<int64_t>(a) * L;
     for (int l = 0; l < L; ++l) {
@@ -74,33 +90,121 @@ __global__ void nbr_candidate_kernel(int n, int L, const int32_t *__restrict__ k
     if (best != kNoKey) atomicMin(&ub[cc], static_cast<unsigned>(best >> 32));
 }
 
-// K5: the points that still need a scan, appended with one atomic per warp.
-__global__ void active_kernel(int n, const unsigned char *__restrict__ proven,
-                              const float *__restrict__ core, const int *__restrict__ comp,
-                              const unsigned *__restrict__ ub, int *__restrict__ act_idx,
-                              int *__restrict__ act_count) {
-    const int a = blockIdx.x * blockDim.x + threadIdx.x;
-    bool act = false;
-    if (a < n) {
-        act = true;
-        if (proven && proven[a]) act = false;
-        // skip only when core_a exceeds the bound strictly: an equal weight
-        // could still win on index
-        if (act && ub && core[a] > __uint_as_float(ub[comp[a]])) act = false;
+// K5: which points still need a scan (active), and per component the number
+// of points and of active points.  Counts are aggregated per warp over lanes
+// of the same component.
+__global__ void classify_kernel(int n, const unsigned char *__restrict__ proven,
+                                const float *__restrict__ core, const int *__restrict__ comp,
+                                const unsigned *__restrict__ ub,
+                                unsigned char *__restrict__ act_flag, int *__restrict__ size,
+                                int *__restrict__ act_size, int *__restrict__ act_count) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const bool valid = i < n;
+    const int c = valid ? comp[i] : -1;
+    bool act = valid;
+    if (act && proven && proven[i]) act = false;
+    // skip only when core_a exceeds the bound strictly: an equal weight could
+    // still win on index
+    if (act && ub && core[i] > __uint_as_float(ub[c])) act = false;
+    if (valid) act_flag[i] = act ? 1 : 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    if (valid && lane == __ffs(peers) - 1) atomicAdd(&size[c], __popc(peers));
+    const unsigned actb = __ballot_sync(0xffffffffu, act);
+    const unsigned apeers = peers & actb;
+    if (act && lane == __ffs(apeers) - 1) atomicAdd(&act_size[c], __popc(apeers));
+    if (lane == 0 && actb) atomicAdd(act_count, __popc(actb));
+}
+
+// Give every component a contiguous slot range for its points and for its
+// active points (slot order between components is arbitrary).
+__global__ void slots_kernel(int n, const int *__restrict__ size, const int *__restrict__ act_size,
+                             int *__restrict__ start, int *__restrict__ act_start,
+                             int *__restrict__ totals) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int s = c < n ? size[c] : 0;
+    const int a = c < n ? act_size[c] : 0;
+    int is = s, ia = a;  // inclusive warp prefix sums
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ys = __shfl_up_sync(0xffffffffu, is, o);
+        const int ya = __shfl_up_sync(0xffffffffu, ia, o);
+        if (lane >= o) {
+            is += ys;
+            ia += ya;
+        }
     }
-    const unsigned m = __ballot_sync(0xffffffffu, act);
+    int bs = 0, ba = 0;
+    if (lane == 31) {
+        if (is) bs = atomicAdd(&totals[0], is);
+        if (ia) ba = atomicAdd(&totals[1], ia);
+    }
+    bs = __shfl_sync(0xffffffffu, bs, 31);
+    ba = __shfl_sync(0xffffffffu, ba, 31);
+    if (c < n) {
+        start[c] = bs + is - s;
+        act_start[c] = ba + ia - a;
+    }
+}
+
+// Every point to its component's slot range: the column order of the scan
+// (perm, and the column arrays in that order) and the active rows grouped by
+// component.  Order inside a component is arbitrary; results do not depend
+// on it.
+__global__ void group_kernel(int n, const int *__restrict__ comp, const float *__restrict__ core,
+                             const float *__restrict__ norm,
+                             const unsigned char *__restrict__ act_flag,
+                             const int *__restrict__ start, const int *__restrict__ act_start,
+                             int *__restrict__ cursor, int *__restrict__ act_cursor,
+                             int *__restrict__ perm, int *__restrict__ col_comp,
+                             float *__restrict__ col_core, float *__restrict__ col_norm,
+                             int *__restrict__ act_idx) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const bool valid = i < n;
+    const int c = valid ? comp[i] : -1;
+    const bool act = valid && act_flag[i];
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const int leader = __ffs(peers) - 1;
     int base = 0;
-    if ((threadIdx.x & 31) == 0 && m) base = atomicAdd(act_count, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (act) act_idx[base + __popc(m & lanemask_lt())] = a;
+    if (valid && lane == leader) base = atomicAdd(&cursor[c], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    const unsigned apeers = peers & __ballot_sync(0xffffffffu, act);
+    const int aleader = apeers ? __ffs(apeers) - 1 : 0;
+    int abase = 0;
+    if (act && lane == aleader) abase = atomicAdd(&act_cursor[c], __popc(apeers));
+    abase = __shfl_sync(0xffffffffu, abase, aleader);
+    if (valid) {
+        const int pos = start[c] + base + __popc(peers & lanemask_lt());
+        perm[pos] = i;
+        col_comp[pos] = c;
+        col_core[pos] = core[i];
+        col_norm[pos] = norm[i];
+    }
+    if (act) act_idx[act_start[c] + abase + __popc(apeers & lanemask_lt())] = i;
+}
+
+// Columns in grouped order into their own feature-major buffer; padding
+// columns are zero with norm +inf.
+__global__ void gather_cols_kernel(int n, int n_pad, const int *__restrict__ perm,
+                                   const float *__restrict__ Xf, float *__restrict__ Xs,
+                                   float *__restrict__ col_norm) {
+    const int pos = blockIdx.x * blockDim.x + threadIdx.x;
+    const int f = blockIdx.y;
+    if (pos >= n_pad) return;
+    const int g = pos < n ? perm[pos] : -1;
+    Xs[static_cast<int64_t>(f) * n_pad + pos] = g >= 0 ? Xf[static_cast<int64_t>(f) * n_pad + g] : 0.f;
+    if (f == 0 && g < 0) col_norm[pos] = INFINITY;
 }
 
 // Active rows into their own padded feature-major buffer.
 __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict__ act_idx,
                               const float *__restrict__ Xf, int64_t ldx,
                               const float *__restrict__ core, const int *__restrict__ comp,
-                              float *__restrict__ Xa, float *__restrict__ act_core,
-                              int *__restrict__ act_comp) {
+                              const float *__restrict__ norm, float *__restrict__ Xa,
+                              float *__restrict__ act_core, int *__restrict__ act_comp,
+                              float *__restrict__ act_norm) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     const int f = blockIdx.y;
     if (r >= na_pad) return;
@@ -109,150 +213,23 @@ __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict_
     if (f == 0) {
         act_core[r] = g >= 0 ? core[g] : 0.f;
         act_comp[r] = g >= 0 ? comp[g] : -1;
+        act_norm[r] = g >= 0 ? norm[g] : 0.f;
     }
 }
 
-// K6: for every active row, the least (w, other end) over all points of other
-// components.  Register-blocked 128 x 128 tile like the k-NN engine, but each
-// pair accumulates the library's exact squared distance (difference, then
-// fused square-add, ascending features), so the weight is bit-identical to
-// the one the neighbour lists carry.
-struct ScanSmem {
-    float As[2][kBK][kBM];
-    float Bs[2][kBK][kBN];
-    float rcore[kBM];
-    int rcomp[kBM];
-};
-
-__device__ __forceinline__ int srow(int ty, int i) { return (i < 4 ? 0 : 60) + ty * 4 + i; }
-__device__ __forceinline__ int scol(int tx, int j) { return (j < 4 ? 0 : 60) + tx * 4 + j; }
-
-__global__ void __launch_bounds__(kThreads, 2) scan_kernel(const ScanArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ScanSmem &S = *reinterpret_cast<ScanSmem *>(smem_raw);
-    const int tid = threadIdx.x;
-    const int ty = tid >> 4, tx = tid & 15;
-    const int r0 = blockIdx.x * kBM;
-    const int ct_begin = blockIdx.y * a.tiles_per_split;
-    const int ct_end = min(ct_begin + a.tiles_per_split, a.col_tiles);
-
-    if (tid < kBM) {
-        const int r = r0 + tid;
-        S.rcore[tid] = r < a.na ? a.act_core[r] : 0.f;
-        S.rcomp[tid] = r < a.na ? a.act_comp[r] : -1;
-    }
-    __syncthreads();
-
-    unsigned long long best[8];
-    float thr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        best[i] = kNoKey;
-        thr[i] = INFINITY;
-    }
-
-    const int nchunks = a.dk / kBK;
-    const int nsteps = max(ct_end - ct_begin, 0) * nchunks;
-    auto issue = [&](int step, int buf) {
-        const int ct = ct_begin + step / nchunks;
-        const int kc = step - (step / nchunks) * nchunks;
-        const float *ga = a.Xa + static_cast<int64_t>(kc * kBK) * a.lda + r0;
-        const float *gb = a.Xf + static_cast<int64_t>(kc * kBK) * a.ldx + static_cast<int64_t>(ct) * kBN;
-#pragma unroll
-        for (int v = tid; v < kBK * kBM / 4; v += kThreads) {
-            const int kr = v >> 5, c4 = (v & 31) * 4;
-            cp_async16(&S.As[buf][kr][c4], ga + static_cast<int64_t>(kr) * a.lda + c4);
-            cp_async16(&S.Bs[buf][kr][c4], gb + static_cast<int64_t>(kr) * a.ldx + c4);
-        }
-        cp_async_commit();
-    };
-
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-    if (nsteps > 0) issue(0, 0);
-    for (int step = 0; step < nsteps; ++step) {
-        const int buf = step & 1;
-        cp_async_wait_all();
-        __syncthreads();
-        if (step + 1 < nsteps) issue(step + 1, buf ^ 1);
-#pragma unroll
-        for (int kk = 0; kk < kBK; ++kk) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][64 + tx * 4]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = sqdiff_fma(av[i], bv[j], acc[i][j]);
-        }
-        if ((step + 1) % nchunks == 0) {
-            const int col0 = (ct_begin + step / nchunks) * kBN;
-            float cb[8];
-            int cc[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = col0 + scol(tx, j);
-                const bool ok = c < a.n;
-                cb[j] = ok ? __ldg(a.core + c) : 0.f;
-                cc[j] = ok ? __ldg(a.comp + c) : INT_MIN;  // padding: never another component
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = srow(ty, i);
-                const int rc = S.rcomp[r];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float d2 = acc[i][j];
-                    if (cc[j] != rc && cc[j] != INT_MIN && d2 <= thr[i]) {
-                        const float w = fmaxf(fmaxf(S.rcore[r], cb[j]), __fsqrt_rn(d2));
-                        const unsigned long long key =
-                            key64(w, static_cast<unsigned>(col0 + scol(tx, j)));
-                        if (key < best[i]) {
-                            best[i] = key;
-                            // sqrt(d2) <= w requires d2 <= w^2 (1 + 2.1 u); this
-                            // threshold keeps every pair that could tie or win
-                            thr[i] = __fmul_rn(__fmul_rn(w, w), 1.0f + 0x1p-20f);
-                        }
-                    }
-                    acc[i][j] = 0.f;
-                }
-            }
-        }
-    }
-    // least key per row: the 16 lanes of a half-warp share the same rows
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        unsigned long long k = best[i];
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) k = min(k, __shfl_xor_sync(0xffffffffu, k, o));
-        best[i] = k;
-    }
-    if (tx == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + srow(ty, i);
-            if (r < a.na && best[i] != kNoKey) {
-                const int g = a.act_idx ? a.act_idx[r] : r;
-                atomicMin(&a.cand[g], best[i]);
-            }
-        }
-    }
-}
-
-// K7: per component, the least (w, lo, hi) over its points' candidates.
+// K7: per component, the least (w, lo, hi) over its points' candidates.  The
+// first pass also records, for the next round, the candidates that are exact
+// (proven or scanned); the others (skipped by the bound) are not.
 __global__ void comp_min_lo_kernel(int n, const unsigned long long *__restrict__ cand,
                                    const int *__restrict__ comp,
-                                   unsigned long long *__restrict__ ck64) {
+                                   unsigned long long *__restrict__ ck64,
+                                   const unsigned char *__restrict__ proven,
+                                   const unsigned char *__restrict__ act_flag,
+                                   unsigned long long *__restrict__ cache) {
     const int a = blockIdx.x * blockDim.x + threadIdx.x;
     if (a >= n) return;
     const unsigned long long k = cand[a];
+    if (cache) cache[a] = (proven[a] || act_flag[a]) ? k : kNoKey;
     if (k == kNoKey) return;
     const unsigned b = key_i(k);
     const unsigned lo = min(static_cast<unsigned>(a), b);
@@ -345,48 +322,65 @@ inline int blocks_for(int n, int t) { return (n + t - 1) / t; }
 }  // namespace
 
 cudaError_t launch_mst_init(int n, int *comp, unsigned long long *cand, unsigned long long *ck64,
-                            unsigned *chi, unsigned *ub, cudaStream_t s) {
-    mst_init_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, cand, ck64, chi, ub);
+                            unsigned *chi, unsigned *ub, unsigned long long *cache,
+                            cudaStream_t s) {
+    mst_init_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, cand, ck64, chi, ub, cache);
     return cudaGetLastError();
 }
 
 cudaError_t launch_nbr_candidate(int n, int L, const int32_t *kidx, const float *kdist,
-                                 const float *core, const int *comp, unsigned long long *cand,
+                                 const float *core, const int *comp,
+                                 const unsigned long long *cache, unsigned long long *cand,
                                  unsigned char *proven, unsigned *ub, unsigned *status,
                                  cudaStream_t s) {
-    nbr_candidate_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, L, kidx, kdist, core, comp, cand,
-                                                            proven, ub, status);
+    nbr_candidate_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, L, kidx, kdist, core, comp, cache,
+                                                            cand, proven, ub, status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_active(int n, const unsigned char *proven, const float *core, const int *comp,
-                          const unsigned *ub, int *act_idx, int *act_count, cudaStream_t s) {
-    active_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, proven, core, comp, ub, act_idx,
-                                                     act_count);
+cudaError_t launch_classify(int n, const unsigned char *proven, const float *core,
+                            const int *comp, const unsigned *ub, unsigned char *act_flag,
+                            int *size, int *act_size, int *act_count, cudaStream_t s) {
+    classify_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, proven, core, comp, ub, act_flag, size,
+                                                       act_size, act_count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group(int n, int n_pad, int dk, const int *comp, const float *core,
+                         const float *norm, const unsigned char *act_flag, const int *size,
+                         const int *act_size, int *start, int *act_start, int *cursor,
+                         int *act_cursor, int *totals, int *perm, int *col_comp, float *col_core,
+                         float *col_norm, int *act_idx, const float *Xf, float *Xs,
+                         cudaStream_t s) {
+    slots_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, size, act_size, start, act_start, totals);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    group_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, core, norm, act_flag, start, act_start,
+                                                    cursor, act_cursor, perm, col_comp, col_core,
+                                                    col_norm, act_idx);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gather_cols_kernel<<<dim3(blocks_for(n_pad, 256), dk), 256, 0, s>>>(n, n_pad, perm, Xf, Xs,
+                                                                        col_norm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(int na, int na_pad, int dk, const int *act_idx, const float *Xf,
-                          int64_t ldx, const float *core, const int *comp, float *Xa,
-                          float *act_core, int *act_comp, cudaStream_t s) {
+                          int64_t ldx, const float *core, const int *comp, const float *norm,
+                          float *Xa, float *act_core, int *act_comp, float *act_norm,
+                          cudaStream_t s) {
     gather_kernel<<<dim3(blocks_for(na_pad, 256), dk), 256, 0, s>>>(
-        na, na_pad, dk, act_idx, Xf, ldx, core, comp, Xa, act_core, act_comp);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s) {
-    const size_t smem = sizeof(ScanSmem);
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    scan_kernel<<<dim3(row_tiles, splits), kThreads, smem, s>>>(a);
+        na, na_pad, dk, act_idx, Xf, ldx, core, comp, norm, Xa, act_core, act_comp, act_norm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *comp,
-                            unsigned long long *ck64, unsigned *chi, cudaStream_t s, int stage) {
+                            unsigned long long *ck64, unsigned *chi, const unsigned char *proven,
+                            const unsigned char *act_flag, unsigned long long *cache,
+                            cudaStream_t s, int stage) {
     if (stage == 0)
-        comp_min_lo_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, cand, comp, ck64);
+        comp_min_lo_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, cand, comp, ck64, proven,
+                                                              act_flag, cache);
     else
         comp_min_hi_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, cand, comp, ck64, chi);
     return cudaGetLastError();

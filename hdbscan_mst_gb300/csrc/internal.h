@@ -67,38 +67,73 @@ cudaError_t launch_knn_exact(int KP, const KnnExactArgs &a, int blocks, cudaStre
 
 // ---------------------------------------------------------------- boruvka.cu
 cudaError_t launch_mst_init(int n, int *comp, unsigned long long *cand, unsigned long long *ck64,
-                            unsigned *chi, unsigned *ub, cudaStream_t s);
+                            unsigned *chi, unsigned *ub, unsigned long long *cache,
+                            cudaStream_t s);
 cudaError_t launch_nbr_candidate(int n, int L, const int32_t *kidx, const float *kdist,
-                                 const float *core, const int *comp, unsigned long long *cand,
+                                 const float *core, const int *comp,
+                                 const unsigned long long *cache, unsigned long long *cand,
                                  unsigned char *proven, unsigned *ub, unsigned *status,
                                  cudaStream_t s);
-cudaError_t launch_active(int n, const unsigned char *proven, const float *core, const int *comp,
-                          const unsigned *ub, int *act_idx, int *act_count, cudaStream_t s);
+cudaError_t launch_classify(int n, const unsigned char *proven, const float *core,
+                            const int *comp, const unsigned *ub, unsigned char *act_flag,
+                            int *size, int *act_size, int *act_count, cudaStream_t s);
+// Slots per component, then the grouped column order (perm and the column
+// arrays), the active rows grouped by component (act_idx), and the grouped
+// feature-major copy Xs.  size, act_size, cursor, act_cursor and totals must
+// start at zero.
+cudaError_t launch_group(int n, int n_pad, int dk, const int *comp, const float *core,
+                         const float *norm, const unsigned char *act_flag, const int *size,
+                         const int *act_size, int *start, int *act_start, int *cursor,
+                         int *act_cursor, int *totals, int *perm, int *col_comp, float *col_core,
+                         float *col_norm, int *act_idx, const float *Xf, float *Xs,
+                         cudaStream_t s);
 cudaError_t launch_gather(int na, int na_pad, int dk, const int *act_idx, const float *Xf,
-                          int64_t ldx, const float *core, const int *comp, float *Xa,
-                          float *act_core, int *act_comp, cudaStream_t s);
+                          int64_t ldx, const float *core, const int *comp, const float *norm,
+                          float *Xa, float *act_core, int *act_comp, float *act_norm,
+                          cudaStream_t s);
 
 struct ScanArgs {
-    const float *Xa;        // [dk][lda] active rows, feature-major
-    int64_t lda;
-    const int *act_idx;     // [na] global index of each active row, or nullptr (identity)
+    // rows: the active points grouped by component
+    const float *Xa;        // [dk][lda] feature-major
+    int64_t lda;            // padded active rows (also the stride of the candidate slabs)
+    const int *act_idx;     // [na] point index of each active row
     const float *act_core;  // [na]
     const int *act_comp;    // [na]
+    const float *act_norm;  // [na] |a|^2
     int na;
-    const float *Xf;        // [dk][ldx] all points
+    // columns: all points grouped by component
+    const float *Xs;        // [dk][ldx] feature-major
     int64_t ldx;
+    const int *col_orig;    // [n] point index of each column
+    const float *col_norm;  // [ldx] |b|^2, +inf past the last point
+    const float *col_core;  // [n]
+    const int *col_comp;    // [n]
+    const int *comp_start;  // [n] first column of each component label
+    const int *comp_size;   // [n] columns of each component label
+    // by point index (refine and exact search)
+    const float *Xp;        // [ldx][dk] point-major
     const float *core;      // [n]
     const int *comp;        // [n]
-    int n;
-    int dk;
-    int col_tiles, tiles_per_split;
-    unsigned long long *cand;  // [n] per-point least edge key, lowered by atomicMin
+    const unsigned *nbmax_bits;
+    int n, d, dk;
+    int col_tiles, tiles_per_split, splits;
+    unsigned long long *part_key;  // [splits][lda][4] kept candidates
+    float *part_tau;               // [splits][lda] least value of a dropped candidate
+    unsigned long long *cand;      // [n] per-point least edge key, lowered by atomicMin
+    int *fb_count;
+    int *fb_rows;
 };
+size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);
+cudaError_t launch_scan_refine(const ScanArgs &a, cudaStream_t s);
+// Rows are the queued points, gathered like the active rows (Xa, act_*, na).
+cudaError_t launch_scan_exact(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);
 
+// stage 0 also records exact candidates into cache (if not NULL) for the next round.
 cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *comp,
-                            unsigned long long *ck64, unsigned *chi, cudaStream_t s,
-                            int stage);
+                            unsigned long long *ck64, unsigned *chi, const unsigned char *proven,
+                            const unsigned char *act_flag, unsigned long long *cache,
+                            cudaStream_t s, int stage);
 cudaError_t launch_hook(int n, const int *comp, const unsigned long long *ck64,
                         const unsigned *chi, int *parent, int *e_lo, int *e_hi, float *e_w,
                         int *edge_count, unsigned *status, cudaStream_t s);
@@ -130,6 +165,8 @@ enum KernelId {
     K_ACTIVE,
     K_GATHER,
     K_SCAN,
+    K_SCAN_REFINE,
+    K_SCAN_EXACT,
     K_COMP_MIN,
     K_HOOK,
     K_ROOTS,

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tile.cuh"
 
 namespace hdbmst {
 
@@ -42,8 +43,7 @@ constexpr int kMaxPass = kBN / kCap + 2;  // pushes per tile are bounded by kBN 
 
 template <int KP>
 struct TileSmem {
-    float As[2][kBK][kBM];
-    float Bs[2][kBK][kBN];
+    TileBuffers T;
     float lkey[kBM][KP + 1];  // +1: rows of consecutive lanes fall in different banks
     int lidx[kBM][KP + 1];
     float ckey[kBM][kCap + 1];
@@ -52,11 +52,6 @@ struct TileSmem {
     float tau[kBM];
 };
 
-// Local row of register-block row i (0..7) of thread row ty, and local column
-// of block column j of thread column tx: two 4-wide halves 64 apart, so the
-// float4 shared loads of a warp are conflict-free.
-__device__ __forceinline__ int row_of(int ty, int i) { return (i < 4 ? 0 : 60) + ty * 4 + i; }
-__device__ __forceinline__ int col_of(int tx, int j) { return (j < 4 ? 0 : 60) + tx * 4 + j; }
 // The 16 local rows that warp w owns (thread rows ty = 2w and 2w + 1).
 __device__ __forceinline__ int warp_row(int w, int q) { return (q < 8 ? 0 : 56) + w * 8 + q; }
 
@@ -212,57 +207,20 @@ __global__ void __launch_bounds__(kThreads, 2) knn_tile_kernel(const KnnTileArgs
     }
     __syncwarp();
 
-    const int nchunks = a.dk / kBK;
-    const int nsteps = max(ct_end - ct_begin, 0) * nchunks;
-
-    auto issue = [&](int step, int buf) {
-        const int ct = ct_begin + step / nchunks;
-        const int kc = step - (step / nchunks) * nchunks;
-        const float *ga = a.Xf + static_cast<int64_t>(kc * kBK) * a.ldx + r0;
-        const float *gb = a.Yf + static_cast<int64_t>(kc * kBK) * a.ldy + static_cast<int64_t>(ct) * kBN;
-#pragma unroll
-        for (int v = tid; v < kBK * kBM / 4; v += kThreads) {
-            const int kr = v >> 5, c4 = (v & 31) * 4;
-            cp_async16(&S.As[buf][kr][c4], ga + static_cast<int64_t>(kr) * a.ldx + c4);
-            cp_async16(&S.Bs[buf][kr][c4], gb + static_cast<int64_t>(kr) * a.ldy + c4);
-        }
-        cp_async_commit();
-    };
-
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    if (nsteps > 0) issue(0, 0);
-    for (int step = 0; step < nsteps; ++step) {
-        const int buf = step & 1;
-        cp_async_wait_all();
-        __syncthreads();
-        if (step + 1 < nsteps) issue(step + 1, buf ^ 1);
+    tile_pipeline(S.T, a.Xf, a.ldx, r0, a.Yf, a.ldy, ct_begin, ct_end, 0, 0, a.dk, acc,
+                  [&](float (&ac)[8][8], int ct) {
+        tile_epilogue<KP>(S, ac, a.ynorm, ct * kBN, warp, lane, ty, tx);
 #pragma unroll
-        for (int kk = 0; kk < kBK; ++kk) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&S.As[buf][kk][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&S.Bs[buf][kk][64 + tx * 4]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
-        }
-        if ((step + 1) % nchunks == 0) {
-            const int ct = ct_begin + step / nchunks;
-            tile_epilogue<KP>(S, acc, a.ynorm, ct * kBN, warp, lane, ty, tx);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-        }
-    }
+            for (int j = 0; j < 8; ++j) ac[i][j] = 0.f;
+    });
     __syncwarp();
     if (lane < 16) {
         const int r = warp_row(warp, lane);
@@ -365,9 +323,9 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
 
     // 4. Proof that the kept set holds the exact top k.  Every dropped column
     //    z has t_z >= A.  With u = 2^-24, the expansion t + |x|^2 differs from
-    //    the true squared distance by at most E = (2d + 4) u (|x|^2 + max|y|^2)
-    //    (dot product and norms are FMA chains of length d, plus two
-    //    roundings), and the exact float32 evaluation is at least
+    //    the true squared distance by at most E = (2d + 10) u (|x|^2 + max|y|^2)
+    //    (dot product and norms are FMA chains of length d, plus a few
+    //    roundings, with slack), and the exact float32 evaluation is at least
     //    (1 - (d + 3) u) times the true value.  If that lower bound still
     //    exceeds the k-th kept distance squared (with sqrt rounding slack),
     //    no dropped column can rank in the top k.
@@ -376,7 +334,7 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
         const double dk = key_w(key);
         const double na = a.xnorm[row];
         const double nb = __uint_as_float(*a.nbmax_bits);
-        const double E = (2.0 * a.d + 4.0) * u * 1.01 * (na + nb);
+        const double E = (2.0 * a.d + 10.0) * u * 1.01 * (na + nb);
         const double lb = (static_cast<double>(A) + na - E) * (1.0 - (a.d + 3.0) * u);
         if (!(lb * (1.0 - 4.0 * u) > dk * dk)) {
             const int pos = atomicAdd(a.fb_count, 1);

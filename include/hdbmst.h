@@ -213,10 +213,13 @@ const char *hdbmst_profile_kernel_name(int i);
 /*
  * Rounds of the most recent hdbmst_mr_mst call in this process: returns the
  * number of Boruvka rounds; for each of the first max_rounds rounds writes
- * the number of points scanned against all others (active[i]) and the tree
- * edges found so far (edges[i]).  Either pointer may be NULL.
+ * the number of points scanned against all others (active[i]), the tree
+ * edges found so far (edges[i]) and how many scanned points the rounding
+ * proof could not settle and were searched again exactly (exact_rows[i]).
+ * Any pointer may be NULL.
  */
-int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int max_rounds);
+int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
+                           int max_rounds);
 
 #ifdef __cplusplus
 }
