@@ -26,6 +26,7 @@ from . import build as _build
 __all__ = [
     "knn", "core_distances", "mr_mst", "hdbscan_mst", "HdbmstError", "HdbmstUnavailable",
     "launch_count", "profile_enable", "profile_read", "last_mst_rounds", "library_path", "KMAX",
+    "set_engine",
 ]
 
 KMAX = 32
@@ -88,6 +89,8 @@ def _load():
                                          ctypes.POINTER(ctypes.c_int64),
                                          ctypes.POINTER(ctypes.c_int64), i32]
     L.hdbmst_last_mst_rounds.restype = i32
+    L.hdbmst_set_engine.argtypes = [i32]
+    L.hdbmst_set_engine.restype = i32
     _lib = L
     return L
 
@@ -258,6 +261,16 @@ def hdbscan_mst(X, min_samples: int, *, shortcuts: bool = True):
 
 
 # ---------------------------------------------------------------- instrumentation
+
+ENGINES = {"auto": 0, "simt": 1, "tensor": 2}
+
+
+def set_engine(engine: str) -> str:
+    """Select the distance-tile engine ("auto", "simt" or "tensor"); returns the
+    previous one.  Results are identical whichever engine runs."""
+    prev = _load().hdbmst_set_engine(ENGINES[engine])
+    return {v: k for k, v in ENGINES.items()}[prev]
+
 
 def launch_count() -> int:
     """Kernels the library has launched in this process."""

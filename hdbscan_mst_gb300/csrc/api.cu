@@ -11,6 +11,7 @@
 #include "../../include/hdbmst.h"
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 using namespace hdbmst;
 
@@ -26,6 +27,13 @@ struct ProfRec {
 };
 std::vector<ProfRec> g_recs;
 std::vector<cudaEvent_t> g_pool;
+// distance-tile engine (HDBMST_ENGINE_*), process-wide
+int g_engine = HDBMST_ENGINE_AUTO;
+
+bool use_tensor(int dk) {
+    return g_engine != HDBMST_ENGINE_SIMT && tc_knn_supported(dk);
+}
+
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
 std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
 
@@ -140,7 +148,7 @@ KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
     p.n = static_cast<int>(n);
     p.m = static_cast<int>(m);
     p.d = d;
-    p.dk = static_cast<int>(round_up(d, kBK));
+    p.dk = padded_features(d);
     p.k = k;
     p.KP = k <= 12 ? 16 : 32;
     p.n_pad = round_up(std::max<int64_t>(n, 1), kBM);
@@ -155,7 +163,7 @@ KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
 }
 
 struct KnnBufs {
-    float *Xf, *Xp, *xnorm, *Yf, *Yp, *ynorm;
+    float *Xf, *Xp, *Xlo, *xnorm, *Yf, *Yp, *Ylo, *ynorm;
     float *part_key;
     int *part_idx;
     int *fb_rows;
@@ -166,15 +174,20 @@ struct KnnBufs {
 
 void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
     b.Xf = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    // the tensor-core tile's low parts exist only where that engine can run
+    const bool lo = p.dk <= 64;
     b.Xp = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xlo = lo ? c.take<float>(static_cast<size_t>(p.dk) * p.n_pad) : nullptr;
     b.xnorm = c.take<float>(p.n_pad);
     if (p.alias) {
         b.Yf = b.Xf;
         b.Yp = b.Xp;
+        b.Ylo = b.Xlo;
         b.ynorm = b.xnorm;
     } else {
         b.Yf = c.take<float>(static_cast<size_t>(p.dk) * p.m_pad);
         b.Yp = c.take<float>(static_cast<size_t>(p.dk) * p.m_pad);
+        b.Ylo = lo ? c.take<float>(static_cast<size_t>(p.dk) * p.m_pad) : nullptr;
         b.ynorm = c.take<float>(p.m_pad);
     }
     const size_t part = static_cast<size_t>(kMaxSplits) * p.chunk_rows * p.KP;
@@ -207,16 +220,20 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
                       const float *Y, int64_t ldy, int32_t *out_idx, float *out_dist,
                       float *out_core, int core_rank, cudaStream_t s) {
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
+    const bool tensor = use_tensor(p.dk) && b.Xlo != nullptr;
     if (p.alias) {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
-                                      b.Xp, b.xnorm, &b.st->status, &b.st->nbmax_bits, s));
+                                      b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
+                                      &b.st->nbmax_bits, s));
     } else {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
-                                      b.Xp, b.xnorm, &b.st->status, nullptr, s));
+                                      b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
+                                      nullptr, s));
         LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
-                                      b.Yp, b.ynorm, &b.st->status, &b.st->nbmax_bits, s));
+                                      b.Yp, tensor ? b.Ylo : nullptr, b.ynorm, &b.st->status,
+                                      &b.st->nbmax_bits, s));
     }
-    const int slots = 2 * sm_count();
+    const int slots = (tensor ? 1 : 2) * sm_count();
     for (int base = 0; base < p.n; base += p.chunk_rows) {
         const int rows = std::min(p.chunk_rows, p.n - base);
         const int row_tiles = (rows + kBM - 1) / kBM;
@@ -237,7 +254,16 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.tiles_per_split = tps;
         ta.part_key = b.part_key;
         ta.part_idx = b.part_idx;
-        LAUNCH(K_KNN_TILE, s, launch_knn_tile(p.KP, ta, row_tiles, S, s));
+        ta.Xp = b.Xp;
+        ta.Yp = b.Yp;
+        ta.m = p.m;
+        ta.status = &b.st->status;
+        if (tensor) {
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
+                                                row_tiles, S, s));
+        } else {
+            LAUNCH(K_KNN_TILE, s, launch_knn_tile(p.KP, ta, row_tiles, S, s));
+        }
         KnnRefineArgs ra{};
         ra.part_key = b.part_key;
         ra.part_idx = b.part_idx;
@@ -249,6 +275,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.Yp = b.Yp;
         ra.xnorm = b.xnorm;
         ra.nbmax_bits = &b.st->nbmax_bits;
+        ra.err_coef = tensor ? tc::err_coef(p.d, p.dk) : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01;
         ra.d = p.d;
         ra.dk = p.dk;
         ra.k = p.k;
@@ -278,6 +305,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     hdbmst_status st = read_status(b.st, h, s);
     if (st != HDBMST_OK) return st;
     if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+    if (h.status & kStatusTimeout) return HDBMST_ERR_CUDA;
     return HDBMST_OK;
 }
 
@@ -293,7 +321,7 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
     MstPlan p{};
     p.n = static_cast<int>(n);
     p.d = d;
-    p.dk = static_cast<int>(round_up(d, kBK));
+    p.dk = padded_features(d);
     p.L = L;
     p.n_pad = round_up(std::max<int64_t>(n, 1), kBM);
     int bits = 1;
@@ -303,7 +331,8 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
 }
 
 struct MstBufs {
-    float *Xf, *Xp, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
+    float *Xf, *Xp, *Xlo, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
+    float *Xs_hi, *Xs_lo, *Xa_hi, *Xa_lo;  // point-major grouped columns / active rows
     int *act_comp, *act_idx, *comp, *parent, *root_of, *perm, *col_comp, *start, *act_start;
     int *counters;  // [4n + 8]: size, act_size, cursor, act_cursor, totals (zeroed per round)
     unsigned char *act_flag;
@@ -328,6 +357,11 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     b.act_comp = c.take<int>(p.n_pad);
     b.act_norm = c.take<float>(p.n_pad);
     b.Xs = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xlo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xs_hi = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xs_lo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xa_hi = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    b.Xa_lo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.col_core = c.take<float>(n);
     b.col_norm = c.take<float>(p.n_pad);
     b.perm = c.take<int>(n);
@@ -522,9 +556,11 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     const int slots = 2 * sm_count();
     const int col_tiles = static_cast<int>(p.n_pad / kBN);
 
+    const bool tensor = use_tensor(p.dk);
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
     LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, b.Xp,
-                                  b.norm, &b.st->status, &b.st->nbmax_bits, s));
+                                  tensor ? b.Xlo : nullptr, b.norm, &b.st->status,
+                                  &b.st->nbmax_bits, s));
     LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
     LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, b.cache, s));
 
@@ -556,14 +592,22 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         const int na = h.act_count;
         if (na > 0) {
             const int na_pad = static_cast<int>(round_up(na, kBM));
-            LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), p.dk, b.comp, core,
-                                             b.norm, b.act_flag, size, act_size, b.start,
-                                             b.act_start, cursor, act_cursor, totals, b.perm,
-                                             b.col_comp, b.col_core, b.col_norm, b.act_idx, b.Xf,
-                                             b.Xs, s));
+            LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), b.comp, core, b.norm,
+                                             b.act_flag, size, act_size, b.start, b.act_start,
+                                             cursor, act_cursor, totals, b.perm, b.col_comp,
+                                             b.col_core, b.col_norm, b.act_idx, s));
             LAUNCH(K_GATHER, s, launch_gather(na, na_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
-                                              b.comp, b.norm, b.Xa, b.act_core, b.act_comp,
-                                              b.act_norm, s));
+                                              b.comp, b.norm, tensor ? nullptr : b.Xa, b.act_core,
+                                              b.act_comp, b.act_norm, s));
+            if (tensor) {
+                LAUNCH(K_GATHER, s, launch_gather_points(N, static_cast<int>(p.n_pad), p.dk, b.perm,
+                                                         b.Xp, b.Xlo, b.Xs_hi, b.Xs_lo, s));
+                LAUNCH(K_GATHER, s, launch_gather_points(na, na_pad, p.dk, b.act_idx, b.Xp, b.Xlo,
+                                                         b.Xa_hi, b.Xa_lo, s));
+            } else {
+                LAUNCH(K_GATHER, s, launch_gather_cols(N, static_cast<int>(p.n_pad), p.dk, b.perm,
+                                                       b.Xf, b.Xs, s));
+            }
             ScanArgs sa{};
             sa.Xa = b.Xa;
             sa.lda = na_pad;
@@ -589,7 +633,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.dk = p.dk;
             sa.col_tiles = col_tiles;
             const int row_tiles = (na + kBM - 1) / kBM;
-            const int S0 = choose_splits(row_tiles, col_tiles, slots);
+            const int S0 = choose_splits(row_tiles, col_tiles, tensor ? slots / 2 : slots);
             const int tps = (col_tiles + S0 - 1) / S0;
             const int S = (col_tiles + tps - 1) / tps;
             sa.tiles_per_split = tps;
@@ -599,16 +643,26 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.cand = b.cand;
             sa.fb_count = &b.st->fb_count;
             sa.fb_rows = b.fb_rows;
+            sa.status = &b.st->status;
             CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
-            LAUNCH(K_SCAN, s, launch_scan(sa, row_tiles, S, s));
+            if (tensor) {
+                LAUNCH(K_SCAN, s, launch_tc_scan(sa, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo, row_tiles,
+                                                 S, s));
+            } else {
+                LAUNCH(K_SCAN, s, launch_scan(sa, row_tiles, S, s));
+            }
             LAUNCH(K_SCAN_REFINE, s, launch_scan_refine(sa, s));
             rs = read_status(b.st, h, s);
             if (rs != HDBMST_OK) return rs;
+            if (h.status & kStatusTimeout) return HDBMST_ERR_CUDA;
             const int nf = h.fb_count;
             fallback = nf;
             if (nf > 0) {
                 // rows the rounding proof left open: gather them as rows and
                 // search them again with the exact weight
+                if (tensor)
+                    LAUNCH(K_GATHER, s, launch_gather_cols(N, static_cast<int>(p.n_pad), p.dk,
+                                                           b.perm, b.Xf, b.Xs, s));
                 const int nf_pad = static_cast<int>(round_up(nf, kBM));
                 LAUNCH(K_GATHER, s, launch_gather(nf, nf_pad, p.dk, b.fb_rows, b.Xf, p.n_pad,
                                                   core, b.comp, b.norm, b.Xa, b.act_core,
@@ -674,6 +728,14 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
     KnnBufs b{};
     carve_knn(c, p, b, false);
     return run_knn(p, b, X, ldx, Y, ldy, out_idx, out_dist, nullptr, 0, s);
+}
+
+int hdbmst_set_engine(int engine) {
+    const int prev = g_engine;
+    if (engine == HDBMST_ENGINE_AUTO || engine == HDBMST_ENGINE_SIMT ||
+        engine == HDBMST_ENGINE_TENSOR)
+        g_engine = engine;
+    return prev;
 }
 
 uint64_t hdbmst_launch_count(void) { return g_launches.load(); }

@@ -186,19 +186,43 @@ __global__ void group_kernel(int n, const int *__restrict__ comp, const float *_
 }
 
 // Columns in grouped order into their own feature-major buffer; padding
-// columns are zero with norm +inf.
+// columns are zero.
 __global__ void gather_cols_kernel(int n, int n_pad, const int *__restrict__ perm,
-                                   const float *__restrict__ Xf, float *__restrict__ Xs,
-                                   float *__restrict__ col_norm) {
+                                   const float *__restrict__ Xf, float *__restrict__ Xs) {
     const int pos = blockIdx.x * blockDim.x + threadIdx.x;
     const int f = blockIdx.y;
     if (pos >= n_pad) return;
     const int g = pos < n ? perm[pos] : -1;
     Xs[static_cast<int64_t>(f) * n_pad + pos] = g >= 0 ? Xf[static_cast<int64_t>(f) * n_pad + g] : 0.f;
-    if (f == 0 && g < 0) col_norm[pos] = INFINITY;
 }
 
-// Active rows into their own padded feature-major buffer.
+// Padding columns of the grouped order never rank (+inf norm).
+__global__ void pad_norms_kernel(int n, int n_pad, float *__restrict__ col_norm) {
+    const int pos = n + blockIdx.x * blockDim.x + threadIdx.x;
+    if (pos < n_pad) col_norm[pos] = INFINITY;
+}
+
+// Point-major rows by index, hi and lo parts, one float4 per thread.
+__global__ void gather_points_kernel(int count, int count_pad, int dk, const int *__restrict__ idx,
+                                     const float4 *__restrict__ src_hi,
+                                     const float4 *__restrict__ src_lo, float4 *__restrict__ dst_hi,
+                                     float4 *__restrict__ dst_lo) {
+    const int q4 = dk / 4;
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= static_cast<int64_t>(count_pad) * q4) return;
+    const int r = static_cast<int>(e / q4), q = static_cast<int>(e - static_cast<int64_t>(r) * q4);
+    float4 h = make_float4(0.f, 0.f, 0.f, 0.f), l = h;
+    if (r < count) {
+        const int64_t g = static_cast<int64_t>(idx[r]) * q4 + q;
+        h = src_hi[g];
+        l = src_lo[g];
+    }
+    dst_hi[e] = h;
+    dst_lo[e] = l;
+}
+
+// Active rows into their own padded feature-major buffer (skipped when Xa is
+// null), with their core distance, component and squared norm.
 __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict__ act_idx,
                               const float *__restrict__ Xf, int64_t ldx,
                               const float *__restrict__ core, const int *__restrict__ comp,
@@ -209,7 +233,8 @@ __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict_
     const int f = blockIdx.y;
     if (r >= na_pad) return;
     const int g = r < na ? act_idx[r] : -1;
-    Xa[static_cast<int64_t>(f) * na_pad + r] = g >= 0 ? Xf[static_cast<int64_t>(f) * ldx + g] : 0.f;
+    if (Xa)
+        Xa[static_cast<int64_t>(f) * na_pad + r] = g >= 0 ? Xf[static_cast<int64_t>(f) * ldx + g] : 0.f;
     if (f == 0) {
         act_core[r] = g >= 0 ? core[g] : 0.f;
         act_comp[r] = g >= 0 ? comp[g] : -1;
@@ -346,11 +371,10 @@ cudaError_t launch_classify(int n, const unsigned char *proven, const float *cor
     return cudaGetLastError();
 }
 
-cudaError_t launch_group(int n, int n_pad, int dk, const int *comp, const float *core,
-                         const float *norm, const unsigned char *act_flag, const int *size,
-                         const int *act_size, int *start, int *act_start, int *cursor,
-                         int *act_cursor, int *totals, int *perm, int *col_comp, float *col_core,
-                         float *col_norm, int *act_idx, const float *Xf, float *Xs,
+cudaError_t launch_group(int n, int n_pad, const int *comp, const float *core, const float *norm,
+                         const unsigned char *act_flag, const int *size, const int *act_size,
+                         int *start, int *act_start, int *cursor, int *act_cursor, int *totals,
+                         int *perm, int *col_comp, float *col_core, float *col_norm, int *act_idx,
                          cudaStream_t s) {
     slots_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, size, act_size, start, act_start, totals);
     cudaError_t e = cudaGetLastError();
@@ -360,8 +384,24 @@ cudaError_t launch_group(int n, int n_pad, int dk, const int *comp, const float 
                                                     col_norm, act_idx);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gather_cols_kernel<<<dim3(blocks_for(n_pad, 256), dk), 256, 0, s>>>(n, n_pad, perm, Xf, Xs,
-                                                                        col_norm);
+    if (n_pad > n) pad_norms_kernel<<<blocks_for(n_pad - n, 256), 256, 0, s>>>(n, n_pad, col_norm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_cols(int n, int n_pad, int dk, const int *perm, const float *Xf,
+                               float *Xs, cudaStream_t s) {
+    gather_cols_kernel<<<dim3(blocks_for(n_pad, 256), dk), 256, 0, s>>>(n, n_pad, perm, Xf, Xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_points(int count, int count_pad, int dk, const int *idx,
+                                 const float *src_hi, const float *src_lo, float *dst_hi,
+                                 float *dst_lo, cudaStream_t s) {
+    const int64_t total = static_cast<int64_t>(count_pad) * (dk / 4);
+    gather_points_kernel<<<static_cast<int>((total + 255) / 256), 256, 0, s>>>(
+        count, count_pad, dk, idx, reinterpret_cast<const float4 *>(src_hi),
+        reinterpret_cast<const float4 *>(src_lo), reinterpret_cast<float4 *>(dst_hi),
+        reinterpret_cast<float4 *>(dst_lo));
     return cudaGetLastError();
 }
 
@@ -369,7 +409,7 @@ cudaError_t launch_gather(int na, int na_pad, int dk, const int *act_idx, const 
                           int64_t ldx, const float *core, const int *comp, const float *norm,
                           float *Xa, float *act_core, int *act_comp, float *act_norm,
                           cudaStream_t s) {
-    gather_kernel<<<dim3(blocks_for(na_pad, 256), dk), 256, 0, s>>>(
+    gather_kernel<<<dim3(blocks_for(na_pad, 256), Xa ? dk : 1), 256, 0, s>>>(
         na, na_pad, dk, act_idx, Xf, ldx, core, comp, norm, Xa, act_core, act_comp, act_norm);
     return cudaGetLastError();
 }

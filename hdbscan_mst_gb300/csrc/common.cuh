@@ -19,6 +19,7 @@ constexpr unsigned kStatusNonFinite = 1u;
 constexpr unsigned kStatusNoConverge = 2u;
 constexpr unsigned kStatusOverflow = 4u;
 constexpr unsigned kStatusBadList = 8u;
+constexpr unsigned kStatusTimeout = 16u;  // a bounded wait on the tensor core gave up
 
 constexpr unsigned long long kNoKey = ~0ull;
 
@@ -42,6 +43,15 @@ __device__ __forceinline__ float key_w(unsigned long long k) {
     return __uint_as_float(static_cast<unsigned>(k >> 32));
 }
 __device__ __forceinline__ unsigned key_i(unsigned long long k) { return static_cast<unsigned>(k); }
+
+// Order-preserving map of any float (negative ones included) to unsigned.
+__device__ __forceinline__ unsigned float_order(float v) {
+    const unsigned b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float order_float(unsigned o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
 
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;

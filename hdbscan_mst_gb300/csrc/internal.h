@@ -9,12 +9,13 @@ namespace hdbmst {
 
 // ---------------------------------------------------------------- pack.cu
 // Copy a caller [d, n] set (leading dim ld) into the padded feature-major
-// buffer Xf [dk][n_pad] and, if Xp != nullptr, the point-major buffer
-// Xp [n_pad][dk]; write norm[i] = sum of x^2 (+inf for padding points);
-// flag non-finite values; raise *nbmax_bits to the largest norm's bits.
+// buffer Xf [dk][n_pad] and, if not nullptr, the point-major buffer
+// Xp [n_pad][dk] and its tensor-core low parts Xlo = x - tf32(x); write
+// norm[i] = sum of x^2 (+inf for padding points); flag non-finite values;
+// raise *nbmax_bits to the largest norm's bits.
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
-                        float *Xp, float *norm, unsigned *status, unsigned *nbmax_bits,
-                        cudaStream_t s);
+                        float *Xp, float *Xlo, float *norm, unsigned *status,
+                        unsigned *nbmax_bits, cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
 
@@ -32,9 +33,22 @@ struct KnnTileArgs {
     int tiles_per_split;
     float *part_key;     // [S][chunk_rows_pad][KP] approximate keys
     int *part_idx;       // [S][chunk_rows_pad][KP] column indices
+    // tensor-core engine only
+    const float *Xp, *Yp;  // point-major [.][dk] query rows and columns
+    int m;                 // columns
+    unsigned *status;      // device status word (timeouts)
 };
 cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
                             cudaStream_t s);
+// tc_knn.cu: the same tile on tcgen05 TF32 MMAs (three passes), one CTA per SM,
+// operands by TMA from the point-major arrays (Xp / Yp and their low parts).
+bool tc_knn_supported(int dk);
+cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
+                          int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
+                          cudaStream_t s);
+// Padded feature count: whole 32-feature slabs up to 64 (the tensor-core tile's
+// operand granule), multiples of 16 beyond.
+inline int padded_features(int d) { return d <= 64 ? (d + 31) / 32 * 32 : (d + 15) / 16 * 16; }
 
 struct KnnRefineArgs {
     const float *part_key;
@@ -43,6 +57,7 @@ struct KnnRefineArgs {
     const float *Xp, *Yp;  // point-major [.][dk]
     const float *xnorm;
     const unsigned *nbmax_bits;
+    double err_coef;  // E = err_coef (|x|^2 + max |y|^2) bounds the ranking error
     int d, dk, k, m;
     int core_rank;  // 1-based list position copied to out_core (0: none)
     int32_t *out_idx;
@@ -78,15 +93,22 @@ cudaError_t launch_classify(int n, const unsigned char *proven, const float *cor
                             const int *comp, const unsigned *ub, unsigned char *act_flag,
                             int *size, int *act_size, int *act_count, cudaStream_t s);
 // Slots per component, then the grouped column order (perm and the column
-// arrays), the active rows grouped by component (act_idx), and the grouped
-// feature-major copy Xs.  size, act_size, cursor, act_cursor and totals must
+// arrays, col_norm +inf for padding columns) and the active rows grouped by
+// component (act_idx).  size, act_size, cursor, act_cursor and totals must
 // start at zero.
-cudaError_t launch_group(int n, int n_pad, int dk, const int *comp, const float *core,
-                         const float *norm, const unsigned char *act_flag, const int *size,
-                         const int *act_size, int *start, int *act_start, int *cursor,
-                         int *act_cursor, int *totals, int *perm, int *col_comp, float *col_core,
-                         float *col_norm, int *act_idx, const float *Xf, float *Xs,
+cudaError_t launch_group(int n, int n_pad, const int *comp, const float *core, const float *norm,
+                         const unsigned char *act_flag, const int *size, const int *act_size,
+                         int *start, int *act_start, int *cursor, int *act_cursor, int *totals,
+                         int *perm, int *col_comp, float *col_core, float *col_norm, int *act_idx,
                          cudaStream_t s);
+// Grouped feature-major columns: Xs[f][pos] = Xf[f][perm[pos]] (0 past n).
+cudaError_t launch_gather_cols(int n, int n_pad, int dk, const int *perm, const float *Xf,
+                               float *Xs, cudaStream_t s);
+// Point-major rows by index: dst[r] = src[idx[r]] for r < count, zero up to
+// count_pad; both the hi (raw) and lo arrays.
+cudaError_t launch_gather_points(int count, int count_pad, int dk, const int *idx,
+                                 const float *src_hi, const float *src_lo, float *dst_hi,
+                                 float *dst_lo, cudaStream_t s);
 cudaError_t launch_gather(int na, int na_pad, int dk, const int *act_idx, const float *Xf,
                           int64_t ldx, const float *core, const int *comp, const float *norm,
                           float *Xa, float *act_core, int *act_comp, float *act_norm,
@@ -122,12 +144,18 @@ struct ScanArgs {
     unsigned long long *cand;      // [n] per-point least edge key, lowered by atomicMin
     int *fb_count;
     int *fb_rows;
+    unsigned *status;              // device status word (tensor-core timeouts)
 };
 size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);
 cudaError_t launch_scan_refine(const ScanArgs &a, cudaStream_t s);
 // Rows are the queued points, gathered like the active rows (Xa, act_*, na).
 cudaError_t launch_scan_exact(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);
+// tc_scan.cu: the scan on tcgen05 TF32 MMAs; A = active rows, B = grouped
+// columns, point-major hi (raw) and lo parts, dk = 32 or 64.
+cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *Xa_lo,
+                           const float *Xs_hi, const float *Xs_lo, int row_tiles, int splits,
+                           cudaStream_t s);
 
 // stage 0 also records exact candidates into cache (if not NULL) for the next round.
 cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *comp,

@@ -322,10 +322,11 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     if (a.out_core && gl == a.core_rank - 1) a.out_core[row] = key_w(key);
 
     // 4. Proof that the kept set holds the exact top k.  Every dropped column
-    //    z has t_z >= A.  With u = 2^-24, the expansion t + |x|^2 differs from
-    //    the true squared distance by at most E = (2d + 10) u (|x|^2 + max|y|^2)
-    //    (dot product and norms are FMA chains of length d, plus a few
-    //    roundings, with slack), and the exact float32 evaluation is at least
+    //    z has t_z >= A.  The expansion t + |x|^2 differs from the true squared
+    //    distance by at most E = err_coef (|x|^2 + max|y|^2) (for the FFMA tile
+    //    err_coef = (2d + 10) u with u = 2^-24: dot product and norms are FMA
+    //    chains of length d, plus a few roundings, with slack; the tensor-core
+    //    tile has its own, larger coefficient), and the exact float32 evaluation is at least
     //    (1 - (d + 3) u) times the true value.  If that lower bound still
     //    exceeds the k-th kept distance squared (with sqrt rounding slack),
     //    no dropped column can rank in the top k.
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
         const double dk = key_w(key);
         const double na = a.xnorm[row];
         const double nb = __uint_as_float(*a.nbmax_bits);
-        const double E = (2.0 * a.d + 10.0) * u * 1.01 * (na + nb);
+        const double E = a.err_coef * (na + nb);
         const double lb = (static_cast<double>(A) + na - E) * (1.0 - (a.d + 3.0) * u);
         if (!(lb * (1.0 - 4.0 * u) > dk * dk)) {
             const int pos = atomicAdd(a.fb_count, 1);

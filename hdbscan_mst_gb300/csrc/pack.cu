@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    int d, int n_pad, int dk,
                                                    float *__restrict__ Xf,
                                                    float *__restrict__ Xp,
+                                                   float *__restrict__ Xlo,
                                                    float *__restrict__ norm,
                                                    unsigned *__restrict__ status,
                                                    unsigned *__restrict__ nbmax_bits) {
@@ -44,6 +45,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
             if (Xp)
                 *reinterpret_cast<float4 *>(Xp + static_cast<int64_t>(i) * dk + f) =
                     make_float4(v[0], v[1], v[2], v[3]);
+            if (Xlo) {
+                // x - tf32(x), where tf32() keeps the top 19 bits (the tensor-core
+                // tile's second operand part)
+                float l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    l[q] = __fsub_rn(v[q], __uint_as_float(__float_as_uint(v[q]) & 0xFFFFE000u));
+                *reinterpret_cast<float4 *>(Xlo + static_cast<int64_t>(i) * dk + f) =
+                    make_float4(l[0], l[1], l[2], l[3]);
+            }
         }
         norm[i] = valid ? acc : INFINITY;
     }
@@ -67,10 +78,11 @@ __global__ void check_core_kernel(const float *__restrict__ core, int n,
 }  // namespace
 
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
-                        float *Xp, float *norm, unsigned *status, unsigned *nbmax_bits,
-                        cudaStream_t s) {
+                        float *Xp, float *Xlo, float *norm, unsigned *status,
+                        unsigned *nbmax_bits, cudaStream_t s) {
     const int blocks = static_cast<int>((n_pad + 255) / 256);
-    pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, norm, status, nbmax_bits);
+    pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
+                                       nbmax_bits);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,181 @@
+// Tensor-core (tcgen05, sm_103a) building blocks of the distance tile: TMEM
+// allocation, shared-memory matrix descriptors, the TF32 MMA, completion
+// barriers with bounded waits, and TMEM loads.
+//
+// Operands are K-major tiles in the 128-byte swizzled layout: a 32-feature
+// slab of R rows takes R x 128 bytes; row r sits at (r / 8) * 1024 + (r % 8) * 128
+// and its 16-byte chunk c (features 4c .. 4c+3) at chunk position c ^ (r % 8).
+// Each slab starts on a 1024-byte boundary.  One MMA consumes 8 features
+// (32 bytes); successive MMAs of a slab advance the descriptor's start address
+// by 32 bytes.
+//
+// The dot products use three TF32 passes, x.y ~ hi(x).hi(y) + hi(x).lo(y) +
+// lo(x).hi(y) with lo(x) = x - tf32(x).  The tensor core reads the raw float32
+// value as hi(x): it keeps the top 19 bits (measured on GB300: a raw product
+// matches the truncated-input reference to 2e-7 and differs from the rounded
+// one by 7e-4), so lo(x) is formed against truncation.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace hdbmst {
+namespace tc {
+
+constexpr int kRows = 128;        // rows of a tile = TMEM lanes
+constexpr int kCols = 128;        // columns of a tile (MMA N)
+constexpr int kSlab = 32;         // features per swizzled slab
+constexpr int kSlabBytes = 128;   // bytes per row per slab
+// Every mbarrier wait polls at most kWaitPolls times; each poll may suspend the
+// thread for up to kSuspendNs (it wakes as soon as the phase completes), so a
+// wait gives up after about kWaitPolls * kSuspendNs = 1.6 s.
+constexpr uint32_t kWaitPolls = 1u << 14;
+constexpr uint32_t kSuspendNs = 100000;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of the 16-byte chunk c (0..7) of row r within a slab.
+__device__ __forceinline__ uint32_t swz_chunk(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor: start address, leading offset (unused for
+// swizzled K-major), stride between 8-row groups = 1024 B, version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor: F32 accumulate, TF32 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on `mbar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *mbar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(mbar)));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(count));
+}
+
+// Wait for the given phase parity; returns false if the wait gave up (the
+// caller records an error and winds down).  The thread sleeps inside each
+// poll instead of spinning, so waiting lanes leave the issue slots to the
+// epilogue warps.
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < kWaitPolls && !done; ++it) {
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(mbar)), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+    }
+    return done != 0;
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// One warp allocates `cols` TMEM columns and writes the base address to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void tmem_free(uint32_t base, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols));
+}
+
+// 32 consecutive TMEM columns of this thread's lane (warp w reads lanes 32 (w % 4) ..).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
+}
+
+// Arrive and announce `bytes` of TMA traffic that will complete this phase.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// TMA: copy the box at element coordinates (x, y) of a 2-D tensor map into
+// shared memory, completing `bytes` on `mbar`.  x * 4 bytes must be a
+// multiple of 16 (every caller passes x = 0 or 32).
+__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void *tmap, int x, int y,
+                                            uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+// 16-byte async copy; src_bytes = 0 fills the chunk with zeros without reading.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void *gmem, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem),
+                 "r"(src_bytes));
+}
+
+// lo(x) = x - tf32(x) for four values, where tf32() keeps the top 19 bits.
+__device__ __forceinline__ float4 tf32_lo(float4 x) {
+    float4 l;
+    l.x = __fsub_rn(x.x, __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u));
+    l.y = __fsub_rn(x.y, __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u));
+    l.z = __fsub_rn(x.z, __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u));
+    l.w = __fsub_rn(x.w, __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
+    return l;
+}
+
+// Bound on |computed t - (|y|^2 - 2 x.y)| relative to |x|^2 + |y|^2 for the
+// three-pass TF32 dot: the dropped lo.lo term and the TF32 truncation of the
+// lo parts (3 x 2^-20), float32 accumulation over 3 dk products (3 dk 2^-23),
+// and the norms' FMA chains plus the final rounding ((d + 4) 2^-24), with 5%
+// slack.
+__host__ __device__ inline double err_coef(int d, int dk) {
+    return (3.0 * 0x1p-20 + 3.0 * dk * 0x1p-23 + (d + 4.0) * 0x1p-24) * 1.05;
+}
+
+}  // namespace tc
+}  // namespace hdbmst

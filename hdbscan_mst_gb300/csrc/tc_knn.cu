@@ -1,0 +1,221 @@
+// K1 on the tensor cores: the k-NN distance tile with tcgen05 TF32 MMAs.
+//
+// Same contract as knn_tile_kernel (page "Kilosort4 clustering and matching",
+// gpu/clustering, "k-nearest neighbours are a matrix product": the distances
+// of a block of rows to a set are one matrix product plus two norm vectors,
+// and a small selection keeps the smallest per row).  A CTA owns 128 query
+// rows and a range of 128-column tiles; it writes, per row, the KP best
+// (t = |y|^2 - 2 x.y, column) of its range, which knn_refine_kernel merges,
+// re-evaluates exactly and proves (with this engine's rounding bound).
+//
+// Warp roles (one CTA per SM): E epilogue warps (E = 16 for KP = 16, 8 for
+// KP = 32), then one producer warp and one MMA warp.
+//  * the producer (one lane) streams operands with TMA: the CTA's query rows
+//    once (hi and lo parts, resident), then every column tile slab by slab
+//    (32 features, hi and lo) through a 4-stage ring guarded by full/empty
+//    mbarriers;
+//  * the MMA warp (one lane) issues per slab 3 x 4 TF32 MMAs
+//    (hi.hi + hi.lo + lo.hi) into one of two TMEM accumulators, frees each
+//    ring stage with tcgen05.commit, and signals the accumulator when a tile
+//    is complete;
+//  * epilogue warp w reads TMEM lanes 32 (w % 4) .. (its 32 rows) and the
+//    column quarter (or half) w / 4 of each tile: each row is shared by E / 4
+//    threads, each keeping the best KP of its columns in registers with the
+//    fixed compare-and-swap sink (page "HDBSCAN", "The hang").  The threads
+//    of a row publish their KP-th key in shared memory and filter against the
+//    least of them (a candidate that cannot beat it cannot reach the row's top
+//    KP), so the row's insertions stay those of one list.  At the end the
+//    lists of a row are merged.
+// Every wait is bounded; a wait that gives up flags the status word, stops
+// every role, drains what it issued, and the CTA frees its TMEM.
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tc_pipe.cuh"
+
+namespace hdbmst {
+
+namespace {
+
+using namespace tc;
+
+struct TcKnnParams {
+    PipeMaps maps;  // A: query rows, B: columns, point-major [rows][dk]
+    KnnTileArgs a;
+};
+
+template <int KP>
+struct Epi {
+    static constexpr int kWarps = KP == 16 ? 16 : 8;   // epilogue warps
+    static constexpr int kParts = kWarps / 4;          // threads per row
+    static constexpr int kThreads = (kWarps + 2) * 32; // + producer + MMA warp
+};
+
+__shared__ float g_row_tau[4][kRows];  // per column part and row: that thread's KP-th key
+
+template <int KP>
+__device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float t, int j) {
+    if (t < k[KP - 1] || (t == k[KP - 1] && j < ix[KP - 1])) {
+        k[KP - 1] = t;
+        ix[KP - 1] = j;
+#pragma unroll
+        for (int p = KP - 1; p > 0; --p) {
+            const bool sw = k[p] < k[p - 1] || (k[p] == k[p - 1] && ix[p] < ix[p - 1]);
+            const float kl = sw ? k[p] : k[p - 1], kh = sw ? k[p - 1] : k[p];
+            const int il = sw ? ix[p] : ix[p - 1], ih = sw ? ix[p - 1] : ix[p];
+            k[p - 1] = kl;
+            k[p] = kh;
+            ix[p - 1] = il;
+            ix[p] = ih;
+        }
+    }
+}
+
+template <int KP>
+__global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
+    tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
+    constexpr int kEpiWarps = Epi<KP>::kWarps;
+    constexpr int kParts = Epi<KP>::kParts;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PipeSmem S;
+    const KnnTileArgs &a = P.a;
+    uint8_t *base = pipe_base(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row_tile = blockIdx.x, split = blockIdx.y;
+    const int r0 = a.row_base + row_tile * kRows;
+    const int ct_begin = split * a.tiles_per_split;
+    const TileSeq seq(ct_begin, min(ct_begin + a.tiles_per_split, a.col_tiles), 0, 0);
+
+    for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
+    tc_setup<kEpiWarps>(S);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
+
+    if (warp < kEpiWarps) {
+        // thread = (row, column part): rows 32 (w % 4) + lane, part w / 4
+        const int row = (warp & 3) * 32 + lane;
+        const int part = warp >> 2;
+        float key[KP];
+        int idx[KP];
+#pragma unroll
+        for (int p = 0; p < KP; ++p) {
+            key[p] = INFINITY;
+            idx[p] = INT_MAX;
+        }
+        tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
+#pragma unroll 1
+            for (int cc = 0; cc < kCols / kParts / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tbase + cc * 32, v);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 nb =
+                        __ldg(reinterpret_cast<const float4 *>(a.ynorm + col0 + cc * 32 + j4 * 4));
+                    v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
+                    v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
+                    v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
+                    v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
+                }
+                // the batch's least t by a depth-5 tree, against the least
+                // published KP-th key of the row (stale values only loosen it)
+                float m16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
+#pragma unroll
+                for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+                float tau = key[KP - 1];
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) tau = fminf(tau, g_row_tau[q][row]);
+                if (m16[0] < tau) {
+                    // rare: gather this batch's candidates, then insert them
+                    // with the one copy of the sink
+                    float ct[32];
+                    int cj[32];
+                    int nc = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (v[j] < tau) {
+                            ct[nc] = v[j];
+                            cj[nc] = j;
+                            ++nc;
+                        }
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < nc; ++c)
+                        list_insert<KP>(key, idx, ct[c], col0 + cc * 32 + cj[c]);
+                    g_row_tau[part][row] = key[KP - 1];
+                }
+            }
+        });
+        // merge the row's lists: the ring is idle now, other parts park there
+        if (kParts > 1) {
+            float *pk = reinterpret_cast<float *>(base + 2 * (a.dk / kSlab) * kSlabTile);
+            int *pi = reinterpret_cast<int *>(pk + (kParts - 1) * kRows * KP);
+            epilogue_sync<kEpiWarps>();  // every MMA has been consumed
+            if (part > 0) {
+#pragma unroll
+                for (int p = 0; p < KP; ++p) {
+                    pk[((part - 1) * kRows + row) * KP + p] = key[p];
+                    pi[((part - 1) * kRows + row) * KP + p] = idx[p];
+                }
+            }
+            epilogue_sync<kEpiWarps>();
+            if (part == 0) {
+#pragma unroll 1
+                for (int q = 1; q < kParts; ++q)
+#pragma unroll 1
+                    for (int p = 0; p < KP; ++p)
+                        list_insert<KP>(key, idx, pk[((q - 1) * kRows + row) * KP + p],
+                                        pi[((q - 1) * kRows + row) * KP + p]);
+            }
+        }
+        if (part == 0 && !*(volatile int *)&S.abort && r0 + row < a.row_end) {
+            const int local = row_tile * kRows + row;
+            const int64_t o = (static_cast<int64_t>(split) * a.chunk_rows_pad + local) * KP;
+#pragma unroll
+            for (int p = 0; p < KP; ++p) {
+                a.part_key[o + p] = key[p];
+                a.part_idx[o + p] = idx[p];
+            }
+        }
+    }
+    tc_teardown<kEpiWarps>(S, a.status);
+}
+
+template <int KP>
+cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPipeSmem));
+    if (e != cudaSuccess) return e;
+    tc_knn_kernel<KP><<<dim3(row_tiles, splits), Epi<KP>::kThreads, kPipeSmem, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_knn_supported(int dk) { return (dk == 32 || dk == 64) && tensor_maps_available(); }
+
+cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
+                          int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
+                          cudaStream_t s) {
+    TcKnnParams P;
+    P.a = a;
+    if (!make_point_map(&P.maps.a_hi, a.Xp, x_rows, a.dk) ||
+        !make_point_map(&P.maps.a_lo, Xlo, x_rows, a.dk) ||
+        !make_point_map(&P.maps.b_hi, a.Yp, y_rows, a.dk) ||
+        !make_point_map(&P.maps.b_lo, Ylo, y_rows, a.dk))
+        return cudaErrorInvalidValue;
+    if (KP == 16) return tc_launch<16>(P, row_tiles, splits, s);
+    if (KP == 32) return tc_launch<32>(P, row_tiles, splits, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hdbmst

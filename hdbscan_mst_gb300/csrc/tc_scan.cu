@@ -1,0 +1,214 @@
+// K6 on the tensor cores: the Boruvka scan with tcgen05 TF32 MMAs.
+//
+// Same contract as mst_scan_kernel (page "HDBSCAN", gpu/hdbscan, "Exact
+// shortcuts": only the points the shortcuts leave are scanned against all
+// others, over a list of active points).  Rows are the active points and
+// columns all points, both grouped by component; a row tile whose rows share
+// one component skips the column tiles inside that component.  Per (row,
+// column) the epilogue forms t = |b|^2 - 2 a.b and ranks the pair by
+//     v = max(t, core_b^2 - |a|^2, core_a^2 - |a|^2)  ~  w(a, b)^2 - |a|^2
+// over columns of other components.  Each row is shared by E / 4 threads
+// (column parts); each keeps its 4 best (v, point) keys in registers and the
+// least v it dropped, and the parts of a row filter against the least of
+// their published 4th values.  At the end the parts merge into the row's 4
+// best and a threshold tau that every other column reaches or exceeds, which
+// mst_refine_kernel re-evaluates exactly and proves (this engine's rounding
+// bound) - the same output as the FFMA scan.
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tc_pipe.cuh"
+
+namespace hdbmst {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kKeep = 4;
+constexpr int kEpiWarps = 16;
+constexpr int kParts = kEpiWarps / 4;
+constexpr int kScanThreads = (kEpiWarps + 2) * 32;
+
+struct TcScanParams {
+    PipeMaps maps;  // A: active rows, B: grouped columns, point-major [rows][dk]
+    ScanArgs a;
+};
+
+__shared__ float s_row_thr[kParts][kRows];  // per part and row: its 4th kept v
+__shared__ int s_rcomp[kRows];
+
+__device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
+                                            float &dropped) {
+    if (key < k[kKeep - 1]) {
+        if (k[kKeep - 1] != kNoKey)
+            dropped = fminf(dropped, order_float(static_cast<unsigned>(k[kKeep - 1] >> 32)));
+        k[kKeep - 1] = key;
+#pragma unroll
+        for (int p = kKeep - 1; p > 0; --p) {
+            const unsigned long long lo = min(k[p - 1], k[p]), hi = max(k[p - 1], k[p]);
+            k[p - 1] = lo;
+            k[p] = hi;
+        }
+    } else {
+        dropped = fminf(dropped, order_float(static_cast<unsigned>(key >> 32)));
+    }
+}
+
+__device__ __forceinline__ float key_v(unsigned long long k) {
+    return k == kNoKey ? INFINITY : order_float(static_cast<unsigned>(k >> 32));
+}
+
+__global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_constant__ TcScanParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PipeSmem S;
+    const ScanArgs &a = P.a;
+    uint8_t *base = pipe_base(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * kRows;
+    const int split = blockIdx.y;
+    const int ct_begin = split * a.tiles_per_split;
+    const int ct_end = min(ct_begin + a.tiles_per_split, a.col_tiles);
+
+    for (int i = tid; i < kParts * kRows; i += blockDim.x) (&s_row_thr[0][0])[i] = INFINITY;
+    if (tid < kRows) s_rcomp[tid] = r0 + tid < a.na ? a.act_comp[r0 + tid] : -1;
+    tc_setup<kEpiWarps>(S);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    // rows all in one component: skip the column tiles wholly inside it
+    const bool uniform =
+        __syncthreads_and(tid >= kRows || r0 + tid >= a.na || s_rcomp[tid] == s_rcomp[0]);
+    int skip_lo = 0, skip_hi = 0;
+    if (uniform) {
+        const int C = s_rcomp[0];
+        const int c0 = a.comp_start[C], c1 = c0 + a.comp_size[C];
+        skip_lo = (c0 + kCols - 1) / kCols;
+        skip_hi = c1 / kCols;
+    }
+    const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
+    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
+
+    if (warp < kEpiWarps) {
+        const int row = (warp & 3) * 32 + lane;
+        const int part = warp >> 2;
+        const int r = r0 + row;
+        const bool valid = r < a.na;
+        const float na = valid ? a.act_norm[r] : 0.f;
+        const float ca = valid ? a.act_core[r] : 0.f;
+        const float ra = __fsub_rn(__fmul_rn(ca, ca), na);
+        const int rc = s_rcomp[row];
+        unsigned long long keys[kKeep];
+#pragma unroll
+        for (int p = 0; p < kKeep; ++p) keys[p] = kNoKey;
+        float dropped = INFINITY;
+
+        tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
+            float v[32];
+            tmem_ld32(tbase, v);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 nb = __ldg(reinterpret_cast<const float4 *>(a.col_norm + col0 + j4 * 4));
+                v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
+                v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
+                v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
+                v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
+            }
+            float m16[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
+#pragma unroll
+            for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+            // v >= t, so a batch whose least t does not beat the row's least
+            // published 4th value cannot change any part's 4 best
+            float thr = key_v(keys[kKeep - 1]);
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) thr = fminf(thr, s_row_thr[q][row]);
+            if (m16[0] < thr) {
+                float ct[32];
+                int cj[32];
+                int nc = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (v[j] < thr) {
+                        ct[nc] = v[j];
+                        cj[nc] = j;
+                        ++nc;
+                    }
+                }
+#pragma unroll 1
+                for (int c = 0; c < nc; ++c) {
+                    const int col = col0 + cj[c];
+                    if (col >= a.n || __ldg(a.col_comp + col) == rc) continue;
+                    const float cb = __ldg(a.col_core + col);
+                    const float vv = fmaxf(fmaxf(ct[c], __fsub_rn(__fmul_rn(cb, cb), na)), ra);
+                    const unsigned long long key =
+                        (static_cast<unsigned long long>(float_order(vv)) << 32) |
+                        static_cast<unsigned>(__ldg(a.col_orig + col));
+                    keep_insert(keys, key, dropped);
+                }
+                s_row_thr[part][row] = key_v(keys[kKeep - 1]);
+            }
+        });
+
+        // Merge the parts of each row in the idle ring: tau bounds every
+        // column not kept - dropped ones directly, filtered ones by the 4th
+        // kept value of the part that filtered them.
+        unsigned long long *pk =
+            reinterpret_cast<unsigned long long *>(base + 2 * (a.dk / kSlab) * kSlabTile);
+        float *pt = reinterpret_cast<float *>(pk + (kParts - 1) * kRows * kKeep);
+        float tau = fminf(dropped, key_v(keys[kKeep - 1]));
+        epilogue_sync<kEpiWarps>();
+        if (part > 0) {
+#pragma unroll
+            for (int p = 0; p < kKeep; ++p) pk[((part - 1) * kRows + row) * kKeep + p] = keys[p];
+            pt[(part - 1) * kRows + row] = tau;
+        }
+        epilogue_sync<kEpiWarps>();
+        if (part == 0) {
+#pragma unroll 1
+            for (int q = 1; q < kParts; ++q) {
+                tau = fminf(tau, pt[(q - 1) * kRows + row]);
+#pragma unroll 1
+                for (int p = 0; p < kKeep; ++p) {
+                    const unsigned long long k = pk[((q - 1) * kRows + row) * kKeep + p];
+                    if (k != kNoKey) keep_insert(keys, k, tau);
+                }
+            }
+            if (valid && !*(volatile int *)&S.abort) {
+                const int64_t o = static_cast<int64_t>(split) * a.lda + r;
+#pragma unroll
+                for (int p = 0; p < kKeep; ++p) a.part_key[o * kKeep + p] = keys[p];
+                a.part_tau[o] = tau;
+            }
+        }
+    }
+    tc_teardown<kEpiWarps>(S, a.status);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *Xa_lo,
+                           const float *Xs_hi, const float *Xs_lo, int row_tiles, int splits,
+                           cudaStream_t s) {
+    TcScanParams P;
+    P.a = a;
+    if (!make_point_map(&P.maps.a_hi, Xa_hi, a.lda, a.dk) ||
+        !make_point_map(&P.maps.a_lo, Xa_lo, a.lda, a.dk) ||
+        !make_point_map(&P.maps.b_hi, Xs_hi, a.ldx, a.dk) ||
+        !make_point_map(&P.maps.b_lo, Xs_lo, a.ldx, a.dk))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPipeSmem));
+    if (e != cudaSuccess) return e;
+    tc_scan_kernel<<<dim3(row_tiles, splits), kScanThreads, kPipeSmem, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace hdbmst

@@ -90,13 +90,5 @@ __device__ __forceinline__ void tile_pipeline(TileBuffers &T, const float *__res
     }
 }
 
-// Order-preserving map of any float (negative ones included) to unsigned.
-__device__ __forceinline__ unsigned float_order(float v) {
-    const unsigned b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float order_float(unsigned o) {
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
 
 }  // namespace hdbmst

@@ -174,9 +174,11 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
  *    results: serialise them.  The array keeps the last call's contents; the
  *    call clears what must start at zero itself.
  *  - Problems that need more scratch than the array holds return
- *    HDBMST_ERR_TOO_LARGE before any GPU work.  The need is about
- *    8 * round_up(d, 16) * (round_up(n, 128) + round_up(m, 128)) bytes for the
- *    packed copies (half that when Y is X), plus 4 bytes per query and at
+ *    HDBMST_ERR_TOO_LARGE before any GPU work.  With dk the padded feature
+ *    count (round_up(d, 32) up to 64, round_up(d, 16) beyond), the need is
+ *    about c * dk * (round_up(n, 128) + round_up(m, 128)) bytes for the packed
+ *    copies, c = 12 when d <= 64 (the tensor-core engine's extra low parts)
+ *    and 8 otherwise (half that when Y is X), plus 4 bytes per query and at
  *    least 64 KiB for the neighbour candidates (128 KiB when k > 12).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine; it
  *    synchronises the stream once at the end, as hdbmst_knn does.
@@ -187,6 +189,24 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
 hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const float *Y,
                                  int64_t ldy, int64_t m, int d, int k, int32_t *out_idx,
                                  float *out_dist, hdbmst_stream stream);
+
+/*
+ * Distance-tile engine for the k-NN search (hdbmst_knn, hdbmst_knn_noalloc,
+ * hdbmst_core_distances), process-wide, not thread-safe:
+ *   HDBMST_ENGINE_AUTO   tensor cores where supported (d <= 64), else FP32
+ *                        FFMA (the default);
+ *   HDBMST_ENGINE_SIMT   FP32 FFMA register-blocked tile everywhere;
+ *   HDBMST_ENGINE_TENSOR same as AUTO (tensor cores need d <= 64).
+ * The tensor-core tile ranks candidates with three-pass TF32 products
+ * (tcgen05); both engines report distances re-evaluated exactly with dist()
+ * and prove the kept set against their own rounding bound, so results are
+ * identical bit for bit whichever engine ran.  Returns the previous setting;
+ * unknown values are ignored.
+ */
+#define HDBMST_ENGINE_AUTO 0
+#define HDBMST_ENGINE_SIMT 1
+#define HDBMST_ENGINE_TENSOR 2
+int hdbmst_set_engine(int engine);
 
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);

@@ -1,0 +1,65 @@
+"""The tensor-core and FP32 FFMA distance tiles give bit-identical results:
+both only rank candidates, every reported value is re-evaluated with the
+exact distance, and each engine proves its kept set against its own rounding
+bound.  Also checks the tensor-core engine against the oracle directly."""
+
+import numpy as np
+import pytest
+
+import oracle_pins
+import workloads
+from gpu_common import H, dev, np_, oracle_knn_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def h():
+    mod = H()
+    prev = mod.set_engine("auto")
+    yield mod
+    mod.set_engine(prev)
+
+
+def both(h, fn):
+    h.set_engine("simt")
+    a = fn()
+    h.set_engine("tensor")
+    b = fn()
+    h.set_engine("auto")
+    return a, b
+
+
+@pytest.mark.parametrize("n,m,d,k", [(1, 1, 1, 1), (5, 7, 3, 4), (129, 300, 17, 10),
+                                     (1000, 1000, 61, 11), (777, 2049, 64, 16),
+                                     (300, 130, 33, 32), (2000, 1500, 48, 12)])
+def test_knn_engines_identical(h, n, m, d, k):
+    X = workloads.small(n, d, seed=n + 3 * d, dup_frac=0.05)
+    Y = workloads.small(m, d, seed=m + 5 * d, dup_frac=0.05)
+    (ai, ad), (bi, bd) = both(h, lambda: tuple(np_(t) for t in h.knn(dev(X), dev(Y), k)))
+    assert np.array_equal(ai, bi) and np.array_equal(ad, bd)
+    oracle_knn_check(X, Y, k, bi, bd, where=f"tensor n={n} m={m} d={d}")
+
+
+def test_core_engines_identical_2k(h):
+    X, task = workloads.workload("hdbscan_2k_d61")
+    ms = task["min_samples"]
+    a, b = both(h, lambda: tuple(np_(t) for t in h.core_distances(dev(X), ms)))
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_knn_engines_integer_ties(h):
+    rng = np.random.default_rng(3)
+    X = oracle_pins.int_points(rng, 700, 5, span=3)
+    (ai, ad), (bi, bd) = both(h, lambda: tuple(np_(t) for t in h.knn(dev(X), dev(X), 20)))
+    assert np.array_equal(ai, bi) and np.array_equal(ad, bd)
+
+
+def test_core_engines_identical_200k_sampled_rows(h):
+    """The benchmark's workload: both engines, every row identical."""
+    X, task = workloads.workload("hdbscan_200k_d61")
+    ms = task["min_samples"]
+    a, b = both(h, lambda: tuple(np_(t) for t in h.core_distances(dev(X), ms)))
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
