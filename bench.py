@@ -51,6 +51,9 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # FP32 FFMA: 128 lanes per SM, 2 flops per lane per clock
 FP32_LANES_PER_SM = 128
+# nominal dense tensor rates: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s
+TF32_PER_BF16 = 1.1 / 2.25
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -252,22 +255,39 @@ def run_gpu(args):
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     max_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12  # TFLOP/s
+    bf16 = peaks.get("bf16_tflops")
+    tf32_peak = bf16 * TF32_PER_BF16 if bf16 else FALLBACK_BF16_TFLOPS * TF32_PER_BF16
+    tf32_basis = ("measured bf16 burst x nominal tf32/bf16 (1.1/2.25)" if bf16 else
+                  "fallback bf16 x nominal tf32/bf16 (1.1/2.25)")
 
-    def roofline(prof_, name, flops_per_launch):
+    def roofline(prof_, name, d_, pairs, tensor):
+        """Dominant distance tile: algorithmic flops 2 d per pair over its launches."""
         if name not in prof_:
             return None
         tot_ms, nl = prof_[name]
         avg_s = tot_ms / nl / 1e3
-        ach = flops_per_launch / avg_s / 1e12
-        return {"kernel": name, "bound": "alu", "achieved": round(ach, 2),
+        flops = 2.0 * d_ * pairs
+        ach = flops / avg_s / 1e12
+        if tensor:
+            dk = 32 if d_ <= 32 else 64
+            issued = 3 * 2.0 * dk * pairs / avg_s / 1e12  # three TF32 passes on padded features
+            return {"kernel": name, "engine": "tcgen05 3xTF32", "bound": "tensor",
+                    "achieved": round(ach, 2), "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / tf32_peak, 4), "traffic": None,
+                    "peak_basis": tf32_basis, "avg_launch_ms": round(avg_s * 1e3, 3),
+                    "flops_per_launch": flops, "issued_tflops": round(issued, 1),
+                    "issued_frac": round(issued / tf32_peak, 4),
+                    "fp32_alu_equiv_frac": round(ach / fp32_peak, 4)}
+        return {"kernel": name, "engine": "FP32 FFMA", "bound": "alu", "achieved": round(ach, 2),
                 "peak": round(fp32_peak, 2), "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
                 "traffic": None, "avg_launch_ms": round(avg_s * 1e3, 3),
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz",
-                "flops_per_launch": flops_per_launch}
+                "flops_per_launch": flops}
 
-    # core distances: every clip against every clip, 2 d flops per pair (one launch)
-    main_roof = roofline(prof, "knn_tile", 2.0 * d * n * n)
-    knn_roof = roofline(kprof, "knn_tile", 2.0 * Xk.shape[0] * Xk.shape[1] * Yk.shape[1])
+    # core distances: every clip against every clip (one launch)
+    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 64)
+    knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], float(Xk.shape[1]) * Yk.shape[1],
+                        Xk.shape[0] <= 64)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
                  for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
     line = {

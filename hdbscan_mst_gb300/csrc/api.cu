@@ -644,6 +644,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.fb_count = &b.st->fb_count;
             sa.fb_rows = b.fb_rows;
             sa.status = &b.st->status;
+            sa.err_coef = tensor ? tc::err_coef(d, p.dk) : (2.0 * d + 10.0) * 0x1p-24 * 1.01;
             CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
             if (tensor) {
                 LAUNCH(K_SCAN, s, launch_tc_scan(sa, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo, row_tiles,

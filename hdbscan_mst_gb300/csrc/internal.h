@@ -57,7 +57,7 @@ struct KnnRefineArgs {
     const float *Xp, *Yp;  // point-major [.][dk]
     const float *xnorm;
     const unsigned *nbmax_bits;
-    double err_coef;  // E = err_coef (|x|^2 + max |y|^2) bounds the ranking error
+    double err_coef;  // the engine's ranking error is at most err_coef (|x|^2 + |y|^2)
     int d, dk, k, m;
     int core_rank;  // 1-based list position copied to out_core (0: none)
     int32_t *out_idx;
@@ -145,6 +145,7 @@ struct ScanArgs {
     int *fb_count;
     int *fb_rows;
     unsigned *status;              // device status word (tensor-core timeouts)
+    double err_coef;               // ranking error bound of the engine that ran
 };
 size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);

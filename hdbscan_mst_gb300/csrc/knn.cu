@@ -322,22 +322,23 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     if (a.out_core && gl == a.core_rank - 1) a.out_core[row] = key_w(key);
 
     // 4. Proof that the kept set holds the exact top k.  Every dropped column
-    //    z has t_z >= A.  The expansion t + |x|^2 differs from the true squared
-    //    distance by at most E = err_coef (|x|^2 + max|y|^2) (for the FFMA tile
-    //    err_coef = (2d + 10) u with u = 2^-24: dot product and norms are FMA
-    //    chains of length d, plus a few roundings, with slack; the tensor-core
-    //    tile has its own, larger coefficient), and the exact float32 evaluation is at least
-    //    (1 - (d + 3) u) times the true value.  If that lower bound still
-    //    exceeds the k-th kept distance squared (with sqrt rounding slack),
-    //    no dropped column can rank in the top k.
+    //    z has computed t_z >= A (A = the KP-th kept t).  The ranking error of
+    //    t is at most err_coef (|x|^2 + |z|^2), so z's true squared distance is
+    //    at least |x|^2 + A - err_coef (|x|^2 + |z|^2); by Cauchy-Schwarz it is
+    //    also at least (|z| - |x|)^2.  With T = dist_k^2 M (M covers the exact
+    //    float32 evaluation, (1 - (d + 3) u), and strict sqrt ordering,
+    //    16 u), every z with |z|^2 >= nb_c = (|x| + sqrt(T))^2 is beyond T by
+    //    the second bound, and every other z by the first as soon as
+    //    |x|^2 + A - err_coef (|x|^2 + nb_c) > T.  Then no dropped column can
+    //    rank in the top k.  The bound needs no maximum over all columns.
     if (gl == a.k - 1 && A < INFINITY) {
         const double u = 5.9604644775390625e-8;
         const double dk = key_w(key);
         const double na = a.xnorm[row];
-        const double nb = __uint_as_float(*a.nbmax_bits);
-        const double E = a.err_coef * (na + nb);
-        const double lb = (static_cast<double>(A) + na - E) * (1.0 - (a.d + 3.0) * u);
-        if (!(lb * (1.0 - 4.0 * u) > dk * dk)) {
+        const double T = dk * dk * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
+        const double sq = sqrt(na) + sqrt(T);
+        const double nbc = sq * sq;
+        if (!(static_cast<double>(A) + na - a.err_coef * (na + nbc) > T)) {
             const int pos = atomicAdd(a.fb_count, 1);
             a.fb_rows[pos] = row;
         }

@@ -191,17 +191,26 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
         tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, o));
     }
     if (lane != 0) return;
+    // Proof (lane 0).  A dropped point z has v_z >= tau with
+    // v = max(t, core_b^2 - |a|^2, core_a^2 - |a|^2).  If core_a^2 - |a|^2 <
+    // tau, either core_z^2 - |a|^2 >= tau or t_z >= tau.  With T = w^2 M (w
+    // the best exact weight; M covers the exact float32 evaluation,
+    // (1 - (d + 3) u), and strict sqrt ordering, 16 u), the first gives
+    // core_z > w; for the second the true squared distance is at least
+    // |a|^2 + tau - err_coef (|a|^2 + |z|^2) and, by Cauchy-Schwarz, at least
+    // (|z| - |a|)^2, so every z exceeds T once
+    // |a|^2 + tau - err_coef (|a|^2 + nb_c) > T with nb_c = (|a| + sqrt(T))^2.
     bool proven = false;
     if (exact != kNoKey) {
         const double u = 5.9604644775390625e-8;
         const float na = a.act_norm[r];
         const float ra = __fsub_rn(__fmul_rn(ca, ca), na);
-        const double nbmax = __uint_as_float(*a.nbmax_bits);
-        const double E = (2.0 * a.d + 10.0) * u * 1.01 * (static_cast<double>(na) + nbmax);
-        const double lb = (static_cast<double>(tau) + na - E) * (1.0 - (a.d + 3.0) * u) *
-                          (1.0 - u) * (1.0 - u);
         const double bw = key_w(exact);
-        proven = (ra < tau) && (lb * (1.0 - 4.0 * u) > bw * bw);
+        const double T = bw * bw * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
+        const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
+        const double nbc = sq * sq;
+        proven = (ra < tau) &&
+                 (static_cast<double>(tau) + na - a.err_coef * (na + nbc) > T);
         atomicMin(&a.cand[g], exact);
     } else {
         proven = !(tau < INFINITY);  // nothing kept and nothing dropped: no other component
