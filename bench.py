@@ -10,6 +10,11 @@ core distances and the tree inside the timed region).  A secondary line item
 times exact k-NN on the 200 000 x 192 workload against its 20 000-point
 subset (rows per second).
 
+The K timed steps run without instrumentation; the same K steps then run
+again with a CUDA event pair around every kernel launch, which gives the
+per-kernel breakdown and the roofline of the distance tile
+(``profiled_ms_per_step`` is that second pass's step time).
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 ``--impl reference`` times the float64 CPU oracle instead (a bounded sample of
@@ -179,27 +184,37 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize(device)
 
-    # ---- timed region: data resident, L2 flushed between steps (outside the events)
-    H.profile_enable(True)
-    H.profile_read()
-    launches0 = H.launch_count()
-    times = []
-    barrier(dist, device)
-    torch.cuda.synchronize(device)
-    with ClockSampler(local) as clk:
+    def timed(fn):
+        """K steps with CUDA events on the launching stream around each; L2
+        flushed before each step, outside the events."""
+        out = []
         for _ in range(args.steps):
             flush_l2(flush)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step()
+            fn()
             e1.record(stream)
             e1.synchronize()
-            times.append(e0.elapsed_time(e1))
+            out.append(e0.elapsed_time(e1))
+        return out
+
+    # ---- timed region: data resident, no instrumentation
+    launches0 = H.launch_count()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        times = timed(step)
         torch.cuda.synchronize(device)
     barrier(dist, device)
     launches = H.launch_count() - launches0
     rounds = H.last_mst_rounds()
+
+    # ---- the same K steps again with an event pair around every kernel
+    # launch: per-kernel times for the breakdown and the roofline
+    H.profile_enable(True)
+    H.profile_read()
+    prof_times = timed(step)
     prof = H.profile_read()
     H.profile_enable(False)
     clocks = clk.summary()
@@ -230,18 +245,10 @@ def run_gpu(args):
         flush_l2(flush)
         H.knn(Xkd, Ykd, tk["k"])
     torch.cuda.synchronize(device)
+    kt = timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
     H.profile_enable(True)
     H.profile_read()
-    kt = []
-    for _ in range(args.steps):
-        flush_l2(flush)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        H.knn(Xkd, Ykd, tk["k"])
-        e1.record(stream)
-        e1.synchronize()
-        kt.append(e0.elapsed_time(e1))
+    timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
     kprof = H.profile_read()
     H.profile_enable(False)
     k_total = max_over_ranks(dist, sum(kt), device)
@@ -309,6 +316,7 @@ def run_gpu(args):
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": main_roof,
         "kernel_ms_per_step": breakdown,
+        "profiled_ms_per_step": round(sum(prof_times) / args.steps, 3),
         "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e,
                             "exact_rows": x} for a, e, x in rounds],
         "gpu_launches": launches,

@@ -35,13 +35,15 @@ OP_KNN, OP_CORE, OP_MST = 0, 1, 2
 STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
     4: "non-finite value", 5: "Boruvka made no progress", 6: "CUDA error",
+    7: "too large for the fixed scratch", 8: "a wait inside a kernel gave up",
 }
 
 
 class HdbmstError(RuntimeError):
-    def __init__(self, status: int, what: str):
+    def __init__(self, status: int, what: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{what}: {STATUS.get(status, status)} ({status})")
+        msg = f"{what}: {STATUS.get(status, status)} ({status})"
+        super().__init__(msg + (f" [{detail}]" if detail else ""))
 
 
 class HdbmstUnavailable(ImportError):
@@ -91,6 +93,7 @@ def _load():
     L.hdbmst_last_mst_rounds.restype = i32
     L.hdbmst_set_engine.argtypes = [i32]
     L.hdbmst_set_engine.restype = i32
+    L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
     _lib = L
     return L
 
@@ -102,7 +105,8 @@ def lib():
 
 def _check(status: int, what: str):
     if status != 0:
-        raise HdbmstError(status, what)
+        detail = _lib.hdbmst_last_cuda_error().decode() if status == 6 and _lib else ""
+        raise HdbmstError(status, what, detail)
 
 
 # ---------------------------------------------------------------- marshalling

@@ -27,11 +27,13 @@ constexpr int kRows = 128;        // rows of a tile = TMEM lanes
 constexpr int kCols = 128;        // columns of a tile (MMA N)
 constexpr int kSlab = 32;         // features per swizzled slab
 constexpr int kSlabBytes = 128;   // bytes per row per slab
-// Every mbarrier wait polls at most kWaitPolls times; each poll may suspend the
-// thread for up to kSuspendNs (it wakes as soon as the phase completes), so a
-// wait gives up after about kWaitPolls * kSuspendNs = 1.6 s.
-constexpr uint32_t kWaitPolls = 1u << 14;
-constexpr uint32_t kSuspendNs = 100000;
+// Every mbarrier wait gives up after kWaitNs of global time (read from
+// %globaltimer) or kWaitPolls polls, whichever comes first; between polls the
+// waiting thread sleeps (__nanosleep), so it leaves the issue slots to the
+// warps doing work.  The poll cap alone ends a wait even if the timer stood
+// still: every poll takes at least tens of cycles.
+constexpr uint64_t kWaitNs = 1500000000ull;  // 1.5 s
+constexpr uint32_t kWaitPolls = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -78,22 +80,43 @@ __device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(count));
 }
 
-// Wait for the given phase parity; returns false if the wait gave up (the
-// caller records an error and winds down).  The thread sleeps inside each
-// poll instead of spinning, so waiting lanes leave the issue slots to the
-// epilogue warps.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
-    uint32_t done = 0;
-    for (uint32_t it = 0; it < kWaitPolls && !done; ++it) {
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(smem_u32(mbar)), "r"(parity), "r"(kSuspendNs)
-            : "memory");
-    }
+__device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
     return done != 0;
 }
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the given phase parity; returns false if the wait gave up (the
+// caller records an error and winds down).  After a failed test the thread
+// sleeps 16 ns, doubling up to kMaxSleepNs, between tests: a role on the
+// critical path (the MMA issuer) takes a short cap, the others longer ones.
+template <uint32_t kMaxSleepNs>
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
+    if (mbar_test(mbar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t sleep = 16;
+    for (uint32_t it = 1; it < kWaitPolls; ++it) {
+        __nanosleep(sleep);
+        if (mbar_test(mbar, parity)) return true;
+        sleep = min(2 * sleep, kMaxSleepNs);
+        if ((it & 15) == 0 && global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
+// Sleep caps of the pipeline roles.
+constexpr uint32_t kSleepMma = 64, kSleepProducer = 256, kSleepEpilogue = 128;
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -166,6 +189,28 @@ __device__ __forceinline__ float4 tf32_lo(float4 x) {
     l.z = __fsub_rn(x.z, __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u));
     l.w = __fsub_rn(x.w, __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
     return l;
+}
+
+// v[j] for a run-time j in 0 .. 31 by a tree of selects on the bits of j, so
+// that v stays in registers (an indexed load would move it to local memory).
+__device__ __forceinline__ float pick32(const float (&v)[32], int j) {
+    float a[16], b[8], c[4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (j & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = (j & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[2 * i + 1] : b[2 * i];
+    const float d0 = (j & 8) ? c[1] : c[0], d1 = (j & 8) ? c[3] : c[2];
+    return (j & 16) ? d1 : d0;
+}
+
+// Bit j set where v[j] < thr.
+__device__ __forceinline__ uint32_t below_mask(const float (&v)[32], float thr) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) m |= (v[j] < thr ? 1u : 0u) << j;
+    return m;
 }
 
 // Bound on |computed t - (|y|^2 - 2 x.y)| relative to |x|^2 + |y|^2 for the

@@ -15,17 +15,17 @@
 //    (32 features, hi and lo) through a 4-stage ring guarded by full/empty
 //    mbarriers;
 //  * the MMA warp (one lane) issues per slab 3 x 4 TF32 MMAs
-//    (hi.hi + hi.lo + lo.hi) into one of two TMEM accumulators, frees each
+//    (hi.hi + hi.lo + lo.hi) into one of four TMEM accumulators, frees each
 //    ring stage with tcgen05.commit, and signals the accumulator when a tile
 //    is complete;
-//  * epilogue warp w reads TMEM lanes 32 (w % 4) .. (its 32 rows) and the
-//    column quarter (or half) w / 4 of each tile: each row is shared by E / 4
-//    threads, each keeping the best KP of its columns in registers with the
-//    fixed compare-and-swap sink (page "HDBSCAN", "The hang").  The threads
-//    of a row publish their KP-th key in shared memory and filter against the
-//    least of them (a candidate that cannot beat it cannot reach the row's top
-//    KP), so the row's insertions stay those of one list.  At the end the
-//    lists of a row are merged.
+//  * the epilogue warps form E / 4 groups; group g takes every (E / 4)-th
+//    tile whole, and warp w of it reads TMEM lanes 32 (w % 4) .. (its 32
+//    rows), 32 columns at a time.  Each row thus has one list per group, kept
+//    in registers by the fixed compare-and-swap sink (page "HDBSCAN", "The
+//    hang").  The groups publish each row's KP-th key in shared memory and
+//    filter against the least of them (a candidate that cannot beat it cannot
+//    reach the row's top KP), so the row's insertions stay close to those of
+//    one list.  At the end the lists of a row are merged.
 // Every wait is bounded; a wait that gives up flags the status word, stops
 // every role, drains what it issued, and the CTA frees its TMEM.
 #include <climits>
@@ -50,11 +50,11 @@ struct TcKnnParams {
 template <int KP>
 struct Epi {
     static constexpr int kWarps = KP == 16 ? 16 : 8;   // epilogue warps
-    static constexpr int kParts = kWarps / 4;          // threads per row
+    static constexpr int kParts = kWarps / 4;          // groups: lists per row
     static constexpr int kThreads = (kWarps + 2) * 32; // + producer + MMA warp
 };
 
-__shared__ float g_row_tau[4][kRows];  // per column part and row: that thread's KP-th key
+__shared__ float g_row_tau[4][kRows];  // per group and row: that list's KP-th key
 
 template <int KP>
 __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float t, int j) {
@@ -97,9 +97,9 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
     tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
 
     if (warp < kEpiWarps) {
-        // thread = (row, column part): rows 32 (w % 4) + lane, part w / 4
+        // thread = (row, group): rows 32 (w % 4) + lane, group w / 4
         const int row = (warp & 3) * 32 + lane;
-        const int part = warp >> 2;
+        const int group = warp >> 2;
         float key[KP];
         int idx[KP];
 #pragma unroll
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
         }
         tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
 #pragma unroll 1
-            for (int cc = 0; cc < kCols / kParts / 32; ++cc) {
+            for (int cc = 0; cc < kCols / 32; ++cc) {
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
 #pragma unroll
@@ -134,40 +134,33 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kParts; ++q) tau = fminf(tau, g_row_tau[q][row]);
                 if (m16[0] < tau) {
-                    // rare: gather this batch's candidates, then insert them
+                    // rare: insert this batch's candidates in column order
                     // with the one copy of the sink
-                    float ct[32];
-                    int cj[32];
-                    int nc = 0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (v[j] < tau) {
-                            ct[nc] = v[j];
-                            cj[nc] = j;
-                            ++nc;
-                        }
-                    }
+                    uint32_t mask = below_mask(v, tau);
 #pragma unroll 1
-                    for (int c = 0; c < nc; ++c)
-                        list_insert<KP>(key, idx, ct[c], col0 + cc * 32 + cj[c]);
-                    g_row_tau[part][row] = key[KP - 1];
+                    while (mask) {
+                        const int j = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        list_insert<KP>(key, idx, pick32(v, j), col0 + cc * 32 + j);
+                    }
+                    g_row_tau[group][row] = key[KP - 1];
                 }
             }
         });
-        // merge the row's lists: the ring is idle now, other parts park there
+        // merge the row's lists: the ring is idle now, other groups park there
         if (kParts > 1) {
             float *pk = reinterpret_cast<float *>(base + 2 * (a.dk / kSlab) * kSlabTile);
             int *pi = reinterpret_cast<int *>(pk + (kParts - 1) * kRows * KP);
             epilogue_sync<kEpiWarps>();  // every MMA has been consumed
-            if (part > 0) {
+            if (group > 0) {
 #pragma unroll
                 for (int p = 0; p < KP; ++p) {
-                    pk[((part - 1) * kRows + row) * KP + p] = key[p];
-                    pi[((part - 1) * kRows + row) * KP + p] = idx[p];
+                    pk[((group - 1) * kRows + row) * KP + p] = key[p];
+                    pi[((group - 1) * kRows + row) * KP + p] = idx[p];
                 }
             }
             epilogue_sync<kEpiWarps>();
-            if (part == 0) {
+            if (group == 0) {
 #pragma unroll 1
                 for (int q = 1; q < kParts; ++q)
 #pragma unroll 1
@@ -176,7 +169,7 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
                                         pi[((q - 1) * kRows + row) * KP + p]);
             }
         }
-        if (part == 0 && !*(volatile int *)&S.abort && r0 + row < a.row_end) {
+        if (group == 0 && !*(volatile int *)&S.abort && r0 + row < a.row_end) {
             const int local = row_tile * kRows + row;
             const int64_t o = (static_cast<int64_t>(split) * a.chunk_rows_pad + local) * KP;
 #pragma unroll

@@ -10,9 +10,13 @@
 // Roles: warps 0 .. E-1 are the caller's epilogue, warp E the TMA producer
 // (one lane), warp E+1 the MMA issuer (one lane, also owns the TMEM
 // allocation).  Stages: a 4-deep ring of 32-feature slabs (full/empty
-// mbarriers) and two 128-column TMEM accumulators (afull/aempty).  Every
-// wait is bounded; the first that gives up sets S.abort, every role winds
-// down, and tc_teardown drains and frees TMEM.
+// mbarriers) and four 128-column TMEM accumulators (afull/aempty), all 512
+// columns of TMEM.  The epilogue warps form E / 4 groups of four (one warp per
+// 32-lane TMEM quadrant); group g takes the tiles t with t % (E / 4) = g,
+// whole, so each warp has E / 4 tile periods for one tile and the latency of
+// its chain (TMEM load, norms, selection) hides behind the other groups' work.
+// Every wait is bounded; the first that gives up sets S.abort, every role
+// winds down, and tc_teardown drains and frees TMEM.
 #pragma once
 
 #include <cuda.h>
@@ -24,6 +28,7 @@ namespace hdbmst {
 namespace tc {
 
 constexpr int kStages = 4;
+constexpr int kAcc = 4;  // TMEM accumulators of kCols columns
 constexpr uint32_t kSlabTile = kRows * kSlabBytes;  // 16 KB: one slab of 128 rows
 // dynamic shared memory: resident rows (hi + lo, up to 2 slabs) + the ring
 constexpr size_t kPipeSmem = (2 * 2 + 2 * kStages) * kSlabTile + 1024;
@@ -33,7 +38,7 @@ struct PipeMaps {
 };
 
 struct PipeSmem {
-    uint64_t full[kStages], empty[kStages], afull[2], aempty[2], abar;
+    uint64_t full[kStages], empty[kStages], afull[kAcc], aempty[kAcc], abar;
     uint32_t tmem_base;
     int abort;
 };
@@ -68,15 +73,16 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(&S.afull[i], 1);
-            mbar_init(&S.aempty[i], kEpiWarps * 32);
+            mbar_init(&S.aempty[i], 4 * 32);  // the four warps of one group
         }
         mbar_init(&S.abar, 1);
         S.abort = 0;
         fence_mbar_init();
     }
-    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, 2 * kCols);
+    static_assert(kAcc % (kEpiWarps / 4) == 0, "each accumulator belongs to one group");
+    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kAcc * kCols);
 }
 
 // Producer and MMA roles (warps E and E+1); epilogue warps return at once.
@@ -101,7 +107,8 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
             for (int s = 0; s < slabs; ++s, ++it) {
                 const int st = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait(&S.empty[st], ph ^ 1) || *(volatile int *)&S.abort) {
+                if (!mbar_wait<kSleepProducer>(&S.empty[st], ph ^ 1) ||
+                    *(volatile int *)&S.abort) {
                     S.abort = 1;
                     return;
                 }
@@ -114,17 +121,18 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
     } else if (warp == kEpiWarps + 1 && lane == 0) {
         const uint32_t idesc = instr_desc(kRows, kCols);
         const uint32_t tmem = S.tmem_base;
-        bool ok = mbar_wait(&S.abar, 0);
+        bool ok = mbar_wait<kSleepMma>(&S.abar, 0);
         int it = 0;
         for (int t = 0; t < seq.n && ok; ++t) {
-            const int acc = t & 1;
-            ok = mbar_wait(&S.aempty[acc], ((t >> 1) & 1) ^ 1) && !*(volatile int *)&S.abort;
+            const int acc = t % kAcc;
+            ok = mbar_wait<kSleepMma>(&S.aempty[acc], ((t / kAcc) & 1) ^ 1) &&
+                 !*(volatile int *)&S.abort;
             if (!ok) break;
             fence_after();
             const uint32_t d = tmem + static_cast<uint32_t>(acc * kCols);
             for (int s = 0; s < slabs; ++s, ++it) {
                 const int st = it % kStages;
-                ok = mbar_wait(&S.full[st], (it / kStages) & 1);
+                ok = mbar_wait<kSleepMma>(&S.full[st], (it / kStages) & 1);
                 if (!ok) break;
                 fence_after();
                 const uint32_t hi = ring + st * 2 * kSlabTile;
@@ -147,29 +155,27 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
     }
 }
 
-// Epilogue loop of warp w < E: for every tile k of seq, waits for its
-// accumulator and calls consume(tmem_addr, col0) with the TMEM address of this
-// thread's lane at the column part's first column and the global column of
-// that part's first column; then hands the accumulator back.  Column part of
-// warp w: w / 4 of kParts = E / 4 parts; lanes 32 (w % 4) ...
+// Epilogue loop of warp w < E (group w / 4, TMEM lanes 32 (w % 4) ..): for
+// every tile of its group, waits for the tile's accumulator and calls
+// consume(tmem_addr, col0) with the TMEM address of this thread's lane at the
+// tile's first column and the tile's first global column; then hands the
+// accumulator back.
 template <int kEpiWarps, class Consume>
 __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq,
                                                  Consume &&consume) {
-    constexpr int kParts = kEpiWarps / 4;
-    constexpr int kPartCols = kCols / kParts;
+    constexpr int kGroups = kEpiWarps / 4;
     const int warp = threadIdx.x >> 5;
-    const int part = warp >> 2;
+    const int group = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tmem = S.tmem_base;
-    for (int t = 0; t < seq.n; ++t) {
-        const int acc = t & 1;
-        const bool w = mbar_wait(&S.afull[acc], (t >> 1) & 1);
+    for (int t = group; t < seq.n; t += kGroups) {
+        const int acc = t % kAcc;
+        const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], (t / kAcc) & 1);
         if (!w) S.abort = 1;
         // a warp leaves together: tcgen05.ld is warp-collective
         if (__any_sync(0xffffffffu, !w || *(volatile int *)&S.abort)) break;
         fence_after();
-        consume(tmem + static_cast<uint32_t>(acc * kCols + part * kPartCols) + lane_base,
-                seq.at(t) * kCols + part * kPartCols);
+        consume(tmem + static_cast<uint32_t>(acc * kCols) + lane_base, seq.at(t) * kCols);
         fence_before();
         mbar_arrive(&S.aempty[acc]);
     }
@@ -185,13 +191,13 @@ __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
     if (S.abort) {
         if (tid == 0) {
             atomicOr(status, kStatusTimeout);
-            for (int i = 0; i < 2; ++i) mbar_wait(&S.afull[i], 0);
-            for (int i = 0; i < kStages; ++i) mbar_wait(&S.full[i], 0);
+            for (int i = 0; i < kAcc; ++i) mbar_wait<kSleepProducer>(&S.afull[i], 0);
+            for (int i = 0; i < kStages; ++i) mbar_wait<kSleepProducer>(&S.full[i], 0);
         }
         __syncthreads();
     }
     fence_after();
-    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, 2 * kCols);
+    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, kAcc * kCols);
 }
 
 // Named barrier over the epilogue warps only (barrier 1).

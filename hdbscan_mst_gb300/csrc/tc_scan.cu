@@ -7,11 +7,13 @@
 // one component skips the column tiles inside that component.  Per (row,
 // column) the epilogue forms t = |b|^2 - 2 a.b and ranks the pair by
 //     v = max(t, core_b^2 - |a|^2, core_a^2 - |a|^2)  ~  w(a, b)^2 - |a|^2
-// over columns of other components.  Each row is shared by E / 4 threads
-// (column parts); each keeps its 4 best (v, point) keys in registers and the
-// least v it dropped, and the parts of a row filter against the least of
-// their published 4th values.  At the end the parts merge into the row's 4
-// best and a threshold tau that every other column reaches or exceeds, which
+// over columns of other components.  The epilogue warps form E / 4 groups
+// that take every (E / 4)-th tile whole, so each row has one list per group:
+// its 4 best (v, point) keys in registers and the least v it dropped; the
+// groups of a row filter against the least of their published 4th values.
+// Columns of the row's own component (one run of the grouped order) are
+// masked out by position.  At the end the lists merge into the row's 4 best
+// and a threshold tau that every other column reaches or exceeds, which
 // mst_refine_kernel re-evaluates exactly and proves (this engine's rounding
 // bound) - the same output as the FFMA scan.
 #include <climits>
@@ -38,7 +40,7 @@ struct TcScanParams {
     ScanArgs a;
 };
 
-__shared__ float s_row_thr[kParts][kRows];  // per part and row: its 4th kept v
+__shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
 
     if (warp < kEpiWarps) {
         const int row = (warp & 3) * 32 + lane;
-        const int part = warp >> 2;
+        const int group = warp >> 2;
         const int r = r0 + row;
         const bool valid = r < a.na;
         const float na = valid ? a.act_norm[r] : 0.f;
@@ -106,71 +108,83 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         for (int p = 0; p < kKeep; ++p) keys[p] = kNoKey;
         float dropped = INFINITY;
 
+        // the row's own component is one run of columns [own_lo, own_hi)
+        const int own_lo = valid ? a.comp_start[rc] : 0;
+        const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
+
         tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
-            float v[32];
-            tmem_ld32(tbase, v);
+#pragma unroll 1
+            for (int cc = 0; cc < kCols / 32; ++cc) {
+                const int cb0 = col0 + cc * 32;
+                // own-component columns of this batch: bits [blo, bhi)
+                const int blo = min(max(own_lo - cb0, 0), 32);
+                const int bhi = min(max(own_hi - cb0, 0), 32);
+                // skip a batch that is own-component for every row of the
+                // warp; the skip must be warp-uniform: tcgen05.ld is collective
+                if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
+                float v[32];
+                tmem_ld32(tbase + cc * 32, v);
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 nb = __ldg(reinterpret_cast<const float4 *>(a.col_norm + col0 + j4 * 4));
-                v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
-                v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
-                v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
-                v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
-            }
-            float m16[16];
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 nb =
+                        __ldg(reinterpret_cast<const float4 *>(a.col_norm + cb0 + j4 * 4));
+                    v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
+                    v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
+                    v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
+                    v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
+                }
+                float m16[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
+                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
 #pragma unroll
-            for (int w2 = 8; w2 > 0; w2 >>= 1)
+                for (int w2 = 8; w2 > 0; w2 >>= 1)
 #pragma unroll
-                for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
-            // v >= t, so a batch whose least t does not beat the row's least
-            // published 4th value cannot change any part's 4 best
-            float thr = key_v(keys[kKeep - 1]);
+                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+                // v >= t, so a batch whose least t does not beat the row's
+                // least published 4th value cannot change any list's 4 best
+                float thr = key_v(keys[kKeep - 1]);
 #pragma unroll
-            for (int q = 0; q < kParts; ++q) thr = fminf(thr, s_row_thr[q][row]);
-            if (m16[0] < thr) {
-                float ct[32];
-                int cj[32];
-                int nc = 0;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (v[j] < thr) {
-                        ct[nc] = v[j];
-                        cj[nc] = j;
-                        ++nc;
+                for (int q = 0; q < kParts; ++q) thr = fminf(thr, s_row_thr[q][row]);
+                if (m16[0] < thr) {
+                    const uint32_t own =
+                        bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
+                    uint32_t mask = below_mask(v, thr) & ~own;
+                    if (mask) {
+#pragma unroll 1
+                        while (mask) {
+                            const int j = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const int col = cb0 + j;
+                            if (col >= a.n) break;
+                            const float cbc = __ldg(a.col_core + col);
+                            const float vv = fmaxf(
+                                fmaxf(pick32(v, j), __fsub_rn(__fmul_rn(cbc, cbc), na)), ra);
+                            const unsigned long long key =
+                                (static_cast<unsigned long long>(float_order(vv)) << 32) |
+                                static_cast<unsigned>(__ldg(a.col_orig + col));
+                            keep_insert(keys, key, dropped);
+                        }
+                        s_row_thr[group][row] = key_v(keys[kKeep - 1]);
                     }
                 }
-#pragma unroll 1
-                for (int c = 0; c < nc; ++c) {
-                    const int col = col0 + cj[c];
-                    if (col >= a.n || __ldg(a.col_comp + col) == rc) continue;
-                    const float cb = __ldg(a.col_core + col);
-                    const float vv = fmaxf(fmaxf(ct[c], __fsub_rn(__fmul_rn(cb, cb), na)), ra);
-                    const unsigned long long key =
-                        (static_cast<unsigned long long>(float_order(vv)) << 32) |
-                        static_cast<unsigned>(__ldg(a.col_orig + col));
-                    keep_insert(keys, key, dropped);
-                }
-                s_row_thr[part][row] = key_v(keys[kKeep - 1]);
             }
         });
 
-        // Merge the parts of each row in the idle ring: tau bounds every
+        // Merge the lists of each row in the idle ring: tau bounds every
         // column not kept - dropped ones directly, filtered ones by the 4th
-        // kept value of the part that filtered them.
+        // kept value of the group that filtered them.
         unsigned long long *pk =
             reinterpret_cast<unsigned long long *>(base + 2 * (a.dk / kSlab) * kSlabTile);
         float *pt = reinterpret_cast<float *>(pk + (kParts - 1) * kRows * kKeep);
         float tau = fminf(dropped, key_v(keys[kKeep - 1]));
         epilogue_sync<kEpiWarps>();
-        if (part > 0) {
+        if (group > 0) {
 #pragma unroll
-            for (int p = 0; p < kKeep; ++p) pk[((part - 1) * kRows + row) * kKeep + p] = keys[p];
-            pt[(part - 1) * kRows + row] = tau;
+            for (int p = 0; p < kKeep; ++p) pk[((group - 1) * kRows + row) * kKeep + p] = keys[p];
+            pt[(group - 1) * kRows + row] = tau;
         }
         epilogue_sync<kEpiWarps>();
-        if (part == 0) {
+        if (group == 0) {
 #pragma unroll 1
             for (int q = 1; q < kParts; ++q) {
                 tau = fminf(tau, pt[(q - 1) * kRows + row]);

@@ -48,8 +48,11 @@ typedef enum {
                                 /* with a consistent weight function; reported, never  */
                                 /* looped on)                                          */
     HDBMST_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed         */
-    HDBMST_ERR_TOO_LARGE = 7    /* the problem does not fit hdbmst_knn_noalloc's fixed */
+    HDBMST_ERR_TOO_LARGE = 7,   /* the problem does not fit hdbmst_knn_noalloc's fixed */
                                 /* scratch (HDBMST_NOALLOC_SCRATCH_BYTES)              */
+    HDBMST_ERR_TIMEOUT = 8      /* a wait inside a kernel gave up after its bound      */
+                                /* (about 1.5 s); the kernel returned, the device      */
+                                /* stays usable, the outputs are not valid             */
 } hdbmst_status;
 
 /* Largest k for hdbmst_knn, and largest min_samples + 1 for hdbmst_core_distances. */
@@ -211,6 +214,10 @@ int hdbmst_set_engine(int engine);
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);
 
+/* Name of the CUDA error behind the most recent HDBMST_ERR_CUDA of this
+ * process ("cudaSuccess" if there was none); host-side, not thread-safe. */
+const char *hdbmst_last_cuda_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int hdbmst_version(void);
 
@@ -220,6 +227,8 @@ int hdbmst_version(void);
  * hdbmst_launch_count: kernels this library has launched since load.
  * hdbmst_profile_enable(1): record a CUDA event pair around every kernel
  *   launch, on the launching stream, grouped by kernel; 0 stops recording.
+ *   Enabling creates a pool of events on the current device first, so that
+ *   no event is created between launches.
  * hdbmst_profile_read: synchronises the recorded events, writes per-kernel
  *   total milliseconds and launch counts for up to max_kernels kernels
  *   (either pointer may be NULL), clears the record and returns the number of
