@@ -179,6 +179,10 @@ def run_gpu(args):
         edges, w = H.mr_mst(Xd, core, idx, dist_)
         return core, edges, w
 
+    # the clock sampler starts before the warm-up: nvidia-smi's start-up
+    # (NVML initialisation) must not fall inside the timed steps
+    clk = ClockSampler(local).__enter__()
+    time.sleep(0.5)
     for _ in range(args.warmup):
         flush_l2(flush)
         step()
@@ -203,9 +207,11 @@ def run_gpu(args):
     launches0 = H.launch_count()
     barrier(dist, device)
     torch.cuda.synchronize(device)
-    with ClockSampler(local) as clk:
+    try:
         times = timed(step)
         torch.cuda.synchronize(device)
+    finally:
+        clk.__exit__(None, None, None)
     barrier(dist, device)
     launches = H.launch_count() - launches0
     rounds = H.last_mst_rounds()
@@ -317,6 +323,8 @@ def run_gpu(args):
         "roofline": main_roof,
         "kernel_ms_per_step": breakdown,
         "profiled_ms_per_step": round(sum(prof_times) / args.steps, 3),
+        "step_ms": {"min": round(min(times), 3), "median": round(statistics.median(times), 3),
+                    "max": round(max(times), 3)},
         "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e,
                             "exact_rows": x} for a, e, x in rounds],
         "gpu_launches": launches,

@@ -8,16 +8,17 @@
 // (t = |y|^2 - 2 x.y, column) of its range, which knn_refine_kernel merges,
 // re-evaluates exactly and proves (with this engine's rounding bound).
 //
-// Warp roles (one CTA per SM): E epilogue warps (E = 16 for KP = 16, 8 for
-// KP = 32), then one producer warp and one MMA warp.
-//  * the producer (one lane) streams operands with TMA: the CTA's query rows
-//    once (hi and lo parts, resident), then every column tile slab by slab
-//    (32 features, hi and lo) through a 4-stage ring guarded by full/empty
+// Warp roles (one CTA per SM): E epilogue warps (E = 12 for KP = 16, 8 for
+// KP = 32), then one producer warp and E / 4 MMA warps.
+//  * the first epilogue group writes the CTA's query rows (hi and lo parts)
+//    into TMEM once, where the MMAs read them as the A operand;
+//  * the producer (one lane) streams every column tile with TMA slab by slab
+//    (32 features, hi and lo) through a 6-stage ring guarded by full/empty
 //    mbarriers;
-//  * the MMA warp (one lane) issues per slab 3 x 4 TF32 MMAs
-//    (hi.hi + hi.lo + lo.hi) into one of four TMEM accumulators, frees each
-//    ring stage with tcgen05.commit, and signals the accumulator when a tile
-//    is complete;
+//  * the MMA warps (one lane each, one per group's tiles) issue per slab 3 x 4
+//    TF32 MMAs (hi.hi + hi.lo + lo.hi) into the tile's TMEM accumulator, free
+//    each ring stage with tcgen05.commit, and signal the accumulator when a
+//    tile is complete;
 //  * the epilogue warps form E / 4 groups; group g takes every (E / 4)-th
 //    tile whole, and warp w of it reads TMEM lanes 32 (w % 4) .. (its 32
 //    rows), 32 columns at a time.  Each row thus has one list per group, kept
@@ -25,7 +26,9 @@
 //    hang").  The groups publish each row's KP-th key in shared memory and
 //    filter against the least of them (a candidate that cannot beat it cannot
 //    reach the row's top KP), so the row's insertions stay close to those of
-//    one list.  At the end the lists of a row are merged.
+//    one list.  A warp reads the column norms of a tile from its own shared
+//    buffer, filled by cp.async while the tile before was multiplied.  At the
+//    end the lists of a row are merged.
 // Every wait is bounded; a wait that gives up flags the status word, stops
 // every role, drains what it issued, and the CTA frees its TMEM.
 #include <climits>
@@ -43,18 +46,21 @@ namespace {
 using namespace tc;
 
 struct TcKnnParams {
-    PipeMaps maps;  // A: query rows, B: columns, point-major [rows][dk]
+    PipeMaps maps;               // B: columns, point-major [rows][dk]
+    const float *a_hi, *a_lo;    // A: query rows, point-major [rows][dk]
     KnnTileArgs a;
 };
 
 template <int KP>
 struct Epi {
-    static constexpr int kWarps = KP == 16 ? 16 : 8;   // epilogue warps
+    static constexpr int kWarps = KP == 16 ? 12 : 8;   // epilogue warps
     static constexpr int kParts = kWarps / 4;          // groups: lists per row
-    static constexpr int kThreads = (kWarps + 2) * 32; // + producer + MMA warp
+    static constexpr int kThreads = (kWarps + 1 + kWarps / 4) * 32;  // + producer + MMA warps
 };
 
 __shared__ float g_row_tau[4][kRows];  // per group and row: that list's KP-th key
+constexpr int kMaxEpiWarps = 12;
+__shared__ float4 s_cnorm[kMaxEpiWarps][2][kCols / 4];  // per warp: two tiles' column norms
 
 template <int KP>
 __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float t, int j) {
@@ -94,8 +100,9 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
     fence_before();
     __syncthreads();
     fence_after();
-    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
+    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, seq);
 
+    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, a.dk);
     if (warp < kEpiWarps) {
         // thread = (row, group): rows 32 (w % 4) + lane, group w / 4
         const int row = (warp & 3) * 32 + lane;
@@ -107,15 +114,17 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
             key[p] = INFINITY;
             idx[p] = INT_MAX;
         }
-        tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
+        const auto prefetch = [&](int col0, int buf) {
+            cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
+        };
+        tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
             for (int cc = 0; cc < kCols / 32; ++cc) {
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb =
-                        __ldg(reinterpret_cast<const float4 *>(a.ynorm + col0 + cc * 32 + j4 * 4));
+                    const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
                     v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
                     v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
                     v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
@@ -149,7 +158,7 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
         });
         // merge the row's lists: the ring is idle now, other groups park there
         if (kParts > 1) {
-            float *pk = reinterpret_cast<float *>(base + 2 * (a.dk / kSlab) * kSlabTile);
+            float *pk = reinterpret_cast<float *>(base);
             int *pi = reinterpret_cast<int *>(pk + (kParts - 1) * kRows * KP);
             epilogue_sync<kEpiWarps>();  // every MMA has been consumed
             if (group > 0) {
@@ -201,9 +210,10 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const 
                           cudaStream_t s) {
     TcKnnParams P;
     P.a = a;
-    if (!make_point_map(&P.maps.a_hi, a.Xp, x_rows, a.dk) ||
-        !make_point_map(&P.maps.a_lo, Xlo, x_rows, a.dk) ||
-        !make_point_map(&P.maps.b_hi, a.Yp, y_rows, a.dk) ||
+    P.a_hi = a.Xp;
+    P.a_lo = Xlo;
+    (void)x_rows;
+    if (!make_point_map(&P.maps.b_hi, a.Yp, y_rows, a.dk) ||
         !make_point_map(&P.maps.b_lo, Ylo, y_rows, a.dk))
         return cudaErrorInvalidValue;
     if (KP == 16) return tc_launch<16>(P, row_tiles, splits, s);

@@ -1,20 +1,32 @@
 // The warp-specialized tensor-core distance-tile pipeline shared by the k-NN
 // search and the Boruvka scan.
 //
-// One CTA per SM owns 128 rows (the A operand, resident) and a sequence of
-// 128-column tiles (the B operand, streamed).  Dot products use three TF32
-// passes (hi.hi + hi.lo + lo.hi, see tc.cuh); the operands come from
-// point-major [rows][dk] float32 arrays of hi (raw) and lo parts through 2-D
-// TMA tensor maps with 128-byte swizzle, dk = 32 or 64.
+// One CTA per SM owns 128 rows (the A operand, resident in TMEM) and a
+// sequence of 128-column tiles (the B operand, streamed through shared
+// memory).  Dot products use three TF32 passes (hi.hi + hi.lo + lo.hi, see
+// tc.cuh); the operands come from point-major [rows][dk] float32 arrays of hi
+// (raw) and lo parts, dk = 32 or 64: the first epilogue group writes the A
+// rows into TMEM columns [0, 2 dk) once, and B arrives through 2-D TMA tensor
+// maps with 128-byte swizzle.  With A in TMEM the tensor core reads only B
+// from shared memory, half the bytes per MMA.
 //
 // Roles: warps 0 .. E-1 are the caller's epilogue, warp E the TMA producer
-// (one lane), warp E+1 the MMA issuer (one lane, also owns the TMEM
-// allocation).  Stages: a 4-deep ring of 32-feature slabs (full/empty
-// mbarriers) and four 128-column TMEM accumulators (afull/aempty), all 512
-// columns of TMEM.  The epilogue warps form E / 4 groups of four (one warp per
-// 32-lane TMEM quadrant); group g takes the tiles t with t % (E / 4) = g,
-// whole, so each warp has E / 4 tile periods for one tile and the latency of
-// its chain (TMEM load, norms, selection) hides behind the other groups' work.
+// (one lane), warps E+1 .. E+G the MMA issuers, G = E / 4 (one lane each; E+1
+// also owns the TMEM allocation).  Tile t belongs to group, accumulator and
+// issuer t % G: a single issuing thread is a serial chain of barrier tests,
+// fences, descriptor arithmetic and MMA issues that falls behind the tensor
+// core (measured: 82 cycles of thread time per 64-cycle MMA), several keep its
+// queue fed.  Each issuer owns its accumulator and its share of the ring, so
+// every barrier is used in order by one thread and its phase parity cannot
+// alias.  Stages: a 6-deep ring of 32-feature slabs (full/empty
+// mbarriers) and one 128-column TMEM accumulator per epilogue group
+// (afull/aempty) after the A columns, in a 512-column allocation.  The epilogue warps
+// form E / 4 groups of four (one warp per 32-lane TMEM quadrant); group g
+// takes the tiles t with t % (E / 4) = g, whole, so each warp has E / 4 tile
+// periods for one tile and the latency of its chain (TMEM load, column data,
+// selection) hides behind the other groups' work.  Each epilogue warp
+// prefetches the column data of its next tile with cp.async while the tile
+// before it is multiplied.
 // Every wait is bounded; the first that gives up sets S.abort, every role
 // winds down, and tc_teardown drains and frees TMEM.
 #pragma once
@@ -27,18 +39,43 @@
 namespace hdbmst {
 namespace tc {
 
-constexpr int kStages = 4;
-constexpr int kAcc = 4;  // TMEM accumulators of kCols columns
+constexpr int kStages = 6;
+
+// Ring slot of slab s of tile t with G issuers: issuer j = t % G owns stages
+// [j S, j S + S), S = 6 / G, and uses them in order, so that each stage's uses
+// - and its barrier phases - follow one another in one thread.  u counts the
+// issuer's slabs.
+template <int G>
+struct Slot {
+    static constexpr int kS = kStages / G;
+    int st;
+    uint32_t parity;
+    __device__ Slot(int t, int s, int slabs) {
+        const int u = (t / G) * slabs + s;
+        st = (t % G) * kS + u % kS;
+        parity = static_cast<uint32_t>(u / kS) & 1u;
+    }
+};
+constexpr int kAccMax = 3;          // TMEM accumulators of kCols columns
+constexpr uint32_t kAccBase = 128;  // TMEM columns [0, 2 dk) hold A hi and lo
+constexpr uint32_t kTmemCols = 512; // the allocation
+
+// One accumulator per epilogue group, so that each always belongs to the same
+// group.
+template <int kEpiWarps>
+__host__ __device__ constexpr int acc_count() {
+    return kEpiWarps / 4;
+}
 constexpr uint32_t kSlabTile = kRows * kSlabBytes;  // 16 KB: one slab of 128 rows
-// dynamic shared memory: resident rows (hi + lo, up to 2 slabs) + the ring
-constexpr size_t kPipeSmem = (2 * 2 + 2 * kStages) * kSlabTile + 1024;
+// dynamic shared memory: the ring (a stage holds one slab, hi and lo)
+constexpr size_t kPipeSmem = 2 * kStages * kSlabTile + 1024;
 
 struct PipeMaps {
-    CUtensorMap a_hi, a_lo, b_hi, b_lo;
+    CUtensorMap b_hi, b_lo;
 };
 
 struct PipeSmem {
-    uint64_t full[kStages], empty[kStages], afull[kAcc], aempty[kAcc], abar;
+    uint64_t full[kStages], empty[kStages], afull[kAccMax], aempty[kAccMax], abar;
     uint32_t tmem_base;
     int abort;
 };
@@ -73,41 +110,68 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], 1);
         }
-        for (int i = 0; i < kAcc; ++i) {
+        for (int i = 0; i < acc_count<kEpiWarps>(); ++i) {
             mbar_init(&S.afull[i], 1);
             mbar_init(&S.aempty[i], 4 * 32);  // the four warps of one group
         }
-        mbar_init(&S.abar, 1);
+        mbar_init(&S.abar, 4 * 32);  // the first group, once A is in TMEM
         S.abort = 0;
         fence_mbar_init();
     }
-    static_assert(kAcc % (kEpiWarps / 4) == 0, "each accumulator belongs to one group");
-    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kAcc * kCols);
+    static_assert(acc_count<kEpiWarps>() >= 1 && acc_count<kEpiWarps>() <= kAccMax,
+                  "one accumulator per epilogue group");
+    static_assert(kAccBase + kAccMax * kCols <= kTmemCols, "TMEM budget");
+    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kTmemCols);
 }
 
-// Producer and MMA roles (warps E and E+1); epilogue warps return at once.
-// a_row: first row of the A operand in its tensor map.
+// The A operand into TMEM, by the first epilogue group (warps 0 .. 3, one per
+// 32-lane quadrant): thread (w, lane) copies row 32 w + lane of the CTA's row
+// block - hi parts to columns [0, dk), lo parts to [dk, 2 dk) - then arrives
+// on S.abar.  rows: point-major [..][dk] arrays, row0: the block's first row.
+__device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const float *a_lo,
+                                          int64_t row0, int dk) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t taddr = S.tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+    const int64_t off = (row0 + warp * 32 + lane) * dk;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        const float *src = (h ? a_lo : a_hi) + off;
+#pragma unroll 1
+        for (int c = 0; c < dk; c += 32) {
+            float v[32];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 x = __ldg(reinterpret_cast<const float4 *>(src + c + j4 * 4));
+                v[j4 * 4 + 0] = x.x;
+                v[j4 * 4 + 1] = x.y;
+                v[j4 * 4 + 2] = x.z;
+                v[j4 * 4 + 3] = x.w;
+            }
+            tmem_st32(taddr + static_cast<uint32_t>(h * dk + c), v);
+        }
+    }
+    tmem_wait_st();
+    fence_before();
+    mbar_arrive(&S.abar);
+}
+
+// Producer and MMA roles (warps E, E+1, E+2); epilogue warps return at once.
 template <int kEpiWarps>
 __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeSmem &S,
-                                                        uint32_t sbase, int dk, int a_row,
+                                                        uint32_t sbase, int dk,
                                                         const TileSeq &seq) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slabs = dk / kSlab;
-    const uint32_t a_hi = sbase, a_lo = sbase + slabs * kSlabTile;
-    const uint32_t ring = sbase + 2 * slabs * kSlabTile;
+    const uint32_t ring = sbase;
+    constexpr int kAcc = acc_count<kEpiWarps>();  // = issuers = epilogue groups
+    static_assert(kStages % kAcc == 0, "the ring divides among the issuers");
     if (warp == kEpiWarps && lane == 0) {
-        mbar_expect_tx(&S.abar, 2 * slabs * kSlabTile);
-        for (int s = 0; s < slabs; ++s) {
-            tma_load_2d(a_hi + s * kSlabTile, &M.a_hi, s * kSlab, a_row, &S.abar);
-            tma_load_2d(a_lo + s * kSlabTile, &M.a_lo, s * kSlab, a_row, &S.abar);
-        }
-        int it = 0;
         for (int t = 0; t < seq.n; ++t) {
             const int col0 = seq.at(t) * kCols;
-            for (int s = 0; s < slabs; ++s, ++it) {
-                const int st = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait<kSleepProducer>(&S.empty[st], ph ^ 1) ||
+            for (int s = 0; s < slabs; ++s) {
+                const Slot<kAcc> slot(t, s, slabs);
+                const int st = slot.st;
+                if (!mbar_wait<kSleepProducer>(&S.empty[st], slot.parity ^ 1) ||
                     *(volatile int *)&S.abort) {
                     S.abort = 1;
                     return;
@@ -118,33 +182,39 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                 tma_load_2d(hi + kSlabTile, &M.b_lo, s * kSlab, col0, &S.full[st]);
             }
         }
-    } else if (warp == kEpiWarps + 1 && lane == 0) {
+    } else if (warp > kEpiWarps && warp <= kEpiWarps + kAcc && lane == 0) {
+        const int issuer = warp - kEpiWarps - 1;
         const uint32_t idesc = instr_desc(kRows, kCols);
         const uint32_t tmem = S.tmem_base;
         bool ok = mbar_wait<kSleepMma>(&S.abar, 0);
-        int it = 0;
-        for (int t = 0; t < seq.n && ok; ++t) {
-            const int acc = t % kAcc;
+        if (ok) fence_after();
+        for (int t = issuer; t < seq.n && ok; t += kAcc) {
+            const int acc = issuer;
             ok = mbar_wait<kSleepMma>(&S.aempty[acc], ((t / kAcc) & 1) ^ 1) &&
                  !*(volatile int *)&S.abort;
             if (!ok) break;
             fence_after();
-            const uint32_t d = tmem + static_cast<uint32_t>(acc * kCols);
-            for (int s = 0; s < slabs; ++s, ++it) {
-                const int st = it % kStages;
-                ok = mbar_wait<kSleepMma>(&S.full[st], (it / kStages) & 1);
+            const uint32_t d = tmem + kAccBase + static_cast<uint32_t>(acc * kCols);
+            for (int s = 0; s < slabs; ++s) {
+                const Slot<kAcc> slot(t, s, slabs);
+                const int st = slot.st;
+                ok = mbar_wait<kSleepMma>(&S.full[st], slot.parity);
                 if (!ok) break;
                 fence_after();
-                const uint32_t hi = ring + st * 2 * kSlabTile;
+                // The issuing thread is a serial chain, so keep it short: the
+                // descriptors of the slab's K steps are the slab's first one
+                // plus 32 bytes (2 in the address field) per step.
+                const uint64_t bh = smem_desc(ring + st * 2 * kSlabTile);
+                const uint64_t bl = bh + (kSlabTile >> 4);
+                const uint32_t ah = tmem + static_cast<uint32_t>(s * kSlab), al = ah + dk;
+                mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
+                mma_tf32_ts(d, ah, bl, idesc, 1u);
+                mma_tf32_ts(d, al, bh, idesc, 1u);
 #pragma unroll
-                for (int kk = 0; kk < kSlab / 8; ++kk) {
-                    const uint32_t off = kk * 32;
-                    const uint64_t ah = smem_desc(a_hi + s * kSlabTile + off);
-                    const uint64_t al = smem_desc(a_lo + s * kSlabTile + off);
-                    const uint64_t bh = smem_desc(hi + off), bl = smem_desc(hi + kSlabTile + off);
-                    mma_tf32(d, ah, bh, idesc, (s > 0 || kk > 0) ? 1u : 0u);
-                    mma_tf32(d, ah, bl, idesc, 1u);
-                    mma_tf32(d, al, bh, idesc, 1u);
+                for (int kk = 1; kk < kSlab / 8; ++kk) {
+                    mma_tf32_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
+                    mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
+                    mma_tf32_ts(d, al + kk * 8, bh + 2 * kk, idesc, 1u);
                 }
                 mma_commit(&S.empty[st]);
             }
@@ -156,29 +226,41 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
 }
 
 // Epilogue loop of warp w < E (group w / 4, TMEM lanes 32 (w % 4) ..): for
-// every tile of its group, waits for the tile's accumulator and calls
-// consume(tmem_addr, col0) with the TMEM address of this thread's lane at the
-// tile's first column and the tile's first global column; then hands the
-// accumulator back.
-template <int kEpiWarps, class Consume>
+// every tile of its group, calls prefetch(col0, buf) for the group's next tile
+// (the warp issues cp.async copies of that tile's column data into its buffer
+// buf of two), waits for the tile's accumulator and its own copies, and calls
+// consume(tmem_addr, col0, buf) with the TMEM address of this thread's lane at
+// the tile's first column, the tile's first global column and the buffer
+// holding its column data; then hands the accumulator back.
+template <int kEpiWarps, class Prefetch, class Consume>
 __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq,
-                                                 Consume &&consume) {
+                                                 Prefetch &&prefetch, Consume &&consume) {
     constexpr int kGroups = kEpiWarps / 4;
+    constexpr int kAcc = acc_count<kEpiWarps>();
     const int warp = threadIdx.x >> 5;
     const int group = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tmem = S.tmem_base;
-    for (int t = group; t < seq.n; t += kGroups) {
+    if (group < seq.n) prefetch(seq.at(group) * kCols, 0);
+    cp_async_commit();
+    for (int t = group, k = 0; t < seq.n; t += kGroups, ++k) {
+        if (t + kGroups < seq.n) prefetch(seq.at(t + kGroups) * kCols, (k + 1) & 1);
+        cp_async_commit();
         const int acc = t % kAcc;
         const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], (t / kAcc) & 1);
         if (!w) S.abort = 1;
         // a warp leaves together: tcgen05.ld is warp-collective
         if (__any_sync(0xffffffffu, !w || *(volatile int *)&S.abort)) break;
+        cp_async_wait_one();  // this tile's column data (all but the newest group)
+        __syncwarp();
         fence_after();
-        consume(tmem + static_cast<uint32_t>(acc * kCols) + lane_base, seq.at(t) * kCols);
+        consume(tmem + kAccBase + static_cast<uint32_t>(acc * kCols) + lane_base,
+                seq.at(t) * kCols, k & 1);
         fence_before();
+        __syncwarp();  // the buffer is refilled two tiles later
         mbar_arrive(&S.aempty[acc]);
     }
+    cp_async_wait_all();
 }
 
 // All threads, last: report a give-up, drain what may still be in flight
@@ -191,13 +273,14 @@ __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
     if (S.abort) {
         if (tid == 0) {
             atomicOr(status, kStatusTimeout);
-            for (int i = 0; i < kAcc; ++i) mbar_wait<kSleepProducer>(&S.afull[i], 0);
+            for (int i = 0; i < acc_count<kEpiWarps>(); ++i)
+            mbar_wait<kSleepProducer>(&S.afull[i], 0);
             for (int i = 0; i < kStages; ++i) mbar_wait<kSleepProducer>(&S.full[i], 0);
         }
         __syncthreads();
     }
     fence_after();
-    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, kAcc * kCols);
+    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, kTmemCols);
 }
 
 // Named barrier over the epilogue warps only (barrier 1).

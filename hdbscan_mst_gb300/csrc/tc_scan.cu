@@ -31,17 +31,19 @@ namespace {
 using namespace tc;
 
 constexpr int kKeep = 4;
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 12;
 constexpr int kParts = kEpiWarps / 4;
-constexpr int kScanThreads = (kEpiWarps + 2) * 32;
+constexpr int kScanThreads = (kEpiWarps + 1 + kEpiWarps / 4) * 32;  // + producer + MMA warps
 
 struct TcScanParams {
-    PipeMaps maps;  // A: active rows, B: grouped columns, point-major [rows][dk]
+    PipeMaps maps;             // B: grouped columns, point-major [rows][dk]
+    const float *a_hi, *a_lo;  // A: active rows, point-major [rows][dk]
     ScanArgs a;
 };
 
 __shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
+__shared__ float4 s_cnorm[kEpiWarps][2][kCols / 4];  // per warp: two tiles' column norms
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
                                             float &dropped) {
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         skip_hi = c1 / kCols;
     }
     const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
-    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
+    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, seq);
+    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, a.dk);
 
     if (warp < kEpiWarps) {
         const int row = (warp & 3) * 32 + lane;
@@ -112,7 +115,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         const int own_lo = valid ? a.comp_start[rc] : 0;
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
 
-        tc_epilogue_loop<kEpiWarps>(S, seq, [&](uint32_t tbase, int col0) {
+        const auto prefetch = [&](int col0, int buf) {
+            cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
+        };
+        tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
             for (int cc = 0; cc < kCols / 32; ++cc) {
                 const int cb0 = col0 + cc * 32;
@@ -126,8 +132,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                 tmem_ld32(tbase + cc * 32, v);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb =
-                        __ldg(reinterpret_cast<const float4 *>(a.col_norm + cb0 + j4 * 4));
+                    const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
                     v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
                     v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
                     v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         // column not kept - dropped ones directly, filtered ones by the 4th
         // kept value of the group that filtered them.
         unsigned long long *pk =
-            reinterpret_cast<unsigned long long *>(base + 2 * (a.dk / kSlab) * kSlabTile);
+            reinterpret_cast<unsigned long long *>(base);
         float *pt = reinterpret_cast<float *>(pk + (kParts - 1) * kRows * kKeep);
         float tau = fminf(dropped, key_v(keys[kKeep - 1]));
         epilogue_sync<kEpiWarps>();
@@ -212,9 +217,9 @@ cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *X
                            cudaStream_t s) {
     TcScanParams P;
     P.a = a;
-    if (!make_point_map(&P.maps.a_hi, Xa_hi, a.lda, a.dk) ||
-        !make_point_map(&P.maps.a_lo, Xa_lo, a.lda, a.dk) ||
-        !make_point_map(&P.maps.b_hi, Xs_hi, a.ldx, a.dk) ||
+    P.a_hi = Xa_hi;
+    P.a_lo = Xa_lo;
+    if (!make_point_map(&P.maps.b_hi, Xs_hi, a.ldx, a.dk) ||
         !make_point_map(&P.maps.b_lo, Xs_lo, a.ldx, a.dk))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel,
