@@ -6,7 +6,8 @@
 // and a small selection keeps the smallest per row).  A CTA owns 128 query
 // rows and a range of 128-column tiles; it writes, per row, the KP best
 // (t = |y|^2 - 2 x.y, column) of its range, which knn_refine_kernel merges,
-// re-evaluates exactly and proves (with this engine's rounding bound).
+// re-evaluates exactly and proves (with this engine's rounding bound).  The
+// pipeline works in 64-column tiles, two per 128-column tile of the split.
 //
 // Warp roles (one CTA per SM): E epilogue warps (E = 12 for KP = 16, 8 for
 // KP = 32), then one producer warp and E / 4 MMA warps.
@@ -20,8 +21,8 @@
 //    each ring stage with tcgen05.commit, and signal the accumulator when a
 //    tile is complete;
 //  * the epilogue warps form E / 4 groups; group g takes every (E / 4)-th
-//    tile whole, and warp w of it reads TMEM lanes 32 (w % 4) .. (its 32
-//    rows), 32 columns at a time.  Each row thus has one list per group, kept
+//    tile whole (its two accumulators alternate), and warp w of it reads TMEM
+//    lanes 32 (w % 4) .. (its 32 rows), 32 columns at a time.  Each row thus has one list per group, kept
 //    in registers by the fixed compare-and-swap sink (page "HDBSCAN", "The
 //    hang").  The groups publish each row's KP-th key in shared memory and
 //    filter against the least of them (a candidate that cannot beat it cannot
@@ -60,7 +61,7 @@ struct Epi {
 
 __shared__ float g_row_tau[4][kRows];  // per group and row: that list's KP-th key
 constexpr int kMaxEpiWarps = 12;
-__shared__ float4 s_cnorm[kMaxEpiWarps][2][kCols / 4];  // per warp: two tiles' column norms
+__shared__ float4 s_cnorm[kMaxEpiWarps][2][kTileCols / 4];  // per warp: two tiles' column norms
 
 template <int KP>
 __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float t, int j) {
@@ -92,8 +93,9 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row_tile = blockIdx.x, split = blockIdx.y;
     const int r0 = a.row_base + row_tile * kRows;
+    constexpr int kSub = kCols / kTileCols;  // pipeline tiles per 128-column tile
     const int ct_begin = split * a.tiles_per_split;
-    const TileSeq seq(ct_begin, min(ct_begin + a.tiles_per_split, a.col_tiles), 0, 0);
+    const TileSeq seq(ct_begin * kSub, min(ct_begin + a.tiles_per_split, a.col_tiles) * kSub, 0, 0);
 
     for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
     tc_setup<kEpiWarps>(S);
@@ -115,11 +117,11 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
             idx[p] = INT_MAX;
         }
         const auto prefetch = [&](int col0, int buf) {
-            cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
+            if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
         };
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
-            for (int cc = 0; cc < kCols / 32; ++cc) {
+            for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
 #pragma unroll

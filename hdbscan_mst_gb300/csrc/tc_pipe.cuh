@@ -2,8 +2,8 @@
 // search and the Boruvka scan.
 //
 // One CTA per SM owns 128 rows (the A operand, resident in TMEM) and a
-// sequence of 128-column tiles (the B operand, streamed through shared
-// memory).  Dot products use three TF32 passes (hi.hi + hi.lo + lo.hi, see
+// sequence of 64-column tiles (the B operand, streamed through shared
+// memory in 128-column slabs, each shared by the two tiles it holds).  Dot products use three TF32 passes (hi.hi + hi.lo + lo.hi, see
 // tc.cuh); the operands come from point-major [rows][dk] float32 arrays of hi
 // (raw) and lo parts, dk = 32 or 64: the first epilogue group writes the A
 // rows into TMEM columns [0, 2 dk) once, and B arrives through 2-D TMA tensor
@@ -12,14 +12,16 @@
 //
 // Roles: warps 0 .. E-1 are the caller's epilogue, warp E the TMA producer
 // (one lane), warps E+1 .. E+G the MMA issuers, G = E / 4 (one lane each; E+1
-// also owns the TMEM allocation).  Tile t belongs to group, accumulator and
-// issuer t % G: a single issuing thread is a serial chain of barrier tests,
-// fences, descriptor arithmetic and MMA issues that falls behind the tensor
-// core (measured: 82 cycles of thread time per 64-cycle MMA), several keep its
-// queue fed.  Each issuer owns its accumulator and its share of the ring, so
+// also owns the TMEM allocation).  Tile t belongs to group and issuer t % G: a
+// single issuing thread is a serial chain of barrier tests, fences, descriptor
+// arithmetic and MMA issues that falls behind the tensor core (measured: 82
+// cycles of thread time per 64-cycle MMA), several keep its queue fed.  Each
+// group has two accumulators that its tiles alternate between, so the MMAs
+// of a group's next tile run while the group selects from the current one;
+// each issuer owns its group's accumulators and its share of the ring, so
 // every barrier is used in order by one thread and its phase parity cannot
 // alias.  Stages: a 6-deep ring of 32-feature slabs (full/empty
-// mbarriers) and one 128-column TMEM accumulator per epilogue group
+// mbarriers) and two 64-column TMEM accumulators per epilogue group
 // (afull/aempty) after the A columns, in a 512-column allocation.  The epilogue warps
 // form E / 4 groups of four (one warp per 32-lane TMEM quadrant); group g
 // takes the tiles t with t % (E / 4) = g, whole, so each warp has E / 4 tile
@@ -40,35 +42,49 @@ namespace hdbmst {
 namespace tc {
 
 constexpr int kStages = 6;
+constexpr int kTileCols = 64;   // columns of a tile (MMA N); a ring slab holds kCols = 2 tiles
+constexpr int kAccPerGroup = 2;
 
-// Ring slot of slab s of tile t with G issuers: issuer j = t % G owns stages
-// [j S, j S + S), S = 6 / G, and uses them in order, so that each stage's uses
-// - and its barrier phases - follow one another in one thread.  u counts the
-// issuer's slabs.
-template <int G>
+// Ring slot of slab s of the 128-column block at position h of the sequence:
+// stages are used in order (u counts slabs) and each use is consumed by the
+// two tiles 2h and 2h + 1.  With G = 2 or 3 issuers and a ring of 6 slabs
+// (dk = 64: 3 blocks, dk = 32: 6 blocks) the tiles of block h - ring depth
+// belong to the same two issuers as those of block h, so an issuer that waits
+// on a stage's use has waited on its previous use itself and the phase parity
+// cannot alias.
 struct Slot {
-    static constexpr int kS = kStages / G;
     int st;
     uint32_t parity;
-    __device__ Slot(int t, int s, int slabs) {
-        const int u = (t / G) * slabs + s;
-        st = (t % G) * kS + u % kS;
-        parity = static_cast<uint32_t>(u / kS) & 1u;
+    __device__ Slot(int h, int s, int slabs) {
+        const int u = h * slabs + s;
+        st = u % kStages;
+        parity = static_cast<uint32_t>(u / kStages) & 1u;
     }
 };
-constexpr int kAccMax = 3;          // TMEM accumulators of kCols columns
+constexpr int kAccMax = 6;          // TMEM accumulators of kTileCols columns
 constexpr uint32_t kAccBase = 128;  // TMEM columns [0, 2 dk) hold A hi and lo
 constexpr uint32_t kTmemCols = 512; // the allocation
 
-// One accumulator per epilogue group, so that each always belongs to the same
-// group.
+// Epilogue groups = MMA issuers; each owns kAccPerGroup accumulators.
 template <int kEpiWarps>
 __host__ __device__ constexpr int acc_count() {
     return kEpiWarps / 4;
 }
-constexpr uint32_t kSlabTile = kRows * kSlabBytes;  // 16 KB: one slab of 128 rows
+constexpr uint32_t kSlabTile = kCols * kSlabBytes;  // 16 KB: one slab of 128 columns
 // dynamic shared memory: the ring (a stage holds one slab, hi and lo)
 constexpr size_t kPipeSmem = 2 * kStages * kSlabTile + 1024;
+
+// Accumulator of tile t: group j = t % G alternates between its two.
+template <int G>
+struct AccSlot {
+    int acc;
+    uint32_t parity;  // phase parity of the tile's use of the accumulator
+    __device__ AccSlot(int t) {
+        const int lt = t / G;
+        acc = (t % G) * kAccPerGroup + lt % kAccPerGroup;
+        parity = static_cast<uint32_t>(lt / kAccPerGroup) & 1u;
+    }
+};
 
 struct PipeMaps {
     CUtensorMap b_hi, b_lo;
@@ -108,9 +124,9 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&S.full[i], 1);
-            mbar_init(&S.empty[i], 1);
+            mbar_init(&S.empty[i], 2);  // both tiles of the block
         }
-        for (int i = 0; i < acc_count<kEpiWarps>(); ++i) {
+        for (int i = 0; i < acc_count<kEpiWarps>() * kAccPerGroup; ++i) {
             mbar_init(&S.afull[i], 1);
             mbar_init(&S.aempty[i], 4 * 32);  // the four warps of one group
         }
@@ -118,9 +134,8 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
         S.abort = 0;
         fence_mbar_init();
     }
-    static_assert(acc_count<kEpiWarps>() >= 1 && acc_count<kEpiWarps>() <= kAccMax,
-                  "one accumulator per epilogue group");
-    static_assert(kAccBase + kAccMax * kCols <= kTmemCols, "TMEM budget");
+    static_assert(acc_count<kEpiWarps>() * kAccPerGroup <= kAccMax, "accumulators");
+    static_assert(kAccBase + kAccMax * kTileCols <= kTmemCols, "TMEM budget");
     if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kTmemCols);
 }
 
@@ -164,12 +179,12 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
     const int slabs = dk / kSlab;
     const uint32_t ring = sbase;
     constexpr int kAcc = acc_count<kEpiWarps>();  // = issuers = epilogue groups
-    static_assert(kStages % kAcc == 0, "the ring divides among the issuers");
+    static_assert((kAcc == 2 || kAcc == 3) && kStages == 6, "see Slot");
     if (warp == kEpiWarps && lane == 0) {
-        for (int t = 0; t < seq.n; ++t) {
-            const int col0 = seq.at(t) * kCols;
+        for (int h = 0; 2 * h < seq.n; ++h) {
+            const int col0 = seq.at(2 * h) * kTileCols;
             for (int s = 0; s < slabs; ++s) {
-                const Slot<kAcc> slot(t, s, slabs);
+                const Slot slot(h, s, slabs);
                 const int st = slot.st;
                 if (!mbar_wait<kSleepProducer>(&S.empty[st], slot.parity ^ 1) ||
                     *(volatile int *)&S.abort) {
@@ -184,27 +199,29 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
         }
     } else if (warp > kEpiWarps && warp <= kEpiWarps + kAcc && lane == 0) {
         const int issuer = warp - kEpiWarps - 1;
-        const uint32_t idesc = instr_desc(kRows, kCols);
+        const uint32_t idesc = instr_desc(kRows, kTileCols);
         const uint32_t tmem = S.tmem_base;
         bool ok = mbar_wait<kSleepMma>(&S.abar, 0);
         if (ok) fence_after();
         for (int t = issuer; t < seq.n && ok; t += kAcc) {
-            const int acc = issuer;
-            ok = mbar_wait<kSleepMma>(&S.aempty[acc], ((t / kAcc) & 1) ^ 1) &&
+            const AccSlot<kAcc> as(t);
+            const int acc = as.acc;
+            ok = mbar_wait<kSleepMma>(&S.aempty[acc], as.parity ^ 1) &&
                  !*(volatile int *)&S.abort;
             if (!ok) break;
             fence_after();
-            const uint32_t d = tmem + kAccBase + static_cast<uint32_t>(acc * kCols);
+            const uint32_t d = tmem + kAccBase + static_cast<uint32_t>(acc * kTileCols);
             for (int s = 0; s < slabs; ++s) {
-                const Slot<kAcc> slot(t, s, slabs);
+                const Slot slot(t >> 1, s, slabs);
                 const int st = slot.st;
                 ok = mbar_wait<kSleepMma>(&S.full[st], slot.parity);
                 if (!ok) break;
                 fence_after();
                 // The issuing thread is a serial chain, so keep it short: the
                 // descriptors of the slab's K steps are the slab's first one
-                // plus 32 bytes (2 in the address field) per step.
-                const uint64_t bh = smem_desc(ring + st * 2 * kSlabTile);
+                // plus 32 bytes (2 in the address field) per step; the odd tile
+                // of a block starts 64 rows (8 KB) into the slab.
+                const uint64_t bh = smem_desc(ring + st * 2 * kSlabTile + (t & 1) * (kSlabTile / 2));
                 const uint64_t bl = bh + (kSlabTile >> 4);
                 const uint32_t ah = tmem + static_cast<uint32_t>(s * kSlab), al = ah + dk;
                 mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
@@ -241,21 +258,22 @@ __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq
     const int group = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tmem = S.tmem_base;
-    if (group < seq.n) prefetch(seq.at(group) * kCols, 0);
+    if (group < seq.n) prefetch(seq.at(group) * kTileCols, 0);
     cp_async_commit();
     for (int t = group, k = 0; t < seq.n; t += kGroups, ++k) {
-        if (t + kGroups < seq.n) prefetch(seq.at(t + kGroups) * kCols, (k + 1) & 1);
+        if (t + kGroups < seq.n) prefetch(seq.at(t + kGroups) * kTileCols, (k + 1) & 1);
         cp_async_commit();
-        const int acc = t % kAcc;
-        const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], (t / kAcc) & 1);
+        const AccSlot<kAcc> as(t);
+        const int acc = as.acc;
+        const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], as.parity);
         if (!w) S.abort = 1;
         // a warp leaves together: tcgen05.ld is warp-collective
         if (__any_sync(0xffffffffu, !w || *(volatile int *)&S.abort)) break;
         cp_async_wait_one();  // this tile's column data (all but the newest group)
         __syncwarp();
         fence_after();
-        consume(tmem + kAccBase + static_cast<uint32_t>(acc * kCols) + lane_base,
-                seq.at(t) * kCols, k & 1);
+        consume(tmem + kAccBase + static_cast<uint32_t>(acc * kTileCols) + lane_base,
+                seq.at(t) * kTileCols, k & 1);
         fence_before();
         __syncwarp();  // the buffer is refilled two tiles later
         mbar_arrive(&S.aempty[acc]);
@@ -273,8 +291,8 @@ __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
     if (S.abort) {
         if (tid == 0) {
             atomicOr(status, kStatusTimeout);
-            for (int i = 0; i < acc_count<kEpiWarps>(); ++i)
-            mbar_wait<kSleepProducer>(&S.afull[i], 0);
+            for (int i = 0; i < acc_count<kEpiWarps>() * kAccPerGroup; ++i)
+                mbar_wait<kSleepProducer>(&S.afull[i], 0);
             for (int i = 0; i < kStages; ++i) mbar_wait<kSleepProducer>(&S.full[i], 0);
         }
         __syncthreads();

@@ -43,7 +43,7 @@ struct TcScanParams {
 
 __shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
-__shared__ float4 s_cnorm[kEpiWarps][2][kCols / 4];  // per warp: two tiles' column norms
+__shared__ float4 s_cnorm[kEpiWarps][2][kTileCols / 4];  // per warp: two tiles' column norms
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
                                             float &dropped) {
@@ -74,8 +74,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = blockIdx.x * kRows;
     const int split = blockIdx.y;
-    const int ct_begin = split * a.tiles_per_split;
-    const int ct_end = min(ct_begin + a.tiles_per_split, a.col_tiles);
+    constexpr int kSub = kCols / kTileCols;  // pipeline tiles per 128-column tile
+    const int ct_begin = split * a.tiles_per_split * kSub;
+    const int ct_end = min(split * a.tiles_per_split + a.tiles_per_split, a.col_tiles) * kSub;
 
     for (int i = tid; i < kParts * kRows; i += blockDim.x) (&s_row_thr[0][0])[i] = INFINITY;
     if (tid < kRows) s_rcomp[tid] = r0 + tid < a.na ? a.act_comp[r0 + tid] : -1;
@@ -90,8 +91,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
     if (uniform) {
         const int C = s_rcomp[0];
         const int c0 = a.comp_start[C], c1 = c0 + a.comp_size[C];
-        skip_lo = (c0 + kCols - 1) / kCols;
-        skip_hi = c1 / kCols;
+        // whole 128-column blocks only: a ring slab serves both its tiles
+        skip_lo = (c0 + kCols - 1) / kCols * kSub;
+        skip_hi = c1 / kCols * kSub;
     }
     const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
     tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, seq);
@@ -116,11 +118,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
 
         const auto prefetch = [&](int col0, int buf) {
-            cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
+            if (lane < kTileCols / 4)
+                cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
         };
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
-            for (int cc = 0; cc < kCols / 32; ++cc) {
+            for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 const int cb0 = col0 + cc * 32;
                 // own-component columns of this batch: bits [blo, bhi)
                 const int blo = min(max(own_lo - cb0, 0), 32);
