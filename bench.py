@@ -26,6 +26,7 @@ rank 0 prints the line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -58,6 +59,18 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
 FP32_LANES_PER_SM = 128
 # nominal dense tensor rates: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s
 TF32_PER_BF16 = 1.1 / 2.25
+# DRAM bytes per launch of the dominant kernel from one one-pass ncu capture
+# of the full workload (dram__bytes_read.sum + dram__bytes_write.sum), valid
+# only while the kernel's sources are those the capture ran (their sha256
+# below); otherwise the line reports null.
+TRAFFIC = {
+    ("knn_tile", "hdbscan_200k_d61"): {
+        "bytes": 1.12e9 + 28.41e6,
+        "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
+                    "hdbscan_mst_gb300/csrc/tc.cuh"),
+        "sha256": "6cd6b1687fb3fffc1da2f604b7da3c48affdc1d2f5eef2151eacc84c162c1eb1",
+    },
+}
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -273,7 +286,7 @@ def run_gpu(args):
     tf32_basis = ("measured bf16 burst x nominal tf32/bf16 (1.1/2.25)" if bf16 else
                   "fallback bf16 x nominal tf32/bf16 (1.1/2.25)")
 
-    def roofline(prof_, name, d_, pairs, tensor):
+    def roofline(prof_, name, d_, pairs, tensor, workload=None):
         """Dominant distance tile: algorithmic flops 2 d per pair over its launches."""
         if name not in prof_:
             return None
@@ -286,7 +299,7 @@ def run_gpu(args):
             issued = 3 * 2.0 * dk * pairs / avg_s / 1e12  # three TF32 passes on padded features
             return {"kernel": name, "engine": "tcgen05 3xTF32", "bound": "tensor",
                     "achieved": round(ach, 2), "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(ach / tf32_peak, 4), "traffic": None,
+                    "frac": round(ach / tf32_peak, 4), "traffic": traffic_for(name, workload),
                     "peak_basis": tf32_basis, "avg_launch_ms": round(avg_s * 1e3, 3),
                     "flops_per_launch": flops, "issued_tflops": round(issued, 1),
                     "issued_frac": round(issued / tf32_peak, 4),
@@ -298,7 +311,7 @@ def run_gpu(args):
                 "flops_per_launch": flops}
 
     # core distances: every clip against every clip (one launch)
-    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 64)
+    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 64, args.workload)
     knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], float(Xk.shape[1]) * Yk.shape[1],
                         Xk.shape[0] <= 64)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
@@ -343,6 +356,28 @@ def run_gpu(args):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def sources_sha256(paths) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_for(kernel: str, workload: str):
+    """Measured DRAM bytes per launch, or None when not measured for this
+    kernel and workload or the kernel changed since the capture."""
+    rec = TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    try:
+        if sources_sha256(rec["sources"]) != rec["sha256"]:
+            return None
+    except OSError:
+        return None
+    return rec["bytes"]
 
 
 def load_peaks():

@@ -195,15 +195,16 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
 
 /*
  * Distance-tile engine for the k-NN search (hdbmst_knn, hdbmst_knn_noalloc,
- * hdbmst_core_distances), process-wide, not thread-safe:
+ * hdbmst_core_distances) and the Boruvka scan (hdbmst_mr_mst), process-wide,
+ * not thread-safe:
  *   HDBMST_ENGINE_AUTO   tensor cores where supported (d <= 64), else FP32
  *                        FFMA (the default);
  *   HDBMST_ENGINE_SIMT   FP32 FFMA register-blocked tile everywhere;
  *   HDBMST_ENGINE_TENSOR same as AUTO (tensor cores need d <= 64).
  * The tensor-core tile ranks candidates with three-pass TF32 products
- * (tcgen05); both engines report distances re-evaluated exactly with dist()
- * and prove the kept set against their own rounding bound, so results are
- * identical bit for bit whichever engine ran.  Returns the previous setting;
+ * (tcgen05); both engines report distances and weights re-evaluated exactly
+ * with dist() and prove the kept set against their own rounding bound, so
+ * results are identical bit for bit whichever engine ran.  Returns the previous setting;
  * unknown values are ignored.
  */
 #define HDBMST_ENGINE_AUTO 0
