@@ -295,7 +295,7 @@ def run_gpu(args):
         flops = 2.0 * d_ * pairs
         ach = flops / avg_s / 1e12
         if tensor:
-            dk = 32 if d_ <= 32 else 64
+            dk = (d_ + 31) // 32 * 32  # padded features: whole 32-feature slabs
             issued = 3 * 2.0 * dk * pairs / avg_s / 1e12  # three TF32 passes on padded features
             return {"kernel": name, "engine": "tcgen05 3xTF32", "bound": "tensor",
                     "achieved": round(ach, 2), "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
@@ -311,9 +311,10 @@ def run_gpu(args):
                 "flops_per_launch": flops}
 
     # core distances: every clip against every clip (one launch)
-    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 64, args.workload)
+    # the tensor-core tile serves d <= 192 (k-NN) in the default engine
+    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 192, args.workload)
     knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], float(Xk.shape[1]) * Yk.shape[1],
-                        Xk.shape[0] <= 64)
+                        Xk.shape[0] <= 192, KNN_WORKLOAD if not args.skip_knn else None)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
                  for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
     line = {

@@ -34,6 +34,10 @@ bool use_tensor(int dk) {
     return g_engine != HDBMST_ENGINE_SIMT && tc_knn_supported(dk);
 }
 
+bool use_tensor_scan(int dk) {
+    return g_engine != HDBMST_ENGINE_SIMT && tc_scan_supported(dk);
+}
+
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
 std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
 
@@ -193,7 +197,7 @@ struct KnnBufs {
 void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
     b.Xf = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     // the tensor-core tile's low parts exist only where that engine can run
-    const bool lo = p.dk <= 64;
+    const bool lo = p.dk <= kTensorDkMax;
     b.Xp = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xlo = lo ? c.take<float>(static_cast<size_t>(p.dk) * p.n_pad) : nullptr;
     b.xnorm = c.take<float>(p.n_pad);
@@ -578,7 +582,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     const int slots = 2 * sm_count();
     const int col_tiles = static_cast<int>(p.n_pad / kBN);
 
-    const bool tensor = use_tensor(p.dk);
+    const bool tensor = use_tensor_scan(p.dk);
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
     LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, b.Xp,
                                   tensor ? b.Xlo : nullptr, b.norm, &b.st->status,

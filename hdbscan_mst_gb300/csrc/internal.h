@@ -42,13 +42,20 @@ cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int spl
                             cudaStream_t s);
 // tc_knn.cu: the same tile on tcgen05 TF32 MMAs (three passes), one CTA per SM,
 // operands by TMA from the point-major arrays (Xp / Yp and their low parts).
-bool tc_knn_supported(int dk);
+bool tc_knn_supported(int dk);   // dk a multiple of 32, at most kTensorDkMax
+bool tc_scan_supported(int dk);  // dk = 32 or 64
 cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
                           int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
                           cudaStream_t s);
 // Padded feature count: whole 32-feature slabs up to 64 (the tensor-core tile's
 // operand granule), multiples of 16 beyond.
-inline int padded_features(int d) { return d <= 64 ? (d + 31) / 32 * 32 : (d + 15) / 16 * 16; }
+// Padded feature count: whole 32-feature slabs up to kTensorDkMax (the
+// tensor-core tile works in slabs), else a multiple of 16 (the FFMA tile's K
+// step).
+constexpr int kTensorDkMax = 192;
+inline int padded_features(int d) {
+    return d <= kTensorDkMax ? (d + 31) / 32 * 32 : (d + 15) / 16 * 16;
+}
 
 struct KnnRefineArgs {
     const float *part_key;

@@ -9,8 +9,10 @@
 // re-evaluates exactly and proves (with this engine's rounding bound).  The
 // pipeline works in 64-column tiles, two per 128-column tile of the split.
 //
-// Warp roles (one CTA per SM): E epilogue warps (E = 12 for KP = 16, 8 for
-// KP = 32), then one producer warp and E / 4 MMA warps.
+// Warp roles (one CTA per SM): E epilogue warps (E = 12 for KP = 16 and
+// dk <= 64, else 8), then one producer warp and E / 4 MMA warps.  Rows of
+// more than 64 padded features (up to 192) use the pipeline's wide variant:
+// A hi in TMEM, A lo in shared memory.
 //  * the first epilogue group writes the CTA's query rows (hi and lo parts)
 //    into TMEM once, where the MMAs read them as the A operand;
 //  * the producer (one lane) streams every column tile with TMA slab by slab
@@ -52,9 +54,9 @@ struct TcKnnParams {
     KnnTileArgs a;
 };
 
-template <int KP>
+template <int KP, bool kWide>
 struct Epi {
-    static constexpr int kWarps = KP == 16 ? 12 : 8;   // epilogue warps
+    static constexpr int kWarps = (KP == 16 && !kWide) ? 12 : 8;  // epilogue warps
     static constexpr int kParts = kWarps / 4;          // groups: lists per row
     static constexpr int kThreads = (kWarps + 1 + kWarps / 4) * 32;  // + producer + MMA warps
 };
@@ -81,11 +83,11 @@ __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float
     }
 }
 
-template <int KP>
-__global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
+template <int KP, bool kWide>
+__global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
-    constexpr int kEpiWarps = Epi<KP>::kWarps;
-    constexpr int kParts = Epi<KP>::kParts;
+    constexpr int kEpiWarps = Epi<KP, kWide>::kWarps;
+    constexpr int kParts = Epi<KP, kWide>::kParts;
     extern __shared__ uint8_t smem_raw[];
     __shared__ PipeSmem S;
     const KnnTileArgs &a = P.a;
@@ -98,13 +100,13 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
     const TileSeq seq(ct_begin * kSub, min(ct_begin + a.tiles_per_split, a.col_tiles) * kSub, 0, 0);
 
     for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
-    tc_setup<kEpiWarps>(S);
+    tc_setup<kEpiWarps, kWide>(S);
     fence_before();
     __syncthreads();
     fence_after();
-    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, seq);
+    tc_produce_and_multiply<kEpiWarps, kWide>(P.maps, S, smem_u32(base), a.dk, r0, seq);
 
-    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, a.dk);
+    if (warp < 4) tc_load_a<kWide>(S, P.a_hi, P.a_lo, r0, a.dk);
     if (warp < kEpiWarps) {
         // thread = (row, group): rows 32 (w % 4) + lane, group w / 4
         const int row = (warp & 3) * 32 + lane;
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
         const auto prefetch = [&](int col0, int buf) {
             if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
         };
-        tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+        tc_epilogue_loop<kEpiWarps, kWide>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 float v[32];
@@ -190,22 +192,26 @@ __global__ void __launch_bounds__(Epi<KP>::kThreads, 1)
             }
         }
     }
-    tc_teardown<kEpiWarps>(S, a.status);
+    tc_teardown<kEpiWarps, kWide>(S, a.status);
 }
 
-template <int KP>
+template <int KP, bool kWide>
 cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP>,
+    const size_t smem = kWide ? kWidePipeSmem : kPipeSmem;
+    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP, kWide>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kPipeSmem));
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    tc_knn_kernel<KP><<<dim3(row_tiles, splits), Epi<KP>::kThreads, kPipeSmem, s>>>(P);
+    tc_knn_kernel<KP, kWide><<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool tc_knn_supported(int dk) { return (dk == 32 || dk == 64) && tensor_maps_available(); }
+bool tc_knn_supported(int dk) {
+    static_assert(kWideDkMax == kTensorDkMax, "the packed low parts cover the wide tile");
+    return dk % kSlab == 0 && dk >= kSlab && dk <= kWideDkMax && tensor_maps_available();
+}
 
 cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
                           int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
@@ -214,12 +220,15 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const 
     P.a = a;
     P.a_hi = a.Xp;
     P.a_lo = Xlo;
-    (void)x_rows;
+    const bool wide = a.dk > 64;
     if (!make_point_map(&P.maps.b_hi, a.Yp, y_rows, a.dk) ||
-        !make_point_map(&P.maps.b_lo, Ylo, y_rows, a.dk))
+        !make_point_map(&P.maps.b_lo, Ylo, y_rows, a.dk) ||
+        (wide && !make_point_map(&P.maps.a_lo, Xlo, x_rows, a.dk)))
         return cudaErrorInvalidValue;
-    if (KP == 16) return tc_launch<16>(P, row_tiles, splits, s);
-    if (KP == 32) return tc_launch<32>(P, row_tiles, splits, s);
+    if (!wide && KP == 16) return tc_launch<16, false>(P, row_tiles, splits, s);
+    if (!wide && KP == 32) return tc_launch<32, false>(P, row_tiles, splits, s);
+    if (wide && KP == 16) return tc_launch<16, true>(P, row_tiles, splits, s);
+    if (wide && KP == 32) return tc_launch<32, true>(P, row_tiles, splits, s);
     return cudaErrorInvalidValue;
 }
 

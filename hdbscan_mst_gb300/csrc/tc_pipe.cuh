@@ -29,6 +29,11 @@
 // selection) hides behind the other groups' work.  Each epilogue warp
 // prefetches the column data of its next tile with cp.async while the tile
 // before it is multiplied.
+// Wide rows (kWide, 64 < dk <= 192): the A hi parts alone fill TMEM columns
+// [0, dk), the A lo parts sit in shared memory (TMA, once per CTA) ahead of a
+// 3-stage ring, the lo.hi MMAs read both operands from shared memory, and two
+// epilogue groups keep their accumulators in TMEM columns [256, 512).
+//
 // Every wait is bounded; the first that gives up sets S.abort, every role
 // winds down, and tc_teardown drains and frees TMEM.
 #pragma once
@@ -41,7 +46,9 @@
 namespace hdbmst {
 namespace tc {
 
-constexpr int kStages = 6;
+constexpr int kStages = 6;       // ring slabs (kWide: kWideStages)
+constexpr int kWideStages = 3;
+constexpr int kWideDkMax = 192;
 constexpr int kTileCols = 64;   // columns of a tile (MMA N); a ring slab holds kCols = 2 tiles
 constexpr int kAccPerGroup = 2;
 
@@ -52,14 +59,21 @@ constexpr int kAccPerGroup = 2;
 // belong to the same two issuers as those of block h, so an issuer that waits
 // on a stage's use has waited on its previous use itself and the phase parity
 // cannot alias.
+template <int kSt>
 struct Slot {
     int st;
     uint32_t parity;
     __device__ Slot(int h, int s, int slabs) {
         const int u = h * slabs + s;
-        st = u % kStages;
-        parity = static_cast<uint32_t>(u / kStages) & 1u;
+        st = u % kSt;
+        parity = static_cast<uint32_t>(u / kSt) & 1u;
     }
+};
+
+template <bool kWide>
+struct PipeShape {
+    static constexpr int kSt = kWide ? kWideStages : kStages;
+    static constexpr uint32_t kAccBase = kWide ? 256u : 128u;  // first accumulator column
 };
 constexpr int kAccMax = 6;          // TMEM accumulators of kTileCols columns
 constexpr uint32_t kAccBase = 128;  // TMEM columns [0, 2 dk) hold A hi and lo
@@ -71,8 +85,10 @@ __host__ __device__ constexpr int acc_count() {
     return kEpiWarps / 4;
 }
 constexpr uint32_t kSlabTile = kCols * kSlabBytes;  // 16 KB: one slab of 128 columns
-// dynamic shared memory: the ring (a stage holds one slab, hi and lo)
+// dynamic shared memory: the ring (a stage holds one slab, hi and lo); kWide:
+// the A lo slabs, then the ring
 constexpr size_t kPipeSmem = 2 * kStages * kSlabTile + 1024;
+constexpr size_t kWidePipeSmem = (kWideDkMax / kSlab + 2 * kWideStages) * kSlabTile + 1024;
 
 // Accumulator of tile t: group j = t % G alternates between its two.
 template <int G>
@@ -88,6 +104,7 @@ struct AccSlot {
 
 struct PipeMaps {
     CUtensorMap b_hi, b_lo;
+    CUtensorMap a_lo;  // kWide only: the A rows' lo parts
 };
 
 struct PipeSmem {
@@ -118,7 +135,7 @@ __device__ __forceinline__ uint8_t *pipe_base(uint8_t *smem_raw) {
 }
 
 // Barrier initialisation and TMEM allocation; all threads, before anything else.
-template <int kEpiWarps>
+template <int kEpiWarps, bool kWide = false>
 __device__ __forceinline__ void tc_setup(PipeSmem &S) {
     const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
@@ -130,12 +147,15 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
             mbar_init(&S.afull[i], 1);
             mbar_init(&S.aempty[i], 4 * 32);  // the four warps of one group
         }
-        mbar_init(&S.abar, 4 * 32);  // the first group, once A is in TMEM
+        // warps 0 .. 3 once A is in TMEM (+ the producer's TMA of A lo)
+        mbar_init(&S.abar, 4 * 32 + (kWide ? 1 : 0));
         S.abort = 0;
         fence_mbar_init();
     }
     static_assert(acc_count<kEpiWarps>() * kAccPerGroup <= kAccMax, "accumulators");
     static_assert(kAccBase + kAccMax * kTileCols <= kTmemCols, "TMEM budget");
+    static_assert(!kWide || (acc_count<kEpiWarps>() * kAccPerGroup * kTileCols + 256 <= kTmemCols &&
+                             kWideDkMax <= 256), "TMEM budget, wide rows");
     if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kTmemCols);
 }
 
@@ -143,13 +163,14 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
 // 32-lane quadrant): thread (w, lane) copies row 32 w + lane of the CTA's row
 // block - hi parts to columns [0, dk), lo parts to [dk, 2 dk) - then arrives
 // on S.abar.  rows: point-major [..][dk] arrays, row0: the block's first row.
+template <bool kWide = false>
 __device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const float *a_lo,
                                           int64_t row0, int dk) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t taddr = S.tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t off = (row0 + warp * 32 + lane) * dk;
 #pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < (kWide ? 1 : 2); ++h) {
         const float *src = (h ? a_lo : a_hi) + off;
 #pragma unroll 1
         for (int c = 0; c < dk; c += 32) {
@@ -171,20 +192,27 @@ __device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const 
 }
 
 // Producer and MMA roles (warps E, E+1, E+2); epilogue warps return at once.
-template <int kEpiWarps>
+template <int kEpiWarps, bool kWide = false>
 __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeSmem &S,
-                                                        uint32_t sbase, int dk,
+                                                        uint32_t sbase, int dk, int a_row,
                                                         const TileSeq &seq) {
+    using Sh = PipeShape<kWide>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slabs = dk / kSlab;
-    const uint32_t ring = sbase;
+    const uint32_t alo = sbase;  // kWide: A lo slabs
+    const uint32_t ring = sbase + (kWide ? static_cast<uint32_t>(slabs) * kSlabTile : 0u);
     constexpr int kAcc = acc_count<kEpiWarps>();  // = issuers = epilogue groups
-    static_assert((kAcc == 2 || kAcc == 3) && kStages == 6, "see Slot");
+    static_assert(kWide ? kAcc == 2 : ((kAcc == 2 || kAcc == 3) && kStages == 6), "see Slot");
     if (warp == kEpiWarps && lane == 0) {
+        if (kWide) {
+            mbar_expect_tx(&S.abar, static_cast<uint32_t>(slabs) * kSlabTile);
+            for (int s = 0; s < slabs; ++s)
+                tma_load_2d(alo + s * kSlabTile, &M.a_lo, s * kSlab, a_row, &S.abar);
+        }
         for (int h = 0; 2 * h < seq.n; ++h) {
             const int col0 = seq.at(2 * h) * kTileCols;
             for (int s = 0; s < slabs; ++s) {
-                const Slot slot(h, s, slabs);
+                const Slot<Sh::kSt> slot(h, s, slabs);
                 const int st = slot.st;
                 if (!mbar_wait<kSleepProducer>(&S.empty[st], slot.parity ^ 1) ||
                     *(volatile int *)&S.abort) {
@@ -210,9 +238,9 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                  !*(volatile int *)&S.abort;
             if (!ok) break;
             fence_after();
-            const uint32_t d = tmem + kAccBase + static_cast<uint32_t>(acc * kTileCols);
+            const uint32_t d = tmem + Sh::kAccBase + static_cast<uint32_t>(acc * kTileCols);
             for (int s = 0; s < slabs; ++s) {
-                const Slot slot(t >> 1, s, slabs);
+                const Slot<Sh::kSt> slot(t >> 1, s, slabs);
                 const int st = slot.st;
                 ok = mbar_wait<kSleepMma>(&S.full[st], slot.parity);
                 if (!ok) break;
@@ -224,14 +252,28 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                 const uint64_t bh = smem_desc(ring + st * 2 * kSlabTile + (t & 1) * (kSlabTile / 2));
                 const uint64_t bl = bh + (kSlabTile >> 4);
                 const uint32_t ah = tmem + static_cast<uint32_t>(s * kSlab), al = ah + dk;
-                mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
-                mma_tf32_ts(d, ah, bl, idesc, 1u);
-                mma_tf32_ts(d, al, bh, idesc, 1u);
+                if (kWide) {
+                    // A lo from shared memory: its slab's descriptor, + 2 per K step
+                    const uint64_t als = smem_desc(alo + s * kSlabTile);
+                    mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
+                    mma_tf32_ts(d, ah, bl, idesc, 1u);
+                    mma_tf32(d, als, bh, idesc, 1u);
 #pragma unroll
-                for (int kk = 1; kk < kSlab / 8; ++kk) {
-                    mma_tf32_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
-                    mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
-                    mma_tf32_ts(d, al + kk * 8, bh + 2 * kk, idesc, 1u);
+                    for (int kk = 1; kk < kSlab / 8; ++kk) {
+                        mma_tf32_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
+                        mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
+                        mma_tf32(d, als + 2 * kk, bh + 2 * kk, idesc, 1u);
+                    }
+                } else {
+                    mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
+                    mma_tf32_ts(d, ah, bl, idesc, 1u);
+                    mma_tf32_ts(d, al, bh, idesc, 1u);
+#pragma unroll
+                    for (int kk = 1; kk < kSlab / 8; ++kk) {
+                        mma_tf32_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
+                        mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
+                        mma_tf32_ts(d, al + kk * 8, bh + 2 * kk, idesc, 1u);
+                    }
                 }
                 mma_commit(&S.empty[st]);
             }
@@ -249,9 +291,10 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
 // consume(tmem_addr, col0, buf) with the TMEM address of this thread's lane at
 // the tile's first column, the tile's first global column and the buffer
 // holding its column data; then hands the accumulator back.
-template <int kEpiWarps, class Prefetch, class Consume>
+template <int kEpiWarps, bool kWide = false, class Prefetch, class Consume>
 __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq,
                                                  Prefetch &&prefetch, Consume &&consume) {
+    using Sh = PipeShape<kWide>;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kAcc = acc_count<kEpiWarps>();
     const int warp = threadIdx.x >> 5;
@@ -272,7 +315,7 @@ __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq
         cp_async_wait_one();  // this tile's column data (all but the newest group)
         __syncwarp();
         fence_after();
-        consume(tmem + kAccBase + static_cast<uint32_t>(acc * kTileCols) + lane_base,
+        consume(tmem + Sh::kAccBase + static_cast<uint32_t>(acc * kTileCols) + lane_base,
                 seq.at(t) * kTileCols, k & 1);
         fence_before();
         __syncwarp();  // the buffer is refilled two tiles later
@@ -283,7 +326,7 @@ __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq
 
 // All threads, last: report a give-up, drain what may still be in flight
 // (bounded), free TMEM.
-template <int kEpiWarps>
+template <int kEpiWarps, bool kWide = false>
 __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
     const int tid = threadIdx.x, warp = tid >> 5;
     fence_before();
@@ -293,7 +336,8 @@ __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
             atomicOr(status, kStatusTimeout);
             for (int i = 0; i < acc_count<kEpiWarps>() * kAccPerGroup; ++i)
                 mbar_wait<kSleepProducer>(&S.afull[i], 0);
-            for (int i = 0; i < kStages; ++i) mbar_wait<kSleepProducer>(&S.full[i], 0);
+            for (int i = 0; i < PipeShape<kWide>::kSt; ++i)
+                mbar_wait<kSleepProducer>(&S.full[i], 0);
         }
         __syncthreads();
     }

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         skip_hi = c1 / kCols * kSub;
     }
     const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
-    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, seq);
+    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
     if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, a.dk);
 
     if (warp < kEpiWarps) {
@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
 }
 
 }  // namespace
+
+bool tc_scan_supported(int dk) { return (dk == 32 || dk == 64) && tensor_maps_available(); }
 
 cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *Xa_lo,
                            const float *Xs_hi, const float *Xs_lo, int row_tiles, int splits,

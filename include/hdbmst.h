@@ -178,9 +178,9 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
  *    call clears what must start at zero itself.
  *  - Problems that need more scratch than the array holds return
  *    HDBMST_ERR_TOO_LARGE before any GPU work.  With dk the padded feature
- *    count (round_up(d, 32) up to 64, round_up(d, 16) beyond), the need is
+ *    count (round_up(d, 32) up to 192, round_up(d, 16) beyond), the need is
  *    about c * dk * (round_up(n, 128) + round_up(m, 128)) bytes for the packed
- *    copies, c = 12 when d <= 64 (the tensor-core engine's extra low parts)
+ *    copies, c = 12 when d <= 192 (the tensor-core engine's extra low parts)
  *    and 8 otherwise (half that when Y is X), plus 4 bytes per query and at
  *    least 64 KiB for the neighbour candidates (128 KiB when k > 12).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine; it
@@ -197,15 +197,16 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
  * Distance-tile engine for the k-NN search (hdbmst_knn, hdbmst_knn_noalloc,
  * hdbmst_core_distances) and the Boruvka scan (hdbmst_mr_mst), process-wide,
  * not thread-safe:
- *   HDBMST_ENGINE_AUTO   tensor cores where supported (d <= 64), else FP32
- *                        FFMA (the default);
+ *   HDBMST_ENGINE_AUTO   tensor cores where supported (k-NN and core
+ *                        distances: d <= 192; Boruvka scan: d <= 64), else
+ *                        FP32 FFMA (the default);
  *   HDBMST_ENGINE_SIMT   FP32 FFMA register-blocked tile everywhere;
- *   HDBMST_ENGINE_TENSOR same as AUTO (tensor cores need d <= 64).
+ *   HDBMST_ENGINE_TENSOR same as AUTO.
  * The tensor-core tile ranks candidates with three-pass TF32 products
  * (tcgen05); both engines report distances and weights re-evaluated exactly
  * with dist() and prove the kept set against their own rounding bound, so
- * results are identical bit for bit whichever engine ran.  Returns the previous setting;
- * unknown values are ignored.
+ * results are identical bit for bit whichever engine ran.  Returns the
+ * previous setting; unknown values are ignored.
  */
 #define HDBMST_ENGINE_AUTO 0
 #define HDBMST_ENGINE_SIMT 1

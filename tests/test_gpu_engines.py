@@ -32,7 +32,10 @@ def both(h, fn):
 
 @pytest.mark.parametrize("n,m,d,k", [(1, 1, 1, 1), (5, 7, 3, 4), (129, 300, 17, 10),
                                      (1000, 1000, 61, 11), (777, 2049, 64, 16),
-                                     (300, 130, 33, 32), (2000, 1500, 48, 12)])
+                                     (300, 130, 33, 32), (2000, 1500, 48, 12),
+                                     # wide rows: A lo parts in shared memory
+                                     (500, 700, 65, 10), (300, 1000, 102, 10),
+                                     (257, 900, 192, 16), (200, 300, 150, 32)])
 def test_knn_engines_identical(h, n, m, d, k):
     X = workloads.small(n, d, seed=n + 3 * d, dup_frac=0.05)
     Y = workloads.small(m, d, seed=m + 5 * d, dup_frac=0.05)
@@ -63,3 +66,13 @@ def test_core_engines_identical_200k_sampled_rows(h):
     a, b = both(h, lambda: tuple(np_(t) for t in h.core_distances(dev(X), ms)))
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+def test_knn_engines_identical_200k_d192_sampled_rows(h):
+    """The 200k x 192 k-NN workload (wide rows on the tensor cores): both
+    engines give identical lists on every row."""
+    X, task = workloads.workload("knn_200k_d192")
+    Y = workloads.subset_columns(X, task["y_stride"])
+    k = task["k"]
+    (ai, ad), (bi, bd) = both(h, lambda: tuple(np_(t) for t in h.knn(dev(X), dev(Y), k)))
+    assert np.array_equal(ai, bi) and np.array_equal(ad, bd)

@@ -51,9 +51,10 @@ def test_noalloc_matches_knn_on_consecutive_calls():
     if not torch.cuda.is_available():
         pytest.fail("a CUDA device is required")
     H, L = _lib()
-    # A: 40 000 x 192 against itself fills most of the scratch with the packed
-    #    copy, so the rows go through the candidate lists in many small chunks.
-    XA = workloads.small(40000, 192, seed=21, dup_frac=0.01)
+    # A: 25 000 x 192 against itself fills most of the scratch with the packed
+    #    copies (58 MB of the 64 MiB), so the rows go through the candidate
+    #    lists in many small chunks.
+    XA = workloads.small(25000, 192, seed=21, dup_frac=0.01)
     # B: the 1 416 x 102 section against every 5th point.
     XB, task = workloads.workload("knn_1416_d102")
     YB = workloads.subset_columns(XB, task["y_stride"])
@@ -72,7 +73,7 @@ def test_noalloc_matches_knn_on_consecutive_calls():
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    """Checked on the host before any GPU work: 100 000 x 192 needs about 150 MB."""
+    """Checked on the host before any GPU work: 100 000 x 192 needs about 230 MB."""
     H, L = _lib()
     vp = ctypes.c_void_p
     st = L.hdbmst_knn_noalloc(vp(256), 100000, 100000, vp(256), 100000, 100000, 192, 10,
