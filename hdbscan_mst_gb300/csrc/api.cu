@@ -385,9 +385,11 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     b.Xs_lo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xa_hi = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xa_lo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
-    b.col_core = c.take<float>(n);
+    // column arrays in grouped order, padded to n_pad: the tensor scan
+    // prefetches them a whole tile at a time (padding entries never rank)
+    b.col_core = c.take<float>(p.n_pad);
     b.col_norm = c.take<float>(p.n_pad);
-    b.perm = c.take<int>(n);
+    b.perm = c.take<int>(p.n_pad);
     b.col_comp = c.take<int>(n);
     b.start = c.take<int>(n);
     b.act_start = c.take<int>(n);

@@ -133,9 +133,9 @@ struct ScanArgs {
     // columns: all points grouped by component
     const float *Xs;        // [dk][ldx] feature-major
     int64_t ldx;
-    const int *col_orig;    // [n] point index of each column
+    const int *col_orig;    // [ldx] point index of each column (entries past n unused)
     const float *col_norm;  // [ldx] |b|^2, +inf past the last point
-    const float *col_core;  // [n]
+    const float *col_core;  // [ldx] (entries past n unused)
     const int *col_comp;    // [n]
     const int *comp_start;  // [n] first column of each component label
     const int *comp_size;   // [n] columns of each component label

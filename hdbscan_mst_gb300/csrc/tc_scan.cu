@@ -43,7 +43,10 @@ struct TcScanParams {
 
 __shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
-__shared__ float4 s_cnorm[kEpiWarps][2][kTileCols / 4];  // per warp: two tiles' column norms
+// per warp, two tiles: the columns' norms, core distances and point indices
+__shared__ float4 s_cnorm[kEpiWarps][2][kTileCols / 4];
+__shared__ float s_ccore[kEpiWarps][2][kTileCols];
+__shared__ int s_corig[kEpiWarps][2][kTileCols];
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
                                             float &dropped) {
@@ -118,8 +121,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
 
         const auto prefetch = [&](int col0, int buf) {
-            if (lane < kTileCols / 4)
+            static_assert(kTileCols == 64, "one 16-byte copy per lane and array half");
+            if (lane < 16) {
                 cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
+                cp_async16(&s_corig[warp][buf][lane * 4], a.col_orig + col0 + lane * 4);
+            } else {
+                cp_async16(&s_ccore[warp][buf][(lane - 16) * 4], a.col_core + col0 + (lane - 16) * 4);
+            }
         };
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
@@ -164,12 +172,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                             mask &= mask - 1;
                             const int col = cb0 + j;
                             if (col >= a.n) break;
-                            const float cbc = __ldg(a.col_core + col);
+                            const float cbc = s_ccore[warp][buf][cc * 32 + j];
                             const float vv = fmaxf(
                                 fmaxf(pick32(v, j), __fsub_rn(__fmul_rn(cbc, cbc), na)), ra);
                             const unsigned long long key =
                                 (static_cast<unsigned long long>(float_order(vv)) << 32) |
-                                static_cast<unsigned>(__ldg(a.col_orig + col));
+                                static_cast<unsigned>(s_corig[warp][buf][cc * 32 + j]);
                             keep_insert(keys, key, dropped);
                         }
                         s_row_thr[group][row] = key_v(keys[kKeep - 1]);
