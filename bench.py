@@ -228,6 +228,7 @@ def run_gpu(args):
     barrier(dist, device)
     launches = H.launch_count() - launches0
     rounds = H.last_mst_rounds()
+    core_exact_rows = H.last_knn_exact_rows()
 
     # ---- the same K steps again with an event pair around every kernel
     # launch: per-kernel times for the breakdown and the roofline
@@ -265,6 +266,7 @@ def run_gpu(args):
         H.knn(Xkd, Ykd, tk["k"])
     torch.cuda.synchronize(device)
     kt = timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
+    knn_exact_rows = H.last_knn_exact_rows()
     H.profile_enable(True)
     H.profile_read()
     timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
@@ -339,6 +341,7 @@ def run_gpu(args):
         "profiled_ms_per_step": round(sum(prof_times) / args.steps, 3),
         "step_ms": {"min": round(min(times), 3), "median": round(statistics.median(times), 3),
                     "max": round(max(times), 3)},
+        "core_exact_rows": core_exact_rows,
         "boruvka_rounds": [{"scanned": a, "scanned_frac": round(a / n, 4), "edges": e,
                             "exact_rows": x} for a, e, x in rounds],
         "gpu_launches": launches,
@@ -349,6 +352,7 @@ def run_gpu(args):
         "knn": None if args.skip_knn else {"metric": "exact k-NN rows/s", "workload": KNN_TEXT,
                 "value": round(ws * Xk.shape[1] * args.steps / (k_total / 1e3), 1),
                 "unit": "rows/s", "ms_per_step": round(k_total / args.steps, 3),
+                "exact_rows": knn_exact_rows,
                 "roofline": knn_roof},
     }
     if not args.no_cpu_baseline:

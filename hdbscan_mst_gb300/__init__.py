@@ -94,6 +94,7 @@ def _load():
     L.hdbmst_set_engine.argtypes = [i32]
     L.hdbmst_set_engine.restype = i32
     L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
+    L.hdbmst_last_knn_exact_rows.restype = ctypes.c_int64
     _lib = L
     return L
 
@@ -295,6 +296,12 @@ def last_mst_rounds() -> list[tuple[int, int, int]]:
     x = (ctypes.c_int64 * 64)()
     r = L.hdbmst_last_mst_rounds(a, e, x, 64)
     return [(int(a[i]), int(e[i]), int(x[i])) for i in range(min(r, 64))]
+
+
+def last_knn_exact_rows() -> int:
+    """Rows of the last k-NN / core-distance call that the rounding proof left
+    open and that were searched exactly over all points."""
+    return int(_load().hdbmst_last_knn_exact_rows())
 
 
 def profile_read() -> dict:

@@ -40,6 +40,8 @@ bool use_tensor_scan(int dk) {
 
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
 std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
+// rows of the last k-NN / core-distance call searched exactly
+int64_t g_knn_exact_rows = 0;
 
 const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
@@ -75,6 +77,14 @@ void after(int id, cudaStream_t s) {
 }
 
 cudaError_t g_last_cuda = cudaSuccess;
+
+}  // namespace
+
+void hdbmst::count_extra_launches(int n) {
+    g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed);
+}
+
+namespace {
 
 hdbmst_status cuda_fail(cudaError_t e) {
     g_last_cuda = e;
@@ -323,10 +333,20 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     xa.out_idx = out_idx;
     xa.out_dist = out_dist;
     xa.out_core = out_core;
+    // queued rows search their columns in up to 32 ranges of >= 4096 columns,
+    // partial lists in the (now idle) candidate-list buffer
+    xa.part = reinterpret_cast<unsigned long long *>(b.part_key);
+    xa.splits = std::max(1, std::min(32, p.m / 4096));
+    {
+        const int64_t slots = static_cast<int64_t>(kMaxSplits) * p.chunk_rows * p.KP / 2;
+        xa.rows_cap = static_cast<int>(
+            std::min<int64_t>(8192, slots / (static_cast<int64_t>(xa.splits) * p.KP)));
+    }
     LAUNCH(K_KNN_EXACT, s, launch_knn_exact(p.KP, xa, 2 * sm_count(), s));
     DevStatus h{};
     hdbmst_status st = read_status(b.st, h, s);
     if (st != HDBMST_OK) return st;
+    g_knn_exact_rows = h.fb_count;
     if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
     if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
     return HDBMST_OK;
@@ -815,6 +835,8 @@ int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
     }
     return r;
 }
+
+int64_t hdbmst_last_knn_exact_rows(void) { return g_knn_exact_rows; }
 
 const char *hdbmst_profile_kernel_name(int i) {
     return (i >= 0 && i < K_COUNT) ? kKernelNames[i] : "";

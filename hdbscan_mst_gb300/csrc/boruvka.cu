@@ -384,7 +384,11 @@ cudaError_t launch_group(int n, int n_pad, const int *comp, const float *core, c
                                                     col_norm, act_idx);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (n_pad > n) pad_norms_kernel<<<blocks_for(n_pad - n, 256), 256, 0, s>>>(n, n_pad, col_norm);
+    count_extra_launches(1);
+    if (n_pad > n) {
+        pad_norms_kernel<<<blocks_for(n_pad - n, 256), 256, 0, s>>>(n, n_pad, col_norm);
+        count_extra_launches(1);
+    }
     return cudaGetLastError();
 }
 

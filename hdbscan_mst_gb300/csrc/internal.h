@@ -84,8 +84,19 @@ struct KnnExactArgs {
     int32_t *out_idx;
     float *out_dist;
     float *out_core;
+    // the first rows_cap queued rows are searched with the columns split in
+    // `splits` ranges, partial lists in part[(f * splits + s) * KP ..]; any
+    // further rows one block per row
+    unsigned long long *part;
+    int splits, rows_cap;
 };
+// Exact search of the queued rows: split pass, merge, then the rows beyond
+// rows_cap.  blocks: the persistent grid of the split pass and the tail.
 cudaError_t launch_knn_exact(int KP, const KnnExactArgs &a, int blocks, cudaStream_t s);
+
+// Launch accounting (api.cu): a wrapper that starts more than one kernel
+// reports the kernels beyond the first, which the caller's count covers.
+void count_extra_launches(int n);
 
 // ---------------------------------------------------------------- boruvka.cu
 cudaError_t launch_mst_init(int n, int *comp, unsigned long long *cand, unsigned long long *ck64,

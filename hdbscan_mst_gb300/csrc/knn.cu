@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(256) knn_exact_kernel(const KnnExactArgs a) {
     __shared__ unsigned long long wmin[8];
     const int tid = threadIdx.x;
     const int count = *a.fb_count;
-    for (int f = blockIdx.x; f < count; f += gridDim.x) {
+    for (int f = a.rows_cap + blockIdx.x; f < count; f += gridDim.x) {
         const int row = a.fb_rows[f];
         for (int q = tid; q < a.dk; q += 256) xrow[q] = a.Xp[static_cast<int64_t>(row) * a.dk + q];
         __syncthreads();
@@ -412,6 +412,102 @@ __global__ void __launch_bounds__(256) knn_exact_kernel(const KnnExactArgs a) {
     }
 }
 
+// Split pass of the exact search: item (f, s) is queued row f < rows_cap
+// against column range s of `splits`; a block keeps per thread the KP least
+// exact (dist, j) keys of its columns (fixed compare-and-swap sink) and writes
+// the k least of the block to the item's partial list.
+template <int KP>
+__global__ void __launch_bounds__(256) knn_exact_split_kernel(const KnnExactArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned long long *lists = reinterpret_cast<unsigned long long *>(smem_raw);  // [256][KP]
+    float *xrow = reinterpret_cast<float *>(lists + 256 * KP);                       // [dk]
+    __shared__ unsigned long long wmin[8];
+    const int tid = threadIdx.x;
+    const int rows = min(*a.fb_count, a.rows_cap);
+    const int span = (a.m + a.splits - 1) / a.splits;
+    for (int item = blockIdx.x; item < rows * a.splits; item += gridDim.x) {
+        const int f = item / a.splits, sp = item % a.splits;
+        const int row = a.fb_rows[f];
+        const int j0 = sp * span, j1 = min(a.m, j0 + span);
+        __syncthreads();  // xrow and lists of the previous item are consumed
+        for (int q = tid; q < a.dk; q += 256) xrow[q] = a.Xp[static_cast<int64_t>(row) * a.dk + q];
+        __syncthreads();
+        unsigned long long L[KP];
+#pragma unroll
+        for (int p = 0; p < KP; ++p) L[p] = kNoKey;
+        for (int j = j0 + tid; j < j1; j += 256) {
+            const float4 *yp = reinterpret_cast<const float4 *>(a.Yp + static_cast<int64_t>(j) * a.dk);
+            const float4 *xp = reinterpret_cast<const float4 *>(xrow);
+            float acc = 0.f;
+            for (int q = 0; q < a.dk / 4; ++q) {
+                const float4 x = xp[q], y = __ldg(yp + q);
+                acc = sqdiff_fma(x.x, y.x, acc);
+                acc = sqdiff_fma(x.y, y.y, acc);
+                acc = sqdiff_fma(x.z, y.z, acc);
+                acc = sqdiff_fma(x.w, y.w, acc);
+            }
+            const unsigned long long key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+            if (key < L[KP - 1]) {
+                L[KP - 1] = key;
+#pragma unroll
+                for (int p = KP - 1; p > 0; --p) {
+                    const unsigned long long lo = min(L[p - 1], L[p]);
+                    const unsigned long long hi = max(L[p - 1], L[p]);
+                    L[p - 1] = lo;
+                    L[p] = hi;
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < KP; ++p) lists[tid * KP + p] = L[p];
+        __syncthreads();
+        // k rounds of a block-wide minimum over the list heads (keys are unique)
+        int h = 0;
+        unsigned long long *out = a.part + static_cast<int64_t>(item) * KP;
+        for (int p = 0; p < a.k; ++p) {
+            const unsigned long long mine = h < KP ? lists[tid * KP + h] : kNoKey;
+            unsigned long long m = mine;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if ((tid & 31) == 0) wmin[tid >> 5] = m;
+            __syncthreads();
+            m = wmin[0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m = min(m, wmin[w]);
+            if (mine == m && m != kNoKey) ++h;
+            if (tid == 0) out[p] = m;
+            __syncthreads();
+        }
+    }
+}
+
+// Merge pass: one warp per queued row f < rows_cap; lane s walks the sorted
+// partial list of split s, and k rounds of a warp minimum pick the row's k
+// least keys.
+template <int KP>
+__global__ void __launch_bounds__(128) knn_exact_merge_kernel(const KnnExactArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int f = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int rows = min(*a.fb_count, a.rows_cap);
+    if (f >= rows) return;
+    const int row = a.fb_rows[f];
+    const unsigned long long *lst = a.part + (static_cast<int64_t>(f) * a.splits + lane) * KP;
+    int h = 0;
+    for (int p = 0; p < a.k; ++p) {
+        const unsigned long long mine = (lane < a.splits && h < a.k) ? lst[h] : kNoKey;
+        unsigned long long m = mine;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (mine == m && m != kNoKey) ++h;
+        if (lane == 0) {
+            const int64_t o = static_cast<int64_t>(row) * a.k + p;
+            a.out_idx[o] = static_cast<int32_t>(key_i(m));
+            a.out_dist[o] = key_w(m);
+            if (a.out_core && p == a.core_rank - 1) a.out_core[row] = key_w(m);
+        }
+    }
+}
+
 template <int KP>
 cudaError_t tile_launch(const KnnTileArgs &a, int row_tiles, int splits, cudaStream_t s) {
     const size_t smem = sizeof(TileSmem<KP>);
@@ -430,6 +526,14 @@ cudaError_t exact_launch(const KnnExactArgs &a, int blocks, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(knn_exact_split_kernel<KP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (a.rows_cap > 0) {
+        knn_exact_split_kernel<KP><<<blocks, 256, smem, s>>>(a);
+        knn_exact_merge_kernel<KP><<<(a.rows_cap + 3) / 4, 128, 0, s>>>(a);
+        count_extra_launches(2);
+    }
     knn_exact_kernel<KP><<<blocks, 256, smem, s>>>(a);
     return cudaGetLastError();
 }

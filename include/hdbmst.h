@@ -242,6 +242,14 @@ int hdbmst_profile_read(double *total_ms, int64_t *launches, int max_kernels);
 const char *hdbmst_profile_kernel_name(int i);
 
 /*
+ * Rows of the most recent hdbmst_knn / hdbmst_knn_noalloc /
+ * hdbmst_core_distances call in this process whose candidate set the rounding
+ * proof could not close, so that they were searched exactly over all points
+ * (host-side, not thread-safe).
+ */
+int64_t hdbmst_last_knn_exact_rows(void);
+
+/*
  * Rounds of the most recent hdbmst_mr_mst call in this process: returns the
  * number of Boruvka rounds; for each of the first max_rounds rounds writes
  * the number of points scanned against all others (active[i]), the tree
