@@ -55,8 +55,10 @@ def load(path: str) -> dict:
         key = key.strip()
         if key == "name":
             g["name"] = rest.strip()
-        elif key in ("dim", "min_samples", "knn_k"):
+        elif key in ("dim", "min_samples", "knn_k", "min_cluster_size"):
             g[key] = int(rest)
+        elif key == "labels":
+            g["labels"] = np.array([int(v) for v in rest.split()], dtype=np.int64)
         elif key == "point":
             g["points"].append(_values(rest))
         elif key == "core":

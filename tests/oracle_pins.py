@@ -222,3 +222,95 @@ def pin_invariants(o):
 
 
 ALL_PINS = (pin_golden, pin_kruskal, pin_scipy_emst, pin_bruteforce_knn, pin_invariants)
+
+
+# ---------------------------------------------------------------------------
+# pins of the back half (oracle/hierarchy.py): labels from the spanning tree
+
+def _partition_equal(a, b):
+    """Same clusters and same noise, up to the numbering of the clusters."""
+    a = np.asarray(a)
+    b = np.asarray(b)
+    if a.shape != b.shape or not np.array_equal(a < 0, b < 0):
+        return False
+    pairs = set(zip(a[a >= 0].tolist(), b[b >= 0].tolist()))
+    return (len(pairs) == len(set(p[0] for p in pairs)) == len(set(p[1] for p in pairs)))
+
+
+def pin_hierarchy_golden(o, h):
+    """Hand-worked labels (tests/golden, the fixtures with a labels line)."""
+    for g in goldens.all_fixtures():
+        if "labels" not in g:
+            continue
+        core = o.core_distances(g["X"], g["min_samples"])
+        lo, hi, w = o.prim_mst(g["X"], core)
+        got = h.hdbscan_labels(g["X"].shape[1], lo, hi, w, g["min_cluster_size"])
+        assert np.array_equal(got, g["labels"]), (g["name"], got, g["labels"])
+
+
+def pin_hierarchy_sklearn(o, h):
+    """scikit-learn's HDBSCAN (the page's upstream) on random blobs.
+
+    With min_samples = 1 every weight is a distinct distance, the spanning tree
+    is unique, and the partitions must be equal.  With min_samples > 1 most
+    points join the tree at exactly their core distance, often through one of
+    several equal edges, and the two programs may place such a point in a
+    cluster or in noise differently (page "HDBSCAN", "A lesson about tests:
+    ties"): there, after matching each cluster to the one it overlaps most, at
+    most 3% of the points may disagree."""
+    try:
+        from sklearn.cluster import HDBSCAN
+    except ImportError:  # pragma: no cover - not installed on every machine
+        return
+    rng = np.random.default_rng(17)
+    for n, d, k, ms, mcs in ((300, 2, 4, 1, 10), (250, 3, 3, 1, 5), (600, 8, 6, 1, 20),
+                             (300, 2, 4, 5, 10), (600, 8, 6, 10, 20), (400, 61, 5, 3, 15)):
+        means = rng.normal(0.0, 6.0, size=(k, d))
+        lab = rng.integers(0, k, size=n)
+        P = (means[lab] + rng.normal(size=(n, d)) * rng.uniform(0.5, 2.0, size=(k, 1))[lab])
+        P[: n // 20] = rng.uniform(P.min(0), P.max(0), size=(n // 20, d))
+        X = np.ascontiguousarray(P.astype(np.float32).T)
+        core = o.core_distances(X, ms)
+        lo, hi, w = o.prim_mst(X, core)
+        got = h.hdbscan_labels(n, lo, hi, w, mcs)
+        ref = HDBSCAN(min_cluster_size=mcs, min_samples=ms, copy=True).fit(
+            X.T.astype(np.float64)).labels_
+        if ms == 1:
+            assert _partition_equal(got, ref), ("sklearn", n, d, ms, mcs)
+            continue
+        assert len(set(got.tolist())) == len(set(ref.tolist())), ("cluster count", n, ms)
+        mapped = np.full(n, -1)
+        for c in set(got.tolist()) - {-1}:
+            vals, cnt = np.unique(ref[got == c], return_counts=True)
+            mapped[got == c] = vals[np.argmax(cnt)]
+        assert np.mean(mapped != ref) <= 0.03, ("sklearn", n, d, ms, mcs, np.mean(mapped != ref))
+
+
+def pin_hierarchy_invariants(o, h):
+    """Every cluster holds at least min_cluster_size points; clusters are
+    numbered by first appearance; an isolated far point is noise; a single
+    blob of exactly min_cluster_size points has no cluster (the root is never
+    selected)."""
+    rng = np.random.default_rng(23)
+    for n, d, ms, mcs in ((500, 4, 5, 12), (300, 2, 2, 6), (120, 6, 4, 30)):
+        P = rng.normal(size=(n, d)) * 0.3 + rng.integers(0, 4, size=(n, 1)) * 5.0
+        X = np.ascontiguousarray(P.astype(np.float32).T)
+        core = o.core_distances(X, ms)
+        lo, hi, w = o.prim_mst(X, core)
+        lab = h.hdbscan_labels(n, lo, hi, w, mcs)
+        ids = [v for v in lab.tolist() if v >= 0]
+        first = []
+        for v in ids:
+            if v not in first:
+                first.append(v)
+        assert first == list(range(len(first))), "numbering by first appearance"
+        for c in set(ids):
+            assert ids.count(c) >= mcs, "cluster below min_cluster_size"
+    X = np.array([[0.0, 0.1, 0.2, 0.3, 0.4, 100.0]], dtype=np.float32)
+    core = o.core_distances(X, 2)
+    lo, hi, w = o.prim_mst(X, core)
+    assert h.hdbscan_labels(6, lo, hi, w, 5).tolist() == [-1] * 6, "one blob: no cluster"
+    assert h.hdbscan_labels(6, lo, hi, w, 2)[5] == -1, "a far point is noise"
+
+
+HIERARCHY_PINS = (pin_hierarchy_golden, pin_hierarchy_sklearn, pin_hierarchy_invariants)

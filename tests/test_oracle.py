@@ -70,3 +70,48 @@ def test_oracle_rejects_bad_arguments():
         oracle.knn(X, X, 4)
     with pytest.raises(ValueError):
         oracle.core_distances(X, 4)
+
+
+# ---------------------------------------------------------------------------
+# the back half (oracle/hierarchy.py)
+
+def _hierarchy_from_source(src: str):
+    import types
+    mod = types.ModuleType("hierarchy_mutant")
+    exec(compile(src, "hierarchy_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("pin", oracle_pins.HIERARCHY_PINS, ids=lambda f: f.__name__)
+def test_hierarchy_pin(pin):
+    from oracle import hierarchy
+    pin(oracle.default(), hierarchy)
+
+
+HIERARCHY_MUTANTS = [
+    ("birth_at_zero", "            birth[child] = lam", "            birth[child] = 0.0"),
+    ("size_rule_strict", "if sa >= min_cluster_size and sb >= min_cluster_size:",
+     "if sa > min_cluster_size and sb > min_cluster_size:"),
+    ("root_selectable", "        if node == n:\n            continue\n", ""),
+    ("eom_inverted", "if below > stab[node]:", "if below < stab[node]:"),
+    ("lambda_is_distance", "return 1.0 / d if d > 0.0 else math.inf", "return d"),
+    ("small_side_continues", "            relabel[b] = me\n            queue.append(b)",
+     "            relabel[a] = me\n            queue.append(a)"),
+    ("root_points_not_noise", "while c is not None and c not in chosen:",
+     "while c is not None and c not in chosen and c != n:"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", HIERARCHY_MUTANTS, ids=[m[0] for m in HIERARCHY_MUTANTS])
+def test_hierarchy_pins_catch_planted_mistake(name, old, new):
+    from oracle import hierarchy
+    src = open(hierarchy.__file__).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutant = _hierarchy_from_source(src.replace(old, new))
+    failed = []
+    for pin in oracle_pins.HIERARCHY_PINS:
+        try:
+            pin(oracle.default(), mutant)
+        except Exception:  # an assertion, or the mutant breaking outright
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches {name}"
