@@ -95,6 +95,8 @@ def _load():
     L.hdbmst_set_engine.restype = i32
     L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
     L.hdbmst_last_knn_exact_rows.restype = ctypes.c_int64
+    L.hdbmst_hdbscan_labels.argtypes = [vp, vp, i64, i32, vp]
+    L.hdbmst_hdbscan_labels.restype = i32
     _lib = L
     return L
 
@@ -263,6 +265,44 @@ def hdbscan_mst(X, min_samples: int, *, shortcuts: bool = True):
     else:
         edges, w = mr_mst(X, core)
     return _out(core, host), _out(edges, host), _out(w, host)
+
+
+def hdbscan_labels(edges, w, min_cluster_size: int):
+    """HDBSCAN labels from a spanning tree (``hdbmst_hdbscan_labels``, host).
+
+    ``edges [n-1, 2]`` int32 and ``w [n-1]`` float32 as ``mr_mst`` returns them
+    (device tensors are copied to the host); returns host ``labels [n]`` int32
+    (clusters 0, 1, ... by smallest point index, -1 for noise)."""
+    import numpy as np
+    E = np.ascontiguousarray(_host_array(edges), dtype=np.int32).reshape(-1, 2)
+    W = np.ascontiguousarray(_host_array(w), dtype=np.float32).reshape(-1)
+    if E.shape[0] != W.shape[0]:
+        raise ValueError("edges and w disagree in length")
+    n = E.shape[0] + 1
+    labels = np.empty(n, dtype=np.int32)
+    st = _load().hdbmst_hdbscan_labels(E.ctypes.data, W.ctypes.data, n, int(min_cluster_size),
+                                       labels.ctypes.data)
+    _check(st, "hdbmst_hdbscan_labels")
+    return labels
+
+
+def hdbscan(X, min_samples: int, min_cluster_size: int):
+    """The whole method: core distances and the MR-MST on the GPU, labels on
+    the host.  Returns host ``(labels [n], core [n], edges [n-1, 2], w [n-1])``."""
+    core, edges, w = hdbscan_mst(X, min_samples)
+    core, edges, w = (_host_array(t) for t in (core, edges, w))
+    if edges.shape[0] == 0:
+        import numpy as np
+        return np.full(core.shape[0], -1, dtype=np.int32), core, edges, w
+    return hdbscan_labels(edges, w, min_cluster_size), core, edges, w
+
+
+def _host_array(t):
+    """A numpy view or copy of a numpy array or a (CPU or CUDA) tensor."""
+    import numpy as np
+    if isinstance(t, np.ndarray):
+        return t
+    return t.detach().cpu().numpy()
 
 
 # ---------------------------------------------------------------- instrumentation

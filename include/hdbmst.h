@@ -194,6 +194,30 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
                                  float *out_dist, hdbmst_stream stream);
 
 /*
+ * HDBSCAN labels from the mutual-reachability minimum spanning tree, on the
+ * HOST (page "HDBSCAN", gpu/hdbscan, "The algorithm on the device": the
+ * hierarchy, its condensed tree and the excess-of-mass selection run on the
+ * host; the upstream sorter runs scikit-learn's HDBSCAN, whose definitions
+ * are followed).  Single-linkage merge tree of the edges in (w, lo, hi)
+ * order, condensed tree for min_cluster_size, stabilities, excess of mass
+ * without a single-cluster result, then each point's nearest selected
+ * cluster.
+ *
+ *   edges  [n-1][2] int32 (lo, hi) and w [n-1] float32, HOST memory, as
+ *          hdbmst_mr_mst writes them (copy them to the host first);
+ *   n      points; min_cluster_size >= 2;
+ *   labels [n] int32 out, HOST memory: cluster numbers 0, 1, ... in ascending
+ *          order of each cluster's smallest point index, -1 for noise.
+ *
+ * Linear in n, single-threaded; no CUDA call, no GPU needed.  Errors:
+ * ERR_ARG (sizes, NULL pointers, an index out of range, or edges that do not
+ * form a spanning tree), ERR_NONFINITE (a weight that is negative, NaN or
+ * infinite).  n = 1 gives one noise point.
+ */
+hdbmst_status hdbmst_hdbscan_labels(const int32_t *edges, const float *w, int64_t n,
+                                    int min_cluster_size, int32_t *labels);
+
+/*
  * Distance-tile engine for the k-NN search (hdbmst_knn, hdbmst_knn_noalloc,
  * hdbmst_core_distances) and the Boruvka scan (hdbmst_mr_mst), process-wide,
  * not thread-safe:

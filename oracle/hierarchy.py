@@ -28,6 +28,7 @@ choices made explicit:
 from __future__ import annotations
 
 import math
+from collections import deque
 
 import numpy as np
 
@@ -81,9 +82,9 @@ def condense(n, tree, min_cluster_size):
         return first[node - n], second[node - n]
 
     def leaves(node):
-        out, queue = [], [node]
+        out, queue = [], deque([node])
         while queue:
-            x = queue.pop(0)
+            x = queue.popleft()
             if x < n:
                 out.append(x)
             else:
@@ -93,9 +94,9 @@ def condense(n, tree, min_cluster_size):
     relabel = {root: n}
     next_label = n + 1
     entries = []
-    queue = [root]
+    queue = deque([root])
     while queue:
-        node = queue.pop(0)
+        node = queue.popleft()
         if node < n:
             continue
         a, b = children(node)
