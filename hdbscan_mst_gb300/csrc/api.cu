@@ -194,10 +194,17 @@ KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
     return p;
 }
 
+// Spatial order of the tensor-core k-NN (order.cu): 128 pivots, used when the
+// column set has at least this many points (below it the sweep is short and
+// the order buys nothing).
+constexpr int kSpatialPivots = 128;
+constexpr int kSpatialMinCols = 16384;
+
 struct KnnBufs {
     float *Xf, *Xp, *Xlo, *xnorm, *Yf, *Yp, *Ylo, *ynorm;
     float *part_key;
     int *part_idx;
+    SpatialOrder order;  // pointers null when not carved
     int *fb_rows;
     DevStatus *st;
     int32_t *list_idx;  // core distances without caller lists
@@ -221,6 +228,25 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
         b.Yp = c.take<float>(static_cast<size_t>(p.dk) * p.m_pad);
         b.Ylo = lo ? c.take<float>(static_cast<size_t>(p.dk) * p.m_pad) : nullptr;
         b.ynorm = c.take<float>(p.m_pad);
+    }
+    b.order = SpatialOrder{};
+    if (lo) {
+        SpatialOrder &o = b.order;
+        o.pivots = kSpatialPivots;
+        o.cellY = c.take<int>(p.m_pad);
+        o.permY = c.take<int>(p.m_pad);
+        o.startY = c.take<int>(kSpatialPivots + 1);
+        if (p.alias) {
+            o.cellX = o.cellY;
+            o.permX = o.permY;
+            o.startX = o.startY;
+        } else {
+            o.cellX = c.take<int>(p.n_pad);
+            o.permX = c.take<int>(p.n_pad);
+            o.startX = c.take<int>(kSpatialPivots + 1);
+        }
+        o.counters = c.take<int>(4 * kSpatialPivots);
+        o.tile_start = c.take<int>(p.n_pad / kBM);
     }
     const size_t part = static_cast<size_t>(kMaxSplits) * p.chunk_rows * p.KP;
     b.part_key = c.take<float>(part);
@@ -253,17 +279,24 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
                       float *out_core, int core_rank, cudaStream_t s) {
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
     const bool tensor = use_tensor(p.dk) && b.Xlo != nullptr;
+    // (not for wide rows: that tile waits on its operand stream, not on the
+    // selection, and the order's gathers cost more than they save there)
+    const bool spatial = tensor && b.order.permY && p.m >= kSpatialMinCols && p.dk <= 64;
+    const int *permX = spatial ? b.order.permX : nullptr;
+    const int *permY = spatial ? b.order.permY : nullptr;
+    if (spatial)
+        LAUNCH(K_PACK, s, launch_spatial_order(b.order, X, ldx, p.n, Y, ldy, p.m, p.alias, p.d, s));
     if (p.alias) {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
                                       b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
-                                      &b.st->nbmax_bits, s));
+                                      &b.st->nbmax_bits, s, permX));
     } else {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
                                       b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
-                                      nullptr, s));
+                                      nullptr, s, permX));
         LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
                                       b.Yp, tensor ? b.Ylo : nullptr, b.ynorm, &b.st->status,
-                                      &b.st->nbmax_bits, s));
+                                      &b.st->nbmax_bits, s, permY));
     }
     const int slots = (tensor ? 1 : 2) * sm_count();
     for (int base = 0; base < p.n; base += p.chunk_rows) {
@@ -291,6 +324,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.Yp = b.Yp;
         ta.m = p.m;
         ta.status = &b.st->status;
+        ta.tile_start = spatial ? b.order.tile_start : nullptr;
         if (tensor) {
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
                                                 row_tiles, S, s));
@@ -319,6 +353,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.out_core = out_core;
         ra.fb_count = &b.st->fb_count;
         ra.fb_rows = b.fb_rows;
+        ra.permX = permX;
+        ra.permY = permY;
         LAUNCH(K_KNN_REFINE, s, launch_knn_refine(p.KP, ra, rows, s));
     }
     KnnExactArgs xa{};
@@ -336,6 +372,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     // queued rows search their columns in up to 32 ranges of >= 4096 columns,
     // partial lists in the (now idle) candidate-list buffer
     xa.part = reinterpret_cast<unsigned long long *>(b.part_key);
+    xa.permX = permX;
+    xa.permY = permY;
     xa.splits = std::max(1, std::min(32, p.m / 4096));
     {
         const int64_t slots = static_cast<int64_t>(kMaxSplits) * p.chunk_rows * p.KP / 2;

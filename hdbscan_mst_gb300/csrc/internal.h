@@ -12,10 +12,26 @@ namespace hdbmst {
 // buffer Xf [dk][n_pad] and, if not nullptr, the point-major buffer
 // Xp [n_pad][dk] and its tensor-core low parts Xlo = x - tf32(x); write
 // norm[i] = sum of x^2 (+inf for padding points); flag non-finite values;
-// raise *nbmax_bits to the largest norm's bits.
+// raise *nbmax_bits to the largest norm's bits.  perm (nullable): position
+// i < n holds the caller's point perm[i].
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
-                        unsigned *nbmax_bits, cudaStream_t s);
+                        unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr);
+
+// ---------------------------------------------------------------- order.cu
+// Spatial order of the tensor-core k-NN (order.cu): nearest of `pivots`
+// column points, counting sort by it, each row tile's first column block.
+struct SpatialOrder {
+    int pivots;              // a multiple of 32
+    int *cellY, *cellX;      // [m], [n] (cellX unused when Y is X)
+    int *permY, *permX;      // sorted position -> caller index
+    int *startY, *startX;    // [pivots + 1]
+    int *counters;           // [4 pivots]
+    int *tile_start;         // [row tiles]: first 128-column block of the sweep
+};
+cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t ldx, int n,
+                                 const float *Y, int64_t ldy, int m, bool alias, int d,
+                                 cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
 
@@ -37,6 +53,8 @@ struct KnnTileArgs {
     const float *Xp, *Yp;  // point-major [.][dk] query rows and columns
     int m;                 // columns
     unsigned *status;      // device status word (timeouts)
+    const int *tile_start;  // nullable: per row tile (absolute), first 128-column block of
+                            // the sweep, which then wraps around (spatial order)
 };
 cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
                             cudaStream_t s);
@@ -72,6 +90,8 @@ struct KnnRefineArgs {
     float *out_core;
     int *fb_count;
     int *fb_rows;
+    // spatial order (nullable): caller index of packed row / column positions
+    const int *permX, *permY;
 };
 cudaError_t launch_knn_refine(int KP, const KnnRefineArgs &a, int rows, cudaStream_t s);
 
@@ -89,6 +109,7 @@ struct KnnExactArgs {
     // further rows one block per row
     unsigned long long *part;
     int splits, rows_cap;
+    const int *permX, *permY;  // as KnnRefineArgs
 };
 // Exact search of the queued rows: split pass, merge, then the rows beyond
 // rows_cap.  blocks: the persistent grid of the split pass and the tail.

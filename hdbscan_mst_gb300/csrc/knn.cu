@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
             acc = sqdiff_fma(x.z, y.z, acc);
             acc = sqdiff_fma(x.w, y.w, acc);
         }
-        key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+        // rank by the caller's column index (the packed order may be spatial)
+        key = key64(__fsqrt_rn(acc), static_cast<unsigned>(a.permY ? a.permY[j] : j));
     }
 
     // 3. Bitonic sort of the group's KP keys, ascending.
@@ -314,12 +315,13 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     }
 
     if (!active) return;
-    const int64_t o = static_cast<int64_t>(row) * a.k;
+    const int orow = a.permX ? a.permX[row] : row;  // the caller's row
+    const int64_t o = static_cast<int64_t>(orow) * a.k;
     if (gl < a.k) {
         a.out_idx[o + gl] = static_cast<int32_t>(key_i(key));
         a.out_dist[o + gl] = key_w(key);
     }
-    if (a.out_core && gl == a.core_rank - 1) a.out_core[row] = key_w(key);
+    if (a.out_core && gl == a.core_rank - 1) a.out_core[orow] = key_w(key);
 
     // 4. Proof that the kept set holds the exact top k.  Every dropped column
     //    z has computed t_z >= A (A = the KP-th kept t).  The ranking error of
@@ -373,7 +375,8 @@ __global__ void __launch_bounds__(256) knn_exact_kernel(const KnnExactArgs a) {
                 acc = sqdiff_fma(x.z, y.z, acc);
                 acc = sqdiff_fma(x.w, y.w, acc);
             }
-            const unsigned long long key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+            const unsigned long long key =
+                key64(__fsqrt_rn(acc), static_cast<unsigned>(a.permY ? a.permY[j] : j));
             if (key < L[KP - 1]) {
                 L[KP - 1] = key;
 #pragma unroll
@@ -402,10 +405,11 @@ __global__ void __launch_bounds__(256) knn_exact_kernel(const KnnExactArgs a) {
             for (int w = 1; w < 8; ++w) m = min(m, wmin[w]);
             if (mine == m && m != kNoKey) ++h;
             if (tid == 0) {
-                const int64_t o = static_cast<int64_t>(row) * a.k + p;
+                const int orow = a.permX ? a.permX[row] : row;
+                const int64_t o = static_cast<int64_t>(orow) * a.k + p;
                 a.out_idx[o] = static_cast<int32_t>(key_i(m));
                 a.out_dist[o] = key_w(m);
-                if (a.out_core && p == a.core_rank - 1) a.out_core[row] = key_w(m);
+                if (a.out_core && p == a.core_rank - 1) a.out_core[orow] = key_w(m);
             }
             __syncthreads();
         }
@@ -446,7 +450,8 @@ __global__ void __launch_bounds__(256) knn_exact_split_kernel(const KnnExactArgs
                 acc = sqdiff_fma(x.z, y.z, acc);
                 acc = sqdiff_fma(x.w, y.w, acc);
             }
-            const unsigned long long key = key64(__fsqrt_rn(acc), static_cast<unsigned>(j));
+            const unsigned long long key =
+                key64(__fsqrt_rn(acc), static_cast<unsigned>(a.permY ? a.permY[j] : j));
             if (key < L[KP - 1]) {
                 L[KP - 1] = key;
 #pragma unroll
@@ -500,10 +505,11 @@ __global__ void __launch_bounds__(128) knn_exact_merge_kernel(const KnnExactArgs
         for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (mine == m && m != kNoKey) ++h;
         if (lane == 0) {
-            const int64_t o = static_cast<int64_t>(row) * a.k + p;
+            const int orow = a.permX ? a.permX[row] : row;
+            const int64_t o = static_cast<int64_t>(orow) * a.k + p;
             a.out_idx[o] = static_cast<int32_t>(key_i(m));
             a.out_dist[o] = key_w(m);
-            if (a.out_core && p == a.core_rank - 1) a.out_core[row] = key_w(m);
+            if (a.out_core && p == a.core_rank - 1) a.out_core[orow] = key_w(m);
         }
     }
 }

@@ -25,10 +25,12 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    float *__restrict__ Xlo,
                                                    float *__restrict__ norm,
                                                    unsigned *__restrict__ status,
-                                                   unsigned *__restrict__ nbmax_bits) {
+                                                   unsigned *__restrict__ nbmax_bits,
+                                                   const int *__restrict__ perm) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool inside = i < n_pad;
     const bool valid = i < n;
+    const int src = (valid && perm) ? perm[i] : i;
     float acc = 0.f;
     bool finite = true;
     if (inside) {
@@ -37,7 +39,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int ff = f + q;
-                v[q] = (valid && ff < d) ? X[static_cast<int64_t>(ff) * ld + i] : 0.f;
+                v[q] = (valid && ff < d) ? X[static_cast<int64_t>(ff) * ld + src] : 0.f;
                 finite = finite && isfinite(v[q]);
                 Xf[static_cast<int64_t>(ff) * n_pad + i] = v[q];
                 acc = __fmaf_rn(v[q], v[q], acc);
@@ -79,10 +81,10 @@ __global__ void check_core_kernel(const float *__restrict__ core, int n,
 
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
-                        unsigned *nbmax_bits, cudaStream_t s) {
+                        unsigned *nbmax_bits, cudaStream_t s, const int *perm) {
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
-                                       nbmax_bits);
+                                       nbmax_bits, perm);
     return cudaGetLastError();
 }
 

@@ -97,7 +97,11 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     const int r0 = a.row_base + row_tile * kRows;
     constexpr int kSub = kCols / kTileCols;  // pipeline tiles per 128-column tile
     const int ct_begin = split * a.tiles_per_split;
-    const TileSeq seq(ct_begin * kSub, min(ct_begin + a.tiles_per_split, a.col_tiles) * kSub, 0, 0);
+    TileSeq seq(ct_begin * kSub, min(ct_begin + a.tiles_per_split, a.col_tiles) * kSub, 0, 0);
+    if (a.tile_start) {  // spatial order: the sweep starts at the rows' own neighbourhood
+        seq.rot = a.tile_start[r0 / kRows] * kSub;
+        seq.wrap = a.col_tiles * kSub;
+    }
 
     for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
     tc_setup<kEpiWarps, kWide>(S);

@@ -113,9 +113,11 @@ struct PipeSmem {
     int abort;
 };
 
-// The column tiles of a CTA: [ct_begin, ct_end) without [skip_lo, skip_hi).
+// The column tiles of a CTA: [ct_begin, ct_end) without [skip_lo, skip_hi),
+// optionally rotated: position t maps to (t + rot) mod wrap (wrap > 0), so a
+// sweep can start anywhere and wrap around (rot and wrap even: whole blocks).
 struct TileSeq {
-    int ct_begin, n, s_lo, gap;
+    int ct_begin, n, s_lo, gap, rot = 0, wrap = 0;
     __device__ TileSeq(int begin, int end, int skip_lo, int skip_hi) {
         ct_begin = begin;
         s_lo = min(max(skip_lo, begin), end);
@@ -124,8 +126,13 @@ struct TileSeq {
         n = max(end - begin - gap, 0);
     }
     __device__ int at(int k) const {
-        const int t = ct_begin + k;
-        return t >= s_lo ? t + gap : t;
+        int t = ct_begin + k;
+        t = t >= s_lo ? t + gap : t;
+        if (wrap > 0) {
+            t += rot;
+            if (t >= wrap) t -= wrap;
+        }
+        return t;
     }
 };
 
