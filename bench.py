@@ -231,6 +231,7 @@ def run_gpu(args):
     launches = H.launch_count() - launches0
     rounds = H.last_mst_rounds()
     core_exact_rows = H.last_knn_exact_rows()
+    core_pairs = H.last_knn_tile_pairs()
 
     # ---- the same K steps again with an event pair around every kernel
     # launch: per-kernel times for the breakdown and the roofline
@@ -277,6 +278,7 @@ def run_gpu(args):
     torch.cuda.synchronize(device)
     kt = timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
     knn_exact_rows = H.last_knn_exact_rows()
+    knn_pairs = H.last_knn_tile_pairs()
     H.profile_enable(True)
     H.profile_read()
     timed(lambda: H.knn(Xkd, Ykd, tk["k"]))
@@ -298,35 +300,42 @@ def run_gpu(args):
     tf32_basis = ("measured bf16 burst x nominal tf32/bf16 (1.1/2.25)" if bf16 else
                   "fallback bf16 x nominal tf32/bf16 (1.1/2.25)")
 
-    def roofline(prof_, name, d_, pairs, tensor, workload=None):
-        """Dominant distance tile: algorithmic flops 2 d per pair over its launches."""
+    def roofline(prof_, name, d_, pairs, dense_pairs, tensor, workload=None):
+        """Dominant distance tile: algorithmic flops 2 d per (row, column) pair
+        the tile evaluated (column blocks the pivot bounds pruned are not
+        evaluated), over the tile's time per step (all its launches)."""
         if name not in prof_:
             return None
         tot_ms, nl = prof_[name]
-        avg_s = tot_ms / nl / 1e3
+        step_s = tot_ms / args.steps / 1e3
         flops = 2.0 * d_ * pairs
-        ach = flops / avg_s / 1e12
+        ach = flops / step_s / 1e12
+        common = {"avg_launch_ms": round(tot_ms / nl, 3), "launches_per_step": nl / args.steps,
+                  "ms_per_step": round(step_s * 1e3, 3), "flops_per_step": flops,
+                  "pairs_evaluated": int(pairs), "pairs_dense": int(dense_pairs),
+                  "evaluated_frac": round(pairs / dense_pairs, 4),
+                  "dense_equivalent_tflops": round(2.0 * d_ * dense_pairs / step_s / 1e12, 1)}
         if tensor:
             dk = (d_ + 31) // 32 * 32  # padded features: whole 32-feature slabs
-            issued = 3 * 2.0 * dk * pairs / avg_s / 1e12  # three TF32 passes on padded features
+            issued = 3 * 2.0 * dk * pairs / step_s / 1e12  # three TF32 passes on padded features
             return {"kernel": name, "engine": "tcgen05 3xTF32", "bound": "tensor",
                     "achieved": round(ach, 2), "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
                     "frac": round(ach / tf32_peak, 4), "traffic": traffic_for(name, workload),
-                    "peak_basis": tf32_basis, "avg_launch_ms": round(avg_s * 1e3, 3),
-                    "flops_per_launch": flops, "issued_tflops": round(issued, 1),
+                    "peak_basis": tf32_basis, "issued_tflops": round(issued, 1),
                     "issued_frac": round(issued / tf32_peak, 4),
-                    "fp32_alu_equiv_frac": round(ach / fp32_peak, 4)}
+                    "fp32_alu_equiv_frac": round(ach / fp32_peak, 4), **common}
         return {"kernel": name, "engine": "FP32 FFMA", "bound": "alu", "achieved": round(ach, 2),
                 "peak": round(fp32_peak, 2), "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
-                "traffic": None, "avg_launch_ms": round(avg_s * 1e3, 3),
+                "traffic": None,
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz",
-                "flops_per_launch": flops}
+                **common}
 
-    # core distances: every clip against every clip (one launch)
+    # core distances: every clip against every clip, pruned by the pivot bounds
     # the tensor-core tile serves d <= 192 (k-NN) in the default engine
-    main_roof = roofline(prof, "knn_tile", d, float(n) * n, d <= 192, args.workload)
-    knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], float(Xk.shape[1]) * Yk.shape[1],
-                        Xk.shape[0] <= 192, KNN_WORKLOAD if not args.skip_knn else None)
+    main_roof = roofline(prof, "knn_tile", d, core_pairs, float(n) * n, d <= 192, args.workload)
+    knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], knn_pairs,
+                        float(Xk.shape[1]) * Yk.shape[1], Xk.shape[0] <= 192,
+                        KNN_WORKLOAD if not args.skip_knn else None)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
                  for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
     line = {

@@ -95,6 +95,7 @@ def _load():
     L.hdbmst_set_engine.restype = i32
     L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
     L.hdbmst_last_knn_exact_rows.restype = ctypes.c_int64
+    L.hdbmst_last_knn_tile_pairs.restype = ctypes.c_int64
     L.hdbmst_hdbscan_labels.argtypes = [vp, vp, i64, i32, vp]
     L.hdbmst_hdbscan_labels.restype = i32
     _lib = L
@@ -342,6 +343,12 @@ def last_knn_exact_rows() -> int:
     """Rows of the last k-NN / core-distance call that the rounding proof left
     open and that were searched exactly over all points."""
     return int(_load().hdbmst_last_knn_exact_rows())
+
+
+def last_knn_tile_pairs() -> int:
+    """(row, column) pairs the distance tile of the last k-NN / core-distance
+    call evaluated, in whole 128 x 128 blocks (pruned blocks excluded)."""
+    return int(_load().hdbmst_last_knn_tile_pairs())
 
 
 def profile_read() -> dict:

@@ -42,12 +42,15 @@ bool use_tensor_scan(int dk) {
 std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
 // rows of the last k-NN / core-distance call searched exactly
 int64_t g_knn_exact_rows = 0;
+// (row, column) pairs the distance tile of the last k-NN / core-distance call
+// evaluated, in whole 128 x 128 blocks
+int64_t g_knn_tile_pairs = 0;
 
 const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
     "nbr_candidate", "active", "gather", "boruvka_scan", "boruvka_refine", "boruvka_exact",
     "comp_min", "hook",
-    "roots",  "relabel",    "sort_edges"};
+    "roots",  "relabel",    "sort_edges", "knn_prune"};
 
 cudaEvent_t take_event() {
     if (!g_pool.empty()) {
@@ -126,7 +129,8 @@ struct DevStatus {
     int fb_count;
     int act_count;
     int edge_count;
-    int pad[3];
+    int pad;
+    unsigned long long tile_blocks;  // 128 x 128 blocks the pruned k-NN tile evaluated
 };
 
 constexpr int kMaxSplits = 8;
@@ -173,10 +177,12 @@ struct KnnPlan {
     bool alias;
     int col_tiles;
     int chunk_rows;  // multiple of kBM
+    bool prune;      // carve the buffers of the pruned search (prune.cu)
 };
 
-KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
+KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias, bool prune = true) {
     KnnPlan p{};
+    p.prune = prune;
     p.n = static_cast<int>(n);
     p.m = static_cast<int>(m);
     p.d = d;
@@ -198,13 +204,16 @@ KnnPlan make_knn_plan(int64_t n, int64_t m, int d, int k, bool alias) {
 // column set has at least this many points (below it the sweep is short and
 // the order buys nothing).
 constexpr int kSpatialPivots = 128;
+constexpr int kSpatialBuckets = 64;  // distance buckets per pivot cell
 constexpr int kSpatialMinCols = 16384;
+static_assert(kSpatialPivots == kPrunePivots, "the pruned search bounds blocks by the order's pivots");
 
 struct KnnBufs {
     float *Xf, *Xp, *Xlo, *xnorm, *Yf, *Yp, *Ylo, *ynorm;
     float *part_key;
     int *part_idx;
     SpatialOrder order;  // pointers null when not carved
+    PruneBufs prune;     // pointers null when not carved
     int *fb_rows;
     DevStatus *st;
     int32_t *list_idx;  // core distances without caller lists
@@ -230,23 +239,46 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
         b.ynorm = c.take<float>(p.m_pad);
     }
     b.order = SpatialOrder{};
+    b.prune = PruneBufs{};
     if (lo) {
         SpatialOrder &o = b.order;
-        o.pivots = kSpatialPivots;
+        const int P = kSpatialPivots, NB = kSpatialPivots * kSpatialBuckets;
+        o.pivots = P;
+        o.buckets = kSpatialBuckets;
         o.cellY = c.take<int>(p.m_pad);
         o.permY = c.take<int>(p.m_pad);
-        o.startY = c.take<int>(kSpatialPivots + 1);
+        o.startY = c.take<int>(NB + 1);
+        o.dcellY = c.take<float>(p.m_pad);
+        o.pdY = p.prune ? c.take<float>(static_cast<size_t>(p.m_pad) * P) : nullptr;
         if (p.alias) {
             o.cellX = o.cellY;
             o.permX = o.permY;
             o.startX = o.startY;
+            o.dcellX = o.dcellY;
+            o.pdX = o.pdY;
         } else {
             o.cellX = c.take<int>(p.n_pad);
             o.permX = c.take<int>(p.n_pad);
-            o.startX = c.take<int>(kSpatialPivots + 1);
+            o.startX = c.take<int>(NB + 1);
+            o.dcellX = c.take<float>(p.n_pad);
+            o.pdX = p.prune ? c.take<float>(static_cast<size_t>(p.n_pad) * P) : nullptr;
         }
-        o.counters = c.take<int>(4 * kSpatialPivots);
+        o.counters = c.take<int>(spatial_counter_ints(P, kSpatialBuckets));
         o.tile_start = c.take<int>(p.n_pad / kBM);
+        if (p.prune) {
+            PruneBufs &q = b.prune;
+            const size_t tiles = static_cast<size_t>(p.chunk_rows / kBM);
+            q.pdSY = c.take<float>(static_cast<size_t>(p.m_pad) * P);
+            q.pdSX = p.alias ? q.pdSY : c.take<float>(static_cast<size_t>(p.n_pad) * P);
+            q.Lm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
+            q.Hm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
+            q.bcell = c.take<int>(p.col_tiles);
+            q.home_lo = c.take<int>(tiles);
+            q.home = c.take<int>(tiles * kHomeBlocks);
+            q.list = c.take<int>(tiles * p.col_tiles);
+            q.count = c.take<int>(tiles);
+            q.slabs = c.take<int>(tiles);
+        }
     }
     const size_t part = static_cast<size_t>(kMaxSplits) * p.chunk_rows * p.KP;
     b.part_key = c.take<float>(part);
@@ -298,14 +330,22 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
                                       b.Yp, tensor ? b.Ylo : nullptr, b.ynorm, &b.st->status,
                                       &b.st->nbmax_bits, s, permY));
     }
+    // pruned search: the spatial order's pivots bound the column blocks (prune.cu)
+    const bool prune = spatial && b.prune.list != nullptr;
+    const int nh = std::min(kHomeBlocks, p.col_tiles);
+    const int chunk_cap = (p.col_tiles + kPruneChunks - 1) / kPruneChunks;
+    if (prune)
+        LAUNCH(K_PRUNE, s, launch_prune_setup(b.order, b.prune, p.n, p.m, p.alias, p.col_tiles,
+                                               p.d, s));
     const int slots = (tensor ? 1 : 2) * sm_count();
     for (int base = 0; base < p.n; base += p.chunk_rows) {
         const int rows = std::min(p.chunk_rows, p.n - base);
         const int row_tiles = (rows + kBM - 1) / kBM;
-        const int S0 = tensor ? choose_splits_tc(row_tiles, p.col_tiles, slots)
+        const int S0 = prune ? 1 + kPruneChunks
+                     : tensor ? choose_splits_tc(row_tiles, p.col_tiles, slots)
                               : choose_splits(row_tiles, p.col_tiles, slots);
         const int tps = (p.col_tiles + S0 - 1) / S0;
-        const int S = (p.col_tiles + tps - 1) / tps;
+        const int S = prune ? S0 : (p.col_tiles + tps - 1) / tps;
         KnnTileArgs ta{};
         ta.Xf = b.Xf;
         ta.Yf = b.Yf;
@@ -325,7 +365,57 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.m = p.m;
         ta.status = &b.st->status;
         ta.tile_start = spatial ? b.order.tile_start : nullptr;
-        if (tensor) {
+        if (prune) {
+            // home pass: slab 0, the kHomeBlocks blocks around the tile's own bin
+            PruneHomeArgs ha{};
+            ha.o = &b.order;
+            ha.n = p.n;
+            ha.m = p.m;
+            ha.col_tiles = p.col_tiles;
+            ha.row_tile0 = base / kBM;
+            ha.row_tiles = row_tiles;
+            ha.alias = p.alias;
+            LAUNCH(K_PRUNE, s, launch_prune_home(ha, b.prune, s));
+            KnnTileArgs h = ta;
+            h.tile_start = nullptr;
+            h.blist = b.prune.home;
+            h.bcount = nullptr;
+            h.blist_count = nh;
+            h.blist_stride = kHomeBlocks;
+            h.chunk_cap = kHomeBlocks;
+            h.slab_base = 0;
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, h, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
+                                                row_tiles, 1, s));
+            // the blocks each row tile still needs, from the home pass's bounds
+            PruneListArgs pa{};
+            pa.part_key = b.part_key;
+            pa.part_idx = b.part_idx;
+            pa.chunk_rows_pad = p.chunk_rows;
+            pa.KP = p.KP;
+            pa.k = p.k;
+            pa.d = p.d;
+            pa.xnorm = b.xnorm;
+            pa.ynorm = b.ynorm;
+            pa.err_coef = tc::err_coef(p.d, p.dk);
+            pa.col_tiles = p.col_tiles;
+            pa.row_base = base;
+            pa.row_end = p.n;
+            pa.row_tiles = row_tiles;
+            pa.chunk_cap = chunk_cap;
+            pa.blocks_total = &b.st->tile_blocks;
+            LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
+            // second pass: slabs 1 .., in chunks of chunk_cap blocks
+            KnnTileArgs q = ta;
+            q.tile_start = nullptr;
+            q.blist = b.prune.list;
+            q.bcount = b.prune.count;
+            q.blist_stride = p.col_tiles;
+            q.chunk_cap = chunk_cap;
+            q.slab_base = 1;
+            q.seed = b.part_key;
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
+                                                row_tiles, kPruneChunks, s));
+        } else if (tensor) {
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
                                                 row_tiles, S, s));
         } else {
@@ -355,6 +445,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.fb_rows = b.fb_rows;
         ra.permX = permX;
         ra.permY = permY;
+        ra.tile_slabs = prune ? b.prune.slabs : nullptr;
         LAUNCH(K_KNN_REFINE, s, launch_knn_refine(p.KP, ra, rows, s));
     }
     KnnExactArgs xa{};
@@ -385,6 +476,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     hdbmst_status st = read_status(b.st, h, s);
     if (st != HDBMST_OK) return st;
     g_knn_exact_rows = h.fb_count;
+    g_knn_tile_pairs = prune ? static_cast<int64_t>(h.tile_blocks) * kBM * kBN
+                             : static_cast<int64_t>((p.n + kBM - 1) / kBM) * p.col_tiles * kBM * kBN;
     if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
     if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
     return HDBMST_OK;
@@ -506,7 +599,7 @@ void *noalloc_scratch() {
 // k-NN plan whose partial lists take what the fixed scratch leaves after the
 // packed copies; chunk_rows = 0 when even one 128-row chunk does not fit.
 KnnPlan make_knn_plan_fixed(int64_t n, int64_t m, int d, int k, bool alias, size_t capacity) {
-    KnnPlan p = make_knn_plan(n, m, d, k, alias);
+    KnnPlan p = make_knn_plan(n, m, d, k, alias, false);
     p.chunk_rows = kBM;
     Carver c(nullptr);
     KnnBufs b{};
@@ -875,6 +968,8 @@ int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
 }
 
 int64_t hdbmst_last_knn_exact_rows(void) { return g_knn_exact_rows; }
+
+int64_t hdbmst_last_knn_tile_pairs(void) { return g_knn_tile_pairs; }
 
 const char *hdbmst_profile_kernel_name(int i) {
     return (i >= 0 && i < K_COUNT) ? kKernelNames[i] : "";

@@ -20,18 +20,67 @@ cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int
 
 // ---------------------------------------------------------------- order.cu
 // Spatial order of the tensor-core k-NN (order.cu): nearest of `pivots`
-// column points, counting sort by it, each row tile's first column block.
+// column points, counting sort by (pivot, bucket of the distance to it), each
+// row tile's first column block.
 struct SpatialOrder {
     int pivots;              // a multiple of 32
-    int *cellY, *cellX;      // [m], [n] (cellX unused when Y is X)
+    int buckets;             // distance buckets per pivot cell
+    int *cellY, *cellX;      // [m], [n]: bin = cell * buckets + bucket (cellX = cellY when Y is X)
     int *permY, *permX;      // sorted position -> caller index
-    int *startY, *startX;    // [pivots + 1]
-    int *counters;           // [4 pivots]
+    int *startY, *startX;    // [pivots * buckets + 1]: first sorted position of each bin
+    int *counters;           // [spatial_counter_ints]
     int *tile_start;         // [row tiles]: first 128-column block of the sweep
+    float *dcellY, *dcellX;  // [m], [n]: distance to the own pivot, caller order
+    float *pdY, *pdX;        // nullable, [m][pivots], [n][pivots]: distances to all
+                             // pivots, caller order (the pruned search only)
 };
+inline int spatial_counter_ints(int pivots, int buckets) { return 4 * pivots * buckets + 2 * pivots; }
 cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t ldx, int n,
                                  const float *Y, int64_t ldy, int m, bool alias, int d,
                                  cudaStream_t s);
+
+// ---------------------------------------------------------------- prune.cu
+// Column blocks of the tensor-core k-NN that can hold none of a row tile's
+// nearest neighbours, bounded through the pivots of the spatial order.
+constexpr int kPrunePivots = 128;   // = SpatialOrder::pivots when pruning
+constexpr int kHomeBlocks = 3;      // blocks of the first pass per row tile
+constexpr int kPruneChunks = 4;     // CTAs per row tile in the second pass (at most)
+struct PruneBufs {
+    float *pdSY, *pdSX;   // [m_pad][P], [n_pad][P] pivot distances in sorted order
+    float *Lm, *Hm;       // [P][col_tiles]: per column block, least / largest pivot
+                          // distance of its points, widened by the distances' rounding bound
+    int *bcell;           // [col_tiles] pivot cell of each block's first point
+    int *home_lo;         // [chunk row tiles] first block of the home range
+    int *home;            // [chunk row tiles][kHomeBlocks] home lists
+    int *list;            // [chunk row tiles][col_tiles] blocks of the second pass
+    int *count;           // [chunk row tiles] entries of list
+    int *slabs;           // [chunk row tiles] partial-list slabs written (1 + chunks)
+};
+// Pivot distances into sorted order (dst[pos] = src[perm[pos]]) and the
+// column blocks' bounds.
+cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n, int m,
+                               bool alias, int col_tiles, int d, cudaStream_t s);
+struct PruneHomeArgs {
+    const SpatialOrder *o;
+    int n, m, col_tiles, row_tile0, row_tiles;  // row tiles of this chunk: row_tile0 ..
+    bool alias;
+};
+// Home range of every row tile of a chunk: the kHomeBlocks blocks around the
+// columns of the tile's own bin.
+cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaStream_t s);
+struct PruneListArgs {
+    const float *part_key;  // slab 0: the home pass's sorted lists
+    const int *part_idx;
+    int chunk_rows_pad, KP, k, d;
+    const float *xnorm, *ynorm;  // sorted order
+    double err_coef;             // the tile's ranking error bound
+    int col_tiles, row_base, row_end, row_tiles;
+    int chunk_cap;               // blocks per CTA of the second pass
+    unsigned long long *blocks_total;  // += blocks the tile evaluates (both passes)
+};
+// Upper bound of each row's k-th distance from its home list, the row tile's
+// hull per pivot, and the list of blocks that the hull cannot exclude.
+cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
 
@@ -55,6 +104,14 @@ struct KnnTileArgs {
     unsigned *status;      // device status word (timeouts)
     const int *tile_start;  // nullable: per row tile (absolute), first 128-column block of
                             // the sweep, which then wraps around (spatial order)
+    // block lists (tensor-core engine, pruned search): the CTA of row tile x
+    // (of the chunk) takes blocks blist[x * blist_stride ..], bcount[x] of
+    // them (or blist_count when bcount is null), in chunks of chunk_cap, chunk
+    // c = gridDim.y - 1 - blockIdx.y, and writes slab slab_base + c
+    const int *blist;
+    const int *bcount;
+    int blist_count, blist_stride, chunk_cap, slab_base;
+    const float *seed;  // nullable: sorted lists of slab 0 (their KP-th key: a first threshold)
 };
 cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
                             cudaStream_t s);
@@ -92,6 +149,7 @@ struct KnnRefineArgs {
     int *fb_rows;
     // spatial order (nullable): caller index of packed row / column positions
     const int *permX, *permY;
+    const int *tile_slabs;  // nullable: slabs written per row tile of the chunk (<= splits)
 };
 cudaError_t launch_knn_refine(int KP, const KnnRefineArgs &a, int rows, cudaStream_t s);
 
@@ -240,6 +298,7 @@ enum KernelId {
     K_ROOTS,
     K_RELABEL,
     K_SORT,
+    K_PRUNE,
     K_COUNT
 };
 

@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     // 1. Merge the sorted partial lists of the splits into the KP best by
     //    (t, index); one lane walks the list heads.
     float A = INFINITY;
+    const int slabs = (a.tile_slabs && active) ? min(a.splits, a.tile_slabs[local / kBM]) : a.splits;
     if (active && gl == 0) {
         int head[8];
 #pragma unroll
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
             int bj = INT_MAX, bs = -1;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
-                if (s < a.splits && head[s] < KP) {
+                if (s < slabs && head[s] < KP) {
                     const int64_t o = (static_cast<int64_t>(s) * a.chunk_rows_pad + local) * KP + head[s];
                     const float t = a.part_key[o];
                     const int j = a.part_idx[o];

@@ -1,0 +1,256 @@
+// Pruned column blocks for the tensor-core k-NN (exact).
+//
+// The page "Kilosort4 clustering and matching" (gpu/clustering, "k-nearest
+// neighbours are a matrix product") computes every row against every column;
+// the page "HDBSCAN" ("Exact shortcuts") skips work only where a bound proves
+// it cannot change the result.  This file applies that rule to the distance
+// tile: a 128-column block is skipped for a 128-row tile when the triangle
+// inequality through one pivot of the spatial order (order.cu) proves that
+// none of its points lies within any of the tile's rows' k-th distance.
+//
+// For a pivot p, a row x and a column z, |d(x, p) - d(z, p)| <= d(x, z).  A
+// block whose points all have d(z, p) in [L, H] is therefore at least
+// max(d(x, p) - H, L - d(x, p)) from x.  With an upper bound ub(x) of x's
+// k-th distance, the block is useless to the tile if, for one pivot p,
+// H < min over rows (d(x, p) - ub(x)) or L > max over rows (d(x, p) + ub(x)).
+//
+// The search runs in two passes of the tile.  The first ("home") pass takes
+// the kHomeBlocks blocks around the columns of the tile's own bin; from its
+// sorted candidates each row gets ub(x), a rigorous bound of the float32
+// distance the refine will rank by (below).  The row tile's hull per pivot
+// then selects the blocks of the second pass, which starts with the home
+// pass's KP-th key as its rows' threshold.  The refine merges both passes and
+// proves every row as before: a column the tile never evaluated lies, by the
+// construction of ub, strictly beyond the refined k-th distance.
+//
+// Rounding.  Pivot distances are float32 direct differences, within relative
+// eps = (d + 8) 2^-24 of the true ones (d + 2 roundings of the squared sum,
+// one of the square root), and every bound is widened outward by eps.  ub(x)
+// bounds the true distance of each of the k best home candidates by
+// |x|^2 + t + c (|x|^2 + |y|^2) (c: the tile's ranking error bound), and is
+// then scaled so that it also covers the float32 evaluation of the refine's
+// distance, its strict-ordering margin and the rounding of this sum.
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hdbmst {
+
+namespace {
+
+constexpr int P = kPrunePivots;
+
+int blocks_for(int64_t n, int per) { return static_cast<int>(n > per ? (n + per - 1) / per : 1); }
+
+// dst[pos][.] = src[perm[pos]][.] for pos < cnt: one warp per point, one
+// float4 per lane (P = 128 floats per point).
+__global__ void pivot_gather_kernel(const float *__restrict__ src, const int *__restrict__ perm,
+                                    int cnt, float *__restrict__ dst) {
+    static_assert(P == 128, "one float4 per lane");
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= cnt) return;
+    const float4 *s = reinterpret_cast<const float4 *>(src + static_cast<int64_t>(perm[w]) * P);
+    reinterpret_cast<float4 *>(dst + w * P)[lane] = __ldg(s + lane);
+}
+
+// Per column block b (one CTA, thread = pivot): least and largest distance of
+// its points to the pivot, widened outward by eps; +inf / -inf for a block
+// without points.  bcell[b]: the pivot cell of the block's first point.
+__global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict__ pdS, int m,
+                                                         int col_tiles, double eps,
+                                                         const int *__restrict__ binY,
+                                                         const int *__restrict__ permY, int B,
+                                                         float *__restrict__ Lm,
+                                                         float *__restrict__ Hm,
+                                                         int *__restrict__ bcell) {
+    const int b = blockIdx.x, p = threadIdx.x;
+    const int pos0 = b * kBN, pos1 = min(pos0 + kBN, m);
+    float lo = INFINITY, hi = -INFINITY;
+    for (int pos = pos0; pos < pos1; ++pos) {
+        const float v = pdS[static_cast<int64_t>(pos) * P + p];
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+    const int64_t o = static_cast<int64_t>(p) * col_tiles + b;
+    Lm[o] = pos1 > pos0 ? __double2float_rd(static_cast<double>(lo) * (1.0 - eps)) : INFINITY;
+    Hm[o] = pos1 > pos0 ? __double2float_ru(static_cast<double>(hi) * (1.0 + eps)) : -INFINITY;
+    if (p == 0) bcell[b] = pos1 > pos0 ? binY[permY[pos0]] / B : 0;
+}
+
+// Home range of each row tile of the chunk: kHomeBlocks blocks centred on the
+// block that holds, in the columns' sorted order, the position matching the
+// tile's middle row (its bin, at the same relative rank).  When Y is X that
+// block holds the tile's own rows.
+__global__ void home_kernel(const int *__restrict__ binX, const int *__restrict__ permX,
+                            const int *__restrict__ startX, const int *__restrict__ startY,
+                            int n, int col_tiles, int row_tile0, int row_tiles, bool alias,
+                            int *__restrict__ home_lo, int *__restrict__ home) {
+    const int rt = blockIdx.x * blockDim.x + threadIdx.x;
+    if (rt >= row_tiles) return;
+    const int gt = row_tile0 + rt;
+    int hb;
+    if (alias) {
+        hb = gt;
+    } else {
+        const int q = min(gt * kBM + kBM / 2, n - 1);
+        const int bin = binX[permX[q]];
+        const int64_t rank = q - startX[bin];
+        const int64_t cx = startX[bin + 1] - startX[bin];
+        const int64_t cy = startY[bin + 1] - startY[bin];
+        const int64_t pos = startY[bin] + (cy > 0 ? min(cy - 1, rank * cy / (cx > 0 ? cx : 1)) : 0);
+        hb = static_cast<int>(pos / kBN);
+    }
+    const int nh = min(kHomeBlocks, col_tiles);
+    const int h0 = max(0, min(hb - kHomeBlocks / 2, col_tiles - nh));
+    home_lo[rt] = h0;
+    for (int i = 0; i < kHomeBlocks; ++i) home[rt * kHomeBlocks + i] = h0 + min(i, nh - 1);
+}
+
+// One CTA (128 threads) per row tile of the chunk.
+__global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
+                                                          const float *__restrict__ pdSX,
+                                                          const float *__restrict__ Lm,
+                                                          const float *__restrict__ Hm,
+                                                          const int *__restrict__ bcell,
+                                                          const int *__restrict__ home_lo,
+                                                          int *__restrict__ list,
+                                                          int *__restrict__ count,
+                                                          int *__restrict__ slabs) {
+    __shared__ float s_ub[kBM];
+    __shared__ float s_A[P], s_B[P];
+    __shared__ int s_wc[kBM / 32];
+    const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int local = rt * kBM + tid;
+    const int row = a.row_base + local;
+    const int nh = min(kHomeBlocks, a.col_tiles);
+
+    // 1. ub(x) from the k best candidates of the home pass (sorted by (t, j)).
+    //    True squared distance of candidate j: at most |x|^2 + t_j + c (|x|^2 +
+    //    |y_j|^2) (the 1.01 covers the computed norms).  The refine ranks by
+    //    the float32 distance; its k-th value squared is at most (1 + (d + 5) u)
+    //    times the largest of these, and a column is provably beyond it when
+    //    its true squared distance exceeds that times (1 + 16 u) / (1 - (d + 3) u)
+    //    (the refine's own margin).  The scale (1 + (4 d + 64) u) covers both
+    //    with room for the rounding of this sum.
+    float ub = -1.f;  // < 0: no row here
+    if (row < a.row_end) {
+        const double xn = a.xnorm[row];
+        double U = 0.0;
+        bool fin = true;
+        for (int j = 0; j < a.k; ++j) {
+            const int64_t o = static_cast<int64_t>(local) * a.KP + j;
+            const float t = a.part_key[o];
+            const int ix = a.part_idx[o];
+            if (!(t < INFINITY) || ix < 0) {
+                fin = false;
+                break;
+            }
+            const double yn = a.ynorm[ix];
+            U = fmax(U, xn + static_cast<double>(t) + a.err_coef * 1.01 * (xn + yn));
+        }
+        const double u = 5.9604644775390625e-8;
+        ub = fin ? __double2float_ru(sqrt(U * (1.0 + (4.0 * a.d + 64.0) * u))) : INFINITY;
+    }
+    s_ub[tid] = ub;
+    __syncthreads();
+
+    // 2. The tile's hull per pivot (thread = pivot): the least d(x, p) - ub(x)
+    //    and the largest d(x, p) + ub(x), d(x, p) widened by eps, in float32
+    //    rounded outward (toward -inf for the least, +inf for the largest).
+    {
+        const float eps = static_cast<float>((a.d + 8) * 5.9604644775390625e-8);
+        const float lo_f = __fsub_rd(1.f, eps), hi_f = __fadd_ru(1.f, eps);
+        float A = INFINITY, Bv = -INFINITY;
+        for (int r = 0; r < kBM; ++r) {
+            const float u = s_ub[r];
+            if (u < 0.f) continue;
+            const float dx = pdSX[static_cast<int64_t>(a.row_base + rt * kBM + r) * P + tid];
+            A = fminf(A, __fsub_rd(__fmul_rd(dx, lo_f), u));
+            Bv = fmaxf(Bv, __fadd_ru(__fmul_ru(dx, hi_f), u));
+        }
+        s_A[tid] = A;
+        s_B[tid] = Bv;
+    }
+    __syncthreads();
+
+    // 3. Blocks outside the home range, outward from it (threads 0..63 to the
+    //    right, 64..127 to the left, 64 offsets per step), kept unless one
+    //    pivot separates them from every row.  The block's own pivot is tried
+    //    first (it separates most far blocks); the others 32 at a time, their
+    //    loads independent of each other.
+    const int h0 = home_lo[rt];
+    const int right0 = h0 + nh, left0 = h0 - 1;
+    int base = 0;
+    for (int o0 = 0; right0 + o0 < a.col_tiles || left0 - o0 >= 0; o0 += 64) {
+        const int o = o0 + (tid & 63);
+        const int b = tid < 64 ? right0 + o : left0 - o;
+        bool need = tid < 64 ? b < a.col_tiles : b >= 0;
+        if (need) {
+            const int p0 = bcell[b];
+            need = !(Hm[static_cast<int64_t>(p0) * a.col_tiles + b] < s_A[p0] ||
+                     Lm[static_cast<int64_t>(p0) * a.col_tiles + b] > s_B[p0]);
+            for (int p = 0; p < P && need; p += 32) {
+                bool sep = false;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int64_t i = static_cast<int64_t>(p + q) * a.col_tiles + b;
+                    sep |= (__ldg(Hm + i) < s_A[p + q]) | (__ldg(Lm + i) > s_B[p + q]);
+                }
+                need = !sep;
+            }
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, need);
+        if (lane == 0) s_wc[warp] = __popc(bal);
+        __syncthreads();
+        int off = base;
+        for (int w = 0; w < warp; ++w) off += s_wc[w];
+        if (need) list[static_cast<int64_t>(rt) * a.col_tiles + off + __popc(bal & lanemask_lt())] = b;
+        for (int w = 0; w < kBM / 32; ++w) base += s_wc[w];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        count[rt] = base;
+        slabs[rt] = 1 + (base + a.chunk_cap - 1) / a.chunk_cap;
+        atomicAdd(a.blocks_total, static_cast<unsigned long long>(base + nh));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n, int m,
+                               bool alias, int col_tiles, int d, cudaStream_t s) {
+    if (o.pivots != P) return cudaErrorInvalidValue;
+    pivot_gather_kernel<<<blocks_for(static_cast<int64_t>(m) * 32, 256), 256, 0, s>>>(
+        o.pdY, o.permY, m, b.pdSY);
+    int extra = 1;
+    if (!alias) {
+        pivot_gather_kernel<<<blocks_for(static_cast<int64_t>(n) * 32, 256), 256, 0, s>>>(
+            o.pdX, o.permX, n, b.pdSX);
+        ++extra;
+    }
+    block_bounds_kernel<<<col_tiles, P, 0, s>>>(b.pdSY, m, col_tiles, (d + 8.0) * 0x1p-24,
+                                                o.cellY, o.permY, o.buckets, b.Lm, b.Hm,
+                                                b.bcell);
+    count_extra_launches(extra);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaStream_t s) {
+    const SpatialOrder &o = *a.o;
+    home_kernel<<<blocks_for(a.row_tiles, 128), 128, 0, s>>>(
+        o.cellX, o.permX, o.startX, o.startY, a.n, a.col_tiles, a.row_tile0, a.row_tiles,
+        a.alias, b.home_lo, b.home);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s) {
+    prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.bcell, b.home_lo,
+                                                   b.list, b.count, b.slabs);
+    return cudaGetLastError();
+}
+
+}  // namespace hdbmst

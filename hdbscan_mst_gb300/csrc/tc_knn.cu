@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     const KnnTileArgs &a = P.a;
     uint8_t *base = pipe_base(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row_tile = blockIdx.x, split = blockIdx.y;
+    const int row_tile = blockIdx.x;
+    int split = blockIdx.y;
     const int r0 = a.row_base + row_tile * kRows;
     constexpr int kSub = kCols / kTileCols;  // pipeline tiles per 128-column tile
     const int ct_begin = split * a.tiles_per_split;
@@ -101,6 +102,18 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     if (a.tile_start) {  // spatial order: the sweep starts at the rows' own neighbourhood
         seq.rot = a.tile_start[r0 / kRows] * kSub;
         seq.wrap = a.col_tiles * kSub;
+    }
+    if (a.blist) {
+        // pruned search: chunk c of the row tile's block list (the last
+        // chunks, which only long lists have, are dispatched first)
+        const int cnt = a.bcount ? a.bcount[row_tile] : a.blist_count;
+        const int c = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+        const int begin = c * a.chunk_cap;
+        const int len = min(a.chunk_cap, cnt - begin);
+        if (len <= 0) return;  // the whole CTA, before any barrier or allocation
+        split = a.slab_base + c;
+        seq = TileSeq(0, 2 * len, 0, 0);
+        seq.list = a.blist + static_cast<int64_t>(row_tile) * a.blist_stride + begin;
     }
 
     for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
@@ -122,6 +135,11 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
             key[p] = INFINITY;
             idx[p] = INT_MAX;
         }
+        // a first threshold: the KP-th key an earlier pass already holds for
+        // the row (a candidate at or above it cannot reach the merged top KP)
+        float seed = INFINITY;
+        if (a.seed && r0 + row < a.row_end)
+            seed = a.seed[static_cast<int64_t>(row_tile * kRows + row) * KP + KP - 1];
         const auto prefetch = [&](int col0, int buf) {
             if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
         };
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                 for (int w2 = 8; w2 > 0; w2 >>= 1)
 #pragma unroll
                     for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
-                float tau = key[KP - 1];
+                float tau = fminf(key[KP - 1], seed);
 #pragma unroll
                 for (int q = 0; q < kParts; ++q) tau = fminf(tau, g_row_tau[q][row]);
                 if (m16[0] < tau) {

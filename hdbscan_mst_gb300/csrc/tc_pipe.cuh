@@ -116,8 +116,11 @@ struct PipeSmem {
 // The column tiles of a CTA: [ct_begin, ct_end) without [skip_lo, skip_hi),
 // optionally rotated: position t maps to (t + rot) mod wrap (wrap > 0), so a
 // sweep can start anywhere and wrap around (rot and wrap even: whole blocks).
+// With a block list, position t is tile t % 2 of the 128-column block
+// list[t / 2] (n = twice the list's length).
 struct TileSeq {
     int ct_begin, n, s_lo, gap, rot = 0, wrap = 0;
+    const int *list = nullptr;
     __device__ TileSeq(int begin, int end, int skip_lo, int skip_hi) {
         ct_begin = begin;
         s_lo = min(max(skip_lo, begin), end);
@@ -126,6 +129,7 @@ struct TileSeq {
         n = max(end - begin - gap, 0);
     }
     __device__ int at(int k) const {
+        if (list) return __ldg(list + (k >> 1)) * 2 + (k & 1);
         int t = ct_begin + k;
         t = t >= s_lo ? t + gap : t;
         if (wrap > 0) {

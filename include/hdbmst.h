@@ -274,6 +274,17 @@ const char *hdbmst_profile_kernel_name(int i);
 int64_t hdbmst_last_knn_exact_rows(void);
 
 /*
+ * (row, column) pairs whose distances the distance tile of the most recent
+ * hdbmst_knn / hdbmst_knn_noalloc / hdbmst_core_distances call evaluated, in
+ * whole blocks of 128 rows x 128 columns (padding included; host-side, not
+ * thread-safe).  On the tensor-core path with the spatial order, column blocks
+ * that the pivots' triangle-inequality bound proves to hold none of a row
+ * block's k nearest are never evaluated (an exact shortcut in the sense of the
+ * page "HDBSCAN", section "Exact shortcuts"), so this can be far below n x m.
+ */
+int64_t hdbmst_last_knn_tile_pairs(void);
+
+/*
  * Rounds of the most recent hdbmst_mr_mst call in this process: returns the
  * number of Boruvka rounds; for each of the first max_rounds rounds writes
  * the number of points scanned against all others (active[i]), the tree
