@@ -308,12 +308,13 @@ def _host_array(t):
 
 # ---------------------------------------------------------------- instrumentation
 
-ENGINES = {"auto": 0, "simt": 1, "tensor": 2}
+ENGINES = {"auto": 0, "simt": 1, "tensor": 2, "tf32": 3}
 
 
 def set_engine(engine: str) -> str:
-    """Select the distance-tile engine ("auto", "simt" or "tensor"); returns the
-    previous one.  Results are identical whichever engine runs."""
+    """Select the distance-tile engine ("auto", "simt", "tensor" or "tf32", the
+    tensor cores with TF32 products only); returns the previous one.  Results
+    are identical whichever engine runs."""
     prev = _load().hdbmst_set_engine(ENGINES[engine])
     return {v: k for k, v in ENGINES.items()}[prev]
 

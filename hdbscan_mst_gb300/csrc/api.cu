@@ -38,6 +38,10 @@ bool use_tensor_scan(int dk) {
     return g_engine != HDBMST_ENGINE_SIMT && tc_scan_supported(dk);
 }
 
+// Two-part FP16 operands on the tensor cores: 64 padded features (one
+// 128-byte row of halves per part), unless TF32 is asked for.
+bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
+
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
 std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
 // rows of the last k-NN / core-distance call searched exactly
@@ -129,7 +133,7 @@ struct DevStatus {
     int fb_count;
     int act_count;
     int edge_count;
-    int pad;
+    unsigned amax_bits;              // largest magnitude of the points (FP16 operands' scale)
     unsigned long long tile_blocks;  // 128 x 128 blocks the pruned k-NN tile evaluated
 };
 
@@ -318,18 +322,37 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     const int *permY = spatial ? b.order.permY : nullptr;
     if (spatial)
         LAUNCH(K_PACK, s, launch_spatial_order(b.order, X, ldx, p.n, Y, ldy, p.m, p.alias, p.d, s));
+    // tensor-core operands: TF32 low parts, or the FP16 halves (hi and lo, dk / 2
+    // words per point each) in the same buffer, with one scale for X and Y
+    const bool f16 = tensor && use_f16(p.dk);
+    const unsigned *amax = &b.st->amax_bits;
+    uint32_t *Xh16 = f16 ? reinterpret_cast<uint32_t *>(b.Xlo) : nullptr;
+    uint32_t *Xl16 = f16 ? Xh16 + p.n_pad * (p.dk / 2) : nullptr;
+    uint32_t *Yh16 = f16 ? reinterpret_cast<uint32_t *>(b.Ylo) : nullptr;
+    uint32_t *Yl16 = f16 ? Yh16 + p.m_pad * (p.dk / 2) : nullptr;
+    float *xlo = tensor && !f16 ? b.Xlo : nullptr, *ylo = tensor && !f16 ? b.Ylo : nullptr;
+    if (f16) {
+        LAUNCH(K_PACK, s, launch_absmax(X, ldx, p.n, p.d, &b.st->amax_bits, s));
+        if (!p.alias) LAUNCH(K_PACK, s, launch_absmax(Y, ldy, p.m, p.d, &b.st->amax_bits, s));
+    }
     if (p.alias) {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
-                                      b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
-                                      &b.st->nbmax_bits, s, permX));
+                                      b.Xp, xlo, b.xnorm, &b.st->status, &b.st->nbmax_bits, s,
+                                      permX, Xh16, Xl16, amax));
     } else {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
-                                      b.Xp, tensor ? b.Xlo : nullptr, b.xnorm, &b.st->status,
-                                      nullptr, s, permX));
+                                      b.Xp, xlo, b.xnorm, &b.st->status, nullptr, s, permX, Xh16,
+                                      Xl16, amax));
         LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
-                                      b.Yp, tensor ? b.Ylo : nullptr, b.ynorm, &b.st->status,
-                                      &b.st->nbmax_bits, s, permY));
+                                      b.Yp, ylo, b.ynorm, &b.st->status, &b.st->nbmax_bits, s,
+                                      permY, Yh16, Yl16, amax));
     }
+    TcOperands ops{};
+    if (f16)
+        ops = TcOperands{Xh16, Xl16, Yh16, Yl16};
+    else
+        ops = TcOperands{b.Xp, b.Xlo, b.Yp, b.Ylo};
+    const double tc_err = f16 ? tc::err_coef_f16(p.d, p.dk) : tc::err_coef(p.d, p.dk);
     // pruned search: the spatial order's pivots bound the column blocks (prune.cu)
     const bool prune = spatial && b.prune.list != nullptr;
     const int nh = std::min(kHomeBlocks, p.col_tiles);
@@ -365,6 +388,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.m = p.m;
         ta.status = &b.st->status;
         ta.tile_start = spatial ? b.order.tile_start : nullptr;
+        ta.f16 = f16 ? 1 : 0;
+        ta.amax_bits = amax;
         if (prune) {
             // home pass: slab 0, the kHomeBlocks blocks around the tile's own bin
             PruneHomeArgs ha{};
@@ -384,8 +409,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             h.blist_stride = kHomeBlocks;
             h.chunk_cap = kHomeBlocks;
             h.slab_base = 0;
-            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, h, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
-                                                row_tiles, 1, s));
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, h, ops, p.n_pad, p.m_pad, row_tiles, 1, s));
             // the blocks each row tile still needs, from the home pass's bounds
             PruneListArgs pa{};
             pa.part_key = b.part_key;
@@ -396,7 +420,10 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.d = p.d;
             pa.xnorm = b.xnorm;
             pa.ynorm = b.ynorm;
-            pa.err_coef = tc::err_coef(p.d, p.dk);
+            pa.err_coef = tc_err;
+            pa.f16 = f16 ? 1 : 0;
+            pa.dk = p.dk;
+            pa.amax_bits = amax;
             pa.col_tiles = p.col_tiles;
             pa.row_base = base;
             pa.row_end = p.n;
@@ -413,11 +440,10 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             q.chunk_cap = chunk_cap;
             q.slab_base = 1;
             q.seed = b.part_key;
-            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
-                                                row_tiles, kPruneChunks, s));
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, ops, p.n_pad, p.m_pad, row_tiles,
+                                                kPruneChunks, s));
         } else if (tensor) {
-            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, b.Xlo, b.Ylo, p.n_pad, p.m_pad,
-                                                row_tiles, S, s));
+            LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, ops, p.n_pad, p.m_pad, row_tiles, S, s));
         } else {
             LAUNCH(K_KNN_TILE, s, launch_knn_tile(p.KP, ta, row_tiles, S, s));
         }
@@ -432,7 +458,9 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.Yp = b.Yp;
         ra.xnorm = b.xnorm;
         ra.nbmax_bits = &b.st->nbmax_bits;
-        ra.err_coef = tensor ? tc::err_coef(p.d, p.dk) : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01;
+        ra.err_coef = tensor ? tc_err : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01;
+        ra.f16 = f16 ? 1 : 0;
+        ra.amax_bits = amax;
         ra.d = p.d;
         ra.dk = p.dk;
         ra.k = p.k;
@@ -736,10 +764,21 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     const int col_tiles = static_cast<int>(p.n_pad / kBN);
 
     const bool tensor = use_tensor_scan(p.dk);
+    // tensor-core operands: TF32 low parts, or the FP16 halves (hi and lo,
+    // dk / 2 words per point each) in the same buffer
+    const bool f16 = tensor && use_f16(p.dk);
+    const int dkw = f16 ? p.dk / 2 : p.dk;  // 32-bit words per point of each part
+    const float *op_hi = f16 ? b.Xlo : b.Xp;
+    const float *op_lo = f16 ? b.Xlo + p.n_pad * dkw : b.Xlo;
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
+    if (f16) LAUNCH(K_PACK, s, launch_absmax(X, ldx, N, d, &b.st->amax_bits, s));
     LAUNCH(K_PACK, s, launch_pack(X, ldx, N, d, static_cast<int>(p.n_pad), p.dk, b.Xf, b.Xp,
-                                  tensor ? b.Xlo : nullptr, b.norm, &b.st->status,
-                                  &b.st->nbmax_bits, s));
+                                  tensor && !f16 ? b.Xlo : nullptr, b.norm, &b.st->status,
+                                  &b.st->nbmax_bits, s, nullptr,
+                                  f16 ? reinterpret_cast<uint32_t *>(b.Xlo) : nullptr,
+                                  f16 ? reinterpret_cast<uint32_t *>(b.Xlo) + p.n_pad * dkw
+                                      : nullptr,
+                                  &b.st->amax_bits));
     LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
     LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, b.cache, s));
 
@@ -779,9 +818,9 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                               b.comp, b.norm, tensor ? nullptr : b.Xa, b.act_core,
                                               b.act_comp, b.act_norm, s));
             if (tensor) {
-                LAUNCH(K_GATHER, s, launch_gather_points(N, static_cast<int>(p.n_pad), p.dk, b.perm,
-                                                         b.Xp, b.Xlo, b.Xs_hi, b.Xs_lo, s));
-                LAUNCH(K_GATHER, s, launch_gather_points(na, na_pad, p.dk, b.act_idx, b.Xp, b.Xlo,
+                LAUNCH(K_GATHER, s, launch_gather_points(N, static_cast<int>(p.n_pad), dkw, b.perm,
+                                                         op_hi, op_lo, b.Xs_hi, b.Xs_lo, s));
+                LAUNCH(K_GATHER, s, launch_gather_points(na, na_pad, dkw, b.act_idx, op_hi, op_lo,
                                                          b.Xa_hi, b.Xa_lo, s));
             } else {
                 LAUNCH(K_GATHER, s, launch_gather_cols(N, static_cast<int>(p.n_pad), p.dk, b.perm,
@@ -824,7 +863,11 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.fb_count = &b.st->fb_count;
             sa.fb_rows = b.fb_rows;
             sa.status = &b.st->status;
-            sa.err_coef = tensor ? tc::err_coef(d, p.dk) : (2.0 * d + 10.0) * 0x1p-24 * 1.01;
+            sa.err_coef = f16      ? tc::err_coef_f16(d, p.dk)
+                          : tensor ? tc::err_coef(d, p.dk)
+                                   : (2.0 * d + 10.0) * 0x1p-24 * 1.01;
+            sa.f16 = f16 ? 1 : 0;
+            sa.amax_bits = &b.st->amax_bits;
             CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
             if (tensor) {
                 LAUNCH(K_SCAN, s, launch_tc_scan(sa, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo, row_tiles,
@@ -914,7 +957,7 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
 int hdbmst_set_engine(int engine) {
     const int prev = g_engine;
     if (engine == HDBMST_ENGINE_AUTO || engine == HDBMST_ENGINE_SIMT ||
-        engine == HDBMST_ENGINE_TENSOR)
+        engine == HDBMST_ENGINE_TENSOR || engine == HDBMST_ENGINE_TF32)
         g_engine = engine;
     return prev;
 }

@@ -1,7 +1,9 @@
 // Device helpers shared by the kernels of the hdbmst library.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -51,6 +53,37 @@ __device__ __forceinline__ unsigned float_order(float v) {
 }
 __device__ __forceinline__ float order_float(unsigned o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// Two-part FP16 operands of the tensor-core tiles (tc.cuh, err_coef_f16).
+// The scale 2^e of a point set puts its largest magnitude amax in
+// [2^14, 2^15), clamped to |e| <= 60; amax_bits are amax's float bits.
+__host__ __device__ inline int f16_scale_exp(unsigned amax_bits) {
+    const int E = static_cast<int>((amax_bits >> 23) & 0xffu) - 127;
+    const int e = 14 - E;
+    return e < -60 ? -60 : (e > 60 ? 60 : e);
+}
+// Absolute part of the FP16 form's ranking error in t (squared-distance
+// units): (2^30 sqrt(dk) + 2 dk) h^2 with h = 2^(-14 - e), 5% slack; zero for
+// the other engines.
+__host__ __device__ inline double f16_abs_err(bool f16, int dk, unsigned amax_bits) {
+    if (!f16) return 0.0;
+    const double h = ldexp(1.0, -14 - f16_scale_exp(amax_bits));
+    return (0x1p30 * sqrt(static_cast<double>(dk)) + 2.0 * dk) * h * h * 1.05;
+}
+
+// hi, lo halves of x 2^e (scale = 2^e): hi = fp16(x 2^e),
+// lo = fp16(x 2^e - hi), each flushed to zero below 2^-14.  x 2^e - hi is
+// exact in float32 (hi is x 2^e rounded to fewer bits at no smaller exponent).
+__device__ __forceinline__ void f16_split(float x, float scale, unsigned short &hi,
+                                          unsigned short &lo) {
+    const float xs = __fmul_rn(x, scale);
+    float h = __half2float(__float2half_rn(xs));
+    if (fabsf(h) < 0x1p-14f) h = 0.f;
+    float l = __half2float(__float2half_rn(__fsub_rn(xs, h)));
+    if (fabsf(l) < 0x1p-14f) l = 0.f;
+    hi = __half_as_ushort(__float2half_rn(h));
+    lo = __half_as_ushort(__float2half_rn(l));
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {

@@ -13,10 +13,17 @@ namespace hdbmst {
 // Xp [n_pad][dk] and its tensor-core low parts Xlo = x - tf32(x); write
 // norm[i] = sum of x^2 (+inf for padding points); flag non-finite values;
 // raise *nbmax_bits to the largest norm's bits.  perm (nullable): position
-// i < n holds the caller's point perm[i].
+// i < n holds the caller's point perm[i].  Xh16 / Xl16 (nullable): the
+// two-part FP16 operands of the tensor-core tile, point-major [n_pad][dk / 2]
+// 32-bit words (two halves each, f16_split with the scale of *amax_bits).
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
-                        unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr);
+                        unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr,
+                        uint32_t *Xh16 = nullptr, uint32_t *Xl16 = nullptr,
+                        const unsigned *amax_bits = nullptr);
+// Raise *amax_bits to the largest magnitude of a caller [d, n] set.
+cudaError_t launch_absmax(const float *X, int64_t ld, int n, int d, unsigned *amax_bits,
+                          cudaStream_t s);
 
 // ---------------------------------------------------------------- order.cu
 // Spatial order of the tensor-core k-NN (order.cu): nearest of `pivots`
@@ -74,6 +81,8 @@ struct PruneListArgs {
     int chunk_rows_pad, KP, k, d;
     const float *xnorm, *ynorm;  // sorted order
     double err_coef;             // the tile's ranking error bound
+    int f16, dk;                 // FP16 operands: also f16_abs_err(dk, *amax_bits)
+    const unsigned *amax_bits;
     int col_tiles, row_base, row_end, row_tiles;
     int chunk_cap;               // blocks per CTA of the second pass
     unsigned long long *blocks_total;  // += blocks the tile evaluates (both passes)
@@ -112,6 +121,16 @@ struct KnnTileArgs {
     const int *bcount;
     int blist_count, blist_stride, chunk_cap, slab_base;
     const float *seed;  // nullable: sorted lists of slab 0 (their KP-th key: a first threshold)
+    // tensor-core engine: two-part FP16 operands (dk = 64 only) with the scale of
+    // *amax_bits, else three-pass TF32
+    int f16;
+    const unsigned *amax_bits;
+};
+// Operands of the tensor-core tiles, point-major: TF32 - a_hi / b_hi the raw
+// float32 rows (dk floats), a_lo / b_lo their low parts; FP16 - the hi and lo
+// halves (dk / 2 words each).
+struct TcOperands {
+    const void *a_hi, *a_lo, *b_hi, *b_lo;
 };
 cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int splits,
                             cudaStream_t s);
@@ -119,9 +138,8 @@ cudaError_t launch_knn_tile(int KP, const KnnTileArgs &a, int row_tiles, int spl
 // operands by TMA from the point-major arrays (Xp / Yp and their low parts).
 bool tc_knn_supported(int dk);   // dk a multiple of 32, at most kTensorDkMax
 bool tc_scan_supported(int dk);  // dk = 32 or 64
-cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
-                          int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
-                          cudaStream_t s);
+cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int64_t x_rows,
+                          int64_t y_rows, int row_tiles, int splits, cudaStream_t s);
 // Padded feature count: whole 32-feature slabs up to 64 (the tensor-core tile's
 // operand granule), multiples of 16 beyond.
 // Padded feature count: whole 32-feature slabs up to kTensorDkMax (the
@@ -140,6 +158,8 @@ struct KnnRefineArgs {
     const float *xnorm;
     const unsigned *nbmax_bits;
     double err_coef;  // the engine's ranking error is at most err_coef (|x|^2 + |y|^2)
+    int f16;          // FP16 operands: plus f16_abs_err(dk, *amax_bits)
+    const unsigned *amax_bits;
     int d, dk, k, m;
     int core_rank;  // 1-based list position copied to out_core (0: none)
     int32_t *out_idx;
@@ -243,6 +263,8 @@ struct ScanArgs {
     int *fb_rows;
     unsigned *status;              // device status word (tensor-core timeouts)
     double err_coef;               // ranking error bound of the engine that ran
+    int f16;                       // FP16 operands: plus f16_abs_err(dk, *amax_bits)
+    const unsigned *amax_bits;
 };
 size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);

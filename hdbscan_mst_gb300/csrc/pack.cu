@@ -26,13 +26,18 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    float *__restrict__ norm,
                                                    unsigned *__restrict__ status,
                                                    unsigned *__restrict__ nbmax_bits,
-                                                   const int *__restrict__ perm) {
+                                                   const int *__restrict__ perm,
+                                                   uint2 *__restrict__ Xh16,
+                                                   uint2 *__restrict__ Xl16,
+                                                   const unsigned *__restrict__ amax_bits) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool inside = i < n_pad;
     const bool valid = i < n;
     const int src = (valid && perm) ? perm[i] : i;
     float acc = 0.f;
     bool finite = true;
+    // two-part FP16 operands: the set's scale 2^e (an exact power of two)
+    const float scale = Xh16 ? ldexpf(1.f, f16_scale_exp(*amax_bits)) : 1.f;
     if (inside) {
         for (int f = 0; f < dk; f += 4) {
             float v[4];
@@ -57,6 +62,17 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                 *reinterpret_cast<float4 *>(Xlo + static_cast<int64_t>(i) * dk + f) =
                     make_float4(l[0], l[1], l[2], l[3]);
             }
+            if (Xh16) {
+                // four halves = two 32-bit words, lower feature in the low half
+                unsigned short h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) f16_split(v[q], scale, h[q], l[q]);
+                const int64_t o = (static_cast<int64_t>(i) * dk + f) / 4;
+                Xh16[o] = make_uint2(h[0] | (static_cast<unsigned>(h[1]) << 16),
+                                     h[2] | (static_cast<unsigned>(h[3]) << 16));
+                Xl16[o] = make_uint2(l[0] | (static_cast<unsigned>(l[1]) << 16),
+                                     l[2] | (static_cast<unsigned>(l[3]) << 16));
+            }
         }
         norm[i] = valid ? acc : INFINITY;
     }
@@ -66,6 +82,24 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bits = max(bits, __shfl_xor_sync(0xffffffffu, bits, o));
     if ((threadIdx.x & 31) == 0 && nbmax_bits && bits) atomicMax(nbmax_bits, bits);
+}
+
+// Largest magnitude of the caller's [d, n] set, raised into *amax_bits
+// (non-negative floats order like their bits; non-finite values are the pack
+// kernel's to report).
+__global__ void __launch_bounds__(256) absmax_kernel(const float *__restrict__ X, int64_t ld,
+                                                     int n, int d,
+                                                     unsigned *__restrict__ amax_bits) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    unsigned bits = 0u;
+    if (i < n)
+        for (int f = 0; f < d; ++f) {
+            const float v = fabsf(X[static_cast<int64_t>(f) * ld + i]);
+            if (v <= 3.4028234663852886e38f) bits = max(bits, __float_as_uint(v));
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bits = max(bits, __shfl_xor_sync(0xffffffffu, bits, o));
+    if ((threadIdx.x & 31) == 0 && bits) atomicMax(amax_bits, bits);
 }
 
 __global__ void check_core_kernel(const float *__restrict__ core, int n,
@@ -81,10 +115,18 @@ __global__ void check_core_kernel(const float *__restrict__ core, int n,
 
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
-                        unsigned *nbmax_bits, cudaStream_t s, const int *perm) {
+                        unsigned *nbmax_bits, cudaStream_t s, const int *perm, uint32_t *Xh16,
+                        uint32_t *Xl16, const unsigned *amax_bits) {
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
-                                       nbmax_bits, perm);
+                                       nbmax_bits, perm, reinterpret_cast<uint2 *>(Xh16),
+                                       reinterpret_cast<uint2 *>(Xl16), amax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_absmax(const float *X, int64_t ld, int n, int d, unsigned *amax_bits,
+                          cudaStream_t s) {
+    absmax_kernel<<<(n + 255) / 256, 256, 0, s>>>(X, ld, n, d, amax_bits);
     return cudaGetLastError();
 }
 

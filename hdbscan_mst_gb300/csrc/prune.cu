@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
 
     // 1. ub(x) from the k best candidates of the home pass (sorted by (t, j)).
     //    True squared distance of candidate j: at most |x|^2 + t_j + c (|x|^2 +
-    //    |y_j|^2) (the 1.01 covers the computed norms).  The refine ranks by
+    //    |y_j|^2) + e0 (the 1.01 covers the computed norms; e0 the FP16
+    //    operands' absolute part).  The refine ranks by
     //    the float32 distance; its k-th value squared is at most (1 + (d + 5) u)
     //    times the largest of these, and a column is provably beyond it when
     //    its true squared distance exceeds that times (1 + 16 u) / (1 - (d + 3) u)
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     float ub = -1.f;  // < 0: no row here
     if (row < a.row_end) {
         const double xn = a.xnorm[row];
+        const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
         double U = 0.0;
         bool fin = true;
         for (int j = 0; j < a.k; ++j) {
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
                 break;
             }
             const double yn = a.ynorm[ix];
-            U = fmax(U, xn + static_cast<double>(t) + a.err_coef * 1.01 * (xn + yn));
+            U = fmax(U, xn + static_cast<double>(t) + a.err_coef * 1.01 * (xn + yn) + e0);
         }
         const double u = 5.9604644775390625e-8;
         ub = fin ? __double2float_ru(sqrt(U * (1.0 + (4.0 * a.d + 64.0) * u))) : INFINITY;

@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
     // core_z > w; for the second the true squared distance is at least
     // |a|^2 + tau - err_coef (|a|^2 + |z|^2) and, by Cauchy-Schwarz, at least
     // (|z| - |a|)^2, so every z exceeds T once
-    // |a|^2 + tau - err_coef (|a|^2 + nb_c) > T with nb_c = (|a| + sqrt(T))^2.
+    // |a|^2 + tau - err_coef (|a|^2 + nb_c) > T with nb_c = (|a| + sqrt(T))^2
+    // (less the FP16 operands' absolute error part e0 when they ran).
     bool proven = false;
     if (exact != kNoKey) {
         const double u = 5.9604644775390625e-8;
@@ -209,8 +210,9 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
         const double T = bw * bw * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
         const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
         const double nbc = sq * sq;
+        const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
         proven = (ra < tau) &&
-                 (static_cast<double>(tau) + na - a.err_coef * (na + nbc) > T);
+                 (static_cast<double>(tau) + na - a.err_coef * (na + nbc) - e0 > T);
         atomicMin(&a.cand[g], exact);
     } else {
         proven = !(tau < INFINITY);  // nothing kept and nothing dropped: no other component

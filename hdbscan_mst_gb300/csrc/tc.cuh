@@ -61,6 +61,13 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of the FP16 form: F32 accumulate, F16 A and B (format
+// code 0), both K-major, M x N.
+__host__ __device__ constexpr uint32_t instr_desc_f16(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
@@ -78,6 +85,18 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t tmem_d, uint32_t a_tmem, ui
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// FP16 products (kind::f16) with A read from TMEM.  A 32-bit TMEM column holds
+// two consecutive K elements (the lower K index in the low half), so one MMA
+// of K = 16 reads 8 columns; B is the same 128-byte swizzled K-major layout,
+// 32 bytes per K step, as in the TF32 form.
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
@@ -257,6 +276,24 @@ __device__ __forceinline__ uint32_t below_mask(const float (&v)[32], float thr) 
 // slack.
 __host__ __device__ inline double err_coef(int d, int dk) {
     return (3.0 * 0x1p-20 + 3.0 * dk * 0x1p-23 + (d + 4.0) * 0x1p-24) * 1.05;
+}
+
+// The two-part FP16 form (f16_split in common.cuh): each value, scaled by
+// the power of two 2^e of the whole set, is hi + lo with hi = fp16(x 2^e) and
+// lo = fp16(x 2^e - hi), parts below the smallest normal half (2^-14)
+// flushed to zero, and x.y ~ hi.hi' + hi.lo' + lo.hi' over 2^2e.  Per element
+// the relative error is at most 2^-22 (lo's rounding; hi.hi', hi.lo', lo.hi'
+// are exact products) plus 2^-22 for the dropped lo.lo', and the flushing
+// adds at most h = 2^(-14 - e) absolutely.  Relative part, as err_coef: the
+// three product terms (3 2^-22), float32 accumulation over 3 dk products
+// (3 dk 2^-23), the norms (d + 4) 2^-24, and 2^-29 sqrt(dk) from splitting
+// the absolute part, 2 h sqrt(dk) (|x| + |y|) + 2 dk h^2 in t, as
+// 2^-30 (|x|^2 + |y|^2) + 2^30 h^2 per norm; what remains is the absolute
+// f16_abs_err (common.cuh), added to every bound that uses this one.
+__host__ __device__ inline double err_coef_f16(int d, int dk) {
+    return (3.0 * 0x1p-22 + 3.0 * dk * 0x1p-23 + (d + 4.0) * 0x1p-24 +
+            0x1p-29 * sqrt(static_cast<double>(dk))) *
+           1.05;
 }
 
 }  // namespace tc

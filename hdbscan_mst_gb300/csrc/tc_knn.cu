@@ -83,7 +83,7 @@ __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float
     }
 }
 
-template <int KP, bool kWide>
+template <int KP, bool kWide, bool kF16>
 __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
     constexpr int kEpiWarps = Epi<KP, kWide>::kWarps;
@@ -121,9 +121,11 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     fence_before();
     __syncthreads();
     fence_after();
-    tc_produce_and_multiply<kEpiWarps, kWide>(P.maps, S, smem_u32(base), a.dk, r0, seq);
+    // the MMA operands: dk floats (TF32), or dk / 2 words of two halves (FP16)
+    const int dk_mma = kF16 ? a.dk / 2 : a.dk;
+    tc_produce_and_multiply<kEpiWarps, kWide, kF16>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
 
-    if (warp < 4) tc_load_a<kWide>(S, P.a_hi, P.a_lo, r0, a.dk);
+    if (warp < 4) tc_load_a<kWide>(S, P.a_hi, P.a_lo, r0, dk_mma);
     if (warp < kEpiWarps) {
         // thread = (row, group): rows 32 (w % 4) + lane, group w / 4
         const int row = (warp & 3) * 32 + lane;
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
         float seed = INFINITY;
         if (a.seed && r0 + row < a.row_end)
             seed = a.seed[static_cast<int64_t>(row_tile * kRows + row) * KP + KP - 1];
+        // t = |y|^2 - 2 x.y; the FP16 products carry the set's scale 2^2e
+        const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
         const auto prefetch = [&](int col0, int buf) {
             if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
         };
@@ -151,10 +155,10 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
+                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
+                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
+                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
+                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
                 }
                 // the batch's least t by a depth-5 tree, against the least
                 // published KP-th key of the row (stale values only loosen it)
@@ -217,14 +221,15 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     tc_teardown<kEpiWarps, kWide>(S, a.status);
 }
 
-template <int KP, bool kWide>
+template <int KP, bool kWide, bool kF16>
 cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStream_t s) {
     const size_t smem = kWide ? kWidePipeSmem : kPipeSmem;
-    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP, kWide>,
+    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP, kWide, kF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    tc_knn_kernel<KP, kWide><<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
+    tc_knn_kernel<KP, kWide, kF16>
+        <<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
@@ -235,22 +240,26 @@ bool tc_knn_supported(int dk) {
     return dk % kSlab == 0 && dk >= kSlab && dk <= kWideDkMax && tensor_maps_available();
 }
 
-cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const float *Xlo, const float *Ylo,
-                          int64_t x_rows, int64_t y_rows, int row_tiles, int splits,
-                          cudaStream_t s) {
+cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int64_t x_rows,
+                          int64_t y_rows, int row_tiles, int splits, cudaStream_t s) {
     TcKnnParams P;
     P.a = a;
-    P.a_hi = a.Xp;
-    P.a_lo = Xlo;
+    // the pipeline moves 32-bit words: floats (TF32) or pairs of halves (FP16)
+    P.a_hi = static_cast<const float *>(o.a_hi);
+    P.a_lo = static_cast<const float *>(o.a_lo);
+    const float *b_hi = static_cast<const float *>(o.b_hi), *b_lo = static_cast<const float *>(o.b_lo);
     const bool wide = a.dk > 64;
-    if (!make_point_map(&P.maps.b_hi, a.Yp, y_rows, a.dk) ||
-        !make_point_map(&P.maps.b_lo, Ylo, y_rows, a.dk) ||
-        (wide && !make_point_map(&P.maps.a_lo, Xlo, x_rows, a.dk)))
+    const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
+    if ((a.f16 && (wide || dk_mma != kSlab)) || !make_point_map(&P.maps.b_hi, b_hi, y_rows, dk_mma) ||
+        !make_point_map(&P.maps.b_lo, b_lo, y_rows, dk_mma) ||
+        (wide && !make_point_map(&P.maps.a_lo, P.a_lo, x_rows, a.dk)))
         return cudaErrorInvalidValue;
-    if (!wide && KP == 16) return tc_launch<16, false>(P, row_tiles, splits, s);
-    if (!wide && KP == 32) return tc_launch<32, false>(P, row_tiles, splits, s);
-    if (wide && KP == 16) return tc_launch<16, true>(P, row_tiles, splits, s);
-    if (wide && KP == 32) return tc_launch<32, true>(P, row_tiles, splits, s);
+    if (a.f16 && KP == 16) return tc_launch<16, false, true>(P, row_tiles, splits, s);
+    if (a.f16 && KP == 32) return tc_launch<32, false, true>(P, row_tiles, splits, s);
+    if (!wide && KP == 16) return tc_launch<16, false, false>(P, row_tiles, splits, s);
+    if (!wide && KP == 32) return tc_launch<32, false, false>(P, row_tiles, splits, s);
+    if (wide && KP == 16) return tc_launch<16, true, false>(P, row_tiles, splits, s);
+    if (wide && KP == 32) return tc_launch<32, true, false>(P, row_tiles, splits, s);
     return cudaErrorInvalidValue;
 }
 

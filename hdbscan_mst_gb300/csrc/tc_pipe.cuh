@@ -203,10 +203,15 @@ __device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const 
 }
 
 // Producer and MMA roles (warps E, E+1, E+2); epilogue warps return at once.
-template <int kEpiWarps, bool kWide = false>
+// kF16: the operands are the two-part FP16 halves (tc.cuh), two per 32-bit
+// word; dk then counts words, and the K steps, slabs, TMEM columns and
+// descriptors are those of the TF32 form on dk words, only the MMA kind
+// differs (K = 16 halves per MMA instead of 8 floats: the same 32 bytes).
+template <int kEpiWarps, bool kWide = false, bool kF16 = false>
 __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeSmem &S,
                                                         uint32_t sbase, int dk, int a_row,
                                                         const TileSeq &seq) {
+    static_assert(!(kWide && kF16), "the wide rows stay on TF32");
     using Sh = PipeShape<kWide>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slabs = dk / kSlab;
@@ -238,7 +243,8 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
         }
     } else if (warp > kEpiWarps && warp <= kEpiWarps + kAcc && lane == 0) {
         const int issuer = warp - kEpiWarps - 1;
-        const uint32_t idesc = instr_desc(kRows, kTileCols);
+        const uint32_t idesc =
+            kF16 ? instr_desc_f16(kRows, kTileCols) : instr_desc(kRows, kTileCols);
         const uint32_t tmem = S.tmem_base;
         bool ok = mbar_wait<kSleepMma>(&S.abar, 0);
         if (ok) fence_after();
@@ -274,6 +280,16 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                         mma_tf32_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
                         mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
                         mma_tf32(d, als + 2 * kk, bh + 2 * kk, idesc, 1u);
+                    }
+                } else if (kF16) {
+                    mma_f16_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
+                    mma_f16_ts(d, ah, bl, idesc, 1u);
+                    mma_f16_ts(d, al, bh, idesc, 1u);
+#pragma unroll
+                    for (int kk = 1; kk < kSlab / 8; ++kk) {
+                        mma_f16_ts(d, ah + kk * 8, bh + 2 * kk, idesc, 1u);
+                        mma_f16_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
+                        mma_f16_ts(d, al + kk * 8, bh + 2 * kk, idesc, 1u);
                     }
                 } else {
                     mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);

@@ -69,6 +69,7 @@ __device__ __forceinline__ float key_v(unsigned long long k) {
     return k == kNoKey ? INFINITY : order_float(static_cast<unsigned>(k >> 32));
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_constant__ TcScanParams P) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ PipeSmem S;
@@ -99,8 +100,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         skip_hi = c1 / kCols * kSub;
     }
     const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
-    tc_produce_and_multiply<kEpiWarps>(P.maps, S, smem_u32(base), a.dk, r0, seq);
-    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, a.dk);
+    // the MMA operands: dk floats (TF32), or dk / 2 words of two halves (FP16)
+    const int dk_mma = kF16 ? a.dk / 2 : a.dk;
+    tc_produce_and_multiply<kEpiWarps, false, kF16>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, dk_mma);
 
     if (warp < kEpiWarps) {
         const int row = (warp & 3) * 32 + lane;
@@ -116,6 +119,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         for (int p = 0; p < kKeep; ++p) keys[p] = kNoKey;
         float dropped = INFINITY;
 
+        // t = |b|^2 - 2 a.b; the FP16 products carry the set's scale 2^2e
+        const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
         // the row's own component is one run of columns [own_lo, own_hi)
         const int own_lo = valid ? a.comp_start[rc] : 0;
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
@@ -144,10 +149,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(-2.f, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(-2.f, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(-2.f, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(-2.f, v[j4 * 4 + 3], nb.w);
+                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
+                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
+                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
+                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
                 }
                 float m16[16];
 #pragma unroll
@@ -232,14 +237,15 @@ cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *X
     P.a = a;
     P.a_hi = Xa_hi;
     P.a_lo = Xa_lo;
-    if (!make_point_map(&P.maps.b_hi, Xs_hi, a.ldx, a.dk) ||
-        !make_point_map(&P.maps.b_lo, Xs_lo, a.ldx, a.dk))
+    const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
+    if ((a.f16 && dk_mma != kSlab) || !make_point_map(&P.maps.b_hi, Xs_hi, a.ldx, dk_mma) ||
+        !make_point_map(&P.maps.b_lo, Xs_lo, a.ldx, dk_mma))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const auto kernel = a.f16 ? tc_scan_kernel<true> : tc_scan_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPipeSmem));
     if (e != cudaSuccess) return e;
-    tc_scan_kernel<<<dim3(row_tiles, splits), kScanThreads, kPipeSmem, s>>>(P);
+    kernel<<<dim3(row_tiles, splits), kScanThreads, kPipeSmem, s>>>(P);
     return cudaGetLastError();
 }
 

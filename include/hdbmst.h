@@ -225,16 +225,20 @@ hdbmst_status hdbmst_hdbscan_labels(const int32_t *edges, const float *w, int64_
  *                        distances: d <= 192; Boruvka scan: d <= 64), else
  *                        FP32 FFMA (the default);
  *   HDBMST_ENGINE_SIMT   FP32 FFMA register-blocked tile everywhere;
- *   HDBMST_ENGINE_TENSOR same as AUTO.
- * The tensor-core tile ranks candidates with three-pass TF32 products
- * (tcgen05); both engines report distances and weights re-evaluated exactly
- * with dist() and prove the kept set against their own rounding bound, so
- * results are identical bit for bit whichever engine ran.  Returns the
- * previous setting; unknown values are ignored.
+ *   HDBMST_ENGINE_TENSOR same as AUTO;
+ *   HDBMST_ENGINE_TF32   tensor cores as AUTO, always with TF32 products.
+ * The tensor-core tile ranks candidates (tcgen05) with two-part FP16 products
+ * (every value, scaled by one power of two per call, split into a high and a
+ * low half; hi.hi + hi.lo + lo.hi) where the points have 33 to 64 features,
+ * else with three-pass TF32 products.  Every engine reports distances and
+ * weights re-evaluated exactly with dist() and proves the kept set against
+ * its own rounding bound, so results are identical bit for bit whichever
+ * engine ran.  Returns the previous setting; unknown values are ignored.
  */
 #define HDBMST_ENGINE_AUTO 0
 #define HDBMST_ENGINE_SIMT 1
 #define HDBMST_ENGINE_TENSOR 2
+#define HDBMST_ENGINE_TF32 3
 int hdbmst_set_engine(int engine);
 
 /* Human-readable text of a status code (a static string). */

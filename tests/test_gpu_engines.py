@@ -76,3 +76,50 @@ def test_knn_engines_identical_200k_d192_sampled_rows(h):
     k = task["k"]
     (ai, ad), (bi, bd) = both(h, lambda: tuple(np_(t) for t in h.knn(dev(X), dev(Y), k)))
     assert np.array_equal(ai, bi) and np.array_equal(ad, bd)
+
+
+@pytest.mark.parametrize("n,m,d,k", [(1000, 1000, 61, 11), (777, 2049, 64, 16), (2000, 1500, 48, 12),
+                                     (300, 130, 33, 32), (20000, 20000, 61, 11)])
+def test_fp16_tf32_simt_identical(h, n, m, d, k):
+    """The two-part FP16 operands (33 to 64 features), the TF32 operands and the
+    FP32 FFMA tile: identical lists; the FP16 form's ranking must be tight
+    enough that the rounding proof settles almost every row (an MMA that
+    computed something else would show up here as a flood of exact rows or
+    as different lists)."""
+    X = workloads.small(n, d, seed=n + 11 * d, dup_frac=0.02)
+    Y = workloads.small(m, d, seed=m + 13 * d, dup_frac=0.02)
+    out, exact = {}, {}
+    for eng in ("simt", "tf32", "tensor"):
+        h.set_engine(eng)
+        out[eng] = tuple(np_(t) for t in h.knn(dev(X), dev(Y), k))
+        exact[eng] = h.last_knn_exact_rows()
+    h.set_engine("auto")
+    for eng in ("tf32", "tensor"):
+        assert np.array_equal(out[eng][0], out["simt"][0]), eng
+        assert np.array_equal(out[eng][1], out["simt"][1]), eng
+    # (k = 32 fills the whole candidate list, so every engine searches every
+    # row exactly there: compare with the TF32 form's count)
+    assert exact["tensor"] <= max(5, n // 100, exact["tf32"]), exact
+
+
+def test_fp16_mst_identical_50k(h):
+    """The Boruvka scan on the FP16 operands against the TF32 and FP32 scans:
+    the same tree, bit for bit, on the 50k-clip workload."""
+    X, task = workloads.workload("hdbscan_50k_d61")
+    ms = task["min_samples"]
+    Xd = dev(X)
+    core, idx, dist = h.core_distances(Xd, ms)
+    trees = {}
+    for eng in ("simt", "tf32", "tensor"):
+        h.set_engine(eng)
+        e, w = h.mr_mst(Xd, core, idx, dist)
+        trees[eng] = (np_(e), np_(w))
+        if eng == "tensor":
+            rounds = h.last_mst_rounds()
+    h.set_engine("auto")
+    for eng in ("tf32", "tensor"):
+        assert np.array_equal(trees[eng][0], trees["simt"][0]), eng
+        assert np.array_equal(trees[eng][1], trees["simt"][1]), eng
+    scanned = sum(a for a, _, _ in rounds)
+    redone = sum(x for _, _, x in rounds)
+    assert redone <= max(50, scanned // 100), rounds
