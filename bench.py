@@ -61,16 +61,27 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
 FP32_LANES_PER_SM = 128
 # nominal dense tensor rates: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s
 TF32_PER_BF16 = 1.1 / 2.25
-# DRAM bytes per launch of the dominant kernel from one one-pass ncu capture
-# of the full workload (dram__bytes_read.sum + dram__bytes_write.sum), valid
-# only while the kernel's sources are those the capture ran (their sha256
-# below); otherwise the line reports null.
+# DRAM bytes per step of each distance tile (all its launches in one step,
+# like the roofline's achieved rate) from one one-pass ncu capture of the full
+# workload (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
+# the kernel's sources are those the capture ran (their sha256 below);
+# otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        "bytes": 5.234e9 + 29.04e6,
+        # per step: the home pass (52.08 MB read, 2.59 MB written) and the
+        # pruned second pass (74.57 MB read, 26.32 MB written)
+        "bytes": 52.08e6 + 2.59e6 + 74.57e6 + 26.32e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "154c8016ff7490919295a3dcf700a42facd86e06fa7c000adf97790d92b5cd39",
+        "sha256": "d8d232505c67120036fcce50ca5c5d39732e48320ae91936f68e5821470ceef8",
+    },
+    ("boruvka_scan", "hdbscan_200k_d61"): {
+        # per step: the four rounds' launches (54.88 + 53.99 + 158.41 + 120.57 MB
+        # read, 0.00 + 0.00 + 3.46 + 3.15 MB written)
+        "bytes": (54.88 + 53.99 + 158.41 + 120.57 + 3.46 + 3.15) * 1e6,
+        "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
+                    "hdbscan_mst_gb300/csrc/tc.cuh"),
+        "sha256": "18597b2f2a9f00a43c4817c4ce591306f1b76348ab59ec1aafc6d61cfcc484d8",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -232,6 +243,7 @@ def run_gpu(args):
     rounds = H.last_mst_rounds()
     core_exact_rows = H.last_knn_exact_rows()
     core_pairs = H.last_knn_tile_pairs()
+    scan_pairs = H.last_mst_scan_pairs()
 
     # ---- the same K steps again with an event pair around every kernel
     # launch: per-kernel times for the breakdown and the roofline
@@ -300,10 +312,16 @@ def run_gpu(args):
     tf32_basis = ("measured bf16 burst x nominal tf32/bf16 (1.1/2.25)" if bf16 else
                   "fallback bf16 x nominal tf32/bf16 (1.1/2.25)")
 
-    def roofline(prof_, name, d_, pairs, dense_pairs, tensor, workload=None):
-        """Dominant distance tile: algorithmic flops 2 d per (row, column) pair
-        the tile evaluated (column blocks the pivot bounds pruned are not
-        evaluated), over the tile's time per step (all its launches)."""
+    def engine_of(d_):
+        """The tensor-core operand form the default engine uses for d features."""
+        if d_ > 192:
+            return "fp32"
+        return "f16" if 32 < d_ <= 64 else "tf32"
+
+    def roofline(prof_, name, d_, pairs, dense_pairs, engine, workload=None):
+        """A distance tile: algorithmic flops 2 d per (row, column) pair the
+        tile evaluated (blocks the bounds prune are not evaluated), over the
+        tile's time per step (all its launches)."""
         if name not in prof_:
             return None
         tot_ms, nl = prof_[name]
@@ -313,16 +331,25 @@ def run_gpu(args):
         common = {"avg_launch_ms": round(tot_ms / nl, 3), "launches_per_step": nl / args.steps,
                   "ms_per_step": round(step_s * 1e3, 3), "flops_per_step": flops,
                   "pairs_evaluated": int(pairs), "pairs_dense": int(dense_pairs),
-                  "evaluated_frac": round(pairs / dense_pairs, 4),
+                  "evaluated_frac": round(pairs / dense_pairs, 4) if dense_pairs else None,
                   "dense_equivalent_tflops": round(2.0 * d_ * dense_pairs / step_s / 1e12, 1)}
-        if tensor:
-            dk = (d_ + 31) // 32 * 32  # padded features: whole 32-feature slabs
-            issued = 3 * 2.0 * dk * pairs / step_s / 1e12  # three TF32 passes on padded features
-            return {"kernel": name, "engine": "tcgen05 3xTF32", "bound": "tensor",
-                    "achieved": round(ach, 2), "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(ach / tf32_peak, 4), "traffic": traffic_for(name, workload),
-                    "peak_basis": tf32_basis, "issued_tflops": round(issued, 1),
-                    "issued_frac": round(issued / tf32_peak, 4),
+        if engine in ("f16", "tf32"):
+            if engine == "f16":
+                dk = 64  # padded halves per part
+                peak = bf16 if bf16 else FALLBACK_BF16_TFLOPS
+                basis = ("measured bf16 burst (dense fp16 runs at the bf16 rate)" if bf16 else
+                         "fallback bf16 (dense fp16 runs at the bf16 rate)")
+                eng = "tcgen05 kind::f16, two-part fp16 operands (3 products)"
+            else:
+                dk = (d_ + 31) // 32 * 32  # padded features: whole 32-feature slabs
+                peak, basis = tf32_peak, tf32_basis
+                eng = "tcgen05 kind::tf32 (3 products)"
+            issued = 3 * 2.0 * dk * pairs / step_s / 1e12
+            return {"kernel": name, "engine": eng, "bound": "tensor",
+                    "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / peak, 4), "traffic": traffic_for(name, workload),
+                    "peak_basis": basis, "issued_tflops": round(issued, 1),
+                    "issued_frac": round(issued / peak, 4),
                     "fp32_alu_equiv_frac": round(ach / fp32_peak, 4), **common}
         return {"kernel": name, "engine": "FP32 FFMA", "bound": "alu", "achieved": round(ach, 2),
                 "peak": round(fp32_peak, 2), "unit": "TFLOP/s", "frac": round(ach / fp32_peak, 4),
@@ -330,11 +357,18 @@ def run_gpu(args):
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {max_mhz:.0f} MHz",
                 **common}
 
-    # core distances: every clip against every clip, pruned by the pivot bounds
-    # the tensor-core tile serves d <= 192 (k-NN) in the default engine
-    main_roof = roofline(prof, "knn_tile", d, core_pairs, float(n) * n, d <= 192, args.workload)
+    # core distances: every clip against every clip, pruned by the pivot bounds;
+    # the Boruvka scan: every active clip against the clips of other components
+    knn_tile_roof = roofline(prof, "knn_tile", d, core_pairs, float(n) * n, engine_of(d),
+                             args.workload)
+    scan_dense = float(sum(a for a, _, _ in rounds)) * n
+    scan_roof = roofline(prof, "boruvka_scan", d, scan_pairs, scan_dense, engine_of(d),
+                         args.workload)
+    # the line's roofline is the dominant kernel's (the larger share of the step)
+    cands = [r for r in (scan_roof, knn_tile_roof) if r is not None]
+    main_roof = max(cands, key=lambda r: r["ms_per_step"]) if cands else None
     knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], knn_pairs,
-                        float(Xk.shape[1]) * Yk.shape[1], Xk.shape[0] <= 192,
+                        float(Xk.shape[1]) * Yk.shape[1], engine_of(Xk.shape[0]),
                         KNN_WORKLOAD if not args.skip_knn else None)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
                  for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
@@ -356,6 +390,7 @@ def run_gpu(args):
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": main_roof,
+        "rooflines": {"boruvka_scan": scan_roof, "knn_tile": knn_tile_roof},
         "kernel_ms_per_step": breakdown,
         "profiled_ms_per_step": round(sum(prof_times) / args.steps, 3),
         "step_ms": {"min": round(min(times), 3), "median": round(statistics.median(times), 3),
@@ -399,7 +434,7 @@ def sources_sha256(paths) -> str:
 
 
 def traffic_for(kernel: str, workload: str):
-    """Measured DRAM bytes per launch, or None when not measured for this
+    """Measured DRAM bytes per step, or None when not measured for this
     kernel and workload or the kernel changed since the capture."""
     rec = TRAFFIC.get((kernel, workload))
     if rec is None:

@@ -96,6 +96,7 @@ def _load():
     L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
     L.hdbmst_last_knn_exact_rows.restype = ctypes.c_int64
     L.hdbmst_last_knn_tile_pairs.restype = ctypes.c_int64
+    L.hdbmst_last_mst_scan_pairs.restype = ctypes.c_int64
     L.hdbmst_hdbscan_labels.argtypes = [vp, vp, i64, i32, vp]
     L.hdbmst_hdbscan_labels.restype = i32
     _lib = L
@@ -350,6 +351,12 @@ def last_knn_tile_pairs() -> int:
     """(row, column) pairs the distance tile of the last k-NN / core-distance
     call evaluated, in whole 128 x 128 blocks (pruned blocks excluded)."""
     return int(_load().hdbmst_last_knn_tile_pairs())
+
+
+def last_mst_scan_pairs() -> int:
+    """(row, column) pairs the Boruvka scan tiles of the last mr_mst call
+    evaluated, over all rounds."""
+    return int(_load().hdbmst_last_mst_scan_pairs())
 
 
 def profile_read() -> dict:

@@ -49,6 +49,8 @@ int64_t g_knn_exact_rows = 0;
 // (row, column) pairs the distance tile of the last k-NN / core-distance call
 // evaluated, in whole 128 x 128 blocks
 int64_t g_knn_tile_pairs = 0;
+// (row, column) pairs the Boruvka scan tiles of the last mr_mst call evaluated
+int64_t g_mst_scan_pairs = 0;
 
 const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
@@ -135,6 +137,7 @@ struct DevStatus {
     int edge_count;
     unsigned amax_bits;              // largest magnitude of the points (FP16 operands' scale)
     unsigned long long tile_blocks;  // 128 x 128 blocks the pruned k-NN tile evaluated
+    unsigned long long scan_pairs;   // (row, column) pairs the Boruvka scan evaluated
 };
 
 constexpr int kMaxSplits = 8;
@@ -282,6 +285,7 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
             q.list = c.take<int>(tiles * p.col_tiles);
             q.count = c.take<int>(tiles);
             q.slabs = c.take<int>(tiles);
+            q.gthr = c.take<unsigned>(static_cast<size_t>(p.chunk_rows));
         }
     }
     const size_t part = static_cast<size_t>(kMaxSplits) * p.chunk_rows * p.KP;
@@ -440,6 +444,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             q.chunk_cap = chunk_cap;
             q.slab_base = 1;
             q.seed = b.part_key;
+            q.gthr = b.prune.gthr;
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, ops, p.n_pad, p.m_pad, row_tiles,
                                                 kPruneChunks, s));
         } else if (tensor) {
@@ -789,6 +794,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     g_round_active.clear();
     g_round_edges.clear();
     g_round_exact.clear();
+    g_mst_scan_pairs = 0;
     int *size = b.counters, *act_size = b.counters + N, *cursor = b.counters + 2 * N,
         *act_cursor = b.counters + 3 * N, *totals = b.counters + 4 * N;
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
@@ -868,6 +874,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                    : (2.0 * d + 10.0) * 0x1p-24 * 1.01;
             sa.f16 = f16 ? 1 : 0;
             sa.amax_bits = &b.st->amax_bits;
+            sa.tile_pairs = &b.st->scan_pairs;
             CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
             if (tensor) {
                 LAUNCH(K_SCAN, s, launch_tc_scan(sa, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo, row_tiles,
@@ -892,6 +899,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                                   core, b.comp, b.norm, b.Xa, b.act_core,
                                                   b.act_comp, b.act_norm, s));
                 ScanArgs xa = sa;
+                xa.tile_pairs = nullptr;  // the exact re-scan is not the ranking tile
                 xa.lda = nf_pad;
                 xa.act_idx = b.fb_rows;
                 xa.na = nf;
@@ -924,6 +932,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         g_round_edges.push_back(edges);
         g_round_exact.push_back(fallback);
     }
+    g_mst_scan_pairs = static_cast<int64_t>(h.scan_pairs);
     if (edges != N - 1) return HDBMST_ERR_NOCONVERGE;
     cudaError_t e = sort_edges(N - 1, p.index_bits, b.e_w, b.e_lo, b.e_hi, b.w2, b.lo2, b.hi2,
                                b.hist, out_edges, out_w, s, before, after);
@@ -1013,6 +1022,8 @@ int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
 int64_t hdbmst_last_knn_exact_rows(void) { return g_knn_exact_rows; }
 
 int64_t hdbmst_last_knn_tile_pairs(void) { return g_knn_tile_pairs; }
+
+int64_t hdbmst_last_mst_scan_pairs(void) { return g_mst_scan_pairs; }
 
 const char *hdbmst_profile_kernel_name(int i) {
     return (i >= 0 && i < K_COUNT) ? kKernelNames[i] : "";

@@ -62,6 +62,7 @@ struct PruneBufs {
     int *list;            // [chunk row tiles][col_tiles] blocks of the second pass
     int *count;           // [chunk row tiles] entries of list
     int *slabs;           // [chunk row tiles] partial-list slabs written (1 + chunks)
+    unsigned *gthr;       // [chunk rows] shared thresholds of the second pass (KnnTileArgs::gthr)
 };
 // Pivot distances into sorted order (dst[pos] = src[perm[pos]]) and the
 // column blocks' bounds.
@@ -121,6 +122,10 @@ struct KnnTileArgs {
     const int *bcount;
     int blist_count, blist_stride, chunk_cap, slab_base;
     const float *seed;  // nullable: sorted lists of slab 0 (their KP-th key: a first threshold)
+    // nullable: per row of the chunk, the least KP-th key any CTA of the row's
+    // tile holds (float_order bits), read once per tile and lowered with
+    // atomicMin: the chunks of one row tile share their thresholds
+    unsigned *gthr;
     // tensor-core engine: two-part FP16 operands (dk = 64 only) with the scale of
     // *amax_bits, else three-pass TF32
     int f16;
@@ -265,6 +270,7 @@ struct ScanArgs {
     double err_coef;               // ranking error bound of the engine that ran
     int f16;                       // FP16 operands: plus f16_abs_err(dk, *amax_bits)
     const unsigned *amax_bits;
+    unsigned long long *tile_pairs;  // nullable: += (row, column) pairs the tile evaluates
 };
 size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);

@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
                                                           const int *__restrict__ home_lo,
                                                           int *__restrict__ list,
                                                           int *__restrict__ count,
-                                                          int *__restrict__ slabs) {
+                                                          int *__restrict__ slabs,
+                                                          unsigned *__restrict__ b_gthr) {
     __shared__ float s_ub[kBM];
     __shared__ float s_A[P], s_B[P];
     __shared__ int s_wc[kBM / 32];
@@ -158,6 +159,9 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         ub = fin ? __double2float_ru(sqrt(U * (1.0 + (4.0 * a.d + 64.0) * u))) : INFINITY;
     }
     s_ub[tid] = ub;
+    // the second pass's shared threshold starts at the home list's KP-th key
+    b_gthr[local] = row < a.row_end ? float_order(a.part_key[static_cast<int64_t>(local) * a.KP + a.KP - 1])
+                                    : float_order(INFINITY);
     __syncthreads();
 
     // 2. The tile's hull per pivot (thread = pivot): the least d(x, p) - ub(x)
@@ -251,7 +255,7 @@ cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaSt
 
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s) {
     prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.bcell, b.home_lo,
-                                                   b.list, b.count, b.slabs);
+                                                   b.list, b.count, b.slabs, b.gthr);
     return cudaGetLastError();
 }
 

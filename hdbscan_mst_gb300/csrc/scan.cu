@@ -86,6 +86,11 @@ __global__ void __launch_bounds__(kThreads, 2) mst_scan_kernel(const ScanArgs a)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
+    if (tid == 0 && a.tile_pairs) {
+        const int gap = max(0, min(skip_hi, ct_end) - max(skip_lo, ct_begin));
+        atomicAdd(a.tile_pairs,
+                  static_cast<unsigned long long>(ct_end - ct_begin - gap) * kBM * kBN);
+    }
     tile_pipeline(S.T, a.Xa, a.lda, r0, a.Xs, a.ldx, ct_begin, ct_end, skip_lo, skip_hi, a.dk, acc,
                   [&](float (&ac)[8][8], int ct) {
         const int col0 = ct * kBN;

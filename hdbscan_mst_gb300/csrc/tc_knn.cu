@@ -62,8 +62,16 @@ struct Epi {
 };
 
 __shared__ float g_row_tau[4][kRows];  // per group and row: that list's KP-th key
+// per group and row: that list's q-th key, q = ceil(KP / groups): once every
+// group holds q keys, their largest q-th key has at least KP keys at or below it
+__shared__ float s_row_tq[4][kRows];
+// the CTA's block list, when it fits: every role reads it per tile
+constexpr int kListCache = 2048;
+__shared__ int s_blist[kListCache];
 constexpr int kMaxEpiWarps = 12;
 __shared__ float4 s_cnorm[kMaxEpiWarps][2][kTileCols / 4];  // per warp: two tiles' column norms
+// per warp, two tiles: its 32 rows' thresholds shared across CTAs (ordered float bits)
+__shared__ uint4 s_gthr[kMaxEpiWarps][2][8];
 
 template <int KP>
 __device__ __forceinline__ void list_insert(float (&k)[KP], int (&ix)[KP], float t, int j) {
@@ -113,10 +121,19 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
         if (len <= 0) return;  // the whole CTA, before any barrier or allocation
         split = a.slab_base + c;
         seq = TileSeq(0, 2 * len, 0, 0);
-        seq.list = a.blist + static_cast<int64_t>(row_tile) * a.blist_stride + begin;
+        const int *gl = a.blist + static_cast<int64_t>(row_tile) * a.blist_stride + begin;
+        if (len <= kListCache) {
+            for (int i = tid; i < len; i += blockDim.x) s_blist[i] = gl[i];
+            seq.list = s_blist;  // visible to all after the barrier below
+        } else {
+            seq.list = gl;
+        }
     }
 
-    for (int i = tid; i < 4 * kRows; i += blockDim.x) (&g_row_tau[0][0])[i] = INFINITY;
+    for (int i = tid; i < 4 * kRows; i += blockDim.x) {
+        (&g_row_tau[0][0])[i] = INFINITY;
+        (&s_row_tq[0][0])[i] = INFINITY;
+    }
     tc_setup<kEpiWarps, kWide>(S);
     fence_before();
     __syncthreads();
@@ -142,10 +159,17 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
         float seed = INFINITY;
         if (a.seed && r0 + row < a.row_end)
             seed = a.seed[static_cast<int64_t>(row_tile * kRows + row) * KP + KP - 1];
+        constexpr int kQ = (KP + kParts - 1) / kParts;
+        unsigned published = 0xffffffffu;  // the least threshold this thread put in gthr
         // t = |y|^2 - 2 x.y; the FP16 products carry the set's scale 2^2e
         const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
+        // the warp's 32 rows of the shared thresholds (pruned second pass)
+        const int local_row = row_tile * kRows + row;
+        const unsigned *gthr_warp = a.gthr ? a.gthr + row_tile * kRows + (warp & 3) * 32 : nullptr;
         const auto prefetch = [&](int col0, int buf) {
             if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
+            else if (gthr_warp && lane < kTileCols / 4 + 8)
+                cp_async16(&s_gthr[warp][buf][lane - kTileCols / 4], gthr_warp + (lane - kTileCols / 4) * 4);
         };
         tc_epilogue_loop<kEpiWarps, kWide>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
@@ -169,9 +193,18 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                 for (int w2 = 8; w2 > 0; w2 >>= 1)
 #pragma unroll
                     for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
-                float tau = fminf(key[KP - 1], seed);
+                // the least of: every list's KP-th key, the largest of the
+                // lists' q-th keys, the seed and the shared threshold
+                float tau = fminf(key[KP - 1], seed), tq = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < kParts; ++q) tau = fminf(tau, g_row_tau[q][row]);
+                for (int q = 0; q < kParts; ++q) {
+                    tau = fminf(tau, g_row_tau[q][row]);
+                    tq = fmaxf(tq, s_row_tq[q][row]);
+                }
+                tau = fminf(tau, tq);
+                if (gthr_warp)  // the least KP-th key any CTA of the row tile has published
+                    tau = fminf(tau, order_float(reinterpret_cast<const unsigned *>(
+                                         &s_gthr[warp][buf][0])[lane]));
                 if (m16[0] < tau) {
                     // rare: insert this batch's candidates in column order
                     // with the one copy of the sink
@@ -183,6 +216,21 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                         list_insert<KP>(key, idx, pick32(v, j), col0 + cc * 32 + j);
                     }
                     g_row_tau[group][row] = key[KP - 1];
+                    s_row_tq[group][row] = key[kQ - 1];
+                    if (gthr_warp && r0 + row < a.row_end) {
+                        // the CTA's threshold for this row, for the other CTAs
+                        float tc = key[KP - 1], tm = -INFINITY;
+#pragma unroll
+                        for (int q = 0; q < kParts; ++q) {
+                            tc = fminf(tc, g_row_tau[q][row]);
+                            tm = fmaxf(tm, s_row_tq[q][row]);
+                        }
+                        const unsigned o = float_order(fminf(tc, tm));
+                        if (o < published && fminf(tc, tm) < INFINITY) {
+                            published = o;
+                            atomicMin(a.gthr + local_row, o);
+                        }
+                    }
                 }
             }
         });

@@ -129,7 +129,7 @@ struct TileSeq {
         n = max(end - begin - gap, 0);
     }
     __device__ int at(int k) const {
-        if (list) return __ldg(list + (k >> 1)) * 2 + (k & 1);
+        if (list) return list[k >> 1] * 2 + (k & 1);  // shared or global memory
         int t = ct_begin + k;
         t = t >= s_lo ? t + gap : t;
         if (wrap > 0) {

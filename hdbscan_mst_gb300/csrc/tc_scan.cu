@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         skip_hi = c1 / kCols * kSub;
     }
     const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
+    if (tid == 0 && a.tile_pairs)
+        atomicAdd(a.tile_pairs, static_cast<unsigned long long>(seq.n) * kTileCols * kRows);
     // the MMA operands: dk floats (TF32), or dk / 2 words of two halves (FP16)
     const int dk_mma = kF16 ? a.dk / 2 : a.dk;
     tc_produce_and_multiply<kEpiWarps, false, kF16>(P.maps, S, smem_u32(base), dk_mma, r0, seq);

@@ -289,6 +289,16 @@ int64_t hdbmst_last_knn_exact_rows(void);
 int64_t hdbmst_last_knn_tile_pairs(void);
 
 /*
+ * (row, column) pairs whose distances the Boruvka scan tiles of the most
+ * recent hdbmst_mr_mst call evaluated, over all rounds, in whole tiles
+ * (padding included; the exact re-scan of rows the rounding proof left open
+ * is not counted; host-side, not thread-safe).  Rows are the points the
+ * shortcuts of the page "HDBSCAN" ("Exact shortcuts") leave active; tiles
+ * wholly inside a row tile's own component are not evaluated.
+ */
+int64_t hdbmst_last_mst_scan_pairs(void);
+
+/*
  * Rounds of the most recent hdbmst_mr_mst call in this process: returns the
  * number of Boruvka rounds; for each of the first max_rounds rounds writes
  * the number of points scanned against all others (active[i]), the tree
