@@ -875,6 +875,10 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.f16 = f16 ? 1 : 0;
             sa.amax_bits = &b.st->amax_bits;
             sa.tile_pairs = &b.st->scan_pairs;
+            // the component bounds: a threshold per row (tensor scan) and the
+            // refine's acceptance of rows with no edge at or below U_C
+            sa.ub = tensor && shortcuts ? b.ub : nullptr;
+            sa.act_flag = b.act_flag;
             CUDA_OK(cudaMemsetAsync(&b.st->fb_count, 0, sizeof(int), s));
             if (tensor) {
                 LAUNCH(K_SCAN, s, launch_tc_scan(sa, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo, row_tiles,
@@ -900,6 +904,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                                   b.act_comp, b.act_norm, s));
                 ScanArgs xa = sa;
                 xa.tile_pairs = nullptr;  // the exact re-scan is not the ranking tile
+                xa.ub = nullptr;
                 xa.lda = nf_pad;
                 xa.act_idx = b.fb_rows;
                 xa.na = nf;

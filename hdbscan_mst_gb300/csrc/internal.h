@@ -271,6 +271,12 @@ struct ScanArgs {
     int f16;                       // FP16 operands: plus f16_abs_err(dk, *amax_bits)
     const unsigned *amax_bits;
     unsigned long long *tile_pairs;  // nullable: += (row, column) pairs the tile evaluates
+    // ub (nullable, tensor-core scan): the component bounds U_C; a row then
+    // starts from the threshold that U_C implies, and the refine accepts
+    // without exactness a row proven to have no edge at or below U_C (it
+    // clears the row's act_flag, so the edge is not cached)
+    const unsigned *ub;
+    unsigned char *act_flag;
 };
 size_t scan_part_entries(int splits, int64_t lda);
 cudaError_t launch_scan(const ScanArgs &a, int row_tiles, int splits, cudaStream_t s);

@@ -206,19 +206,30 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
     // (|z| - |a|)^2, so every z exceeds T once
     // |a|^2 + tau - err_coef (|a|^2 + nb_c) > T with nb_c = (|a| + sqrt(T))^2
     // (less the FP16 operands' absolute error part e0 when they ran).
+    //
+    // With the component bound U_C (a.ub) the row only matters if it has an
+    // edge of weight at most U_C (the component already holds an edge of
+    // weight U_C).  The proof then runs with w_ref = min(w, U_C): columns the
+    // pruned blocks left out have float32 weights above U_C by the pruning
+    // bound; if the proof holds and w > U_C, the row has no edge at or below
+    // U_C - its kept edge is real but not necessarily its least, so the row
+    // is not cached for the next round (act_flag cleared).
     bool proven = false;
-    if (exact != kNoKey) {
+    const double uc = a.ub ? static_cast<double>(__uint_as_float(a.ub[a.act_comp[r]])) : INFINITY;
+    const double bw = exact != kNoKey ? static_cast<double>(key_w(exact)) : INFINITY;
+    const double wref = fmin(bw, uc);
+    if (wref < INFINITY) {
         const double u = 5.9604644775390625e-8;
         const float na = a.act_norm[r];
         const float ra = __fsub_rn(__fmul_rn(ca, ca), na);
-        const double bw = key_w(exact);
-        const double T = bw * bw * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
+        const double T = wref * wref * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
         const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
         const double nbc = sq * sq;
         const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
         proven = (ra < tau) &&
                  (static_cast<double>(tau) + na - a.err_coef * (na + nbc) - e0 > T);
-        atomicMin(&a.cand[g], exact);
+        if (exact != kNoKey) atomicMin(&a.cand[g], exact);
+        if (proven && bw > uc && a.act_flag) a.act_flag[g] = 0;
     } else {
         proven = !(tau < INFINITY);  // nothing kept and nothing dropped: no other component
     }

@@ -120,6 +120,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
 #pragma unroll
         for (int p = 0; p < kKeep; ++p) keys[p] = kNoKey;
         float dropped = INFINITY;
+        // With the component bound U_C the row needs no column of weight above
+        // it: tau0 is the least v a column can have without the refine's proof
+        // (with w = U_C) ruling it out, so columns at or above tau0 are dropped
+        // and tau0 joins the row's threshold.
+        float tau0 = INFINITY;
+        if (a.ub && valid) {
+            const double uc = __uint_as_float(a.ub[rc]);
+            if (uc < INFINITY) {
+                const double u = 5.9604644775390625e-8;
+                const double T = uc * uc * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
+                const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
+                const double X = T + a.err_coef * (na + sq * sq) +
+                                 f16_abs_err(kF16, a.dk, kF16 ? *a.amax_bits : 0u) - na;
+                tau0 = __double2float_ru(X + fabs(X) * 0x1p-20);
+            }
+        }
 
         // t = |b|^2 - 2 a.b; the FP16 products carry the set's scale 2^2e
         const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
@@ -165,7 +181,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                     for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
                 // v >= t, so a batch whose least t does not beat the row's
                 // least published 4th value cannot change any list's 4 best
-                float thr = key_v(keys[kKeep - 1]);
+                float thr = fminf(key_v(keys[kKeep - 1]), tau0);
 #pragma unroll
                 for (int q = 0; q < kParts; ++q) thr = fminf(thr, s_row_thr[q][row]);
                 if (m16[0] < thr) {
@@ -199,7 +215,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         unsigned long long *pk =
             reinterpret_cast<unsigned long long *>(base);
         float *pt = reinterpret_cast<float *>(pk + (kParts - 1) * kRows * kKeep);
-        float tau = fminf(dropped, key_v(keys[kKeep - 1]));
+        float tau = fminf(fminf(dropped, key_v(keys[kKeep - 1])), tau0);
         epilogue_sync<kEpiWarps>();
         if (group > 0) {
 #pragma unroll
