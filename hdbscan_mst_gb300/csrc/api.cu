@@ -136,9 +136,17 @@ struct DevStatus {
     int act_count;
     int edge_count;
     unsigned amax_bits;              // largest magnitude of the points (FP16 operands' scale)
+    float e0;                        // the FP16 form's absolute ranking error (0 otherwise)
     unsigned long long tile_blocks;  // 128 x 128 blocks the pruned k-NN tile evaluated
     unsigned long long scan_pairs;   // (row, column) pairs the Boruvka scan evaluated
 };
+
+// A ranking error coefficient as the float32 the proofs use, rounded up.
+float coef_up(double c) {
+    float f = static_cast<float>(c);
+    if (static_cast<double>(f) < c) f = std::nextafter(f, INFINITY);
+    return f;
+}
 
 constexpr int kMaxSplits = 8;
 constexpr size_t kPartialBudget = size_t(256) << 20;  // bytes of partial lists per chunk
@@ -342,14 +350,14 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     if (p.alias) {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
                                       b.Xp, xlo, b.xnorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      permX, Xh16, Xl16, amax));
+                                      permX, Xh16, Xl16, amax, &b.st->e0));
     } else {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
                                       b.Xp, xlo, b.xnorm, &b.st->status, nullptr, s, permX, Xh16,
                                       Xl16, amax));
         LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
                                       b.Yp, ylo, b.ynorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      permY, Yh16, Yl16, amax));
+                                      permY, Yh16, Yl16, amax, &b.st->e0));
     }
     TcOperands ops{};
     if (f16)
@@ -424,10 +432,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.d = p.d;
             pa.xnorm = b.xnorm;
             pa.ynorm = b.ynorm;
-            pa.err_coef = tc_err;
-            pa.f16 = f16 ? 1 : 0;
-            pa.dk = p.dk;
-            pa.amax_bits = amax;
+            pa.err_c = coef_up(tc_err);
+            pa.e0 = &b.st->e0;
             pa.col_tiles = p.col_tiles;
             pa.row_base = base;
             pa.row_end = p.n;
@@ -463,9 +469,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.Yp = b.Yp;
         ra.xnorm = b.xnorm;
         ra.nbmax_bits = &b.st->nbmax_bits;
-        ra.err_coef = tensor ? tc_err : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01;
-        ra.f16 = f16 ? 1 : 0;
-        ra.amax_bits = amax;
+        ra.err_c = coef_up(tensor ? tc_err : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01);
+        ra.e0 = &b.st->e0;
         ra.d = p.d;
         ra.dk = p.dk;
         ra.k = p.k;
@@ -783,7 +788,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                   f16 ? reinterpret_cast<uint32_t *>(b.Xlo) : nullptr,
                                   f16 ? reinterpret_cast<uint32_t *>(b.Xlo) + p.n_pad * dkw
                                       : nullptr,
-                                  &b.st->amax_bits));
+                                  &b.st->amax_bits, &b.st->e0));
     LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
     LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, b.cache, s));
 
@@ -869,9 +874,10 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.fb_count = &b.st->fb_count;
             sa.fb_rows = b.fb_rows;
             sa.status = &b.st->status;
-            sa.err_coef = f16      ? tc::err_coef_f16(d, p.dk)
-                          : tensor ? tc::err_coef(d, p.dk)
-                                   : (2.0 * d + 10.0) * 0x1p-24 * 1.01;
+            sa.err_c = coef_up(f16      ? tc::err_coef_f16(d, p.dk)
+                               : tensor ? tc::err_coef(d, p.dk)
+                                        : (2.0 * d + 10.0) * 0x1p-24 * 1.01);
+            sa.e0 = &b.st->e0;
             sa.f16 = f16 ? 1 : 0;
             sa.amax_bits = &b.st->amax_bits;
             sa.tile_pairs = &b.st->scan_pairs;

@@ -86,6 +86,22 @@ __device__ __forceinline__ void f16_split(float x, float scale, unsigned short &
     lo = __half_as_ushort(__float2half_rn(l));
 }
 
+// The rounding proofs of the refines (knn.cu, scan.cu), in float32 with every
+// operation rounded in the safe direction (float64 is slow on this part).
+// T = w^2 (1 + 16 u) / (1 - (d + 3) u), u = 2^-24, rounded up; both factors
+// are exact floats.
+__device__ __forceinline__ float proof_T_up(float w, int d) {
+    const float m1 = 1.f + 0x1p-20f;
+    const float m2 = 1.f - static_cast<float>(d + 3) * 0x1p-24f;
+    return __fdiv_ru(__fmul_ru(__fmul_ru(w, w), m1), m2);
+}
+// |a|^2 + tau - c (|a|^2 + nb_c) - e0, nb_c = (|a| + sqrt(T))^2, rounded down.
+__device__ __forceinline__ float proof_lhs_down(float tau, float na, float T, float c, float e0) {
+    const float sq = __fadd_ru(__fsqrt_ru(na), __fsqrt_ru(T));
+    const float nbc = __fmul_ru(sq, sq);
+    return __fsub_rd(__fsub_rd(__fadd_rd(tau, na), __fmul_ru(c, __fadd_ru(na, nbc))), e0);
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

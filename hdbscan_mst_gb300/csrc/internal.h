@@ -15,12 +15,13 @@ namespace hdbmst {
 // raise *nbmax_bits to the largest norm's bits.  perm (nullable): position
 // i < n holds the caller's point perm[i].  Xh16 / Xl16 (nullable): the
 // two-part FP16 operands of the tensor-core tile, point-major [n_pad][dk / 2]
-// 32-bit words (two halves each, f16_split with the scale of *amax_bits).
+// 32-bit words (two halves each, f16_split with the scale of *amax_bits);
+// *e0_out (nullable) then receives the form's absolute error part, rounded up.
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr,
                         uint32_t *Xh16 = nullptr, uint32_t *Xl16 = nullptr,
-                        const unsigned *amax_bits = nullptr);
+                        const unsigned *amax_bits = nullptr, float *e0_out = nullptr);
 // Raise *amax_bits to the largest magnitude of a caller [d, n] set.
 cudaError_t launch_absmax(const float *X, int64_t ld, int n, int d, unsigned *amax_bits,
                           cudaStream_t s);
@@ -81,9 +82,8 @@ struct PruneListArgs {
     const int *part_idx;
     int chunk_rows_pad, KP, k, d;
     const float *xnorm, *ynorm;  // sorted order
-    double err_coef;             // the tile's ranking error bound
-    int f16, dk;                 // FP16 operands: also f16_abs_err(dk, *amax_bits)
-    const unsigned *amax_bits;
+    float err_c;                 // the tile's ranking error coefficient, rounded up
+    const float *e0;             // its absolute part (FP16 operands; 0 otherwise)
     int col_tiles, row_base, row_end, row_tiles;
     int chunk_cap;               // blocks per CTA of the second pass
     unsigned long long *blocks_total;  // += blocks the tile evaluates (both passes)
@@ -162,9 +162,8 @@ struct KnnRefineArgs {
     const float *Xp, *Yp;  // point-major [.][dk]
     const float *xnorm;
     const unsigned *nbmax_bits;
-    double err_coef;  // the engine's ranking error is at most err_coef (|x|^2 + |y|^2)
-    int f16;          // FP16 operands: plus f16_abs_err(dk, *amax_bits)
-    const unsigned *amax_bits;
+    float err_c;      // the ranking error is at most err_c (|x|^2 + |y|^2) + *e0
+    const float *e0;  // (err_c rounded up; e0 the FP16 operands' absolute part, else 0)
     int d, dk, k, m;
     int core_rank;  // 1-based list position copied to out_core (0: none)
     int32_t *out_idx;
@@ -267,8 +266,9 @@ struct ScanArgs {
     int *fb_count;
     int *fb_rows;
     unsigned *status;              // device status word (tensor-core timeouts)
-    double err_coef;               // ranking error bound of the engine that ran
-    int f16;                       // FP16 operands: plus f16_abs_err(dk, *amax_bits)
+    float err_c;                   // ranking error coefficient of the engine that ran (rounded up)
+    const float *e0;               // its absolute part (FP16 operands; 0 otherwise)
+    int f16;                       // FP16 operands (scale of *amax_bits)
     const unsigned *amax_bits;
     unsigned long long *tile_pairs;  // nullable: += (row, column) pairs the tile evaluates
     // ub (nullable, tensor-core scan): the component bounds U_C; a row then

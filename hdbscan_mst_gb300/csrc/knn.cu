@@ -334,16 +334,11 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     //    the second bound, and every other z by the first as soon as
     //    |x|^2 + A - err_coef (|x|^2 + nb_c) > T.  Then no dropped column can
     //    rank in the top k.  The bound needs no maximum over all columns.  The
-    //    FP16 operands add an absolute part e0 to the ranking error.
+    //    FP16 operands add an absolute part e0 to the ranking error.  Every
+    //    step is float32 rounded in the safe direction (proof_* in common.cuh).
     if (gl == a.k - 1 && A < INFINITY) {
-        const double u = 5.9604644775390625e-8;
-        const double dk = key_w(key);
-        const double na = a.xnorm[row];
-        const double T = dk * dk * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
-        const double sq = sqrt(na) + sqrt(T);
-        const double nbc = sq * sq;
-        const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
-        if (!(static_cast<double>(A) + na - a.err_coef * (na + nbc) - e0 > T)) {
+        const float T = proof_T_up(key_w(key), a.d);
+        if (!(proof_lhs_down(A, a.xnorm[row], T, a.err_c, *a.e0) > T)) {
             const int pos = atomicAdd(a.fb_count, 1);
             a.fb_rows[pos] = row;
         }

@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    const int *__restrict__ perm,
                                                    uint2 *__restrict__ Xh16,
                                                    uint2 *__restrict__ Xl16,
-                                                   const unsigned *__restrict__ amax_bits) {
+                                                   const unsigned *__restrict__ amax_bits,
+                                                   float *__restrict__ e0_out) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool inside = i < n_pad;
     const bool valid = i < n;
@@ -38,6 +39,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
     bool finite = true;
     // two-part FP16 operands: the set's scale 2^e (an exact power of two)
     const float scale = Xh16 ? ldexpf(1.f, f16_scale_exp(*amax_bits)) : 1.f;
+    // the FP16 form's absolute error part, once per call for every proof
+    if (Xh16 && e0_out && i == 0) *e0_out = __double2float_ru(f16_abs_err(true, dk, *amax_bits));
     if (inside) {
         for (int f = 0; f < dk; f += 4) {
             float v[4];
@@ -116,11 +119,11 @@ __global__ void check_core_kernel(const float *__restrict__ core, int n,
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm, uint32_t *Xh16,
-                        uint32_t *Xl16, const unsigned *amax_bits) {
+                        uint32_t *Xl16, const unsigned *amax_bits, float *e0_out) {
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
                                        nbmax_bits, perm, reinterpret_cast<uint2 *>(Xh16),
-                                       reinterpret_cast<uint2 *>(Xl16), amax_bits);
+                                       reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out);
     return cudaGetLastError();
 }
 

@@ -140,9 +140,10 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     //    with room for the rounding of this sum.
     float ub = -1.f;  // < 0: no row here
     if (row < a.row_end) {
-        const double xn = a.xnorm[row];
-        const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
-        double U = 0.0;
+        const float xn = a.xnorm[row], e0 = *a.e0;
+        // the 1.01 covers the computed norms; float32 rounded upward throughout
+        const float c = __fmul_ru(a.err_c, 1.01f);
+        float U = 0.f;
         bool fin = true;
         for (int j = 0; j < a.k; ++j) {
             const int64_t o = static_cast<int64_t>(local) * a.KP + j;
@@ -152,11 +153,11 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
                 fin = false;
                 break;
             }
-            const double yn = a.ynorm[ix];
-            U = fmax(U, xn + static_cast<double>(t) + a.err_coef * 1.01 * (xn + yn) + e0);
+            const float yn = a.ynorm[ix];
+            U = fmaxf(U, __fadd_ru(__fadd_ru(xn, t), __fadd_ru(__fmul_ru(c, __fadd_ru(xn, yn)), e0)));
         }
-        const double u = 5.9604644775390625e-8;
-        ub = fin ? __double2float_ru(sqrt(U * (1.0 + (4.0 * a.d + 64.0) * u))) : INFINITY;
+        const float scale = 1.f + static_cast<float>(4 * a.d + 64) * 0x1p-24f;  // rounds up
+        ub = fin ? __fsqrt_ru(__fmul_ru(U, __fadd_ru(scale, 0x1p-23f))) : INFINITY;
     }
     s_ub[tid] = ub;
     // the second pass's shared threshold starts at the home list's KP-th key

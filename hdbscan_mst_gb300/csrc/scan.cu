@@ -215,19 +215,14 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
     // U_C - its kept edge is real but not necessarily its least, so the row
     // is not cached for the next round (act_flag cleared).
     bool proven = false;
-    const double uc = a.ub ? static_cast<double>(__uint_as_float(a.ub[a.act_comp[r]])) : INFINITY;
-    const double bw = exact != kNoKey ? static_cast<double>(key_w(exact)) : INFINITY;
-    const double wref = fmin(bw, uc);
+    const float uc = a.ub ? __uint_as_float(a.ub[a.act_comp[r]]) : INFINITY;
+    const float bw = exact != kNoKey ? key_w(exact) : INFINITY;
+    const float wref = fminf(bw, uc);
     if (wref < INFINITY) {
-        const double u = 5.9604644775390625e-8;
         const float na = a.act_norm[r];
         const float ra = __fsub_rn(__fmul_rn(ca, ca), na);
-        const double T = wref * wref * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
-        const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
-        const double nbc = sq * sq;
-        const double e0 = f16_abs_err(a.f16 != 0, a.dk, a.f16 ? *a.amax_bits : 0u);
-        proven = (ra < tau) &&
-                 (static_cast<double>(tau) + na - a.err_coef * (na + nbc) - e0 > T);
+        const float T = proof_T_up(wref, a.d);
+        proven = (ra < tau) && (proof_lhs_down(tau, na, T, a.err_c, *a.e0) > T);
         if (exact != kNoKey) atomicMin(&a.cand[g], exact);
         if (proven && bw > uc && a.act_flag) a.act_flag[g] = 0;
     } else {

@@ -126,17 +126,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         // and tau0 joins the row's threshold.
         float tau0 = INFINITY;
         if (a.ub && valid) {
-            const double uc = __uint_as_float(a.ub[rc]);
+            const float uc = __uint_as_float(a.ub[rc]);
             if (uc < INFINITY) {
-                const double u = 5.9604644775390625e-8;
-                const double T = uc * uc * (1.0 + 16.0 * u) / (1.0 - (a.d + 3.0) * u);
-                const double sq = sqrt(static_cast<double>(na)) + sqrt(T);
-                const double X = T + a.err_coef * (na + sq * sq) +
-                                 f16_abs_err(kF16, a.dk, kF16 ? *a.amax_bits : 0u) - na;
-                tau0 = __double2float_ru(X + fabs(X) * 0x1p-20);
+                // T(U_C) + c (|a|^2 + nb_c) + e0 - |a|^2, rounded up, plus a margin
+                // of 2^-20 of its magnitude (the refine's check rounds down)
+                const float T = proof_T_up(uc, a.d);
+                const float sq = __fadd_ru(__fsqrt_ru(na), __fsqrt_ru(T));
+                const float X = __fsub_ru(
+                    __fadd_ru(__fadd_ru(T, __fmul_ru(a.err_c, __fadd_ru(na, __fmul_ru(sq, sq)))),
+                              *a.e0),
+                    na);
+                tau0 = __fadd_ru(X, __fmul_ru(__fadd_ru(fabsf(X), __fadd_ru(na, T)), 0x1p-20f));
             }
         }
-
         // t = |b|^2 - 2 a.b; the FP16 products carry the set's scale 2^2e
         const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
         // the row's own component is one run of columns [own_lo, own_hi)
