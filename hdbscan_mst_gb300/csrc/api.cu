@@ -262,24 +262,28 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
         o.buckets = kSpatialBuckets;
         o.cellY = c.take<int>(p.m_pad);
         o.permY = c.take<int>(p.m_pad);
+        o.invY = c.take<int>(p.m_pad);
         o.startY = c.take<int>(NB + 1);
         o.dcellY = c.take<float>(p.m_pad);
         o.pdY = p.prune ? c.take<float>(static_cast<size_t>(p.m_pad) * P) : nullptr;
         if (p.alias) {
             o.cellX = o.cellY;
             o.permX = o.permY;
+            o.invX = o.invY;
             o.startX = o.startY;
             o.dcellX = o.dcellY;
             o.pdX = o.pdY;
         } else {
             o.cellX = c.take<int>(p.n_pad);
             o.permX = c.take<int>(p.n_pad);
+            o.invX = c.take<int>(p.n_pad);
             o.startX = c.take<int>(NB + 1);
             o.dcellX = c.take<float>(p.n_pad);
             o.pdX = p.prune ? c.take<float>(static_cast<size_t>(p.n_pad) * P) : nullptr;
         }
         o.counters = c.take<int>(spatial_counter_ints(P, kSpatialBuckets));
         o.tile_start = c.take<int>(p.n_pad / kBM);
+        o.pivf = c.take<float>(static_cast<size_t>(kSpatialMaxD) * P);
         if (p.prune) {
             PruneBufs &q = b.prune;
             const size_t tiles = static_cast<size_t>(p.chunk_rows / kBM);
@@ -327,9 +331,9 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
                       float *out_core, int core_rank, cudaStream_t s) {
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
     const bool tensor = use_tensor(p.dk) && b.Xlo != nullptr;
-    // (not for wide rows: that tile waits on its operand stream, not on the
-    // selection, and the order's gathers cost more than they save there)
-    const bool spatial = tensor && b.order.permY && p.m >= kSpatialMinCols && p.dk <= 64;
+    // the spatial order, and with it the pruned search, once the column set is
+    // large enough for the bounds to pay for themselves
+    const bool spatial = tensor && b.order.permY && p.m >= kSpatialMinCols;
     const int *permX = spatial ? b.order.permX : nullptr;
     const int *permY = spatial ? b.order.permY : nullptr;
     if (spatial)
@@ -347,17 +351,21 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         LAUNCH(K_PACK, s, launch_absmax(X, ldx, p.n, p.d, &b.st->amax_bits, s));
         if (!p.alias) LAUNCH(K_PACK, s, launch_absmax(Y, ldy, p.m, p.d, &b.st->amax_bits, s));
     }
+    // the spatial order: points go to their sorted positions, read in caller
+    // order; the feature-major copy only the FP32 tile reads is left out
+    const int *invX = spatial ? b.order.invX : nullptr, *invY = spatial ? b.order.invY : nullptr;
+    float *Xf = spatial ? nullptr : b.Xf, *Yf = spatial ? nullptr : b.Yf;
     if (p.alias) {
-        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
+        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, Xf,
                                       b.Xp, xlo, b.xnorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      permX, Xh16, Xl16, amax, &b.st->e0));
+                                      nullptr, Xh16, Xl16, amax, &b.st->e0, invX));
     } else {
-        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, b.Xf,
-                                      b.Xp, xlo, b.xnorm, &b.st->status, nullptr, s, permX, Xh16,
-                                      Xl16, amax));
-        LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, b.Yf,
+        LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, Xf,
+                                      b.Xp, xlo, b.xnorm, &b.st->status, nullptr, s, nullptr, Xh16,
+                                      Xl16, amax, &b.st->e0, invX));
+        LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, Yf,
                                       b.Yp, ylo, b.ynorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      permY, Yh16, Yl16, amax, &b.st->e0));
+                                      nullptr, Yh16, Yl16, amax, &b.st->e0, invY));
     }
     TcOperands ops{};
     if (f16)

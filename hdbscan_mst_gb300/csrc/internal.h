@@ -13,7 +13,9 @@ namespace hdbmst {
 // Xp [n_pad][dk] and its tensor-core low parts Xlo = x - tf32(x); write
 // norm[i] = sum of x^2 (+inf for padding points); flag non-finite values;
 // raise *nbmax_bits to the largest norm's bits.  perm (nullable): position
-// i < n holds the caller's point perm[i].  Xh16 / Xl16 (nullable): the
+// i < n holds the caller's point perm[i]; or inv (nullable, instead of perm):
+// the caller's point i goes to position inv[i] (read in caller order; Xf may
+// then be null).  Xh16 / Xl16 (nullable): the
 // two-part FP16 operands of the tensor-core tile, point-major [n_pad][dk / 2]
 // 32-bit words (two halves each, f16_split with the scale of *amax_bits);
 // *e0_out (nullable) then receives the form's absolute error part, rounded up.
@@ -21,7 +23,8 @@ cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr,
                         uint32_t *Xh16 = nullptr, uint32_t *Xl16 = nullptr,
-                        const unsigned *amax_bits = nullptr, float *e0_out = nullptr);
+                        const unsigned *amax_bits = nullptr, float *e0_out = nullptr,
+                        const int *inv = nullptr);
 // Raise *amax_bits to the largest magnitude of a caller [d, n] set.
 cudaError_t launch_absmax(const float *X, int64_t ld, int n, int d, unsigned *amax_bits,
                           cudaStream_t s);
@@ -35,14 +38,17 @@ struct SpatialOrder {
     int buckets;             // distance buckets per pivot cell
     int *cellY, *cellX;      // [m], [n]: bin = cell * buckets + bucket (cellX = cellY when Y is X)
     int *permY, *permX;      // sorted position -> caller index
+    int *invY, *invX;        // caller index -> sorted position
     int *startY, *startX;    // [pivots * buckets + 1]: first sorted position of each bin
     int *counters;           // [spatial_counter_ints]
     int *tile_start;         // [row tiles]: first 128-column block of the sweep
+    float *pivf;             // [kSpatialMaxD][pivots]: the pivots' features, feature-major
     float *dcellY, *dcellX;  // [m], [n]: distance to the own pivot, caller order
     float *pdY, *pdX;        // nullable, [m][pivots], [n][pivots]: distances to all
                              // pivots, caller order (the pruned search only)
 };
 inline int spatial_counter_ints(int pivots, int buckets) { return 4 * pivots * buckets + 2 * pivots; }
+constexpr int kSpatialMaxD = 192;  // features the spatial order handles (the tensor tile's)
 cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t ldx, int n,
                                  const float *Y, int64_t ldy, int m, bool alias, int d,
                                  cudaStream_t s);

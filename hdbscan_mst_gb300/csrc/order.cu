@@ -29,59 +29,104 @@ namespace {
 
 int blocks_for(int n, int per) { return std::max(1, (n + per - 1) / per); }
 
-// Nearest pivot of each point of S (feature-major, leading dimension lds):
-// pivots in shared memory, 32 at a time per thread, ties to the lower pivot.
-// Also writes the point's distance to its own pivot (dcell), its distances to
-// all P pivots if pd is not null (point-major [cnt][P]), and raises cmax[cell]
-// to its distance to its own pivot.
+// The pivots' features, feature-major [dp][P] (dp = d rounded up to 16, zero
+// rows past d): pivot p is the column point p * stride of Y.
+__global__ void pivots_kernel(const float *__restrict__ Y, int64_t ldy, int stride, int d, int dp,
+                              int P, float *__restrict__ piv) {
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= dp * P) return;
+    const int f = q / P, p = q % P;
+    piv[q] = f < d ? Y[static_cast<int64_t>(f) * ldy + static_cast<int64_t>(p) * stride] : 0.f;
+}
+
+// Nearest pivot of each point of S (feature-major, leading dimension lds),
+// ties to the lower pivot; also the point's distance to its own pivot
+// (dcell), its distances to all 128 pivots if pd is not null (point-major
+// [cnt][128]), and cmax[cell] raised to the distance to its own pivot.  A CTA
+// of 256 threads takes 64 points against the 128 pivots; each thread
+// accumulates 4 points x 8 pivots with features staged 16 at a time in shared
+// memory.  Each squared distance is the same ascending-feature chain of fused
+// multiply-adds of differences as one point at a time would give.
+constexpr int kCellPts = 64, kCellPiv = 128, kCellK = 16;
 __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S, int64_t lds,
-                                                    int cnt, const float *__restrict__ Y,
-                                                    int64_t ldy, int stride, int d, int P,
-                                                    int *__restrict__ cell,
+                                                    int cnt, int d, const float *__restrict__ piv,
+                                                    int dp, int *__restrict__ cell,
                                                     float *__restrict__ dcell,
                                                     float *__restrict__ pd,
                                                     unsigned *__restrict__ cmax) {
-    extern __shared__ float piv[];  // [P][d]
-    for (int q = threadIdx.x; q < P * d; q += blockDim.x) {
-        const int p = q / d, f = q % d;
-        piv[q] = Y[static_cast<int64_t>(f) * ldy + static_cast<int64_t>(p) * stride];
+    __shared__ __align__(16) float xs[kCellK][kCellPts];
+    __shared__ __align__(16) float ps[kCellK][kCellPiv];
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int i0 = blockIdx.x * kCellPts;
+    float acc[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    for (int f0 = 0; f0 < dp; f0 += kCellK) {
+        for (int q = tid; q < kCellK * kCellPts; q += 256) {
+            const int f = q / kCellPts, c = q % kCellPts;
+            const int i = i0 + c;
+            xs[f][c] = (i < cnt && f0 + f < d) ? S[static_cast<int64_t>(f0 + f) * lds + i] : 0.f;
+        }
+        for (int q = tid; q < kCellK * kCellPiv; q += 256)
+            (&ps[0][0])[q] = piv[static_cast<int64_t>(f0) * kCellPiv + q];
+        __syncthreads();
+#pragma unroll
+        for (int f = 0; f < kCellK; ++f) {
+            const float4 x = *reinterpret_cast<const float4 *>(&xs[f][ty * 4]);
+            const float4 p0 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8]);
+            const float4 p1 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8 + 4]);
+            const float xv[4] = {x.x, x.y, x.z, x.w};
+            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const float t = __fsub_rn(xv[a], pv[b]);
+                    acc[a][b] = __fmaf_rn(t, t, acc[a][b]);
+                }
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= cnt) return;
-    float best = INFINITY;
-    int arg = 0;
-    for (int c = 0; c < P; c += 32) {
-        float acc[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-        for (int f = 0; f < d; ++f) {
-            const float x = S[static_cast<int64_t>(f) * lds + i];
+    for (int a = 0; a < 4; ++a) {
+        const int i = i0 + ty * 4 + a;
+        float best = acc[a][0];
+        int arg = tx * 8;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const float t = x - piv[(c + q) * d + f];
-                acc[q] = __fmaf_rn(t, t, acc[q]);
+        for (int b = 1; b < 8; ++b)
+            if (acc[a][b] < best) {
+                best = acc[a][b];
+                arg = tx * 8 + b;
+            }
+        // least (value, pivot) over the 16 lanes of this point (one half-warp)
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+            if (ob < best || (ob == best && oa < arg)) {
+                best = ob;
+                arg = oa;
             }
         }
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-            if (acc[q] < best) {
-                best = acc[q];
-                arg = c + q;
+        if (i < cnt) {
+            if (pd) {
+                float4 *o = reinterpret_cast<float4 *>(pd + static_cast<int64_t>(i) * kCellPiv + tx * 8);
+                o[0] = make_float4(__fsqrt_rn(acc[a][0]), __fsqrt_rn(acc[a][1]),
+                                   __fsqrt_rn(acc[a][2]), __fsqrt_rn(acc[a][3]));
+                o[1] = make_float4(__fsqrt_rn(acc[a][4]), __fsqrt_rn(acc[a][5]),
+                                   __fsqrt_rn(acc[a][6]), __fsqrt_rn(acc[a][7]));
             }
-        if (pd) {  // the point's distances to these 32 pivots (its point-major row of P)
-            float4 *o = reinterpret_cast<float4 *>(pd + static_cast<int64_t>(i) * P + c);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                o[q] = make_float4(__fsqrt_rn(acc[4 * q]), __fsqrt_rn(acc[4 * q + 1]),
-                                   __fsqrt_rn(acc[4 * q + 2]), __fsqrt_rn(acc[4 * q + 3]));
+            if (tx == 0) {
+                cell[i] = arg;
+                const float dc = __fsqrt_rn(best);
+                dcell[i] = dc;
+                // non-negative floats order like their bits
+                atomicMax(&cmax[arg], __float_as_uint(dc));
+            }
         }
     }
-    cell[i] = arg;
-    const float dc = __fsqrt_rn(best);
-    dcell[i] = dc;
-    // non-negative floats order like their bits
-    atomicMax(&cmax[arg], __float_as_uint(dc));
 }
 
 // Bin of each point: its cell's bucket of distance to the pivot (B buckets
@@ -123,11 +168,13 @@ __global__ void start_cells_kernel(const int *__restrict__ count, int P, int *__
 
 __global__ void scatter_cells_kernel(const int *__restrict__ cell, int cnt,
                                      const int *__restrict__ start, int *__restrict__ cursor,
-                                     int *__restrict__ perm) {
+                                     int *__restrict__ perm, int *__restrict__ inv) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < cnt) {
         const int c = cell[i];
-        perm[start[c] + atomicAdd(&cursor[c], 1)] = i;
+        const int pos = start[c] + atomicAdd(&cursor[c], 1);
+        perm[pos] = i;
+        inv[i] = pos;
     }
 }
 
@@ -148,31 +195,31 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
                                  const float *Y, int64_t ldy, int m, bool alias, int d,
                                  cudaStream_t s) {
     const int P = o.pivots, B = o.buckets, NB = P * B;
+    if (P != kCellPiv || d > kSpatialMaxD) return cudaErrorInvalidValue;
     const int stride = m / P;
-    const size_t smem = static_cast<size_t>(P) * d * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(cells_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    const int dp = (d + kCellK - 1) / kCellK * kCellK;
+    pivots_kernel<<<blocks_for(dp * P, 256), 256, 0, s>>>(Y, ldy, stride, d, dp, P, o.pivf);
     // counters: count and cursor of Y's bins (and of X's), the cells' largest
     // pivot distances of Y (and of X), zeroed
-    e = cudaMemsetAsync(o.counters, 0, sizeof(int) * spatial_counter_ints(P, B), s);
+    cudaError_t e = cudaMemsetAsync(o.counters, 0, sizeof(int) * spatial_counter_ints(P, B), s);
     if (e != cudaSuccess) return e;
     int *countY = o.counters, *cursorY = o.counters + NB, *countX = o.counters + 2 * NB,
         *cursorX = o.counters + 3 * NB;
     unsigned *cmaxY = reinterpret_cast<unsigned *>(o.counters + 4 * NB), *cmaxX = cmaxY + P;
-    cells_kernel<<<blocks_for(m, 256), 256, smem, s>>>(Y, ldy, m, Y, ldy, stride, d, P, o.cellY,
-                                                       o.dcellY, o.pdY, cmaxY);
+    cells_kernel<<<blocks_for(m, kCellPts), 256, 0, s>>>(Y, ldy, m, d, o.pivf, dp, o.cellY,
+                                                         o.dcellY, o.pdY, cmaxY);
     bins_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, o.dcellY, cmaxY, B, m, countY);
     start_cells_kernel<<<1, 32, 0, s>>>(countY, NB, o.startY);
-    scatter_cells_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, m, o.startY, cursorY, o.permY);
-    int extra = 4;  // cells, bins, start, scatter, tile start: 5 kernels, one counted by the caller
+    scatter_cells_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, m, o.startY, cursorY, o.permY,
+                                                           o.invY);
+    int extra = 5;  // pivots, cells, bins, start, scatter, tile start: 6 kernels, one counted by the caller
     if (!alias) {
-        cells_kernel<<<blocks_for(n, 256), 256, smem, s>>>(X, ldx, n, Y, ldy, stride, d, P,
-                                                           o.cellX, o.dcellX, o.pdX, cmaxX);
+        cells_kernel<<<blocks_for(n, kCellPts), 256, 0, s>>>(X, ldx, n, d, o.pivf, dp, o.cellX,
+                                                             o.dcellX, o.pdX, cmaxX);
         bins_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, o.dcellX, cmaxX, B, n, countX);
         start_cells_kernel<<<1, 32, 0, s>>>(countX, NB, o.startX);
         scatter_cells_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, n, o.startX, cursorX,
-                                                               o.permX);
+                                                               o.permX, o.invX);
         extra += 4;
     }
     const int row_tiles = (n + kBM - 1) / kBM;

@@ -30,11 +30,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    uint2 *__restrict__ Xh16,
                                                    uint2 *__restrict__ Xl16,
                                                    const unsigned *__restrict__ amax_bits,
-                                                   float *__restrict__ e0_out) {
+                                                   float *__restrict__ e0_out,
+                                                   const int *__restrict__ inv) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool inside = i < n_pad;
     const bool valid = i < n;
+    // perm: thread i writes position i from the caller's point perm[i]; inv:
+    // thread i reads the caller's point i (coalesced) and writes position
+    // inv[i] (rows of dk floats are contiguous; Xf is then not written)
     const int src = (valid && perm) ? perm[i] : i;
+    const int dst = (valid && inv) ? inv[i] : i;
     float acc = 0.f;
     bool finite = true;
     // two-part FP16 operands: the set's scale 2^e (an exact power of two)
@@ -49,11 +54,11 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                 const int ff = f + q;
                 v[q] = (valid && ff < d) ? X[static_cast<int64_t>(ff) * ld + src] : 0.f;
                 finite = finite && isfinite(v[q]);
-                Xf[static_cast<int64_t>(ff) * n_pad + i] = v[q];
+                if (Xf) Xf[static_cast<int64_t>(ff) * n_pad + dst] = v[q];
                 acc = __fmaf_rn(v[q], v[q], acc);
             }
             if (Xp)
-                *reinterpret_cast<float4 *>(Xp + static_cast<int64_t>(i) * dk + f) =
+                *reinterpret_cast<float4 *>(Xp + static_cast<int64_t>(dst) * dk + f) =
                     make_float4(v[0], v[1], v[2], v[3]);
             if (Xlo) {
                 // x - tf32(x), where tf32() keeps the top 19 bits (the tensor-core
@@ -62,7 +67,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     l[q] = __fsub_rn(v[q], __uint_as_float(__float_as_uint(v[q]) & 0xFFFFE000u));
-                *reinterpret_cast<float4 *>(Xlo + static_cast<int64_t>(i) * dk + f) =
+                *reinterpret_cast<float4 *>(Xlo + static_cast<int64_t>(dst) * dk + f) =
                     make_float4(l[0], l[1], l[2], l[3]);
             }
             if (Xh16) {
@@ -70,14 +75,14 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                 unsigned short h[4], l[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) f16_split(v[q], scale, h[q], l[q]);
-                const int64_t o = (static_cast<int64_t>(i) * dk + f) / 4;
+                const int64_t o = (static_cast<int64_t>(dst) * dk + f) / 4;
                 Xh16[o] = make_uint2(h[0] | (static_cast<unsigned>(h[1]) << 16),
                                      h[2] | (static_cast<unsigned>(h[3]) << 16));
                 Xl16[o] = make_uint2(l[0] | (static_cast<unsigned>(l[1]) << 16),
                                      l[2] | (static_cast<unsigned>(l[3]) << 16));
             }
         }
-        norm[i] = valid ? acc : INFINITY;
+        norm[dst] = valid ? acc : INFINITY;
     }
     if (!finite) atomicOr(status, kStatusNonFinite);
     // largest norm over valid points: warp maximum, one atomic per warp
@@ -119,11 +124,12 @@ __global__ void check_core_kernel(const float *__restrict__ core, int n,
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm, uint32_t *Xh16,
-                        uint32_t *Xl16, const unsigned *amax_bits, float *e0_out) {
+                        uint32_t *Xl16, const unsigned *amax_bits, float *e0_out,
+                        const int *inv) {
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
                                        nbmax_bits, perm, reinterpret_cast<uint2 *>(Xh16),
-                                       reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out);
+                                       reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out, inv);
     return cudaGetLastError();
 }
 
