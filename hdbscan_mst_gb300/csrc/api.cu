@@ -292,6 +292,7 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
             q.Lm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
             q.Hm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
             q.bcell = c.take<int>(p.col_tiles);
+            q.minH = c.take<float>(2 * P);
             q.home_lo = c.take<int>(tiles);
             q.home = c.take<int>(tiles * kHomeBlocks);
             q.list = c.take<int>(tiles * p.col_tiles);
@@ -476,6 +477,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ra.Xp = b.Xp;
         ra.Yp = b.Yp;
         ra.xnorm = b.xnorm;
+        ra.ynorm = b.ynorm;
         ra.nbmax_bits = &b.st->nbmax_bits;
         ra.err_c = coef_up(tensor ? tc_err : (2.0 * p.d + 10.0) * 0x1p-24 * 1.01);
         ra.e0 = &b.st->e0;

@@ -64,6 +64,7 @@ struct PruneBufs {
     float *Lm, *Hm;       // [P][col_tiles]: per column block, least / largest pivot
                           // distance of its points, widened by the distances' rounding bound
     int *bcell;           // [col_tiles] pivot cell of each block's first point
+    float *minH;          // [2 P]: per pivot the least H, then the largest L, over all blocks
     int *home_lo;         // [chunk row tiles] first block of the home range
     int *home;            // [chunk row tiles][kHomeBlocks] home lists
     int *list;            // [chunk row tiles][col_tiles] blocks of the second pass
@@ -166,7 +167,7 @@ struct KnnRefineArgs {
     const int *part_idx;
     int splits, chunk_rows_pad, row_base, row_end;
     const float *Xp, *Yp;  // point-major [.][dk]
-    const float *xnorm;
+    const float *xnorm, *ynorm;
     const unsigned *nbmax_bits;
     float err_c;      // the ranking error is at most err_c (|x|^2 + |y|^2) + *e0
     const float *e0;  // (err_c rounded up; e0 the FP16 operands' absolute part, else 0)

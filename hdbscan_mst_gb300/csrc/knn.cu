@@ -285,10 +285,32 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     __syncwarp();
     A = __shfl_sync(0xffffffffu, A, leader);
 
-    // 2. Exact distance of every kept candidate.
+    // 2. Exact distance of every kept candidate that can still reach the top
+    //    k.  The first k by t each have a true squared distance of at most
+    //    xn + t + c (xn + yn) + e0; a candidate whose lower bound xn + t -
+    //    c (xn + yn) - e0 exceeds the largest of those by more than the float32
+    //    evaluation of dist() can move (both sides, rounded outward) ranks
+    //    after the k-th and needs no exact distance (its key stays last).
     const int j = sel_j[group * KP + gl];
+    bool need = active && j >= 0 && j < a.m;
+    {
+        const float xn = active ? a.xnorm[row] : 0.f;
+        const float tj = sel_t[group * KP + gl];
+        float hi = -INFINITY, lo = INFINITY;
+        if (need) {
+            const float err = __fadd_ru(__fmul_ru(a.err_c, __fadd_ru(xn, a.ynorm[j])), *a.e0);
+            if (gl < a.k) hi = __fadd_ru(tj, err);
+            lo = __fsub_rd(tj, err);
+        }
+#pragma unroll
+        for (int o = 1; o < KP; o <<= 1) hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        const float mg = static_cast<float>(a.d + 8) * 0x1p-24f;
+        if (need && gl >= a.k &&
+            __fmul_rd(__fadd_rd(lo, xn), __fsub_rd(1.f, mg)) > __fmul_ru(__fadd_ru(hi, xn), __fadd_ru(1.f, mg)))
+            need = false;
+    }
     unsigned long long key = kNoKey;
-    if (active && j >= 0 && j < a.m) {
+    if (need) {
         const float4 *xp = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(row) * a.dk);
         const float4 *yp = reinterpret_cast<const float4 *>(a.Yp + static_cast<int64_t>(j) * a.dk);
         float acc = 0.f;

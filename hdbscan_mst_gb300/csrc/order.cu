@@ -147,23 +147,41 @@ __global__ void bins_kernel(int *__restrict__ cell, const float *__restrict__ dc
     atomicAdd(&count[bin], 1);
 }
 
-// start[c] = points in bins before c (one warp), start[P] = all
-__global__ void start_cells_kernel(const int *__restrict__ count, int P, int *__restrict__ start) {
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int b = 0; b < P; b += 32) {
-        const int c = b + lane;
-        const int v = c < P ? count[c] : 0;
-        int incl = v;
+// start[c] = points in bins before c, start[P] = all: one CTA of 1024
+// threads, each summing a run of consecutive bins, then a block-wide scan of
+// the runs' totals.
+__global__ void __launch_bounds__(1024) start_cells_kernel(const int *__restrict__ count, int P,
+                                                           int *__restrict__ start) {
+    __shared__ int s_warp[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (P + 1023) / 1024;
+    const int b0 = min(tid * per, P), b1 = min(b0 + per, P);
+    int run = 0;
+    for (int c = b0; c < b1; ++c) run += count[c];
+    int incl = run;  // inclusive scan of the runs: within the warp, then over warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
         }
-        if (c < P) start[c] = carry + incl - v;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+        s_warp[lane] = w;
     }
-    if (lane == 0) start[P] = carry;
+    __syncthreads();
+    int acc = (warp ? s_warp[warp - 1] : 0) + incl - run;
+    for (int c = b0; c < b1; ++c) {
+        start[c] = acc;
+        acc += count[c];
+    }
+    if (tid == 1023) start[P] = acc;
 }
 
 __global__ void scatter_cells_kernel(const int *__restrict__ cell, int cnt,
@@ -209,7 +227,7 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
     cells_kernel<<<blocks_for(m, kCellPts), 256, 0, s>>>(Y, ldy, m, d, o.pivf, dp, o.cellY,
                                                          o.dcellY, o.pdY, cmaxY);
     bins_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, o.dcellY, cmaxY, B, m, countY);
-    start_cells_kernel<<<1, 32, 0, s>>>(countY, NB, o.startY);
+    start_cells_kernel<<<1, 1024, 0, s>>>(countY, NB, o.startY);
     scatter_cells_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, m, o.startY, cursorY, o.permY,
                                                            o.invY);
     int extra = 5;  // pivots, cells, bins, start, scatter, tile start: 6 kernels, one counted by the caller
@@ -217,7 +235,7 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
         cells_kernel<<<blocks_for(n, kCellPts), 256, 0, s>>>(X, ldx, n, d, o.pivf, dp, o.cellX,
                                                              o.dcellX, o.pdX, cmaxX);
         bins_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, o.dcellX, cmaxX, B, n, countX);
-        start_cells_kernel<<<1, 32, 0, s>>>(countX, NB, o.startX);
+        start_cells_kernel<<<1, 1024, 0, s>>>(countX, NB, o.startX);
         scatter_cells_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, n, o.startX, cursorX,
                                                                o.permX, o.invX);
         extra += 4;

@@ -76,9 +76,43 @@ __global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict
         hi = fmaxf(hi, v);
     }
     const int64_t o = static_cast<int64_t>(p) * col_tiles + b;
-    Lm[o] = pos1 > pos0 ? __double2float_rd(static_cast<double>(lo) * (1.0 - eps)) : INFINITY;
-    Hm[o] = pos1 > pos0 ? __double2float_ru(static_cast<double>(hi) * (1.0 + eps)) : -INFINITY;
+    const float L = pos1 > pos0 ? __double2float_rd(static_cast<double>(lo) * (1.0 - eps)) : INFINITY;
+    const float H = pos1 > pos0 ? __double2float_ru(static_cast<double>(hi) * (1.0 + eps)) : -INFINITY;
+    Lm[o] = L;
+    Hm[o] = H;
     if (p == 0) bcell[b] = pos1 > pos0 ? binY[permY[pos0]] / B : 0;
+}
+
+// Per pivot (one CTA each): the least H and the largest L over all blocks.
+__global__ void __launch_bounds__(256) pivot_range_kernel(const float *__restrict__ Lm,
+                                                          const float *__restrict__ Hm,
+                                                          int col_tiles, float *__restrict__ minH,
+                                                          float *__restrict__ maxL) {
+    __shared__ float s_h[8], s_l[8];
+    const int p = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float h = INFINITY, l = -INFINITY;
+    for (int b = tid; b < col_tiles; b += 256) {
+        h = fminf(h, Hm[static_cast<int64_t>(p) * col_tiles + b]);
+        l = fmaxf(l, Lm[static_cast<int64_t>(p) * col_tiles + b]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        h = fminf(h, __shfl_xor_sync(0xffffffffu, h, o));
+        l = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, o));
+    }
+    if (lane == 0) {
+        s_h[warp] = h;
+        s_l[warp] = l;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < 8; ++w) {
+            h = fminf(h, s_h[w]);
+            l = fmaxf(l, s_l[w]);
+        }
+        minH[p] = h;
+        maxL[p] = l;
+    }
 }
 
 // Home range of each row tile of the chunk: kHomeBlocks blocks centred on the
@@ -120,10 +154,13 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
                                                           int *__restrict__ list,
                                                           int *__restrict__ count,
                                                           int *__restrict__ slabs,
-                                                          unsigned *__restrict__ b_gthr) {
+                                                          unsigned *__restrict__ b_gthr,
+                                                          const float *__restrict__ minH,
+                                                          const float *__restrict__ maxL) {
     __shared__ float s_ub[kBM];
     __shared__ float s_A[P], s_B[P];
     __shared__ int s_wc[kBM / 32];
+    __shared__ int s_useful[P], s_nuseful;
     const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int local = rt * kBM + tid;
     const int row = a.row_base + local;
@@ -181,8 +218,25 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         }
         s_A[tid] = A;
         s_B[tid] = Bv;
+        // a pivot that separates no block from this hull is not worth testing
+        // (an outlier tile's hull covers every block for most pivots)
+        const bool useful = minH[tid] < A || maxL[tid] > Bv;
+        const unsigned bal = __ballot_sync(0xffffffffu, useful);
+        if (lane == 0) s_wc[warp] = __popc(bal);
+        __syncthreads();
+        int off = 0;
+        for (int w = 0; w < warp; ++w) off += s_wc[w];
+        if (useful) s_useful[off + __popc(bal & lanemask_lt())] = tid;
+        const int nu = s_wc[0] + s_wc[1] + s_wc[2] + s_wc[3];
+        __syncthreads();
+        // pad to whole groups of 32 with repeats of the first useful pivot (a
+        // repeated test changes nothing), so the tests below run 32 at a time
+        const int npad = (nu + 31) / 32 * 32;
+        if (tid >= nu && tid < npad) s_useful[tid] = s_useful[0];
+        if (tid == 0) s_nuseful = npad;
     }
     __syncthreads();
+    const int nuseful = s_nuseful;
 
     // 3. Blocks outside the home range, outward from it (threads 0..63 to the
     //    right, 64..127 to the left, 64 offsets per step), kept unless one
@@ -200,12 +254,13 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
             const int p0 = bcell[b];
             need = !(Hm[static_cast<int64_t>(p0) * a.col_tiles + b] < s_A[p0] ||
                      Lm[static_cast<int64_t>(p0) * a.col_tiles + b] > s_B[p0]);
-            for (int p = 0; p < P && need; p += 32) {
+            for (int u = 0; u < nuseful && need; u += 32) {
                 bool sep = false;
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
-                    const int64_t i = static_cast<int64_t>(p + q) * a.col_tiles + b;
-                    sep |= (__ldg(Hm + i) < s_A[p + q]) | (__ldg(Lm + i) > s_B[p + q]);
+                    const int pp = s_useful[u + q];
+                    const int64_t i = static_cast<int64_t>(pp) * a.col_tiles + b;
+                    sep |= (__ldg(Hm + i) < s_A[pp]) | (__ldg(Lm + i) > s_B[pp]);
                 }
                 need = !sep;
             }
@@ -242,6 +297,8 @@ cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n,
     block_bounds_kernel<<<col_tiles, P, 0, s>>>(b.pdSY, m, col_tiles, (d + 8.0) * 0x1p-24,
                                                 o.cellY, o.permY, o.buckets, b.Lm, b.Hm,
                                                 b.bcell);
+    pivot_range_kernel<<<P, 256, 0, s>>>(b.Lm, b.Hm, col_tiles, b.minH, b.minH + P);
+    ++extra;
     count_extra_launches(extra);
     return cudaGetLastError();
 }
@@ -256,7 +313,8 @@ cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaSt
 
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s) {
     prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.bcell, b.home_lo,
-                                                   b.list, b.count, b.slabs, b.gthr);
+                                                   b.list, b.count, b.slabs, b.gthr, b.minH,
+                                                   b.minH + P);
     return cudaGetLastError();
 }
 
