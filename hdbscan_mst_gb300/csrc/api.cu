@@ -376,7 +376,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     const double tc_err = f16 ? tc::err_coef_f16(p.d, p.dk) : tc::err_coef(p.d, p.dk);
     // pruned search: the spatial order's pivots bound the column blocks (prune.cu)
     const bool prune = spatial && b.prune.list != nullptr;
-    const int nh = std::min(kHomeBlocks, p.col_tiles);
+    const int nh = home_blocks(p.col_tiles);
     const int chunk_cap = (p.col_tiles + kPruneChunks - 1) / kPruneChunks;
     if (prune)
         LAUNCH(K_PRUNE, s, launch_prune_setup(b.order, b.prune, p.n, p.m, p.alias, p.col_tiles,
@@ -412,7 +412,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.f16 = f16 ? 1 : 0;
         ta.amax_bits = amax;
         if (prune) {
-            // home pass: slab 0, the kHomeBlocks blocks around the tile's own bin
+            // home pass: slab 0, the nh blocks around the tile's own bin
             PruneHomeArgs ha{};
             ha.o = &b.order;
             ha.n = p.n;
@@ -420,6 +420,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             ha.col_tiles = p.col_tiles;
             ha.row_tile0 = base / kBM;
             ha.row_tiles = row_tiles;
+            ha.nh = nh;
             ha.alias = p.alias;
             LAUNCH(K_PRUNE, s, launch_prune_home(ha, b.prune, s));
             KnnTileArgs h = ta;
@@ -448,6 +449,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.row_end = p.n;
             pa.row_tiles = row_tiles;
             pa.chunk_cap = chunk_cap;
+            pa.nh = nh;
             pa.blocks_total = &b.st->tile_blocks;
             LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
             // second pass: slabs 1 .., in chunks of chunk_cap blocks

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 
@@ -57,7 +58,14 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
 // Column blocks of the tensor-core k-NN that can hold none of a row tile's
 // nearest neighbours, bounded through the pivots of the spatial order.
 constexpr int kPrunePivots = 128;   // = SpatialOrder::pivots when pruning
-constexpr int kHomeBlocks = 3;      // blocks of the first pass per row tile
+// Blocks of the first pass per row tile: about 1% of the column blocks, 3 to
+// kHomeBlocks (200k x 61, of 1, 3, 5, 7, 9, 13, 21 and 31 blocks 13 was
+// fastest: a larger home gives the second pass a tighter first threshold).
+constexpr int kHomeBlocks = 13;
+inline int home_blocks(int col_tiles) {
+    const int h = col_tiles / 100;
+    return std::min(col_tiles, h < 3 ? 3 : (h > kHomeBlocks ? kHomeBlocks : h));
+}
 constexpr int kPruneChunks = 4;     // CTAs per row tile in the second pass (at most)
 struct PruneBufs {
     float *pdSY, *pdSX;   // [m_pad][P], [n_pad][P] pivot distances in sorted order
@@ -79,6 +87,7 @@ cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n,
 struct PruneHomeArgs {
     const SpatialOrder *o;
     int n, m, col_tiles, row_tile0, row_tiles;  // row tiles of this chunk: row_tile0 ..
+    int nh;                                     // home_blocks(col_tiles)
     bool alias;
 };
 // Home range of every row tile of a chunk: the kHomeBlocks blocks around the
@@ -93,6 +102,7 @@ struct PruneListArgs {
     const float *e0;             // its absolute part (FP16 operands; 0 otherwise)
     int col_tiles, row_base, row_end, row_tiles;
     int chunk_cap;               // blocks per CTA of the second pass
+    int nh;                      // blocks of the home range
     unsigned long long *blocks_total;  // += blocks the tile evaluates (both passes)
 };
 // Upper bound of each row's k-th distance from its home list, the row tile's

@@ -15,7 +15,7 @@
 // H < min over rows (d(x, p) - ub(x)) or L > max over rows (d(x, p) + ub(x)).
 //
 // The search runs in two passes of the tile.  The first ("home") pass takes
-// the kHomeBlocks blocks around the columns of the tile's own bin; from its
+// a few blocks (home_blocks) around the columns of the tile's own bin; from its
 // sorted candidates each row gets ub(x), a rigorous bound of the float32
 // distance the refine will rank by (below).  The row tile's hull per pivot
 // then selects the blocks of the second pass, which starts with the home
@@ -115,14 +115,14 @@ __global__ void __launch_bounds__(256) pivot_range_kernel(const float *__restric
     }
 }
 
-// Home range of each row tile of the chunk: kHomeBlocks blocks centred on the
+// Home range of each row tile of the chunk: nh blocks centred on the
 // block that holds, in the columns' sorted order, the position matching the
 // tile's middle row (its bin, at the same relative rank).  When Y is X that
 // block holds the tile's own rows.
 __global__ void home_kernel(const int *__restrict__ binX, const int *__restrict__ permX,
                             const int *__restrict__ startX, const int *__restrict__ startY,
-                            int n, int col_tiles, int row_tile0, int row_tiles, bool alias,
-                            int *__restrict__ home_lo, int *__restrict__ home) {
+                            int n, int col_tiles, int row_tile0, int row_tiles, int nh,
+                            bool alias, int *__restrict__ home_lo, int *__restrict__ home) {
     const int rt = blockIdx.x * blockDim.x + threadIdx.x;
     if (rt >= row_tiles) return;
     const int gt = row_tile0 + rt;
@@ -138,10 +138,9 @@ __global__ void home_kernel(const int *__restrict__ binX, const int *__restrict_
         const int64_t pos = startY[bin] + (cy > 0 ? min(cy - 1, rank * cy / (cx > 0 ? cx : 1)) : 0);
         hb = static_cast<int>(pos / kBN);
     }
-    const int nh = min(kHomeBlocks, col_tiles);
-    const int h0 = max(0, min(hb - kHomeBlocks / 2, col_tiles - nh));
+    const int h0 = max(0, min(hb - nh / 2, col_tiles - nh));
     home_lo[rt] = h0;
-    for (int i = 0; i < kHomeBlocks; ++i) home[rt * kHomeBlocks + i] = h0 + min(i, nh - 1);
+    for (int i = 0; i < nh; ++i) home[rt * kHomeBlocks + i] = h0 + i;
 }
 
 // One CTA (128 threads) per row tile of the chunk.
@@ -164,7 +163,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int local = rt * kBM + tid;
     const int row = a.row_base + local;
-    const int nh = min(kHomeBlocks, a.col_tiles);
+    const int nh = a.nh;
 
     // 1. ub(x) from the k best candidates of the home pass (sorted by (t, j)).
     //    True squared distance of candidate j: at most |x|^2 + t_j + c (|x|^2 +
@@ -306,7 +305,7 @@ cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n,
 cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaStream_t s) {
     const SpatialOrder &o = *a.o;
     home_kernel<<<blocks_for(a.row_tiles, 128), 128, 0, s>>>(
-        o.cellX, o.permX, o.startX, o.startY, a.n, a.col_tiles, a.row_tile0, a.row_tiles,
+        o.cellX, o.permX, o.startX, o.startY, a.n, a.col_tiles, a.row_tile0, a.row_tiles, a.nh,
         a.alias, b.home_lo, b.home);
     return cudaGetLastError();
 }
