@@ -68,20 +68,20 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.08 MB read, 2.59 MB written) and the
-        # pruned second pass (74.57 MB read, 26.32 MB written)
-        "bytes": 52.08e6 + 2.59e6 + 74.57e6 + 26.32e6,
+        # per step: the home pass (52.14 MB read, 3.19 MB written) and the
+        # pruned second pass (74.68 MB read, 25.46 MB written)
+        "bytes": 52.14e6 + 3.19e6 + 74.68e6 + 25.46e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
         "sha256": "d8d232505c67120036fcce50ca5c5d39732e48320ae91936f68e5821470ceef8",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the four rounds' launches (54.88 + 53.99 + 158.41 + 120.57 MB
-        # read, 0.00 + 0.00 + 3.46 + 3.15 MB written)
-        "bytes": (54.88 + 53.99 + 158.41 + 120.57 + 3.46 + 3.15) * 1e6,
+        # per step: the four rounds' launches (55.20 + 54.10 + 156.43 + 121.29 MB
+        # read, 0.00 + 0.00 + 4.43 + 2.52 MB written)
+        "bytes": (55.20 + 54.10 + 156.43 + 121.29 + 4.43 + 2.52) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "18597b2f2a9f00a43c4817c4ce591306f1b76348ab59ec1aafc6d61cfcc484d8",
+        "sha256": "1f8679e6ae0be27e1770d7a76151d4fd64596bb4c6a03fb9b1b11521c68e6be8",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0

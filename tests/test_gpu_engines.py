@@ -123,3 +123,26 @@ def test_fp16_mst_identical_50k(h):
     scanned = sum(a for a, _, _ in rounds)
     redone = sum(x for _, _, x in rounds)
     assert redone <= max(50, scanned // 100), rounds
+
+
+def test_fp16_wide_dynamic_range(h):
+    """Clusters of unit scale next to a few points 1e5 away: the FP16 form's
+    scale is set by the far points, its absolute error term dwarfs the
+    clusters' distances, and the rounding proof must send those rows to the
+    exact search rather than accept a wrong list.  Lists and trees stay
+    identical to the FP32 engine's."""
+    X = workloads.small(20000, 48, seed=21, dup_frac=0.01).astype(np.float64)
+    X /= np.abs(X).max()
+    X[:, :8] *= 1.0e5  # eight far points
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    out, trees = {}, {}
+    for eng in ("simt", "tensor"):
+        h.set_engine(eng)
+        out[eng] = tuple(np_(t) for t in h.core_distances(dev(X), 7))
+        e, w = h.mr_mst(dev(X), *(dev(t) for t in out[eng]))
+        trees[eng] = (np_(e), np_(w))
+    h.set_engine("auto")
+    for u, v in zip(out["simt"], out["tensor"]):
+        assert np.array_equal(u, v)
+    assert np.array_equal(trees["simt"][0], trees["tensor"][0])
+    assert np.array_equal(trees["simt"][1], trees["tensor"][1])
