@@ -43,10 +43,8 @@ struct TcScanParams {
 
 __shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
-// per warp, two tiles: the columns' norms, core distances and point indices
+// per warp, two tiles: the columns' norms
 __shared__ float4 s_cnorm[kEpiWarps][2][kTileCols / 4];
-__shared__ float s_ccore[kEpiWarps][2][kTileCols];
-__shared__ int s_corig[kEpiWarps][2][kTileCols];
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
                                             float &dropped) {
@@ -145,16 +143,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         const int own_lo = valid ? a.comp_start[rc] : 0;
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
 
+        // only the column norms are read per tile; the rare candidate path
+        // reads a column's core distance and point index from global memory
         const auto prefetch = [&](int col0, int buf) {
-            static_assert(kTileCols == 64, "one 16-byte copy per lane and array half");
-            if (lane < 16) {
-                cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
-                cp_async16(&s_corig[warp][buf][lane * 4], a.col_orig + col0 + lane * 4);
-            } else {
-                cp_async16(&s_ccore[warp][buf][(lane - 16) * 4], a.col_core + col0 + (lane - 16) * 4);
-            }
+            static_assert(kTileCols == 64, "one 16-byte copy per lane");
+            if (lane < 16) cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
         };
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+            // the other groups' published 4th values, once per tile (a stale
+            // value is only looser)
+            float thr_tile = tau0;
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) thr_tile = fminf(thr_tile, s_row_thr[q][row]);
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 const int cb0 = col0 + cc * 32;
@@ -183,9 +183,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                     for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
                 // v >= t, so a batch whose least t does not beat the row's
                 // least published 4th value cannot change any list's 4 best
-                float thr = fminf(key_v(keys[kKeep - 1]), tau0);
-#pragma unroll
-                for (int q = 0; q < kParts; ++q) thr = fminf(thr, s_row_thr[q][row]);
+                const float thr = fminf(key_v(keys[kKeep - 1]), thr_tile);
                 if (m16[0] < thr) {
                     const uint32_t own =
                         bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
@@ -197,12 +195,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                             mask &= mask - 1;
                             const int col = cb0 + j;
                             if (col >= a.n) break;
-                            const float cbc = s_ccore[warp][buf][cc * 32 + j];
+                            const float cbc = __ldg(a.col_core + col);
                             const float vv = fmaxf(
                                 fmaxf(pick32(v, j), __fsub_rn(__fmul_rn(cbc, cbc), na)), ra);
                             const unsigned long long key =
                                 (static_cast<unsigned long long>(float_order(vv)) << 32) |
-                                static_cast<unsigned>(s_corig[warp][buf][cc * 32 + j]);
+                                static_cast<unsigned>(__ldg(a.col_orig + col));
                             keep_insert(keys, key, dropped);
                         }
                         s_row_thr[group][row] = key_v(keys[kKeep - 1]);
