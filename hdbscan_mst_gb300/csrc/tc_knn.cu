@@ -112,13 +112,16 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
         seq.wrap = a.col_tiles * kSub;
     }
     if (a.blist) {
-        // pruned search: chunk c of the row tile's block list (the last
-        // chunks, which only long lists have, are dispatched first)
+        // pruned search: the CTAs of chunks c >= 1, which only long lists
+        // have, are dispatched first (c = gridDim.y - 1 - blockIdx.y); the
+        // first of a row tile's CTAs to run takes the list's first range (its
+        // nearest blocks), so the threshold it shares tightens early
         const int cnt = a.bcount ? a.bcount[row_tile] : a.blist_count;
         const int c = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
-        const int begin = c * a.chunk_cap;
+        const int nch = (cnt + a.chunk_cap - 1) / a.chunk_cap;
+        if (c >= nch) return;  // the whole CTA, before any barrier or allocation
+        const int begin = (nch - 1 - c) * a.chunk_cap;
         const int len = min(a.chunk_cap, cnt - begin);
-        if (len <= 0) return;  // the whole CTA, before any barrier or allocation
         split = a.slab_base + c;
         seq = TileSeq(0, 2 * len, 0, 0);
         const int *gl = a.blist + static_cast<int64_t>(row_tile) * a.blist_stride + begin;
