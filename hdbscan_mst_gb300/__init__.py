@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "knn", "core_distances", "mr_mst", "hdbscan_mst", "HdbmstError", "HdbmstUnavailable",
     "launch_count", "profile_enable", "profile_read", "last_mst_rounds", "library_path", "KMAX",
-    "set_engine",
+    "set_engine", "set_scan_form",
 ]
 
 KMAX = 32
@@ -93,6 +93,10 @@ def _load():
     L.hdbmst_last_mst_rounds.restype = i32
     L.hdbmst_set_engine.argtypes = [i32]
     L.hdbmst_set_engine.restype = i32
+    L.hdbmst_set_scan_form.argtypes = [i32]
+    L.hdbmst_set_scan_form.restype = i32
+    L.hdbmst_last_mst_symmetric.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
+    L.hdbmst_last_mst_symmetric.restype = i32
     L.hdbmst_last_cuda_error.restype = ctypes.c_char_p
     L.hdbmst_last_knn_exact_rows.restype = ctypes.c_int64
     L.hdbmst_last_knn_tile_pairs.restype = ctypes.c_int64
@@ -318,6 +322,26 @@ def set_engine(engine: str) -> str:
     are identical whichever engine runs."""
     prev = _load().hdbmst_set_engine(ENGINES[engine])
     return {v: k for k, v in ENGINES.items()}[prev]
+
+
+SCAN_FORMS = {"auto": 0, "one_sided": 1, "symmetric": 2}
+
+
+def set_scan_form(form: str) -> str:
+    """Select the form of the Boruvka scan on the tensor cores ("auto",
+    "one_sided" or "symmetric"); returns the previous one.  The tree is the
+    same whichever form runs."""
+    prev = _load().hdbmst_set_scan_form(SCAN_FORMS[form])
+    return {v: k for k, v in SCAN_FORMS.items()}[prev]
+
+
+def last_mst_symmetric() -> list[int]:
+    """Per Boruvka round of the last mr_mst call: pairs the symmetric scan
+    recorded, or -1 for a one-sided round."""
+    L = _load()
+    a = (ctypes.c_int64 * 64)()
+    r = L.hdbmst_last_mst_symmetric(a, 64)
+    return [int(a[i]) for i in range(min(r, 64))]
 
 
 def launch_count() -> int:

@@ -42,8 +42,12 @@ bool use_tensor_scan(int dk) {
 // 128-byte row of halves per part), unless TF32 is asked for.
 bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
 
-// per-round record of the last hdbmst_mr_mst call: points scanned, edges so far
-std::vector<int64_t> g_round_active, g_round_edges, g_round_exact;
+// Form of the Boruvka scan on the tensor cores (HDBMST_SCAN_*), process-wide.
+int g_scan_form = HDBMST_SCAN_AUTO;
+
+// per-round record of the last hdbmst_mr_mst call: points scanned, edges so
+// far, rows searched exactly, pairs the symmetric scan recorded (-1: one-sided)
+std::vector<int64_t> g_round_active, g_round_edges, g_round_exact, g_round_sym;
 // rows of the last k-NN / core-distance call searched exactly
 int64_t g_knn_exact_rows = 0;
 // (row, column) pairs the distance tile of the last k-NN / core-distance call
@@ -139,6 +143,8 @@ struct DevStatus {
     float e0;                        // the FP16 form's absolute ranking error (0 otherwise)
     unsigned long long tile_blocks;  // 128 x 128 blocks the pruned k-NN tile evaluated
     unsigned long long scan_pairs;   // (row, column) pairs the Boruvka scan evaluated
+    unsigned sym_umax;               // symmetric scan: the largest component bound
+    int sym_pairs;                   // symmetric scan: pairs recorded (may exceed the list)
 };
 
 // A ranking error coefficient as the float32 the proofs use, rounded up.
@@ -814,24 +820,110 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     g_mst_scan_pairs = 0;
     int *size = b.counters, *act_size = b.counters + N, *cursor = b.counters + 2 * N,
         *act_cursor = b.counters + 3 * N, *totals = b.counters + 4 * N;
+    const float err_c = coef_up(f16      ? tc::err_coef_f16(d, p.dk)
+                                : tensor ? tc::err_coef(d, p.dk)
+                                         : (2.0 * d + 10.0) * 0x1p-24 * 1.01);
+    g_round_sym.clear();
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
         int fallback = 0;
+        int64_t recorded = -1;
         if (shortcuts) {
             LAUNCH(K_NBR_CANDIDATE, s, launch_nbr_candidate(N, L, knn_idx, knn_dist, core, b.comp,
                                                             b.cache, b.cand, b.proven, b.ub,
                                                             &b.st->status, s));
         }
-        CUDA_OK(cudaMemsetAsync(b.counters, 0, sizeof(int) * (4 * static_cast<size_t>(N) + 8), s));
-        CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
-        LAUNCH(K_ACTIVE, s, launch_classify(N, shortcuts ? b.proven : nullptr, core, b.comp,
-                                            shortcuts ? b.ub : nullptr, b.act_flag, size, act_size,
-                                            &b.st->act_count, s));
-        hdbmst_status rs = read_status(b.st, h, s);
+        // the points that need a scan (act_flag) and the per-label counts
+        const auto classify = [&]() -> hdbmst_status {
+            CUDA_OK(cudaMemsetAsync(b.counters, 0, sizeof(int) * (4 * static_cast<size_t>(N) + 8), s));
+            CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
+            LAUNCH(K_ACTIVE, s, launch_classify(N, shortcuts ? b.proven : nullptr, core, b.comp,
+                                                shortcuts ? b.ub : nullptr, b.act_flag, size,
+                                                act_size, &b.st->act_count, s));
+            return HDBMST_OK;
+        };
+        hdbmst_status rs = classify();
+        if (rs != HDBMST_OK) return rs;
+        rs = read_status(b.st, h, s);
         if (rs != HDBMST_OK) return rs;
         if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
         if (h.status & kStatusBadList) return HDBMST_ERR_ARG;
-        const int na = h.act_count;
-        if (na > 0) {
+        int na = h.act_count;
+        bool sym_done = false;
+        const bool sym = na > 0 && tensor && shortcuts && g_scan_form != HDBMST_SCAN_ONE_SIDED &&
+                         (g_scan_form == HDBMST_SCAN_SYMMETRIC || 2 * static_cast<int64_t>(na) >= N);
+        if (sym) {
+            // the set P in grouped order: rows and columns of the symmetric scan
+            CUDA_OK(cudaMemsetAsync(b.counters, 0, sizeof(int) * (4 * static_cast<size_t>(N) + 8), s));
+            CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
+            CUDA_OK(cudaMemsetAsync(&b.st->sym_umax, 0, 2 * sizeof(unsigned), s));
+            LAUNCH(K_ACTIVE, s, launch_sym_classify(N, b.comp, b.ub, core, &b.st->sym_umax,
+                                                    b.act_flag, size, act_size, &b.st->act_count, s));
+            rs = read_status(b.st, h, s);
+            if (rs != HDBMST_OK) return rs;
+            const int np = h.act_count;
+            const int np_pad = static_cast<int>(round_up(std::max(np, 1), kBM));
+            LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), b.comp, core, b.norm,
+                                             b.act_flag, size, act_size, b.start, b.act_start,
+                                             cursor, act_cursor, totals, b.perm, b.col_comp,
+                                             b.col_core, b.col_norm, b.act_idx, s));
+            LAUNCH(K_GATHER, s, launch_gather(np, np_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
+                                              b.comp, b.norm, nullptr, b.act_core, b.act_comp,
+                                              b.act_norm, s));
+            LAUNCH(K_GATHER, s, launch_gather_points(np, np_pad, dkw, b.act_idx, op_hi, op_lo,
+                                                     b.Xa_hi, b.Xa_lo, s));
+            // scratch of the one-sided scan, idle in this round: the tile
+            // records, the bounds (the sort's buffer, used after the rounds)
+            // and the list of recorded pairs
+            int4 *tile_meta = reinterpret_cast<int4 *>(b.part_tau);
+            unsigned *theta = b.w2;
+            int2 *pairs = reinterpret_cast<int2 *>(b.part_key);
+            LAUNCH(K_GATHER, s, launch_sym_prepare(N, np, np_pad, b.act_comp, b.ub, theta,
+                                                   b.act_norm, tile_meta, s));
+            SymArgs ya{};
+            ya.np = np;
+            ya.ld = np_pad;
+            ya.blocks = np_pad / kBM;
+            ya.idx = b.act_idx;
+            ya.core = b.act_core;
+            ya.comp = b.act_comp;
+            ya.norm = b.act_norm;
+            ya.comp_start = b.act_start;
+            ya.comp_size = act_size;
+            ya.tile_meta = tile_meta;
+            ya.theta = theta;
+            ya.cand = b.cand;
+            ya.pairs = pairs;
+            ya.pair_count = &b.st->sym_pairs;
+            ya.pair_cap = static_cast<int>(
+                std::min<size_t>(scan_part_entries(kMaxSplits, p.n_pad), 1u << 30));
+            ya.d = d;
+            ya.dk = p.dk;
+            ya.err_c = err_c;
+            ya.e0 = &b.st->e0;
+            ya.f16 = f16 ? 1 : 0;
+            ya.amax_bits = &b.st->amax_bits;
+            ya.tile_pairs = &b.st->scan_pairs;
+            ya.status = &b.st->status;
+            LAUNCH(K_SCAN, s, launch_tc_sym(ya, b.Xa_hi, b.Xa_lo, s));
+            rs = read_status(b.st, h, s);
+            if (rs != HDBMST_OK) return rs;
+            if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
+            if (h.sym_pairs <= ya.pair_cap) {
+                LAUNCH(K_SCAN_REFINE, s, launch_sym_pairs_exact(pairs, h.sym_pairs, b.act_idx, b.Xp,
+                                                                p.dk, core, b.cand, s));
+                sym_done = true;
+                recorded = h.sym_pairs;
+                na = np;
+            } else {
+                // the list overflowed: this round one-sided
+                rs = classify();
+                if (rs != HDBMST_OK) return rs;
+                rs = read_status(b.st, h, s);
+                if (rs != HDBMST_OK) return rs;
+                na = h.act_count;
+            }
+        }
+        if (na > 0 && !sym_done) {
             const int na_pad = static_cast<int>(round_up(na, kBM));
             LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), b.comp, core, b.norm,
                                              b.act_flag, size, act_size, b.start, b.act_start,
@@ -886,9 +978,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.fb_count = &b.st->fb_count;
             sa.fb_rows = b.fb_rows;
             sa.status = &b.st->status;
-            sa.err_c = coef_up(f16      ? tc::err_coef_f16(d, p.dk)
-                               : tensor ? tc::err_coef(d, p.dk)
-                                        : (2.0 * d + 10.0) * 0x1p-24 * 1.01);
+            sa.err_c = err_c;
             sa.e0 = &b.st->e0;
             sa.f16 = f16 ? 1 : 0;
             sa.amax_bits = &b.st->amax_bits;
@@ -937,7 +1027,8 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             }
         }
         LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, b.proven,
-                                              b.act_flag, shortcuts ? b.cache : nullptr, s, 0));
+                                              sym_done ? nullptr : b.act_flag,
+                                              shortcuts ? b.cache : nullptr, s, 0));
         LAUNCH(K_COMP_MIN, s, launch_comp_min(N, b.cand, b.comp, b.ck64, b.chi, nullptr, nullptr,
                                               nullptr, s, 1));
         LAUNCH(K_HOOK, s, launch_hook(N, b.comp, b.ck64, b.chi, b.parent, b.e_lo, b.e_hi,
@@ -954,6 +1045,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         g_round_active.push_back(na);
         g_round_edges.push_back(edges);
         g_round_exact.push_back(fallback);
+        g_round_sym.push_back(recorded);
     }
     g_mst_scan_pairs = static_cast<int64_t>(h.scan_pairs);
     if (edges != N - 1) return HDBMST_ERR_NOCONVERGE;
@@ -991,6 +1083,13 @@ int hdbmst_set_engine(int engine) {
     if (engine == HDBMST_ENGINE_AUTO || engine == HDBMST_ENGINE_SIMT ||
         engine == HDBMST_ENGINE_TENSOR || engine == HDBMST_ENGINE_TF32)
         g_engine = engine;
+    return prev;
+}
+
+int hdbmst_set_scan_form(int form) {
+    const int prev = g_scan_form;
+    if (form == HDBMST_SCAN_AUTO || form == HDBMST_SCAN_ONE_SIDED || form == HDBMST_SCAN_SYMMETRIC)
+        g_scan_form = form;
     return prev;
 }
 
@@ -1039,6 +1138,13 @@ int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
         if (edges) edges[i] = g_round_edges[i];
         if (exact_rows) exact_rows[i] = g_round_exact[i];
     }
+    return r;
+}
+
+int hdbmst_last_mst_symmetric(int64_t *recorded, int max_rounds) {
+    const int r = static_cast<int>(g_round_sym.size());
+    for (int i = 0; i < std::min(r, max_rounds); ++i)
+        if (recorded) recorded[i] = g_round_sym[i];
     return r;
 }
 

@@ -244,7 +244,8 @@ __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict_
 
 // K7: per component, the least (w, lo, hi) over its points' candidates.  The
 // first pass also records, for the next round, the candidates that are exact
-// (proven or scanned); the others (skipped by the bound) are not.
+// (proven, or scanned one-sided: act_flag); the others (skipped by the
+// bound, or only bounded by the symmetric scan) are not.
 __global__ void comp_min_lo_kernel(int n, const unsigned long long *__restrict__ cand,
                                    const int *__restrict__ comp,
                                    unsigned long long *__restrict__ ck64,
@@ -254,7 +255,7 @@ __global__ void comp_min_lo_kernel(int n, const unsigned long long *__restrict__
     const int a = blockIdx.x * blockDim.x + threadIdx.x;
     if (a >= n) return;
     const unsigned long long k = cand[a];
-    if (cache) cache[a] = (proven[a] || act_flag[a]) ? k : kNoKey;
+    if (cache) cache[a] = (proven[a] || (act_flag && act_flag[a])) ? k : kNoKey;
     if (k == kNoKey) return;
     const unsigned b = key_i(k);
     const unsigned lo = min(static_cast<unsigned>(a), b);

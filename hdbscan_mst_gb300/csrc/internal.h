@@ -306,7 +306,50 @@ cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *X
                            const float *Xs_hi, const float *Xs_lo, int row_tiles, int splits,
                            cudaStream_t s);
 
-// stage 0 also records exact candidates into cache (if not NULL) for the next round.
+// tc_sym.cu: the symmetric scan.  The points of the set P in one order,
+// grouped by component, serve as rows and as columns; per component a live
+// bound theta (float bits); the pairs that could be a component's cheapest
+// edge are recorded as position pairs.
+struct SymArgs {
+    int np;                  // points in P
+    int64_t ld;              // np rounded up to 128 (rows of the operand arrays)
+    int blocks;              // ld / 128
+    const int *idx;          // [np] point index of each position
+    const float *core;       // [ld] core distance by position
+    const int *comp;         // [ld] component by position
+    const float *norm;       // [ld] |p|^2 by position, +inf past np
+    const int *comp_start;   // [n] first position of each component label
+    const int *comp_size;    // [n] positions of each component label
+    const int4 *tile_meta;   // [ld / 64] (component or -1, largest starting bound bits, 0, 0)
+    unsigned *theta;         // [n] live bound per component label
+    unsigned long long *cand;  // [n] per-point least edge key (weight, other end)
+    int2 *pairs;             // [pair_cap] recorded (row, column) positions
+    int *pair_count;         // may exceed pair_cap: then the list is incomplete
+    int pair_cap;
+    int d, dk;
+    float err_c;             // ranking error coefficient of the engine (rounded up)
+    const float *e0;         // its absolute part
+    int f16;
+    const unsigned *amax_bits;
+    unsigned long long *tile_pairs;
+    unsigned *status;
+};
+// P = the points with core distance at most the largest U_C over the
+// components (act_flag), with per-label counts like launch_classify.
+cudaError_t launch_sym_classify(int n, const int *comp, const unsigned *ub, const float *core,
+                                unsigned *umax, unsigned char *act_flag, int *size, int *act_size,
+                                int *act_count, cudaStream_t s);
+// theta = ub, norm past np = +inf, the tile records.
+cudaError_t launch_sym_prepare(int n, int np, int ld, const int *pcomp, const unsigned *ub,
+                               unsigned *theta, float *norm, int4 *tile_meta, cudaStream_t s);
+cudaError_t launch_tc_sym(const SymArgs &a, const float *x_hi, const float *x_lo, cudaStream_t s);
+// The recorded pairs' exact weights into both ends' candidate keys.
+cudaError_t launch_sym_pairs_exact(const int2 *pairs, int count, const int *idx, const float *Xp,
+                                   int dk, const float *core, unsigned long long *cand,
+                                   cudaStream_t s);
+
+// stage 0 also records exact candidates into cache (if not NULL) for the next
+// round: the proven ones, and the scanned ones when act_flag is not NULL.
 cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *comp,
                             unsigned long long *ck64, unsigned *chi, const unsigned char *proven,
                             const unsigned char *act_flag, unsigned long long *cache,

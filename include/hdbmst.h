@@ -241,6 +241,31 @@ hdbmst_status hdbmst_hdbscan_labels(const int32_t *edges, const float *w, int64_
 #define HDBMST_ENGINE_TF32 3
 int hdbmst_set_engine(int engine);
 
+/*
+ * Form of the Boruvka scan on the tensor cores (hdbmst_mr_mst), process-wide,
+ * not thread-safe:
+ *   HDBMST_SCAN_AUTO       symmetric in the rounds where at least half the
+ *                          points need a scan, one-sided otherwise (default);
+ *   HDBMST_SCAN_ONE_SIDED  every scanned point against all points, each
+ *                          edge seen from both ends (page "HDBSCAN", "Exact
+ *                          shortcuts": the active points are the rows);
+ *   HDBMST_SCAN_SYMMETRIC  symmetric in every round that scans.
+ * The symmetric form visits each unordered pair of points of different
+ * components once and tests it for both components: per component a bound
+ * that an already recorded edge meets (the shortcuts' bound to begin with)
+ * is lowered by every pair recorded, and a pair is recorded when its exact
+ * weight could be at most either bound; the recorded pairs are then weighed
+ * exactly.  The tree is the same whichever form runs (the minimum edge per
+ * component is exact in both).  With the FP32 FFMA engine, or without
+ * nearest lists (no bound), the scan is one-sided.  If a round records more
+ * pairs than its list holds, that round is redone one-sided.  Returns the
+ * previous setting; unknown values are ignored.
+ */
+#define HDBMST_SCAN_AUTO 0
+#define HDBMST_SCAN_ONE_SIDED 1
+#define HDBMST_SCAN_SYMMETRIC 2
+int hdbmst_set_scan_form(int form);
+
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);
 
@@ -308,6 +333,14 @@ int64_t hdbmst_last_mst_scan_pairs(void);
  */
 int hdbmst_last_mst_rounds(int64_t *active, int64_t *edges, int64_t *exact_rows,
                            int max_rounds);
+
+/*
+ * Per round of the most recent hdbmst_mr_mst call: the pairs the symmetric
+ * scan recorded (recorded[i]), or -1 where the round scanned one-sided (for a
+ * symmetric round, active[i] of hdbmst_last_mst_rounds is the size of the
+ * set that was scanned).  Returns the number of rounds; recorded may be NULL.
+ */
+int hdbmst_last_mst_symmetric(int64_t *recorded, int max_rounds);
 
 #ifdef __cplusplus
 }
