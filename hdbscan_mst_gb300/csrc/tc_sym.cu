@@ -37,10 +37,12 @@
 // sym_tau), and a pair whose core distances exceed theta does too.  Each
 // thread (one row) filters a tile's columns against tau(max(theta_row,
 // theta_col)), theta_col the bound of the tile's component (of a tile that
-// spans several components, the largest of their starting bounds).  Both
-// bounds are read from global memory a tile ahead (a column component's
-// first tile waits for its read), so they may be a tile stale - stale
-// bounds are only larger, and a larger bound only records more.  Within a
+// spans several components, the largest of their starting bounds; a tile
+// of two components filters each column range with its own bound).  The
+// bounds are read from global memory every few tiles, ahead of their use (a
+// column component's first tile waits for its read), so they may be a few
+// tiles stale - stale bounds are only larger, and a larger bound only
+// records more.  Within a
 // 32 x 32 batch the warp first finds the least upper bound of its candidates
 // per component and lowers the bounds to it, then records what can still
 // win; otherwise every row of every warp would record its own descending
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
         const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
         const float kdot = a.f16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
         const float c = a.err_c, e0 = *a.e0;
-        // the row's bound: the value read one tile ago, and what this thread recorded
+        // the row's bound: the value read a few tiles ago, and what this thread recorded
         float pend_r = valid ? load_theta(a.theta, rc) : INFINITY;
         float own_r = INFINITY;
         // the column tile's bound, read one tile ago for component cached_tc
@@ -176,7 +178,21 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
         const auto tau_of = [&](float t) {
             return (!valid || ca > t) ? -INFINITY : sym_tau(t, na, c, e0, a.d);
         };
+        // thr = tau(th_last) with th_last >= th: a bound that rose is
+        // converted at once; one that dropped keeps the looser filter until
+        // it has dropped by 1/256 (the conversion is a chain of correctly
+        // rounded square roots and a division)
+        const auto retau = [&](float th) {
+            if (th > th_last || th < th_last * (1.f - 0x1p-8f)) {
+                th_last = th;
+                thr = tau_of(th);
+            }
+        };
+        int k_tile = 0;
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+            // the live bounds are read every 4th tile of the warp (each read
+            // is used by the tiles after it; a stale bound is only larger)
+            const bool refresh = (k_tile++ & 3) == 0;
             // The tile's columns [0, kb) belong to component c1 with bound
             // th_c, [kb, 64) to c2 with th_c2 (a tile of one component: kb =
             // 64; of three or more: both are the largest starting bound and
@@ -194,33 +210,18 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
                     cached_tc = tcomp;
                 }
                 th_c = th_c2 = pend_c;
-                pend_c = load_theta(a.theta, tcomp);
+                if (refresh) pend_c = load_theta(a.theta, tcomp);
             } else if (two) {
                 th_c = load_theta(a.theta, meta.z);
                 th_c2 = load_theta(a.theta, meta.w);
             }
             float th_r = fminf(pend_r, own_r);
-            if (valid) pend_r = load_theta(a.theta, rc);
+            if (valid && refresh) pend_r = load_theta(a.theta, rc);
             float th = fmaxf(th_r, th_c), th2 = fmaxf(th_r, th_c2);
-            if (th != th_last) {
-                th_last = th;
-                thr = tau_of(th);
-            }
+            retau(th);
             float thr2 = kb < kTileCols ? tau_of(th2) : thr;
-            // A column whose core distance exceeds every row's bound in the
-            // warp weighs more than both bounds with any of them: its norm
-            // becomes +inf (t = +inf), so the filter drops it at no cost per
-            // pair.
             float *nbs = reinterpret_cast<float *>(&s_snorm[warp][buf][0]);
             const float *cbs = reinterpret_cast<const float *>(&s_score[warp][buf][0]);
-            const float thm = fmaxf(th, th2);
-            const float th_w =
-                __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(valid && ca <= thm ? thm : 0.f)));
-            const bool e0l = cbs[lane] <= th_w, e1l = cbs[lane + 32] <= th_w;
-            if (!e0l) nbs[lane] = INFINITY;
-            if (!e1l) nbs[lane + 32] = INFINITY;
-            if (!__any_sync(0xffffffffu, e0l || e1l)) return;  // no column can be recorded
-            __syncwarp();
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 const int cb0 = col0 + cc * 32;
@@ -347,10 +348,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
                 }
                 th = fmaxf(th_r, th_c);
                 th2 = fmaxf(th_r, th_c2);
-                if (th != th_last) {
-                    th_last = th;
-                    thr = tau_of(th);
-                }
+                retau(th);
                 thr2 = kb < kTileCols ? tau_of(th2) : thr;
             }
         });
