@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "knn", "core_distances", "mr_mst", "hdbscan_mst", "HdbmstError", "HdbmstUnavailable",
     "launch_count", "profile_enable", "profile_read", "last_mst_rounds", "library_path", "KMAX",
-    "set_engine", "set_scan_form",
+    "set_engine", "set_scan_form", "set_scan_pruning",
 ]
 
 KMAX = 32
@@ -93,6 +93,8 @@ def _load():
     L.hdbmst_last_mst_rounds.restype = i32
     L.hdbmst_set_engine.argtypes = [i32]
     L.hdbmst_set_engine.restype = i32
+    L.hdbmst_set_scan_pruning.argtypes = [i32]
+    L.hdbmst_set_scan_pruning.restype = i32
     L.hdbmst_set_scan_form.argtypes = [i32]
     L.hdbmst_set_scan_form.restype = i32
     L.hdbmst_last_mst_symmetric.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
@@ -333,6 +335,12 @@ def set_scan_form(form: str) -> str:
     same whichever form runs."""
     prev = _load().hdbmst_set_scan_form(SCAN_FORMS[form])
     return {v: k for k, v in SCAN_FORMS.items()}[prev]
+
+
+def set_scan_pruning(on: bool) -> bool:
+    """Turn the block pruning of the symmetric scan on or off; returns the
+    previous setting.  The tree is the same either way."""
+    return bool(_load().hdbmst_set_scan_pruning(1 if on else 0))
 
 
 def last_mst_symmetric() -> list[int]:

@@ -42,8 +42,10 @@ bool use_tensor_scan(int dk) {
 // 128-byte row of halves per part), unless TF32 is asked for.
 bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
 
-// Form of the Boruvka scan on the tensor cores (HDBMST_SCAN_*), process-wide.
+// Form of the Boruvka scan on the tensor cores (HDBMST_SCAN_*), process-wide,
+// and whether the symmetric form prunes block pairs.
 int g_scan_form = HDBMST_SCAN_AUTO;
+bool g_sym_prune = true;
 
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so
 // far, rows searched exactly, pairs the symmetric scan recorded (-1: one-sided)
@@ -60,7 +62,7 @@ const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
     "nbr_candidate", "active", "gather", "boruvka_scan", "boruvka_refine", "boruvka_exact",
     "comp_min", "hook",
-    "roots",  "relabel",    "sort_edges", "knn_prune"};
+    "roots",  "relabel",    "sort_edges", "knn_prune", "mst_prune"};
 
 cudaEvent_t take_event() {
     if (!g_pool.empty()) {
@@ -145,6 +147,7 @@ struct DevStatus {
     unsigned long long scan_pairs;   // (row, column) pairs the Boruvka scan evaluated
     unsigned sym_umax;               // symmetric scan: the largest component bound
     int sym_pairs;                   // symmetric scan: pairs recorded (may exceed the list)
+    int sym_ncomp;                   // symmetric scan: components with points in P
 };
 
 // A ranking error coefficient as the float32 the proofs use, rounded up.
@@ -545,6 +548,7 @@ struct MstPlan {
     int n, d, dk, L;
     int64_t n_pad;
     int index_bits;
+    bool sprune;  // buffers of the pruned symmetric scan
 };
 
 MstPlan make_mst_plan(int64_t n, int d, int L) {
@@ -557,6 +561,9 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
     int bits = 1;
     while (bits < 31 && (int64_t(1) << bits) <= std::max<int64_t>(n - 1, 1)) ++bits;
     p.index_bits = bits;
+    // the pruned symmetric scan: nearest lists (bounds), the tensor-core
+    // scan's feature counts, enough points, and blocks^2 arrays that stay small
+    p.sprune = L > 0 && p.dk <= 64 && n >= kSymPruneMinN && p.n_pad / kBM <= kSymPruneMaxBlocks;
     return p;
 }
 
@@ -575,6 +582,7 @@ struct MstBufs {
     int *e_lo, *e_hi, *lo2, *hi2;
     unsigned *e_w, *w2, *hist;
     DevStatus *st;
+    SymPruneBufs sp;  // all null unless the plan's sprune
 };
 
 void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
@@ -623,6 +631,38 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     b.w2 = c.take<unsigned>(n);
     b.hist = c.take<unsigned>(sort_hist_entries(static_cast<int>(n)));
     b.st = c.take<DevStatus>(1);
+    b.sp = SymPruneBufs{};
+    if (p.sprune) {
+        SymPruneBufs &q = b.sp;
+        SpatialOrder &o = q.order;
+        const int P = kSpatialPivots, NB = kSpatialPivots * kSpatialBuckets;
+        const size_t blocks = static_cast<size_t>(p.n_pad / kBM);
+        const size_t chunks = (n + kSymChunk - 1) / kSymChunk;
+        o.pivots = P;
+        o.buckets = kSpatialBuckets;
+        o.cellY = o.cellX = c.take<int>(p.n_pad);
+        o.permY = o.permX = c.take<int>(p.n_pad);
+        o.invY = o.invX = c.take<int>(p.n_pad);
+        o.startY = o.startX = c.take<int>(NB + 1);
+        o.dcellY = o.dcellX = c.take<float>(p.n_pad);
+        o.pdY = o.pdX = c.take<float>(static_cast<size_t>(p.n_pad) * P);
+        o.counters = c.take<int>(spatial_counter_ints(P, kSpatialBuckets));
+        o.tile_start = c.take<int>(p.n_pad / kBM);
+        o.pivf = c.take<float>(static_cast<size_t>(kSpatialMaxD) * P);
+        q.kcount = c.take<int>(1);
+        q.cidx = c.take<int>(n);
+        q.cstart = c.take<int>(kSymMaxComps);
+        q.off = c.take<int>(chunks * kSymMaxComps);
+        q.Lb = c.take<float>(blocks * P);
+        q.Hb = c.take<float>(blocks * P);
+        q.bcomp = c.take<int>(blocks);
+        q.LB = c.take<float>(blocks * blocks);
+        q.bth = c.take<float>(blocks);
+        q.home = c.take<int>(blocks * kSymHome);
+        q.hcount = c.take<int>(blocks);
+        q.list = c.take<int>(blocks * blocks);
+        q.lcount = c.take<int>(blocks);
+    }
 }
 
 bool bad_sizes(int64_t n, int d) { return n < 0 || d < 1; }
@@ -824,6 +864,12 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                 : tensor ? tc::err_coef(d, p.dk)
                                          : (2.0 * d + 10.0) * 0x1p-24 * 1.01);
     g_round_sym.clear();
+    // the spatial order of all points (pivots, bins, pivot distances) for the
+    // pruned symmetric scan, once per call
+    const bool sp_ready = p.sprune && tensor && shortcuts && g_scan_form != HDBMST_SCAN_ONE_SIDED &&
+                          g_sym_prune;
+    if (sp_ready)
+        LAUNCH(K_SYM_PRUNE, s, launch_spatial_order(b.sp.order, X, ldx, N, X, ldx, N, true, d, s));
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
         int fallback = 0;
         int64_t recorded = -1;
@@ -855,17 +901,24 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             // the set P in grouped order: rows and columns of the symmetric scan
             CUDA_OK(cudaMemsetAsync(b.counters, 0, sizeof(int) * (4 * static_cast<size_t>(N) + 8), s));
             CUDA_OK(cudaMemsetAsync(&b.st->act_count, 0, sizeof(int), s));
-            CUDA_OK(cudaMemsetAsync(&b.st->sym_umax, 0, 2 * sizeof(unsigned), s));
+            CUDA_OK(cudaMemsetAsync(&b.st->sym_umax, 0, 3 * sizeof(unsigned), s));
             LAUNCH(K_ACTIVE, s, launch_sym_classify(N, b.comp, b.ub, core, &b.st->sym_umax,
-                                                    b.act_flag, size, act_size, &b.st->act_count, s));
+                                                    b.act_flag, size, act_size, &b.st->act_count,
+                                                    &b.st->sym_ncomp, s));
             rs = read_status(b.st, h, s);
             if (rs != HDBMST_OK) return rs;
             const int np = h.act_count;
+            // pruned by blocks when the spatial order exists and the
+            // components fit the grouping
+            const bool pruned = sp_ready && h.sym_ncomp <= kSymMaxComps;
             const int np_pad = static_cast<int>(round_up(std::max(np, 1), kBM));
             LAUNCH(K_GATHER, s, launch_group(N, static_cast<int>(p.n_pad), b.comp, core, b.norm,
                                              b.act_flag, size, act_size, b.start, b.act_start,
                                              cursor, act_cursor, totals, b.perm, b.col_comp,
                                              b.col_core, b.col_norm, b.act_idx, s));
+            if (pruned)
+                LAUNCH(K_SYM_PRUNE, s, launch_sym_group(b.sp, N, b.act_flag, b.comp, b.act_start,
+                                                     act_size, b.act_idx, s));
             LAUNCH(K_GATHER, s, launch_gather(np, np_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
                                               b.comp, b.norm, nullptr, b.act_core, b.act_comp,
                                               b.act_norm, s));
@@ -904,6 +957,20 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             ya.amax_bits = &b.st->amax_bits;
             ya.tile_pairs = &b.st->scan_pairs;
             ya.status = &b.st->status;
+            if (pruned) {
+                // bounds of the blocks, the home pass, then the lists
+                const int blocks = np_pad / kBM;
+                LAUNCH(K_SYM_PRUNE, s, launch_sym_blocks(b.sp, np, blocks, b.act_idx, b.act_comp, d, s));
+                SymArgs ha = ya;
+                ha.list = b.sp.home;
+                ha.list_count = b.sp.hcount;
+                ha.list_stride = kSymHome;
+                LAUNCH(K_SCAN, s, launch_tc_sym(ha, b.Xa_hi, b.Xa_lo, s));
+                LAUNCH(K_SYM_PRUNE, s, launch_sym_lists(b.sp, np, blocks, b.act_comp, theta, d, s));
+                ya.list = b.sp.list;
+                ya.list_count = b.sp.lcount;
+                ya.list_stride = blocks;
+            }
             LAUNCH(K_SCAN, s, launch_tc_sym(ya, b.Xa_hi, b.Xa_lo, s));
             rs = read_status(b.st, h, s);
             if (rs != HDBMST_OK) return rs;
@@ -1083,6 +1150,12 @@ int hdbmst_set_engine(int engine) {
     if (engine == HDBMST_ENGINE_AUTO || engine == HDBMST_ENGINE_SIMT ||
         engine == HDBMST_ENGINE_TENSOR || engine == HDBMST_ENGINE_TF32)
         g_engine = engine;
+    return prev;
+}
+
+int hdbmst_set_scan_pruning(int on) {
+    const int prev = g_sym_prune ? 1 : 0;
+    g_sym_prune = on != 0;
     return prev;
 }
 

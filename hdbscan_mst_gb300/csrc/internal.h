@@ -333,12 +333,53 @@ struct SymArgs {
     const unsigned *amax_bits;
     unsigned long long *tile_pairs;
     unsigned *status;
+    // nullable: the 128-point blocks of each row tile ([blocks][list_stride],
+    // list_count[blocks] entries each) instead of the blocks at or after it
+    const int *list;
+    const int *list_count;
+    int list_stride;
 };
+// The pruned symmetric scan (symprune.cu).  Blocks of 128 positions of P are
+// bounded through the pivots of a spatial order of all points; a home pass
+// over each row tile's kSymHome nearest blocks (by that bound) of other
+// components brings the component bounds close to their final values, and a
+// second pass visits the blocks j >= i whose distance bound is at most the
+// larger of the two blocks' component bounds.
+constexpr int kSymHome = 8;              // blocks per row tile of the home pass
+constexpr int kSymMaxComps = 1024;       // components of P the spatial grouping handles
+constexpr int kSymChunk = 1024;          // positions of the spatial order per grouping warp
+constexpr int kSymPruneMaxBlocks = 8192; // blocks of P (the block-pair arrays are blocks^2)
+constexpr int kSymPruneMinN = 16384;     // points below which the scan is not pruned
+struct SymPruneBufs {
+    SpatialOrder order;  // of all points (X as rows and columns), with pdY [n][128]
+    int *kcount;         // [1] compact components assigned
+    int *cidx;           // [n] compact index of a component label
+    int *cstart;         // [kSymMaxComps] first position of each compact component
+    int *off;            // [chunks][kSymMaxComps] counts, then running offsets
+    float *Lb, *Hb;      // [blocks][128] least / largest pivot distance per block, widened
+    int *bcomp;          // [blocks] component of a block of one component, else -1
+    float *LB;           // [blocks][blocks] lower bound of the distance between two blocks
+    float *bth;          // [blocks] largest component bound over a block's points
+    int *home, *hcount;  // [blocks][kSymHome], [blocks]
+    int *list, *lcount;  // [blocks][blocks], [blocks]
+};
+// P grouped by component in the spatial order (act_idx rewritten): within a
+// component, positions follow o.permY.  Needs act_start / act_size of
+// launch_group; ncomp <= kSymMaxComps components with points in P.
+cudaError_t launch_sym_group(const SymPruneBufs &b, int n, const unsigned char *act_flag,
+                             const int *comp, const int *act_start, const int *act_size,
+                             int *act_idx, cudaStream_t s);
+// Block bounds (Lb, Hb, bcomp), the block-pair bounds LB and the home lists.
+cudaError_t launch_sym_blocks(const SymPruneBufs &b, int np, int blocks, const int *act_idx,
+                              const int *pcomp, int d, cudaStream_t s);
+// After the home pass: bth from the live bounds, and the lists of the second pass.
+cudaError_t launch_sym_lists(const SymPruneBufs &b, int np, int blocks, const int *pcomp,
+                             const unsigned *theta, int d, cudaStream_t s);
 // P = the points with core distance at most the largest U_C over the
 // components (act_flag), with per-label counts like launch_classify.
 cudaError_t launch_sym_classify(int n, const int *comp, const unsigned *ub, const float *core,
                                 unsigned *umax, unsigned char *act_flag, int *size, int *act_size,
-                                int *act_count, cudaStream_t s);
+                                int *act_count, int *ncomp, cudaStream_t s);
 // theta = ub, norm past np = +inf, the tile records.
 cudaError_t launch_sym_prepare(int n, int np, int ld, const int *pcomp, const unsigned *ub,
                                unsigned *theta, float *norm, int4 *tile_meta, cudaStream_t s);
@@ -393,6 +434,7 @@ enum KernelId {
     K_RELABEL,
     K_SORT,
     K_PRUNE,
+    K_SYM_PRUNE,
     K_COUNT
 };
 

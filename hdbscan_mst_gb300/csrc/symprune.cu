@@ -1,0 +1,349 @@
+// Pruning of the symmetric Boruvka scan (tc_sym.cu): which 128 x 128 block
+// pairs of the set P can hold a pair that is some component's cheapest edge.
+//
+// Page "HDBSCAN" ("Exact shortcuts"): work is skipped only where a bound
+// proves that it cannot change the result.  The bound here is the triangle
+// inequality through pivots, as in the pruned k-NN (prune.cu): for a pivot p
+// and points a, b, |d(a, p) - d(b, p)| <= d(a, b), so two blocks whose
+// points' distances to p lie in [L_i, H_i] and [L_j, H_j] are at least
+// LB(i, j) = max over p of max(L_j - H_i, L_i - H_j) apart.  A pair (a, b)
+// of blocks i, j weighs at least its distance; if LB(i, j) exceeds the
+// bounds theta of all components in both blocks, no pair of the two blocks
+// is a cheapest edge of either end's component (theta only falls, and
+// always weighs at least that component's cheapest edge).
+//
+// The bounds are tight only when the points of a block lie close together,
+// so P is grouped by component and, within a component, in the spatial
+// order of order.cu (nearest of 128 pivots, then distance bucket), and only
+// once the component bounds are near their final values: a home pass first
+// evaluates, for each row tile, the kSymHome blocks of other components with
+// the least LB (which hold most components' cheapest edges), and the lists
+// of the second pass are built from the bounds it leaves.
+//
+// Rounding.  Pivot distances are float32 direct differences within relative
+// eps = (d + 8) 2^-24 of the true ones, and L, H are widened outward by eps;
+// LB is formed with downward rounding.  The exact weight is at least its
+// float32 distance, which is at least the true distance times (1 - (d + 4)
+// 2^-24); a block pair is skipped only when LB (1 - 2^-16) exceeds the bound.
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hdbmst {
+
+namespace {
+
+constexpr int P = kPrunePivots;
+constexpr int kRowsPerBlock = kBM;  // positions of a block
+
+int blocks_for(int64_t n, int per) { return static_cast<int>(n > per ? (n + per - 1) / per : 1); }
+
+// Compact index of every component label with points in P, and its first
+// position.
+__global__ void sym_compact_kernel(int n, const int *__restrict__ act_size,
+                                   const int *__restrict__ act_start, int *__restrict__ kcount,
+                                   int *__restrict__ cidx, int *__restrict__ cstart) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= n || act_size[c] == 0) return;
+    const int k = atomicAdd(kcount, 1);
+    if (k >= kSymMaxComps) return;  // the host checks the count first
+    cidx[c] = k;
+    cstart[k] = act_start[c];
+}
+
+// Per chunk of kSymChunk positions of the spatial order (one warp), the
+// points of each compact component that lie in P.
+__global__ void sym_chunk_count_kernel(int n, const int *__restrict__ perm,
+                                       const unsigned char *__restrict__ act_flag,
+                                       const int *__restrict__ comp, const int *__restrict__ cidx,
+                                       int *__restrict__ off) {
+    const int chunk = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    const int p0 = chunk * kSymChunk;
+    if (p0 >= n) return;
+    const int p1 = min(p0 + kSymChunk, n);
+    int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
+    for (int q = p0 + lane; q < p1; q += 32) {
+        const int x = perm[q];
+        if (act_flag[x]) atomicAdd(&row[cidx[comp[x]]], 1);
+    }
+}
+
+// Per compact component, the running position at the start of each chunk.
+__global__ void sym_chunk_scan_kernel(int chunks, int ncomp, const int *__restrict__ cstart,
+                                      int *__restrict__ off) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= ncomp) return;
+    int run = cstart[k];
+    for (int ch = 0; ch < chunks; ++ch) {
+        int *e = off + static_cast<int64_t>(ch) * kSymMaxComps + k;
+        const int cnt = *e;
+        *e = run;
+        run += cnt;
+    }
+}
+
+// Positions in chunk order and, within a chunk, in spatial order: one warp
+// walks its chunk 32 points at a time; lanes of one component take
+// consecutive positions in lane order.
+__global__ void sym_scatter_kernel(int n, const int *__restrict__ perm,
+                                   const unsigned char *__restrict__ act_flag,
+                                   const int *__restrict__ comp, const int *__restrict__ cidx,
+                                   int *__restrict__ off, int *__restrict__ act_idx) {
+    const int chunk = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    const int p0 = chunk * kSymChunk;
+    if (p0 >= n) return;
+    const int p1 = min(p0 + kSymChunk, n);
+    int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
+    for (int q0 = p0; q0 < p1; q0 += 32) {
+        const int q = q0 + lane;
+        const int x = q < p1 ? perm[q] : -1;
+        const bool in = x >= 0 && act_flag[x];
+        const int k = in ? cidx[comp[x]] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, k);
+        const int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (in) base = row[k];
+        __syncwarp();
+        if (in) {
+            act_idx[base + __popc(peers & lanemask_lt())] = x;
+            if (lane == leader) row[k] = base + __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
+// Per block b of P (one CTA, thread = pivot): the least and largest pivot
+// distance of its points, widened outward by eps; and bcomp[b], the
+// component of a block whose points all have the same one (else -1).
+__global__ void __launch_bounds__(P) sym_bounds_kernel(int np, const int *__restrict__ act_idx,
+                                                       const int *__restrict__ pcomp,
+                                                       const float *__restrict__ pd, double eps,
+                                                       float *__restrict__ Lb,
+                                                       float *__restrict__ Hb,
+                                                       int *__restrict__ bcomp) {
+    const int b = blockIdx.x, p = threadIdx.x;
+    const int q0 = b * kRowsPerBlock, q1 = min(q0 + kRowsPerBlock, np);
+    float lo = INFINITY, hi = -INFINITY;
+    for (int q = q0; q < q1; ++q) {
+        const float v = pd[static_cast<int64_t>(act_idx[q]) * P + p];
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+    Lb[static_cast<int64_t>(b) * P + p] = __double2float_rd(static_cast<double>(lo) * (1.0 - eps));
+    Hb[static_cast<int64_t>(b) * P + p] = __double2float_ru(static_cast<double>(hi) * (1.0 + eps));
+    if (p == 0) {
+        const int c0 = pcomp[q0];
+        bool same = true;
+        for (int q = q0 + 1; q < q1; ++q) same = same && pcomp[q] == c0;
+        bcomp[b] = same ? c0 : -1;
+    }
+}
+
+// LB[i][j] for all block pairs, 16 x 16 pairs per CTA (thread = pair), the
+// two blocks' bounds staged in shared memory.
+constexpr int kLbTile = 16;
+__global__ void __launch_bounds__(kLbTile * kLbTile) sym_lb_kernel(int blocks,
+                                                                   const float *__restrict__ Lb,
+                                                                   const float *__restrict__ Hb,
+                                                                   float *__restrict__ LB) {
+    __shared__ float sLi[kLbTile][P + 1], sHi[kLbTile][P + 1], sLj[kLbTile][P + 1],
+        sHj[kLbTile][P + 1];
+    const int i0 = blockIdx.y * kLbTile, j0 = blockIdx.x * kLbTile;
+    const int t = threadIdx.x;
+    for (int e = t; e < kLbTile * P; e += blockDim.x) {
+        const int r = e / P, p = e % P;
+        const int bi = min(i0 + r, blocks - 1), bj = min(j0 + r, blocks - 1);
+        sLi[r][p] = Lb[static_cast<int64_t>(bi) * P + p];
+        sHi[r][p] = Hb[static_cast<int64_t>(bi) * P + p];
+        sLj[r][p] = Lb[static_cast<int64_t>(bj) * P + p];
+        sHj[r][p] = Hb[static_cast<int64_t>(bj) * P + p];
+    }
+    __syncthreads();
+    const int ri = t / kLbTile, rj = t % kLbTile;
+    float lb = 0.f;
+#pragma unroll 8
+    for (int p = 0; p < P; ++p) {
+        lb = fmaxf(lb, __fsub_rd(sLj[rj][p], sHi[ri][p]));
+        lb = fmaxf(lb, __fsub_rd(sLi[ri][p], sHj[rj][p]));
+    }
+    const int i = i0 + ri, j = j0 + rj;
+    if (i < blocks && j < blocks) LB[static_cast<int64_t>(i) * blocks + j] = lb;
+}
+
+__device__ __forceinline__ bool own_pair(const int *bcomp, int i, int j) {
+    const int ci = bcomp[i];
+    return ci >= 0 && bcomp[j] == ci;
+}
+
+// Home list of row tile i (one CTA): its kSymHome blocks of least LB that
+// are not wholly inside its own component (block i itself included when it
+// holds two components).  Each thread keeps its best kSymHome keys (LB bits,
+// block); the CTA then pops the least head kSymHome times.
+constexpr int kHomeThreads = 256;
+__global__ void __launch_bounds__(kHomeThreads) sym_home_kernel(int blocks,
+                                                                const float *__restrict__ LB,
+                                                                const int *__restrict__ bcomp,
+                                                                int *__restrict__ home,
+                                                                int *__restrict__ hcount) {
+    __shared__ unsigned long long s_min[kHomeThreads / 32];
+    __shared__ unsigned long long s_win;
+    const int i = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    unsigned long long best[kSymHome];
+#pragma unroll
+    for (int q = 0; q < kSymHome; ++q) best[q] = kNoKey;
+    for (int j = t; j < blocks; j += kHomeThreads) {
+        if (own_pair(bcomp, i, j)) continue;
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(LB[static_cast<int64_t>(i) * blocks + j])) << 32) |
+            static_cast<unsigned>(j);
+        if (key < best[kSymHome - 1]) {
+            best[kSymHome - 1] = key;
+#pragma unroll
+            for (int q = kSymHome - 1; q > 0; --q) {
+                const unsigned long long lo = min(best[q - 1], best[q]), hi = max(best[q - 1], best[q]);
+                best[q - 1] = lo;
+                best[q] = hi;
+            }
+        }
+    }
+    int head = 0, cnt = 0;
+    for (int r = 0; r < kSymHome; ++r) {
+        unsigned long long h = head < kSymHome ? best[0] : kNoKey;
+#pragma unroll
+        for (int q = 1; q < kSymHome; ++q)
+            if (q == head) h = best[q];
+        unsigned long long m = h;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_min[warp] = m;
+        __syncthreads();
+        if (t == 0) {
+            unsigned long long w = s_min[0];
+            for (int q = 1; q < kHomeThreads / 32; ++q) w = min(w, s_min[q]);
+            s_win = w;
+        }
+        __syncthreads();
+        const unsigned long long w = s_win;
+        if (w == kNoKey) break;
+        if (h == w) ++head;  // keys are distinct (block index)
+        if (t == 0) home[static_cast<int64_t>(i) * kSymHome + cnt] = static_cast<int>(w & 0xffffffffu);
+        ++cnt;
+        __syncthreads();
+    }
+    if (t == 0) hcount[i] = cnt;
+}
+
+// bth[b]: the largest live bound over the components of block b's points.
+__global__ void __launch_bounds__(kRowsPerBlock) sym_block_theta_kernel(int np,
+                                                                        const int *__restrict__ pcomp,
+                                                                        const unsigned *__restrict__ theta,
+                                                                        float *__restrict__ bth) {
+    __shared__ unsigned s_max[kRowsPerBlock / 32];
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int q = b * kRowsPerBlock + t;
+    unsigned m = q < np ? __ldcg(theta + pcomp[q]) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((t & 31) == 0) s_max[t >> 5] = m;
+    __syncthreads();
+    if (t == 0) {
+        unsigned w = s_max[0];
+        for (int k = 1; k < kRowsPerBlock / 32; ++k) w = max(w, s_max[k]);
+        bth[b] = __uint_as_float(w);
+    }
+}
+
+// List of row tile i (one CTA, order kept): the blocks j >= i, not wholly
+// inside i's component and not in its home list, whose bound LB (1 - 2^-16)
+// does not exceed max(bth[i], bth[j]).
+constexpr int kListThreads = 256;
+__global__ void __launch_bounds__(kListThreads) sym_list_kernel(int blocks,
+                                                                const float *__restrict__ LB,
+                                                                const float *__restrict__ bth,
+                                                                const int *__restrict__ bcomp,
+                                                                const int *__restrict__ home,
+                                                                const int *__restrict__ hcount,
+                                                                int *__restrict__ list,
+                                                                int *__restrict__ lcount) {
+    __shared__ int s_home[kSymHome];
+    __shared__ int s_warp[kListThreads / 32];
+    const int i = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int hc = hcount[i];
+    if (t < kSymHome) s_home[t] = t < hc ? home[static_cast<int64_t>(i) * kSymHome + t] : -1;
+    __syncthreads();
+    const float thi = bth[i];
+    int cnt = 0;
+    for (int j0 = i; j0 < blocks; j0 += kListThreads) {
+        const int j = j0 + t;
+        bool keep = false;
+        if (j < blocks && !own_pair(bcomp, i, j)) {
+            const float lb = __fmul_rd(LB[static_cast<int64_t>(i) * blocks + j], 1.f - 0x1p-16f);
+            keep = !(lb > fmaxf(thi, bth[j]));
+#pragma unroll
+            for (int q = 0; q < kSymHome; ++q) keep = keep && s_home[q] != j;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0) s_warp[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < kListThreads / 32; ++w) {
+            before += w < warp ? s_warp[w] : 0;
+            total += s_warp[w];
+        }
+        if (keep) list[static_cast<int64_t>(i) * blocks + cnt + before + __popc(bal & lanemask_lt())] = j;
+        cnt += total;
+        __syncthreads();
+    }
+    if (t == 0) lcount[i] = cnt;
+}
+
+}  // namespace
+
+cudaError_t launch_sym_group(const SymPruneBufs &b, int n, const unsigned char *act_flag,
+                             const int *comp, const int *act_start, const int *act_size,
+                             int *act_idx, cudaStream_t s) {
+    const int chunks = blocks_for(n, kSymChunk);
+    cudaError_t e = cudaMemsetAsync(b.kcount, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(b.off, 0, sizeof(int) * static_cast<size_t>(chunks) * kSymMaxComps, s);
+    if (e != cudaSuccess) return e;
+    sym_compact_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, act_size, act_start, b.kcount, b.cidx,
+                                                          b.cstart);
+    sym_chunk_count_kernel<<<blocks_for(static_cast<int64_t>(chunks) * 32, 256), 256, 0, s>>>(
+        n, b.order.permY, act_flag, comp, b.cidx, b.off);
+    sym_chunk_scan_kernel<<<blocks_for(kSymMaxComps, 256), 256, 0, s>>>(chunks, kSymMaxComps,
+                                                                        b.cstart, b.off);
+    sym_scatter_kernel<<<blocks_for(static_cast<int64_t>(chunks) * 32, 256), 256, 0, s>>>(
+        n, b.order.permY, act_flag, comp, b.cidx, b.off, act_idx);
+    count_extra_launches(3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sym_blocks(const SymPruneBufs &b, int np, int blocks, const int *act_idx,
+                              const int *pcomp, int d, cudaStream_t s) {
+    const double eps = (d + 8.0) * 0x1p-24;
+    sym_bounds_kernel<<<blocks, P, 0, s>>>(np, act_idx, pcomp, b.order.pdY, eps, b.Lb, b.Hb,
+                                           b.bcomp);
+    const int g = (blocks + kLbTile - 1) / kLbTile;
+    sym_lb_kernel<<<dim3(g, g), kLbTile * kLbTile, 0, s>>>(blocks, b.Lb, b.Hb, b.LB);
+    sym_home_kernel<<<blocks, kHomeThreads, 0, s>>>(blocks, b.LB, b.bcomp, b.home, b.hcount);
+    count_extra_launches(2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sym_lists(const SymPruneBufs &b, int np, int blocks, const int *pcomp,
+                             const unsigned *theta, int d, cudaStream_t s) {
+    (void)d;
+    sym_block_theta_kernel<<<blocks, kRowsPerBlock, 0, s>>>(np, pcomp, theta, b.bth);
+    sym_list_kernel<<<blocks, kListThreads, 0, s>>>(blocks, b.LB, b.bth, b.bcomp, b.home,
+                                                    b.hcount, b.list, b.lcount);
+    count_extra_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace hdbmst

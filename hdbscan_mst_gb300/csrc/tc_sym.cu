@@ -74,6 +74,8 @@ struct TcSymParams {
 __shared__ float4 s_snorm[kEpiWarps][2][kTileCols / 4];
 __shared__ float4 s_score[kEpiWarps][2][kTileCols / 4];
 __shared__ int4 s_smeta[kEpiWarps][2];
+constexpr int kListCache = 2048;  // list entries kept in shared memory
+__shared__ int s_list[kListCache];
 
 // The least t a pair can have without weighing more than th, from the row's
 // side (|a|^2 = na): with T = th^2 (1 + 16 u) / (1 - (d + 3) u), a pair's true
@@ -139,8 +141,20 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
         skip_lo = (c0 + kCols - 1) / kCols * kSub;
         skip_hi = c1 / kCols * kSub;
     }
-    // the blocks j >= i of the row tile
-    const TileSeq seq(i * kSub, a.blocks * kSub, skip_lo, skip_hi);
+    // the blocks j >= i of the row tile, or its list (cached in shared
+    // memory when it fits)
+    TileSeq seq(i * kSub, a.blocks * kSub, skip_lo, skip_hi);
+    if (a.list) {
+        const int cnt = a.list_count[i];
+        const int *src = a.list + static_cast<int64_t>(i) * a.list_stride;
+        if (cnt <= kListCache) {
+            for (int q = tid; q < cnt; q += blockDim.x) s_list[q] = src[q];
+            src = s_list;
+        }
+        seq.list = src;
+        seq.n = 2 * cnt;
+        __syncthreads();
+    }
     if (tid == 0 && a.tile_pairs)
         atomicAdd(a.tile_pairs, static_cast<unsigned long long>(seq.n) * kTileCols * kRows);
     const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
@@ -395,11 +409,13 @@ __global__ void sym_bound_max_kernel(int n, const int *__restrict__ comp,
     if ((threadIdx.x & 31) == 0 && m) atomicMax(umax, m);
 }
 
-// The set P (act_flag), per component its point count and its count in P.
+// The set P (act_flag), per component its point count and its count in P,
+// and the number of components with points in P.
 __global__ void sym_classify_kernel(int n, const float *__restrict__ core,
                                     const int *__restrict__ comp, const unsigned *__restrict__ umax,
                                     unsigned char *__restrict__ act_flag, int *__restrict__ size,
-                                    int *__restrict__ act_size, int *__restrict__ act_count) {
+                                    int *__restrict__ act_size, int *__restrict__ act_count,
+                                    int *__restrict__ ncomp) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const bool valid = i < n;
@@ -411,7 +427,8 @@ __global__ void sym_classify_kernel(int n, const float *__restrict__ core,
     if (valid && lane == __ffs(peers) - 1) atomicAdd(&size[cl], __popc(peers));
     const unsigned actb = __ballot_sync(0xffffffffu, act);
     const unsigned apeers = peers & actb;
-    if (act && lane == __ffs(apeers) - 1) atomicAdd(&act_size[cl], __popc(apeers));
+    if (act && lane == __ffs(apeers) - 1 && atomicAdd(&act_size[cl], __popc(apeers)) == 0)
+        atomicAdd(ncomp, 1);
     if (lane == 0 && actb) atomicAdd(act_count, __popc(actb));
 }
 
@@ -455,14 +472,14 @@ __global__ void sym_prepare_kernel(int n, int np, int ld, const int *__restrict_
 
 cudaError_t launch_sym_classify(int n, const int *comp, const unsigned *ub, const float *core,
                                 unsigned *umax, unsigned char *act_flag, int *size, int *act_size,
-                                int *act_count, cudaStream_t s) {
+                                int *act_count, int *ncomp, cudaStream_t s) {
     const int blocks = (n + 255) / 256;
     sym_bound_max_kernel<<<blocks, 256, 0, s>>>(n, comp, ub, umax);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_extra_launches(1);
     sym_classify_kernel<<<blocks, 256, 0, s>>>(n, core, comp, umax, act_flag, size, act_size,
-                                               act_count);
+                                               act_count, ncomp);
     return cudaGetLastError();
 }
 

@@ -266,6 +266,21 @@ int hdbmst_set_engine(int engine);
 #define HDBMST_SCAN_SYMMETRIC 2
 int hdbmst_set_scan_form(int form);
 
+/*
+ * Block pruning of the symmetric scan (process-wide, not thread-safe; on by
+ * default).  It applies with at least 16 384 points, at most 64 features,
+ * at most 1024 components with points to scan and at most 8192 blocks of
+ * 128 such points.  The points are grouped by component in a spatial order
+ * (nearest of 128 pivots, then distance to it); a home pass evaluates each
+ * block's 8 nearest blocks of other components (by the pivots'
+ * triangle-inequality bound); the second pass skips every block pair whose
+ * distance bound exceeds the component bounds the home pass left (page
+ * "HDBSCAN", "Exact shortcuts": work is skipped only where a bound proves it
+ * cannot change the result).  The tree is the same with it on or off.
+ * on = 0 turns it off; returns the previous setting (1 or 0).
+ */
+int hdbmst_set_scan_pruning(int on);
+
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);
 

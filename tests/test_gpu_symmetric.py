@@ -22,14 +22,17 @@ def h():
     mod = H()
     pe = mod.set_engine("auto")
     pf = mod.set_scan_form("auto")
+    pp = mod.set_scan_pruning(True)
     yield mod
     mod.set_engine(pe)
     mod.set_scan_form(pf)
+    mod.set_scan_pruning(pp)
 
 
-def tree(h, X, ms, engine="auto", form="auto", shortcuts=True):
+def tree(h, X, ms, engine="auto", form="auto", shortcuts=True, prune=True, pairs=False):
     h.set_engine(engine)
     h.set_scan_form(form)
+    h.set_scan_pruning(prune)
     Xd = dev(X)
     core, idx, dist = h.core_distances(Xd, ms)
     if shortcuts:
@@ -38,9 +41,12 @@ def tree(h, X, ms, engine="auto", form="auto", shortcuts=True):
         e, w = h.mr_mst(Xd, core)
     e = np_(e)
     rec = h.last_mst_symmetric()
+    scanned = h.last_mst_scan_pairs()
     h.set_engine("auto")
     h.set_scan_form("auto")
-    return e[:, 0].astype(np.int64), e[:, 1].astype(np.int64), np_(w), rec
+    h.set_scan_pruning(True)
+    out = (e[:, 0].astype(np.int64), e[:, 1].astype(np.int64), np_(w), rec)
+    return out + (scanned,) if pairs else out
 
 
 def same(a, b):
@@ -143,3 +149,57 @@ def test_symmetric_far_from_origin(h):
     s = tree(h, X, 5, form="symmetric")
     f = tree(h, X, 5, engine="simt")
     assert same(s, f)
+
+
+def mixture(n, d, seed, clusters=20, outlier_frac=0.05, dup_frac=0.0, mean_sd=4.0):
+    return workloads.draw(workloads.Mixture(n=n, d=d, clusters=clusters, mean_sd=mean_sd,
+                                            sigma=None, sigma_range=(0.5, 2.0),
+                                            outlier_frac=outlier_frac, dup_frac=dup_frac,
+                                            seed=seed))
+
+
+def pruned_vs_unpruned(h, X, ms):
+    a = tree(h, X, ms, form="symmetric", pairs=True)
+    b = tree(h, X, ms, form="symmetric", prune=False, pairs=True)
+    o = tree(h, X, ms, form="one_sided")
+    assert same(a, b) and same(a, o)
+    return a, b
+
+
+def test_pruned_50k(h):
+    """The 50k-clip workload (block pruning on: at least 16 384 points): the
+    pruned, unpruned and one-sided scans give the same tree, and the
+    pruned one evaluates fewer pairs."""
+    X, task = workloads.workload("hdbscan_50k_d61")
+    a, b = pruned_vs_unpruned(h, X, task["min_samples"])
+    assert a[4] < b[4], (a[4], b[4])
+
+
+@pytest.mark.parametrize("n,d,ms,seed", [(20000, 40, 7, 1), (30000, 64, 10, 2), (16384, 33, 5, 3),
+                                         (17001, 20, 4, 4)])
+def test_pruned_mixtures(h, n, d, ms, seed):
+    """Clustered sets with outliers, ragged block counts, 20 to 64 features."""
+    X = mixture(n, d, seed=seed)
+    pruned_vs_unpruned(h, X, ms)
+
+
+def test_pruned_heavy_duplicates(h):
+    """Every point has many exact copies: equal weights everywhere, decided by
+    the index order."""
+    rng = np.random.default_rng(4)
+    base = mixture(400, 24, seed=5, outlier_frac=0.0)
+    X = np.ascontiguousarray(base[:, rng.integers(0, 400, size=24000)])
+    pruned_vs_unpruned(h, X, 6)
+
+
+def test_pruned_far_from_origin(h):
+    """Norms far above the distances."""
+    X = np.ascontiguousarray(mixture(20000, 32, seed=11) + np.float32(300.0), dtype=np.float32)
+    pruned_vs_unpruned(h, X, 7)
+
+
+def test_pruned_many_small_clusters(h):
+    """Hundreds of small clusters: more components than the grouping takes in
+    the early rounds (those run unpruned), fewer later."""
+    X = mixture(40000, 16, seed=9, clusters=600, outlier_frac=0.02, mean_sd=6.0)
+    pruned_vs_unpruned(h, X, 5)
