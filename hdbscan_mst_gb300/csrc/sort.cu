@@ -7,9 +7,10 @@
 // digit radix sort on 8-bit digits: the digits of hi, then lo, then the
 // weight's bits (non-negative floats order like their bit patterns).
 //
-// One pass = per-tile digit histograms, one exclusive scan over
-// (digit, tile) in digit-major order, then a stable scatter in which each
-// warp ranks equal digits with __match_any_sync.
+// One pass = per-tile digit histograms, then a stable scatter: each block
+// sums the histograms into its tile's first position per digit (all smaller
+// digits, then the same digit in earlier tiles) and each warp ranks equal
+// digits with __match_any_sync.
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,51 +37,34 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(int N, const unsigne
     hist[threadIdx.x * tiles + blockIdx.x] = h[threadIdx.x];
 }
 
-// Exclusive scan of `total` counters in place, one block, chunks of 1024.
-__global__ void __launch_bounds__(1024) prefix_kernel(unsigned *__restrict__ v, int total) {
-    __shared__ unsigned warp_sum[32];
-    __shared__ unsigned carry;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int base = 0; base < total; base += 1024) {
-        const int e = base + threadIdx.x;
-        const unsigned x = e < total ? v[e] : 0u;
-        unsigned incl = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) warp_sum[wid] = incl;
-        __syncthreads();
-        if (wid == 0) {
-            unsigned s = warp_sum[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            warp_sum[lane] = s;  // inclusive prefix of warp totals
-        }
-        __syncthreads();
-        const unsigned before = (wid ? warp_sum[wid - 1] : 0u) + carry;
-        if (e < total) v[e] = before + incl - x;
-        __syncthreads();
-        if (threadIdx.x == 1023) carry = before + incl;
-        __syncthreads();
-    }
-}
-
 __global__ void __launch_bounds__(kSortThreads) scatter_kernel(
     int N, int shift, int which, const unsigned *__restrict__ w, const int *__restrict__ lo,
     const int *__restrict__ hi, unsigned *__restrict__ w2, int *__restrict__ lo2,
     int *__restrict__ hi2, const unsigned *__restrict__ hist, int tiles) {
     __shared__ unsigned offset[256];
     __shared__ unsigned wcnt[kSortThreads / 32][256];
+    __shared__ unsigned wsum[kSortThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    offset[tid] = hist[tid * tiles + blockIdx.x];
+    // This tile's first position for digit tid: the count of all smaller
+    // digits plus that of digit tid in the tiles before this one.
+    unsigned before = 0, total = 0;
+    for (int t = 0; t < tiles; ++t) {
+        const unsigned v = hist[tid * tiles + t];
+        before += t < static_cast<int>(blockIdx.x) ? v : 0u;
+        total += v;
+    }
+    unsigned incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[wid] = incl;
     for (int q = 0; q < kSortThreads / 32; ++q) wcnt[q][tid] = 0;
+    __syncthreads();
+    unsigned wbefore = 0;
+    for (int q = 0; q < wid; ++q) wbefore += wsum[q];
+    offset[tid] = wbefore + incl - total + before;
     __syncthreads();
     const int base = blockIdx.x * kSortTile;
     for (int q = 0; q < kSortRounds; ++q) {
@@ -137,7 +121,7 @@ size_t sort_hist_entries(int N) { return static_cast<size_t>(256) * tiles_for(N 
 
 int sort_launches(int N, int index_bits) {
     const int ip = (index_bits + 7) / 8;
-    return (2 * ip + 4) * 3 + 1;
+    return (2 * ip + 4) * 2 + 1;
 }
 
 cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, unsigned *w2,
@@ -161,9 +145,6 @@ cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, uns
                                                      : sw;
         before(K_SORT, s);
         hist_kernel<<<tiles, kSortThreads, 0, s>>>(N, key, passes[p].shift, hist, tiles);
-        after(K_SORT, s);
-        before(K_SORT, s);
-        prefix_kernel<<<1, 1024, 0, s>>>(hist, 256 * tiles);
         after(K_SORT, s);
         before(K_SORT, s);
         scatter_kernel<<<tiles, kSortThreads, 0, s>>>(N, passes[p].shift, passes[p].which, sw, slo,

@@ -144,35 +144,62 @@ __global__ void __launch_bounds__(P) sym_bounds_kernel(int np, const int *__rest
     }
 }
 
-// LB[i][j] for all block pairs, 16 x 16 pairs per CTA (thread = pair), the
-// two blocks' bounds staged in shared memory.
-constexpr int kLbTile = 16;
-__global__ void __launch_bounds__(kLbTile * kLbTile) sym_lb_kernel(int blocks,
-                                                                   const float *__restrict__ Lb,
-                                                                   const float *__restrict__ Hb,
-                                                                   float *__restrict__ LB) {
-    __shared__ float sLi[kLbTile][P + 1], sHi[kLbTile][P + 1], sLj[kLbTile][P + 1],
-        sHj[kLbTile][P + 1];
-    const int i0 = blockIdx.y * kLbTile, j0 = blockIdx.x * kLbTile;
-    const int t = threadIdx.x;
-    for (int e = t; e < kLbTile * P; e += blockDim.x) {
-        const int r = e / P, p = e % P;
-        const int bi = min(i0 + r, blocks - 1), bj = min(j0 + r, blocks - 1);
-        sLi[r][p] = Lb[static_cast<int64_t>(bi) * P + p];
-        sHi[r][p] = Hb[static_cast<int64_t>(bi) * P + p];
-        sLj[r][p] = Lb[static_cast<int64_t>(bj) * P + p];
-        sHj[r][p] = Hb[static_cast<int64_t>(bj) * P + p];
+// LB[i][j] for all block pairs (LB is symmetric: only tiles with j0 >= i0
+// are computed, and written to both halves).  A CTA of 256 threads takes 64
+// x 64 pairs, each thread 4 x 4, with the pivots staged 32 at a time.
+constexpr int kLbTile = 64, kLbPiv = 32;
+__global__ void __launch_bounds__(256) sym_lb_kernel(int blocks, const float *__restrict__ Lb,
+                                                     const float *__restrict__ Hb,
+                                                     float *__restrict__ LB) {
+    const int ti = blockIdx.y, tj = blockIdx.x;
+    if (tj < ti) return;
+    __shared__ float sLi[kLbPiv][kLbTile], sHi[kLbPiv][kLbTile], sLj[kLbPiv][kLbTile],
+        sHj[kLbPiv][kLbTile];
+    const int i0 = ti * kLbTile, j0 = tj * kLbTile;
+    const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+    float lb[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) lb[a][c] = 0.f;
+    for (int p0 = 0; p0 < P; p0 += kLbPiv) {
+        __syncthreads();
+        for (int e = t; e < kLbTile * kLbPiv; e += 256) {
+            const int r = e / kLbPiv, q = e % kLbPiv;
+            const int bi = min(i0 + r, blocks - 1), bj = min(j0 + r, blocks - 1);
+            sLi[q][r] = Lb[static_cast<int64_t>(bi) * P + p0 + q];
+            sHi[q][r] = Hb[static_cast<int64_t>(bi) * P + p0 + q];
+            sLj[q][r] = Lb[static_cast<int64_t>(bj) * P + p0 + q];
+            sHj[q][r] = Hb[static_cast<int64_t>(bj) * P + p0 + q];
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int q = 0; q < kLbPiv; ++q) {
+            float li[4], hi[4], lj[4], hj[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                li[a] = sLi[q][ty + 16 * a];
+                hi[a] = sHi[q][ty + 16 * a];
+                lj[a] = sLj[q][tx + 16 * a];
+                hj[a] = sHj[q][tx + 16 * a];
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    lb[a][c] = fmaxf(lb[a][c], fmaxf(__fsub_rd(lj[c], hi[a]), __fsub_rd(li[a], hj[c])));
+        }
     }
-    __syncthreads();
-    const int ri = t / kLbTile, rj = t % kLbTile;
-    float lb = 0.f;
-#pragma unroll 8
-    for (int p = 0; p < P; ++p) {
-        lb = fmaxf(lb, __fsub_rd(sLj[rj][p], sHi[ri][p]));
-        lb = fmaxf(lb, __fsub_rd(sLi[ri][p], sHj[rj][p]));
-    }
-    const int i = i0 + ri, j = j0 + rj;
-    if (i < blocks && j < blocks) LB[static_cast<int64_t>(i) * blocks + j] = lb;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int i = i0 + ty + 16 * a, j = j0 + tx + 16 * c;
+            if (i < blocks && j < blocks) {
+                LB[static_cast<int64_t>(i) * blocks + j] = lb[a][c];
+                LB[static_cast<int64_t>(j) * blocks + i] = lb[a][c];
+            }
+        }
 }
 
 __device__ __forceinline__ bool own_pair(const int *bcomp, int i, int j) {
@@ -330,7 +357,7 @@ cudaError_t launch_sym_blocks(const SymPruneBufs &b, int np, int blocks, const i
     sym_bounds_kernel<<<blocks, P, 0, s>>>(np, act_idx, pcomp, b.order.pdY, eps, b.Lb, b.Hb,
                                            b.bcomp);
     const int g = (blocks + kLbTile - 1) / kLbTile;
-    sym_lb_kernel<<<dim3(g, g), kLbTile * kLbTile, 0, s>>>(blocks, b.Lb, b.Hb, b.LB);
+    sym_lb_kernel<<<dim3(g, g), 256, 0, s>>>(blocks, b.Lb, b.Hb, b.LB);
     sym_home_kernel<<<blocks, kHomeThreads, 0, s>>>(blocks, b.LB, b.bcomp, b.home, b.hcount);
     count_extra_launches(2);
     return cudaGetLastError();
