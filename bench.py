@@ -68,20 +68,22 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.14 MB read, 3.19 MB written) and the
-        # pruned second pass (74.68 MB read, 25.46 MB written)
-        "bytes": 52.14e6 + 3.19e6 + 74.68e6 + 25.46e6,
+        # per step: the home pass (52.14 MB read, 3.30 MB written) and the
+        # pruned second pass (73.38 MB read, 22.65 MB written)
+        "bytes": 52.14e6 + 3.30e6 + 73.38e6 + 22.65e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "d8d232505c67120036fcce50ca5c5d39732e48320ae91936f68e5821470ceef8",
+        "sha256": "f066b3087b0977501551092bfddf265004c7d31bddca31f46fdd2c8cf8378835",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the four rounds' launches (55.20 + 54.10 + 156.43 + 121.29 MB
-        # read, 0.00 + 0.00 + 4.43 + 2.52 MB written)
-        "bytes": (55.20 + 54.10 + 156.43 + 121.29 + 4.43 + 2.52) * 1e6,
-        "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
-                    "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "1f8679e6ae0be27e1770d7a76151d4fd64596bb4c6a03fb9b1b11521c68e6be8",
+        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.22 MB
+        # read) and the symmetric scans of rounds 3 and 4, home pass and
+        # pruned pass each (49.20 + 51.42 + 48.71 + 49.75 MB read); 0.01 MB
+        # written in all
+        "bytes": (54.99 + 53.22 + 49.20 + 51.42 + 48.71 + 49.75 + 0.01) * 1e6,
+        "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
+                    "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
+        "sha256": "237ea4b5a7e2cf537f751d22d1f9a09b0b76c6754b0a3f85dde1bfd9b8593195",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -192,6 +194,7 @@ def run_gpu(args):
     torch.cuda.set_device(device)
     dist = init_dist(ws, "nccl")
     import hdbscan_mst_gb300 as H
+    H.set_scan_form(args.scan_form)
 
     X, task = workloads.workload(args.workload)
     ms = task["min_samples"]
@@ -388,6 +391,7 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD_TEXT if args.workload == WORKLOAD else args.workload,
                    "n": n, "d": d, "min_samples": ms,
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "scan_form": args.scan_form,
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": main_roof,
         "rooflines": {"boruvka_scan": scan_roof, "knn_tile": knn_tile_roof},
@@ -531,6 +535,9 @@ def main(argv=None):
         help="HDBSCAN workload of the main step (profiling runs use smaller ones)")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer leg")
     ap.add_argument("--skip-knn", action="store_true", help="omit the k-NN line item")
+    ap.add_argument("--scan-form", default="auto", choices=["auto", "one_sided", "symmetric"],
+                    help="form of the Boruvka scan (the tree is the same; profiling of the "
+                         "one-sided form)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least three untimed steps
     if args.impl == "reference":
