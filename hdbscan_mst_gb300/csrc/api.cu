@@ -1067,7 +1067,61 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
             const int nf = h.fb_count;
             fallback = nf;
-            if (nf > 0) {
+            bool rescanned = false;
+            if (nf > 0 && tensor) {
+                // rows the rounding proof left open, on the tensor cores: each
+                // row's key drops to its exact cheapest edge (tc_sym.cu)
+                const int nf_pad = static_cast<int>(round_up(nf, kBM));
+                LAUNCH(K_GATHER, s, launch_gather(nf, nf_pad, p.dk, b.fb_rows, b.Xf, p.n_pad,
+                                                  core, b.comp, b.norm, nullptr, b.act_core,
+                                                  b.act_comp, b.act_norm, s));
+                LAUNCH(K_GATHER, s, launch_gather_points(nf, nf_pad, dkw, b.fb_rows, op_hi, op_lo,
+                                                         b.Xa_hi, b.Xa_lo, s));
+                CUDA_OK(cudaMemsetAsync(&b.st->sym_pairs, 0, sizeof(int), s));
+                RescanArgs ra{};
+                ra.nr = nf;
+                ra.row_idx = b.fb_rows;
+                ra.row_norm = b.act_norm;
+                ra.row_core = b.act_core;
+                ra.row_comp = b.act_comp;
+                ra.n = N;
+                ra.ldx = p.n_pad;
+                ra.col_norm = b.col_norm;
+                ra.col_core = b.col_core;
+                ra.col_orig = b.perm;
+                ra.comp_start = b.start;
+                ra.comp_size = size;
+                ra.col_tiles = col_tiles;
+                const int xt = (nf + kBM - 1) / kBM;
+                const int X0 = std::max(1, std::min(col_tiles, sm_count() / xt));
+                ra.tiles_per_split = (col_tiles + X0 - 1) / X0;
+                const int xs = (col_tiles + ra.tiles_per_split - 1) / ra.tiles_per_split;
+                ra.cand = b.cand;
+                // the scan's candidate slabs, read by the refine before this
+                int2 *pairs = reinterpret_cast<int2 *>(b.part_key);
+                ra.pairs = pairs;
+                ra.pair_count = &b.st->sym_pairs;
+                ra.pair_cap = static_cast<int>(
+                    std::min<size_t>(scan_part_entries(kMaxSplits, p.n_pad), 1u << 30));
+                ra.d = d;
+                ra.dk = p.dk;
+                ra.err_c = err_c;
+                ra.e0 = &b.st->e0;
+                ra.f16 = f16 ? 1 : 0;
+                ra.amax_bits = &b.st->amax_bits;
+                ra.status = &b.st->status;
+                LAUNCH(K_SCAN_EXACT, s, launch_tc_rescan(ra, b.Xa_hi, b.Xa_lo, b.Xs_hi, b.Xs_lo,
+                                                         xt, xs, s));
+                rs = read_status(b.st, h, s);
+                if (rs != HDBMST_OK) return rs;
+                if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
+                if (h.sym_pairs <= ra.pair_cap) {
+                    LAUNCH(K_SCAN_EXACT, s, launch_sym_pairs_exact(pairs, h.sym_pairs, nullptr,
+                                                                   b.Xp, p.dk, core, b.cand, s));
+                    rescanned = true;
+                }
+            }
+            if (nf > 0 && !rescanned) {
                 // rows the rounding proof left open: gather them as rows and
                 // search them again with the exact weight
                 if (tensor)

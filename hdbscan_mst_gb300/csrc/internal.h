@@ -384,7 +384,38 @@ cudaError_t launch_sym_classify(int n, const int *comp, const unsigned *ub, cons
 cudaError_t launch_sym_prepare(int n, int np, int ld, const int *pcomp, const unsigned *ub,
                                unsigned *theta, float *norm, int4 *tile_meta, cudaStream_t s);
 cudaError_t launch_tc_sym(const SymArgs &a, const float *x_hi, const float *x_lo, cudaStream_t s);
-// The recorded pairs' exact weights into both ends' candidate keys.
+// The rows the one-sided refine left open against all points on the tensor
+// cores (tc_sym.cu): each row's key drops to its exact cheapest edge, the
+// columns that need an exact weight appended as point-index pairs.
+struct RescanArgs {
+    int nr;                   // open rows, gathered (A operand rows nr_pad)
+    const int *row_idx;       // [nr] point index
+    const float *row_norm;    // [nr_pad] |a|^2
+    const float *row_core;    // [nr_pad]
+    const int *row_comp;      // [nr_pad]
+    int n;                    // columns: all points grouped by component
+    int64_t ldx;              // padded columns (rows of the B operand arrays)
+    const float *col_norm;    // [ldx] +inf past n
+    const float *col_core;    // [ldx]
+    const int *col_orig;      // [ldx]
+    const int *comp_start, *comp_size;
+    int col_tiles, tiles_per_split;
+    unsigned long long *cand;
+    int2 *pairs;              // [pair_cap] (row point, column point)
+    int *pair_count;
+    int pair_cap;
+    int d, dk;
+    float err_c;
+    const float *e0;
+    int f16;
+    const unsigned *amax_bits;
+    unsigned *status;
+};
+cudaError_t launch_tc_rescan(const RescanArgs &a, const float *a_hi, const float *a_lo,
+                            const float *b_hi, const float *b_lo, int row_tiles, int splits,
+                            cudaStream_t s);
+// The recorded pairs' exact weights into both ends' candidate keys (idx null:
+// the pairs hold point indices).
 cudaError_t launch_sym_pairs_exact(const int2 *pairs, int count, const int *idx, const float *Xp,
                                    int dk, const float *core, unsigned long long *cand,
                                    cudaStream_t s);

@@ -32,7 +32,7 @@
 // component has no bound).
 //
 // The test per pair: with t = |b|^2 - 2 a.b from the tile, a pair with
-// t >= tau(theta) weighs more than theta (the rounding bound of the engine,
+// t >= tau(theta) weighs strictly more than theta (the rounding bound of the engine,
 // err_c and e0, and the float32 evaluation of the exact weight; see
 // sym_tau), and a pair whose core distances exceed theta does too.  Each
 // thread (one row) filters a tile's columns against tau(max(theta_row,
@@ -64,6 +64,12 @@ using namespace tc;
 constexpr int kEpiWarps = 12;
 constexpr int kSymThreads = (kEpiWarps + 1 + kEpiWarps / 4) * 32;  // + producer + MMA warps
 
+struct TcRescanParams {
+    PipeMaps maps;  // B: all points grouped by component, point-major [rows][dk]
+    const float *a_hi, *a_lo;  // A: the open rows, point-major
+    RescanArgs a;
+};
+
 struct TcSymParams {
     PipeMaps maps;  // B: the points of P in grouped order, point-major [rows][dk]
     const float *x_hi, *x_lo;
@@ -77,21 +83,25 @@ __shared__ int4 s_smeta[kEpiWarps][2];
 constexpr int kListCache = 2048;  // list entries kept in shared memory
 __shared__ int s_list[kListCache];
 
-// The least t a pair can have without weighing more than th, from the row's
-// side (|a|^2 = na): with T = th^2 (1 + 16 u) / (1 - (d + 3) u), a pair's true
-// squared distance is at least na + t - c (na + nb) - e0; for nb up to
-// nb_c = (|a| + sqrt(T))^2 that is at least T once t >= T + c (na + nb_c) +
-// e0 - na, and beyond nb_c the distance exceeds sqrt(T) by the triangle
-// inequality.  A true squared distance of T or more evaluates (float32,
-// ascending features, then sqrt) to more than th.  Rounded up, plus 2^-20 of
-// its magnitude.
+// The filter of a bound th from the row's side (|a|^2 = na): a pair with
+// t >= sym_tau(th) weighs strictly more than th.  With th' = max(th, 2^-50)
+// and T = th'^2 (1 + 16 u) / (1 - (d + 3) u), a pair's true squared distance
+// is at least na + t - c (na + nb) - e0; for nb up to nb_c = (|a| +
+// sqrt(T))^2 that exceeds T once t > X = T + c (na + nb_c) + e0 - na, and
+// beyond nb_c the distance exceeds sqrt(T) by the triangle inequality.  A
+// true squared distance above T (> 2^-100, so no squared difference of it
+// underflows) evaluates (float32, ascending features, then sqrt) to more than
+// th'.  X is rounded up, plus 2^-20 of its magnitude; the filter is the next
+// float above it (t < filter <=> t <= X), so that th = 0 - two copies of a
+// point with core distance 0 - still lets equal weights through.
 __device__ __forceinline__ float sym_tau(float th, float na, float c, float e0, int d) {
     if (!(th < INFINITY)) return INFINITY;
-    const float T = proof_T_up(th, d);
+    const float T = proof_T_up(fmaxf(th, 0x1p-50f), d);
     const float sq = __fadd_ru(__fsqrt_ru(na), __fsqrt_ru(T));
     const float X =
         __fsub_ru(__fadd_ru(__fadd_ru(T, __fmul_ru(c, __fadd_ru(na, __fmul_ru(sq, sq)))), e0), na);
-    return __fadd_ru(X, __fmul_ru(__fadd_ru(fabsf(X), __fadd_ru(na, T)), 0x1p-20f));
+    return nextafterf(__fadd_ru(X, __fmul_ru(__fadd_ru(fabsf(X), __fadd_ru(na, T)), 0x1p-20f)),
+                      INFINITY);
 }
 
 // An upper bound of the exact weight's distance part from an upper bound D of
@@ -370,8 +380,138 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
     tc_teardown<kEpiWarps>(S, a.status);
 }
 
-// Exact weights of the recorded pairs (positions in P), into both ends'
-// candidate keys.  The squared distance is the library's: float32
+// The rows the one-sided refine left open (page "HDBSCAN", "Exact
+// shortcuts": only these still lack a proven cheapest edge) against all
+// points, on the tensor cores.  Each row starts from th = the exact weight of
+// its best kept candidate (its key after the refine, a real edge): a column
+// whose weight lower bound (as in the symmetric scan) exceeds th cannot be
+// the row's cheapest edge, not even on index order.  A column whose core
+// distance dominates its distance bound has that core distance as its exact
+// weight and lowers the row's key at once (the ties at the row's own core
+// distance - exact copies of the point in other components - that left the
+// row open); any other column that can win is appended (point indices) for
+// sym_pairs_exact_kernel.  th drops to each recorded column's upper bound.
+// Grid: row tiles x column splits.
+__shared__ float4 s_rnorm[kEpiWarps][2][kTileCols / 4];
+__shared__ float4 s_rcore[kEpiWarps][2][kTileCols / 4];
+
+__global__ void __launch_bounds__(kSymThreads, 1) tc_rescan_kernel(const __grid_constant__ TcRescanParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PipeSmem S;
+    __shared__ int s_rc[kRows];
+    const RescanArgs &a = P.a;
+    uint8_t *base = pipe_base(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * kRows;
+    constexpr int kSub = kCols / kTileCols;
+    const int ct_begin = blockIdx.y * a.tiles_per_split * kSub;
+    const int ct_end = min(blockIdx.y * a.tiles_per_split + a.tiles_per_split, a.col_tiles) * kSub;
+
+    if (tid < kRows) s_rc[tid] = r0 + tid < a.nr ? a.row_comp[r0 + tid] : -1;
+    tc_setup<kEpiWarps>(S);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const bool uniform =
+        __syncthreads_and(tid >= kRows || r0 + tid >= a.nr || s_rc[tid] == s_rc[0]);
+    int skip_lo = 0, skip_hi = 0;
+    if (uniform) {
+        const int C = s_rc[0];
+        const int c0 = a.comp_start[C], c1 = c0 + a.comp_size[C];
+        skip_lo = (c0 + kCols - 1) / kCols * kSub;
+        skip_hi = c1 / kCols * kSub;
+    }
+    const TileSeq seq(ct_begin, ct_end, skip_lo, skip_hi);
+    const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
+    if (a.f16)
+        tc_produce_and_multiply<kEpiWarps, false, true>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+    else
+        tc_produce_and_multiply<kEpiWarps, false, false>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+    if (warp < 4) tc_load_a(S, P.a_hi, P.a_lo, r0, dk_mma);
+
+    if (warp < kEpiWarps) {
+        const int row = (warp & 3) * 32 + lane;
+        const int r = r0 + row;
+        const bool valid = r < a.nr;
+        const float na = valid ? a.row_norm[r] : 0.f;
+        const float ca = valid ? a.row_core[r] : INFINITY;
+        const int rc = s_rc[row];
+        const int ga = valid ? a.row_idx[r] : 0;
+        const int own_lo = valid ? a.comp_start[rc] : 0;
+        const int own_hi = valid ? own_lo + a.comp_size[rc] : 0;
+        const float kdot = a.f16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
+        const float c = a.err_c, e0 = *a.e0;
+        const unsigned long long k0 = valid ? a.cand[ga] : kNoKey;
+        float th = valid ? (k0 == kNoKey ? INFINITY : key_w(k0)) : -INFINITY;
+        float thr = valid ? sym_tau(th, na, c, e0, a.d) : -INFINITY;
+        const auto prefetch = [&](int col0, int buf) {
+            if (lane < 16) cp_async16(&s_rnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
+            else cp_async16(&s_rcore[warp][buf][lane - 16], a.col_core + col0 + (lane - 16) * 4);
+        };
+        tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+            const float *nbs = reinterpret_cast<const float *>(&s_rnorm[warp][buf][0]);
+            const float *cbs = reinterpret_cast<const float *>(&s_rcore[warp][buf][0]);
+#pragma unroll 1
+            for (int cc = 0; cc < kTileCols / 32; ++cc) {
+                const int cb0 = col0 + cc * 32;
+                const int blo = min(max(own_lo - cb0, 0), 32);
+                const int bhi = min(max(own_hi - cb0, 0), 32);
+                if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
+                float v[32];
+                tmem_ld32(tbase + cc * 32, v);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 nb = s_rnorm[warp][buf][cc * 8 + j4];
+                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
+                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
+                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
+                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
+                }
+                float m16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
+#pragma unroll
+                for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+                if (!(m16[0] < thr)) continue;
+                const uint32_t own = bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
+                uint32_t mask = below_mask(v, thr) & ~own;
+#pragma unroll 1
+                while (mask) {
+                    const int j = __ffs(mask) - 1;
+                    mask &= mask - 1;
+                    const int b = cb0 + j;
+                    if (b >= a.n) break;
+                    const float cm = fmaxf(ca, cbs[cc * 32 + j]);
+                    if (cm > th) continue;
+                    const float tj = pick32(v, j);
+                    const float err = __fadd_ru(__fmul_ru(c, __fadd_ru(na, nbs[cc * 32 + j])), e0);
+                    const float wub = fmaxf(cm, sym_dist_up(__fadd_ru(__fadd_ru(tj, na), err), a.d));
+                    const float wlb =
+                        fmaxf(cm, sym_dist_down(__fsub_rd(__fadd_rd(tj, na), err), a.d));
+                    if (wlb > th) continue;
+                    const unsigned gb = static_cast<unsigned>(__ldg(a.col_orig + b));
+                    if (cm >= wub) {
+                        atomicMin(a.cand + ga, key64(cm, gb));
+                    } else {
+                        const int pos = atomicAdd(a.pair_count, 1);
+                        if (pos >= a.pair_cap) continue;  // the host falls back to the exact scan
+                        a.pairs[pos] = make_int2(ga, static_cast<int>(gb));
+                    }
+                    if (wub < th) {
+                        th = wub;
+                        thr = sym_tau(th, na, c, e0, a.d);
+                    }
+                }
+            }
+        });
+    }
+    tc_teardown<kEpiWarps>(S, a.status);
+}
+
+// Exact weights of the recorded pairs (positions in P, or point indices when
+// idx is null), into both ends' candidate keys.  The squared distance is the library's: float32
 // differences squared and summed by FMA in ascending feature order.
 __global__ void __launch_bounds__(256) sym_pairs_exact_kernel(const int2 *__restrict__ pairs,
                                                               int count,
@@ -382,7 +522,7 @@ __global__ void __launch_bounds__(256) sym_pairs_exact_kernel(const int2 *__rest
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= count) return;
     const int2 p = pairs[q];
-    const int ga = idx[p.x], gb = idx[p.y];
+    const int ga = idx ? idx[p.x] : p.x, gb = idx ? idx[p.y] : p.y;
     const float4 *xa = reinterpret_cast<const float4 *>(Xp + static_cast<int64_t>(ga) * dk);
     const float4 *xb = reinterpret_cast<const float4 *>(Xp + static_cast<int64_t>(gb) * dk);
     float acc = 0.f;
@@ -504,6 +644,25 @@ cudaError_t launch_tc_sym(const SymArgs &a, const float *x_hi, const float *x_lo
                                          static_cast<int>(kPipeSmem));
     if (e != cudaSuccess) return e;
     tc_sym_kernel<<<a.blocks, kSymThreads, kPipeSmem, s>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_rescan(const RescanArgs &a, const float *a_hi, const float *a_lo,
+                            const float *b_hi, const float *b_lo, int row_tiles, int splits,
+                            cudaStream_t s) {
+    TcRescanParams P;
+    P.a = a;
+    P.a_hi = a_hi;
+    P.a_lo = a_lo;
+    const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
+    if ((a.f16 && dk_mma != kSlab) || !make_point_map(&P.maps.b_hi, b_hi, a.ldx, dk_mma) ||
+        !make_point_map(&P.maps.b_lo, b_lo, a.ldx, dk_mma))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(tc_rescan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPipeSmem));
+    if (e != cudaSuccess) return e;
+    tc_rescan_kernel<<<dim3(row_tiles, splits), kSymThreads, kPipeSmem, s>>>(P);
     return cudaGetLastError();
 }
 
