@@ -261,6 +261,23 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int j) {
     return (j & 16) ? d1 : d0;
 }
 
+// The least of 32 values by three-input minima (min.f32 with three operands):
+// 17 instructions in 4 levels instead of 31 in 5.
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min32(const float (&v)[32]) {
+    float m[11];
+#pragma unroll
+    for (int j = 0; j < 10; ++j) m[j] = min3f(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+    m[10] = fminf(v[30], v[31]);
+    const float a = min3f(m[0], m[1], m[2]), b = min3f(m[3], m[4], m[5]),
+                c = min3f(m[6], m[7], m[8]);
+    return min3f(min3f(a, b, c), m[9], m[10]);
+}
+
 // Bit j set where v[j] < thr.
 __device__ __forceinline__ uint32_t below_mask(const float (&v)[32], float thr) {
     uint32_t m = 0;

@@ -189,13 +189,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                 }
                 // the batch's least t by a depth-5 tree, against the least
                 // published KP-th key of the row (stale values only loosen it)
-                float m16[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
-#pragma unroll
-                for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+                const float vmin = min32(v);
                 // the least of: every list's KP-th key, the largest of the
                 // lists' q-th keys, the seed and the shared threshold
                 float tau = fminf(key[KP - 1], seed), tq = -INFINITY;
@@ -208,7 +202,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                 if (gthr_warp)  // the least KP-th key any CTA of the row tile has published
                     tau = fminf(tau, order_float(reinterpret_cast<const unsigned *>(
                                          &s_gthr[warp][buf][0])[lane]));
-                if (m16[0] < tau) {
+                if (vmin < tau) {
                     // rare: insert this batch's candidates in column order
                     // with the one copy of the sink
                     uint32_t mask = below_mask(v, tau);

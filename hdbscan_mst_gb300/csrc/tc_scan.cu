@@ -174,17 +174,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                     v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
                     v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
                 }
-                float m16[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
-#pragma unroll
-                for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
+                const float vmin = min32(v);
                 // v >= t, so a batch whose least t does not beat the row's
                 // least published 4th value cannot change any list's 4 best
                 const float thr = fminf(key_v(keys[kKeep - 1]), thr_tile);
-                if (m16[0] < thr) {
+                if (vmin < thr) {
                     const uint32_t own =
                         bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
                     uint32_t mask = below_mask(v, thr) & ~own;

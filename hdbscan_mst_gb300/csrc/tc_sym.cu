@@ -263,14 +263,8 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
                     v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
                     v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
                 }
-                float m16[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
-#pragma unroll
-                for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
-                const bool hit = m16[0] < fmaxf(thr, thr2);
+                const float vmin = min32(v);
+                const bool hit = vmin < fmaxf(thr, thr2);
                 if (!__any_sync(0xffffffffu, hit)) continue;
                 const uint32_t own = bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
                 // columns of this batch in c1's range: bits [0, k1)
@@ -467,16 +461,11 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_rescan_kernel(const __grid_
                     v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
                     v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
                 }
-                float m16[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) m16[j] = fminf(v[j], v[j + 16]);
-#pragma unroll
-                for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w2; ++j) m16[j] = fminf(m16[j], m16[j + w2]);
-                if (!(m16[0] < thr)) continue;
+                const float vmin = min32(v);
+                // warp-uniform exit: the next batch's TMEM load is collective
+                if (!__any_sync(0xffffffffu, vmin < thr)) continue;
                 const uint32_t own = bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;
-                uint32_t mask = below_mask(v, thr) & ~own;
+                uint32_t mask = vmin < thr ? (below_mask(v, thr) & ~own) : 0u;
 #pragma unroll 1
                 while (mask) {
                     const int j = __ffs(mask) - 1;
