@@ -168,6 +168,40 @@ int sm_count() {
     return sms;
 }
 
+// A second stream (per host thread and device) for work that can run beside
+// the caller's stream, with the events that fork it from and join it to
+// that stream.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t side_stream(SideStream **out) {
+    constexpr int kMaxDevices = 64;
+    thread_local SideStream side[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream &x = side[dev];
+    if (!x.s) {
+        if ((e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &x;
+    return cudaSuccess;
+}
+
+// Makes the caller's stream wait for the side stream's work when it goes out
+// of scope (every return path), so no work on the workspace outlives a call.
+struct JoinOnExit {
+    cudaStream_t s;
+    cudaEvent_t e = nullptr;
+    ~JoinOnExit() {
+        if (e) cudaStreamWaitEvent(s, e, 0);
+    }
+};
+
 // Column splits that fill the GPU's CTA slots in whole waves.
 int choose_splits(int row_tiles, int col_tiles, int slots) {
     int best = 1;
@@ -868,8 +902,19 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     // pruned symmetric scan, once per call
     const bool sp_ready = p.sprune && tensor && shortcuts && g_scan_form != HDBMST_SCAN_ONE_SIDED &&
                           g_sym_prune;
-    if (sp_ready)
-        LAUNCH(K_SYM_PRUNE, s, launch_spatial_order(b.sp.order, X, ldx, N, X, ldx, N, true, d, s));
+    // It is first needed by round 3 or so: it runs on a side stream beside
+    // the first rounds, whose one-sided scans leave most SMs idle.
+    JoinOnExit sp_join{s};
+    if (sp_ready) {
+        SideStream *ss = nullptr;
+        CUDA_OK(side_stream(&ss));
+        CUDA_OK(cudaEventRecord(ss->fork, s));
+        CUDA_OK(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+        LAUNCH(K_SYM_PRUNE, ss->s,
+               launch_spatial_order(b.sp.order, X, ldx, N, X, ldx, N, true, d, ss->s));
+        CUDA_OK(cudaEventRecord(ss->join, ss->s));
+        sp_join.e = ss->join;
+    }
     for (int round = 0; round < max_rounds && edges < N - 1; ++round) {
         int fallback = 0;
         int64_t recorded = -1;
@@ -916,9 +961,11 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                              b.act_flag, size, act_size, b.start, b.act_start,
                                              cursor, act_cursor, totals, b.perm, b.col_comp,
                                              b.col_core, b.col_norm, b.act_idx, s));
-            if (pruned)
+            if (pruned) {
+                CUDA_OK(cudaStreamWaitEvent(s, sp_join.e, 0));  // the spatial order
                 LAUNCH(K_SYM_PRUNE, s, launch_sym_group(b.sp, N, b.act_flag, b.comp, b.act_start,
-                                                     act_size, b.act_idx, s));
+                                                        act_size, b.act_idx, s));
+            }
             LAUNCH(K_GATHER, s, launch_gather(np, np_pad, p.dk, b.act_idx, b.Xf, p.n_pad, core,
                                               b.comp, b.norm, nullptr, b.act_core, b.act_comp,
                                               b.act_norm, s));
