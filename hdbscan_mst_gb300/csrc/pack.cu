@@ -92,6 +92,94 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
     if ((threadIdx.x & 31) == 0 && nbmax_bits && bits) atomicMax(nbmax_bits, bits);
 }
 
+// The same outputs as pack_kernel (without perm), staged through shared
+// memory: a CTA takes 32 points, reads 64 features at a time with coalesced
+// rows of the caller's feature-major set, then half-warps write each point's
+// point-major rows (256 bytes of floats, 128 bytes of halves) contiguously.
+// Each point's norm is the same ascending-feature chain of fused
+// multiply-adds as in pack_kernel, so the bits agree.
+constexpr int kPackPts = 32, kPackF = 64;
+__global__ void __launch_bounds__(256) pack_tile_kernel(const float *__restrict__ X, int64_t ld,
+                                                        int n, int d, int n_pad, int dk,
+                                                        float *__restrict__ Xf,
+                                                        float *__restrict__ Xp,
+                                                        float *__restrict__ Xlo,
+                                                        float *__restrict__ norm,
+                                                        unsigned *__restrict__ status,
+                                                        unsigned *__restrict__ nbmax_bits,
+                                                        uint2 *__restrict__ Xh16,
+                                                        uint2 *__restrict__ Xl16,
+                                                        const unsigned *__restrict__ amax_bits,
+                                                        float *__restrict__ e0_out,
+                                                        const int *__restrict__ inv) {
+    __shared__ float xs[kPackF][kPackPts + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = blockIdx.x * kPackPts;
+    const float scale = Xh16 ? ldexpf(1.f, f16_scale_exp(*amax_bits)) : 1.f;
+    if (Xh16 && e0_out && blockIdx.x == 0 && tid == 0)
+        *e0_out = __double2float_ru(f16_abs_err(true, dk, *amax_bits));
+    float acc = 0.f;  // warp 0: point i0 + lane
+    bool finite = true;
+    const int ip = i0 + lane;
+    const int dst_own = (ip < n && inv) ? inv[ip] : ip;
+    for (int f0 = 0; f0 < dk; f0 += kPackF) {
+        const int fc = min(kPackF, dk - f0);
+        __syncthreads();
+        for (int r = warp; r < fc; r += 8) {
+            const int f = f0 + r;
+            const float v = (f < d && ip < n) ? X[static_cast<int64_t>(f) * ld + ip] : 0.f;
+            xs[r][lane] = v;
+            if (Xf && ip < n_pad) Xf[static_cast<int64_t>(f) * n_pad + dst_own] = v;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            for (int r = 0; r < fc; ++r) {
+                const float v = xs[r][lane];
+                finite = finite && isfinite(v);
+                acc = __fmaf_rn(v, v, acc);
+            }
+        }
+        // half-warp h of warp w: points 2 w + h, + 16, ...; lane c: features 4c .. 4c + 3
+        const int c = lane & 15;
+        for (int q = warp * 2 + (lane >> 4); q < kPackPts; q += 16) {
+            const int i = i0 + q;
+            if (4 * c >= fc || i >= n_pad) continue;
+            const int dst = (i < n && inv) ? inv[i] : i;
+            const float v0 = xs[4 * c][q], v1 = xs[4 * c + 1][q], v2 = xs[4 * c + 2][q],
+                        v3 = xs[4 * c + 3][q];
+            const int64_t e = static_cast<int64_t>(dst) * dk + f0 + 4 * c;
+            if (Xp) *reinterpret_cast<float4 *>(Xp + e) = make_float4(v0, v1, v2, v3);
+            if (Xlo) {
+                const float l0 = __fsub_rn(v0, __uint_as_float(__float_as_uint(v0) & 0xFFFFE000u));
+                const float l1 = __fsub_rn(v1, __uint_as_float(__float_as_uint(v1) & 0xFFFFE000u));
+                const float l2 = __fsub_rn(v2, __uint_as_float(__float_as_uint(v2) & 0xFFFFE000u));
+                const float l3 = __fsub_rn(v3, __uint_as_float(__float_as_uint(v3) & 0xFFFFE000u));
+                *reinterpret_cast<float4 *>(Xlo + e) = make_float4(l0, l1, l2, l3);
+            }
+            if (Xh16) {
+                unsigned short h0, h1, h2, h3, lo0, lo1, lo2, lo3;
+                f16_split(v0, scale, h0, lo0);
+                f16_split(v1, scale, h1, lo1);
+                f16_split(v2, scale, h2, lo2);
+                f16_split(v3, scale, h3, lo3);
+                Xh16[e / 4] = make_uint2(h0 | (static_cast<unsigned>(h1) << 16),
+                                         h2 | (static_cast<unsigned>(h3) << 16));
+                Xl16[e / 4] = make_uint2(lo0 | (static_cast<unsigned>(lo1) << 16),
+                                         lo2 | (static_cast<unsigned>(lo3) << 16));
+            }
+        }
+    }
+    if (warp == 0) {
+        const bool valid = ip < n;
+        if (ip < n_pad) norm[dst_own] = valid ? acc : INFINITY;
+        if (!finite) atomicOr(status, kStatusNonFinite);
+        unsigned bits = valid ? __float_as_uint(acc) : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bits = max(bits, __shfl_xor_sync(0xffffffffu, bits, o));
+        if (lane == 0 && nbmax_bits && bits) atomicMax(nbmax_bits, bits);
+    }
+}
+
 // Largest magnitude of the caller's [d, n] set, raised into *amax_bits
 // (non-negative floats order like their bits; non-finite values are the pack
 // kernel's to report).
@@ -126,6 +214,13 @@ cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm, uint32_t *Xh16,
                         uint32_t *Xl16, const unsigned *amax_bits, float *e0_out,
                         const int *inv) {
+    if (!perm && dk % 32 == 0) {
+        pack_tile_kernel<<<(n_pad + kPackPts - 1) / kPackPts, 256, 0, s>>>(
+            X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status, nbmax_bits,
+            reinterpret_cast<uint2 *>(Xh16), reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out,
+            inv);
+        return cudaGetLastError();
+    }
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
                                        nbmax_bits, perm, reinterpret_cast<uint2 *>(Xh16),
