@@ -68,22 +68,22 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.14 MB read, 3.30 MB written) and the
-        # pruned second pass (73.38 MB read, 22.65 MB written)
-        "bytes": 52.14e6 + 3.30e6 + 73.38e6 + 22.65e6,
+        # per step: the home pass (52.14 MB read, 3.13 MB written) and the
+        # pruned second pass (73.67 MB read, 22.70 MB written)
+        "bytes": 52.14e6 + 3.13e6 + 73.67e6 + 22.70e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "f066b3087b0977501551092bfddf265004c7d31bddca31f46fdd2c8cf8378835",
+        "sha256": "f1f663fadf675111e6b552cde31fdf265fa9f9a58c29edd9f783fae36d44a658",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.22 MB
+        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.20 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.20 + 51.42 + 48.71 + 49.75 MB read); 0.01 MB
+        # pruned pass each (49.20 + 51.61 + 48.67 + 49.64 MB read); 0.01 MB
         # written in all
-        "bytes": (54.99 + 53.22 + 49.20 + 51.42 + 48.71 + 49.75 + 0.01) * 1e6,
+        "bytes": (54.99 + 53.20 + 49.20 + 51.61 + 48.67 + 49.64 + 0.01) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "237ea4b5a7e2cf537f751d22d1f9a09b0b76c6754b0a3f85dde1bfd9b8593195",
+        "sha256": "7676b976d31da8182a3eeb8cf563ae0061288cca101d9a1470798d0f0d0ca4a3",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
