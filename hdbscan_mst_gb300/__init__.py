@@ -93,6 +93,8 @@ def _load():
     L.hdbmst_last_mst_rounds.restype = i32
     L.hdbmst_set_engine.argtypes = [i32]
     L.hdbmst_set_engine.restype = i32
+    L.hdbmst_set_scan_list_cap.argtypes = [i64]
+    L.hdbmst_set_scan_list_cap.restype = i64
     L.hdbmst_set_scan_pruning.argtypes = [i32]
     L.hdbmst_set_scan_pruning.restype = i32
     L.hdbmst_set_scan_form.argtypes = [i32]
@@ -341,6 +343,13 @@ def set_scan_pruning(on: bool) -> bool:
     """Turn the block pruning of the symmetric scan on or off; returns the
     previous setting.  The tree is the same either way."""
     return bool(_load().hdbmst_set_scan_pruning(1 if on else 0))
+
+
+def set_scan_list_cap(cap: int) -> int:
+    """Cap the recorded-pair lists of the symmetric scan and of the open-row
+    rescan (0: the default); an overflow sends the round (rows) to the
+    one-sided (exact) scan, with the same tree.  Returns the previous cap."""
+    return int(_load().hdbmst_set_scan_list_cap(int(cap)))
 
 
 def last_mst_symmetric() -> list[int]:

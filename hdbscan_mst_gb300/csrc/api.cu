@@ -46,6 +46,15 @@ bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
 // and whether the symmetric form prunes block pairs.
 int g_scan_form = HDBMST_SCAN_AUTO;
 bool g_sym_prune = true;
+// Cap on the recorded-pair lists of the symmetric scan and of the open-row
+// rescan (0: the whole scratch they use); a list that overflows sends its
+// round to the one-sided scan, or its rows to the FP32 exact scan.
+int64_t g_list_cap = 0;
+int list_cap(size_t scratch_pairs) {
+    size_t cap = std::min<size_t>(scratch_pairs, 1u << 30);
+    if (g_list_cap > 0) cap = std::min<size_t>(cap, static_cast<size_t>(g_list_cap));
+    return static_cast<int>(cap);
+}
 
 // per-round record of the last hdbmst_mr_mst call: points scanned, edges so
 // far, rows searched exactly, pairs the symmetric scan recorded (-1: one-sided)
@@ -994,8 +1003,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             ya.cand = b.cand;
             ya.pairs = pairs;
             ya.pair_count = &b.st->sym_pairs;
-            ya.pair_cap = static_cast<int>(
-                std::min<size_t>(scan_part_entries(kMaxSplits, p.n_pad), 1u << 30));
+            ya.pair_cap = list_cap(scan_part_entries(kMaxSplits, p.n_pad));
             ya.d = d;
             ya.dk = p.dk;
             ya.err_c = err_c;
@@ -1148,8 +1156,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                 int2 *pairs = reinterpret_cast<int2 *>(b.part_key);
                 ra.pairs = pairs;
                 ra.pair_count = &b.st->sym_pairs;
-                ra.pair_cap = static_cast<int>(
-                    std::min<size_t>(scan_part_entries(kMaxSplits, p.n_pad), 1u << 30));
+                ra.pair_cap = list_cap(scan_part_entries(kMaxSplits, p.n_pad));
                 ra.d = d;
                 ra.dk = p.dk;
                 ra.err_c = err_c;
@@ -1251,6 +1258,12 @@ int hdbmst_set_engine(int engine) {
     if (engine == HDBMST_ENGINE_AUTO || engine == HDBMST_ENGINE_SIMT ||
         engine == HDBMST_ENGINE_TENSOR || engine == HDBMST_ENGINE_TF32)
         g_engine = engine;
+    return prev;
+}
+
+int64_t hdbmst_set_scan_list_cap(int64_t cap) {
+    const int64_t prev = g_list_cap;
+    g_list_cap = cap > 0 ? cap : 0;
     return prev;
 }
 

@@ -281,6 +281,18 @@ int hdbmst_set_scan_form(int form);
  */
 int hdbmst_set_scan_pruning(int on);
 
+/*
+ * Largest number of pairs the symmetric scan's list (and the list of the
+ * open-row rescan, the tensor-core search of the rows the one-sided refine
+ * could not prove) may hold; cap <= 0 restores the default (the scratch they
+ * reuse, about 32 entries per point).  A round whose list overflows is
+ * redone with the one-sided scan, rows whose rescan list overflows are
+ * searched by the FP32 exact scan; the tree is the same.  For tests of those
+ * fallbacks; process-wide, not thread-safe.  Returns the previous cap (0 for
+ * the default).
+ */
+int64_t hdbmst_set_scan_list_cap(int64_t cap);
+
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);
 

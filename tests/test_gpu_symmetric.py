@@ -206,3 +206,19 @@ def test_pruned_many_small_clusters(h):
     the early rounds (those run unpruned), fewer later."""
     X = mixture(40000, 16, seed=9, clusters=600, outlier_frac=0.02, mean_sd=6.0)
     pruned_vs_unpruned(h, X, 5)
+
+
+def test_list_overflow_falls_back(h):
+    """Lists capped at 3 pairs: the symmetric rounds that record more
+    overflow and are redone one-sided, and the open rows' rescan overflows to
+    the FP32 exact scan; the tree stays the one-sided FP32 tree."""
+    X = mixture(20000, 40, seed=13, dup_frac=0.02)
+    f = tree(h, X, 7, engine="simt")
+    prev = h.set_scan_list_cap(3)
+    try:
+        s = tree(h, X, 7, form="symmetric")
+        o = tree(h, X, 7, form="one_sided")
+    finally:
+        h.set_scan_list_cap(prev)
+    assert same(s, f) and same(o, f)
+    assert -1 in s[3] and all(r <= 3 for r in s[3]), s[3]  # overflowing rounds fell back
