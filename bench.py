@@ -68,12 +68,12 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.14 MB read, 3.13 MB written) and the
-        # pruned second pass (73.67 MB read, 22.70 MB written)
-        "bytes": 52.14e6 + 3.13e6 + 73.67e6 + 22.70e6,
+        # per step: the home pass (52.14 MB read, 3.14 MB written) and the
+        # pruned second pass (73.70 MB read, 22.81 MB written)
+        "bytes": 52.14e6 + 3.14e6 + 73.70e6 + 22.81e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "f1f663fadf675111e6b552cde31fdf265fa9f9a58c29edd9f783fae36d44a658",
+        "sha256": "f095541b0996feab567e11aca504ddd29152116ad6720d03c2cd9fd0c15ce6d8",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
         # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.20 MB
