@@ -105,3 +105,25 @@ def test_no_oracle_in_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle." not in text.replace("oracle.c", ""), f
+
+
+def test_mst_workspace_holds_the_pruning_buffers(L):
+    """With nearest lists, at most 64 features and at least 16 384 points the
+    MST workspace also holds the symmetric scan's pruning buffers: the pivot
+    distances of every point (n x 128 floats) and the block-pair bounds and
+    lists (blocks^2 each).  Without lists, with wider rows or fewer points it
+    does not."""
+    OP_MST = 2
+    n = 20000
+    blocks = (n + 127) // 128
+    with_lists = L.hdbmst_workspace_bytes(OP_MST, n, 0, 61, 11)
+    without = L.hdbmst_workspace_bytes(OP_MST, n, 0, 61, 0)
+    extra = with_lists - without
+    assert extra >= n * 128 * 4 + 2 * blocks * blocks * 4
+    # 65 features: no tensor-core scan, no pruning buffers (only the lists' own needs differ)
+    wide_extra = (L.hdbmst_workspace_bytes(OP_MST, n, 0, 65, 11)
+                  - L.hdbmst_workspace_bytes(OP_MST, n, 0, 65, 0))
+    assert wide_extra < n * 128 * 4
+    small_extra = (L.hdbmst_workspace_bytes(OP_MST, 16000, 0, 61, 11)
+                   - L.hdbmst_workspace_bytes(OP_MST, 16000, 0, 61, 0))
+    assert small_extra < 16000 * 128 * 4
