@@ -41,7 +41,7 @@ typedef struct CUstream_st *hdbmst_stream;
 typedef enum {
     HDBMST_OK = 0,
     HDBMST_ERR_ARG = 1,         /* a size, pointer, stride or count is invalid        */
-    HDBMST_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (k > KMAX ...) */
+    HDBMST_ERR_UNSUPPORTED = 2, /* valid but beyond the library's limits (k > KMAX ...) */
     HDBMST_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
     HDBMST_ERR_NONFINITE = 4,   /* a NaN or infinity in the points or core distances   */
     HDBMST_ERR_NOCONVERGE = 5,  /* Boruvka made no progress in a round (cannot happen   */
