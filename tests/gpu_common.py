@@ -51,10 +51,20 @@ def oracle_knn_check(X, Y, k, g_idx, g_dist, rows=None, where=""):
 
 
 def golden_total(name, X):
-    """The stored oracle totals of a workload, if this machine drew the same points."""
-    if not os.path.exists(TOTALS):
-        return None
-    g = json.load(open(TOTALS)).get(name)
-    if g is None or g["digest"] != workloads.digest(X):
-        return None
+    """The stored oracle totals of a workload.  A machine that draws other
+    points than the ones the oracle ran on fails here: the stored values
+    would not apply, and a silent skip would hide the missing check."""
+    g = json.load(open(TOTALS))[name]
+    assert g["digest"] == workloads.digest(X), (
+        f"{name}: this machine drew other points than the stored oracle outputs were made from")
     return g
+
+
+def golden_outputs(name, X):
+    """The oracle's stored whole output of a 200 000-point workload
+    (``tests/golden/oracle_<name>.npz``, written by ``make_oracle_totals.py``
+    with the oracle alone); fails on a digest mismatch like golden_total."""
+    z = np.load(os.path.join(HERE, "golden", f"oracle_{name}.npz"))
+    assert str(z["digest"]) == workloads.digest(X), (
+        f"{name}: this machine drew other points than the stored oracle outputs were made from")
+    return {k: z[k] for k in z.files}
