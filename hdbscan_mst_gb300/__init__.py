@@ -107,6 +107,10 @@ def _load():
     L.hdbmst_last_mst_scan_pairs.restype = ctypes.c_int64
     L.hdbmst_hdbscan_labels.argtypes = [vp, vp, i64, i32, vp]
     L.hdbmst_hdbscan_labels.restype = i32
+    L.hdbmst_test_set_tc_hooks.argtypes = [ctypes.c_uint64, i32]
+    L.hdbmst_test_set_tc_hooks.restype = i32
+    L.hdbmst_test_set_mst_caps.argtypes = [i32, i32]
+    L.hdbmst_test_set_mst_caps.restype = None
     _lib = L
     return L
 
@@ -350,6 +354,21 @@ def set_scan_list_cap(cap: int) -> int:
     rescan (0: the default); an overflow sends the round (rows) to the
     one-sided (exact) scan, with the same tree.  Returns the previous cap."""
     return int(_load().hdbmst_set_scan_list_cap(int(cap)))
+
+
+def test_set_tc_hooks(wait_ns: int = 0, withhold_first_slab: bool = False) -> None:
+    """Failure-path test hook, current device: the tensor-core tiles' wait
+    limit (0: the default 1.5 s) and whether every tile leaves its first
+    column slab unloaded (its waits then run out: HDBMST_ERR_TIMEOUT).
+    ``test_set_tc_hooks()`` restores the defaults."""
+    _check(_load().hdbmst_test_set_tc_hooks(int(wait_ns), 1 if withhold_first_slab else 0),
+           "hdbmst_test_set_tc_hooks")
+
+
+def test_set_mst_caps(max_rounds: int = 0, max_jump_launches: int = 0) -> None:
+    """Failure-path test hook: cap mr_mst's Boruvka rounds and its merge's
+    pointer-jumping launches per round (0: no cap, the default)."""
+    _load().hdbmst_test_set_mst_caps(int(max_rounds), int(max_jump_launches))
 
 
 def last_mst_symmetric() -> list[int]:

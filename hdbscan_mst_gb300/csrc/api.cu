@@ -46,6 +46,10 @@ bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
 // and whether the symmetric form prunes block pairs.
 int g_scan_form = HDBMST_SCAN_AUTO;
 bool g_sym_prune = true;
+// Test caps of hdbmst_mr_mst (0: none): Boruvka rounds, and launches of the
+// merge's pointer jumping per round (hdbmst_test_set_mst_caps).
+int g_test_max_rounds = 0;
+int g_test_jump_launches = 0;
 // Cap on the recorded-pair lists of the symmetric scan and of the open-row
 // rescan (0: the whole scratch they use); a list that overflows sends its
 // round to the one-sided scan, or its rows to the FP32 exact scan.
@@ -157,6 +161,7 @@ struct DevStatus {
     unsigned sym_umax;               // symmetric scan: the largest component bound
     int sym_pairs;                   // symmetric scan: pairs recorded (may exceed the list)
     int sym_ncomp;                   // symmetric scan: components with points in P
+    int jump_live[kJumpMaxLaunches]; // merge: round stamps of the pointer-jumping launches
 };
 
 // A ranking error coefficient as the float32 the proofs use, rounded up.
@@ -405,26 +410,29 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         if (!p.alias) LAUNCH(K_PACK, s, launch_absmax(Y, ldy, p.m, p.d, &b.st->amax_bits, s));
     }
     // the spatial order: points go to their sorted positions, read in caller
-    // order; the feature-major copy only the FP32 tile reads is left out
+    // order.  The feature-major copy only the FP32 tile reads is written for
+    // that tile alone; with the TF32 form its buffer holds the operands' high
+    // parts instead (point-major, same size)
     const int *invX = spatial ? b.order.invX : nullptr, *invY = spatial ? b.order.invY : nullptr;
-    float *Xf = spatial ? nullptr : b.Xf, *Yf = spatial ? nullptr : b.Yf;
+    float *Xf = tensor ? nullptr : b.Xf, *Yf = tensor ? nullptr : b.Yf;
+    float *xhi = xlo ? b.Xf : nullptr, *yhi = ylo ? b.Yf : nullptr;
     if (p.alias) {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, Xf,
                                       b.Xp, xlo, b.xnorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      nullptr, Xh16, Xl16, amax, &b.st->e0, invX));
+                                      nullptr, Xh16, Xl16, amax, &b.st->e0, invX, xhi));
     } else {
         LAUNCH(K_PACK, s, launch_pack(X, ldx, p.n, p.d, static_cast<int>(p.n_pad), p.dk, Xf,
                                       b.Xp, xlo, b.xnorm, &b.st->status, nullptr, s, nullptr, Xh16,
-                                      Xl16, amax, &b.st->e0, invX));
+                                      Xl16, amax, &b.st->e0, invX, xhi));
         LAUNCH(K_PACK, s, launch_pack(Y, ldy, p.m, p.d, static_cast<int>(p.m_pad), p.dk, Yf,
                                       b.Yp, ylo, b.ynorm, &b.st->status, &b.st->nbmax_bits, s,
-                                      nullptr, Yh16, Yl16, amax, &b.st->e0, invY));
+                                      nullptr, Yh16, Yl16, amax, &b.st->e0, invY, yhi));
     }
     TcOperands ops{};
     if (f16)
         ops = TcOperands{Xh16, Xl16, Yh16, Yl16};
     else
-        ops = TcOperands{b.Xp, b.Xlo, b.Yp, b.Ylo};
+        ops = TcOperands{b.Xf, b.Xlo, b.Yf, b.Ylo};
     const double tc_err = f16 ? tc::err_coef_f16(p.d, p.dk) : tc::err_coef(p.d, p.dk);
     // pruned search: the spatial order's pivots bound the column blocks (prune.cu)
     const bool prune = spatial && b.prune.list != nullptr;
@@ -611,7 +619,7 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
 }
 
 struct MstBufs {
-    float *Xf, *Xp, *Xlo, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
+    float *Xf, *Xp, *Xhi, *Xlo, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
     float *Xs_hi, *Xs_lo, *Xa_hi, *Xa_lo;  // point-major grouped columns / active rows
     int *act_comp, *act_idx, *comp, *parent, *root_of, *perm, *col_comp, *start, *act_start;
     int *counters;  // [4n + 8]: size, act_size, cursor, act_cursor, totals (zeroed per round)
@@ -639,6 +647,8 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     b.act_norm = c.take<float>(p.n_pad);
     b.Xs = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xlo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
+    // the TF32 form's high parts, where the tensor-core scan can run
+    b.Xhi = tc_scan_supported(p.dk) ? c.take<float>(static_cast<size_t>(p.dk) * p.n_pad) : nullptr;
     b.Xs_hi = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xs_lo = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
     b.Xa_hi = c.take<float>(static_cast<size_t>(p.dk) * p.n_pad);
@@ -879,7 +889,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
     // dk / 2 words per point each) in the same buffer
     const bool f16 = tensor && use_f16(p.dk);
     const int dkw = f16 ? p.dk / 2 : p.dk;  // 32-bit words per point of each part
-    const float *op_hi = f16 ? b.Xlo : b.Xp;
+    const float *op_hi = f16 ? b.Xlo : b.Xhi;
     const float *op_lo = f16 ? b.Xlo + p.n_pad * dkw : b.Xlo;
     CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
     if (f16) LAUNCH(K_PACK, s, launch_absmax(X, ldx, N, d, &b.st->amax_bits, s));
@@ -889,12 +899,14 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                                   f16 ? reinterpret_cast<uint32_t *>(b.Xlo) : nullptr,
                                   f16 ? reinterpret_cast<uint32_t *>(b.Xlo) + p.n_pad * dkw
                                       : nullptr,
-                                  &b.st->amax_bits, &b.st->e0));
+                                  &b.st->amax_bits, &b.st->e0, nullptr,
+                                  tensor && !f16 ? b.Xhi : nullptr));
     LAUNCH(K_CHECK_CORE, s, launch_check_core(core, N, &b.st->status, s));
     LAUNCH(K_MST_INIT, s, launch_mst_init(N, b.comp, b.cand, b.ck64, b.chi, b.ub, b.cache, s));
 
     int max_rounds = 2;
     while ((int64_t(1) << (max_rounds - 2)) < N) ++max_rounds;  // ceil(log2 n) + 2
+    if (g_test_max_rounds > 0) max_rounds = std::min(max_rounds, g_test_max_rounds);
     int edges = 0;
     DevStatus h{};
     g_round_active.clear();
@@ -1209,8 +1221,11 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
         LAUNCH(K_HOOK, s, launch_hook(N, b.comp, b.ck64, b.chi, b.parent, b.e_lo, b.e_hi,
                                       reinterpret_cast<float *>(b.e_w), &b.st->edge_count,
                                       &b.st->status, s));
-        LAUNCH(K_ROOTS, s, launch_roots(N, b.comp, b.parent, b.root_of, &b.st->status, s));
-        LAUNCH(K_RELABEL, s, launch_relabel(N, b.comp, b.root_of, b.cand, b.ck64, b.chi, b.ub, s));
+        LAUNCH(K_ROOTS, s, launch_roots(N, N - edges, b.comp, b.parent, b.root_of,
+                                        b.st->jump_live, round + 1, sm_count(), s,
+                                        g_test_jump_launches));
+        LAUNCH(K_RELABEL, s, launch_relabel(N, b.comp, b.root_of, b.parent, b.cand, b.ck64, b.chi,
+                                            b.ub, &b.st->status, s));
         rs = read_status(b.st, h, s);
         if (rs != HDBMST_OK) return rs;
         if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
@@ -1265,6 +1280,20 @@ int64_t hdbmst_set_scan_list_cap(int64_t cap) {
     const int64_t prev = g_list_cap;
     g_list_cap = cap > 0 ? cap : 0;
     return prev;
+}
+
+hdbmst_status hdbmst_test_set_tc_hooks(uint64_t wait_ns, int withhold_first_slab) {
+    const unsigned long long ns = wait_ns ? wait_ns : tc::kWaitNs;
+    const int w = withhold_first_slab ? 1 : 0;
+    cudaError_t e = tc_knn_test_hooks(ns, w);
+    if (e == cudaSuccess) e = tc_scan_test_hooks(ns, w);
+    if (e == cudaSuccess) e = tc_sym_test_hooks(ns, w);
+    return e == cudaSuccess ? HDBMST_OK : cuda_fail(e);
+}
+
+void hdbmst_test_set_mst_caps(int max_rounds, int max_jump_launches) {
+    g_test_max_rounds = std::max(0, max_rounds);
+    g_test_jump_launches = std::max(0, max_jump_launches);
 }
 
 int hdbmst_set_scan_pruning(int on) {

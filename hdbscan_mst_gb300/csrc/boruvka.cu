@@ -242,10 +242,15 @@ __global__ void gather_kernel(int na, int na_pad, int dk, const int *__restrict_
     }
 }
 
-// K7: per component, the least (w, lo, hi) over its points' candidates.  The
-// first pass also records, for the next round, the candidates that are exact
-// (proven, or scanned one-sided: act_flag); the others (skipped by the
-// bound, or only bounded by the symmetric scan) are not.
+// K7: per component, the least (w, lo, hi) over its points' candidates, in
+// two stages of 32-bit words: (w, lo) as one 64-bit key, then hi among the
+// candidates that hold the least (w, lo).  Each stage first reduces within
+// the warp over the lanes of the same component (__match_any_sync groups
+// them; __reduce_min_sync takes the least w, then the least lo at that w),
+// so one lane per component and warp updates global memory.  The first pass
+// also records, for the next round, the candidates that are exact (proven,
+// or scanned one-sided: act_flag); the others (skipped by the bound, or only
+// bounded by the symmetric scan) are not.
 __global__ void comp_min_lo_kernel(int n, const unsigned long long *__restrict__ cand,
                                    const int *__restrict__ comp,
                                    unsigned long long *__restrict__ ck64,
@@ -253,13 +258,18 @@ __global__ void comp_min_lo_kernel(int n, const unsigned long long *__restrict__
                                    const unsigned char *__restrict__ act_flag,
                                    unsigned long long *__restrict__ cache) {
     const int a = blockIdx.x * blockDim.x + threadIdx.x;
-    if (a >= n) return;
-    const unsigned long long k = cand[a];
-    if (cache) cache[a] = (proven[a] || (act_flag && act_flag[a])) ? k : kNoKey;
-    if (k == kNoKey) return;
-    const unsigned b = key_i(k);
-    const unsigned lo = min(static_cast<unsigned>(a), b);
-    atomicMin(&ck64[comp[a]], (k & 0xffffffff00000000ull) | lo);
+    const bool in = a < n;
+    const unsigned long long k = in ? cand[a] : kNoKey;
+    if (in && cache) cache[a] = (proven[a] || (act_flag && act_flag[a])) ? k : kNoKey;
+    const bool has = k != kNoKey;
+    const int c = has ? comp[a] : -1;  // lanes without a candidate form their own group
+    const unsigned wb = has ? static_cast<unsigned>(k >> 32) : 0xffffffffu;
+    const unsigned lo = has ? min(static_cast<unsigned>(a), key_i(k)) : 0xffffffffu;
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const unsigned wmin = __reduce_min_sync(peers, wb);
+    const unsigned lomin = __reduce_min_sync(peers, wb == wmin ? lo : 0xffffffffu);
+    if (has && (threadIdx.x & 31) == __ffs(peers) - 1)
+        atomicMin(&ck64[c], (static_cast<unsigned long long>(wmin) << 32) | lomin);
 }
 
 __global__ void comp_min_hi_kernel(int n, const unsigned long long *__restrict__ cand,
@@ -267,14 +277,21 @@ __global__ void comp_min_hi_kernel(int n, const unsigned long long *__restrict__
                                    const unsigned long long *__restrict__ ck64,
                                    unsigned *__restrict__ chi) {
     const int a = blockIdx.x * blockDim.x + threadIdx.x;
-    if (a >= n) return;
-    const unsigned long long k = cand[a];
-    if (k == kNoKey) return;
-    const unsigned b = key_i(k);
-    const unsigned lo = min(static_cast<unsigned>(a), b);
-    const unsigned hi = max(static_cast<unsigned>(a), b);
-    const int c = comp[a];
-    if (((k & 0xffffffff00000000ull) | lo) == ck64[c]) atomicMin(&chi[c], hi);
+    const unsigned long long k = a < n ? cand[a] : kNoKey;
+    int c = -1;
+    unsigned hi = 0xffffffffu;
+    if (k != kNoKey) {
+        const unsigned b = key_i(k);
+        const unsigned lo = min(static_cast<unsigned>(a), b);
+        const int ca = comp[a];
+        if (((k & 0xffffffff00000000ull) | lo) == ck64[ca]) {
+            c = ca;
+            hi = max(static_cast<unsigned>(a), b);
+        }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const unsigned himin = __reduce_min_sync(peers, hi);
+    if (c >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicMin(&chi[c], himin);
 }
 
 // K8: every component hooks onto the component at the other end of its
@@ -314,29 +331,66 @@ __global__ void hook_kernel(int n, const int *__restrict__ comp,
     }
 }
 
-// Root of every component: follow parent pointers (read only here), at most
-// n steps.
-__global__ void roots_kernel(int n, const int *__restrict__ comp, const int *__restrict__ parent,
-                             int *__restrict__ root_of, unsigned *__restrict__ status) {
+// Root of every component by pointer jumping, in a counter-bounded number of
+// launches (the merge of page "HDBSCAN", "The algorithm on the device", on
+// the device).  The hooks form a forest over the components; its depth is
+// below the number of components.  The first launch walks each component's
+// parent pointers for at most kJumpSteps steps; every further launch walks
+// at most kJumpSteps steps over the pointers the launches before it wrote,
+// each of which already skips kJumpSteps^j levels (or ends at a root), so
+// after launch j every pointer is kJumpSteps^(j+1) levels up or at its
+// root.  root_of[x] == x exactly for the roots.  Updates happen in place:
+// a pointer read while another thread rewrites it is still an ancestor, so
+// a fresher value only helps.  A launch returns at once when the launch
+// before it found every pointer at a root (live[j] holds the round stamp of
+// the last launch j that did not); relabel_kernel checks the result.
+constexpr int kJumpSteps = 16;
+
+__global__ void roots_init_kernel(int n, const int *__restrict__ comp,
+                                  const int *__restrict__ parent, int *__restrict__ root_of,
+                                  int *__restrict__ live, int stamp) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= n || comp[c] != c) return;
     int r = c;
-    for (int s = 0; s < n; ++s) {
+#pragma unroll 1
+    for (int s = 0; s < kJumpSteps; ++s) {
         const int p = parent[r];
         if (p == r) break;
         r = p;
     }
-    if (parent[r] != r) atomicOr(status, kStatusNoConverge);
     root_of[c] = r;
+    if (parent[r] != r) live[0] = stamp;
 }
 
+__global__ void roots_jump_kernel(int n, const int *__restrict__ comp, int *root_of, int *live,
+                                  int pass, int stamp) {
+    if (live[pass - 1] != stamp) return;  // every pointer already at its root
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n; c += gridDim.x * blockDim.x) {
+        if (comp[c] != c) continue;
+        int r = root_of[c];
+#pragma unroll 1
+        for (int s = 0; s < kJumpSteps; ++s) {
+            const int p = root_of[r];
+            if (p == r) break;
+            r = p;
+        }
+        root_of[c] = r;
+        if (root_of[r] != r) live[pass] = stamp;
+    }
+}
+
+// Every point takes its component's root; a root that is not one (the
+// bounded jumping did not reach it) is reported instead of used.
 __global__ void relabel_kernel(int n, int *__restrict__ comp, const int *__restrict__ root_of,
+                               const int *__restrict__ parent,
                                unsigned long long *__restrict__ cand,
                                unsigned long long *__restrict__ ck64, unsigned *__restrict__ chi,
-                               unsigned *__restrict__ ub) {
+                               unsigned *__restrict__ ub, unsigned *__restrict__ status) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    comp[i] = root_of[comp[i]];
+    const int r = root_of[comp[i]];
+    if (parent[r] != r) atomicOr(status, kStatusNoConverge);
+    comp[i] = r;
     cand[i] = kNoKey;
     ck64[i] = kNoKey;
     chi[i] = 0xffffffffu;
@@ -439,16 +493,36 @@ cudaError_t launch_hook(int n, const int *comp, const unsigned long long *ck64,
     return cudaGetLastError();
 }
 
-cudaError_t launch_roots(int n, const int *comp, const int *parent, int *root_of,
-                         unsigned *status, cudaStream_t s) {
-    roots_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, parent, root_of, status);
-    return cudaGetLastError();
+int roots_launches(int components) {
+    int launches = 1;
+    int64_t reach = kJumpSteps;
+    while (reach < components && launches < kJumpMaxLaunches) {
+        reach *= kJumpSteps;
+        ++launches;
+    }
+    return launches;
 }
 
-cudaError_t launch_relabel(int n, int *comp, const int *root_of, unsigned long long *cand,
-                           unsigned long long *ck64, unsigned *chi, unsigned *ub,
-                           cudaStream_t s) {
-    relabel_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, root_of, cand, ck64, chi, ub);
+cudaError_t launch_roots(int n, int components, const int *comp, const int *parent, int *root_of,
+                         int *live, int stamp, int sms, cudaStream_t s, int launch_cap) {
+    roots_init_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, parent, root_of, live, stamp);
+    cudaError_t e = cudaGetLastError();
+    int launches = roots_launches(components);
+    if (launch_cap > 0) launches = std::min(launches, launch_cap);
+    const int grid = std::max(1, std::min(blocks_for(n, 256), 4 * sms));
+    for (int j = 1; j < launches && e == cudaSuccess; ++j) {
+        roots_jump_kernel<<<grid, 256, 0, s>>>(n, comp, root_of, live, j, stamp);
+        count_extra_launches(1);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+cudaError_t launch_relabel(int n, int *comp, const int *root_of, const int *parent,
+                           unsigned long long *cand, unsigned long long *ck64, unsigned *chi,
+                           unsigned *ub, unsigned *status, cudaStream_t s) {
+    relabel_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, comp, root_of, parent, cand, ck64, chi,
+                                                      ub, status);
     return cudaGetLastError();
 }
 

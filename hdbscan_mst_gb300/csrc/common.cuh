@@ -72,6 +72,13 @@ __host__ __device__ inline double f16_abs_err(bool f16, int dk, unsigned amax_bi
     return (0x1p30 * sqrt(static_cast<double>(dk)) + 2.0 * dk) * h * h * 1.05;
 }
 
+// x cut to its top 19 bits (sign, exponent, 10 mantissa bits): a TF32 value,
+// which a TF32 MMA reads exactly whether it truncates or rounds its inputs;
+// x - tf32_trunc(x) is exact in float32 and below 2^-10 |x|.
+__device__ __forceinline__ float tf32_trunc(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
 // hi, lo halves of x 2^e (scale = 2^e): hi = fp16(x 2^e),
 // lo = fp16(x 2^e - hi), each flushed to zero below 2^-14.  x 2^e - hi is
 // exact in float32 (hi is x 2^e rounded to fewer bits at no smaller exponent).

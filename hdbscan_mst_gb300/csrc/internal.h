@@ -11,7 +11,9 @@ namespace hdbmst {
 // ---------------------------------------------------------------- pack.cu
 // Copy a caller [d, n] set (leading dim ld) into the padded feature-major
 // buffer Xf [dk][n_pad] and, if not nullptr, the point-major buffer
-// Xp [n_pad][dk] and its tensor-core low parts Xlo = x - tf32(x); write
+// Xp [n_pad][dk] and, with Xlo, the tensor-core TF32 operand parts
+// Xhi = tf32_trunc(x) and Xlo = x - Xhi (both point-major [n_pad][dk], both
+// or neither); write
 // norm[i] = sum of x^2 (+inf for padding points); flag non-finite values;
 // raise *nbmax_bits to the largest norm's bits.  perm (nullable): position
 // i < n holds the caller's point perm[i]; or inv (nullable, instead of perm):
@@ -25,7 +27,7 @@ cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr,
                         uint32_t *Xh16 = nullptr, uint32_t *Xl16 = nullptr,
                         const unsigned *amax_bits = nullptr, float *e0_out = nullptr,
-                        const int *inv = nullptr);
+                        const int *inv = nullptr, float *Xhi = nullptr);
 // Raise *amax_bits to the largest magnitude of a caller [d, n] set.
 cudaError_t launch_absmax(const float *X, int64_t ld, int n, int d, unsigned *amax_bits,
                           cudaStream_t s);
@@ -162,6 +164,11 @@ bool tc_knn_supported(int dk);   // dk a multiple of 32, at most kTensorDkMax
 bool tc_scan_supported(int dk);  // dk = 32 or 64
 cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int64_t x_rows,
                           int64_t y_rows, int row_tiles, int splits, cudaStream_t s);
+// Test hooks of the tensor-core tiles' failure path, one per translation unit
+// (tc.cuh: set_test_hooks), on the current device.
+cudaError_t tc_knn_test_hooks(unsigned long long wait_ns, int withhold);
+cudaError_t tc_scan_test_hooks(unsigned long long wait_ns, int withhold);
+cudaError_t tc_sym_test_hooks(unsigned long long wait_ns, int withhold);
 // Padded feature count: whole 32-feature slabs up to 64 (the tensor-core tile's
 // operand granule), multiples of 16 beyond.
 // Padded feature count: whole 32-feature slabs up to kTensorDkMax (the
@@ -429,11 +436,20 @@ cudaError_t launch_comp_min(int n, const unsigned long long *cand, const int *co
 cudaError_t launch_hook(int n, const int *comp, const unsigned long long *ck64,
                         const unsigned *chi, int *parent, int *e_lo, int *e_hi, float *e_w,
                         int *edge_count, unsigned *status, cudaStream_t s);
-cudaError_t launch_roots(int n, const int *comp, const int *parent, int *root_of,
-                         unsigned *status, cudaStream_t s);
-cudaError_t launch_relabel(int n, int *comp, const int *root_of, unsigned long long *cand,
-                           unsigned long long *ck64, unsigned *chi, unsigned *ub,
-                           cudaStream_t s);
+// Roots of the hook forest by pointer jumping: a first launch and up to
+// kJumpMaxLaunches - 1 more, as many as `components` (an upper bound on the
+// forest's size) needs (roots_launches); live[kJumpMaxLaunches] holds round
+// stamps (any value but `stamp` on entry), so no reset is needed per round.
+// relabel sets kStatusNoConverge if a component's pointer did not reach its
+// root.
+constexpr int kJumpMaxLaunches = 8;  // 16^8 > the largest point count
+int roots_launches(int components);
+// launch_cap > 0 caps the launches (a test of the bound's detection)
+cudaError_t launch_roots(int n, int components, const int *comp, const int *parent, int *root_of,
+                         int *live, int stamp, int sms, cudaStream_t s, int launch_cap = 0);
+cudaError_t launch_relabel(int n, int *comp, const int *root_of, const int *parent,
+                           unsigned long long *cand, unsigned long long *ck64, unsigned *chi,
+                           unsigned *ub, unsigned *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- sort.cu
 // Sort N edges by (w, lo, hi) ascending and write (lo, hi) pairs and weights.

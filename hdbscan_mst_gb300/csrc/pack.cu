@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                                                    uint2 *__restrict__ Xl16,
                                                    const unsigned *__restrict__ amax_bits,
                                                    float *__restrict__ e0_out,
-                                                   const int *__restrict__ inv) {
+                                                   const int *__restrict__ inv,
+                                                   float *__restrict__ Xhi) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool inside = i < n_pad;
     const bool valid = i < n;
@@ -61,14 +62,18 @@ __global__ void __launch_bounds__(256) pack_kernel(const float *__restrict__ X, 
                 *reinterpret_cast<float4 *>(Xp + static_cast<int64_t>(dst) * dk + f) =
                     make_float4(v[0], v[1], v[2], v[3]);
             if (Xlo) {
-                // x - tf32(x), where tf32() keeps the top 19 bits (the tensor-core
-                // tile's second operand part)
-                float l[4];
+                // the tensor-core tile's two operand parts: hi = x cut to its top
+                // 19 bits (a TF32 value, exact whatever rounding the MMA applies
+                // to its inputs) and lo = x - hi (exact in float32)
+                float hh[4], l[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    l[q] = __fsub_rn(v[q], __uint_as_float(__float_as_uint(v[q]) & 0xFFFFE000u));
-                *reinterpret_cast<float4 *>(Xlo + static_cast<int64_t>(dst) * dk + f) =
-                    make_float4(l[0], l[1], l[2], l[3]);
+                for (int q = 0; q < 4; ++q) {
+                    hh[q] = tf32_trunc(v[q]);
+                    l[q] = __fsub_rn(v[q], hh[q]);
+                }
+                const int64_t e = static_cast<int64_t>(dst) * dk + f;
+                *reinterpret_cast<float4 *>(Xhi + e) = make_float4(hh[0], hh[1], hh[2], hh[3]);
+                *reinterpret_cast<float4 *>(Xlo + e) = make_float4(l[0], l[1], l[2], l[3]);
             }
             if (Xh16) {
                 // four halves = two 32-bit words, lower feature in the low half
@@ -111,7 +116,8 @@ __global__ void __launch_bounds__(256) pack_tile_kernel(const float *__restrict_
                                                         uint2 *__restrict__ Xl16,
                                                         const unsigned *__restrict__ amax_bits,
                                                         float *__restrict__ e0_out,
-                                                        const int *__restrict__ inv) {
+                                                        const int *__restrict__ inv,
+                                                        float *__restrict__ Xhi) {
     __shared__ float xs[kPackF][kPackPts + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i0 = blockIdx.x * kPackPts;
@@ -150,11 +156,12 @@ __global__ void __launch_bounds__(256) pack_tile_kernel(const float *__restrict_
             const int64_t e = static_cast<int64_t>(dst) * dk + f0 + 4 * c;
             if (Xp) *reinterpret_cast<float4 *>(Xp + e) = make_float4(v0, v1, v2, v3);
             if (Xlo) {
-                const float l0 = __fsub_rn(v0, __uint_as_float(__float_as_uint(v0) & 0xFFFFE000u));
-                const float l1 = __fsub_rn(v1, __uint_as_float(__float_as_uint(v1) & 0xFFFFE000u));
-                const float l2 = __fsub_rn(v2, __uint_as_float(__float_as_uint(v2) & 0xFFFFE000u));
-                const float l3 = __fsub_rn(v3, __uint_as_float(__float_as_uint(v3) & 0xFFFFE000u));
-                *reinterpret_cast<float4 *>(Xlo + e) = make_float4(l0, l1, l2, l3);
+                const float h0 = tf32_trunc(v0), h1 = tf32_trunc(v1), h2 = tf32_trunc(v2),
+                            h3 = tf32_trunc(v3);
+                *reinterpret_cast<float4 *>(Xhi + e) = make_float4(h0, h1, h2, h3);
+                *reinterpret_cast<float4 *>(Xlo + e) =
+                    make_float4(__fsub_rn(v0, h0), __fsub_rn(v1, h1), __fsub_rn(v2, h2),
+                                __fsub_rn(v3, h3));
             }
             if (Xh16) {
                 unsigned short h0, h1, h2, h3, lo0, lo1, lo2, lo3;
@@ -213,18 +220,20 @@ cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm, uint32_t *Xh16,
                         uint32_t *Xl16, const unsigned *amax_bits, float *e0_out,
-                        const int *inv) {
+                        const int *inv, float *Xhi) {
+    if ((Xlo == nullptr) != (Xhi == nullptr)) return cudaErrorInvalidValue;
     if (!perm && dk % 32 == 0) {
         pack_tile_kernel<<<(n_pad + kPackPts - 1) / kPackPts, 256, 0, s>>>(
             X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status, nbmax_bits,
             reinterpret_cast<uint2 *>(Xh16), reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out,
-            inv);
+            inv, Xhi);
         return cudaGetLastError();
     }
     const int blocks = static_cast<int>((n_pad + 255) / 256);
     pack_kernel<<<blocks, 256, 0, s>>>(X, ld, n, d, n_pad, dk, Xf, Xp, Xlo, norm, status,
                                        nbmax_bits, perm, reinterpret_cast<uint2 *>(Xh16),
-                                       reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out, inv);
+                                       reinterpret_cast<uint2 *>(Xl16), amax_bits, e0_out, inv,
+                                       Xhi);
     return cudaGetLastError();
 }
 

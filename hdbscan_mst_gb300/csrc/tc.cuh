@@ -10,10 +10,11 @@
 // by 32 bytes.
 //
 // The dot products use three TF32 passes, x.y ~ hi(x).hi(y) + hi(x).lo(y) +
-// lo(x).hi(y) with lo(x) = x - tf32(x).  The tensor core reads the raw float32
-// value as hi(x): it keeps the top 19 bits (measured on GB300: a raw product
-// matches the truncated-input reference to 2e-7 and differs from the rounded
-// one by 7e-4), so lo(x) is formed against truncation.
+// lo(x).hi(y).  The pack kernel writes hi(x) = x cut to its top 19 bits (a
+// value TF32 represents exactly, so the MMA reads it without error whether it
+// truncates or rounds its inputs) and lo(x) = x - hi(x) (exact); the MMA's own
+// conversion of lo(x) to TF32 costs at most 2^-10 |lo(x)|, which the ranking
+// error bound covers.
 #pragma once
 
 #include <cstdint>
@@ -27,13 +28,27 @@ constexpr int kRows = 128;        // rows of a tile = TMEM lanes
 constexpr int kCols = 128;        // columns of a tile (MMA N)
 constexpr int kSlab = 32;         // features per swizzled slab
 constexpr int kSlabBytes = 128;   // bytes per row per slab
-// Every mbarrier wait gives up after kWaitNs of global time (read from
+// Every mbarrier wait gives up after kWaitNs of global time (g_wait_ns below) (read from
 // %globaltimer) or kWaitPolls polls, whichever comes first; between polls the
 // waiting thread sleeps (__nanosleep), so it leaves the issue slots to the
 // warps doing work.  The poll cap alone ends a wait even if the timer stood
 // still: every poll takes at least tens of cycles.
 constexpr uint64_t kWaitNs = 1500000000ull;  // 1.5 s
 constexpr uint32_t kWaitPolls = 1u << 26;
+
+// Test hooks of the failure path (off unless a test sets them through the C
+// ABI): the wait limit, and a switch that makes every CTA's producer leave its
+// first ring slab unloaded, so that the waits on it run out and the kernel
+// ends with the timeout status.  Each translation unit that includes this
+// header has its own copy; the library sets all of them together.
+static __device__ unsigned long long g_wait_ns = kWaitNs;
+static __device__ int g_withhold_first_slab = 0;
+
+static inline cudaError_t set_test_hooks(unsigned long long wait_ns, int withhold) {
+    cudaError_t e = cudaMemcpyToSymbol(g_wait_ns, &wait_ns, sizeof(wait_ns));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_withhold_first_slab, &withhold, sizeof(int));
+    return e;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -136,12 +151,13 @@ template <uint32_t kMaxSleepNs>
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
     if (mbar_test(mbar, parity)) return true;
     const uint64_t t0 = global_ns();
+    const uint64_t limit = *reinterpret_cast<volatile unsigned long long *>(&g_wait_ns);
     uint32_t sleep = 16;
     for (uint32_t it = 1; it < kWaitPolls; ++it) {
         __nanosleep(sleep);
         if (mbar_test(mbar, parity)) return true;
         sleep = min(2 * sleep, kMaxSleepNs);
-        if ((it & 15) == 0 && global_ns() - t0 > kWaitNs) return false;
+        if ((it & 15) == 0 && global_ns() - t0 > limit) return false;
     }
     return false;
 }
@@ -237,16 +253,6 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void *gme
                  "r"(src_bytes));
 }
 
-// lo(x) = x - tf32(x) for four values, where tf32() keeps the top 19 bits.
-__device__ __forceinline__ float4 tf32_lo(float4 x) {
-    float4 l;
-    l.x = __fsub_rn(x.x, __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u));
-    l.y = __fsub_rn(x.y, __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u));
-    l.z = __fsub_rn(x.z, __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u));
-    l.w = __fsub_rn(x.w, __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
-    return l;
-}
-
 // v[j] for a run-time j in 0 .. 31 by a tree of selects on the bits of j, so
 // that v stays in registers (an indexed load would move it to local memory).
 __device__ __forceinline__ float pick32(const float (&v)[32], int j) {
@@ -287,8 +293,10 @@ __device__ __forceinline__ uint32_t below_mask(const float (&v)[32], float thr) 
 }
 
 // Bound on |computed t - (|y|^2 - 2 x.y)| relative to |x|^2 + |y|^2 for the
-// three-pass TF32 dot: the dropped lo.lo term and the TF32 truncation of the
-// lo parts (3 x 2^-20), float32 accumulation over 3 dk products (3 dk 2^-23),
+// three-pass TF32 dot: the dropped lo.lo term and the MMA's TF32 conversion
+// of the lo parts, at most 2^-10 |lo| whether it truncates or rounds, with
+// |lo| < 2^-10 |x| (3 x 2^-20; the hi parts are TF32 values and read
+// exactly), float32 accumulation over 3 dk products (3 dk 2^-23),
 // and the norms' FMA chains plus the final rounding ((d + 4) 2^-24), with 5%
 // slack.
 __host__ __device__ inline double err_coef(int d, int dk) {

@@ -314,4 +314,8 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int
     return cudaErrorInvalidValue;
 }
 
+cudaError_t tc_knn_test_hooks(unsigned long long wait_ns, int withhold) {
+    return tc::set_test_hooks(wait_ns, withhold);
+}
+
 }  // namespace hdbmst

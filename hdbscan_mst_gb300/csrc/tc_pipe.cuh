@@ -225,9 +225,11 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
             for (int s = 0; s < slabs; ++s)
                 tma_load_2d(alo + s * kSlabTile, &M.a_lo, s * kSlab, a_row, &S.abar);
         }
+        const bool withhold = *reinterpret_cast<volatile int *>(&g_withhold_first_slab) != 0;
         for (int h = 0; 2 * h < seq.n; ++h) {
             const int col0 = seq.at(2 * h) * kTileCols;
             for (int s = 0; s < slabs; ++s) {
+                if (withhold && h == 0 && s == 0) continue;  // test hook: never arrives
                 const Slot<Sh::kSt> slot(h, s, slabs);
                 const int st = slot.st;
                 if (!mbar_wait<kSleepProducer>(&S.empty[st], slot.parity ^ 1) ||

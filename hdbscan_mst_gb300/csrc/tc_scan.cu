@@ -261,4 +261,8 @@ cudaError_t launch_tc_scan(const ScanArgs &a, const float *Xa_hi, const float *X
     return cudaGetLastError();
 }
 
+cudaError_t tc_scan_test_hooks(unsigned long long wait_ns, int withhold) {
+    return tc::set_test_hooks(wait_ns, withhold);
+}
+
 }  // namespace hdbmst

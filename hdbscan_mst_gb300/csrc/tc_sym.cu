@@ -664,4 +664,8 @@ cudaError_t launch_sym_pairs_exact(const int2 *pairs, int count, const int *idx,
     return cudaGetLastError();
 }
 
+cudaError_t tc_sym_test_hooks(unsigned long long wait_ns, int withhold) {
+    return tc::set_test_hooks(wait_ns, withhold);
+}
+
 }  // namespace hdbmst

@@ -144,7 +144,15 @@ hdbmst_status hdbmst_core_distances(const float *X, int64_t ldx, int64_t n, int 
  *   workspace: hdbmst_workspace_bytes(HDBMST_OP_MST, n, 0, d, knn_len).
  *
  * The host reads one small status block per Boruvka round (at most
- * ceil(log2 n) + 1 rounds), so this call synchronises the stream each round.
+ * ceil(log2 n) + 2 rounds), so this call synchronises the stream each round.
+ * The merge runs on the device: each component hooks onto the component at
+ * the other end of its cheapest edge, and the roots of the hook forest are
+ * found by pointer jumping in a bounded number of launches (16 steps each,
+ * as many launches as log16 of the component count needs).  On its first
+ * call from a host thread on a device, the call creates a non-blocking side
+ * stream and two events for that thread and device (work beside the caller's
+ * stream, joined back before the call returns); they are kept for reuse and
+ * released when the process exits.
  * Errors: ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE (points or
  * core), ERR_NOCONVERGE, ERR_CUDA.
  */
@@ -161,10 +169,13 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
  * hand the library a workspace: a host application that reserved all device
  * memory up front and gives its plugins no allocator, a latency-critical loop
  * where an allocation could synchronise the device, a process under a hard
- * memory quota.  hdbmst_knn_noalloc computes exactly what hdbmst_knn computes
- * (same kernels, same results bit for bit) but takes its scratch from one
- * fixed array of HDBMST_NOALLOC_SCRATCH_BYTES in the library's device image
- * instead of a caller workspace.  The caller still owns X, Y, out_idx and
+ * memory quota.  hdbmst_knn_noalloc returns exactly what hdbmst_knn returns
+ * (the exact k nearest under dist() in the same order, so the same bits) but
+ * takes its scratch from one fixed array of HDBMST_NOALLOC_SCRATCH_BYTES in
+ * the library's device image instead of a caller workspace.  To fit that
+ * array it searches every column block, without the block pruning hdbmst_knn
+ * applies to large sets (which skips only blocks that provably hold none of a
+ * row's neighbours), and in smaller row chunks.  The caller still owns X, Y, out_idx and
  * out_dist, with the meaning, layout and limits of hdbmst_knn.
  *
  *  - The array is allocated once per GPU when the library's device code is
@@ -292,6 +303,34 @@ int hdbmst_set_scan_pruning(int on);
  * the default).
  */
 int64_t hdbmst_set_scan_list_cap(int64_t cap);
+
+/*
+ * Test hooks of the failure paths (page "HDBSCAN", gpu/hdbscan, section "The
+ * hang": every loop on the device is bounded, and a bound must end in a
+ * reported error, not a hang).  They exist so that tests can drive the
+ * bounds; leave them off in production.  Both are process-wide and not
+ * thread-safe.
+ *
+ * hdbmst_test_set_tc_hooks: on the CURRENT device, sets how long a wait
+ *   inside a tensor-core distance tile may last before it gives up (wait_ns;
+ *   0 restores the default of 1.5 s), and, when withhold_first_slab is
+ *   non-zero, makes every such tile leave the first slab of its column
+ *   stream unloaded.  The tile's waits on that slab then run out: the kernel
+ *   winds down, frees its tensor memory and returns, and the call that
+ *   launched it returns HDBMST_ERR_TIMEOUT with its outputs invalid; the
+ *   device stays usable.  Call (0, 0) to restore.  Synchronous (a small copy
+ *   to device memory); returns HDBMST_OK or HDBMST_ERR_CUDA.
+ *
+ * hdbmst_test_set_mst_caps: caps hdbmst_mr_mst's Boruvka rounds (max_rounds)
+ *   and the pointer-jumping launches of each round's merge
+ *   (max_jump_launches); 0 means no cap (the default bounds: ceil(log2 n) + 2
+ *   rounds, and as many launches of 16-step jumps as the number of
+ *   components needs).  A call that runs out of rounds before the tree is
+ *   complete, or whose merge leaves a component pointer short of its root,
+ *   returns HDBMST_ERR_NOCONVERGE.
+ */
+hdbmst_status hdbmst_test_set_tc_hooks(uint64_t wait_ns, int withhold_first_slab);
+void hdbmst_test_set_mst_caps(int max_rounds, int max_jump_launches);
 
 /* Human-readable text of a status code (a static string). */
 const char *hdbmst_status_string(hdbmst_status status);

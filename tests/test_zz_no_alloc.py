@@ -66,10 +66,10 @@ def test_noalloc_matches_knn_on_consecutive_calls():
     for X, Y, ref in ((a, a, ref_a), (b, yb, ref_b), (a, a, ref_a)):
         st, gi, gd = _noalloc(L, X, Y, 10)
         assert st == 0, L.hdbmst_status_string(st)
-        # same kernels on the same inputs: identical indices, distances within
-        # the 1e-5 relative tolerance of the parity tests (in fact equal)
+        # both entry points return the exact k nearest under the library's
+        # one distance function, with the same tie order: identical bits
         assert np.array_equal(gi, ref[0])
-        assert np.allclose(gd, ref[1], rtol=1e-5, atol=0)
+        assert np.array_equal(gd, ref[1])
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
