@@ -150,7 +150,3 @@ def test_mst_200k_d61_bench_config():
     tot = golden_total("hdbscan_200k_d61", X)["mst_total"]
     assert np.sum(ow) == tot
     print(f"200k x 61: {exchanged} near-tie exchanges against the oracle tree")
-    with pytest.raises(h.HdbmstError):
-        h.knn(dev(X), dev(X), 11)
-    with pytest.raises(h.HdbmstError):
-        h.knn(dev(X), dev(workloads.small(40, 4, seed=3)), 33)
