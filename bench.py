@@ -54,6 +54,12 @@ KNN_TEXT = "200,000 points x 192 fp32 features, 100 clusters, k=10 against every
 L2_FLUSH_BYTES = 256 << 20
 # the page's "Results" quote min_cluster_size = 20
 MIN_CLUSTER_SIZE = 20
+# the k-NN graph consumer: 200 initial clusters (the seed count of page
+# "Kilosort4 clustering and matching"), resolution 1, on the k-NN lists above
+ASSIGN_CLUSTERS = 200
+ASSIGN_TEXT = ("bipartite modularity assignment over the k-NN graph of the 200,000 x 192 "
+               "workload (k=10 into the 20,000-point subset), 200 seeded initial clusters, "
+               "gamma=1, rounds until no spike moves")
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -301,6 +307,40 @@ def run_gpu(args):
     H.profile_enable(False)
     k_total = max_over_ranks(dist, sum(kt), device)
 
+    # ---- the k-NN graph consumer on the GPU's own lists: bipartite
+    # modularity assignment of the spikes and the subset, 200 initial clusters
+    a_item = None
+    if not args.skip_knn:
+        gi_k, _ = H.knn(Xkd, Ykd, tk["k"])
+        mk = Yk.shape[1]
+        r0 = torch.from_numpy(np.random.default_rng(12).integers(0, ASSIGN_CLUSTERS, mk)
+                              .astype(np.int32)).to(device)
+        res = {}
+
+        def assign_call():
+            res["out"] = H.bipartite_assign(gi_k, mk, r0, ASSIGN_CLUSTERS, 1.0)
+
+        for _ in range(args.warmup):
+            flush_l2(flush)
+            assign_call()
+        torch.cuda.synchronize(device)
+        at = timed(assign_call)
+        a_rounds, a_moved = res["out"][2], res["out"][3]
+        H.profile_enable(True)
+        H.profile_read()
+        timed(assign_call)
+        aprof = H.profile_read()
+        H.profile_enable(False)
+        a_total = max_over_ranks(dist, sum(at), device)
+        a_item = {"metric": "bipartite assignment spikes/s (all rounds of one call)",
+                  "workload": ASSIGN_TEXT,
+                  "value": round(ws * Xk.shape[1] * args.steps / (a_total / 1e3), 1),
+                  "unit": "spikes/s", "ms_per_call": round(a_total / args.steps, 3),
+                  "rounds": a_rounds, "moved": a_moved,
+                  "kernel_ms_per_call": {
+                      k_: {"ms": round(v[0] / args.steps, 4), "launches": v[1] / args.steps}
+                      for k_, v in sorted(aprof.items(), key=lambda kv: -kv[1][0])}}
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -420,6 +460,7 @@ def run_gpu(args):
                 "unit": "rows/s", "ms_per_step": round(k_total / args.steps, 3),
                 "exact_rows": knn_exact_rows,
                 "roofline": knn_roof},
+        "assign": a_item,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)

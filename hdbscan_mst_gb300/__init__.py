@@ -30,7 +30,7 @@ __all__ = [
 ]
 
 KMAX = 32
-OP_KNN, OP_CORE, OP_MST = 0, 1, 2
+OP_KNN, OP_CORE, OP_MST, OP_ASSIGN = 0, 1, 2, 3
 
 STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
@@ -107,6 +107,11 @@ def _load():
     L.hdbmst_last_mst_scan_pairs.restype = ctypes.c_int64
     L.hdbmst_hdbscan_labels.argtypes = [vp, vp, i64, i32, vp]
     L.hdbmst_hdbscan_labels.restype = i32
+    L.hdbmst_bipartite_assign.argtypes = [vp, i64, i32, i64, i32, ctypes.c_double, vp, vp, vp,
+                                          i32, ctypes.POINTER(i32), vp, sz, vp]
+    L.hdbmst_bipartite_assign.restype = i32
+    L.hdbmst_last_assign_moved.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
+    L.hdbmst_last_assign_moved.restype = i32
     L.hdbmst_test_set_tc_hooks.argtypes = [ctypes.c_uint64, i32]
     L.hdbmst_test_set_tc_hooks.restype = i32
     L.hdbmst_test_set_mst_caps.argtypes = [i32, i32]
@@ -279,6 +284,58 @@ def hdbscan_mst(X, min_samples: int, *, shortcuts: bool = True):
     else:
         edges, w = mr_mst(X, core)
     return _out(core, host), _out(edges, host), _out(w, host)
+
+
+def _device_int32(a, name: str):
+    """Return (contiguous int32 CUDA tensor, was_host)."""
+    host = False
+    if isinstance(a, np.ndarray):
+        a = torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+        host = True
+    if not isinstance(a, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor or numpy array")
+    if a.device.type != "cuda":
+        host = True
+        a = a.to(dtype=torch.int32).pin_memory().to("cuda", non_blocking=True)
+    if a.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return a.contiguous(), host
+
+
+def bipartite_assign(nbr, m: int, right_init, n_clusters: int, gamma: float = 1.0,
+                     max_rounds: int = 200, *, workspace=None):
+    """Bipartite modularity assignment over the k-NN graph ``nbr [n, k]``
+    (indices into m subset points, as ``knn`` returns them against the
+    subset), from the subset's initial labels ``right_init [m]``.
+
+    Returns ``(left int32 [n], right int32 [m], rounds, moved)``: the spikes'
+    and the subset's labels, the left steps taken and the spikes each moved
+    (the last 0 when the labels converged)."""
+    L = _load()
+    nb_t, h1 = _device_int32(nbr, "nbr")
+    r0, h2 = _device_int32(right_init, "right_init")
+    if nb_t.dim() != 2:
+        raise ValueError("nbr must be [n, k]")
+    n, k = nb_t.shape
+    if r0.shape != (m,):
+        raise ValueError("right_init must have one label per subset point")
+    dev = r0.device
+    left = torch.empty(n, dtype=torch.int32, device=dev)
+    right = torch.empty(m, dtype=torch.int32, device=dev)
+    nb = L.hdbmst_workspace_bytes(OP_ASSIGN, n, m, n_clusters, k)
+    if nb == 0:
+        _check(2 if (k > KMAX or n_clusters > 65536 or n > (1 << 23)) else 1, "bipartite_assign")
+    ws = _workspace(nb, dev, workspace)
+    rounds = ctypes.c_int(0)
+    st = L.hdbmst_bipartite_assign(nb_t.data_ptr(), n, k, m, n_clusters, float(gamma),
+                                   r0.data_ptr(), left.data_ptr(), right.data_ptr(),
+                                   int(max_rounds), ctypes.byref(rounds), ws.data_ptr(), nb,
+                                   _stream())
+    _check(st, "hdbmst_bipartite_assign")
+    moved = (ctypes.c_int64 * 1024)()
+    r = L.hdbmst_last_assign_moved(moved, 1024)
+    host = h1 or h2
+    return _out(left, host), _out(right, host), int(rounds.value), [int(moved[i]) for i in range(r)]
 
 
 def hdbscan_labels(edges, w, min_cluster_size: int):

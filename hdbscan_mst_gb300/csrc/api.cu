@@ -75,7 +75,8 @@ const char *const kKernelNames[K_COUNT] = {
     "pack",   "check_core", "knn_tile", "knn_refine", "knn_exact", "mst_init",
     "nbr_candidate", "active", "gather", "boruvka_scan", "boruvka_refine", "boruvka_exact",
     "comp_min", "hook",
-    "roots",  "relabel",    "sort_edges", "knn_prune", "mst_prune"};
+    "roots",  "relabel",    "sort_edges", "knn_prune", "mst_prune", "assign_init",
+    "assign_left", "assign_right"};
 
 cudaEvent_t take_event() {
     if (!g_pool.empty()) {
@@ -764,6 +765,28 @@ KnnPlan make_knn_plan_fixed(int64_t n, int64_t m, int d, int k, bool alias, size
     return p;
 }
 
+// Bipartite assignment scratch: right degrees, the two sides' cluster
+// masses, the right step's [m][C] counts, one moved counter per round.
+struct AssignBufs {
+    int *deg_r;
+    unsigned long long *KR, *KL;
+    unsigned *counts;
+    int *moved;
+    DevStatus *st;
+};
+
+void carve_assign(Carver &c, int64_t m, int C, AssignBufs &b) {
+    b.deg_r = c.take<int>(static_cast<size_t>(m));
+    b.KR = c.take<unsigned long long>(static_cast<size_t>(C));
+    b.KL = c.take<unsigned long long>(static_cast<size_t>(C));
+    b.counts = c.take<unsigned>(static_cast<size_t>(m) * static_cast<size_t>(C));
+    b.moved = c.take<int>(HDBMST_ASSIGN_MAX_ROUNDS);
+    b.st = c.take<DevStatus>(1);
+}
+
+// spikes each round's left step moved, for the last assignment call
+std::vector<int64_t> g_assign_moved;
+
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
@@ -790,6 +813,15 @@ const char *hdbmst_status_string(hdbmst_status status) {
 }
 
 size_t hdbmst_workspace_bytes(int op, int64_t n, int64_t m, int d, int k) {
+    if (op == HDBMST_OP_ASSIGN) {
+        if (n < 0 || n > HDBMST_ASSIGN_NMAX || m < 1 || m > HDBMST_NMAX || d < 1 ||
+            d > HDBMST_ASSIGN_CMAX || k < 1 || k > HDBMST_KMAX)
+            return 0;
+        Carver c(nullptr);
+        AssignBufs b{};
+        carve_assign(c, m, d, b);
+        return c.off;
+    }
     if (d < 1 || d > HDBMST_DMAX || n < 0 || n > HDBMST_NMAX) return 0;
     Carver c(nullptr);
     if (op == HDBMST_OP_KNN) {
@@ -1266,6 +1298,67 @@ hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const f
     KnnBufs b{};
     carve_knn(c, p, b, false);
     return run_knn(p, b, X, ldx, Y, ldy, out_idx, out_dist, nullptr, 0, s);
+}
+
+hdbmst_status hdbmst_bipartite_assign(const int32_t *nbr, int64_t n, int k, int64_t m,
+                                      int n_clusters, double gamma, const int32_t *right_init,
+                                      int32_t *out_left, int32_t *out_right, int max_rounds,
+                                      int *out_rounds, void *workspace, size_t workspace_bytes,
+                                      hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    g_assign_moved.clear();
+    if (n < 0 || m < 1 || k < 1 || n_clusters < 1 || max_rounds < 1 || !(gamma >= 0.0) ||
+        !std::isfinite(gamma))
+        return HDBMST_ERR_ARG;
+    if (k > HDBMST_KMAX || n > HDBMST_ASSIGN_NMAX || m > HDBMST_NMAX ||
+        n_clusters > HDBMST_ASSIGN_CMAX || max_rounds > HDBMST_ASSIGN_MAX_ROUNDS)
+        return HDBMST_ERR_UNSUPPORTED;
+    if (!right_init || !out_right || (n > 0 && (!nbr || !out_left))) return HDBMST_ERR_ARG;
+    const size_t need = hdbmst_workspace_bytes(HDBMST_OP_ASSIGN, n, m, n_clusters, k);
+    if (!ws_ok(workspace, workspace_bytes, need)) return HDBMST_ERR_WORKSPACE;
+    Carver c(workspace);
+    AssignBufs b{};
+    carve_assign(c, m, n_clusters, b);
+    const int N = static_cast<int>(n), M = static_cast<int>(m), C = n_clusters;
+    CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(DevStatus), s));
+    CUDA_OK(cudaMemsetAsync(b.deg_r, 0, sizeof(int) * static_cast<size_t>(M), s));
+    CUDA_OK(cudaMemsetAsync(b.moved, 0, sizeof(int) * HDBMST_ASSIGN_MAX_ROUNDS, s));
+    if (out_right != right_init)
+        CUDA_OK(cudaMemcpyAsync(out_right, right_init, sizeof(int32_t) * static_cast<size_t>(M),
+                                cudaMemcpyDeviceToDevice, s));
+    // indices and initial labels are checked before any kernel uses them
+    LAUNCH(K_ASSIGN_INIT, s, launch_assign_degree(nbr, N, k, M, b.deg_r, out_left, &b.st->status, s));
+    LAUNCH(K_ASSIGN_INIT, s, launch_assign_right_mass(out_right, M, C, b.deg_r, b.KR,
+                                                      &b.st->status, s));
+    DevStatus h{};
+    hdbmst_status rs = read_status(b.st, h, s);
+    if (rs != HDBMST_OK) return rs;
+    if (h.status & kStatusBadList) return HDBMST_ERR_ARG;
+    int rounds = 0;
+    for (int round = 0; round < max_rounds; ++round) {
+        if (round > 0)
+            LAUNCH(K_ASSIGN_LEFT, s, launch_assign_right_mass(out_right, M, C, b.deg_r, b.KR,
+                                                              &b.st->status, s));
+        LAUNCH(K_ASSIGN_LEFT, s, launch_assign_left(nbr, N, k, C, out_right, b.KR, gamma, out_left,
+                                                    b.KL, b.moved + round, s));
+        int moved = 0;
+        CUDA_OK(cudaMemcpyAsync(&moved, b.moved + round, sizeof(int), cudaMemcpyDeviceToHost, s));
+        CUDA_OK(cudaStreamSynchronize(s));
+        ++rounds;
+        g_assign_moved.push_back(moved);
+        if (moved == 0) break;
+        LAUNCH(K_ASSIGN_RIGHT, s, launch_assign_right(nbr, N, k, M, C, out_left, b.deg_r, b.KL,
+                                                      gamma, b.counts, out_right, s));
+    }
+    if (out_rounds) *out_rounds = rounds;
+    return HDBMST_OK;
+}
+
+int hdbmst_last_assign_moved(int64_t *moved, int max_rounds) {
+    const int r = static_cast<int>(g_assign_moved.size());
+    for (int i = 0; i < std::min(r, max_rounds); ++i)
+        if (moved) moved[i] = g_assign_moved[i];
+    return r;
 }
 
 int hdbmst_set_engine(int engine) {

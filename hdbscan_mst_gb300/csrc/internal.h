@@ -461,6 +461,26 @@ cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, uns
                        cudaStream_t s, void (*before)(int, cudaStream_t),
                        void (*after)(int, cudaStream_t));
 
+// ---------------------------------------------------------------- assign.cu
+// Bipartite modularity assignment over a k-NN graph (nbr [n, k] int32 indices
+// into the m subset points; labels int32 in [0, C)).  degree: right degrees
+// (deg_r zeroed by the caller), index checks (kStatusBadList), spikes set to
+// -1.  right_mass: K_c of the subset points (zeroes KR first; label checks).
+// left: the left step (zeroes KL first, then adds the left masses); *moved
+// (zeroed by the caller) counts the spikes that moved.  right: the right step
+// (zeroes counts [m][C] first).
+cudaError_t launch_assign_degree(const int32_t *nbr, int n, int k, int m, int *deg_r,
+                                 int32_t *left, unsigned *status, cudaStream_t s);
+cudaError_t launch_assign_right_mass(const int32_t *right, int m, int C, const int *deg_r,
+                                     unsigned long long *KR, unsigned *status, cudaStream_t s);
+cudaError_t launch_assign_left(const int32_t *nbr, int n, int k, int C, const int32_t *right,
+                               const unsigned long long *KR, double gamma, int32_t *left,
+                               unsigned long long *KL, int *moved, cudaStream_t s);
+cudaError_t launch_assign_right(const int32_t *nbr, int n, int k, int m, int C,
+                                const int32_t *left, const int *deg_r,
+                                const unsigned long long *KL, double gamma, unsigned *counts,
+                                int32_t *right, cudaStream_t s);
+
 // Kernel ids for launch accounting and profiling.
 enum KernelId {
     K_PACK = 0,
@@ -482,6 +502,9 @@ enum KernelId {
     K_SORT,
     K_PRUNE,
     K_SYM_PRUNE,
+    K_ASSIGN_INIT,
+    K_ASSIGN_LEFT,
+    K_ASSIGN_RIGHT,
     K_COUNT
 };
 

@@ -62,7 +62,12 @@ typedef enum {
 /* Largest number of points in a set (indices are int32). */
 #define HDBMST_NMAX 1073741823LL
 
-typedef enum { HDBMST_OP_KNN = 0, HDBMST_OP_CORE = 1, HDBMST_OP_MST = 2 } hdbmst_op;
+typedef enum {
+    HDBMST_OP_KNN = 0,
+    HDBMST_OP_CORE = 1,
+    HDBMST_OP_MST = 2,
+    HDBMST_OP_ASSIGN = 3 /* hdbmst_bipartite_assign: d = n_clusters, k = list length */
+} hdbmst_op;
 
 /*
  * Workspace bytes that `op` needs for these sizes (m and k are ignored where
@@ -203,6 +208,59 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
 hdbmst_status hdbmst_knn_noalloc(const float *X, int64_t ldx, int64_t n, const float *Y,
                                  int64_t ldy, int64_t m, int d, int k, int32_t *out_idx,
                                  float *out_dist, hdbmst_stream stream);
+
+/*
+ * Bipartite modularity assignment over a k-NN graph (page "Kilosort4
+ * clustering and matching", gpu/clustering, section "Assignment in parallel:
+ * why the graph is bipartite").  Left nodes are the n spikes, right nodes the
+ * m subset points; spike t has one edge to each of the k subset points its
+ * list names (as hdbmst_knn writes it against the subset).  Given the right
+ * labels, every spike takes its best cluster at once; then, given the spikes'
+ * labels, every subset point; alternately.  A node v of degree k_v takes,
+ * among its neighbours' labels, the cluster c of largest
+ *     2m * n_vc - gamma * (k_v * K_c)
+ * with n_vc its edges to nodes labelled c, K_c the degree sum of the OTHER
+ * side's nodes labelled c and 2m = 2 n k (the score n_vc - gamma k_v K_c / 2m
+ * scaled by 2m), in float64 with the integer product exact, the product with
+ * gamma rounded once and the difference rounded once; equal scores go to the
+ * lowest label; a subset point no spike lists keeps its label.  A round is a
+ * left step and, unless it moved no spike, a right step (the first left step
+ * counts every spike as moved); the call stops after the round in which no
+ * spike moved, or after max_rounds left steps.
+ *
+ *   nbr        [n, k] int32, row-major: indices into the subset, in [0, m).
+ *   right_init [m] int32: initial labels of the subset points, in
+ *              [0, n_clusters) (the page draws them by k-means++ seeding,
+ *              which is the caller's); may alias out_right.
+ *   out_left   [n] int32, out_right [m] int32: final labels.
+ *   gamma      resolution, finite and >= 0; max_rounds 1 ..
+ *              HDBMST_ASSIGN_MAX_ROUNDS (the page caps at 200).
+ *   out_rounds HOST int or NULL: left steps taken; the moved spikes of each
+ *              are in hdbmst_last_assign_moved (the last is 0 when the labels
+ *              converged).
+ *   workspace: hdbmst_workspace_bytes(HDBMST_OP_ASSIGN, n, m, n_clusters, k)
+ *              bytes (about 4 m n_clusters for the right step's counts).
+ *
+ * Limits: n <= HDBMST_ASSIGN_NMAX (keeps every integer product of the score
+ * exact in float64), k <= HDBMST_KMAX, n_clusters <= HDBMST_ASSIGN_CMAX.
+ * Synchronises the stream once to check the indices and labels, then once
+ * per round to read the moved-spike counter.  Errors: ERR_ARG (sizes, NULL
+ * pointers, gamma, an index or initial label out of range), ERR_UNSUPPORTED,
+ * ERR_WORKSPACE, ERR_CUDA.
+ */
+#define HDBMST_ASSIGN_NMAX (1LL << 23)
+#define HDBMST_ASSIGN_CMAX 65536
+#define HDBMST_ASSIGN_MAX_ROUNDS 1024
+hdbmst_status hdbmst_bipartite_assign(const int32_t *nbr, int64_t n, int k, int64_t m,
+                                      int n_clusters, double gamma, const int32_t *right_init,
+                                      int32_t *out_left, int32_t *out_right, int max_rounds,
+                                      int *out_rounds, void *workspace, size_t workspace_bytes,
+                                      hdbmst_stream stream);
+
+/* Spikes each left step of the most recent hdbmst_bipartite_assign call moved
+ * (up to max_rounds entries; moved may be NULL); returns the number of rounds.
+ * Host-side, not thread-safe. */
+int hdbmst_last_assign_moved(int64_t *moved, int max_rounds);
 
 /*
  * HDBSCAN labels from the mutual-reachability minimum spanning tree, on the
