@@ -30,7 +30,7 @@ __all__ = [
 ]
 
 KMAX = 32
-OP_KNN, OP_CORE, OP_MST, OP_ASSIGN = 0, 1, 2, 3
+OP_KNN, OP_CORE, OP_MST, OP_ASSIGN, OP_MOMENT = 0, 1, 2, 3, 4
 
 STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "workspace missing or too small",
@@ -112,6 +112,8 @@ def _load():
     L.hdbmst_bipartite_assign.restype = i32
     L.hdbmst_last_assign_moved.argtypes = [ctypes.POINTER(ctypes.c_int64), i32]
     L.hdbmst_last_assign_moved.restype = i32
+    L.hdbmst_second_moment.argtypes = [vp, i64, i32, i64, i64, i32, i32, vp, vp, sz, vp]
+    L.hdbmst_second_moment.restype = i32
     L.hdbmst_test_set_tc_hooks.argtypes = [ctypes.c_uint64, i32]
     L.hdbmst_test_set_tc_hooks.restype = i32
     L.hdbmst_test_set_mst_caps.argtypes = [i32, i32]
@@ -336,6 +338,49 @@ def bipartite_assign(nbr, m: int, right_init, n_clusters: int, gamma: float = 1.
     r = L.hdbmst_last_assign_moved(moved, 1024)
     host = h1 or h2
     return _out(left, host), _out(right, host), int(rounds.value), [int(moved[i]) for i in range(r)]
+
+
+def second_moment(X, t0: int = 0, n: int | None = None, *, centred: bool = True, out=None,
+                  accumulate: bool = False, workspace=None):
+    """Covariance ``(V - mu)(V - mu)^T / n`` (``centred``) or second moment
+    ``V V^T / n`` of the window ``V = X[:, t0:t0 + n]`` of a channel-major
+    recording ``X [channels, samples]`` (float32).  Returns ``out``
+    ``[channels, channels]`` float32 (a new tensor, or the given one, written
+    or, with ``accumulate``, added to)."""
+    L = _load()
+    host = False
+    if isinstance(X, np.ndarray):
+        X = torch.from_numpy(np.ascontiguousarray(X, dtype=np.float32))
+        host = True
+    if X.dim() != 2:
+        raise ValueError("X must be channel-major [channels, samples]")
+    if X.device.type != "cuda":
+        host = True
+        X = X.to(dtype=torch.float32).contiguous().pin_memory().to("cuda", non_blocking=True)
+    if X.dtype != torch.float32:
+        raise TypeError("X must be float32")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    C, T = X.shape
+    n = T - t0 if n is None else n
+    ld = X.stride(0) if C > 1 else T
+    dev = X.device
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an out tensor")
+        out = torch.empty((C, C), dtype=torch.float32, device=dev)
+    elif out.device.type != "cuda" or out.dtype != torch.float32 or out.shape != (C, C) \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 [channels, channels] CUDA tensor")
+    nb = L.hdbmst_workspace_bytes(OP_MOMENT, n, 0, C, 0)
+    if nb == 0:
+        _check(1, "second_moment")
+    ws = _workspace(nb, dev, workspace)
+    st = L.hdbmst_second_moment(X.data_ptr(), ld, C, t0, n, 1 if centred else 0,
+                                1 if accumulate else 0, out.data_ptr(), ws.data_ptr(), nb,
+                                _stream())
+    _check(st, "hdbmst_second_moment")
+    return _out(out, host)
 
 
 def hdbscan_labels(edges, w, min_cluster_size: int):

@@ -76,7 +76,7 @@ const char *const kKernelNames[K_COUNT] = {
     "nbr_candidate", "active", "gather", "boruvka_scan", "boruvka_refine", "boruvka_exact",
     "comp_min", "hook",
     "roots",  "relabel",    "sort_edges", "knn_prune", "mst_prune", "assign_init",
-    "assign_left", "assign_right"};
+    "assign_left", "assign_right", "moment_prep", "moment_product", "moment_sum"};
 
 cudaEvent_t take_event() {
     if (!g_pool.empty()) {
@@ -784,6 +784,30 @@ void carve_assign(Carver &c, int64_t m, int C, AssignBufs &b) {
     b.st = c.take<DevStatus>(1);
 }
 
+// Second-moment scratch: channel means, bounds, the split operands and the
+// per-split partial products.
+struct MomentBufs {
+    double *sum;
+    float *mu_hi, *mu_lo;
+    int *scale_e;
+    MomentStatus *st;
+    uint32_t *hi, *lo;
+    float *partial;
+};
+
+void carve_moment(Carver &c, int64_t n, int C, MomentBufs &b) {
+    const int64_t c_pad = round_up(C, kBM);
+    const int64_t S = moment_splits(n);
+    b.sum = c.take<double>(static_cast<size_t>(c_pad));
+    b.mu_hi = c.take<float>(static_cast<size_t>(c_pad));
+    b.mu_lo = c.take<float>(static_cast<size_t>(c_pad));
+    b.scale_e = c.take<int>(static_cast<size_t>(c_pad));
+    b.st = c.take<MomentStatus>(1);
+    b.hi = c.take<uint32_t>(static_cast<size_t>(S * c_pad * (kMomentSplit / 2)));
+    b.lo = c.take<uint32_t>(static_cast<size_t>(S * c_pad * (kMomentSplit / 2)));
+    b.partial = c.take<float>(static_cast<size_t>(S * c_pad * c_pad));
+}
+
 // spikes each round's left step moved, for the last assignment call
 std::vector<int64_t> g_assign_moved;
 
@@ -813,6 +837,13 @@ const char *hdbmst_status_string(hdbmst_status status) {
 }
 
 size_t hdbmst_workspace_bytes(int op, int64_t n, int64_t m, int d, int k) {
+    if (op == HDBMST_OP_MOMENT) {
+        if (n < 1 || n > HDBMST_MOMENT_NMAX || d < 1 || d > HDBMST_DMAX) return 0;
+        Carver c(nullptr);
+        MomentBufs b{};
+        carve_moment(c, n, d, b);
+        return c.off;
+    }
     if (op == HDBMST_OP_ASSIGN) {
         if (n < 0 || n > HDBMST_ASSIGN_NMAX || m < 1 || m > HDBMST_NMAX || d < 1 ||
             d > HDBMST_ASSIGN_CMAX || k < 1 || k > HDBMST_KMAX)
@@ -1354,6 +1385,39 @@ hdbmst_status hdbmst_bipartite_assign(const int32_t *nbr, int64_t n, int k, int6
     return HDBMST_OK;
 }
 
+hdbmst_status hdbmst_second_moment(const float *X, int64_t ld, int channels, int64_t t0,
+                                   int64_t n, int centred, int accumulate, float *out,
+                                   void *workspace, size_t workspace_bytes,
+                                   hdbmst_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (channels < 1 || n < 1 || t0 < 0 || ld < t0 + n || !X || !out) return HDBMST_ERR_ARG;
+    if (channels > HDBMST_DMAX || n > HDBMST_MOMENT_NMAX) return HDBMST_ERR_UNSUPPORTED;
+    if (!moment_supported()) return HDBMST_ERR_UNSUPPORTED;
+    const size_t need = hdbmst_workspace_bytes(HDBMST_OP_MOMENT, n, 0, channels, 0);
+    if (!ws_ok(workspace, workspace_bytes, need)) return HDBMST_ERR_WORKSPACE;
+    Carver c(workspace);
+    MomentBufs b{};
+    carve_moment(c, n, channels, b);
+    const int c_pad = static_cast<int>(round_up(channels, kBM));
+    const int cen = centred ? 1 : 0;
+    CUDA_OK(cudaMemsetAsync(b.st, 0, sizeof(MomentStatus), s));
+    CUDA_OK(cudaMemsetAsync(b.scale_e, 0, sizeof(int) * static_cast<size_t>(c_pad), s));
+    LAUNCH(K_MOMENT_PREP, s, launch_moment_stats(X, ld, channels, t0, n, b.sum, b.mu_hi, b.mu_lo,
+                                                 b.scale_e, b.st, s));
+    LAUNCH(K_MOMENT_PREP, s, launch_moment_split(X, ld, channels, c_pad, t0, n, b.mu_hi, b.mu_lo,
+                                                 b.scale_e, b.hi, b.lo, s));
+    LAUNCH(K_MOMENT_PRODUCT, s, launch_moment_product(b.hi, b.lo, c_pad, n, b.scale_e, b.partial,
+                                                      &b.st->status, s));
+    LAUNCH(K_MOMENT_SUM, s, launch_moment_sum(b.partial, c_pad, channels, n, cen, b.sum, b.mu_hi,
+                                              b.mu_lo, accumulate ? 1 : 0, out, s));
+    MomentStatus h{};
+    CUDA_OK(cudaMemcpyAsync(&h, b.st, sizeof(MomentStatus), cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaStreamSynchronize(s));
+    if (h.status & kStatusNonFinite) return HDBMST_ERR_NONFINITE;
+    if (h.status & kStatusTimeout) return HDBMST_ERR_TIMEOUT;
+    return HDBMST_OK;
+}
+
 int hdbmst_last_assign_moved(int64_t *moved, int max_rounds) {
     const int r = static_cast<int>(g_assign_moved.size());
     for (int i = 0; i < std::min(r, max_rounds); ++i)
@@ -1381,6 +1445,7 @@ hdbmst_status hdbmst_test_set_tc_hooks(uint64_t wait_ns, int withhold_first_slab
     cudaError_t e = tc_knn_test_hooks(ns, w);
     if (e == cudaSuccess) e = tc_scan_test_hooks(ns, w);
     if (e == cudaSuccess) e = tc_sym_test_hooks(ns, w);
+    if (e == cudaSuccess) e = moment_test_hooks(ns, w);
     return e == cudaSuccess ? HDBMST_OK : cuda_fail(e);
 }
 

@@ -481,6 +481,34 @@ cudaError_t launch_assign_right(const int32_t *nbr, int n, int k, int m, int C,
                                 const unsigned long long *KL, double gamma, unsigned *counts,
                                 int32_t *right, cudaStream_t s);
 
+// ---------------------------------------------------------------- moments.cu
+// Split-product second moment / covariance of a channel-major window.
+constexpr int kMomentSplit = 4096;  // samples per split
+struct MomentStatus {
+    unsigned status;  // kStatus* bits
+};
+int moment_splits(int64_t n);
+bool moment_supported();  // the tensor maps the product kernel needs
+// stats: channel sums, means (mu_hi + mu_lo) and power-of-two scale
+// exponents (scale_e [c_pad], zeroed by the caller for the padding)
+cudaError_t launch_moment_stats(const float *X, int64_t ld, int C, int64_t t0, int64_t n,
+                                double *sum, float *mu_hi, float *mu_lo, int *scale_e,
+                                MomentStatus *st, cudaStream_t s);
+// split: the two-part FP16 operands hi, lo [S][c_pad][2048] words of the
+// centred window
+cudaError_t launch_moment_split(const float *X, int64_t ld, int C, int c_pad, int64_t t0,
+                                int64_t n, const float *mu_hi, const float *mu_lo,
+                                const int *scale_e, uint32_t *hi, uint32_t *lo, cudaStream_t s);
+// product: partial [S][c_pad][c_pad] (upper-triangle 128-tiles) on the tensor cores
+cudaError_t launch_moment_product(const uint32_t *hi, const uint32_t *lo, int c_pad, int64_t n,
+                                  const int *scale_e, float *partial, unsigned *status,
+                                  cudaStream_t s);
+// sum: out [C][C] = (or +=) sum over splits / n (+ the centring, uncentred)
+cudaError_t launch_moment_sum(const float *partial, int c_pad, int C, int64_t n, int centred,
+                              const double *sum, const float *mu_hi, const float *mu_lo,
+                              int accumulate, float *out, cudaStream_t s);
+cudaError_t moment_test_hooks(unsigned long long wait_ns, int withhold);
+
 // Kernel ids for launch accounting and profiling.
 enum KernelId {
     K_PACK = 0,
@@ -505,6 +533,9 @@ enum KernelId {
     K_ASSIGN_INIT,
     K_ASSIGN_LEFT,
     K_ASSIGN_RIGHT,
+    K_MOMENT_PREP,
+    K_MOMENT_PRODUCT,
+    K_MOMENT_SUM,
     K_COUNT
 };
 

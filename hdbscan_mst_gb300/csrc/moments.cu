@@ -1,0 +1,431 @@
+// The split-product second moment and covariance (page "Covariance",
+// gpu/covariance): C = (X - mu)(X - mu)^T / n and X X^T / n over a window of
+// n samples [t0, t0 + n) of a channel-major recording, in splits of 4 096
+// samples.
+//
+//  1. stats: one block per channel sums the window in a fixed order
+//     (compensated float32 per thread, then float64), giving the channel
+//     sum, the mean as a float32 pair (mu_hi + mu_lo), and the channel's
+//     scale exponent from its largest |x| and |mu|.
+//  2. split: copies the window into a split-major buffer [S][C_pad][4096]
+//     (the page's split_rows copy: the batch is the outermost stride, the
+//     window's column offset is applied here, so any start column and any
+//     odd length are fine, and the last split's tail and the padding
+//     channels are zero, which adds nothing to the products).  The centred
+//     value v = (x - mu_hi) - mu_lo, for the second moment too, is split into
+//     the two-part FP16 operands of the tensor cores: with a power of two 2^e
+//     per channel putting the channel's largest magnitude below 2^15,
+//     hi = fp16(v 2^e), lo = fp16(v 2^e - hi) (a quiet channel beside a loud
+//     one keeps its precision).  Centring keeps the split
+//     sums from growing along a split: measured on uncentred windows with a
+//     DC level, products of raw values came out 3e-5 off relative to
+//     sum |x_i x_j|, centred ones 2e-7.
+//  3. product: one CTA per (tile pair I <= J of 128 channels, split):
+//     tcgen05 kind::f16 MMAs over the split's 4 096 samples, both operands
+//     staged by TMA through a 3-stage ring, hi.hi' + hi.lo' + lo.hi' into
+//     128 x 128 float32 TMEM accumulators, 256 samples each, added up in
+//     registers, then written (times 2^-(e_i + e_j), exact) as the split's
+//     partial product.  No single sum adds more than 4 096 products, the page's
+//     reason for the splits.
+//  4. sum: every output entry adds its S partials in float64, in split
+//     order, adds back the centring for the second moment (in float64),
+//     divides by the true sample count n and writes or adds the float32
+//     result; entry (i, j) and (j, i) both read the partial of (min, max),
+//     so the result is exactly symmetric.
+#include <cuda.h>
+
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tc_pipe.cuh"
+
+namespace hdbmst {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kWords = kMomentSplit / 2;         // 32-bit words (two halves) per split row
+constexpr int kMomSlabs = kWords / kSlab;         // 64 slabs of 64 halves
+constexpr int kMomStages = 3;
+constexpr uint32_t kMomStage = 4 * kSlabTile;     // A hi, A lo, B hi, B lo
+constexpr size_t kMomSmem = kMomStages * kMomStage + 1024;
+constexpr int kMomThreads = 6 * 32;               // producer, MMA, four epilogue warps
+
+__global__ void __launch_bounds__(256) moment_stats_kernel(const float *__restrict__ X, int64_t ld,
+                                                           int64_t t0, int64_t n,
+                                                           double *__restrict__ sum,
+                                                           float *__restrict__ mu_hi,
+                                                           float *__restrict__ mu_lo,
+                                                           int *__restrict__ scale_e,
+                                                           MomentStatus *__restrict__ st) {
+    __shared__ double red[8];
+    __shared__ unsigned redm[8];
+    const int c = blockIdx.x, tid = threadIdx.x;
+    const float *row = X + static_cast<int64_t>(c) * ld + t0;
+    // compensated float32 sum per thread (Kahan), then float64 across threads
+    float part = 0.f, comp = 0.f, amax = 0.f;
+    for (int64_t t = tid; t < n; t += blockDim.x) {
+        const float x = row[t];
+        amax = fmaxf(amax, fabsf(x));
+        const float y = __fsub_rn(x, comp);
+        const float u = __fadd_rn(part, y);
+        comp = __fsub_rn(__fsub_rn(u, part), y);
+        part = u;
+    }
+    double acc = static_cast<double>(part) - static_cast<double>(comp);
+    unsigned m = isfinite(amax) ? __float_as_uint(amax) : 0x7f800000u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+    if ((tid & 31) == 0) {
+        red[tid >> 5] = acc;
+        redm[tid >> 5] = m;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double s = 0.0;
+        unsigned mm = 0u;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+            s += red[w];
+            mm = max(mm, redm[w]);
+        }
+        const double mu = s / static_cast<double>(n);
+        const float h = static_cast<float>(mu);
+        sum[c] = s;
+        mu_hi[c] = h;
+        mu_lo[c] = static_cast<float>(mu - static_cast<double>(h));
+        if (mm >= 0x7f800000u || !isfinite(mu)) atomicOr(&st->status, kStatusNonFinite);
+        // the channel's power-of-two scale: its centred values are at most
+        // max |x| + |mu| (rounded up)
+        const float b = __fadd_ru(__uint_as_float(mm), __fmul_ru(fabsf(h), 1.0000002f));
+        scale_e[c] = f16_scale_exp(__float_as_uint(b));
+    }
+}
+
+__global__ void __launch_bounds__(256) moment_split_kernel(
+    const float *__restrict__ X, int64_t ld, int C, int c_pad, int64_t t0, int64_t n, int S,
+    const float *__restrict__ mu_hi, const float *__restrict__ mu_lo,
+    const int *__restrict__ scale_e, uint32_t *__restrict__ hi, uint32_t *__restrict__ lo) {
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t words = static_cast<int64_t>(S) * c_pad * kWords;
+    if (w >= words) return;
+    const int64_t s = w / (static_cast<int64_t>(c_pad) * kWords);
+    const int r = static_cast<int>((w / kWords) % c_pad);
+    const int64_t t = s * kMomentSplit + 2 * (w % kWords);  // sample within the window
+    const float scale = r < C ? ldexpf(1.f, scale_e[r]) : 1.f;
+    unsigned short h[2], l[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float v = 0.f;
+        if (r < C && t + q < n)
+            v = __fsub_rn(__fsub_rn(X[static_cast<int64_t>(r) * ld + t0 + t + q], mu_hi[r]),
+                          mu_lo[r]);
+        f16_split(v, scale, h[q], l[q]);
+    }
+    hi[w] = h[0] | (static_cast<unsigned>(h[1]) << 16);
+    lo[w] = l[0] | (static_cast<unsigned>(l[1]) << 16);
+}
+
+constexpr int kChunkSlabs = 4;                    // 256 samples per TMEM accumulation
+constexpr int kChunks = kMomSlabs / kChunkSlabs;  // 16 per split
+constexpr int kEpiThreads = 4 * 32;
+
+struct MomSmem {
+    uint64_t full[kMomStages], empty[kMomStages], afull[2], aempty[2];
+    uint32_t tmem_base;
+    int abort;
+    int last_load[kMomStages];  // slab last loaded into each stage (-1: none)
+    int last_mma;               // slab whose MMAs were committed last (-1: none)
+};
+
+struct MomParams {
+    CUtensorMap hi, lo;  // [S * c_pad rows][kWords words], boxes of 128 rows x 32 words
+    float *partial;      // [S][c_pad][c_pad]
+    int c_pad, blocks;
+    const int *scale_e;  // [c_pad] per-channel exponents (0 for padding)
+    unsigned *status;
+};
+
+// One CTA per (tile pair, split).  The split's 64 slabs go through a
+// 3-stage TMA ring; the MMAs of every 4 slabs (256 samples) accumulate in one
+// of two TMEM accumulators, alternately, and the epilogue adds each chunk's
+// 128 x 128 result into float32 registers while the next chunk is
+// multiplied.  Short TMEM accumulations keep the rounding of the running
+// accumulator from building up along the split (measured: one accumulation
+// over all 4 096 samples left the same-sign sums of a variance 3e-5 low).
+__global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
+    const __grid_constant__ MomParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ MomSmem S;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // tile pair (I, J), I <= J, numbered row by row
+    int p = blockIdx.x, I = 0;
+    while (I < P.blocks && p >= P.blocks - I) {
+        p -= P.blocks - I;
+        ++I;
+    }
+    const int J = I + p;
+    const int s = blockIdx.y;
+    const bool diag = I == J;
+    const int rowA = s * P.c_pad + I * kRows, rowB = s * P.c_pad + J * kRows;
+    const uint32_t sb = smem_u32(pipe_base(smem_raw));
+    if (tid == 0) {
+        for (int i = 0; i < kMomStages; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], 1);
+            S.last_load[i] = -1;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&S.afull[i], 1);
+            mbar_init(&S.aempty[i], kEpiThreads);
+        }
+        S.abort = 0;
+        S.last_mma = -1;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&S.tmem_base, 256);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = S.tmem_base;
+    if (warp == 0 && lane == 0) {
+        // producer: the split's 64 slabs of rows I (and J), hi and lo parts
+        const uint32_t bytes = (diag ? 2u : 4u) * kSlabTile;
+        for (int k = 0; k < kMomSlabs; ++k) {
+            const int st = k % kMomStages;
+            const uint32_t par = static_cast<uint32_t>(k / kMomStages) & 1u;
+            if (!mbar_wait<kSleepProducer>(&S.empty[st], par ^ 1u) ||
+                *reinterpret_cast<volatile int *>(&S.abort)) {
+                S.abort = 1;
+                break;
+            }
+            const uint32_t a = sb + st * kMomStage;
+            mbar_expect_tx(&S.full[st], bytes);
+            tma_load_2d(a, &P.hi, k * kSlab, rowA, &S.full[st]);
+            tma_load_2d(a + kSlabTile, &P.lo, k * kSlab, rowA, &S.full[st]);
+            if (!diag) {
+                tma_load_2d(a + 2 * kSlabTile, &P.hi, k * kSlab, rowB, &S.full[st]);
+                tma_load_2d(a + 3 * kSlabTile, &P.lo, k * kSlab, rowB, &S.full[st]);
+            }
+            S.last_load[st] = k;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: per slab 4 K steps of 16 halves, three products each
+        const uint32_t idesc = instr_desc_f16(kRows, kRows);
+        bool ok = true;
+        for (int k = 0; k < kMomSlabs && ok; ++k) {
+            const int c = k / kChunkSlabs, acc = c & 1;
+            const uint32_t d = tmem + static_cast<uint32_t>(acc * kRows);
+            if (k % kChunkSlabs == 0 && c >= 2) {
+                // the epilogue has taken chunk c - 2 out of this accumulator
+                ok = mbar_wait<kSleepMma>(&S.aempty[acc], static_cast<uint32_t>(c / 2 - 1) & 1u);
+                if (!ok) break;
+                fence_after();
+            }
+            const int st = k % kMomStages;
+            const uint32_t par = static_cast<uint32_t>(k / kMomStages) & 1u;
+            ok = mbar_wait<kSleepMma>(&S.full[st], par) &&
+                 !*reinterpret_cast<volatile int *>(&S.abort);
+            if (!ok) break;
+            fence_after();
+            const uint32_t a = sb + st * kMomStage;
+            const uint64_t ah = smem_desc(a), al = smem_desc(a + kSlabTile);
+            const uint64_t bh = diag ? ah : smem_desc(a + 2 * kSlabTile);
+            const uint64_t bl = diag ? al : smem_desc(a + 3 * kSlabTile);
+#pragma unroll
+            for (int kk = 0; kk < kSlab / 8; ++kk) {
+                const uint32_t first = (k % kChunkSlabs == 0 && kk == 0) ? 0u : 1u;
+                mma_f16_ss(d, ah + 2 * kk, bh + 2 * kk, idesc, first);
+                mma_f16_ss(d, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
+                mma_f16_ss(d, al + 2 * kk, bh + 2 * kk, idesc, 1u);
+            }
+            mma_commit(&S.empty[st]);
+            S.last_mma = k;
+            if (k % kChunkSlabs == kChunkSlabs - 1) mma_commit(&S.afull[acc]);
+        }
+        if (!ok) S.abort = 1;
+    } else if (warp >= 2) {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. (its 32 rows of I)
+        const int q = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        float sum[kRows];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) sum[j] = 0.f;
+        bool ok = true;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+            const int acc = c & 1;
+            const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], static_cast<uint32_t>(c / 2) & 1u);
+            if (!w) S.abort = 1;
+            // a warp leaves together: tcgen05.ld is warp-collective
+            if (__any_sync(0xffffffffu, !w || *reinterpret_cast<volatile int *>(&S.abort))) {
+                ok = false;
+                break;
+            }
+            fence_after();
+#pragma unroll
+            for (int cc = 0; cc < kRows / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tmem + lane_base + static_cast<uint32_t>(acc * kRows + cc * 32), v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sum[cc * 32 + j] += v[j];
+            }
+            fence_before();
+            mbar_arrive(&S.aempty[acc]);
+        }
+        if (ok) {
+            // undo the two channels' scales: 2^-(e_row + e_col), exact
+            const int row = q * 32 + lane;
+            const int er = P.scale_e[I * kRows + row];
+            const int *ec = P.scale_e + J * kRows;
+            float *dst = P.partial +
+                         (static_cast<int64_t>(s) * P.c_pad + I * kRows + row) * P.c_pad + J * kRows;
+#pragma unroll
+            for (int j4 = 0; j4 < kRows / 4; ++j4)
+                *reinterpret_cast<float4 *>(dst + j4 * 4) = make_float4(
+                    ldexpf(sum[j4 * 4], -(er + ec[j4 * 4])), ldexpf(sum[j4 * 4 + 1], -(er + ec[j4 * 4 + 1])),
+                    ldexpf(sum[j4 * 4 + 2], -(er + ec[j4 * 4 + 2])),
+                    ldexpf(sum[j4 * 4 + 3], -(er + ec[j4 * 4 + 3])));
+        }
+    }
+    // teardown: after a give-up, drain the copies and products still in
+    // flight (bounded waits), then free TMEM
+    fence_before();
+    __syncthreads();
+    if (S.abort && tid == 0) {
+        atomicOr(P.status, kStatusTimeout);
+        for (int i = 0; i < kMomStages; ++i)
+            if (S.last_load[i] >= 0)
+                mbar_wait<kSleepProducer>(&S.full[i],
+                                          static_cast<uint32_t>(S.last_load[i] / kMomStages) & 1u);
+        if (S.last_mma >= 0)
+            mbar_wait<kSleepProducer>(&S.empty[S.last_mma % kMomStages],
+                                      static_cast<uint32_t>(S.last_mma / kMomStages) & 1u);
+    }
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_free(tmem, 256);
+}
+
+// Sum of the splits: a block takes one 32 x 32 tile of the output; it reads
+// the tile of the upper triangle that holds its entries, (min, max), row by
+// row through shared memory, adds the splits in float64 in order, and for the
+// second moment adds back what the centring took out: with v = x - mu' and
+// s = sum_t v = sum_t x - n mu', sum_t x_i x_j = sum_t v_i v_j + mu'_i s_j +
+// mu'_j s_i + n mu'_i mu'_j (exact algebra for any offset mu').  Then it
+// divides by n and writes (or adds) the float32 result.
+__global__ void __launch_bounds__(256) moment_sum_kernel(const float *__restrict__ partial, int S,
+                                                         int c_pad, int C, int64_t n, int centred,
+                                                         const double *__restrict__ sum,
+                                                         const float *__restrict__ mu_hi,
+                                                         const float *__restrict__ mu_lo,
+                                                         int accumulate, float *__restrict__ out) {
+    __shared__ float tile[32][33];
+    const int bi = blockIdx.y, bj = blockIdx.x;  // output tile
+    const int ua = min(bi, bj), ub = max(bi, bj);  // the upper-triangle tile that holds it
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 per pass
+    double acc[4] = {0.0, 0.0, 0.0, 0.0};
+    for (int s = 0; s < S; ++s) {
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = ty + 8 * k;
+            tile[r][tx] = partial[(static_cast<int64_t>(s) * c_pad + ua * 32 + r) * c_pad + ub * 32 + tx];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = ty + 8 * k;  // output entry (bi*32 + r, bj*32 + tx)
+            const int i = bi * 32 + r, j = bj * 32 + tx;
+            // entry (min(i, j), max(i, j)) of the upper tile (ua, ub)
+            const int a = min(i, j) - ua * 32, b = max(i, j) - ub * 32;
+            acc[k] += static_cast<double>(tile[a][b]);
+        }
+    }
+    const double dn = static_cast<double>(n);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = bi * 32 + ty + 8 * k, j = bj * 32 + tx;
+        if (i < C && j < C) {
+            double v = acc[k];
+            if (!centred) {
+                const double mi = static_cast<double>(mu_hi[i]) + static_cast<double>(mu_lo[i]);
+                const double mj = static_cast<double>(mu_hi[j]) + static_cast<double>(mu_lo[j]);
+                const double si = sum[i] - dn * mi, sj = sum[j] - dn * mj;
+                // the same float64 operations for (i, j) and (j, i): symmetric
+                v += min(mi * sj, mj * si) + max(mi * sj, mj * si) + dn * (mi * mj);
+            }
+            const float f = static_cast<float>(v / dn);
+            float *o = out + static_cast<int64_t>(i) * C + j;
+            *o = accumulate ? *o + f : f;
+        }
+    }
+}
+
+}  // namespace
+
+bool moment_supported() { return tensor_maps_available(); }
+
+int moment_splits(int64_t n) { return static_cast<int>((n + kMomentSplit - 1) / kMomentSplit); }
+
+cudaError_t launch_moment_stats(const float *X, int64_t ld, int C, int64_t t0, int64_t n,
+                                double *sum, float *mu_hi, float *mu_lo, int *scale_e,
+                                MomentStatus *st, cudaStream_t s) {
+    moment_stats_kernel<<<C, 256, 0, s>>>(X, ld, t0, n, sum, mu_hi, mu_lo, scale_e, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moment_split(const float *X, int64_t ld, int C, int c_pad, int64_t t0,
+                                int64_t n, const float *mu_hi, const float *mu_lo,
+                                const int *scale_e, uint32_t *hi, uint32_t *lo, cudaStream_t s) {
+    const int S = moment_splits(n);
+    const int64_t words = static_cast<int64_t>(S) * c_pad * kWords;
+    moment_split_kernel<<<static_cast<int>((words + 255) / 256), 256, 0, s>>>(
+        X, ld, C, c_pad, t0, n, S, mu_hi, mu_lo, scale_e, hi, lo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moment_product(const uint32_t *hi, const uint32_t *lo, int c_pad, int64_t n,
+                                  const int *scale_e, float *partial, unsigned *status,
+                                  cudaStream_t s) {
+    const int S = moment_splits(n);
+    MomParams P{};
+    const int64_t rows = static_cast<int64_t>(S) * c_pad;
+    if (!make_point_map(&P.hi, reinterpret_cast<const float *>(hi), rows, kWords) ||
+        !make_point_map(&P.lo, reinterpret_cast<const float *>(lo), rows, kWords))
+        return cudaErrorInvalidValue;
+    P.partial = partial;
+    P.c_pad = c_pad;
+    P.blocks = c_pad / kRows;
+    P.scale_e = scale_e;
+    P.status = status;
+    cudaError_t e = cudaFuncSetAttribute(moment_product_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMomSmem));
+    if (e != cudaSuccess) return e;
+    const int pairs = P.blocks * (P.blocks + 1) / 2;
+    moment_product_kernel<<<dim3(pairs, S), kMomThreads, kMomSmem, s>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moment_sum(const float *partial, int c_pad, int C, int64_t n, int centred,
+                              const double *sum, const float *mu_hi, const float *mu_lo,
+                              int accumulate, float *out, cudaStream_t s) {
+    const int tiles = (C + 31) / 32;
+    moment_sum_kernel<<<dim3(tiles, tiles), 256, 0, s>>>(partial, moment_splits(n), c_pad, C, n,
+                                                         centred, sum, mu_hi, mu_lo, accumulate,
+                                                         out);
+    return cudaGetLastError();
+}
+
+cudaError_t moment_test_hooks(unsigned long long wait_ns, int withhold) {
+    return tc::set_test_hooks(wait_ns, withhold);
+}
+
+}  // namespace hdbmst

@@ -91,6 +91,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// The FP16 MMA with both operands in shared memory (descriptors), F32
+// accumulate: the form of a plain product whose K is too long for TMEM.
+__device__ __forceinline__ void mma_f16_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
 // The same MMA with A read from TMEM: a_tmem addresses the K slice (lane 0,
 // the slice's first column); A row i sits in lane i, one 32-bit element per
 // column.  Only B then travels from shared memory, which halves the operand

@@ -66,7 +66,8 @@ typedef enum {
     HDBMST_OP_KNN = 0,
     HDBMST_OP_CORE = 1,
     HDBMST_OP_MST = 2,
-    HDBMST_OP_ASSIGN = 3 /* hdbmst_bipartite_assign: d = n_clusters, k = list length */
+    HDBMST_OP_ASSIGN = 3, /* hdbmst_bipartite_assign: d = n_clusters, k = list length */
+    HDBMST_OP_MOMENT = 4  /* hdbmst_second_moment: n = samples, d = channels */
 } hdbmst_op;
 
 /*
@@ -261,6 +262,43 @@ hdbmst_status hdbmst_bipartite_assign(const int32_t *nbr, int64_t n, int k, int6
  * (up to max_rounds entries; moved may be NULL); returns the number of rounds.
  * Host-side, not thread-safe. */
 int hdbmst_last_assign_moved(int64_t *moved, int max_rounds);
+
+/*
+ * Split-product second moment and covariance of a window of a channel-major
+ * recording (page "Covariance", gpu/covariance, sections "After: split
+ * products" and "The bug a test with an odd length found"):
+ *     centred != 0:  C = (V - mu)(V - mu)^T / n   (covariance)
+ *     centred == 0:  C = V V^T / n                (second moment)
+ * with V the window's samples and mu its channel means.  The window is
+ * copied, centred, into a split-major buffer of 4 096-sample splits (any
+ * start column and any length; the last split is zero-padded), each split's
+ * product is taken on the tensor cores (two-part FP16 operands with one
+ * power-of-two scale per channel, hi.hi + hi.lo + lo.hi, float32
+ * accumulation in runs of 256 samples added in registers, so no single sum
+ * adds more than 4 096 products), and the splits are added in float64 in
+ * order and divided by n.  The second moment is formed from the centred
+ * products plus the means' part, mu_i s_j + mu_j s_i + n mu_i mu_j with
+ * s = sum(x) - n mu, in float64: the same value, without the growth of the
+ * running sums that raw products with a common offset would have.
+ *
+ *   X   [channels, ld] float32, row-major (channel c's sample t at
+ *       X[c * ld + t]); the window is columns [t0, t0 + n), t0 + n <= ld.
+ *   out [channels, channels] float32, row-major, exactly symmetric; written,
+ *       or added to when accumulate != 0 (a running sum over windows).
+ *   workspace: hdbmst_workspace_bytes(HDBMST_OP_MOMENT, n, 0, channels, 0)
+ *       bytes (about 8 bytes per sample and padded channel, plus the split
+ *       partials, 4 * splits * round_up(channels, 128)^2 bytes).
+ *
+ * Limits: 1 <= channels <= HDBMST_DMAX, 1 <= n <= HDBMST_MOMENT_NMAX.
+ * Synchronises the stream once at the end to read its status.  Errors:
+ * ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_NONFINITE (a NaN or infinity
+ * in the window), ERR_TIMEOUT, ERR_CUDA.
+ */
+#define HDBMST_MOMENT_NMAX (1LL << 30)
+hdbmst_status hdbmst_second_moment(const float *X, int64_t ld, int channels, int64_t t0,
+                                   int64_t n, int centred, int accumulate, float *out,
+                                   void *workspace, size_t workspace_bytes,
+                                   hdbmst_stream stream);
 
 /*
  * HDBSCAN labels from the mutual-reachability minimum spanning tree, on the
