@@ -28,7 +28,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -54,6 +53,23 @@ KNN_TEXT = "200,000 points x 192 fp32 features, 100 clusters, k=10 against every
 L2_FLUSH_BYTES = 256 << 20
 # the page's "Results" quote min_cluster_size = 20
 MIN_CLUSTER_SIZE = 20
+# the split-product covariance: windows of 60 000 samples of a recording of
+# 384 (and 64) channels, starting at an odd column
+MOMENT_CHANNELS = (384, 64)
+MOMENT_SAMPLES = 60000
+MOMENT_OFFSET = 1001
+
+
+def moment_recording(channels: int) -> np.ndarray:
+    """A synthetic channel-major recording: per channel a DC level, a scale and
+    white noise, seeded; 1 001 + 60 000 + 999 samples."""
+    rng = np.random.default_rng(7 + channels)
+    T = MOMENT_OFFSET + MOMENT_SAMPLES + 999
+    scale = rng.uniform(5.0, 50.0, (channels, 1))
+    level = rng.uniform(-200.0, 200.0, (channels, 1))
+    return (rng.standard_normal((channels, T)) * scale + level).astype(np.float32)
+
+
 # the k-NN graph consumer: 200 initial clusters (the seed count of page
 # "Kilosort4 clustering and matching"), resolution 1, on the k-NN lists above
 ASSIGN_CLUSTERS = 200
@@ -341,6 +357,53 @@ def run_gpu(args):
                       k_: {"ms": round(v[0] / args.steps, 4), "launches": v[1] / args.steps}
                       for k_, v in sorted(aprof.items(), key=lambda kv: -kv[1][0])}}
 
+    # ---- the split-product covariance of a 384-channel window of 60 000
+    # samples (the configuration the covariance page reports), 64 channels too
+    m_items = None
+    if not args.skip_knn:
+        m_items = {}
+        for mc in MOMENT_CHANNELS:
+            Xm = torch.from_numpy(moment_recording(mc)).to(device)
+            t0m = MOMENT_OFFSET
+            res_m = {}
+
+            def moment_call():
+                res_m["out"] = H.second_moment(Xm, t0m, MOMENT_SAMPLES, centred=True,
+                                               out=res_m.get("out"))
+
+            for _ in range(args.warmup):
+                flush_l2(flush)
+                moment_call()
+            torch.cuda.synchronize(device)
+            mt = timed(moment_call)
+            H.profile_enable(True)
+            H.profile_read()
+            timed(moment_call)
+            mprof = H.profile_read()
+            H.profile_enable(False)
+            m_total = max_over_ranks(dist, sum(mt), device)
+            ms_call = m_total / args.steps
+            splits = -(-MOMENT_SAMPLES // 4096)
+            cpad = -(-mc // 128) * 128
+            blocks = cpad // 128
+            pairs = blocks * (blocks + 1) // 2
+            # algorithmic work: the upper triangle's products, 2 flop per
+            # (channel pair, sample); issued: 3 products over whole 128 x 128
+            # tiles and 4096-sample splits
+            alg_flop = 2.0 * mc * (mc + 1) / 2 * MOMENT_SAMPLES
+            issued = 3 * 2.0 * pairs * 128 * 128 * 4096 * splits
+            prod_ms = mprof.get("moment_product", (float("nan"), 1))[0] / args.steps
+            m_items[f"{mc}ch"] = {
+                "metric": "covariance windows/s", "channels": mc, "samples": MOMENT_SAMPLES,
+                "value": round(ws * args.steps / (m_total / 1e3), 1), "unit": "windows/s",
+                "ms_per_call": round(ms_call, 4),
+                "input_gb_per_s": round(4.0 * mc * MOMENT_SAMPLES / (ms_call / 1e3) / 1e9, 1),
+                "kernel_ms_per_call": {
+                    k_: {"ms": round(v[0] / args.steps, 4), "launches": v[1] / args.steps}
+                    for k_, v in sorted(mprof.items(), key=lambda kv: -kv[1][0])},
+                "product_tflops_algorithmic": round(alg_flop / (prod_ms / 1e3) / 1e12, 1),
+                "product_tflops_issued": round(issued / (prod_ms / 1e3) / 1e12, 1)}
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -461,6 +524,7 @@ def run_gpu(args):
                 "exact_rows": knn_exact_rows,
                 "roofline": knn_roof},
         "assign": a_item,
+        "covariance": m_items,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
@@ -520,12 +584,20 @@ def oracle_sample_rate(n_sample: int):
     return dt, n / full_seconds, oracle.threads()
 
 
-def cpu_baseline(args, n_sample: int = 40000):
+# One bounded sample of the workload for both CPU legs (the cpu_baseline key
+# of the GPU line and the reference arm): the first 20 000 clips, about 1.6 s
+# on 16 host cores (26 core-seconds), scaled to 200 000 by the oracle's
+# O(n^2) cost.
+ORACLE_SAMPLE = 20000
+
+
+def cpu_baseline(args, n_sample: int = ORACLE_SAMPLE):
     dt, rate, thr = oracle_sample_rate(n_sample)
     return {"value": round(rate, 2), "unit": "clips/s", "cores": thr, "kind": "oracle",
             "sample": (f"oracle core distances + dense Prim on the first {n_sample} of the "
                        f"200,000 clips ({dt:.1f} s), scaled to 200,000 by the oracle's "
                        f"O(n^2) cost"),
+            "extrapolated_from": n_sample, "extrapolation": "(200000 / n_sample)^2",
             "measured_sample_clips_per_s": round(n_sample / dt, 1)}
 
 
@@ -533,16 +605,13 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    # each step a bounded sample sized so the whole run stays within a few minutes
-    per_step_s = 150.0 / max(1, args.steps + args.warmup)
-    n_sample = int(max(4000, min(40000, 40000 * math.sqrt(per_step_s / 10.0))))
+    n_sample = ORACLE_SAMPLE
     for _ in range(args.warmup):
         oracle_sample_rate(n_sample)
-    secs, rates, thr = [], [], 0
+    secs, thr = [], 0
     for _ in range(args.steps):
-        dt, rate, thr = oracle_sample_rate(n_sample)
+        dt, _, thr = oracle_sample_rate(n_sample)
         secs.append(dt)
-        rates.append(rate)
     value = args.steps * 200000 / (sum(secs) * (200000 / n_sample) ** 2)
     sample = (f"oracle core distances + dense Prim on the first {n_sample} of the 200,000 clips "
               f"per step, scaled to 200,000 by the oracle's O(n^2) cost")
@@ -550,12 +619,14 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "clips/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(secs) / args.steps * (200000 / n_sample) ** 2, 1),
+        "measured_ms_per_step": round(1e3 * sum(secs) / args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT, "n": 200000, "d": 61, "min_samples": 10,
                    "sample_clips": n_sample},
         "cpu_baseline": {"value": round(value, 2), "unit": "clips/s", "cores": thr,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "extrapolated_from": n_sample,
+                         "extrapolation": "(200000 / n_sample)^2"},
         "e2e": {"value": round(value, 2), "unit": "clips/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
