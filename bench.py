@@ -92,20 +92,20 @@ TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
         # per step: the home pass (52.14 MB read, 3.14 MB written) and the
         # pruned second pass (73.70 MB read, 22.81 MB written)
-        "bytes": 52.14e6 + 3.14e6 + 73.70e6 + 22.81e6,
+        "bytes": 52.15e6 + 3.19e6 + 73.67e6 + 22.78e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "f095541b0996feab567e11aca504ddd29152116ad6720d03c2cd9fd0c15ce6d8",
+        "sha256": "590ca1f5bb9af07ee21ed79a89081958f803911ad3855f997143c327d4bcfa49",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.20 MB
+        # per step: the one-sided scans of rounds 1 and 2 (55.00 + 53.23 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.20 + 51.61 + 48.67 + 49.64 MB read); 0.01 MB
+        # pruned pass each (49.21 + 51.65 + 48.68 + 49.83 MB read); 0.01 MB
         # written in all
-        "bytes": (54.99 + 53.20 + 49.20 + 51.61 + 48.67 + 49.64 + 0.01) * 1e6,
+        "bytes": (55.00 + 53.23 + 49.21 + 51.65 + 48.68 + 49.83 + 0.01) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "7676b976d31da8182a3eeb8cf563ae0061288cca101d9a1470798d0f0d0ca4a3",
+        "sha256": "7340beb8c0110603e29515441d5e8236312fdf392997a5ae6af5ed674b4bb4dc",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0

@@ -805,7 +805,8 @@ void carve_moment(Carver &c, int64_t n, int C, MomentBufs &b) {
     b.st = c.take<MomentStatus>(1);
     b.hi = c.take<uint32_t>(static_cast<size_t>(S * c_pad * (kMomentSplit / 2)));
     b.lo = c.take<uint32_t>(static_cast<size_t>(S * c_pad * (kMomentSplit / 2)));
-    b.partial = c.take<float>(static_cast<size_t>(S * c_pad * c_pad));
+    const int64_t sub = moment_subsplits(static_cast<int>(c_pad), n);
+    b.partial = c.take<float>(static_cast<size_t>(S * sub * c_pad * c_pad));
 }
 
 // spikes each round's left step moved, for the last assignment call

@@ -488,6 +488,11 @@ struct MomentStatus {
     unsigned status;  // kStatus* bits
 };
 int moment_splits(int64_t n);
+// Sub-splits of each split the product takes (a power of two up to 16, so
+// that small problems still give about kMomentTargetCtas CTAs); the partial
+// products are [splits * sub][c_pad][c_pad].
+constexpr int kMomentTargetCtas = 128;
+int moment_subsplits(int c_pad, int64_t n);
 bool moment_supported();  // the tensor maps the product kernel needs
 // stats: channel sums, means (mu_hi + mu_lo) and power-of-two scale
 // exponents (scale_e [c_pad], zeroed by the caller for the padding)

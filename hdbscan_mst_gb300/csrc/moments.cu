@@ -4,7 +4,7 @@
 // samples.
 //
 //  1. stats: one block per channel sums the window in a fixed order
-//     (compensated float32 per thread, then float64), giving the channel
+//     (two compensated float32 sums per thread, then float64), giving the channel
 //     sum, the mean as a float32 pair (mu_hi + mu_lo), and the channel's
 //     scale exponent from its largest |x| and |mu|.
 //  2. split: copies the window into a split-major buffer [S][C_pad][4096]
@@ -20,14 +20,15 @@
 //     sums from growing along a split: measured on uncentred windows with a
 //     DC level, products of raw values came out 3e-5 off relative to
 //     sum |x_i x_j|, centred ones 2e-7.
-//  3. product: one CTA per (tile pair I <= J of 128 channels, split):
+//  3. product: one CTA per (tile pair I <= J of 128 channels, split), or per
+//     sub-split of 2048 .. 256 samples when that leaves the GPU idle:
 //     tcgen05 kind::f16 MMAs over the split's 4 096 samples, both operands
 //     staged by TMA through a 3-stage ring, hi.hi' + hi.lo' + lo.hi' into
 //     128 x 128 float32 TMEM accumulators, 256 samples each, added up in
 //     registers, then written (times 2^-(e_i + e_j), exact) as the split's
 //     partial product.  No single sum adds more than 4 096 products, the page's
 //     reason for the splits.
-//  4. sum: every output entry adds its S partials in float64, in split
+//  4. sum: every output entry (a thread each) adds its S partials in float64, in split
 //     order, adds back the centring for the second moment (in float64),
 //     divides by the true sample count n and writes or adds the float32
 //     result; entry (i, j) and (j, i) both read the partial of (min, max),
@@ -55,28 +56,41 @@ constexpr uint32_t kMomStage = 4 * kSlabTile;     // A hi, A lo, B hi, B lo
 constexpr size_t kMomSmem = kMomStages * kMomStage + 1024;
 constexpr int kMomThreads = 6 * 32;               // producer, MMA, four epilogue warps
 
-__global__ void __launch_bounds__(256) moment_stats_kernel(const float *__restrict__ X, int64_t ld,
-                                                           int64_t t0, int64_t n,
-                                                           double *__restrict__ sum,
-                                                           float *__restrict__ mu_hi,
-                                                           float *__restrict__ mu_lo,
-                                                           int *__restrict__ scale_e,
-                                                           MomentStatus *__restrict__ st) {
-    __shared__ double red[8];
-    __shared__ unsigned redm[8];
+constexpr int kStatsThreads = 1024;
+
+__device__ __forceinline__ void kahan_add(float &sum, float &comp, float x) {
+    const float y = __fsub_rn(x, comp);
+    const float u = __fadd_rn(sum, y);
+    comp = __fsub_rn(__fsub_rn(u, sum), y);
+    sum = u;
+}
+
+__global__ void __launch_bounds__(kStatsThreads) moment_stats_kernel(
+    const float *__restrict__ X, int64_t ld, int64_t t0, int64_t n, double *__restrict__ sum,
+    float *__restrict__ mu_hi, float *__restrict__ mu_lo, int *__restrict__ scale_e,
+    MomentStatus *__restrict__ st) {
+    __shared__ double red[kStatsThreads / 32];
+    __shared__ unsigned redm[kStatsThreads / 32];
     const int c = blockIdx.x, tid = threadIdx.x;
     const float *row = X + static_cast<int64_t>(c) * ld + t0;
-    // compensated float32 sum per thread (Kahan), then float64 across threads
-    float part = 0.f, comp = 0.f, amax = 0.f;
-    for (int64_t t = tid; t < n; t += blockDim.x) {
-        const float x = row[t];
-        amax = fmaxf(amax, fabsf(x));
-        const float y = __fsub_rn(x, comp);
-        const float u = __fadd_rn(part, y);
-        comp = __fsub_rn(__fsub_rn(u, part), y);
-        part = u;
+    // two compensated float32 sums per thread (samples t and t + stride,
+    // interleaved), then float64 across threads in a fixed order
+    float s0 = 0.f, c0 = 0.f, s1 = 0.f, c1 = 0.f, amax = 0.f;
+    const int64_t stride = 2 * static_cast<int64_t>(kStatsThreads);
+    int64_t t = tid;
+    for (; t + kStatsThreads < n; t += stride) {
+        const float x0 = row[t], x1 = row[t + kStatsThreads];
+        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+        kahan_add(s0, c0, x0);
+        kahan_add(s1, c1, x1);
     }
-    double acc = static_cast<double>(part) - static_cast<double>(comp);
+    if (t < n) {
+        const float x0 = row[t];
+        amax = fmaxf(amax, fabsf(x0));
+        kahan_add(s0, c0, x0);
+    }
+    double acc = (static_cast<double>(s0) - static_cast<double>(c0)) +
+                 (static_cast<double>(s1) - static_cast<double>(c1));
     unsigned m = isfinite(amax) ? __float_as_uint(amax) : 0x7f800000u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -89,15 +103,15 @@ __global__ void __launch_bounds__(256) moment_stats_kernel(const float *__restri
     }
     __syncthreads();
     if (tid == 0) {
-        double s = 0.0;
+        double sm = 0.0;
         unsigned mm = 0u;
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
-            s += red[w];
+        for (int w = 0; w < kStatsThreads / 32; ++w) {
+            sm += red[w];
             mm = max(mm, redm[w]);
         }
-        const double mu = s / static_cast<double>(n);
+        const double mu = sm / static_cast<double>(n);
         const float h = static_cast<float>(mu);
-        sum[c] = s;
+        sum[c] = sm;
         mu_hi[c] = h;
         mu_lo[c] = static_cast<float>(mu - static_cast<double>(h));
         if (mm >= 0x7f800000u || !isfinite(mu)) atomicOr(&st->status, kStatusNonFinite);
@@ -108,33 +122,36 @@ __global__ void __launch_bounds__(256) moment_stats_kernel(const float *__restri
     }
 }
 
+// grid: (kWords / 256 word blocks, c_pad channels, split blocks); a
+// thread makes one 32-bit word (two halves) of each split it visits
 __global__ void __launch_bounds__(256) moment_split_kernel(
     const float *__restrict__ X, int64_t ld, int C, int c_pad, int64_t t0, int64_t n, int S,
     const float *__restrict__ mu_hi, const float *__restrict__ mu_lo,
     const int *__restrict__ scale_e, uint32_t *__restrict__ hi, uint32_t *__restrict__ lo) {
-    const int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t words = static_cast<int64_t>(S) * c_pad * kWords;
-    if (w >= words) return;
-    const int64_t s = w / (static_cast<int64_t>(c_pad) * kWords);
-    const int r = static_cast<int>((w / kWords) % c_pad);
-    const int64_t t = s * kMomentSplit + 2 * (w % kWords);  // sample within the window
-    const float scale = r < C ? ldexpf(1.f, scale_e[r]) : 1.f;
-    unsigned short h[2], l[2];
+    const int wd = blockIdx.x * blockDim.x + threadIdx.x;  // word within the split row
+    const int r = blockIdx.y;
+    const bool ch = r < C;
+    const float scale = ch ? ldexpf(1.f, scale_e[r]) : 1.f;
+    const float mh = ch ? mu_hi[r] : 0.f, ml = ch ? mu_lo[r] : 0.f;
+    const float *row = X + static_cast<int64_t>(ch ? r : 0) * ld + t0;
+    for (int s = blockIdx.z; s < S; s += gridDim.z) {
+        const int64_t t = static_cast<int64_t>(s) * kMomentSplit + 2 * wd;  // sample in the window
+        unsigned short h[2], l[2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        float v = 0.f;
-        if (r < C && t + q < n)
-            v = __fsub_rn(__fsub_rn(X[static_cast<int64_t>(r) * ld + t0 + t + q], mu_hi[r]),
-                          mu_lo[r]);
-        f16_split(v, scale, h[q], l[q]);
+        for (int q = 0; q < 2; ++q) {
+            float v = 0.f;
+            if (ch && t + q < n) v = __fsub_rn(__fsub_rn(row[t + q], mh), ml);
+            f16_split(v, scale, h[q], l[q]);
+        }
+        const int64_t w = (static_cast<int64_t>(s) * c_pad + r) * kWords + wd;
+        hi[w] = h[0] | (static_cast<unsigned>(h[1]) << 16);
+        lo[w] = l[0] | (static_cast<unsigned>(l[1]) << 16);
     }
-    hi[w] = h[0] | (static_cast<unsigned>(h[1]) << 16);
-    lo[w] = l[0] | (static_cast<unsigned>(l[1]) << 16);
 }
 
 constexpr int kChunkSlabs = 4;                    // 256 samples per TMEM accumulation
-constexpr int kChunks = kMomSlabs / kChunkSlabs;  // 16 per split
 constexpr int kEpiThreads = 4 * 32;
+constexpr int kMaxSub = kMomSlabs / kChunkSlabs;  // sub-splits of a split: at most 16
 
 struct MomSmem {
     uint64_t full[kMomStages], empty[kMomStages], afull[2], aempty[2];
@@ -146,8 +163,9 @@ struct MomSmem {
 
 struct MomParams {
     CUtensorMap hi, lo;  // [S * c_pad rows][kWords words], boxes of 128 rows x 32 words
-    float *partial;      // [S][c_pad][c_pad]
+    float *partial;      // [S * sub][c_pad][c_pad]
     int c_pad, blocks;
+    int sub;             // CTAs per split, each over 64 / sub slabs
     const int *scale_e;  // [c_pad] per-channel exponents (0 for padding)
     unsigned *status;
 };
@@ -171,7 +189,8 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
         ++I;
     }
     const int J = I + p;
-    const int s = blockIdx.y;
+    const int s = blockIdx.y / P.sub, part = blockIdx.y % P.sub;
+    const int nslabs = kMomSlabs / P.sub, slab0 = part * nslabs, nchunks = nslabs / kChunkSlabs;
     const bool diag = I == J;
     const int rowA = s * P.c_pad + I * kRows, rowB = s * P.c_pad + J * kRows;
     const uint32_t sb = smem_u32(pipe_base(smem_raw));
@@ -197,7 +216,7 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
     if (warp == 0 && lane == 0) {
         // producer: the split's 64 slabs of rows I (and J), hi and lo parts
         const uint32_t bytes = (diag ? 2u : 4u) * kSlabTile;
-        for (int k = 0; k < kMomSlabs; ++k) {
+        for (int k = 0; k < nslabs; ++k) {
             const int st = k % kMomStages;
             const uint32_t par = static_cast<uint32_t>(k / kMomStages) & 1u;
             if (!mbar_wait<kSleepProducer>(&S.empty[st], par ^ 1u) ||
@@ -206,12 +225,13 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
                 break;
             }
             const uint32_t a = sb + st * kMomStage;
+            const int x = (slab0 + k) * kSlab;
             mbar_expect_tx(&S.full[st], bytes);
-            tma_load_2d(a, &P.hi, k * kSlab, rowA, &S.full[st]);
-            tma_load_2d(a + kSlabTile, &P.lo, k * kSlab, rowA, &S.full[st]);
+            tma_load_2d(a, &P.hi, x, rowA, &S.full[st]);
+            tma_load_2d(a + kSlabTile, &P.lo, x, rowA, &S.full[st]);
             if (!diag) {
-                tma_load_2d(a + 2 * kSlabTile, &P.hi, k * kSlab, rowB, &S.full[st]);
-                tma_load_2d(a + 3 * kSlabTile, &P.lo, k * kSlab, rowB, &S.full[st]);
+                tma_load_2d(a + 2 * kSlabTile, &P.hi, x, rowB, &S.full[st]);
+                tma_load_2d(a + 3 * kSlabTile, &P.lo, x, rowB, &S.full[st]);
             }
             S.last_load[st] = k;
         }
@@ -219,7 +239,7 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
         // MMA issuer: per slab 4 K steps of 16 halves, three products each
         const uint32_t idesc = instr_desc_f16(kRows, kRows);
         bool ok = true;
-        for (int k = 0; k < kMomSlabs && ok; ++k) {
+        for (int k = 0; k < nslabs && ok; ++k) {
             const int c = k / kChunkSlabs, acc = c & 1;
             const uint32_t d = tmem + static_cast<uint32_t>(acc * kRows);
             if (k % kChunkSlabs == 0 && c >= 2) {
@@ -259,7 +279,7 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
         for (int j = 0; j < kRows; ++j) sum[j] = 0.f;
         bool ok = true;
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < nchunks; ++c) {
             const int acc = c & 1;
             const bool w = mbar_wait<kSleepEpilogue>(&S.afull[acc], static_cast<uint32_t>(c / 2) & 1u);
             if (!w) S.abort = 1;
@@ -284,8 +304,8 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
             const int row = q * 32 + lane;
             const int er = P.scale_e[I * kRows + row];
             const int *ec = P.scale_e + J * kRows;
-            float *dst = P.partial +
-                         (static_cast<int64_t>(s) * P.c_pad + I * kRows + row) * P.c_pad + J * kRows;
+            float *dst = P.partial + (static_cast<int64_t>(blockIdx.y) * P.c_pad + I * kRows + row) *
+                                         P.c_pad + J * kRows;
 #pragma unroll
             for (int j4 = 0; j4 < kRows / 4; ++j4)
                 *reinterpret_cast<float4 *>(dst + j4 * 4) = make_float4(
@@ -313,59 +333,46 @@ __global__ void __launch_bounds__(kMomThreads, 1) moment_product_kernel(
     if (warp == 1) tmem_free(tmem, 256);
 }
 
-// Sum of the splits: a block takes one 32 x 32 tile of the output; it reads
-// the tile of the upper triangle that holds its entries, (min, max), row by
-// row through shared memory, adds the splits in float64 in order, and for the
-// second moment adds back what the centring took out: with v = x - mu' and
-// s = sum_t v = sum_t x - n mu', sum_t x_i x_j = sum_t v_i v_j + mu'_i s_j +
-// mu'_j s_i + n mu'_i mu'_j (exact algebra for any offset mu').  Then it
-// divides by n and writes (or adds) the float32 result.
+// Sum of the splits: one thread per output entry (i, j) adds the partials of
+// (min(i, j), max(i, j)) over the splits in float64, in order (so (i, j) and
+// (j, i) get the same bits), and for the second moment adds back what the
+// centring took out: with v = x - mu' and s = sum_t v = sum_t x - n mu',
+// sum_t x_i x_j = sum_t v_i v_j + mu'_i s_j + mu'_j s_i + n mu'_i mu'_j
+// (exact algebra for any offset mu').  Then it divides by n and writes (or
+// adds) the float32 result.
 __global__ void __launch_bounds__(256) moment_sum_kernel(const float *__restrict__ partial, int S,
                                                          int c_pad, int C, int64_t n, int centred,
                                                          const double *__restrict__ sum,
                                                          const float *__restrict__ mu_hi,
                                                          const float *__restrict__ mu_lo,
                                                          int accumulate, float *__restrict__ out) {
-    __shared__ float tile[32][33];
-    const int bi = blockIdx.y, bj = blockIdx.x;  // output tile
-    const int ua = min(bi, bj), ub = max(bi, bj);  // the upper-triangle tile that holds it
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 per pass
-    double acc[4] = {0.0, 0.0, 0.0, 0.0};
-    for (int s = 0; s < S; ++s) {
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = ty + 8 * k;
-            tile[r][tx] = partial[(static_cast<int64_t>(s) * c_pad + ua * 32 + r) * c_pad + ub * 32 + tx];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = ty + 8 * k;  // output entry (bi*32 + r, bj*32 + tx)
-            const int i = bi * 32 + r, j = bj * 32 + tx;
-            // entry (min(i, j), max(i, j)) of the upper tile (ua, ub)
-            const int a = min(i, j) - ua * 32, b = max(i, j) - ub * 32;
-            acc[k] += static_cast<double>(tile[a][b]);
-        }
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= static_cast<int64_t>(C) * C) return;
+    const int i = static_cast<int>(e / C), j = static_cast<int>(e % C);
+    const int a = min(i, j), b = max(i, j);
+    const float *p = partial + static_cast<int64_t>(a) * c_pad + b;
+    const int64_t plane = static_cast<int64_t>(c_pad) * c_pad;
+    double acc = 0.0;
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {
+        const float p0 = p[s * plane], p1 = p[(s + 1) * plane], p2 = p[(s + 2) * plane],
+                    p3 = p[(s + 3) * plane];
+        acc += static_cast<double>(p0);
+        acc += static_cast<double>(p1);
+        acc += static_cast<double>(p2);
+        acc += static_cast<double>(p3);
     }
+    for (; s < S; ++s) acc += static_cast<double>(p[s * plane]);
     const double dn = static_cast<double>(n);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = bi * 32 + ty + 8 * k, j = bj * 32 + tx;
-        if (i < C && j < C) {
-            double v = acc[k];
-            if (!centred) {
-                const double mi = static_cast<double>(mu_hi[i]) + static_cast<double>(mu_lo[i]);
-                const double mj = static_cast<double>(mu_hi[j]) + static_cast<double>(mu_lo[j]);
-                const double si = sum[i] - dn * mi, sj = sum[j] - dn * mj;
-                // the same float64 operations for (i, j) and (j, i): symmetric
-                v += min(mi * sj, mj * si) + max(mi * sj, mj * si) + dn * (mi * mj);
-            }
-            const float f = static_cast<float>(v / dn);
-            float *o = out + static_cast<int64_t>(i) * C + j;
-            *o = accumulate ? *o + f : f;
-        }
+    if (!centred) {
+        const double mi = static_cast<double>(mu_hi[i]) + static_cast<double>(mu_lo[i]);
+        const double mj = static_cast<double>(mu_hi[j]) + static_cast<double>(mu_lo[j]);
+        const double si = sum[i] - dn * mi, sj = sum[j] - dn * mj;
+        // the same float64 operations for (i, j) and (j, i): symmetric
+        acc += min(mi * sj, mj * si) + max(mi * sj, mj * si) + dn * (mi * mj);
     }
+    const float f = static_cast<float>(acc / dn);
+    out[e] = accumulate ? out[e] + f : f;
 }
 
 }  // namespace
@@ -377,7 +384,7 @@ int moment_splits(int64_t n) { return static_cast<int>((n + kMomentSplit - 1) / 
 cudaError_t launch_moment_stats(const float *X, int64_t ld, int C, int64_t t0, int64_t n,
                                 double *sum, float *mu_hi, float *mu_lo, int *scale_e,
                                 MomentStatus *st, cudaStream_t s) {
-    moment_stats_kernel<<<C, 256, 0, s>>>(X, ld, t0, n, sum, mu_hi, mu_lo, scale_e, st);
+    moment_stats_kernel<<<C, kStatsThreads, 0, s>>>(X, ld, t0, n, sum, mu_hi, mu_lo, scale_e, st);
     return cudaGetLastError();
 }
 
@@ -385,10 +392,18 @@ cudaError_t launch_moment_split(const float *X, int64_t ld, int C, int c_pad, in
                                 int64_t n, const float *mu_hi, const float *mu_lo,
                                 const int *scale_e, uint32_t *hi, uint32_t *lo, cudaStream_t s) {
     const int S = moment_splits(n);
-    const int64_t words = static_cast<int64_t>(S) * c_pad * kWords;
-    moment_split_kernel<<<static_cast<int>((words + 255) / 256), 256, 0, s>>>(
-        X, ld, C, c_pad, t0, n, S, mu_hi, mu_lo, scale_e, hi, lo);
+    const dim3 grid(kWords / 256, c_pad, std::min(S, 65535));
+    moment_split_kernel<<<grid, 256, 0, s>>>(X, ld, C, c_pad, t0, n, S, mu_hi, mu_lo, scale_e, hi,
+                                             lo);
     return cudaGetLastError();
+}
+
+int moment_subsplits(int c_pad, int64_t n) {
+    const int64_t pairs = static_cast<int64_t>(c_pad / kRows) * (c_pad / kRows + 1) / 2;
+    const int64_t ctas = pairs * moment_splits(n);
+    int sub = 1;
+    while (sub < kMaxSub && ctas * sub * 2 <= kMomentTargetCtas) sub *= 2;
+    return sub;
 }
 
 cudaError_t launch_moment_product(const uint32_t *hi, const uint32_t *lo, int c_pad, int64_t n,
@@ -403,6 +418,7 @@ cudaError_t launch_moment_product(const uint32_t *hi, const uint32_t *lo, int c_
     P.partial = partial;
     P.c_pad = c_pad;
     P.blocks = c_pad / kRows;
+    P.sub = moment_subsplits(c_pad, n);
     P.scale_e = scale_e;
     P.status = status;
     cudaError_t e = cudaFuncSetAttribute(moment_product_kernel,
@@ -410,17 +426,17 @@ cudaError_t launch_moment_product(const uint32_t *hi, const uint32_t *lo, int c_
                                          static_cast<int>(kMomSmem));
     if (e != cudaSuccess) return e;
     const int pairs = P.blocks * (P.blocks + 1) / 2;
-    moment_product_kernel<<<dim3(pairs, S), kMomThreads, kMomSmem, s>>>(P);
+    moment_product_kernel<<<dim3(pairs, S * P.sub), kMomThreads, kMomSmem, s>>>(P);
     return cudaGetLastError();
 }
 
 cudaError_t launch_moment_sum(const float *partial, int c_pad, int C, int64_t n, int centred,
                               const double *sum, const float *mu_hi, const float *mu_lo,
                               int accumulate, float *out, cudaStream_t s) {
-    const int tiles = (C + 31) / 32;
-    moment_sum_kernel<<<dim3(tiles, tiles), 256, 0, s>>>(partial, moment_splits(n), c_pad, C, n,
-                                                         centred, sum, mu_hi, mu_lo, accumulate,
-                                                         out);
+    const int64_t entries = static_cast<int64_t>(C) * C;
+    moment_sum_kernel<<<static_cast<int>((entries + 255) / 256), 256, 0, s>>>(
+        partial, moment_splits(n) * moment_subsplits(c_pad, n), c_pad, C, n, centred, sum, mu_hi,
+        mu_lo, accumulate, out);
     return cudaGetLastError();
 }
 

@@ -101,7 +101,63 @@ __device__ __forceinline__ void list_insert(unsigned long long (&k)[KP], unsigne
     }
 }
 
-template <int KP, bool kWide, bool kF16>
+// k <- the KP least of the two sorted lists k and o (keys are distinct):
+// k[p] and o[KP - 1 - p] pair the list with the other reversed, so the KP
+// lesser of each pair are exactly the KP least of the union, as a bitonic
+// sequence; a bitonic half-cleaner cascade then sorts them.
+template <int KP>
+__device__ __forceinline__ void list_merge(unsigned long long (&k)[KP],
+                                           const unsigned long long (&o)[KP]) {
+#pragma unroll
+    for (int p = 0; p < KP; ++p) k[p] = min(k[p], o[KP - 1 - p]);
+#pragma unroll
+    for (int h = KP / 2; h > 0; h >>= 1)
+#pragma unroll
+        for (int p = 0; p < KP; ++p)
+            if ((p & h) == 0) {
+                const unsigned long long lo = min(k[p], k[p + h]), hi = max(k[p], k[p + h]);
+                k[p] = lo;
+                k[p + h] = hi;
+            }
+}
+
+// The 16 least of a 32-column batch (columns in mask, the others absent)
+// merged into a 16-long list: a bitonic sort of the batch's 32 keys, then
+// list_merge with its first 16.
+template <int KP>
+__device__ __forceinline__ void batch_merge(unsigned long long (&lk)[KP], const float (&v)[32],
+                                            uint32_t mask, int c0) {
+    if constexpr (KP == 16) {
+        unsigned long long b[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            b[j] = ((mask >> j) & 1u) ? pack_tj(v[j], c0 + j) : ~0ull;
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+            for (int h = k >> 1; h > 0; h >>= 1)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int l = i ^ h;
+                    if (l > i) {
+                        const bool up = (i & k) == 0;
+                        const unsigned long long lo = min(b[i], b[l]), hi = max(b[i], b[l]);
+                        b[i] = up ? lo : hi;
+                        b[l] = up ? hi : lo;
+                    }
+                }
+        unsigned long long o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = b[j];
+        list_merge<16>(lk, o);
+    }
+}
+
+// kFill: the home pass of the pruned search, whose lists start empty: a
+// batch where some row has many candidates is sorted and merged whole
+// (batch_merge) instead of inserted one candidate at a time.  A separate
+// instance, so that the other passes keep their register allocation.
+template <int KP, bool kWide, bool kF16, bool kFill>
 __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
     tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
     constexpr int kEpiWarps = Epi<KP, kWide>::kWarps;
@@ -212,11 +268,17 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
                     // rare: insert this batch's candidates in column order
                     // with the one copy of the sink
                     uint32_t mask = below_mask(v, tau);
+                    if (kFill && __any_sync(__activemask(), __popc(mask) > 14)) {
+                        // many candidates (a list still filling): sort the
+                        // batch's keys and merge its 16 least into the list
+                        batch_merge(lk, v, mask, col0 + cc * 32);
+                    } else {
 #pragma unroll 1
-                    while (mask) {
-                        const int j = __ffs(mask) - 1;
-                        mask &= mask - 1;
-                        list_insert<KP>(lk, pack_tj(pick32(v, j), col0 + cc * 32 + j));
+                        while (mask) {
+                            const int j = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            list_insert<KP>(lk, pack_tj(pick32(v, j), col0 + cc * 32 + j));
+                        }
                     }
                     g_row_tau[group][row] = key_t(lk[KP - 1]);
                     s_row_tq[group][row] = key_t(lk[kQ - 1]);
@@ -252,11 +314,14 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
             epilogue_sync<kEpiWarps>();
             if (group == 0) {
 #pragma unroll 1
-                for (int q = 1; q < kParts; ++q)
-#pragma unroll 1
+                for (int q = 1; q < kParts; ++q) {
+                    unsigned long long o[KP];
+#pragma unroll
                     for (int p = 0; p < KP; ++p)
-                        list_insert<KP>(lk, pack_tj(pk[((q - 1) * kRows + row) * KP + p],
-                                                    pi[((q - 1) * kRows + row) * KP + p]));
+                        o[p] = pack_tj(pk[((q - 1) * kRows + row) * KP + p],
+                                       pi[((q - 1) * kRows + row) * KP + p]);
+                    list_merge<KP>(lk, o);
+                }
             }
         }
         if (group == 0 && !*(volatile int *)&S.abort && r0 + row < a.row_end) {
@@ -275,12 +340,13 @@ __global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
 template <int KP, bool kWide, bool kF16>
 cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStream_t s) {
     const size_t smem = kWide ? kWidePipeSmem : kPipeSmem;
-    cudaError_t e = cudaFuncSetAttribute(tc_knn_kernel<KP, kWide, kF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the home pass of the pruned search: a block list and no seed
+    const bool fill = KP == 16 && P.a.blist != nullptr && P.a.seed == nullptr;
+    auto kern = fill ? tc_knn_kernel<KP, kWide, kF16, KP == 16> : tc_knn_kernel<KP, kWide, kF16, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    tc_knn_kernel<KP, kWide, kF16>
-        <<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
+    kern<<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
