@@ -54,9 +54,12 @@ struct TcKnnParams {
     KnnTileArgs a;
 };
 
-template <int KP, bool kWide>
+template <int KP, bool kWide, bool kFill = false>
 struct Epi {
-    static constexpr int kWarps = (KP == 16 && !kWide) ? 12 : 8;  // epilogue warps
+    // epilogue warps: 12 (three groups) where the lists are short and the
+    // epilogue keeps pace with the products; 8 with more registers each for
+    // 32-long lists, wide rows and the home pass (fewer lists to fill)
+    static constexpr int kWarps = (KP == 16 && !kWide && !kFill) ? 12 : 8;
     static constexpr int kParts = kWarps / 4;          // groups: lists per row
     static constexpr int kThreads = (kWarps + 1 + kWarps / 4) * 32;  // + producer + MMA warps
 };
@@ -158,10 +161,10 @@ __device__ __forceinline__ void batch_merge(unsigned long long (&lk)[KP], const 
 // (batch_merge) instead of inserted one candidate at a time.  A separate
 // instance, so that the other passes keep their register allocation.
 template <int KP, bool kWide, bool kF16, bool kFill>
-__global__ void __launch_bounds__(Epi<KP, kWide>::kThreads, 1)
+__global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, 1)
     tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
-    constexpr int kEpiWarps = Epi<KP, kWide>::kWarps;
-    constexpr int kParts = Epi<KP, kWide>::kParts;
+    constexpr int kEpiWarps = Epi<KP, kWide, kFill>::kWarps;
+    constexpr int kParts = Epi<KP, kWide, kFill>::kParts;
     extern __shared__ uint8_t smem_raw[];
     __shared__ PipeSmem S;
     const KnnTileArgs &a = P.a;
@@ -343,10 +346,11 @@ cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStrea
     // the home pass of the pruned search: a block list and no seed
     const bool fill = KP == 16 && P.a.blist != nullptr && P.a.seed == nullptr;
     auto kern = fill ? tc_knn_kernel<KP, kWide, kF16, KP == 16> : tc_knn_kernel<KP, kWide, kF16, false>;
+    const int threads = fill ? Epi<KP, kWide, KP == 16>::kThreads : Epi<KP, kWide, false>::kThreads;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<dim3(row_tiles, splits), Epi<KP, kWide>::kThreads, smem, s>>>(P);
+    kern<<<dim3(row_tiles, splits), threads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
