@@ -34,6 +34,7 @@
 //     result; entry (i, j) and (j, i) both read the partial of (min, max),
 //     so the result is exactly symmetric.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <climits>
 #include <cmath>
@@ -122,6 +123,24 @@ __global__ void __launch_bounds__(kStatsThreads) moment_stats_kernel(
     }
 }
 
+// f16_split (common.cuh) of two values at once, packed as the operand words
+// hold them (the first value in the low half): hi = fp16(x 2^e),
+// lo = fp16(x 2^e - hi), each flushed to zero below 2^-14; the paired
+// conversions give the same halves as the single ones.
+__device__ __forceinline__ void f16_split2(float x0, float x1, float scale, uint32_t &hw,
+                                           uint32_t &lw) {
+    const float s0 = __fmul_rn(x0, scale), s1 = __fmul_rn(x1, scale);
+    float2 h = __half22float2(__floats2half2_rn(s0, s1));
+    h.x = fabsf(h.x) < 0x1p-14f ? 0.f : h.x;
+    h.y = fabsf(h.y) < 0x1p-14f ? 0.f : h.y;
+    float2 l = __half22float2(__floats2half2_rn(__fsub_rn(s0, h.x), __fsub_rn(s1, h.y)));
+    l.x = fabsf(l.x) < 0x1p-14f ? 0.f : l.x;
+    l.y = fabsf(l.y) < 0x1p-14f ? 0.f : l.y;
+    const __half2 hh = __floats2half2_rn(h.x, h.y), ll = __floats2half2_rn(l.x, l.y);
+    hw = *reinterpret_cast<const uint32_t *>(&hh);
+    lw = *reinterpret_cast<const uint32_t *>(&ll);
+}
+
 // grid: (kWords / 256 word blocks, c_pad channels, split blocks); a
 // thread makes one 32-bit word (two halves) of each split it visits
 __global__ void __launch_bounds__(256) moment_split_kernel(
@@ -136,16 +155,13 @@ __global__ void __launch_bounds__(256) moment_split_kernel(
     const float *row = X + static_cast<int64_t>(ch ? r : 0) * ld + t0;
     for (int s = blockIdx.z; s < S; s += gridDim.z) {
         const int64_t t = static_cast<int64_t>(s) * kMomentSplit + 2 * wd;  // sample in the window
-        unsigned short h[2], l[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float v = 0.f;
-            if (ch && t + q < n) v = __fsub_rn(__fsub_rn(row[t + q], mh), ml);
-            f16_split(v, scale, h[q], l[q]);
-        }
+        const float v0 = (ch && t < n) ? __fsub_rn(__fsub_rn(row[t], mh), ml) : 0.f;
+        const float v1 = (ch && t + 1 < n) ? __fsub_rn(__fsub_rn(row[t + 1], mh), ml) : 0.f;
+        uint32_t hw, lw;
+        f16_split2(v0, v1, scale, hw, lw);
         const int64_t w = (static_cast<int64_t>(s) * c_pad + r) * kWords + wd;
-        hi[w] = h[0] | (static_cast<unsigned>(h[1]) << 16);
-        lo[w] = l[0] | (static_cast<unsigned>(l[1]) << 16);
+        hi[w] = hw;
+        lo[w] = lw;
     }
 }
 
