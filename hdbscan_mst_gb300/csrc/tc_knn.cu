@@ -59,7 +59,10 @@ struct Epi {
     // epilogue warps: 12 (three groups) where the lists are short and the
     // epilogue keeps pace with the products; 8 with more registers each for
     // 32-long lists, wide rows and the home pass (fewer lists to fill)
-    static constexpr int kWarps = (KP == 16 && !kWide && !kFill) ? 12 : 8;
+    // the narrow home pass: one group on the small pipeline, two CTAs per SM
+    static constexpr bool kSmall = kFill && !kWide;
+    static constexpr int kWarps = kSmall ? 4 : (KP == 16 && !kWide && !kFill) ? 12 : 8;
+    static constexpr int kMinBlocks = kSmall ? 2 : 1;
     static constexpr int kParts = kWarps / 4;          // groups: lists per row
     static constexpr int kThreads = (kWarps + 1 + kWarps / 4) * 32;  // + producer + MMA warps
 };
@@ -161,10 +164,11 @@ __device__ __forceinline__ void batch_merge(unsigned long long (&lk)[KP], const 
 // (batch_merge) instead of inserted one candidate at a time.  A separate
 // instance, so that the other passes keep their register allocation.
 template <int KP, bool kWide, bool kF16, bool kFill>
-__global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, 1)
+__global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide, kFill>::kMinBlocks)
     tc_knn_kernel(const __grid_constant__ TcKnnParams P) {
     constexpr int kEpiWarps = Epi<KP, kWide, kFill>::kWarps;
     constexpr int kParts = Epi<KP, kWide, kFill>::kParts;
+    constexpr bool kSmall = Epi<KP, kWide, kFill>::kSmall;
     extern __shared__ uint8_t smem_raw[];
     __shared__ PipeSmem S;
     const KnnTileArgs &a = P.a;
@@ -206,13 +210,13 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, 1)
         (&g_row_tau[0][0])[i] = INFINITY;
         (&s_row_tq[0][0])[i] = INFINITY;
     }
-    tc_setup<kEpiWarps, kWide>(S);
+    tc_setup<kEpiWarps, kWide, kSmall>(S);
     fence_before();
     __syncthreads();
     fence_after();
     // the MMA operands: dk floats (TF32), or dk / 2 words of two halves (FP16)
     const int dk_mma = kF16 ? a.dk / 2 : a.dk;
-    tc_produce_and_multiply<kEpiWarps, kWide, kF16>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+    tc_produce_and_multiply<kEpiWarps, kWide, kF16, kSmall>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
 
     if (warp < 4) tc_load_a<kWide>(S, P.a_hi, P.a_lo, r0, dk_mma);
     if (warp < kEpiWarps) {
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, 1)
             else if (gthr_warp && lane < kTileCols / 4 + 8)
                 cp_async16(&s_gthr[warp][buf][lane - kTileCols / 4], gthr_warp + (lane - kTileCols / 4) * 4);
         };
-        tc_epilogue_loop<kEpiWarps, kWide>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+        tc_epilogue_loop<kEpiWarps, kWide, kSmall>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 float v[32];
@@ -337,14 +341,14 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, 1)
             }
         }
     }
-    tc_teardown<kEpiWarps, kWide>(S, a.status);
+    tc_teardown<kEpiWarps, kWide, kSmall>(S, a.status);
 }
 
 template <int KP, bool kWide, bool kF16>
 cudaError_t tc_launch(const TcKnnParams &P, int row_tiles, int splits, cudaStream_t s) {
-    const size_t smem = kWide ? kWidePipeSmem : kPipeSmem;
     // the home pass of the pruned search: a block list and no seed
     const bool fill = KP == 16 && P.a.blist != nullptr && P.a.seed == nullptr;
+    const size_t smem = kWide ? kWidePipeSmem : (fill ? kSmallPipeSmem : kPipeSmem);
     auto kern = fill ? tc_knn_kernel<KP, kWide, kF16, KP == 16> : tc_knn_kernel<KP, kWide, kF16, false>;
     const int threads = fill ? Epi<KP, kWide, KP == 16>::kThreads : Epi<KP, kWide, false>::kThreads;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

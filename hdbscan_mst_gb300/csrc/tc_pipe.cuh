@@ -48,6 +48,7 @@ namespace tc {
 
 constexpr int kStages = 6;       // ring slabs (kWide: kWideStages)
 constexpr int kWideStages = 3;
+constexpr int kSmallStages = 2;
 constexpr int kWideDkMax = 192;
 constexpr int kTileCols = 64;   // columns of a tile (MMA N); a ring slab holds kCols = 2 tiles
 constexpr int kAccPerGroup = 2;
@@ -70,10 +71,13 @@ struct Slot {
     }
 };
 
-template <bool kWide>
+// kSmall: a narrow pipeline for two CTAs per SM (a 2-slab ring, 256 TMEM
+// columns: A in [0, 128), one group's two accumulators in [128, 256)).
+template <bool kWide, bool kSmall = false>
 struct PipeShape {
-    static constexpr int kSt = kWide ? kWideStages : kStages;
+    static constexpr int kSt = kWide ? kWideStages : (kSmall ? kSmallStages : kStages);
     static constexpr uint32_t kAccBase = kWide ? 256u : 128u;  // first accumulator column
+    static constexpr uint32_t kCols = kSmall ? 256u : 512u;    // the TMEM allocation
 };
 constexpr int kAccMax = 6;          // TMEM accumulators of kTileCols columns
 constexpr uint32_t kAccBase = 128;  // TMEM columns [0, 2 dk) hold A hi and lo
@@ -89,6 +93,7 @@ constexpr uint32_t kSlabTile = kCols * kSlabBytes;  // 16 KB: one slab of 128 co
 // the A lo slabs, then the ring
 constexpr size_t kPipeSmem = 2 * kStages * kSlabTile + 1024;
 constexpr size_t kWidePipeSmem = (kWideDkMax / kSlab + 2 * kWideStages) * kSlabTile + 1024;
+constexpr size_t kSmallPipeSmem = 2 * kSmallStages * kSlabTile + 1024;
 
 // Accumulator of tile t: group j = t % G alternates between its two.
 template <int G>
@@ -146,7 +151,7 @@ __device__ __forceinline__ uint8_t *pipe_base(uint8_t *smem_raw) {
 }
 
 // Barrier initialisation and TMEM allocation; all threads, before anything else.
-template <int kEpiWarps, bool kWide = false>
+template <int kEpiWarps, bool kWide = false, bool kSmall = false>
 __device__ __forceinline__ void tc_setup(PipeSmem &S) {
     const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
@@ -165,9 +170,12 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
     }
     static_assert(acc_count<kEpiWarps>() * kAccPerGroup <= kAccMax, "accumulators");
     static_assert(kAccBase + kAccMax * kTileCols <= kTmemCols, "TMEM budget");
+    static_assert(!kSmall || (!kWide && kAccBase + acc_count<kEpiWarps>() * kAccPerGroup * kTileCols <=
+                                            PipeShape<false, true>::kCols),
+                  "TMEM budget, small pipeline");
     static_assert(!kWide || (acc_count<kEpiWarps>() * kAccPerGroup * kTileCols + 256 <= kTmemCols &&
                              kWideDkMax <= 256), "TMEM budget, wide rows");
-    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, kTmemCols);
+    if (warp == kEpiWarps + 1) tmem_alloc(&S.tmem_base, PipeShape<kWide, kSmall>::kCols);
 }
 
 // The A operand into TMEM, by the first epilogue group (warps 0 .. 3, one per
@@ -207,18 +215,21 @@ __device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const 
 // word; dk then counts words, and the K steps, slabs, TMEM columns and
 // descriptors are those of the TF32 form on dk words, only the MMA kind
 // differs (K = 16 halves per MMA instead of 8 floats: the same 32 bytes).
-template <int kEpiWarps, bool kWide = false, bool kF16 = false>
+template <int kEpiWarps, bool kWide = false, bool kF16 = false, bool kSmall = false>
 __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeSmem &S,
                                                         uint32_t sbase, int dk, int a_row,
                                                         const TileSeq &seq) {
     static_assert(!(kWide && kF16), "the wide rows stay on TF32");
-    using Sh = PipeShape<kWide>;
+    using Sh = PipeShape<kWide, kSmall>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slabs = dk / kSlab;
     const uint32_t alo = sbase;  // kWide: A lo slabs
     const uint32_t ring = sbase + (kWide ? static_cast<uint32_t>(slabs) * kSlabTile : 0u);
     constexpr int kAcc = acc_count<kEpiWarps>();  // = issuers = epilogue groups
-    static_assert(kWide ? kAcc == 2 : ((kAcc == 2 || kAcc == 3) && kStages == 6), "see Slot");
+    // one issuer (kSmall) owns every stage, so no phase parity can alias
+    static_assert(kWide ? kAcc == 2
+                        : kSmall ? kAcc == 1 : ((kAcc == 2 || kAcc == 3) && kStages == 6),
+                  "see Slot");
     if (warp == kEpiWarps && lane == 0) {
         if (kWide) {
             mbar_expect_tx(&S.abar, static_cast<uint32_t>(slabs) * kSlabTile);
@@ -320,10 +331,10 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
 // consume(tmem_addr, col0, buf) with the TMEM address of this thread's lane at
 // the tile's first column, the tile's first global column and the buffer
 // holding its column data; then hands the accumulator back.
-template <int kEpiWarps, bool kWide = false, class Prefetch, class Consume>
+template <int kEpiWarps, bool kWide = false, bool kSmall = false, class Prefetch, class Consume>
 __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq,
                                                  Prefetch &&prefetch, Consume &&consume) {
-    using Sh = PipeShape<kWide>;
+    using Sh = PipeShape<kWide, kSmall>;
     constexpr int kGroups = kEpiWarps / 4;
     constexpr int kAcc = acc_count<kEpiWarps>();
     const int warp = threadIdx.x >> 5;
@@ -355,7 +366,7 @@ __device__ __forceinline__ void tc_epilogue_loop(PipeSmem &S, const TileSeq &seq
 
 // All threads, last: report a give-up, drain what may still be in flight
 // (bounded), free TMEM.
-template <int kEpiWarps, bool kWide = false>
+template <int kEpiWarps, bool kWide = false, bool kSmall = false>
 __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
     const int tid = threadIdx.x, warp = tid >> 5;
     fence_before();
@@ -365,13 +376,13 @@ __device__ __forceinline__ void tc_teardown(PipeSmem &S, unsigned *status) {
             atomicOr(status, kStatusTimeout);
             for (int i = 0; i < acc_count<kEpiWarps>() * kAccPerGroup; ++i)
                 mbar_wait<kSleepProducer>(&S.afull[i], 0);
-            for (int i = 0; i < PipeShape<kWide>::kSt; ++i)
+            for (int i = 0; i < PipeShape<kWide, kSmall>::kSt; ++i)
                 mbar_wait<kSleepProducer>(&S.full[i], 0);
         }
         __syncthreads();
     }
     fence_after();
-    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, kTmemCols);
+    if (warp == kEpiWarps + 1) tmem_free(S.tmem_base, PipeShape<kWide, kSmall>::kCols);
 }
 
 // Named barrier over the epilogue warps only (barrier 1).
