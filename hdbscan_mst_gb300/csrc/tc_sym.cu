@@ -126,7 +126,12 @@ __device__ __forceinline__ float load_theta(const unsigned *theta, int c) {
     return __uint_as_float(__ldcg(theta + c));
 }
 
-__global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_constant__ TcSymParams P) {
+// kEW epilogue warps; kSmall: the home pass on the small pipeline (one
+// group, a 2-slab ring, 256 TMEM columns), two CTAs per SM.
+template <int kEW, bool kSmall>
+__global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
+    tc_sym_kernel(const __grid_constant__ TcSymParams P) {
+    constexpr int kEpiWarps = kEW;
     extern __shared__ uint8_t smem_raw[];
     __shared__ PipeSmem S;
     __shared__ int s_rcomp[kRows];
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
     constexpr int kSub = kCols / kTileCols;
 
     if (tid < kRows) s_rcomp[tid] = r0 + tid < a.np ? a.comp[r0 + tid] : -1;
-    tc_setup<kEpiWarps>(S);
+    tc_setup<kEpiWarps, false, kSmall>(S);
     fence_before();
     __syncthreads();
     fence_after();
@@ -169,9 +174,9 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
         atomicAdd(a.tile_pairs, static_cast<unsigned long long>(seq.n) * kTileCols * kRows);
     const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
     if (a.f16)
-        tc_produce_and_multiply<kEpiWarps, false, true>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+        tc_produce_and_multiply<kEpiWarps, false, true, kSmall>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
     else
-        tc_produce_and_multiply<kEpiWarps, false, false>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
+        tc_produce_and_multiply<kEpiWarps, false, false, kSmall>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
     if (warp < 4) tc_load_a(S, P.x_hi, P.x_lo, r0, dk_mma);
 
     if (warp < kEpiWarps) {
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
             }
         };
         int k_tile = 0;
-        tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+        tc_epilogue_loop<kEpiWarps, false, kSmall>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
             // the live bounds are read every 4th tile of the warp (each read
             // is used by the tiles after it; a stale bound is only larger)
             const bool refresh = (k_tile++ & 3) == 0;
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_sym_kernel(const __grid_con
             }
         });
     }
-    tc_teardown<kEpiWarps>(S, a.status);
+    tc_teardown<kEpiWarps, false, kSmall>(S, a.status);
 }
 
 // The rows the one-sided refine left open (page "HDBSCAN", "Exact
@@ -629,10 +634,14 @@ cudaError_t launch_tc_sym(const SymArgs &a, const float *x_hi, const float *x_lo
     if ((a.f16 && dk_mma != kSlab) || !make_point_map(&P.maps.b_hi, x_hi, a.ld, dk_mma) ||
         !make_point_map(&P.maps.b_lo, x_lo, a.ld, dk_mma))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_sym_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kPipeSmem));
+    // the home pass (its short block list) on the small pipeline
+    const bool home = a.list_stride == kSymHome;
+    auto kern = home ? tc_sym_kernel<4, true> : tc_sym_kernel<kEpiWarps, false>;
+    const size_t smem = home ? kSmallPipeSmem : kPipeSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    tc_sym_kernel<<<a.blocks, kSymThreads, kPipeSmem, s>>>(P);
+    kern<<<a.blocks, home ? (4 + 1 + 1) * 32 : kSymThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
