@@ -173,6 +173,7 @@ float coef_up(double c) {
 }
 
 constexpr int kMaxSplits = 8;
+constexpr int kScanMaxSplits = 16;  // column splits of the one-sided tensor scan (few rows)
 constexpr size_t kPartialBudget = size_t(256) << 20;  // bytes of partial lists per chunk
 
 int sm_count() {
@@ -1164,7 +1165,13 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.dk = p.dk;
             sa.col_tiles = col_tiles;
             const int row_tiles = (na + kBM - 1) / kBM;
-            const int S0 = tensor ? choose_splits_tc(row_tiles, col_tiles, slots / 2)
+            // the tensor scan splits the columns so that a few active rows
+            // still give every SM a CTA, as far as the partial lists' scratch
+            // (kMaxSplits x n_pad rows) holds that many splits of na_pad rows
+            const int scan_cap = static_cast<int>(std::min<int64_t>(
+                kScanMaxSplits, static_cast<int64_t>(kMaxSplits) * p.n_pad / na_pad));
+            const int S0 = tensor ? std::max(1, std::min({scan_cap, col_tiles,
+                                                          (slots / 2) / std::max(row_tiles, 1)}))
                                   : choose_splits(row_tiles, col_tiles, slots);
             const int tps = (col_tiles + S0 - 1) / S0;
             const int S = (col_tiles + tps - 1) / tps;

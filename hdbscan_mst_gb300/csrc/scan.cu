@@ -168,14 +168,16 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= a.na) return;  // whole warp
     const int g = a.act_idx[r];
-    const int s = lane / kKeep, q = lane % kKeep;
-    unsigned long long key = kNoKey;
-    float tau = INFINITY;
-    if (s < a.splits) key = a.part_key[(static_cast<int64_t>(s) * a.lda + r) * kKeep + q];
-    if (lane < a.splits) tau = a.part_tau[static_cast<int64_t>(lane) * a.lda + r];
+    const int q = lane % kKeep;
     const float ca = a.act_core[r];
+    // the splits' kept candidates, 32 / kKeep splits per pass of the warp
     unsigned long long exact = kNoKey;
-    if (key != kNoKey) {
+    float tau = INFINITY;
+    for (int sb = 0; sb < a.splits; sb += 32 / kKeep) {
+        const int s = sb + lane / kKeep;
+        const unsigned long long key =
+            s < a.splits ? a.part_key[(static_cast<int64_t>(s) * a.lda + r) * kKeep + q] : kNoKey;
+        if (key == kNoKey) continue;
         const int b = static_cast<int>(key & 0xffffffffu);
         const float4 *xa = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(g) * a.dk);
         const float4 *xb = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(b) * a.dk);
@@ -188,8 +190,10 @@ __global__ void __launch_bounds__(256) mst_refine_kernel(const ScanArgs a) {
             acc = sqdiff_fma(u.w, v.w, acc);
         }
         const float w = fmaxf(fmaxf(ca, __ldg(a.core + b)), __fsqrt_rn(acc));
-        exact = key64(w, static_cast<unsigned>(b));
+        exact = min(exact, key64(w, static_cast<unsigned>(b)));
     }
+    for (int s = lane; s < a.splits; s += 32)
+        tau = fminf(tau, a.part_tau[static_cast<int64_t>(s) * a.lda + r]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         exact = min(exact, __shfl_xor_sync(0xffffffffu, exact, o));
