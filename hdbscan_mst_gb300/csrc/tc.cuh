@@ -35,6 +35,7 @@ constexpr int kSlabBytes = 128;   // bytes per row per slab
 // still: every poll takes at least tens of cycles.
 constexpr uint64_t kWaitNs = 1500000000ull;  // 1.5 s
 constexpr uint32_t kWaitPolls = 1u << 26;
+constexpr uint32_t kSuspendNs = 20000;  // a suspended test's time limit
 
 // Test hooks of the failure path (off unless a test sets them through the C
 // ABI): the wait limit, and a switch that makes every CTA's producer leave its
@@ -147,6 +148,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity) {
     return done != 0;
 }
 
+// The same test, but a thread whose phase is still open is suspended by the
+// hardware until the phase completes or about hint_ns pass, whichever comes
+// first: a waiting role takes no issue slots and wakes as the phase completes.
+__device__ __forceinline__ bool mbar_test_suspend(uint64_t *mbar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(mbar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -164,8 +179,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
     const uint64_t limit = *reinterpret_cast<volatile unsigned long long *>(&g_wait_ns);
     uint32_t sleep = 16;
     for (uint32_t it = 1; it < kWaitPolls; ++it) {
-        __nanosleep(sleep);
-        if (mbar_test(mbar, parity)) return true;
+        if (mbar_test_suspend(mbar, parity, kSuspendNs)) return true;
+        __nanosleep(sleep);  // only if the suspension ended early
         sleep = min(2 * sleep, kMaxSleepNs);
         if ((it & 15) == 0 && global_ns() - t0 > limit) return false;
     }

@@ -96,15 +96,14 @@ __device__ __forceinline__ int key_j(unsigned long long x) {
 
 template <int KP>
 __device__ __forceinline__ void list_insert(unsigned long long (&k)[KP], unsigned long long x) {
-    if (x < k[KP - 1]) {
-        k[KP - 1] = x;
+    // keys distinct, k sorted: slot p keeps k[p] if it is below x, else
+    // takes x (when k[p - 1] is below x) or k[p - 1]; every slot at once
+    bool below[KP];
 #pragma unroll
-        for (int p = KP - 1; p > 0; --p) {
-            const unsigned long long lo = min(k[p - 1], k[p]), hi = max(k[p - 1], k[p]);
-            k[p - 1] = lo;
-            k[p] = hi;
-        }
-    }
+    for (int p = 0; p < KP; ++p) below[p] = k[p] < x;
+#pragma unroll
+    for (int p = KP - 1; p > 0; --p) k[p] = below[p] ? k[p] : (below[p - 1] ? x : k[p - 1]);
+    k[0] = below[0] ? k[0] : x;
 }
 
 // k <- the KP least of the two sorted lists k and o (keys are distinct):
