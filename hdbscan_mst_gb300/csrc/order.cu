@@ -58,19 +58,22 @@ __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S,
     __shared__ __align__(16) float ps[kCellK][kCellPiv];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int i0 = blockIdx.x * kCellPts;
-    float acc[4][8];
+    // acc[a][b] = (pivot 2b, pivot 2b + 1) of point a: packed FP32 pairs,
+    // each half summed in feature order exactly as a scalar FMA chain
+    float2 acc[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        for (int b = 0; b < 4; ++b) acc[a][b] = make_float2(0.f, 0.f);
     for (int f0 = 0; f0 < dp; f0 += kCellK) {
         for (int q = tid; q < kCellK * kCellPts; q += 256) {
             const int f = q / kCellPts, c = q % kCellPts;
             const int i = i0 + c;
             xs[f][c] = (i < cnt && f0 + f < d) ? S[static_cast<int64_t>(f0 + f) * lds + i] : 0.f;
         }
+        // the pivots negated: x + (-p) rounds exactly as x - p
         for (int q = tid; q < kCellK * kCellPiv; q += 256)
-            (&ps[0][0])[q] = piv[static_cast<int64_t>(f0) * kCellPiv + q];
+            (&ps[0][0])[q] = -piv[static_cast<int64_t>(f0) * kCellPiv + q];
         __syncthreads();
 #pragma unroll
         for (int f = 0; f < kCellK; ++f) {
@@ -78,26 +81,31 @@ __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S,
             const float4 p0 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8]);
             const float4 p1 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8 + 4]);
             const float xv[4] = {x.x, x.y, x.z, x.w};
-            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const float2 pv[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w),
+                                  make_float2(p1.x, p1.y), make_float2(p1.z, p1.w)};
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int a = 0; a < 4; ++a) {
+                const float2 x2 = make_float2(xv[a], xv[a]);
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const float t = __fsub_rn(xv[a], pv[b]);
-                    acc[a][b] = __fmaf_rn(t, t, acc[a][b]);
+                for (int b = 0; b < 4; ++b) {
+                    const float2 t = __fadd2_rn(x2, pv[b]);
+                    acc[a][b] = __ffma2_rn(t, t, acc[a][b]);
                 }
+            }
         }
         __syncthreads();
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         const int i = i0 + ty * 4 + a;
-        float best = acc[a][0];
+        const float sq[8] = {acc[a][0].x, acc[a][0].y, acc[a][1].x, acc[a][1].y,
+                             acc[a][2].x, acc[a][2].y, acc[a][3].x, acc[a][3].y};
+        float best = sq[0];
         int arg = tx * 8;
 #pragma unroll
         for (int b = 1; b < 8; ++b)
-            if (acc[a][b] < best) {
-                best = acc[a][b];
+            if (sq[b] < best) {
+                best = sq[b];
                 arg = tx * 8 + b;
             }
         // least (value, pivot) over the 16 lanes of this point (one half-warp)
@@ -113,10 +121,10 @@ __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S,
         if (i < cnt) {
             if (pd) {
                 float4 *o = reinterpret_cast<float4 *>(pd + static_cast<int64_t>(i) * kCellPiv + tx * 8);
-                o[0] = make_float4(__fsqrt_rn(acc[a][0]), __fsqrt_rn(acc[a][1]),
-                                   __fsqrt_rn(acc[a][2]), __fsqrt_rn(acc[a][3]));
-                o[1] = make_float4(__fsqrt_rn(acc[a][4]), __fsqrt_rn(acc[a][5]),
-                                   __fsqrt_rn(acc[a][6]), __fsqrt_rn(acc[a][7]));
+                o[0] = make_float4(__fsqrt_rn(sq[0]), __fsqrt_rn(sq[1]), __fsqrt_rn(sq[2]),
+                                   __fsqrt_rn(sq[3]));
+                o[1] = make_float4(__fsqrt_rn(sq[4]), __fsqrt_rn(sq[5]), __fsqrt_rn(sq[6]),
+                                   __fsqrt_rn(sq[7]));
             }
             if (tx == 0) {
                 cell[i] = arg;

@@ -292,6 +292,23 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int j) {
     return (j & 16) ? d1 : d0;
 }
 
+// v[j] <- kdot v[j] + nb[j] for a batch of 32 columns (the expansion
+// t = |y|^2 - 2 x.y from the accumulated dot products), two columns per
+// packed FP32 FMA: each half rounds exactly as __fmaf_rn.
+__device__ __forceinline__ void expand32(float (&v)[32], const float4 *nb, float kdot) {
+    const float2 k2 = make_float2(kdot, kdot);
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 n = nb[j4];
+        const float2 a = __ffma2_rn(k2, make_float2(v[4 * j4], v[4 * j4 + 1]), make_float2(n.x, n.y));
+        const float2 b = __ffma2_rn(k2, make_float2(v[4 * j4 + 2], v[4 * j4 + 3]), make_float2(n.z, n.w));
+        v[4 * j4] = a.x;
+        v[4 * j4 + 1] = a.y;
+        v[4 * j4 + 2] = b.x;
+        v[4 * j4 + 3] = b.y;
+    }
+}
+
 // The least of 32 values by three-input minima (min.f32 with three operands):
 // 17 instructions in 4 levels instead of 31 in 5.
 __device__ __forceinline__ float min3f(float a, float b, float c) {

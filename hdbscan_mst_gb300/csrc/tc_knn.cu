@@ -71,6 +71,10 @@ __shared__ float g_row_tau[4][kRows];  // per group and row: that list's KP-th k
 // per group and row: that list's q-th key, q = ceil(KP / groups): once every
 // group holds q keys, their largest q-th key has at least KP keys at or below it
 __shared__ float s_row_tq[4][kRows];
+// per row: the CTA's threshold, the least of the groups' KP-th keys and the
+// largest of their q-th keys, written by the thread that last inserted
+// (every value written is a valid bound, so a stale one only loosens it)
+__shared__ float s_row_thr[kRows];
 // the CTA's block list, when it fits: every role reads it per tile
 constexpr int kListCache = 2048;
 __shared__ int s_blist[kListCache];
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
     for (int i = tid; i < 4 * kRows; i += blockDim.x) {
         (&g_row_tau[0][0])[i] = INFINITY;
         (&s_row_tq[0][0])[i] = INFINITY;
+        if (i < kRows) s_row_thr[i] = INFINITY;
     }
     tc_setup<kEpiWarps, kWide, kSmall>(S);
     fence_before();
@@ -242,34 +247,24 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
             else if (gthr_warp && lane < kTileCols / 4 + 8)
                 cp_async16(&s_gthr[warp][buf][lane - kTileCols / 4], gthr_warp + (lane - kTileCols / 4) * 4);
         };
+        float own = INFINITY;  // this list's KP-th key
         tc_epilogue_loop<kEpiWarps, kWide, kSmall>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
+            // the seed and the least KP-th key any CTA of the row tile has
+            // published (read once per tile)
+            const float tile_thr =
+                gthr_warp ? fminf(seed, order_float(reinterpret_cast<const unsigned *>(&s_gthr[warp][buf][0])[lane]))
+                          : seed;
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
-                }
+                expand32(v, &s_cnorm[warp][buf][cc * 8], kdot);
                 // the batch's least t by a depth-5 tree, against the least
                 // published KP-th key of the row (stale values only loosen it)
                 const float vmin = min32(v);
-                // the least of: every list's KP-th key, the largest of the
-                // lists' q-th keys, the seed and the shared threshold
-                float tau = fminf(key_t(lk[KP - 1]), seed), tq = -INFINITY;
-#pragma unroll
-                for (int q = 0; q < kParts; ++q) {
-                    tau = fminf(tau, g_row_tau[q][row]);
-                    tq = fmaxf(tq, s_row_tq[q][row]);
-                }
-                tau = fminf(tau, tq);
-                if (gthr_warp)  // the least KP-th key any CTA of the row tile has published
-                    tau = fminf(tau, order_float(reinterpret_cast<const unsigned *>(
-                                         &s_gthr[warp][buf][0])[lane]));
+                // the least of: this list's KP-th key, the CTA's threshold,
+                // the seed and the shared threshold
+                const float tau = fminf(fminf(own, tile_thr), s_row_thr[row]);
                 if (vmin < tau) {
                     // rare: insert this batch's candidates in column order
                     // with the one copy of the sink
@@ -286,18 +281,23 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
                             list_insert<KP>(lk, pack_tj(pick32(v, j), col0 + cc * 32 + j));
                         }
                     }
-                    g_row_tau[group][row] = key_t(lk[KP - 1]);
+                    own = key_t(lk[KP - 1]);
+                    g_row_tau[group][row] = own;
                     s_row_tq[group][row] = key_t(lk[kQ - 1]);
-                    if (gthr_warp && r0 + row < a.row_end) {
-                        // the CTA's threshold for this row, for the other CTAs
-                        float tc = key_t(lk[KP - 1]), tm = -INFINITY;
+                    // the CTA's threshold for this row: the least KP-th key
+                    // and the largest q-th key of the groups' lists
+                    float tc = own, tm = -INFINITY;
 #pragma unroll
-                        for (int q = 0; q < kParts; ++q) {
-                            tc = fminf(tc, g_row_tau[q][row]);
-                            tm = fmaxf(tm, s_row_tq[q][row]);
-                        }
-                        const unsigned o = float_order(fminf(tc, tm));
-                        if (o < published && fminf(tc, tm) < INFINITY) {
+                    for (int q = 0; q < kParts; ++q) {
+                        tc = fminf(tc, g_row_tau[q][row]);
+                        tm = fmaxf(tm, s_row_tq[q][row]);
+                    }
+                    const float cta = fminf(tc, tm);
+                    s_row_thr[row] = cta;
+                    if (gthr_warp && r0 + row < a.row_end) {
+                        // for the other CTAs of the row tile
+                        const unsigned o = float_order(cta);
+                        if (o < published && cta < INFINITY) {
                             published = o;
                             atomicMin(a.gthr + local_row, o);
                         }

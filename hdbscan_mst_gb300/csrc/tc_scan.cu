@@ -166,14 +166,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb = s_cnorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
-                }
+                expand32(v, &s_cnorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
                 // v >= t, so a batch whose least t does not beat the row's
                 // least published 4th value cannot change any list's 4 best

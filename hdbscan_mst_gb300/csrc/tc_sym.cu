@@ -260,14 +260,7 @@ __global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb = s_snorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
-                }
+                expand32(v, &s_snorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
                 const bool hit = vmin < fmaxf(thr, thr2);
                 if (!__any_sync(0xffffffffu, hit)) continue;
@@ -458,14 +451,7 @@ __global__ void __launch_bounds__(kSymThreads, 1) tc_rescan_kernel(const __grid_
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
                 tmem_ld32(tbase + cc * 32, v);
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 nb = s_rnorm[warp][buf][cc * 8 + j4];
-                    v[j4 * 4 + 0] = __fmaf_rn(kdot, v[j4 * 4 + 0], nb.x);
-                    v[j4 * 4 + 1] = __fmaf_rn(kdot, v[j4 * 4 + 1], nb.y);
-                    v[j4 * 4 + 2] = __fmaf_rn(kdot, v[j4 * 4 + 2], nb.z);
-                    v[j4 * 4 + 3] = __fmaf_rn(kdot, v[j4 * 4 + 3], nb.w);
-                }
+                expand32(v, &s_rnorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
                 // warp-uniform exit: the next batch's TMEM load is collective
                 if (!__any_sync(0xffffffffu, vmin < thr)) continue;
