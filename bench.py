@@ -90,22 +90,22 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.14 MB read, 3.14 MB written) and the
-        # pruned second pass (73.70 MB read, 22.81 MB written)
-        "bytes": 52.15e6 + 3.19e6 + 73.67e6 + 22.78e6,
+        # per step: the home pass (52.17 MB read, 2.83 MB written) and the
+        # pruned second pass (73.81 MB read, 22.82 MB written)
+        "bytes": 52.17e6 + 2.83e6 + 73.81e6 + 22.82e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "590ca1f5bb9af07ee21ed79a89081958f803911ad3855f997143c327d4bcfa49",
+        "sha256": "e4f10ecedf4f042dfbedab3358126d63285577f76b60b73d18bad8351bc1e315",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (55.00 + 53.23 MB
+        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.22 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.21 + 51.65 + 48.68 + 49.83 MB read); 0.01 MB
+        # pruned pass each (49.20 + 51.54 + 48.67 + 49.61 MB read); 0.01 MB
         # written in all
-        "bytes": (55.00 + 53.23 + 49.21 + 51.65 + 48.68 + 49.83 + 0.01) * 1e6,
+        "bytes": (54.99 + 53.22 + 49.20 + 51.54 + 48.67 + 49.61 + 0.01) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "7340beb8c0110603e29515441d5e8236312fdf392997a5ae6af5ed674b4bb4dc",
+        "sha256": "622d8592d8e4e080df391c4f4a725a5c23d3695ec1b1686d6484265f03234474",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
