@@ -284,6 +284,7 @@ static_assert(kSpatialPivots == kPrunePivots, "the pruned search bounds blocks b
 
 struct KnnBufs {
     float *Xf, *Xp, *Xlo, *xnorm, *Yf, *Yp, *Ylo, *ynorm;
+    float *ynmin;  // [m_pad / 32] least column norm per batch (tensor tile)
     float *part_key;
     int *part_idx;
     SpatialOrder order;  // pointers null when not carved
@@ -312,6 +313,7 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
         b.Ylo = lo ? c.take<float>(static_cast<size_t>(p.dk) * p.m_pad) : nullptr;
         b.ynorm = c.take<float>(p.m_pad);
     }
+    b.ynmin = lo ? c.take<float>(p.m_pad / 32) : nullptr;
     b.order = SpatialOrder{};
     b.prune = PruneBufs{};
     if (lo) {
@@ -430,6 +432,9 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
                                       b.Yp, ylo, b.ynorm, &b.st->status, &b.st->nbmax_bits, s,
                                       nullptr, Yh16, Yl16, amax, &b.st->e0, invY, yhi));
     }
+    // the least column norm of every 32 columns: the tensor tile's floor of
+    // a batch's t
+    if (tensor) LAUNCH(K_PACK, s, launch_norm_min32(b.ynorm, p.m_pad, b.ynmin, s));
     TcOperands ops{};
     if (f16)
         ops = TcOperands{Xh16, Xl16, Yh16, Yl16};
@@ -456,6 +461,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
         ta.Xf = b.Xf;
         ta.Yf = b.Yf;
         ta.ynorm = b.ynorm;
+        ta.ynmin = b.ynmin;
         ta.ldx = p.n_pad;
         ta.ldy = p.m_pad;
         ta.dk = p.dk;
@@ -622,6 +628,7 @@ MstPlan make_mst_plan(int64_t n, int d, int L) {
 
 struct MstBufs {
     float *Xf, *Xp, *Xhi, *Xlo, *Xs, *norm, *Xa, *act_core, *act_norm, *col_core, *col_norm;
+    float *nmin;  // [n_pad / 32] least column norm per batch of the tensor scans
     float *Xs_hi, *Xs_lo, *Xa_hi, *Xa_lo;  // point-major grouped columns / active rows
     int *act_comp, *act_idx, *comp, *parent, *root_of, *perm, *col_comp, *start, *act_start;
     int *counters;  // [4n + 8]: size, act_size, cursor, act_cursor, totals (zeroed per round)
@@ -659,6 +666,7 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
     // prefetches them a whole tile at a time (padding entries never rank)
     b.col_core = c.take<float>(p.n_pad);
     b.col_norm = c.take<float>(p.n_pad);
+    b.nmin = c.take<float>(p.n_pad / 32);
     b.perm = c.take<int>(p.n_pad);
     b.col_comp = c.take<int>(n);
     b.start = c.take<int>(n);
@@ -1065,6 +1073,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             int2 *pairs = reinterpret_cast<int2 *>(b.part_key);
             LAUNCH(K_GATHER, s, launch_sym_prepare(N, np, np_pad, b.act_comp, b.ub, theta,
                                                    b.act_norm, tile_meta, s));
+            LAUNCH(K_GATHER, s, launch_norm_min32(b.act_norm, np_pad, b.nmin, s));
             SymArgs ya{};
             ya.np = np;
             ya.ld = np_pad;
@@ -1073,6 +1082,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             ya.core = b.act_core;
             ya.comp = b.act_comp;
             ya.norm = b.act_norm;
+            ya.nmin = b.nmin;
             ya.comp_start = b.act_start;
             ya.comp_size = act_size;
             ya.tile_meta = tile_meta;
@@ -1134,6 +1144,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             if (tensor) {
                 LAUNCH(K_GATHER, s, launch_gather_points(N, static_cast<int>(p.n_pad), dkw, b.perm,
                                                          op_hi, op_lo, b.Xs_hi, b.Xs_lo, s));
+                LAUNCH(K_GATHER, s, launch_norm_min32(b.col_norm, p.n_pad, b.nmin, s));
                 LAUNCH(K_GATHER, s, launch_gather_points(na, na_pad, dkw, b.act_idx, op_hi, op_lo,
                                                          b.Xa_hi, b.Xa_lo, s));
             } else {
@@ -1152,6 +1163,7 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
             sa.ldx = p.n_pad;
             sa.col_orig = b.perm;
             sa.col_norm = b.col_norm;
+            sa.col_nmin = b.nmin;
             sa.col_core = b.col_core;
             sa.col_comp = b.col_comp;
             sa.comp_start = b.start;

@@ -22,6 +22,9 @@ namespace hdbmst {
 // two-part FP16 operands of the tensor-core tile, point-major [n_pad][dk / 2]
 // 32-bit words (two halves each, f16_split with the scale of *amax_bits);
 // *e0_out (nullable) then receives the form's absolute error part, rounded up.
+// The least squared norm of each 32 consecutive entries of norm[n_pad]
+// (n_pad a multiple of 32) into nmin[n_pad / 32].
+cudaError_t launch_norm_min32(const float *norm, int64_t n_pad, float *nmin, cudaStream_t s);
 cudaError_t launch_pack(const float *X, int64_t ld, int n, int d, int n_pad, int dk, float *Xf,
                         float *Xp, float *Xlo, float *norm, unsigned *status,
                         unsigned *nbmax_bits, cudaStream_t s, const int *perm = nullptr,
@@ -118,6 +121,7 @@ struct KnnTileArgs {
     const float *Xf;     // [dk][ldx] query rows, feature-major, padded
     const float *Yf;     // [dk][ldy] searched columns, feature-major, padded
     const float *ynorm;  // [ldy] squared norms, +inf past the last column
+    const float *ynmin;  // [ldy / 32] least squared norm of each 32 columns (tensor tiles)
     int64_t ldx, ldy;
     int dk;
     int row_base;        // first query row of this chunk
@@ -273,6 +277,7 @@ struct ScanArgs {
     int64_t ldx;
     const int *col_orig;    // [ldx] point index of each column (entries past n unused)
     const float *col_norm;  // [ldx] |b|^2, +inf past the last point
+    const float *col_nmin;  // [ldx / 32] least |b|^2 of each 32 columns (tensor scan)
     const float *col_core;  // [ldx] (entries past n unused)
     const int *col_comp;    // [n]
     const int *comp_start;  // [n] first column of each component label
@@ -325,6 +330,7 @@ struct SymArgs {
     const float *core;       // [ld] core distance by position
     const int *comp;         // [ld] component by position
     const float *norm;       // [ld] |p|^2 by position, +inf past np
+    const float *nmin;       // [ld / 32] least |p|^2 of each 32 positions
     const int *comp_start;   // [n] first position of each component label
     const int *comp_size;    // [n] positions of each component label
     const int4 *tile_meta;   // [ld / 64] (component or -1, largest starting bound bits, 0, 0)

@@ -248,4 +248,23 @@ cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaSt
     return cudaGetLastError();
 }
 
+// The least squared norm of every 32 consecutive points (the tensor-core
+// tiles' batches of columns), from norms padded to a multiple of 32 (+inf
+// past the last point): one warp per batch.
+__global__ void norm_min32_kernel(const float *__restrict__ norm, int64_t n_pad,
+                                  float *__restrict__ nmin) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n_pad) return;  // whole warps: n_pad is a multiple of 32
+    // non-negative floats (and +inf) order like their bits
+    const unsigned m = __reduce_min_sync(0xffffffffu, __float_as_uint(norm[i]));
+    if ((threadIdx.x & 31) == 0) nmin[i >> 5] = __uint_as_float(m);
+}
+
+cudaError_t launch_norm_min32(const float *norm, int64_t n_pad, float *nmin, cudaStream_t s) {
+    if (n_pad <= 0) return cudaSuccess;
+    if (n_pad % 32 != 0) return cudaErrorInvalidValue;
+    norm_min32_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, s>>>(norm, n_pad, nmin);
+    return cudaGetLastError();
+}
+
 }  // namespace hdbmst

@@ -224,6 +224,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// tmem_ld32, plus the largest of the 32 values: the load's own max reduction
+// (tcgen05.ld.red; measured on GB300 to return exactly the maximum of the
+// values the thread loads), so a batch can be judged without a 31-step tree.
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    float m;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+        "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    return m;
+}
+
+// A lower bound of every t = fma(kdot, acc_j, nb_j) of a batch (kdot < 0):
+// amax the batch's largest accumulated dot product, nmin its least column
+// norm.  kdot amax + nmin <= kdot acc_j + nb_j exactly, and rounding down
+// then to nearest keeps the order, so the bound never exceeds a computed t:
+// a batch whose bound is at or above a row's threshold has no t below it.
+__device__ __forceinline__ float batch_t_floor(float kdot, float amax, float nmin) {
+    return __fmaf_rd(kdot, amax, nmin);
+}
+
 // 32 consecutive TMEM columns of this thread's lane from registers; the warp
 // writes lanes 32 (w % 4) ...  tmem_wait_st() waits for the warp's stores.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {

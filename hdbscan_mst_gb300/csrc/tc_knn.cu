@@ -80,6 +80,7 @@ constexpr int kListCache = 2048;
 __shared__ int s_blist[kListCache];
 constexpr int kMaxEpiWarps = 12;
 __shared__ float4 s_cnorm[kMaxEpiWarps][2][kTileCols / 4];  // per warp: two tiles' column norms
+__shared__ float2 s_nmin[kMaxEpiWarps][2];  // per warp, two tiles: each batch's least column norm
 // per warp, two tiles: its 32 rows' thresholds shared across CTAs (ordered float bits)
 __shared__ uint4 s_gthr[kMaxEpiWarps][2][8];
 
@@ -246,6 +247,8 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
             if (lane < kTileCols / 4) cp_async16(&s_cnorm[warp][buf][lane], a.ynorm + col0 + lane * 4);
             else if (gthr_warp && lane < kTileCols / 4 + 8)
                 cp_async16(&s_gthr[warp][buf][lane - kTileCols / 4], gthr_warp + (lane - kTileCols / 4) * 4);
+            else if (lane == 31)
+                cp_async8(&s_nmin[warp][buf], a.ynmin + (col0 >> 5));
         };
         float own = INFINITY;  // this list's KP-th key
         tc_epilogue_loop<kEpiWarps, kWide, kSmall>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
@@ -257,14 +260,18 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
                 float v[32];
-                tmem_ld32(tbase + cc * 32, v);
+                const float amax = tmem_ld32_max(tbase + cc * 32, v);
+                // the least of: this list's KP-th key, the CTA's threshold,
+                // the seed and the shared threshold
+                const float tau = fminf(fminf(own, tile_thr), s_row_thr[row]);
+                // most batches end here: their floor of t (the largest dot
+                // product against the least norm) reaches every row's threshold
+                const float nmin = cc ? s_nmin[warp][buf].y : s_nmin[warp][buf].x;
+                if (!__any_sync(0xffffffffu, batch_t_floor(kdot, amax, nmin) < tau)) continue;
                 expand32(v, &s_cnorm[warp][buf][cc * 8], kdot);
                 // the batch's least t by a depth-5 tree, against the least
                 // published KP-th key of the row (stale values only loosen it)
                 const float vmin = min32(v);
-                // the least of: this list's KP-th key, the CTA's threshold,
-                // the seed and the shared threshold
-                const float tau = fminf(fminf(own, tile_thr), s_row_thr[row]);
                 if (vmin < tau) {
                     // rare: insert this batch's candidates in column order
                     // with the one copy of the sink

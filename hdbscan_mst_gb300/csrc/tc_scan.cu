@@ -45,6 +45,7 @@ __shared__ float s_row_thr[kParts][kRows];  // per group and row: its 4th kept v
 __shared__ int s_rcomp[kRows];
 // per warp, two tiles: the columns' norms
 __shared__ float4 s_cnorm[kEpiWarps][2][kTileCols / 4];
+__shared__ float2 s_cnmin[kEpiWarps][2];  // per warp, two tiles: each batch's least norm
 
 __device__ __forceinline__ void keep_insert(unsigned long long (&k)[kKeep], unsigned long long key,
                                             float &dropped) {
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
         const auto prefetch = [&](int col0, int buf) {
             static_assert(kTileCols == 64, "one 16-byte copy per lane");
             if (lane < 16) cp_async16(&s_cnorm[warp][buf][lane], a.col_norm + col0 + lane * 4);
+            else if (lane == 16) cp_async8(&s_cnmin[warp][buf], a.col_nmin + (col0 >> 5));
         };
         tc_epilogue_loop<kEpiWarps>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
             // the other groups' published 4th values, once per tile (a stale
@@ -165,12 +167,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(const __grid_c
                 // warp; the skip must be warp-uniform: tcgen05.ld is collective
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
-                tmem_ld32(tbase + cc * 32, v);
+                const float amax = tmem_ld32_max(tbase + cc * 32, v);
+                // v >= t, so a batch whose least t does not beat the row's
+                // least published 4th value cannot change any list's 4 best;
+                // most batches are ruled out by the floor of their t alone
+                const float thr = fminf(key_v(keys[kKeep - 1]), thr_tile);
+                const float nmin = cc ? s_cnmin[warp][buf].y : s_cnmin[warp][buf].x;
+                if (!__any_sync(0xffffffffu, batch_t_floor(kdot, amax, nmin) < thr)) continue;
                 expand32(v, &s_cnorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
-                // v >= t, so a batch whose least t does not beat the row's
-                // least published 4th value cannot change any list's 4 best
-                const float thr = fminf(key_v(keys[kKeep - 1]), thr_tile);
                 if (vmin < thr) {
                     const uint32_t own =
                         bhi > blo ? ((bhi == 32 ? 0u : (1u << bhi)) - (1u << blo)) : 0u;

@@ -78,6 +78,7 @@ struct TcSymParams {
 
 // per warp, two tiles: the columns' norms and core distances, the tile's record
 __shared__ float4 s_snorm[kEpiWarps][2][kTileCols / 4];
+__shared__ float2 s_snmin[kEpiWarps][2];  // per warp, two tiles: each batch's least norm
 __shared__ float4 s_score[kEpiWarps][2][kTileCols / 4];
 __shared__ int4 s_smeta[kEpiWarps][2];
 constexpr int kListCache = 2048;  // list entries kept in shared memory
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
             if (lane < 16) cp_async16(&s_snorm[warp][buf][lane], a.norm + col0 + lane * 4);
             else cp_async16(&s_score[warp][buf][lane - 16], a.core + col0 + (lane - 16) * 4);
             if (lane == 0) cp_async16(&s_smeta[warp][buf], a.tile_meta + col0 / kTileCols);
+            if (lane == 1) cp_async8(&s_snmin[warp][buf], a.nmin + (col0 >> 5));
         };
         const auto tau_of = [&](float t) {
             return (!valid || ca > t) ? -INFINITY : sym_tau(t, na, c, e0, a.d);
@@ -259,7 +261,13 @@ __global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
                 // tcgen05.ld is warp-collective: skip only what is own for the whole warp
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
-                tmem_ld32(tbase + cc * 32, v);
+                const float amax = tmem_ld32_max(tbase + cc * 32, v);
+                // nearly every batch ends here: the floor of its t (the
+                // largest dot product against the least norm) reaches the
+                // row's filter in every row of the warp
+                const float nmin = cc ? s_snmin[warp][buf].y : s_snmin[warp][buf].x;
+                if (!__any_sync(0xffffffffu, batch_t_floor(kdot, amax, nmin) < fmaxf(thr, thr2)))
+                    continue;
                 expand32(v, &s_snorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
                 const bool hit = vmin < fmaxf(thr, thr2);

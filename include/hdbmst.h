@@ -198,8 +198,10 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
  *    count (round_up(d, 32) up to 192, round_up(d, 16) beyond), the need is
  *    about c * dk * (round_up(n, 128) + round_up(m, 128)) bytes for the packed
  *    copies, c = 12 when d <= 192 (the tensor-core engine's extra low parts)
- *    and 8 otherwise (half that when Y is X), plus 4 bytes per query and at
- *    least 64 KiB for the neighbour candidates (128 KiB when k > 12).
+ *    and 8 otherwise (half that when Y is X), plus 4 bytes per query, 4
+ *    bytes per 32 reference points when d <= 192 (each column batch's least
+ *    norm) and at least 64 KiB for the neighbour candidates (128 KiB when
+ *    k > 12).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine; it
  *    synchronises the stream once at the end, as hdbmst_knn does.
  *
