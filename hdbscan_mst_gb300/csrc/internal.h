@@ -459,9 +459,9 @@ cudaError_t launch_relabel(int n, int *comp, const int *root_of, const int *pare
 
 // ---------------------------------------------------------------- sort.cu
 // Sort N edges by (w, lo, hi) ascending and write (lo, hi) pairs and weights.
-// tmp buffers hold N entries each; hist holds sort_hist_entries(N) entries.
+// tmp buffers hold N entries each; hist holds sort_hist_entries(N) entries
+// (three rotating sets of per-tile digit histograms).
 size_t sort_hist_entries(int N);
-int sort_launches(int N, int index_bits);
 cudaError_t sort_edges(int N, int index_bits, unsigned *w, int *lo, int *hi, unsigned *w2,
                        int *lo2, int *hi2, unsigned *hist, int32_t *out_edges, float *out_w,
                        cudaStream_t s, void (*before)(int, cudaStream_t),
