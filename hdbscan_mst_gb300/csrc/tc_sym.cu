@@ -253,21 +253,28 @@ __global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
             float thr2 = kb < kTileCols ? tau_of(th2) : thr;
             float *nbs = reinterpret_cast<float *>(&s_snorm[warp][buf][0]);
             const float *cbs = reinterpret_cast<const float *>(&s_score[warp][buf][0]);
+            // nearly every tile ends here: the floor of each batch's t (its
+            // largest dot product against its least norm) reaches the row's
+            // filter in every row of the warp; both batches judged after one
+            // wait (a batch that passes is loaded again: the accumulator is
+            // held until the tile is done)
+            float amax0, amax1;
+            tmem_ld64_max2(tbase, amax0, amax1);
+            const float2 nm2 = s_snmin[warp][buf];
+            const unsigned pass =
+                (__any_sync(0xffffffffu, batch_t_floor(kdot, amax0, nm2.x) < fmaxf(thr, thr2)) ? 1u : 0u) |
+                (__any_sync(0xffffffffu, batch_t_floor(kdot, amax1, nm2.y) < fmaxf(thr, thr2)) ? 2u : 0u);
+            if (pass == 0u) return;
 #pragma unroll 1
             for (int cc = 0; cc < kTileCols / 32; ++cc) {
+                if (!((pass >> cc) & 1u)) continue;
                 const int cb0 = col0 + cc * 32;
                 const int blo = min(max(own_lo - cb0, 0), 32);
                 const int bhi = min(max(own_hi - cb0, 0), 32);
                 // tcgen05.ld is warp-collective: skip only what is own for the whole warp
                 if (__all_sync(0xffffffffu, blo == 0 && bhi == 32)) continue;
                 float v[32];
-                const float amax = tmem_ld32_max(tbase + cc * 32, v);
-                // nearly every batch ends here: the floor of its t (the
-                // largest dot product against the least norm) reaches the
-                // row's filter in every row of the warp
-                const float nmin = cc ? s_snmin[warp][buf].y : s_snmin[warp][buf].x;
-                if (!__any_sync(0xffffffffu, batch_t_floor(kdot, amax, nmin) < fmaxf(thr, thr2)))
-                    continue;
+                tmem_ld32(tbase + cc * 32, v);
                 expand32(v, &s_snorm[warp][buf][cc * 8], kdot);
                 const float vmin = min32(v);
                 const bool hit = vmin < fmaxf(thr, thr2);
