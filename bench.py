@@ -90,22 +90,22 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.17 MB read, 2.83 MB written) and the
-        # pruned second pass (73.81 MB read, 22.82 MB written)
-        "bytes": 52.17e6 + 2.83e6 + 73.81e6 + 22.82e6,
+        # per step: the home pass (52.20 MB read, 2.90 MB written) and the
+        # pruned second pass (73.86 MB read, 23.41 MB written)
+        "bytes": 52.20e6 + 2.90e6 + 73.86e6 + 23.41e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "e4f10ecedf4f042dfbedab3358126d63285577f76b60b73d18bad8351bc1e315",
+        "sha256": "351b9e50b30675aa4b908570be710811a175b034414f0ab9935c3a51419d2400",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (54.99 + 53.22 MB
+        # per step: the one-sided scans of rounds 1 and 2 (55.02 + 53.27 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.20 + 51.54 + 48.67 + 49.61 MB read); 0.01 MB
-        # written in all
-        "bytes": (54.99 + 53.22 + 49.20 + 51.54 + 48.67 + 49.61 + 0.01) * 1e6,
+        # pruned pass each (49.22 + 51.50 + 48.73 + 49.71 MB read); under
+        # 0.01 MB written in all
+        "bytes": (55.02 + 53.27 + 49.22 + 51.50 + 48.73 + 49.71 + 0.004) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "622d8592d8e4e080df391c4f4a725a5c23d3695ec1b1686d6484265f03234474",
+        "sha256": "d2b128dc2173c4f74ca59176bd29afa15ae404542fd50fb934c94a0af8eeb589",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
