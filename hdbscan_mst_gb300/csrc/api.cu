@@ -529,6 +529,9 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             q.chunk_cap = chunk_cap;
             q.slab_base = 1;
             q.seed = b.part_key;
+            q.seed_idx = b.part_idx;
+            q.home_lo = b.prune.home_lo;
+            q.nh = nh;
             q.gthr = b.prune.gthr;
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, ops, p.n_pad, p.m_pad, row_tiles,
                                                 kPruneChunks, s));

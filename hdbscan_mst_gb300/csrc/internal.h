@@ -145,6 +145,13 @@ struct KnnTileArgs {
     const int *bcount;
     int blist_count, blist_stride, chunk_cap, slab_base;
     const float *seed;  // nullable: sorted lists of slab 0 (their KP-th key: a first threshold)
+    // nullable (tensor tile, pruned pass): the columns of slab 0's lists; with
+    // them every epilogue group's list starts as the row's home list, and the
+    // columns of the home range (blocks home_lo[tile] .. + nh - 1) are taken
+    // out again before the pass writes its lists (slab 0 holds them)
+    const int *seed_idx;
+    const int *home_lo;
+    int nh;
     // nullable: per row of the chunk, the least KP-th key any CTA of the row's
     // tile holds (float_order bits), read once per tile and lowered with
     // atomicMin: the chunks of one row tile share their thresholds

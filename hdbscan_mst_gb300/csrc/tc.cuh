@@ -225,8 +225,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // tmem_ld32, plus the largest of the 32 values: the load's own max reduction
-// (tcgen05.ld.red; measured on GB300 to return exactly the maximum of the
-// values the thread loads), so a batch can be judged without a 31-step tree.
+// (tcgen05.ld.red, whose extra result is the reduction of the values the
+// thread loads; an in-bounds check on GB300 with known values confirmed the
+// exact maximum), so a batch can be judged without a 31-step tree.  The
+// batch floor's decisions change results if this ever returned less than
+// the maximum, so the full-size parity tests exercise it on every batch.
 __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     float m;

@@ -131,6 +131,34 @@ __device__ __forceinline__ void list_merge(unsigned long long (&k)[KP],
             }
 }
 
+// k sorted ascending (a bitonic network; no key needs to be distinct).
+template <int KP>
+__device__ __forceinline__ void list_sort(unsigned long long (&k)[KP]) {
+#pragma unroll
+    for (int w = 2; w <= KP; w <<= 1)
+#pragma unroll
+        for (int h = w >> 1; h > 0; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < KP; ++i) {
+                const int l = i ^ h;
+                if (l > i) {
+                    const bool up = (i & w) == 0;
+                    const unsigned long long lo = min(k[i], k[l]), hi = max(k[i], k[l]);
+                    k[i] = up ? lo : hi;
+                    k[l] = up ? hi : lo;
+                }
+            }
+}
+
+// k[i] for a run-time i (a chain of selects: the list stays in registers)
+template <int KP>
+__device__ __forceinline__ unsigned long long list_at(const unsigned long long (&k)[KP], int i) {
+    unsigned long long r = k[0];
+#pragma unroll
+    for (int p = 1; p < KP; ++p) r = i == p ? k[p] : r;
+    return r;
+}
+
 // The 16 least of a 32-column batch (columns in mask, the others absent)
 // merged into a 16-long list: a bitonic sort of the batch's 32 keys, then
 // list_merge with its first 16.
@@ -231,12 +259,30 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
         unsigned long long lk[KP];  // the row's list, sorted (pack_tj)
 #pragma unroll
         for (int p = 0; p < KP; ++p) lk[p] = pack_tj(INFINITY, INT_MAX);
+        // Group g's q_g-th key (q_g = KP / groups, one more for the first
+        // KP % groups groups: the q_g add up to KP): once every group holds
+        // q_g keys, the largest of those keys has at least KP keys of the
+        // disjoint lists at or below it.
+        const int qg = KP / kParts + (group < KP % kParts ? 1 : 0);
+        // The pruned pass: the groups' lists start as the row's home list
+        // dealt out (entries g, g + groups, ... to group g: q_g of them), so
+        // that bound is the home list's KP-th key from the first tile on and
+        // drops with every insertion.
+        const bool seeded = a.seed_idx != nullptr;
+        if (seeded && r0 + row < a.row_end) {
+            const int64_t so = static_cast<int64_t>(row_tile * kRows + row) * KP;
+#pragma unroll
+            for (int p = 0; p < KP; ++p) {
+                const int e = group + p * kParts;
+                if (e < KP) lk[p] = pack_tj(a.seed[so + e], a.seed_idx[so + e]);
+            }
+            s_row_tq[group][row] = key_t(list_at(lk, qg - 1));
+        }
         // a first threshold: the KP-th key an earlier pass already holds for
         // the row (a candidate at or above it cannot reach the merged top KP)
         float seed = INFINITY;
         if (a.seed && r0 + row < a.row_end)
             seed = a.seed[static_cast<int64_t>(row_tile * kRows + row) * KP + KP - 1];
-        constexpr int kQ = (KP + kParts - 1) / kParts;
         unsigned published = 0xffffffffu;  // the least threshold this thread put in gthr
         // t = |y|^2 - 2 x.y; the FP16 products carry the set's scale 2^2e
         const float kdot = kF16 ? -ldexpf(2.f, -2 * f16_scale_exp(*a.amax_bits)) : -2.f;
@@ -250,7 +296,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
             else if (lane == 31)
                 cp_async8(&s_nmin[warp][buf], a.ynmin + (col0 >> 5));
         };
-        float own = INFINITY;  // this list's KP-th key
+        float own = key_t(lk[KP - 1]);  // this list's KP-th key
         tc_epilogue_loop<kEpiWarps, kWide, kSmall>(S, seq, prefetch, [&](uint32_t tbase, int col0, int buf) {
             // the seed and the least KP-th key any CTA of the row tile has
             // published (read once per tile)
@@ -290,9 +336,9 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
                     }
                     own = key_t(lk[KP - 1]);
                     g_row_tau[group][row] = own;
-                    s_row_tq[group][row] = key_t(lk[kQ - 1]);
+                    s_row_tq[group][row] = key_t(list_at(lk, qg - 1));
                     // the CTA's threshold for this row: the least KP-th key
-                    // and the largest q-th key of the groups' lists
+                    // and the largest q_g-th key of the groups' lists
                     float tc = own, tm = -INFINITY;
 #pragma unroll
                     for (int q = 0; q < kParts; ++q) {
@@ -312,6 +358,16 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
                 }
             }
         });
+        // the home range's columns leave the lists again (slab 0 holds them)
+        if (seeded) {
+            const int h0 = a.home_lo[row_tile];
+#pragma unroll
+            for (int p = 0; p < KP; ++p) {
+                const int blk = key_j(lk[p]) / kCols;
+                if (blk >= h0 && blk < h0 + a.nh) lk[p] = pack_tj(INFINITY, INT_MAX);
+            }
+            list_sort<KP>(lk);
+        }
         // merge the row's lists: the ring is idle now, other groups park there
         if (kParts > 1) {
             float *pk = reinterpret_cast<float *>(base);
