@@ -251,39 +251,38 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     const int leader = (threadIdx.x & 31) & ~(KP - 1);
 
     // 1. Merge the sorted partial lists of the splits into the KP best by
-    //    (t, index); one lane walks the list heads.
+    //    (t, index), the KP lanes of the row together: lane p holds entry p
+    //    of the running list; a further list is merged by pairing entry p
+    //    with the other's entry KP - 1 - p (the KP lesser of the pairs are
+    //    the KP least of both, as a bitonic sequence) and a half-cleaner
+    //    cascade over the lanes.  Keys are (t, index) as order-preserving
+    //    bits (t + 0 turns -0 into +0, which key_less treats alike).
     float A = INFINITY;
     const int slabs = (a.tile_slabs && active) ? min(a.splits, a.tile_slabs[local / kBM]) : a.splits;
-    if (active && gl == 0) {
-        int head[8];
+    const auto load_key = [&](int s, int pos) -> unsigned long long {
+        const int64_t o = (static_cast<int64_t>(s) * a.chunk_rows_pad + local) * KP + pos;
+        const float t = __fadd_rn(a.part_key[o], 0.f);
+        return (static_cast<unsigned long long>(float_order(t)) << 32) |
+               static_cast<unsigned>(a.part_idx[o]);
+    };
+    constexpr unsigned long long kEmpty = 0xFF8000007FFFFFFFull;  // (+inf, INT_MAX)
+    unsigned long long mk = active ? load_key(0, gl) : kEmpty;
+    // every lane of the warp runs the same merges (the shuffles)
+    const int slabs_w = __reduce_max_sync(0xffffffffu, active ? slabs : 0);
+    for (int sl = 1; sl < slabs_w; ++sl) {
+        const unsigned long long o = (active && sl < slabs) ? load_key(sl, KP - 1 - gl) : kEmpty;
+        mk = min(mk, o);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) head[s] = 0;
-        for (int p = 0; p < KP; ++p) {
-            float bt = INFINITY;
-            int bj = INT_MAX, bs = -1;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                if (s < slabs && head[s] < KP) {
-                    const int64_t o = (static_cast<int64_t>(s) * a.chunk_rows_pad + local) * KP + head[s];
-                    const float t = a.part_key[o];
-                    const int j = a.part_idx[o];
-                    if (key_less(t, j, bt, bj)) {
-                        bt = t;
-                        bj = j;
-                        bs = s;
-                    }
-                }
-            }
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                if (s == bs) ++head[s];
-            sel_t[group * KP + p] = bt;
-            sel_j[group * KP + p] = bj;
+        for (int h = KP / 2; h > 0; h >>= 1) {
+            const unsigned long long q = __shfl_xor_sync(0xffffffffu, mk, h);
+            mk = (gl & h) ? max(mk, q) : min(mk, q);
         }
-        A = sel_t[group * KP + KP - 1];
     }
+    sel_t[group * KP + gl] = order_float(static_cast<unsigned>(mk >> 32));
+    sel_j[group * KP + gl] = static_cast<int>(mk & 0xffffffffu);
+    if (gl == KP - 1) A = sel_t[group * KP + KP - 1];
     __syncwarp();
-    A = __shfl_sync(0xffffffffu, A, leader);
+    A = __shfl_sync(0xffffffffu, A, leader + KP - 1);
 
     // 2. Exact distance of every kept candidate that can still reach the top
     //    k.  The first k by t each have a true squared distance of at most
