@@ -208,12 +208,18 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         const float eps = static_cast<float>((a.d + 8) * 5.9604644775390625e-8);
         const float lo_f = __fsub_rd(1.f, eps), hi_f = __fadd_ru(1.f, eps);
         float A = INFINITY, Bv = -INFINITY;
+        // every row of the tile is in the array (n_pad rows), so the loads
+        // need no branch and many are in flight; rows past the last point
+        // (u < 0) are read and not used
+        const float *pd = pdSX + static_cast<int64_t>(a.row_base + rt * kBM) * P + tid;
+#pragma unroll 16
         for (int r = 0; r < kBM; ++r) {
             const float u = s_ub[r];
-            if (u < 0.f) continue;
-            const float dx = pdSX[static_cast<int64_t>(a.row_base + rt * kBM + r) * P + tid];
-            A = fminf(A, __fsub_rd(__fmul_rd(dx, lo_f), u));
-            Bv = fmaxf(Bv, __fadd_ru(__fmul_ru(dx, hi_f), u));
+            const float dx = pd[static_cast<int64_t>(r) * P];
+            if (u >= 0.f) {
+                A = fminf(A, __fsub_rd(__fmul_rd(dx, lo_f), u));
+                Bv = fmaxf(Bv, __fadd_ru(__fmul_ru(dx, hi_f), u));
+            }
         }
         s_A[tid] = A;
         s_B[tid] = Bv;
