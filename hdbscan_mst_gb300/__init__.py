@@ -117,6 +117,8 @@ def _load():
     L.hdbmst_test_set_tc_hooks.argtypes = [ctypes.c_uint64, i32]
     L.hdbmst_test_set_tc_hooks.restype = i32
     L.hdbmst_test_set_mst_caps.argtypes = [i32, i32]
+    L.hdbmst_test_tmem_max.argtypes = [ctypes.c_void_p]
+    L.hdbmst_test_tmem_max.restype = i32
     L.hdbmst_test_set_mst_caps.restype = None
     _lib = L
     return L
@@ -465,6 +467,18 @@ def test_set_tc_hooks(wait_ns: int = 0, withhold_first_slab: bool = False) -> No
     ``test_set_tc_hooks()`` restores the defaults."""
     _check(_load().hdbmst_test_set_tc_hooks(int(wait_ns), 1 if withhold_first_slab else 0),
            "hdbmst_test_set_tc_hooks")
+
+
+def test_tmem_max():
+    """Hardware check the tensor-core tiles' batch floor rests on (current
+    device): a [128, 68] float32 tensor - per TMEM lane its 64 stored values
+    read back, then the maxima of columns 0..31 and 32..63 from the
+    one-batch and from the two-batch max-reducing loads (the stored values
+    are defined in include/hdbmst.h, hdbmst_test_tmem_max)."""
+    import torch
+    out = torch.empty((128, 68), dtype=torch.float32, device="cuda")
+    _check(_load().hdbmst_test_tmem_max(ctypes.c_void_p(out.data_ptr())), "hdbmst_test_tmem_max")
+    return out
 
 
 def test_set_mst_caps(max_rounds: int = 0, max_jump_launches: int = 0) -> None:

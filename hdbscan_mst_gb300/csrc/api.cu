@@ -1472,6 +1472,12 @@ hdbmst_status hdbmst_test_set_tc_hooks(uint64_t wait_ns, int withhold_first_slab
     return e == cudaSuccess ? HDBMST_OK : cuda_fail(e);
 }
 
+hdbmst_status hdbmst_test_tmem_max(float *out) {
+    if (!out) return HDBMST_ERR_ARG;
+    if (cudaSuccess != tc_tmem_max_probe(out, nullptr)) return HDBMST_ERR_CUDA;
+    return cudaSuccess == cudaStreamSynchronize(nullptr) ? HDBMST_OK : HDBMST_ERR_CUDA;
+}
+
 void hdbmst_test_set_mst_caps(int max_rounds, int max_jump_launches) {
     g_test_max_rounds = std::max(0, max_rounds);
     g_test_jump_launches = std::max(0, max_jump_launches);

@@ -178,6 +178,9 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int
 // Test hooks of the tensor-core tiles' failure path, one per translation unit
 // (tc.cuh: set_test_hooks), on the current device.
 cudaError_t tc_knn_test_hooks(unsigned long long wait_ns, int withhold);
+// One CTA: 64 known values per row of 128 TMEM lanes stored and read back
+// with the tiles' max-reducing loads; out holds 128 x 68 floats.
+cudaError_t tc_tmem_max_probe(float *out, cudaStream_t s);
 cudaError_t tc_scan_test_hooks(unsigned long long wait_ns, int withhold);
 cudaError_t tc_sym_test_hooks(unsigned long long wait_ns, int withhold);
 // Padded feature count: whole 32-feature slabs up to 64 (the tensor-core tile's

@@ -450,6 +450,59 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int
     return cudaErrorInvalidValue;
 }
 
+// Check of the TMEM loads' max reduction that the tiles' batch floor rests
+// on: one CTA of 128 threads allocates 64 TMEM columns, each warp stores 64
+// known values per row of its 32 lanes, and the row's values and maxima come
+// back as the tiles read them (tmem_ld32_max per 32-column batch, and
+// tmem_ld64_max2 for both).  out[row * 68 + c]: the 64 values, then the two
+// batch maxima of each form.  The values: ((37 r + 11 c + 5 (r ^ c)) mod 97 -
+// 48) * 0.75, except 100 + r at c = r mod 64 and -200 - r at c = (r + 7) mod
+// 64 (a unique largest and least value per row).
+__global__ void __launch_bounds__(128) tmem_max_probe_kernel(float *out) {
+    __shared__ uint32_t s_base;
+    const int warp = threadIdx.x >> 5, row = threadIdx.x;
+    if (warp == 0) tmem_alloc(&s_base, 64);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t taddr = s_base + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int c = 32 * h + j;
+            float x = static_cast<float>((37 * row + 11 * c + 5 * (row ^ c)) % 97 - 48) * 0.75f;
+            if (c == row % 64) x = 100.f + static_cast<float>(row);
+            if (c == (row + 7) % 64) x = -200.f - static_cast<float>(row);
+            w[j] = x;
+        }
+        tmem_st32(taddr + 32 * h, w);
+    }
+    tmem_wait_st();
+    float v[32];
+    const float m0 = tmem_ld32_max(taddr, v);
+    for (int j = 0; j < 32; ++j) out[row * 68 + j] = v[j];
+    const float m1 = tmem_ld32_max(taddr + 32, v);
+    for (int j = 0; j < 32; ++j) out[row * 68 + 32 + j] = v[j];
+    float p0, p1;
+    tmem_ld64_max2(taddr, p0, p1);
+    out[row * 68 + 64] = m0;
+    out[row * 68 + 65] = m1;
+    out[row * 68 + 66] = p0;
+    out[row * 68 + 67] = p1;
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) tmem_free(s_base, 64);
+}
+
+cudaError_t tc_tmem_max_probe(float *out, cudaStream_t s) {
+    if (!out) return cudaErrorInvalidValue;
+    tmem_max_probe_kernel<<<1, 128, 0, s>>>(out);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_knn_test_hooks(unsigned long long wait_ns, int withhold) {
     return tc::set_test_hooks(wait_ns, withhold);
 }

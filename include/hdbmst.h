@@ -428,6 +428,23 @@ int64_t hdbmst_set_scan_list_cap(int64_t cap);
  *   returns HDBMST_ERR_NOCONVERGE.
  */
 hdbmst_status hdbmst_test_set_tc_hooks(uint64_t wait_ns, int withhold_first_slab);
+
+/*
+ * hdbmst_test_tmem_max: on the CURRENT device, checks the tensor-memory
+ *   load with a max reduction that the tensor-core tiles use to rule out a
+ *   32-column batch by the floor of its t (page "Kilosort4 clustering and
+ *   matching", "k-nearest neighbours are a matrix product": the batch's
+ *   least t is at least its least column norm minus twice its largest dot
+ *   product).  One CTA stores 64 known values in each of 128 TMEM lanes and
+ *   reads them back as the tiles do; out (device, 128 x 68 floats, row-major)
+ *   receives per lane the 64 values read back, then the maxima of columns
+ *   0..31 and 32..63 from the one-batch load and from the two-batch load.
+ *   The values: ((37 r + 11 c + 5 (r xor c)) mod 97 - 48) * 0.75 for lane r and
+ *   column c, except 100 + r at c = r mod 64 and -200 - r at c = (r + 7) mod
+ *   64.  Synchronous on the legacy default stream; returns HDBMST_OK,
+ *   HDBMST_ERR_ARG (null out) or HDBMST_ERR_CUDA.
+ */
+hdbmst_status hdbmst_test_tmem_max(float *out);
 void hdbmst_test_set_mst_caps(int max_rounds, int max_jump_launches);
 
 /* Human-readable text of a status code (a static string). */
