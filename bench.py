@@ -90,22 +90,23 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.20 MB read, 2.90 MB written) and the
-        # pruned second pass (73.86 MB read, 23.41 MB written)
-        "bytes": 52.20e6 + 2.90e6 + 73.86e6 + 23.41e6,
+        # per step: the home pass (52.25 MB read, 2.96 MB written) and the
+        # pruned second pass (95.21 MB read - the home lists it starts from
+        # included - and 25.08 MB written)
+        "bytes": 52.25e6 + 2.96e6 + 95.21e6 + 25.08e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "351b9e50b30675aa4b908570be710811a175b034414f0ab9935c3a51419d2400",
+        "sha256": "e4f425e1bc6c3827dcc730f536d20ca7a100149007dd1558d299c0a15a06d4da",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (55.02 + 53.27 MB
+        # per step: the one-sided scans of rounds 1 and 2 (55.02 + 53.29 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.22 + 51.50 + 48.73 + 49.71 MB read); under
+        # pruned pass each (49.23 + 51.52 + 48.69 + 49.68 MB read); under
         # 0.01 MB written in all
-        "bytes": (55.02 + 53.27 + 49.22 + 51.50 + 48.73 + 49.71 + 0.004) * 1e6,
+        "bytes": (55.02 + 53.29 + 49.23 + 51.52 + 48.69 + 49.68 + 0.006) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "d2b128dc2173c4f74ca59176bd29afa15ae404542fd50fb934c94a0af8eeb589",
+        "sha256": "67e22b95eb669393cc6f99e14fc5296ad0b8512003f3a49b98be271b4b811d79",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
