@@ -419,11 +419,14 @@ def run_gpu(args):
     tf32_basis = ("measured bf16 burst x nominal tf32/bf16 (1.1/2.25)" if bf16 else
                   "fallback bf16 x nominal tf32/bf16 (1.1/2.25)")
 
-    def engine_of(d_):
-        """The tensor-core operand form the default engine uses for d features."""
+    def engine_of(d_, knn=False):
+        """The tensor-core operand form the default engine uses for d features
+        (padded to whole 32-feature slabs): two-part FP16 at 64, and for the
+        k-NN tile also at 128 and 192; else three-pass TF32."""
         if d_ > 192:
             return "fp32"
-        return "f16" if 32 < d_ <= 64 else "tf32"
+        dk = (d_ + 31) // 32 * 32
+        return "f16" if dk == 64 or (knn and dk in (128, 192)) else "tf32"
 
     def roofline(prof_, name, d_, pairs, dense_pairs, engine, workload=None):
         """A distance tile: algorithmic flops 2 d per (row, column) pair the
@@ -442,7 +445,7 @@ def run_gpu(args):
                   "dense_equivalent_tflops": round(2.0 * d_ * dense_pairs / step_s / 1e12, 1)}
         if engine in ("f16", "tf32"):
             if engine == "f16":
-                dk = 64  # padded halves per part
+                dk = (d_ + 31) // 32 * 32  # padded halves per part
                 peak = bf16 if bf16 else FALLBACK_BF16_TFLOPS
                 basis = ("measured bf16 burst (dense fp16 runs at the bf16 rate)" if bf16 else
                          "fallback bf16 (dense fp16 runs at the bf16 rate)")
@@ -466,7 +469,7 @@ def run_gpu(args):
 
     # core distances: every clip against every clip, pruned by the pivot bounds;
     # the Boruvka scan: every active clip against the clips of other components
-    knn_tile_roof = roofline(prof, "knn_tile", d, core_pairs, float(n) * n, engine_of(d),
+    knn_tile_roof = roofline(prof, "knn_tile", d, core_pairs, float(n) * n, engine_of(d, knn=True),
                              args.workload)
     scan_dense = float(sum(a for a, _, _ in rounds)) * n
     scan_roof = roofline(prof, "boruvka_scan", d, scan_pairs, scan_dense, engine_of(d),
@@ -475,7 +478,7 @@ def run_gpu(args):
     cands = [r for r in (scan_roof, knn_tile_roof) if r is not None]
     main_roof = max(cands, key=lambda r: r["ms_per_step"]) if cands else None
     knn_roof = roofline(kprof, "knn_tile", Xk.shape[0], knn_pairs,
-                        float(Xk.shape[1]) * Yk.shape[1], engine_of(Xk.shape[0]),
+                        float(Xk.shape[1]) * Yk.shape[1], engine_of(Xk.shape[0], knn=True),
                         KNN_WORKLOAD if not args.skip_knn else None)
     breakdown = {k: {"ms_per_step": round(v[0] / args.steps, 3), "launches_per_step": v[1] / args.steps}
                  for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}

@@ -40,7 +40,11 @@ bool use_tensor_scan(int dk) {
 
 // Two-part FP16 operands on the tensor cores: 64 padded features (one
 // 128-byte row of halves per part), unless TF32 is asked for.
-bool use_f16(int dk) { return g_engine != HDBMST_ENGINE_TF32 && dk == 64; }
+// The two-part FP16 form: 64 padded features, and (the k-NN tile's wide
+// rows) 128 or 192; other widths stay on three-pass TF32.
+bool use_f16(int dk) {
+    return g_engine != HDBMST_ENGINE_TF32 && (dk == 64 || dk == 128 || dk == 192);
+}
 
 // Form of the Boruvka scan on the tensor cores (HDBMST_SCAN_*), process-wide,
 // and whether the symmetric form prunes block pairs.

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
     const int dk_mma = kF16 ? a.dk / 2 : a.dk;
     tc_produce_and_multiply<kEpiWarps, kWide, kF16, kSmall>(P.maps, S, smem_u32(base), dk_mma, r0, seq);
 
-    if (warp < 4) tc_load_a<kWide>(S, P.a_hi, P.a_lo, r0, dk_mma);
+    if (warp < 4) tc_load_a<kWide, !kWide || kF16>(S, P.a_hi, P.a_lo, r0, dk_mma);
     if (warp < kEpiWarps) {
         // thread = (row, group): rows 32 (w % 4) + lane, group w / 4
         const int row = (warp & 3) * 32 + lane;
@@ -436,13 +436,18 @@ cudaError_t launch_tc_knn(int KP, const KnnTileArgs &a, const TcOperands &o, int
     P.a_lo = static_cast<const float *>(o.a_lo);
     const float *b_hi = static_cast<const float *>(o.b_hi), *b_lo = static_cast<const float *>(o.b_lo);
     const bool wide = a.dk > 64;
+    // FP16: dk / 2 words of two halves, whole 32-word slabs (dk = 64, 128 or
+    // 192); past 64 features both A parts sit in TMEM [0, dk) below the wide
+    // layout's accumulators
     const int dk_mma = a.f16 ? a.dk / 2 : a.dk;
-    if ((a.f16 && (wide || dk_mma != kSlab)) || !make_point_map(&P.maps.b_hi, b_hi, y_rows, dk_mma) ||
+    if ((a.f16 && dk_mma % kSlab != 0) || !make_point_map(&P.maps.b_hi, b_hi, y_rows, dk_mma) ||
         !make_point_map(&P.maps.b_lo, b_lo, y_rows, dk_mma) ||
-        (wide && !make_point_map(&P.maps.a_lo, P.a_lo, x_rows, a.dk)))
+        (wide && !a.f16 && !make_point_map(&P.maps.a_lo, P.a_lo, x_rows, a.dk)))
         return cudaErrorInvalidValue;
-    if (a.f16 && KP == 16) return tc_launch<16, false, true>(P, row_tiles, splits, s);
-    if (a.f16 && KP == 32) return tc_launch<32, false, true>(P, row_tiles, splits, s);
+    if (a.f16 && !wide && KP == 16) return tc_launch<16, false, true>(P, row_tiles, splits, s);
+    if (a.f16 && !wide && KP == 32) return tc_launch<32, false, true>(P, row_tiles, splits, s);
+    if (a.f16 && wide && KP == 16) return tc_launch<16, true, true>(P, row_tiles, splits, s);
+    if (a.f16 && wide && KP == 32) return tc_launch<32, true, true>(P, row_tiles, splits, s);
     if (!wide && KP == 16) return tc_launch<16, false, false>(P, row_tiles, splits, s);
     if (!wide && KP == 32) return tc_launch<32, false, false>(P, row_tiles, splits, s);
     if (wide && KP == 16) return tc_launch<16, true, false>(P, row_tiles, splits, s);

@@ -182,14 +182,16 @@ __device__ __forceinline__ void tc_setup(PipeSmem &S) {
 // 32-lane quadrant): thread (w, lane) copies row 32 w + lane of the CTA's row
 // block - hi parts to columns [0, dk), lo parts to [dk, 2 dk) - then arrives
 // on S.abar.  rows: point-major [..][dk] arrays, row0: the block's first row.
-template <bool kWide = false>
+// kBoth: A's lo parts go to TMEM too (after the hi parts), as everywhere but
+// the wide TF32 rows, whose lo parts the producer loads into shared memory.
+template <bool kWide = false, bool kBoth = !kWide>
 __device__ __forceinline__ void tc_load_a(PipeSmem &S, const float *a_hi, const float *a_lo,
                                           int64_t row0, int dk) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t taddr = S.tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t off = (row0 + warp * 32 + lane) * dk;
 #pragma unroll 1
-    for (int h = 0; h < (kWide ? 1 : 2); ++h) {
+    for (int h = 0; h < (kBoth ? 2 : 1); ++h) {
         const float *src = (h ? a_lo : a_hi) + off;
 #pragma unroll 1
         for (int c = 0; c < dk; c += 32) {
@@ -219,7 +221,6 @@ template <int kEpiWarps, bool kWide = false, bool kF16 = false, bool kSmall = fa
 __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeSmem &S,
                                                         uint32_t sbase, int dk, int a_row,
                                                         const TileSeq &seq) {
-    static_assert(!(kWide && kF16), "the wide rows stay on TF32");
     using Sh = PipeShape<kWide, kSmall>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slabs = dk / kSlab;
@@ -231,10 +232,14 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                         : kSmall ? kAcc == 1 : ((kAcc == 2 || kAcc == 3) && kStages == 6),
                   "see Slot");
     if (warp == kEpiWarps && lane == 0) {
-        if (kWide) {
+        if constexpr (kWide && !kF16) {
             mbar_expect_tx(&S.abar, static_cast<uint32_t>(slabs) * kSlabTile);
             for (int s = 0; s < slabs; ++s)
                 tma_load_2d(alo + s * kSlabTile, &M.a_lo, s * kSlab, a_row, &S.abar);
+        } else if constexpr (kWide) {
+            // wide FP16 rows: both A parts are in TMEM (tc_load_a); the
+            // producer's arrival that A's lo parts would have completed
+            mbar_arrive(&S.abar);
         }
         const bool withhold = *reinterpret_cast<volatile int *>(&g_withhold_first_slab) != 0;
         for (int h = 0; 2 * h < seq.n; ++h) {
@@ -282,7 +287,7 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                 const uint64_t bh = smem_desc(ring + st * 2 * kSlabTile + (t & 1) * (kSlabTile / 2));
                 const uint64_t bl = bh + (kSlabTile >> 4);
                 const uint32_t ah = tmem + static_cast<uint32_t>(s * kSlab), al = ah + dk;
-                if (kWide) {
+                if constexpr (kWide && !kF16) {
                     // A lo from shared memory: its slab's descriptor, + 2 per K step
                     const uint64_t als = smem_desc(alo + s * kSlabTile);
                     mma_tf32_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
@@ -294,7 +299,8 @@ __device__ __forceinline__ void tc_produce_and_multiply(const PipeMaps &M, PipeS
                         mma_tf32_ts(d, ah + kk * 8, bl + 2 * kk, idesc, 1u);
                         mma_tf32(d, als + 2 * kk, bh + 2 * kk, idesc, 1u);
                     }
-                } else if (kF16) {
+                } else if constexpr (kF16) {
+                    // A hi in TMEM columns [0, dk), A lo in [dk, 2 dk)
                     mma_f16_ts(d, ah, bh, idesc, s > 0 ? 1u : 0u);
                     mma_f16_ts(d, ah, bl, idesc, 1u);
                     mma_f16_ts(d, al, bh, idesc, 1u);

@@ -338,8 +338,9 @@ hdbmst_status hdbmst_hdbscan_labels(const int32_t *edges, const float *w, int64_
  *   HDBMST_ENGINE_TF32   tensor cores as AUTO, always with TF32 products.
  * The tensor-core tile ranks candidates (tcgen05) with two-part FP16 products
  * (every value, scaled by one power of two per call, split into a high and a
- * low half; hi.hi + hi.lo + lo.hi) where the points have 33 to 64 features,
- * else with three-pass TF32 products.  Every engine reports distances and
+ * low half; hi.hi + hi.lo + lo.hi) where the points have 33 to 64 features
+ * (and, for the k-NN, 97 to 128 or 161 to 192), else with three-pass TF32
+ * products.  Every engine reports distances and
  * weights re-evaluated exactly with dist() and proves the kept set against
  * its own rounding bound, so results are identical bit for bit whichever
  * engine ran.  Returns the previous setting; unknown values are ignored.
