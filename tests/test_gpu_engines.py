@@ -79,9 +79,12 @@ def test_knn_engines_identical_200k_d192_sampled_rows(h):
 
 
 @pytest.mark.parametrize("n,m,d,k", [(1000, 1000, 61, 11), (777, 2049, 64, 16), (2000, 1500, 48, 12),
-                                     (300, 130, 33, 32), (20000, 20000, 61, 11)])
+                                     (300, 130, 33, 32), (20000, 20000, 61, 11),
+                                     # wide rows on FP16: both A parts in TMEM
+                                     (1500, 2200, 120, 10), (900, 1300, 190, 16)])
 def test_fp16_tf32_simt_identical(h, n, m, d, k):
-    """The two-part FP16 operands (33 to 64 features), the TF32 operands and the
+    """The two-part FP16 operands (33 to 64 features, and 97 to 128 or 161 to
+    192 in the k-NN), the TF32 operands and the
     FP32 FFMA tile: identical lists; the FP16 form's ranking must be tight
     enough that the rounding proof settles almost every row (an MMA that
     computed something else would show up here as a flood of exact rows or
