@@ -43,48 +43,70 @@ __global__ void pivots_kernel(const float *__restrict__ Y, int64_t ldy, int stri
 // ties to the lower pivot; also the point's distance to its own pivot
 // (dcell), its distances to all 128 pivots if pd is not null (point-major
 // [cnt][128]), and cmax[cell] raised to the distance to its own pivot.  A CTA
-// of 256 threads takes 64 points against the 128 pivots; each thread
-// accumulates 4 points x 8 pivots with features staged 16 at a time in shared
-// memory.  Each squared distance is the same ascending-feature chain of fused
+// of 256 threads takes 128 points against the 128 pivots; thread (ty, tx)
+// accumulates points 8 ty .. 8 ty + 7 against pivots 4 tx .. 4 tx + 3 and
+// 64 + 4 tx .. 64 + 4 tx + 3, so that the eight lanes of a quarter warp read
+// 128 contiguous bytes of pivots from shared memory (one wavefront) and one
+// broadcast word group of points.  Features go 16 at a time through shared
+// memory; the next 16 are loaded into registers while these are used.  Each
+// squared distance is the same ascending-feature chain of fused
 // multiply-adds of differences as one point at a time would give.
-constexpr int kCellPts = 64, kCellPiv = 128, kCellK = 16;
-__global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S, int64_t lds,
-                                                    int cnt, int d, const float *__restrict__ piv,
-                                                    int dp, int *__restrict__ cell,
-                                                    float *__restrict__ dcell,
-                                                    float *__restrict__ pd,
-                                                    unsigned *__restrict__ cmax) {
+constexpr int kCellPts = 128, kCellPiv = 128, kCellK = 16;
+constexpr int kCellLoads = kCellK * kCellPts / 256;  // per thread and stage, for each operand
+static_assert(kCellPts == kCellPiv, "one load pattern for points and pivots");
+
+__global__ void __launch_bounds__(256, 2) cells_kernel(const float *__restrict__ S, int64_t lds,
+                                                       int cnt, int d, const float *__restrict__ piv,
+                                                       int dp, int *__restrict__ cell,
+                                                       float *__restrict__ dcell,
+                                                       float *__restrict__ pd,
+                                                       unsigned *__restrict__ cmax) {
     __shared__ __align__(16) float xs[kCellK][kCellPts];
     __shared__ __align__(16) float ps[kCellK][kCellPiv];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int i0 = blockIdx.x * kCellPts;
-    // acc[a][b] = (pivot 2b, pivot 2b + 1) of point a: packed FP32 pairs,
-    // each half summed in feature order exactly as a scalar FMA chain
-    float2 acc[4][4];
+    // stage loads: element tid + 256 r of the [16][128] tile, r < kCellLoads
+    const int lc = tid & (kCellPts - 1), lf = tid / kCellPts;
+    float rx[kCellLoads], rp[kCellLoads];
+    const auto load_stage = [&](int f0) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+        for (int r = 0; r < kCellLoads; ++r) {
+            const int f = f0 + lf + r * (256 / kCellPts);
+            const int i = i0 + lc;
+            rx[r] = (i < cnt && f < d) ? S[static_cast<int64_t>(f) * lds + i] : 0.f;
+            // the pivots negated: x + (-p) rounds exactly as x - p
+            rp[r] = -piv[static_cast<int64_t>(f) * kCellPiv + lc];
+        }
+    };
+    // acc[a][b]: point 8 ty + a against pivots 4 tx + 2 b, + 1 (b < 2) or
+    // 64 + 4 tx + 2 (b - 2), + 1 (b >= 2): packed FP32 pairs, each half
+    // summed in feature order exactly as a scalar FMA chain
+    float2 acc[8][4];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = make_float2(0.f, 0.f);
+    load_stage(0);
     for (int f0 = 0; f0 < dp; f0 += kCellK) {
-        for (int q = tid; q < kCellK * kCellPts; q += 256) {
-            const int f = q / kCellPts, c = q % kCellPts;
-            const int i = i0 + c;
-            xs[f][c] = (i < cnt && f0 + f < d) ? S[static_cast<int64_t>(f0 + f) * lds + i] : 0.f;
-        }
-        // the pivots negated: x + (-p) rounds exactly as x - p
-        for (int q = tid; q < kCellK * kCellPiv; q += 256)
-            (&ps[0][0])[q] = -piv[static_cast<int64_t>(f0) * kCellPiv + q];
         __syncthreads();
 #pragma unroll
+        for (int r = 0; r < kCellLoads; ++r) {
+            xs[lf + r * (256 / kCellPts)][lc] = rx[r];
+            ps[lf + r * (256 / kCellPts)][lc] = rp[r];
+        }
+        __syncthreads();
+        if (f0 + kCellK < dp) load_stage(f0 + kCellK);
+#pragma unroll
         for (int f = 0; f < kCellK; ++f) {
-            const float4 x = *reinterpret_cast<const float4 *>(&xs[f][ty * 4]);
-            const float4 p0 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8]);
-            const float4 p1 = *reinterpret_cast<const float4 *>(&ps[f][tx * 8 + 4]);
-            const float xv[4] = {x.x, x.y, x.z, x.w};
+            const float4 x0 = *reinterpret_cast<const float4 *>(&xs[f][ty * 8]);
+            const float4 x1 = *reinterpret_cast<const float4 *>(&xs[f][ty * 8 + 4]);
+            const float4 p0 = *reinterpret_cast<const float4 *>(&ps[f][tx * 4]);
+            const float4 p1 = *reinterpret_cast<const float4 *>(&ps[f][64 + tx * 4]);
+            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             const float2 pv[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w),
                                   make_float2(p1.x, p1.y), make_float2(p1.z, p1.w)};
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
+            for (int a = 0; a < 8; ++a) {
                 const float2 x2 = make_float2(xv[a], xv[a]);
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
@@ -93,20 +115,20 @@ __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S,
                 }
             }
         }
-        __syncthreads();
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = i0 + ty * 4 + a;
+    for (int a = 0; a < 8; ++a) {
+        const int i = i0 + ty * 8 + a;
+        // the thread's pivots in ascending order
         const float sq[8] = {acc[a][0].x, acc[a][0].y, acc[a][1].x, acc[a][1].y,
                              acc[a][2].x, acc[a][2].y, acc[a][3].x, acc[a][3].y};
         float best = sq[0];
-        int arg = tx * 8;
+        int arg = tx * 4;
 #pragma unroll
         for (int b = 1; b < 8; ++b)
             if (sq[b] < best) {
                 best = sq[b];
-                arg = tx * 8 + b;
+                arg = (b < 4 ? 0 : 60) + tx * 4 + b;
             }
         // least (value, pivot) over the 16 lanes of this point (one half-warp)
 #pragma unroll
@@ -120,11 +142,13 @@ __global__ void __launch_bounds__(256) cells_kernel(const float *__restrict__ S,
         }
         if (i < cnt) {
             if (pd) {
-                float4 *o = reinterpret_cast<float4 *>(pd + static_cast<int64_t>(i) * kCellPiv + tx * 8);
-                o[0] = make_float4(__fsqrt_rn(sq[0]), __fsqrt_rn(sq[1]), __fsqrt_rn(sq[2]),
-                                   __fsqrt_rn(sq[3]));
-                o[1] = make_float4(__fsqrt_rn(sq[4]), __fsqrt_rn(sq[5]), __fsqrt_rn(sq[6]),
-                                   __fsqrt_rn(sq[7]));
+                float *row = pd + static_cast<int64_t>(i) * kCellPiv;
+                *reinterpret_cast<float4 *>(row + tx * 4) =
+                    make_float4(__fsqrt_rn(sq[0]), __fsqrt_rn(sq[1]), __fsqrt_rn(sq[2]),
+                                __fsqrt_rn(sq[3]));
+                *reinterpret_cast<float4 *>(row + 64 + tx * 4) =
+                    make_float4(__fsqrt_rn(sq[4]), __fsqrt_rn(sq[5]), __fsqrt_rn(sq[6]),
+                                __fsqrt_rn(sq[7]));
             }
             if (tx == 0) {
                 cell[i] = arg;
