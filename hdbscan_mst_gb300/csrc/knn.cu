@@ -238,17 +238,31 @@ __global__ void __launch_bounds__(kThreads, 2) knn_tile_kernel(const KnnTileArgs
 
 // ------------------------------------------------------------------ refine
 
-// Groups of KP lanes; each group owns one query row.
+// Groups of KP lanes; each group owns one query row.  The candidates' rows
+// are read kSegF features at a time into shared memory (rows padded to
+// kSegStride floats: the lanes' 16-byte reads of their own rows then fall on
+// distinct banks in each quarter warp); the query row (up to kRefineXMax
+// features) is copied whole at the start.
+constexpr int kSegF = 32, kSegStride = 36, kRefineXMax = 192;
+
 template <int KP>
 __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) {
     __shared__ float sel_t[128];
     __shared__ int sel_j[128];
+    __shared__ __align__(16) float s_seg[2][128 / KP][KP][kSegStride];
+    __shared__ __align__(16) float s_x[128 / KP][kRefineXMax];
     const int gl = threadIdx.x % KP;
     const int group = threadIdx.x / KP;
     const int local = blockIdx.x * (128 / KP) + group;
     const int row = a.row_base + local;
     const bool active = row < a.row_end;
     const int leader = (threadIdx.x & 31) & ~(KP - 1);
+    // the query row, in flight while the lists merge
+    const bool x_smem = a.dk <= kRefineXMax;
+    if (x_smem && active)
+        for (int q = gl; q < a.dk / 4; q += KP)
+            cp_async16(&s_x[group][q * 4], a.Xp + static_cast<int64_t>(row) * a.dk + q * 4);
+    cp_async_commit();
 
     // 1. Merge the sorted partial lists of the splits into the KP best by
     //    (t, index), the KP lanes of the row together: lane p holds entry p
@@ -267,15 +281,23 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
     };
     constexpr unsigned long long kEmpty = 0xFF8000007FFFFFFFull;  // (+inf, INT_MAX)
     unsigned long long mk = active ? load_key(0, gl) : kEmpty;
-    // every lane of the warp runs the same merges (the shuffles)
+    // every lane of the warp runs the same merges (the shuffles); the
+    // further lists are loaded four at a time
     const int slabs_w = __reduce_max_sync(0xffffffffu, active ? slabs : 0);
-    for (int sl = 1; sl < slabs_w; ++sl) {
-        const unsigned long long o = (active && sl < slabs) ? load_key(sl, KP - 1 - gl) : kEmpty;
-        mk = min(mk, o);
+    for (int s0 = 1; s0 < slabs_w; s0 += 4) {
+        unsigned long long o[4];
 #pragma unroll
-        for (int h = KP / 2; h > 0; h >>= 1) {
-            const unsigned long long q = __shfl_xor_sync(0xffffffffu, mk, h);
-            mk = (gl & h) ? max(mk, q) : min(mk, q);
+        for (int u = 0; u < 4; ++u)
+            o[u] = (active && s0 + u < slabs) ? load_key(s0 + u, KP - 1 - gl) : kEmpty;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (s0 + u >= slabs_w) break;
+            mk = min(mk, o[u]);
+#pragma unroll
+            for (int h = KP / 2; h > 0; h >>= 1) {
+                const unsigned long long q = __shfl_xor_sync(0xffffffffu, mk, h);
+                mk = (gl & h) ? max(mk, q) : min(mk, q);
+            }
         }
     }
     sel_t[group * KP + gl] = order_float(static_cast<unsigned>(mk >> 32));
@@ -308,20 +330,54 @@ __global__ void __launch_bounds__(128) knn_refine_kernel(const KnnRefineArgs a) 
             __fmul_rd(__fadd_rd(lo, xn), __fsub_rd(1.f, mg)) > __fmul_ru(__fadd_ru(hi, xn), __fadd_ru(1.f, mg)))
             need = false;
     }
+    //    The group copies its candidates' rows kSegF features at a time,
+    //    eight lanes per candidate segment (whole 32-byte sectors), two
+    //    stages in flight; each lane then runs its own candidate's chain in
+    //    feature order from shared memory.
     unsigned long long key = kNoKey;
-    if (need) {
-        const float4 *xp = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(row) * a.dk);
-        const float4 *yp = reinterpret_cast<const float4 *>(a.Yp + static_cast<int64_t>(j) * a.dk);
+    {
+        const unsigned needs = __ballot_sync(0xffffffffu, need) >> leader;  // bit p: candidate p
+        const float4 *xp = reinterpret_cast<const float4 *>(a.Xp + static_cast<int64_t>(active ? row : 0) * a.dk);
+        const int nseg = (a.dk + kSegF - 1) / kSegF;
+        const auto issue = [&](int c) {
+            const int f0 = c * kSegF, w = min(kSegF, a.dk - f0), q = gl & 7;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int p = it * (KP / 8) + (gl >> 3);
+                if (((needs >> p) & 1u) && q * 4 < w)
+                    cp_async16_ca(&s_seg[c & 1][group][p][q * 4],
+                                  a.Yp + static_cast<int64_t>(sel_j[group * KP + p]) * a.dk + f0 + q * 4);
+            }
+            cp_async_commit();
+        };
         float acc = 0.f;
-        for (int q = 0; q < a.dk / 4; ++q) {
-            const float4 x = __ldg(xp + q), y = __ldg(yp + q);
-            acc = sqdiff_fma(x.x, y.x, acc);
-            acc = sqdiff_fma(x.y, y.y, acc);
-            acc = sqdiff_fma(x.z, y.z, acc);
-            acc = sqdiff_fma(x.w, y.w, acc);
+        issue(0);
+        for (int c = 0; c < nseg; ++c) {
+            if (c + 1 < nseg) {
+                issue(c + 1);
+                cp_async_wait_one();
+            } else {
+                cp_async_wait_all();
+            }
+            __syncwarp();
+            if (need) {
+                const int f0 = c * kSegF, w = min(kSegF, a.dk - f0);
+                const float *ys = &s_seg[c & 1][group][gl][0];
+#pragma unroll 4
+                for (int f = 0; f < w; f += 4) {
+                    const float4 x = x_smem ? *reinterpret_cast<const float4 *>(&s_x[group][f0 + f])
+                                            : __ldg(xp + (f0 + f) / 4);
+                    const float4 y = *reinterpret_cast<const float4 *>(ys + f);
+                    acc = sqdiff_fma(x.x, y.x, acc);
+                    acc = sqdiff_fma(x.y, y.y, acc);
+                    acc = sqdiff_fma(x.z, y.z, acc);
+                    acc = sqdiff_fma(x.w, y.w, acc);
+                }
+            }
+            __syncwarp();  // every lane is done with the stage before it is refilled
         }
         // rank by the caller's column index (the packed order may be spatial)
-        key = key64(__fsqrt_rn(acc), static_cast<unsigned>(a.permY ? a.permY[j] : j));
+        if (need) key = key64(__fsqrt_rn(acc), static_cast<unsigned>(a.permY ? a.permY[j] : j));
     }
 
     // 3. Bitonic sort of the group's KP keys, ascending.
