@@ -128,16 +128,31 @@ __global__ void __launch_bounds__(256) pack_tile_kernel(const float *__restrict_
     bool finite = true;
     const int ip = i0 + lane;
     const int dst_own = (ip < n && inv) ? inv[ip] : ip;
+    // warp w stages features w, w + 8, ... of the chunk: all eight loads in
+    // flight at once, the next chunk's while this one is written
+    constexpr int kRows = kPackF / 8;
+    float vr[kRows];
+    const auto load_chunk = [&](int f0) {
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int f = f0 + warp + 8 * u;
+            vr[u] = (f < d && f < dk && ip < n) ? X[static_cast<int64_t>(f) * ld + ip] : 0.f;
+        }
+    };
+    load_chunk(0);
     for (int f0 = 0; f0 < dk; f0 += kPackF) {
         const int fc = min(kPackF, dk - f0);
         __syncthreads();
-        for (int r = warp; r < fc; r += 8) {
-            const int f = f0 + r;
-            const float v = (f < d && ip < n) ? X[static_cast<int64_t>(f) * ld + ip] : 0.f;
-            xs[r][lane] = v;
-            if (Xf && ip < n_pad) Xf[static_cast<int64_t>(f) * n_pad + dst_own] = v;
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const int r = warp + 8 * u;
+            if (r < fc) {
+                xs[r][lane] = vr[u];
+                if (Xf && ip < n_pad) Xf[static_cast<int64_t>(f0 + r) * n_pad + dst_own] = vr[u];
+            }
         }
         __syncthreads();
+        if (f0 + kPackF < dk) load_chunk(f0 + kPackF);
         if (warp == 0) {
             for (int r = 0; r < fc; ++r) {
                 const float v = xs[r][lane];
