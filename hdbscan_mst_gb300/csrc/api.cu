@@ -356,6 +356,7 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
             q.pdSX = p.alias ? q.pdSY : c.take<float>(static_cast<size_t>(p.n_pad) * P);
             q.Lm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
             q.Hm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
+            q.HLt = c.take<float2>(static_cast<size_t>(P) * p.col_tiles);
             q.bcell = c.take<int>(p.col_tiles);
             q.minH = c.take<float>(2 * P);
             q.home_lo = c.take<int>(tiles);

@@ -76,6 +76,7 @@ struct PruneBufs {
     float *pdSY, *pdSX;   // [m_pad][P], [n_pad][P] pivot distances in sorted order
     float *Lm, *Hm;       // [P][col_tiles]: per column block, least / largest pivot
                           // distance of its points, widened by the distances' rounding bound
+    float2 *HLt;          // [col_tiles][P]: the same (H, L) pairs, block-major
     int *bcell;           // [col_tiles] pivot cell of each block's first point
     float *minH;          // [2 P]: per pivot the least H, then the largest L, over all blocks
     int *home_lo;         // [chunk row tiles] first block of the home range

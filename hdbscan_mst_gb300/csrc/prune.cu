@@ -59,13 +59,15 @@ __global__ void pivot_gather_kernel(const float *__restrict__ src, const int *__
 
 // Per column block b (one CTA, thread = pivot): least and largest distance of
 // its points to the pivot, widened outward by eps; +inf / -inf for a block
-// without points.  bcell[b]: the pivot cell of the block's first point.
+// without points; pivot-major (Lm, Hm) and block-major (HLt) copies.
+// bcell[b]: the pivot cell of the block's first point.
 __global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict__ pdS, int m,
                                                          int col_tiles, double eps,
                                                          const int *__restrict__ binY,
                                                          const int *__restrict__ permY, int B,
                                                          float *__restrict__ Lm,
                                                          float *__restrict__ Hm,
+                                                         float2 *__restrict__ HLt,
                                                          int *__restrict__ bcell) {
     const int b = blockIdx.x, p = threadIdx.x;
     const int pos0 = b * kBN, pos1 = min(pos0 + kBN, m);
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict
     const float H = pos1 > pos0 ? __double2float_ru(static_cast<double>(hi) * (1.0 + eps)) : -INFINITY;
     Lm[o] = L;
     Hm[o] = H;
+    HLt[static_cast<int64_t>(b) * P + p] = make_float2(H, L);
     if (p == 0) bcell[b] = pos1 > pos0 ? binY[permY[pos0]] / B : 0;
 }
 
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
                                                           const float *__restrict__ pdSX,
                                                           const float *__restrict__ Lm,
                                                           const float *__restrict__ Hm,
+                                                          const float2 *__restrict__ HLt,
                                                           const int *__restrict__ bcell,
                                                           const int *__restrict__ home_lo,
                                                           int *__restrict__ list,
@@ -160,6 +164,8 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     __shared__ float s_A[P], s_B[P];
     __shared__ int s_wc[kBM / 32];
     __shared__ int s_useful[P], s_nuseful;
+    __shared__ int s_cand[kBM];
+    __shared__ int s_keep[kBM];
     const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int local = rt * kBM + tid;
     const int row = a.row_base + local;
@@ -242,12 +248,22 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     }
     __syncthreads();
     const int nuseful = s_nuseful;
+    // lane l tests pivot s_useful[32 g + l] of group g
+    int pv[P / 32];
+    float2 abv[P / 32];
+#pragma unroll
+    for (int g = 0; g < P / 32; ++g) {
+        const int q = g * 32 + lane < nuseful ? s_useful[g * 32 + lane] : 0;
+        pv[g] = q;
+        abv[g] = make_float2(s_A[q], s_B[q]);
+    }
 
     // 3. Blocks outside the home range, outward from it (threads 0..63 to the
     //    right, 64..127 to the left, 64 offsets per step), kept unless one
     //    pivot separates them from every row.  The block's own pivot is tried
-    //    first (it separates most far blocks); the others 32 at a time, their
-    //    loads independent of each other.
+    //    first (it separates most far blocks); the blocks it leaves are then
+    //    taken one per warp against the useful pivots, a lane per pivot, 32
+    //    at a time until one separates the block.
     const int h0 = home_lo[rt];
     const int right0 = h0 + nh, left0 = h0 - 1;
     int base = 0;
@@ -259,18 +275,31 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
             const int p0 = bcell[b];
             need = !(Hm[static_cast<int64_t>(p0) * a.col_tiles + b] < s_A[p0] ||
                      Lm[static_cast<int64_t>(p0) * a.col_tiles + b] > s_B[p0]);
-            for (int u = 0; u < nuseful && need; u += 32) {
-                bool sep = false;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int pp = s_useful[u + q];
-                    const int64_t i = static_cast<int64_t>(pp) * a.col_tiles + b;
-                    sep |= (__ldg(Hm + i) < s_A[pp]) | (__ldg(Lm + i) > s_B[pp]);
-                }
-                need = !sep;
-            }
         }
-        const unsigned bal = __ballot_sync(0xffffffffu, need);
+        // the blocks left, in thread order
+        unsigned bal = __ballot_sync(0xffffffffu, need);
+        if (lane == 0) s_wc[warp] = __popc(bal);
+        __syncthreads();
+        int ci = 0;
+        for (int w = 0; w < warp; ++w) ci += s_wc[w];
+        const int nc = s_wc[0] + s_wc[1] + s_wc[2] + s_wc[3];
+        ci += __popc(bal & lanemask_lt());
+        if (need) s_cand[ci] = b;
+        __syncthreads();
+        for (int c = warp; c < nc; c += kBM / 32) {
+            const float2 *hl = HLt + static_cast<int64_t>(s_cand[c]) * P;
+            bool sep = false;
+#pragma unroll
+            for (int g = 0; g < P / 32; ++g) {
+                if (sep || g * 32 >= nuseful) break;
+                const float2 v = __ldg(hl + pv[g]);  // (H, L)
+                sep = __any_sync(0xffffffffu, v.x < abv[g].x || v.y > abv[g].y);
+            }
+            if (lane == 0) s_keep[c] = sep ? 0 : 1;
+        }
+        __syncthreads();
+        if (need) need = s_keep[ci] != 0;
+        bal = __ballot_sync(0xffffffffu, need);
         if (lane == 0) s_wc[warp] = __popc(bal);
         __syncthreads();
         int off = base;
@@ -301,7 +330,7 @@ cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n,
     }
     block_bounds_kernel<<<col_tiles, P, 0, s>>>(b.pdSY, m, col_tiles, (d + 8.0) * 0x1p-24,
                                                 o.cellY, o.permY, o.buckets, b.Lm, b.Hm,
-                                                b.bcell);
+                                                b.HLt, b.bcell);
     pivot_range_kernel<<<P, 256, 0, s>>>(b.Lm, b.Hm, col_tiles, b.minH, b.minH + P);
     ++extra;
     count_extra_launches(extra);
@@ -317,7 +346,7 @@ cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaSt
 }
 
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s) {
-    prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.bcell, b.home_lo,
+    prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.HLt, b.bcell, b.home_lo,
                                                    b.list, b.count, b.slabs, b.gthr, b.minH,
                                                    b.minH + P);
     return cudaGetLastError();
