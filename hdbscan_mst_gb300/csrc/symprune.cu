@@ -146,15 +146,17 @@ __global__ void __launch_bounds__(P) sym_bounds_kernel(int np, const int *__rest
 
 // LB[i][j] for all block pairs (LB is symmetric: only tiles with j0 >= i0
 // are computed, and written to both halves).  A CTA of 256 threads takes 64
-// x 64 pairs, each thread 4 x 4, with the pivots staged 32 at a time.
-constexpr int kLbTile = 64, kLbPiv = 32;
+// x 64 pairs, each thread 4 x 4, with the pivots staged 32 at a time (rows
+// padded by one word: the staging writes a pivot per lane, which would
+// otherwise all fall on one bank).
+constexpr int kLbTile = 64, kLbPiv = 32, kLbPad = kLbTile + 1;
 __global__ void __launch_bounds__(256) sym_lb_kernel(int blocks, const float *__restrict__ Lb,
                                                      const float *__restrict__ Hb,
                                                      float *__restrict__ LB) {
     const int ti = blockIdx.y, tj = blockIdx.x;
     if (tj < ti) return;
-    __shared__ float sLi[kLbPiv][kLbTile], sHi[kLbPiv][kLbTile], sLj[kLbPiv][kLbTile],
-        sHj[kLbPiv][kLbTile];
+    __shared__ float sLi[kLbPiv][kLbPad], sHi[kLbPiv][kLbPad], sLj[kLbPiv][kLbPad],
+        sHj[kLbPiv][kLbPad];
     const int i0 = ti * kLbTile, j0 = tj * kLbTile;
     const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
     float lb[4][4];
