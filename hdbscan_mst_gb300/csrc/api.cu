@@ -352,8 +352,6 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
         if (p.prune) {
             PruneBufs &q = b.prune;
             const size_t tiles = static_cast<size_t>(p.chunk_rows / kBM);
-            q.pdSY = c.take<float>(static_cast<size_t>(p.m_pad) * P);
-            q.pdSX = p.alias ? q.pdSY : c.take<float>(static_cast<size_t>(p.n_pad) * P);
             q.Lm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
             q.Hm = c.take<float>(static_cast<size_t>(P) * p.col_tiles);
             q.HLt = c.take<float2>(static_cast<size_t>(P) * p.col_tiles);
@@ -451,8 +449,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     const int nh = home_blocks(p.col_tiles);
     const int chunk_cap = (p.col_tiles + kPruneChunks - 1) / kPruneChunks;
     if (prune)
-        LAUNCH(K_PRUNE, s, launch_prune_setup(b.order, b.prune, p.n, p.m, p.alias, p.col_tiles,
-                                               p.d, s));
+        LAUNCH(K_PRUNE, s, launch_prune_setup(b.order, b.prune, p.m, p.col_tiles, p.d, s));
     const int slots = (tensor ? 1 : 2) * sm_count();
     for (int base = 0; base < p.n; base += p.chunk_rows) {
         const int rows = std::min(p.chunk_rows, p.n - base);
@@ -524,6 +521,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.chunk_cap = chunk_cap;
             pa.nh = nh;
             pa.blocks_total = &b.st->tile_blocks;
+            pa.pdX = b.order.pdX;
+            pa.permX = b.order.permX;
             LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
             // second pass: slabs 1 .., in chunks of chunk_cap blocks
             KnnTileArgs q = ta;

@@ -73,7 +73,6 @@ inline int home_blocks(int col_tiles) {
 }
 constexpr int kPruneChunks = 4;     // CTAs per row tile in the second pass (at most)
 struct PruneBufs {
-    float *pdSY, *pdSX;   // [m_pad][P], [n_pad][P] pivot distances in sorted order
     float *Lm, *Hm;       // [P][col_tiles]: per column block, least / largest pivot
                           // distance of its points, widened by the distances' rounding bound
     float2 *HLt;          // [col_tiles][P]: the same (H, L) pairs, block-major
@@ -86,10 +85,9 @@ struct PruneBufs {
     int *slabs;           // [chunk row tiles] partial-list slabs written (1 + chunks)
     unsigned *gthr;       // [chunk rows] shared thresholds of the second pass (KnnTileArgs::gthr)
 };
-// Pivot distances into sorted order (dst[pos] = src[perm[pos]]) and the
-// column blocks' bounds.
-cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n, int m,
-                               bool alias, int col_tiles, int d, cudaStream_t s);
+// The column blocks' bounds (from the columns' pivot distances).
+cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int m, int col_tiles,
+                               int d, cudaStream_t s);
 struct PruneHomeArgs {
     const SpatialOrder *o;
     int n, m, col_tiles, row_tile0, row_tiles;  // row tiles of this chunk: row_tile0 ..
@@ -110,6 +108,8 @@ struct PruneListArgs {
     int chunk_cap;               // blocks per CTA of the second pass
     int nh;                      // blocks of the home range
     unsigned long long *blocks_total;  // += blocks the tile evaluates (both passes)
+    const float *pdX;            // [n_pad][P] the rows' pivot distances, callers' order
+    const int *permX;            // callers' index of each sorted row position
 };
 // Upper bound of each row's k-th distance from its home list, the row tile's
 // hull per pivot, and the list of blocks that the hull cannot exclude.

@@ -45,23 +45,13 @@ constexpr int P = kPrunePivots;
 
 int blocks_for(int64_t n, int per) { return static_cast<int>(n > per ? (n + per - 1) / per : 1); }
 
-// dst[pos][.] = src[perm[pos]][.] for pos < cnt: one warp per point, one
-// float4 per lane (P = 128 floats per point).
-__global__ void pivot_gather_kernel(const float *__restrict__ src, const int *__restrict__ perm,
-                                    int cnt, float *__restrict__ dst) {
-    static_assert(P == 128, "one float4 per lane");
-    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= cnt) return;
-    const float4 *s = reinterpret_cast<const float4 *>(src + static_cast<int64_t>(perm[w]) * P);
-    reinterpret_cast<float4 *>(dst + w * P)[lane] = __ldg(s + lane);
-}
-
 // Per column block b (one CTA, thread = pivot): least and largest distance of
 // its points to the pivot, widened outward by eps; +inf / -inf for a block
-// without points; pivot-major (Lm, Hm) and block-major (HLt) copies.
-// bcell[b]: the pivot cell of the block's first point.
-__global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict__ pdS, int m,
+// without points; pivot-major (Lm, Hm) and block-major (HLt) copies.  The
+// pivot distances are in the callers' order (pdY[j][P]); a block holds the
+// points permY[pos] of its sorted positions.  bcell[b]: the pivot cell of
+// the block's first point.
+__global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict__ pdY, int m,
                                                          int col_tiles, double eps,
                                                          const int *__restrict__ binY,
                                                          const int *__restrict__ permY, int B,
@@ -69,11 +59,16 @@ __global__ void __launch_bounds__(P) block_bounds_kernel(const float *__restrict
                                                          float *__restrict__ Hm,
                                                          float2 *__restrict__ HLt,
                                                          int *__restrict__ bcell) {
+    static_assert(kBN == P, "one position per thread");
+    __shared__ int s_pt[kBN];
     const int b = blockIdx.x, p = threadIdx.x;
     const int pos0 = b * kBN, pos1 = min(pos0 + kBN, m);
+    s_pt[p] = pos0 + p < pos1 ? permY[pos0 + p] : 0;
+    __syncthreads();
     float lo = INFINITY, hi = -INFINITY;
-    for (int pos = pos0; pos < pos1; ++pos) {
-        const float v = pdS[static_cast<int64_t>(pos) * P + p];
+#pragma unroll 8
+    for (int q = 0; q < pos1 - pos0; ++q) {
+        const float v = pdY[static_cast<int64_t>(s_pt[q]) * P + p];
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
     }
@@ -148,7 +143,6 @@ __global__ void home_kernel(const int *__restrict__ binX, const int *__restrict_
 
 // One CTA (128 threads) per row tile of the chunk.
 __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
-                                                          const float *__restrict__ pdSX,
                                                           const float *__restrict__ Lm,
                                                           const float *__restrict__ Hm,
                                                           const float2 *__restrict__ HLt,
@@ -166,6 +160,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     __shared__ int s_useful[P], s_nuseful;
     __shared__ int s_cand[kBM];
     __shared__ int s_keep[kBM];
+    __shared__ int s_prow[kBM];  // the tile's points in the callers' order
     const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int local = rt * kBM + tid;
     const int row = a.row_base + local;
@@ -202,6 +197,7 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         ub = fin ? __fsqrt_ru(__fmul_ru(U, __fadd_ru(scale, 0x1p-23f))) : INFINITY;
     }
     s_ub[tid] = ub;
+    s_prow[tid] = row < a.row_end ? a.permX[row] : 0;
     // the second pass's shared threshold starts at the home list's KP-th key
     b_gthr[local] = row < a.row_end ? float_order(a.part_key[static_cast<int64_t>(local) * a.KP + a.KP - 1])
                                     : float_order(INFINITY);
@@ -214,14 +210,13 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         const float eps = static_cast<float>((a.d + 8) * 5.9604644775390625e-8);
         const float lo_f = __fsub_rd(1.f, eps), hi_f = __fadd_ru(1.f, eps);
         float A = INFINITY, Bv = -INFINITY;
-        // every row of the tile is in the array (n_pad rows), so the loads
-        // need no branch and many are in flight; rows past the last point
-        // (u < 0) are read and not used
-        const float *pd = pdSX + static_cast<int64_t>(a.row_base + rt * kBM) * P + tid;
+        // the loads need no branch, so many are in flight: rows past the last
+        // point (u < 0) read point 0's distances and do not use them
+        const float *pd = a.pdX + tid;
 #pragma unroll 16
         for (int r = 0; r < kBM; ++r) {
             const float u = s_ub[r];
-            const float dx = pd[static_cast<int64_t>(r) * P];
+            const float dx = pd[static_cast<int64_t>(s_prow[r]) * P];
             if (u >= 0.f) {
                 A = fminf(A, __fsub_rd(__fmul_rd(dx, lo_f), u));
                 Bv = fmaxf(Bv, __fadd_ru(__fmul_ru(dx, hi_f), u));
@@ -317,23 +312,14 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
 
 }  // namespace
 
-cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int n, int m,
-                               bool alias, int col_tiles, int d, cudaStream_t s) {
+cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int m, int col_tiles,
+                               int d, cudaStream_t s) {
     if (o.pivots != P) return cudaErrorInvalidValue;
-    pivot_gather_kernel<<<blocks_for(static_cast<int64_t>(m) * 32, 256), 256, 0, s>>>(
-        o.pdY, o.permY, m, b.pdSY);
-    int extra = 1;
-    if (!alias) {
-        pivot_gather_kernel<<<blocks_for(static_cast<int64_t>(n) * 32, 256), 256, 0, s>>>(
-            o.pdX, o.permX, n, b.pdSX);
-        ++extra;
-    }
-    block_bounds_kernel<<<col_tiles, P, 0, s>>>(b.pdSY, m, col_tiles, (d + 8.0) * 0x1p-24,
+    block_bounds_kernel<<<col_tiles, P, 0, s>>>(o.pdY, m, col_tiles, (d + 8.0) * 0x1p-24,
                                                 o.cellY, o.permY, o.buckets, b.Lm, b.Hm,
                                                 b.HLt, b.bcell);
     pivot_range_kernel<<<P, 256, 0, s>>>(b.Lm, b.Hm, col_tiles, b.minH, b.minH + P);
-    ++extra;
-    count_extra_launches(extra);
+    count_extra_launches(1);
     return cudaGetLastError();
 }
 
@@ -346,7 +332,7 @@ cudaError_t launch_prune_home(const PruneHomeArgs &a, const PruneBufs &b, cudaSt
 }
 
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s) {
-    prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.pdSX, b.Lm, b.Hm, b.HLt, b.bcell, b.home_lo,
+    prune_lists_kernel<<<a.row_tiles, kBM, 0, s>>>(a, b.Lm, b.Hm, b.HLt, b.bcell, b.home_lo,
                                                    b.list, b.count, b.slabs, b.gthr, b.minH,
                                                    b.minH + P);
     return cudaGetLastError();
