@@ -90,23 +90,23 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.25 MB read, 2.96 MB written) and the
-        # pruned second pass (95.21 MB read - the home lists it starts from
-        # included - and 25.08 MB written)
-        "bytes": 52.25e6 + 2.96e6 + 95.21e6 + 25.08e6,
+        # per step: the home pass (52.20 MB read, 3.87 MB written) and the
+        # pruned second pass (95.22 MB read - the home lists it starts from
+        # included - and 25.54 MB written)
+        "bytes": 52.20e6 + 3.87e6 + 95.22e6 + 25.54e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "e4f425e1bc6c3827dcc730f536d20ca7a100149007dd1558d299c0a15a06d4da",
+        "sha256": "6cf9da1f7f849889741d648bda9e24d73be23e05c7d1049977e4b6161d694b7e",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (55.02 + 53.29 MB
+        # per step: the one-sided scans of rounds 1 and 2 (55.01 + 53.27 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.23 + 51.52 + 48.69 + 49.68 MB read); under
+        # pruned pass each (49.26 + 51.68 + 48.69 + 49.68 MB read); under
         # 0.01 MB written in all
-        "bytes": (55.02 + 53.29 + 49.23 + 51.52 + 48.69 + 49.68 + 0.006) * 1e6,
+        "bytes": (55.01 + 53.27 + 49.26 + 51.68 + 48.69 + 49.68 + 0.006) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "67e22b95eb669393cc6f99e14fc5296ad0b8512003f3a49b98be271b4b811d79",
+        "sha256": "e0fff907bf285803002e54abe1fc699b3c317ccda4fb060234bc25ccbf4577ec",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0

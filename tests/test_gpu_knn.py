@@ -17,6 +17,9 @@ CASES = [
     (1, 1, 1, 1), (2, 3, 1, 2), (3, 5, 3, 5), (5, 2, 61, 1), (127, 129, 61, 10),
     (129, 127, 64, 10), (130, 300, 65, 7), (1001, 777, 102, 10), (2000, 400, 192, 16),
     (300, 2000, 3, 12), (257, 1000, 61, 13), (600, 640, 61, 32), (40, 40, 17, 32),
+    # past the tensor tile's 192 features: rows padded to 208 (a 16-feature
+    # last segment in the refine) and to 256
+    (300, 400, 200, 10), (129, 257, 250, 16),
 ]
 
 
