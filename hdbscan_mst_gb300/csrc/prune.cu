@@ -142,7 +142,7 @@ __global__ void home_kernel(const int *__restrict__ binX, const int *__restrict_
 }
 
 // One CTA (128 threads) per row tile of the chunk.
-__global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
+__global__ void __launch_bounds__(kBM, 12) prune_lists_kernel(const PruneListArgs a,
                                                           const float *__restrict__ Lm,
                                                           const float *__restrict__ Hm,
                                                           const float2 *__restrict__ HLt,
@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     __shared__ int s_cand[kBM];
     __shared__ int s_keep[kBM];
     __shared__ int s_prow[kBM];  // the tile's points in the callers' order
+    __shared__ unsigned long long s_near[kBM / 32];
+    __shared__ float2 s_ABu[P];
     const int rt = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int local = rt * kBM + tid;
     const int row = a.row_base + local;
@@ -243,22 +245,30 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
     }
     __syncthreads();
     const int nuseful = s_nuseful;
-    // lane l tests pivot s_useful[32 g + l] of group g
-    int pv[P / 32];
-    float2 abv[P / 32];
+    // the pivot nearest the whole tile (least B, the lower index on ties):
+    // it separates most of the far blocks
+    {
+        unsigned long long kb = (static_cast<unsigned long long>(float_order(s_B[tid])) << 32) |
+                                static_cast<unsigned>(tid);
 #pragma unroll
-    for (int g = 0; g < P / 32; ++g) {
-        const int q = g * 32 + lane < nuseful ? s_useful[g * 32 + lane] : 0;
-        pv[g] = q;
-        abv[g] = make_float2(s_A[q], s_B[q]);
+        for (int o = 16; o > 0; o >>= 1) kb = min(kb, __shfl_xor_sync(0xffffffffu, kb, o));
+        if (lane == 0) s_near[warp] = kb;
     }
+    __syncthreads();
+    const int pnear = static_cast<int>(min(min(s_near[0], s_near[1]), min(s_near[2], s_near[3])) & 0xffffffffu);
+    // lane l tests pivot s_useful[32 g + l] of group g, whose (A, B) is
+    // s_ABu[32 g + l]
+    int pv[P / 32];
+#pragma unroll
+    for (int g = 0; g < P / 32; ++g) pv[g] = g * 32 + lane < nuseful ? s_useful[g * 32 + lane] : 0;
+    if (tid < nuseful) s_ABu[tid] = make_float2(s_A[s_useful[tid]], s_B[s_useful[tid]]);
 
     // 3. Blocks outside the home range, outward from it (threads 0..63 to the
     //    right, 64..127 to the left, 64 offsets per step), kept unless one
-    //    pivot separates them from every row.  The block's own pivot is tried
-    //    first (it separates most far blocks); the blocks it leaves are then
-    //    taken one per warp against the useful pivots, a lane per pivot, 32
-    //    at a time until one separates the block.
+    //    pivot separates them from every row.  The block's own pivot and the
+    //    pivot nearest the tile are tried first (they separate most far
+    //    blocks); the blocks they leave are then tested by a warp against
+    //    all the useful pivots at once, a lane per pivot.
     const int h0 = home_lo[rt];
     const int right0 = h0 + nh, left0 = h0 - 1;
     int base = 0;
@@ -269,7 +279,9 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         if (need) {
             const int p0 = bcell[b];
             need = !(Hm[static_cast<int64_t>(p0) * a.col_tiles + b] < s_A[p0] ||
-                     Lm[static_cast<int64_t>(p0) * a.col_tiles + b] > s_B[p0]);
+                     Lm[static_cast<int64_t>(p0) * a.col_tiles + b] > s_B[p0]) &&
+                   !(Hm[static_cast<int64_t>(pnear) * a.col_tiles + b] < s_A[pnear] ||
+                     Lm[static_cast<int64_t>(pnear) * a.col_tiles + b] > s_B[pnear]);
         }
         // the blocks left, in thread order
         unsigned bal = __ballot_sync(0xffffffffu, need);
@@ -281,15 +293,23 @@ __global__ void __launch_bounds__(kBM) prune_lists_kernel(const PruneListArgs a,
         ci += __popc(bal & lanemask_lt());
         if (need) s_cand[ci] = b;
         __syncthreads();
+        // every group's bounds of a block loaded at once (the loads, not the
+        // tests, bound this loop)
         for (int c = warp; c < nc; c += kBM / 32) {
             const float2 *hl = HLt + static_cast<int64_t>(s_cand[c]) * P;
+            float2 v[P / 32];
+#pragma unroll
+            for (int g = 0; g < P / 32; ++g)
+                if (g * 32 < nuseful) v[g] = __ldg(hl + pv[g]);  // (H, L)
             bool sep = false;
 #pragma unroll
             for (int g = 0; g < P / 32; ++g) {
-                if (sep || g * 32 >= nuseful) break;
-                const float2 v = __ldg(hl + pv[g]);  // (H, L)
-                sep = __any_sync(0xffffffffu, v.x < abv[g].x || v.y > abv[g].y);
+                if (g * 32 < nuseful) {
+                    const float2 ab = s_ABu[g * 32 + lane];
+                    sep = sep || v[g].x < ab.x || v[g].y > ab.y;
+                }
             }
+            sep = __any_sync(0xffffffffu, sep);
             if (lane == 0) s_keep[c] = sep ? 0 : 1;
         }
         __syncthreads();
