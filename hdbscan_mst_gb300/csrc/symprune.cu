@@ -54,22 +54,51 @@ __global__ void sym_compact_kernel(int n, const int *__restrict__ act_size,
     cstart[k] = act_start[c];
 }
 
-// Per chunk of kSymChunk positions of the spatial order (one warp), the
-// points of each compact component that lie in P.
-__global__ void sym_chunk_count_kernel(int n, const int *__restrict__ perm,
-                                       const unsigned char *__restrict__ act_flag,
-                                       const int *__restrict__ comp, const int *__restrict__ cidx,
-                                       int *__restrict__ off) {
-    const int chunk = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    const int p0 = chunk * kSymChunk;
-    if (p0 >= n) return;
-    const int p1 = min(p0 + kSymChunk, n);
-    int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
-    for (int q = p0 + lane; q < p1; q += 32) {
-        const int x = perm[q];
-        if (act_flag[x]) atomicAdd(&row[cidx[comp[x]]], 1);
+// Per chunk of kSymChunk positions of the spatial order (one CTA; warp w
+// takes the chunk's kSubChunk positions from w kSubChunk on), the points of
+// each compact component that lie in P: lanes of one component add their
+// number at once into the CTA's shared row, which is then written out whole
+// (zeros included).
+constexpr int kGroupWarps = 8, kSubChunk = kSymChunk / kGroupWarps;
+static_assert(kSubChunk == 4 * 32, "four steps of 32 positions per warp");
+
+// The compact component (or -1) and the point of the four steps of warp w.
+__device__ __forceinline__ void sub_chunk_points(int p0, int p1, int warp, int lane,
+                                                 const int *__restrict__ perm,
+                                                 const unsigned char *__restrict__ act_flag,
+                                                 const int *__restrict__ comp,
+                                                 const int *__restrict__ cidx, int (&x)[4],
+                                                 int (&k)[4]) {
+    const int s0 = p0 + warp * kSubChunk + lane;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = s0 + 32 * u < p1 ? perm[s0 + 32 * u] : -1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) k[u] = (x[u] >= 0 && act_flag[x[u]]) ? comp[x[u]] : -1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) k[u] = k[u] >= 0 ? cidx[k[u]] : -1;
+}
+
+__global__ void __launch_bounds__(kGroupWarps * 32)
+    sym_chunk_count_kernel(int n, const int *__restrict__ perm,
+                           const unsigned char *__restrict__ act_flag,
+                           const int *__restrict__ comp, const int *__restrict__ cidx,
+                           int *__restrict__ off) {
+    __shared__ int s_cnt[kSymMaxComps];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int chunk = blockIdx.x;
+    const int p0 = chunk * kSymChunk, p1 = min(p0 + kSymChunk, n);
+    for (int k = t; k < kSymMaxComps; k += kGroupWarps * 32) s_cnt[k] = 0;
+    __syncthreads();
+    int x[4], k[4];
+    sub_chunk_points(p0, p1, warp, lane, perm, act_flag, comp, cidx, x, k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const unsigned peers = __match_any_sync(0xffffffffu, k[u]);
+        if (k[u] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[k[u]], __popc(peers));
     }
+    __syncthreads();
+    int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
+    for (int c = t; c < kSymMaxComps; c += kGroupWarps * 32) row[c] = s_cnt[c];
 }
 
 // Per compact component, the running position at the start of each chunk.
@@ -86,32 +115,51 @@ __global__ void sym_chunk_scan_kernel(int chunks, int ncomp, const int *__restri
     }
 }
 
-// Positions in chunk order and, within a chunk, in spatial order: one warp
-// walks its chunk 32 points at a time; lanes of one component take
-// consecutive positions in lane order.
-__global__ void sym_scatter_kernel(int n, const int *__restrict__ perm,
-                                   const unsigned char *__restrict__ act_flag,
-                                   const int *__restrict__ comp, const int *__restrict__ cidx,
-                                   int *__restrict__ off, int *__restrict__ act_idx) {
-    const int chunk = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    const int p0 = chunk * kSymChunk;
-    if (p0 >= n) return;
-    const int p1 = min(p0 + kSymChunk, n);
-    int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
-    for (int q0 = p0; q0 < p1; q0 += 32) {
-        const int q = q0 + lane;
-        const int x = q < p1 ? perm[q] : -1;
-        const bool in = x >= 0 && act_flag[x];
-        const int k = in ? cidx[comp[x]] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, k);
-        const int leader = __ffs(peers) - 1;
-        int base = 0;
-        if (in) base = row[k];
+// Positions in chunk order and, within a chunk, in spatial order (one CTA
+// per chunk): each warp counts its sub-chunk's points per component, a
+// prefix over the warps per component gives each warp's first positions from
+// the chunk's, and each warp then places its points 32 at a time, lanes of
+// one component at consecutive positions in lane order.
+__global__ void __launch_bounds__(kGroupWarps * 32)
+    sym_scatter_kernel(int n, const int *__restrict__ perm,
+                       const unsigned char *__restrict__ act_flag,
+                       const int *__restrict__ comp, const int *__restrict__ cidx,
+                       const int *__restrict__ off, int *__restrict__ act_idx) {
+    __shared__ int s_pos[kGroupWarps][kSymMaxComps];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int chunk = blockIdx.x;
+    const int p0 = chunk * kSymChunk, p1 = min(p0 + kSymChunk, n);
+    for (int c = t; c < kGroupWarps * kSymMaxComps; c += kGroupWarps * 32) (&s_pos[0][0])[c] = 0;
+    __syncthreads();
+    int x[4], k[4];
+    sub_chunk_points(p0, p1, warp, lane, perm, act_flag, comp, cidx, x, k);
+    int *own = s_pos[warp];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const unsigned peers = __match_any_sync(0xffffffffu, k[u]);
+        if (k[u] >= 0 && lane == __ffs(peers) - 1) own[k[u]] += __popc(peers);
         __syncwarp();
-        if (in) {
-            act_idx[base + __popc(peers & lanemask_lt())] = x;
-            if (lane == leader) row[k] = base + __popc(peers);
+    }
+    __syncthreads();
+    const int *row = off + static_cast<int64_t>(chunk) * kSymMaxComps;
+    for (int c = t; c < kSymMaxComps; c += kGroupWarps * 32) {
+        int run = row[c];
+#pragma unroll
+        for (int w = 0; w < kGroupWarps; ++w) {
+            const int cnt = s_pos[w][c];
+            s_pos[w][c] = run;
+            run += cnt;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const unsigned peers = __match_any_sync(0xffffffffu, k[u]);
+        const int base = k[u] >= 0 ? own[k[u]] : 0;
+        __syncwarp();
+        if (k[u] >= 0) {
+            act_idx[base + __popc(peers & lanemask_lt())] = x[u];
+            if (lane == __ffs(peers) - 1) own[k[u]] = base + __popc(peers);
         }
         __syncwarp();
     }
@@ -339,16 +387,14 @@ cudaError_t launch_sym_group(const SymPruneBufs &b, int n, const unsigned char *
     const int chunks = blocks_for(n, kSymChunk);
     cudaError_t e = cudaMemsetAsync(b.kcount, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(b.off, 0, sizeof(int) * static_cast<size_t>(chunks) * kSymMaxComps, s);
-    if (e != cudaSuccess) return e;
     sym_compact_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, act_size, act_start, b.kcount, b.cidx,
                                                           b.cstart);
-    sym_chunk_count_kernel<<<blocks_for(static_cast<int64_t>(chunks) * 32, 256), 256, 0, s>>>(
-        n, b.order.permY, act_flag, comp, b.cidx, b.off);
+    sym_chunk_count_kernel<<<chunks, kGroupWarps * 32, 0, s>>>(n, b.order.permY, act_flag, comp,
+                                                              b.cidx, b.off);
     sym_chunk_scan_kernel<<<blocks_for(kSymMaxComps, 256), 256, 0, s>>>(chunks, kSymMaxComps,
                                                                         b.cstart, b.off);
-    sym_scatter_kernel<<<blocks_for(static_cast<int64_t>(chunks) * 32, 256), 256, 0, s>>>(
-        n, b.order.permY, act_flag, comp, b.cidx, b.off, act_idx);
+    sym_scatter_kernel<<<chunks, kGroupWarps * 32, 0, s>>>(n, b.order.permY, act_flag, comp,
+                                                          b.cidx, b.off, act_idx);
     count_extra_launches(3);
     return cudaGetLastError();
 }
