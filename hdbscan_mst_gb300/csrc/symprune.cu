@@ -174,22 +174,25 @@ __global__ void __launch_bounds__(P) sym_bounds_kernel(int np, const int *__rest
                                                        float *__restrict__ Lb,
                                                        float *__restrict__ Hb,
                                                        int *__restrict__ bcomp) {
+    static_assert(kRowsPerBlock == P, "one position per thread");
+    __shared__ int s_pt[kRowsPerBlock];
     const int b = blockIdx.x, p = threadIdx.x;
     const int q0 = b * kRowsPerBlock, q1 = min(q0 + kRowsPerBlock, np);
+    // the block's points, and whether they all share the first one's component
+    const bool in = q0 + p < q1;
+    s_pt[p] = in ? act_idx[q0 + p] : 0;
+    const int c0 = pcomp[q0];
+    const bool same = __syncthreads_and(!in || pcomp[q0 + p] == c0);
     float lo = INFINITY, hi = -INFINITY;
-    for (int q = q0; q < q1; ++q) {
-        const float v = pd[static_cast<int64_t>(act_idx[q]) * P + p];
+#pragma unroll 8
+    for (int q = 0; q < q1 - q0; ++q) {
+        const float v = pd[static_cast<int64_t>(s_pt[q]) * P + p];
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
     }
     Lb[static_cast<int64_t>(b) * P + p] = __double2float_rd(static_cast<double>(lo) * (1.0 - eps));
     Hb[static_cast<int64_t>(b) * P + p] = __double2float_ru(static_cast<double>(hi) * (1.0 + eps));
-    if (p == 0) {
-        const int c0 = pcomp[q0];
-        bool same = true;
-        for (int q = q0 + 1; q < q1; ++q) same = same && pcomp[q] == c0;
-        bcomp[b] = same ? c0 : -1;
-    }
+    if (p == 0) bcomp[b] = same ? c0 : -1;
 }
 
 // LB[i][j] for all block pairs (LB is symmetric: only tiles with j0 >= i0
