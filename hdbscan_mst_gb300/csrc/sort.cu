@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kSortThreads) scatter_kernel(const SortPassArg
     // digits plus that of digit tid in the tiles before this one (each step
     // over the tiles one coalesced row of 256 counts, several in flight)
     unsigned before = 0, total = 0;
-#pragma unroll 8
+#pragma unroll 32
     for (int t = 0; t < a.tiles; ++t) {
         const unsigned v = a.hist[t * 256 + tid];
         before += t < static_cast<int>(blockIdx.x) ? v : 0u;
@@ -100,17 +100,26 @@ __global__ void __launch_bounds__(kSortThreads) scatter_kernel(const SortPassArg
     offset[tid] = wbefore + incl - total + before;
     __syncthreads();
     const int base = blockIdx.x * kSortTile;
+    // each round's edge is loaded one round ahead
+    unsigned nw = 0;
+    int nlo = 0, nhi = 0;
+    if (base + tid < a.N) {
+        nw = a.w[base + tid];
+        nlo = a.lo[base + tid];
+        nhi = a.hi[base + tid];
+    }
     for (int q = 0; q < kSortRounds; ++q) {
         const int e = base + q * kSortThreads + tid;
         const bool valid = e < a.N;
-        unsigned kw = 0, digit = 256u + lane;  // invalid lanes: a digit of their own
-        int klo = 0, khi = 0;
-        if (valid) {
-            kw = a.w[e];
-            klo = a.lo[e];
-            khi = a.hi[e];
-            digit = digit_of(a.which, a.shift, kw, klo, khi);
+        const unsigned kw = nw;
+        const int klo = nlo, khi = nhi;
+        if (q + 1 < kSortRounds && e + kSortThreads < a.N) {
+            nw = a.w[e + kSortThreads];
+            nlo = a.lo[e + kSortThreads];
+            nhi = a.hi[e + kSortThreads];
         }
+        unsigned digit = 256u + lane;  // invalid lanes: a digit of their own
+        if (valid) digit = digit_of(a.which, a.shift, kw, klo, khi);
         const unsigned peers = __match_any_sync(0xffffffffu, digit);
         const unsigned rank = __popc(peers & lanemask_lt());
         if (valid && rank == 0) wcnt[wid][digit] = __popc(peers);
