@@ -361,6 +361,7 @@ void carve_knn(Carver &c, const KnnPlan &p, KnnBufs &b, bool own_lists) {
             q.home = c.take<int>(tiles * kHomeBlocks);
             q.list = c.take<int>(tiles * p.col_tiles);
             q.count = c.take<int>(tiles);
+            q.order = c.take<int>(tiles);
             q.slabs = c.take<int>(tiles);
             q.gthr = c.take<unsigned>(static_cast<size_t>(p.chunk_rows));
         }
@@ -524,8 +525,12 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.pdX = b.order.pdX;
             pa.permX = b.order.permX;
             LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
-            // second pass: slabs 1 .., in chunks of chunk_cap blocks
+            const bool ordered = row_tiles <= kOrderMax;
+            if (ordered) LAUNCH(K_PRUNE, s, launch_prune_order(b.prune, row_tiles, s));
+            // second pass: slabs 1 .., in chunks of chunk_cap blocks, the
+            // longest lists first
             KnnTileArgs q = ta;
+            q.tile_order = ordered ? b.prune.order : nullptr;
             q.tile_start = nullptr;
             q.blist = b.prune.list;
             q.bcount = b.prune.count;

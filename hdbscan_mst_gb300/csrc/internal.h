@@ -82,6 +82,8 @@ struct PruneBufs {
     int *home;            // [chunk row tiles][kHomeBlocks] home lists
     int *list;            // [chunk row tiles][col_tiles] blocks of the second pass
     int *count;           // [chunk row tiles] entries of list
+    int *order;           // [chunk row tiles] row tiles by decreasing count (the second
+                          // pass's dispatch order)
     int *slabs;           // [chunk row tiles] partial-list slabs written (1 + chunks)
     unsigned *gthr;       // [chunk rows] shared thresholds of the second pass (KnnTileArgs::gthr)
 };
@@ -114,6 +116,10 @@ struct PruneListArgs {
 // Upper bound of each row's k-th distance from its home list, the row tile's
 // hull per pivot, and the list of blocks that the hull cannot exclude.
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s);
+// The chunk's row tiles by decreasing list length, ties to the lower tile
+// (b.order from b.count), for at most kOrderMax row tiles.
+constexpr int kOrderMax = 4096;
+cudaError_t launch_prune_order(const PruneBufs &b, int row_tiles, cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
 
@@ -145,6 +151,7 @@ struct KnnTileArgs {
     const int *blist;
     const int *bcount;
     int blist_count, blist_stride, chunk_cap, slab_base;
+    const int *tile_order;  // nullable: the row tile of CTA x (longest lists first)
     const float *seed;  // nullable: sorted lists of slab 0 (their KP-th key: a first threshold)
     // nullable (tensor tile, pruned pass): the columns of slab 0's lists; with
     // them every epilogue group's list starts as the row's home list, and the

@@ -330,7 +330,46 @@ __global__ void __launch_bounds__(kBM, 12) prune_lists_kernel(const PruneListArg
     }
 }
 
+// The row tiles by decreasing list length (ties: the lower tile first), so
+// that the pruned pass, which dispatches its CTAs in this order, starts the
+// longest first and ends on the shortest: one CTA, a bitonic sort of
+// (count, tile) keys in shared memory.
+__global__ void __launch_bounds__(1024) order_tiles_kernel(const int *__restrict__ count,
+                                                           int row_tiles, int *__restrict__ order) {
+    __shared__ unsigned long long key[kOrderMax];
+    int npow = 1;
+    while (npow < row_tiles) npow <<= 1;
+    for (int i = threadIdx.x; i < npow; i += blockDim.x)
+        key[i] = i < row_tiles
+                     ? (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(count[i])) << 32) |
+                           static_cast<unsigned>(i)
+                     : ~0ull;
+    __syncthreads();
+    for (int size = 2; size <= npow; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const unsigned long long x = key[i], y = key[j];
+                    if ((x > y) == ((i & size) == 0)) {
+                        key[i] = y;
+                        key[j] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < row_tiles; i += blockDim.x) order[i] = static_cast<int>(key[i] & 0xffffffffu);
+}
+
 }  // namespace
+
+cudaError_t launch_prune_order(const PruneBufs &b, int row_tiles, cudaStream_t s) {
+    if (row_tiles < 1 || row_tiles > kOrderMax) return cudaErrorInvalidValue;
+    order_tiles_kernel<<<1, 1024, 0, s>>>(b.count, row_tiles, b.order);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prune_setup(const SpatialOrder &o, const PruneBufs &b, int m, int col_tiles,
                                int d, cudaStream_t s) {

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(Epi<KP, kWide, kFill>::kThreads, Epi<KP, kWide
     const KnnTileArgs &a = P.a;
     uint8_t *base = pipe_base(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row_tile = blockIdx.x;
+    const int row_tile = a.tile_order ? a.tile_order[blockIdx.x] : static_cast<int>(blockIdx.x);
     int split = blockIdx.y;
     const int r0 = a.row_base + row_tile * kRows;
     constexpr int kSub = kCols / kTileCols;  // pipeline tiles per 128-column tile
