@@ -526,7 +526,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.permX = b.order.permX;
             LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
             const bool ordered = row_tiles <= kOrderMax;
-            if (ordered) LAUNCH(K_PRUNE, s, launch_prune_order(b.prune, row_tiles, s));
+            if (ordered)
+                LAUNCH(K_PRUNE, s, launch_tile_order(b.prune.count, row_tiles, b.prune.order, s));
             // second pass: slabs 1 .., in chunks of chunk_cap blocks, the
             // longest lists first
             KnnTileArgs q = ta;
@@ -737,6 +738,7 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
         q.hcount = c.take<int>(blocks);
         q.list = c.take<int>(blocks * blocks);
         q.lcount = c.take<int>(blocks);
+        q.tile_order = c.take<int>(blocks);
     }
 }
 
@@ -1124,6 +1126,12 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                 ya.list = b.sp.list;
                 ya.list_count = b.sp.lcount;
                 ya.list_stride = blocks;
+                if (blocks <= kOrderMax) {
+                    // the longest lists first
+                    LAUNCH(K_SYM_PRUNE, s,
+                           launch_tile_order(b.sp.lcount, blocks, b.sp.tile_order, s));
+                    ya.tile_order = b.sp.tile_order;
+                }
             }
             LAUNCH(K_SCAN, s, launch_tc_sym(ya, b.Xa_hi, b.Xa_lo, s));
             rs = read_status(b.st, h, s);

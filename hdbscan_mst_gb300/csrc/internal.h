@@ -116,10 +116,10 @@ struct PruneListArgs {
 // Upper bound of each row's k-th distance from its home list, the row tile's
 // hull per pivot, and the list of blocks that the hull cannot exclude.
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s);
-// The chunk's row tiles by decreasing list length, ties to the lower tile
-// (b.order from b.count), for at most kOrderMax row tiles.
+// Row tiles by decreasing list length, ties to the lower tile: order[x] for
+// x < row_tiles from count[row_tiles], for at most kOrderMax row tiles.
 constexpr int kOrderMax = 4096;
-cudaError_t launch_prune_order(const PruneBufs &b, int row_tiles, cudaStream_t s);
+cudaError_t launch_tile_order(const int *count, int row_tiles, int *order, cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
 
@@ -369,6 +369,7 @@ struct SymArgs {
     const int *list;
     const int *list_count;
     int list_stride;
+    const int *tile_order;  // nullable: the row tile of CTA x (longest lists first)
 };
 // The pruned symmetric scan (symprune.cu).  Blocks of 128 positions of P are
 // bounded through the pivots of a spatial order of all points; a home pass
@@ -393,6 +394,7 @@ struct SymPruneBufs {
     float *bth;          // [blocks] largest component bound over a block's points
     int *home, *hcount;  // [blocks][kSymHome], [blocks]
     int *list, *lcount;  // [blocks][blocks], [blocks]
+    int *tile_order;     // [blocks] row tiles by decreasing lcount (second pass's dispatch)
 };
 // P grouped by component in the spatial order (act_idx rewritten): within a
 // component, positions follow o.permY.  Needs act_start / act_size of

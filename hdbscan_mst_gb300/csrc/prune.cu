@@ -365,9 +365,9 @@ __global__ void __launch_bounds__(1024) order_tiles_kernel(const int *__restrict
 
 }  // namespace
 
-cudaError_t launch_prune_order(const PruneBufs &b, int row_tiles, cudaStream_t s) {
+cudaError_t launch_tile_order(const int *count, int row_tiles, int *order, cudaStream_t s) {
     if (row_tiles < 1 || row_tiles > kOrderMax) return cudaErrorInvalidValue;
-    order_tiles_kernel<<<1, 1024, 0, s>>>(b.count, row_tiles, b.order);
+    order_tiles_kernel<<<1, 1024, 0, s>>>(count, row_tiles, order);
     return cudaGetLastError();
 }
 

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__((kEW + 1 + kEW / 4) * 32, kSmall ? 2 : 1)
     const SymArgs &a = P.a;
     uint8_t *base = pipe_base(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i = blockIdx.x;
+    const int i = a.tile_order ? a.tile_order[blockIdx.x] : static_cast<int>(blockIdx.x);
     const int r0 = i * kRows;
     constexpr int kSub = kCols / kTileCols;
 
