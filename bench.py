@@ -26,6 +26,7 @@ rank 0 prints the line.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -242,17 +243,25 @@ def run_gpu(args):
 
     def timed(fn):
         """K steps with CUDA events on the launching stream around each; L2
-        flushed before each step, outside the events."""
+        flushed before each step, outside the events.  Python's garbage
+        collector is paused meanwhile: a collection inside a step would leave
+        the GPU waiting for the host's next launch."""
         out = []
-        for _ in range(args.steps):
-            flush_l2(flush)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            e1.synchronize()
-            out.append(e0.elapsed_time(e1))
+        gc_on = gc.isenabled()
+        gc.disable()
+        try:
+            for _ in range(args.steps):
+                flush_l2(flush)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                out.append(e0.elapsed_time(e1))
+        finally:
+            if gc_on:
+                gc.enable()
         return out
 
     # ---- timed region: data resident, no instrumentation
@@ -286,6 +295,8 @@ def run_gpu(args):
     # ---- end to end through the public API with host buffers
     Xh = torch.from_numpy(X).pin_memory()
     e2e_times = []
+    gc_on = gc.isenabled()
+    gc.disable()
     for i in range(0 if args.skip_e2e else args.warmup + args.steps):
         flush_l2(flush)
         torch.cuda.synchronize(device)
@@ -294,6 +305,8 @@ def run_gpu(args):
         t1 = time.perf_counter()
         if i >= args.warmup:
             e2e_times.append((t1 - t0) * 1e3)
+    if gc_on:
+        gc.enable()
     e2e_total = max_over_ranks(dist, sum(e2e_times), device)
 
     # ---- the back half on the host (labels from the tree of the last call):

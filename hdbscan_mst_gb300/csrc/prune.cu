@@ -331,43 +331,42 @@ __global__ void __launch_bounds__(kBM, 12) prune_lists_kernel(const PruneListArg
 }
 
 // The row tiles by decreasing list length (ties: the lower tile first), so
-// that the pruned pass, which dispatches its CTAs in this order, starts the
-// longest first and ends on the shortest: one CTA, a bitonic sort of
-// (count, tile) keys in shared memory.
-__global__ void __launch_bounds__(1024) order_tiles_kernel(const int *__restrict__ count,
-                                                           int row_tiles, int *__restrict__ order) {
-    __shared__ unsigned long long key[kOrderMax];
-    int npow = 1;
-    while (npow < row_tiles) npow <<= 1;
-    for (int i = threadIdx.x; i < npow; i += blockDim.x)
-        key[i] = i < row_tiles
-                     ? (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(count[i])) << 32) |
-                           static_cast<unsigned>(i)
-                     : ~0ull;
+// that a pruned pass, which dispatches its CTAs in this order, starts the
+// longest first and ends on the shortest.  A thread per row tile counts the
+// tiles that precede it in that order (the keys are distinct, so the counts
+// are a permutation), reading all the lengths from shared memory.
+constexpr int kOrderThreads = 128;
+__global__ void __launch_bounds__(kOrderThreads) order_tiles_kernel(const int *__restrict__ count,
+                                                                    int row_tiles,
+                                                                    int *__restrict__ order) {
+    __shared__ int4 s_cnt4[kOrderMax / 4];
+    int *s_cnt = reinterpret_cast<int *>(s_cnt4);
+    const int n4 = (row_tiles + 3) / 4;
+    // past the last tile -1: lengths are never negative, so it precedes none
+    for (int q = threadIdx.x; q < 4 * n4; q += kOrderThreads) s_cnt[q] = q < row_tiles ? count[q] : -1;
     __syncthreads();
-    for (int size = 2; size <= npow; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < npow; i += blockDim.x) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const unsigned long long x = key[i], y = key[j];
-                    if ((x > y) == ((i & size) == 0)) {
-                        key[i] = y;
-                        key[j] = x;
-                    }
-                }
-            }
-            __syncthreads();
-        }
+    const int i = blockIdx.x * kOrderThreads + threadIdx.x;
+    if (i >= row_tiles) return;
+    const int ci = s_cnt[i];
+    int rank = 0;
+#pragma unroll 4
+    for (int q = 0; q < n4; ++q) {
+        const int4 c = s_cnt4[q];
+        const int j = 4 * q;
+        rank += (c.x > ci || (c.x == ci && j < i)) ? 1 : 0;
+        rank += (c.y > ci || (c.y == ci && j + 1 < i)) ? 1 : 0;
+        rank += (c.z > ci || (c.z == ci && j + 2 < i)) ? 1 : 0;
+        rank += (c.w > ci || (c.w == ci && j + 3 < i)) ? 1 : 0;
     }
-    for (int i = threadIdx.x; i < row_tiles; i += blockDim.x) order[i] = static_cast<int>(key[i] & 0xffffffffu);
+    order[rank] = i;
 }
 
 }  // namespace
 
 cudaError_t launch_tile_order(const int *count, int row_tiles, int *order, cudaStream_t s) {
     if (row_tiles < 1 || row_tiles > kOrderMax) return cudaErrorInvalidValue;
-    order_tiles_kernel<<<1, 1024, 0, s>>>(count, row_tiles, order);
+    order_tiles_kernel<<<(row_tiles + kOrderThreads - 1) / kOrderThreads, kOrderThreads, 0, s>>>(
+        count, row_tiles, order);
     return cudaGetLastError();
 }
 
