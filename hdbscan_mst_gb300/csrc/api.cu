@@ -448,14 +448,19 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     // pruned search: the spatial order's pivots bound the column blocks (prune.cu)
     const bool prune = spatial && b.prune.list != nullptr;
     const int nh = home_blocks(p.col_tiles);
-    const int chunk_cap = (p.col_tiles + kPruneChunks - 1) / kPruneChunks;
     if (prune)
         LAUNCH(K_PRUNE, s, launch_prune_setup(b.order, b.prune, p.m, p.col_tiles, p.d, s));
     const int slots = (tensor ? 1 : 2) * sm_count();
     for (int base = 0; base < p.n; base += p.chunk_rows) {
         const int rows = std::min(p.chunk_rows, p.n - base);
         const int row_tiles = (rows + kBM - 1) / kBM;
-        const int S0 = prune ? 1 + kPruneChunks
+        // the second pass dispatches its row tiles longest list first when
+        // they can be ordered, one CTA each; otherwise a long list is split
+        // over up to kPruneChunks CTAs so that it does not finish alone
+        const bool ordered = prune && row_tiles <= kOrderMax;
+        const int chunks = ordered ? 1 : kPruneChunks;
+        const int chunk_cap = (p.col_tiles + chunks - 1) / chunks;
+        const int S0 = prune ? 1 + chunks
                      : tensor ? choose_splits_tc(row_tiles, p.col_tiles, slots)
                               : choose_splits(row_tiles, p.col_tiles, slots);
         const int tps = (p.col_tiles + S0 - 1) / S0;
@@ -525,7 +530,6 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             pa.pdX = b.order.pdX;
             pa.permX = b.order.permX;
             LAUNCH(K_PRUNE, s, launch_prune_lists(pa, b.prune, s));
-            const bool ordered = row_tiles <= kOrderMax;
             if (ordered)
                 LAUNCH(K_PRUNE, s, launch_tile_order(b.prune.count, row_tiles, b.prune.order, s));
             // second pass: slabs 1 .., in chunks of chunk_cap blocks, the
@@ -544,7 +548,7 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             q.nh = nh;
             q.gthr = b.prune.gthr;
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, ops, p.n_pad, p.m_pad, row_tiles,
-                                                kPruneChunks, s));
+                                                chunks, s));
         } else if (tensor) {
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, ta, ops, p.n_pad, p.m_pad, row_tiles, S, s));
         } else {

@@ -71,7 +71,8 @@ inline int home_blocks(int col_tiles) {
     const int h = col_tiles / 100;
     return std::min(col_tiles, h < 3 ? 3 : (h > kHomeBlocks ? kHomeBlocks : h));
 }
-constexpr int kPruneChunks = 4;     // CTAs per row tile in the second pass (at most)
+constexpr int kPruneChunks = 4;     // CTAs per row tile in the second pass (at most) when
+                                    // its row tiles are not ordered by list length
 struct PruneBufs {
     float *Lm, *Hm;       // [P][col_tiles]: per column block, least / largest pivot
                           // distance of its points, widened by the distances' rounding bound
@@ -118,7 +119,7 @@ struct PruneListArgs {
 cudaError_t launch_prune_lists(const PruneListArgs &a, const PruneBufs &b, cudaStream_t s);
 // Row tiles by decreasing list length, ties to the lower tile: order[x] for
 // x < row_tiles from count[row_tiles], for at most kOrderMax row tiles.
-constexpr int kOrderMax = 4096;
+constexpr int kOrderMax = 8192;
 cudaError_t launch_tile_order(const int *count, int row_tiles, int *order, cudaStream_t s);
 // Flag core distances that are negative or not finite.
 cudaError_t launch_check_core(const float *core, int n, unsigned *status, cudaStream_t s);
