@@ -91,23 +91,23 @@ TF32_PER_BF16 = 1.1 / 2.25
 # otherwise the line reports null.
 TRAFFIC = {
     ("knn_tile", "hdbscan_200k_d61"): {
-        # per step: the home pass (52.20 MB read, 3.87 MB written) and the
-        # pruned second pass (95.22 MB read - the home lists it starts from
-        # included - and 25.54 MB written)
-        "bytes": 52.20e6 + 3.87e6 + 95.22e6 + 25.54e6,
+        # per step: the home pass (52.20 MB read, 3.79 MB written) and the
+        # pruned second pass (83.95 MB read - the home lists it starts from
+        # included - and 9.26 MB written)
+        "bytes": 52.20e6 + 3.79e6 + 83.95e6 + 9.26e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_knn.cu", "hdbscan_mst_gb300/csrc/tc_pipe.cuh",
                     "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "6cf9da1f7f849889741d648bda9e24d73be23e05c7d1049977e4b6161d694b7e",
+        "sha256": "5aa1b00de8a6d67783d45effb35cf8d64ea1cf55ff642e7ac4b8bd2004b8defa",
     },
     ("boruvka_scan", "hdbscan_200k_d61"): {
-        # per step: the one-sided scans of rounds 1 and 2 (55.01 + 53.27 MB
+        # per step: the one-sided scans of rounds 1 and 2 (55.01 + 53.26 MB
         # read) and the symmetric scans of rounds 3 and 4, home pass and
-        # pruned pass each (49.26 + 51.68 + 48.69 + 49.68 MB read); under
+        # pruned pass each (49.22 + 51.48 + 48.69 + 49.69 MB read); under
         # 0.01 MB written in all
-        "bytes": (55.01 + 53.27 + 49.26 + 51.68 + 48.69 + 49.68 + 0.006) * 1e6,
+        "bytes": (55.01 + 53.26 + 49.22 + 51.48 + 48.69 + 49.69 + 0.006) * 1e6,
         "sources": ("hdbscan_mst_gb300/csrc/tc_scan.cu", "hdbscan_mst_gb300/csrc/tc_sym.cu",
                     "hdbscan_mst_gb300/csrc/tc_pipe.cuh", "hdbscan_mst_gb300/csrc/tc.cuh"),
-        "sha256": "e0fff907bf285803002e54abe1fc699b3c317ccda4fb060234bc25ccbf4577ec",
+        "sha256": "c6010b05c9ae77cec18fa7607374edf66545da9f3fb8398cf3876a9047ab17fe",
     },
 }
 FALLBACK_BF16_TFLOPS = 1900.0
