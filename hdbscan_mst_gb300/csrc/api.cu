@@ -402,18 +402,21 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
     const bool spatial = tensor && b.order.permY && p.m >= kSpatialMinCols;
     const int *permX = spatial ? b.order.permX : nullptr;
     const int *permY = spatial ? b.order.permY : nullptr;
-    if (spatial)
-        LAUNCH(K_PACK, s, launch_spatial_order(b.order, X, ldx, p.n, Y, ldy, p.m, p.alias, p.d, s));
     // tensor-core operands: TF32 low parts, or the FP16 halves (hi and lo, dk / 2
     // words per point each) in the same buffer, with one scale for X and Y
     const bool f16 = tensor && use_f16(p.dk);
+    // the spatial order reads every value of X and Y: it also takes their
+    // largest magnitude, the FP16 scale
+    if (spatial)
+        LAUNCH(K_PACK, s, launch_spatial_order(b.order, X, ldx, p.n, Y, ldy, p.m, p.alias, p.d, s,
+                                               f16 ? &b.st->amax_bits : nullptr));
     const unsigned *amax = &b.st->amax_bits;
     uint32_t *Xh16 = f16 ? reinterpret_cast<uint32_t *>(b.Xlo) : nullptr;
     uint32_t *Xl16 = f16 ? Xh16 + p.n_pad * (p.dk / 2) : nullptr;
     uint32_t *Yh16 = f16 ? reinterpret_cast<uint32_t *>(b.Ylo) : nullptr;
     uint32_t *Yl16 = f16 ? Yh16 + p.m_pad * (p.dk / 2) : nullptr;
     float *xlo = tensor && !f16 ? b.Xlo : nullptr, *ylo = tensor && !f16 ? b.Ylo : nullptr;
-    if (f16) {
+    if (f16 && !spatial) {
         LAUNCH(K_PACK, s, launch_absmax(X, ldx, p.n, p.d, &b.st->amax_bits, s));
         if (!p.alias) LAUNCH(K_PACK, s, launch_absmax(Y, ldy, p.m, p.d, &b.st->amax_bits, s));
     }

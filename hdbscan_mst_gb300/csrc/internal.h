@@ -55,9 +55,11 @@ struct SpatialOrder {
 };
 inline int spatial_counter_ints(int pivots, int buckets) { return 4 * pivots * buckets + 2 * pivots; }
 constexpr int kSpatialMaxD = 192;  // features the spatial order handles (the tensor tile's)
+// amax_bits (nullable): raised to the largest finite magnitude of X and Y
+// (the FP16 operands' scale), read on the way.
 cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t ldx, int n,
                                  const float *Y, int64_t ldy, int m, bool alias, int d,
-                                 cudaStream_t s);
+                                 cudaStream_t s, unsigned *amax_bits = nullptr);
 
 // ---------------------------------------------------------------- prune.cu
 // Column blocks of the tensor-core k-NN that can hold none of a row tile's

@@ -42,7 +42,8 @@ __global__ void pivots_kernel(const float *__restrict__ Y, int64_t ldy, int stri
 // Nearest pivot of each point of S (feature-major, leading dimension lds),
 // ties to the lower pivot; also the point's distance to its own pivot
 // (dcell), its distances to all 128 pivots if pd is not null (point-major
-// [cnt][128]), and cmax[cell] raised to the distance to its own pivot.  A CTA
+// [cnt][128]), cmax[cell] raised to the distance to its own pivot, and
+// *amax_bits (if not null) to the largest finite magnitude in S.  A CTA
 // of 256 threads takes 128 points against the 128 pivots; thread (ty, tx)
 // accumulates points 8 ty .. 8 ty + 7 against pivots 4 tx .. 4 tx + 3 and
 // 64 + 4 tx .. 64 + 4 tx + 3, so that the eight lanes of a quarter warp read
@@ -60,7 +61,8 @@ __global__ void __launch_bounds__(256, 2) cells_kernel(const float *__restrict__
                                                        int dp, int *__restrict__ cell,
                                                        float *__restrict__ dcell,
                                                        float *__restrict__ pd,
-                                                       unsigned *__restrict__ cmax) {
+                                                       unsigned *__restrict__ cmax,
+                                                       unsigned *__restrict__ amax_bits) {
     __shared__ __align__(16) float xs[kCellK][kCellPts];
     __shared__ __align__(16) float ps[kCellK][kCellPiv];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -68,6 +70,7 @@ __global__ void __launch_bounds__(256, 2) cells_kernel(const float *__restrict__
     // stage loads: element tid + 256 r of the [16][128] tile, r < kCellLoads
     const int lc = tid & (kCellPts - 1), lf = tid / kCellPts;
     float rx[kCellLoads], rp[kCellLoads];
+    unsigned amax = 0u;  // the largest finite magnitude this thread loaded (as bits)
     const auto load_stage = [&](int f0) {
 #pragma unroll
         for (int r = 0; r < kCellLoads; ++r) {
@@ -76,6 +79,13 @@ __global__ void __launch_bounds__(256, 2) cells_kernel(const float *__restrict__
             rx[r] = (i < cnt && f < d) ? S[static_cast<int64_t>(f) * lds + i] : 0.f;
             // the pivots negated: x + (-p) rounds exactly as x - p
             rp[r] = -piv[static_cast<int64_t>(f) * kCellPiv + lc];
+        }
+#pragma unroll
+        for (int r = 0; r < kCellLoads; ++r) {
+            // non-negative floats order like their bits; non-finite values
+            // are the pack kernel's to report
+            const float v = fabsf(rx[r]);
+            if (v <= 3.4028234663852886e38f) amax = max(amax, __float_as_uint(v));
         }
     };
     // acc[a][b]: point 8 ty + a against pivots 4 tx + 2 b, + 1 (b < 2) or
@@ -115,6 +125,11 @@ __global__ void __launch_bounds__(256, 2) cells_kernel(const float *__restrict__
                 }
             }
         }
+    }
+    if (amax_bits) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((tid & 31) == 0 && amax) atomicMax(amax_bits, amax);
     }
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
@@ -243,7 +258,7 @@ __global__ void tile_start_kernel(const int *__restrict__ permX, const int *__re
 
 cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t ldx, int n,
                                  const float *Y, int64_t ldy, int m, bool alias, int d,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, unsigned *amax_bits) {
     const int P = o.pivots, B = o.buckets, NB = P * B;
     if (P != kCellPiv || d > kSpatialMaxD) return cudaErrorInvalidValue;
     const int stride = m / P;
@@ -257,7 +272,7 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
         *cursorX = o.counters + 3 * NB;
     unsigned *cmaxY = reinterpret_cast<unsigned *>(o.counters + 4 * NB), *cmaxX = cmaxY + P;
     cells_kernel<<<blocks_for(m, kCellPts), 256, 0, s>>>(Y, ldy, m, d, o.pivf, dp, o.cellY,
-                                                         o.dcellY, o.pdY, cmaxY);
+                                                         o.dcellY, o.pdY, cmaxY, amax_bits);
     bins_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, o.dcellY, cmaxY, B, m, countY);
     start_cells_kernel<<<1, 1024, 0, s>>>(countY, NB, o.startY);
     scatter_cells_kernel<<<blocks_for(m, 256), 256, 0, s>>>(o.cellY, m, o.startY, cursorY, o.permY,
@@ -265,7 +280,7 @@ cudaError_t launch_spatial_order(const SpatialOrder &o, const float *X, int64_t 
     int extra = 5;  // pivots, cells, bins, start, scatter, tile start: 6 kernels, one counted by the caller
     if (!alias) {
         cells_kernel<<<blocks_for(n, kCellPts), 256, 0, s>>>(X, ldx, n, d, o.pivf, dp, o.cellX,
-                                                             o.dcellX, o.pdX, cmaxX);
+                                                             o.dcellX, o.pdX, cmaxX, amax_bits);
         bins_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, o.dcellX, cmaxX, B, n, countX);
         start_cells_kernel<<<1, 1024, 0, s>>>(countX, NB, o.startX);
         scatter_cells_kernel<<<blocks_for(n, 256), 256, 0, s>>>(o.cellX, n, o.startX, cursorX,
