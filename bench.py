@@ -444,7 +444,9 @@ def run_gpu(args):
     def roofline(prof_, name, d_, pairs, dense_pairs, engine, workload=None):
         """A distance tile: algorithmic flops 2 d per (row, column) pair the
         tile evaluated (blocks the bounds prune are not evaluated), over the
-        tile's time per step (all its launches)."""
+        tile's time per step (all its launches: the same ratio as a launch's
+        average); traffic, the measured DRAM bytes per launch (the step's
+        bytes over its launches), with the step's total beside it."""
         if name not in prof_:
             return None
         tot_ms, nl = prof_[name]
@@ -468,9 +470,14 @@ def run_gpu(args):
                 peak, basis = tf32_peak, tf32_basis
                 eng = "tcgen05 kind::tf32 (3 products)"
             issued = 3 * 2.0 * dk * pairs / step_s / 1e12
+            # DRAM bytes per launch, like achieved: the step's measured bytes
+            # over its launches of the tile
+            tstep = traffic_for(name, workload)
+            tlaunch = round(tstep / (nl / args.steps)) if tstep is not None else None
             return {"kernel": name, "engine": eng, "bound": "tensor",
                     "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                    "frac": round(ach / peak, 4), "traffic": traffic_for(name, workload),
+                    "frac": round(ach / peak, 4), "traffic": tlaunch,
+                    "traffic_per_step": tstep,
                     "peak_basis": basis, "issued_tflops": round(issued, 1),
                     "issued_frac": round(issued / peak, 4),
                     "fp32_alu_equiv_frac": round(ach / fp32_peak, 4), **common}
