@@ -549,7 +549,8 @@ hdbmst_status run_knn(const KnnPlan &p, const KnnBufs &b, const float *X, int64_
             q.seed_idx = b.part_idx;
             q.home_lo = b.prune.home_lo;
             q.nh = nh;
-            q.gthr = b.prune.gthr;
+            // a CTA per row tile shares its thresholds with no other CTA
+            q.gthr = ordered ? nullptr : b.prune.gthr;
             LAUNCH(K_KNN_TILE, s, launch_tc_knn(p.KP, q, ops, p.n_pad, p.m_pad, row_tiles,
                                                 chunks, s));
         } else if (tensor) {
