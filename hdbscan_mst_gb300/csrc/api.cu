@@ -747,6 +747,7 @@ void carve_mst(Carver &c, const MstPlan &p, MstBufs &b) {
         q.list = c.take<int>(blocks * blocks);
         q.lcount = c.take<int>(blocks);
         q.tile_order = c.take<int>(blocks);
+        q.hkey = c.take<int>(blocks);
     }
 }
 
@@ -1129,6 +1130,12 @@ hdbmst_status hdbmst_mr_mst(const float *X, int64_t ldx, int64_t n, int d, const
                 ha.list = b.sp.home;
                 ha.list_count = b.sp.hcount;
                 ha.list_stride = kSymHome;
+                if (blocks <= kOrderMax) {
+                    // the row tiles nearest another component (the most work) first
+                    LAUNCH(K_SYM_PRUNE, s,
+                           launch_tile_order(b.sp.hkey, blocks, b.sp.tile_order, s));
+                    ha.tile_order = b.sp.tile_order;
+                }
                 LAUNCH(K_SCAN, s, launch_tc_sym(ha, b.Xa_hi, b.Xa_lo, s));
                 LAUNCH(K_SYM_PRUNE, s, launch_sym_lists(b.sp, np, blocks, b.act_comp, theta, d, s));
                 ya.list = b.sp.list;

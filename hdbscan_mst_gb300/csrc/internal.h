@@ -396,6 +396,7 @@ struct SymPruneBufs {
     float *LB;           // [blocks][blocks] lower bound of the distance between two blocks
     float *bth;          // [blocks] largest component bound over a block's points
     int *home, *hcount;  // [blocks][kSymHome], [blocks]
+    int *hkey;           // [blocks] the home pass's work estimate (larger: more work)
     int *list, *lcount;  // [blocks][blocks], [blocks]
     int *tile_order;     // [blocks] row tiles by decreasing lcount (second pass's dispatch)
 };

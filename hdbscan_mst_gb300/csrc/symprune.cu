@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(kHomeThreads) sym_home_kernel(int blocks,
                                                                 const float *__restrict__ LB,
                                                                 const int *__restrict__ bcomp,
                                                                 int *__restrict__ home,
-                                                                int *__restrict__ hcount) {
+                                                                int *__restrict__ hcount,
+                                                                int *__restrict__ hkey) {
     __shared__ unsigned long long s_min[kHomeThreads / 32];
     __shared__ unsigned long long s_win;
     const int i = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -312,10 +313,17 @@ __global__ void __launch_bounds__(kHomeThreads) sym_home_kernel(int blocks,
         if (w == kNoKey) break;
         if (h == w) ++head;  // keys are distinct (block index)
         if (t == 0) home[static_cast<int64_t>(i) * kSymHome + cnt] = static_cast<int>(w & 0xffffffffu);
+        // the home pass's work estimate: the nearer the tile's nearest block
+        // of another component, the more pairs it records (a bound's bits,
+        // non-negative, order like the bound)
+        if (t == 0 && cnt == 0) hkey[i] = 0x7fffffff - static_cast<int>(min(static_cast<unsigned>(w >> 32), 0x7fffffffu));
         ++cnt;
         __syncthreads();
     }
-    if (t == 0) hcount[i] = cnt;
+    if (t == 0) {
+        hcount[i] = cnt;
+        if (cnt == 0) hkey[i] = 0;
+    }
 }
 
 // bth[b]: the largest live bound over the components of block b's points.
@@ -409,7 +417,8 @@ cudaError_t launch_sym_blocks(const SymPruneBufs &b, int np, int blocks, const i
                                            b.bcomp);
     const int g = (blocks + kLbTile - 1) / kLbTile;
     sym_lb_kernel<<<dim3(g, g), 256, 0, s>>>(blocks, b.Lb, b.Hb, b.LB);
-    sym_home_kernel<<<blocks, kHomeThreads, 0, s>>>(blocks, b.LB, b.bcomp, b.home, b.hcount);
+    sym_home_kernel<<<blocks, kHomeThreads, 0, s>>>(blocks, b.LB, b.bcomp, b.home, b.hcount,
+                                                     b.hkey);
     count_extra_launches(2);
     return cudaGetLastError();
 }
